@@ -1,0 +1,358 @@
+// cbs_api.cu -- the C ABI (include/cbs.h): planning, argument checks and
+// dispatch to the kernels.  Planning is pure host code with no CUDA call.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "cbs_internal.cuh"
+
+namespace cbs {
+
+namespace {
+thread_local char g_msg[512] = "";
+}
+
+cbs_status fail(cbs_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+cbs_status cuda_check(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return CBS_OK;
+    return fail(CBS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+namespace {
+
+int round_up(int v, int m) { return (v + m - 1) / m * m; }
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+size_t elem_bytes(int prec) {
+    switch (prec) {
+        case CBS_FP32: case CBS_TF32: return 4;
+        case CBS_BF16: return 2;
+        default: return 1;
+    }
+}
+
+// Pick the CUDA-core tile and split-K by a simple throughput model:
+// time ~ waves * (CTAs per SM) * tile work / (FMA lanes * efficiency),
+// divided by an occupancy factor when too few warps are resident.
+void plan_simt(cbs_plan_t &p) {
+    const cbs_layer_desc &d = p.desc;
+    const long long M = (long long)d.n * p.oh * p.ow;
+    const int K = d.k * d.k * d.c_in;
+    double best = 1e300;
+    int best_t = 1, best_split = 1;
+    for (int t = 0; t < kNumSimtTiles; ++t) {
+        if (d.force_block_n > 0 && kSimtTiles[t].bn != d.force_block_n) continue;
+        const SimtTile T = kSimtTiles[t];
+        const int nt = (T.bm / T.tm) * (T.bn / T.tn);
+        const int regs = T.tm * T.tn + 48;
+        int res = 65536 / (nt * (regs < 64 ? 64 : regs));
+        if (res > 2048 / nt) res = 2048 / nt;
+        if (res < 1) res = 1;
+        const double eff = (T.tm * T.tn >= 64) ? 0.85 : (T.tm * T.tn >= 32 ? 0.75 : 0.6);
+        const long long tiles = (long long)ceil_div(M, T.bm) * ceil_div(d.c_out, T.bn);
+        int max_split = K / (kSimtBK * 4) > 1 ? K / (kSimtBK * 4) : 1;
+        if (max_split > 32) max_split = 32;
+        if (d.force_split_k > 0) max_split = d.force_split_k;
+        for (int split = 1; split <= max_split; ++split) {
+            if (d.force_split_k > 0 && split != d.force_split_k) continue;
+            const long long kc = (long long)round_up(ceil_div(K, split), kSimtBK);
+            const long long ctas = tiles * split;
+            const long long slots = (long long)kNumSMs * res;
+            const long long waves = (ctas + slots - 1) / slots;
+            double warps = (double)(ctas < slots ? ctas : slots) / kNumSMs * nt / 32.0;
+            const double occ = warps >= 16 ? 1.0 : warps / 16.0;
+            double est = (double)waves * res * T.bm * T.bn * kc / (128.0 * eff) / occ;
+            est *= 1.0 + 0.04 * (split - 1);
+            if (est < best) { best = est; best_t = t; best_split = split; }
+        }
+    }
+    const SimtTile T = kSimtTiles[best_t];
+    p.block_m = T.bm;
+    p.block_n = T.bn;
+    p.block_k = kSimtBK;
+    p.stages = 2;
+    p.threads = (T.bm / T.tm) * (T.bn / T.tn);
+    p.smem_bytes = 0;
+    p.m_tiles = ceil_div(M, T.bm);
+    p.n_tiles = ceil_div(d.c_out, T.bn);
+    // K per split, a multiple of BK; recompute the split so none is empty.
+    const int kc = round_up(ceil_div(K, best_split), kSimtBK);
+    p.split_k = ceil_div(K, kc);
+    p.grid_ctas = p.m_tiles * p.n_tiles * p.split_k;
+    p.variant = CBS_VARIANT_SIMT_FP32;
+    p.workspace_bytes = 0;
+    if (p.split_k > 1) {
+        const size_t tiles = (size_t)p.m_tiles * p.n_tiles;
+        const size_t counters = (tiles * sizeof(unsigned) + 255) / 256 * 256;
+        p.workspace_bytes = counters + tiles * p.split_k * (size_t)T.bm * T.bn * sizeof(float);
+    }
+}
+
+int simt_tile_index(const cbs_plan_t &p) {
+    for (int t = 0; t < kNumSimtTiles; ++t)
+        if (kSimtTiles[t].bm == p.block_m && kSimtTiles[t].bn == p.block_n) return t;
+    return -1;
+}
+
+cbs_status check_plan(const cbs_plan_t *p) {
+    if (!p) return fail(CBS_ERR_INVALID_ARG, "plan is NULL");
+    if (p->size != sizeof(cbs_plan_t) || p->abi_version != CBS_ABI_VERSION)
+        return fail(CBS_ERR_PLAN_MISMATCH, "plan was not made by cbs_plan of this library (size %u, abi %u)",
+                    p->size, p->abi_version);
+    return CBS_OK;
+}
+
+cbs_status check_ptr(const void *ptr, const char *name, bool nullable = false) {
+    if (!ptr) return nullable ? CBS_OK : fail(CBS_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!aligned16(ptr)) return fail(CBS_ERR_MISALIGNED, "%s is not 16-byte aligned", name);
+    return CBS_OK;
+}
+
+#define CBS_TRY(expr)                      \
+    do {                                   \
+        cbs_status _s = (expr);            \
+        if (_s != CBS_OK) return _s;       \
+    } while (0)
+
+}  // namespace
+}  // namespace cbs
+
+using namespace cbs;
+
+extern "C" {
+
+int cbs_abi_version(void) { return CBS_ABI_VERSION; }
+
+const char *cbs_last_error(void) { return g_msg; }
+
+const char *cbs_status_string(cbs_status s) {
+    switch (s) {
+        case CBS_OK: return "CBS_OK";
+        case CBS_ERR_INVALID_ARG: return "CBS_ERR_INVALID_ARG";
+        case CBS_ERR_UNSUPPORTED: return "CBS_ERR_UNSUPPORTED";
+        case CBS_ERR_MISALIGNED: return "CBS_ERR_MISALIGNED";
+        case CBS_ERR_WORKSPACE: return "CBS_ERR_WORKSPACE";
+        case CBS_ERR_CUDA: return "CBS_ERR_CUDA";
+        case CBS_ERR_TIMEOUT: return "CBS_ERR_TIMEOUT";
+        case CBS_ERR_PLAN_MISMATCH: return "CBS_ERR_PLAN_MISMATCH";
+    }
+    return "CBS_ERR_UNKNOWN";
+}
+
+cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
+    if (!d || !out) return fail(CBS_ERR_INVALID_ARG, "desc or plan pointer is NULL");
+    const cbs_layer_desc D = *d;
+    if (D.n < 0 || D.c_in < 1 || D.c_out < 1 || D.h < 1 || D.w < 1 || D.k < 1 || D.stride < 1 ||
+        D.pad < 0)
+        return fail(CBS_ERR_INVALID_ARG, "bad shape n=%d c_in=%d c_out=%d h=%d w=%d k=%d stride=%d pad=%d",
+                    D.n, D.c_in, D.c_out, D.h, D.w, D.k, D.stride, D.pad);
+    if (D.k > 15 || D.stride > 8 || D.pad >= D.k)
+        return fail(CBS_ERR_UNSUPPORTED, "k=%d stride=%d pad=%d outside the supported range (k<=15, stride<=8, pad<k)",
+                    D.k, D.stride, D.pad);
+    if (D.h + 2 * D.pad < D.k || D.w + 2 * D.pad < D.k)
+        return fail(CBS_ERR_INVALID_ARG, "filter larger than the padded image");
+    if ((D.in_layout != CBS_NCHW && D.in_layout != CBS_NHWC) ||
+        (D.out_layout != CBS_NCHW && D.out_layout != CBS_NHWC))
+        return fail(CBS_ERR_INVALID_ARG, "unknown layout");
+    if (D.prec < CBS_FP32 || D.prec > CBS_INT8) return fail(CBS_ERR_INVALID_ARG, "unknown precision %d", D.prec);
+
+    cbs_plan_t p;
+    std::memset(&p, 0, sizeof(p));
+    p.size = sizeof(cbs_plan_t);
+    p.abi_version = CBS_ABI_VERSION;
+    p.desc = D;
+    p.oh = (D.h + 2 * D.pad - D.k) / D.stride + 1;
+    p.ow = (D.w + 2 * D.pad - D.k) / D.stride + 1;
+    const long long M = (long long)D.n * p.oh * p.ow;
+    if (M > 0x7fffffffLL || (long long)D.n * D.c_in * D.h * D.w > (1LL << 40))
+        return fail(CBS_ERR_UNSUPPORTED, "problem too large for 32-bit pixel indexing");
+
+    int variant = D.force_variant;
+    if (variant < 0) variant = D.prec;  // enum values line up: FP32->SIMT, TF32, BF16, INT8
+    const int need_prec[] = {CBS_FP32, CBS_TF32, CBS_BF16, CBS_INT8};
+    if (variant < 0 || variant > 3 || need_prec[variant] != D.prec)
+        return fail(CBS_ERR_INVALID_ARG, "variant %d does not compute precision %d", variant, D.prec);
+    p.variant = variant;
+
+    if (D.out_row_stride != 0) {
+        if (D.out_layout != CBS_NCHW)
+            return fail(CBS_ERR_INVALID_ARG, "out_row_stride applies to NCHW output only");
+        if (D.out_row_stride < p.ow)
+            return fail(CBS_ERR_INVALID_ARG, "out_row_stride %d < OW %d", D.out_row_stride, p.ow);
+    }
+    p.out_row_stride = D.out_row_stride ? D.out_row_stride : p.ow;
+
+    const size_t eb = elem_bytes(D.prec);
+    if (variant == CBS_VARIANT_SIMT_FP32) {
+        p.c_in_pad = D.c_in;
+    } else {
+        if (D.in_layout != CBS_NHWC)
+            return fail(CBS_ERR_UNSUPPORTED, "tensor-core variants read NHWC input (use cbs_pack_input)");
+        p.c_in_pad = round_up(D.c_in, (int)(16 / eb));
+    }
+    p.k_gemm = D.k * D.k * p.c_in_pad;
+    p.x_bytes = (size_t)D.n * D.h * D.w * p.c_in_pad * eb;
+    if (D.out_layout == CBS_NCHW)
+        p.y_bytes = (size_t)D.n * D.c_out * p.oh * p.out_row_stride * eb;
+    else
+        p.y_bytes = (size_t)M * D.c_out * eb;
+    p.w_packed_bytes = (size_t)D.c_out * p.k_gemm * (variant == CBS_VARIANT_SIMT_FP32 || variant == CBS_VARIANT_TC_TF32 ? 4 : 2);
+    p.bias_bytes = (size_t)D.c_out * 4;
+
+    if (variant == CBS_VARIANT_SIMT_FP32) {
+        plan_simt(p);
+    } else {
+        CBS_TRY(plan_tc(p));
+    }
+    *out = p;
+    return CBS_OK;
+}
+
+cbs_status cbs_fold_bn(const cbs_plan_t *p, const float *w_oihw, const float *conv_bias,
+                       const float *gamma, const float *beta, const float *mean, const float *var,
+                       float eps, float s_x, void *w_packed, void *bias, float *m_c, void *stream) {
+    CBS_TRY(check_plan(p));
+    CBS_TRY(check_ptr(w_oihw, "w"));
+    CBS_TRY(check_ptr(conv_bias, "conv_bias", true));
+    CBS_TRY(check_ptr(gamma, "gamma"));
+    CBS_TRY(check_ptr(beta, "beta"));
+    CBS_TRY(check_ptr(mean, "mean"));
+    CBS_TRY(check_ptr(var, "var"));
+    CBS_TRY(check_ptr(w_packed, "w_packed"));
+    CBS_TRY(check_ptr(bias, "bias"));
+    if (!(eps > 0.0f)) return fail(CBS_ERR_INVALID_ARG, "eps must be > 0");
+    if (p->variant == CBS_VARIANT_TC_INT8) {
+        CBS_TRY(check_ptr(m_c, "m_c"));
+        if (!(s_x > 0.0f)) return fail(CBS_ERR_INVALID_ARG, "s_x must be > 0 for INT8");
+    }
+    FoldLaunch L;
+    L.w = w_oihw; L.conv_bias = conv_bias; L.gamma = gamma; L.beta = beta; L.mean = mean; L.var = var;
+    L.eps = eps; L.s_x = s_x;
+    L.C_out = p->desc.c_out; L.C_in = p->desc.c_in; L.KS = p->desc.k; L.c_in_pad = p->c_in_pad;
+    L.variant = p->variant; L.w_packed = w_packed; L.bias = bias; L.m_c = m_c;
+    return cuda_check(launch_fold(L, (cudaStream_t)stream), "fold kernel launch");
+}
+
+cbs_status cbs_pack_input(const cbs_plan_t *p, const float *x_nchw, void *x_packed, float s_x,
+                          void *stream) {
+    CBS_TRY(check_plan(p));
+    CBS_TRY(check_ptr(x_nchw, "x_nchw"));
+    CBS_TRY(check_ptr(x_packed, "x_packed"));
+    const cbs_layer_desc &d = p->desc;
+    if (d.n == 0) return CBS_OK;
+    int dtype = 0;
+    if (d.prec == CBS_BF16) dtype = 1;
+    if (d.prec == CBS_INT8) {
+        dtype = 2;
+        if (!(s_x > 0.0f)) return fail(CBS_ERR_INVALID_ARG, "s_x must be > 0 for INT8");
+    }
+    const int to_nhwc = d.in_layout == CBS_NHWC;
+    return cuda_check(launch_pack_input(x_nchw, x_packed, d.n, d.c_in, d.h, d.w, p->c_in_pad, to_nhwc,
+                                        dtype, s_x, (cudaStream_t)stream),
+                      "pack kernel launch");
+}
+
+static cbs_status check_conv_common(const cbs_plan_t *p, const void *x, const void *w, const void *bias,
+                                    const void *y, const void *ws, size_t ws_bytes) {
+    CBS_TRY(check_ptr(x, "x"));
+    CBS_TRY(check_ptr(w, "w_packed"));
+    CBS_TRY(check_ptr(bias, "bias"));
+    CBS_TRY(check_ptr(y, "y"));
+    if (p->workspace_bytes > 0) {
+        if (!ws) return fail(CBS_ERR_WORKSPACE, "plan needs %zu bytes of workspace, got NULL", p->workspace_bytes);
+        if (ws_bytes < p->workspace_bytes)
+            return fail(CBS_ERR_WORKSPACE, "workspace %zu bytes < %zu required", ws_bytes, p->workspace_bytes);
+        CBS_TRY(check_ptr(ws, "workspace"));
+    }
+    return CBS_OK;
+}
+
+cbs_status cbs_conv_bn_silu_f32(const cbs_plan_t *p, const void *x, const void *w_packed,
+                                const float *bias, void *y, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+    CBS_TRY(check_plan(p));
+    if (p->variant == CBS_VARIANT_TC_INT8)
+        return fail(CBS_ERR_INVALID_ARG, "INT8 plans run through cbs_conv_bn_silu_i8");
+    CBS_TRY(check_conv_common(p, x, w_packed, bias, y, workspace, workspace_bytes));
+    const cbs_layer_desc &d = p->desc;
+    if (d.n == 0) return CBS_OK;
+    if (p->variant == CBS_VARIANT_SIMT_FP32) {
+        SimtLaunch L;
+        std::memset(&L, 0, sizeof(L));
+        L.x = (const float *)x; L.w = (const float *)w_packed; L.bias = bias; L.y = (float *)y;
+        L.N = d.n; L.C = d.c_in; L.H = d.h; L.W = d.w; L.Cout = d.c_out; L.OH = p->oh; L.OW = p->ow;
+        L.KS = d.k; L.stride = d.stride; L.pad = d.pad;
+        L.M = d.n * p->oh * p->ow;
+        L.K = d.k * d.k * d.c_in;
+        L.split = p->split_k;
+        L.k_chunk = (L.K + L.split - 1) / L.split;
+        L.k_chunk = (L.k_chunk + kSimtBK - 1) / kSimtBK * kSimtBK;
+        L.out_row_stride = p->out_row_stride;
+        L.tile = simt_tile_index(*p);
+        if (L.tile < 0) return fail(CBS_ERR_PLAN_MISMATCH, "unknown SIMT tile %dx%d", p->block_m, p->block_n);
+        L.in_nhwc = d.in_layout == CBS_NHWC;
+        L.out_nhwc = d.out_layout == CBS_NHWC;
+        L.m_tiles = p->m_tiles; L.n_tiles = p->n_tiles;
+        if (L.split > 1) {
+            const size_t tiles = (size_t)p->m_tiles * p->n_tiles;
+            const size_t counters = (tiles * sizeof(unsigned) + 255) / 256 * 256;
+            L.counters = (unsigned int *)workspace;
+            L.partials = (float *)((char *)workspace + counters);
+        }
+        return cuda_check(launch_simt(L, (cudaStream_t)stream), "SIMT kernel launch");
+    }
+    return launch_tc(*p, x, w_packed, bias, nullptr, 0.0f, y, workspace, (cudaStream_t)stream);
+}
+
+cbs_status cbs_conv_bn_silu_i8(const cbs_plan_t *p, const int8_t *x, const void *w_packed,
+                               const int32_t *bias_i32, const float *m_c, float s_y, int8_t *y,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+    CBS_TRY(check_plan(p));
+    if (p->variant != CBS_VARIANT_TC_INT8)
+        return fail(CBS_ERR_INVALID_ARG, "plan is not an INT8 plan");
+    CBS_TRY(check_conv_common(p, x, w_packed, bias_i32, y, workspace, workspace_bytes));
+    CBS_TRY(check_ptr(m_c, "m_c"));
+    if (!(s_y > 0.0f) || !(s_y < 3.0e38f)) return fail(CBS_ERR_INVALID_ARG, "s_y must be a positive finite float");
+    if (p->desc.n == 0) return CBS_OK;
+    const float inv_s_y = 1.0f / s_y;
+    return launch_tc(*p, x, w_packed, bias_i32, m_c, inv_s_y, y, workspace, (cudaStream_t)stream);
+}
+
+cbs_status cbs_upsample2x_concat(const void *a, int ca, const void *b, int cb, void *out, int n, int h,
+                                 int w, int layout, int elem_bytes, void *stream) {
+    CBS_TRY(check_ptr(a, "a"));
+    CBS_TRY(check_ptr(b, "b"));
+    CBS_TRY(check_ptr(out, "out"));
+    if (ca < 1 || cb < 1 || n < 0 || h < 2 || w < 2 || (h & 1) || (w & 1))
+        return fail(CBS_ERR_INVALID_ARG, "bad upsample/concat shape (ca=%d cb=%d n=%d h=%d w=%d; h, w even)",
+                    ca, cb, n, h, w);
+    if (layout != CBS_NCHW && layout != CBS_NHWC) return fail(CBS_ERR_INVALID_ARG, "unknown layout %d", layout);
+    if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4)
+        return fail(CBS_ERR_INVALID_ARG, "elem_bytes must be 1, 2 or 4 (got %d; ca=%d cb=%d n=%d h=%d w=%d layout=%d)",
+                    elem_bytes, ca, cb, n, h, w, layout);
+    if (n == 0) return CBS_OK;
+    return cuda_check(launch_upsample_concat(a, ca, b, cb, out, n, h, w, layout == CBS_NHWC, elem_bytes,
+                                             (cudaStream_t)stream),
+                      "upsample/concat launch");
+}
+
+cbs_status cbs_workspace_init(void *workspace, size_t bytes, void *stream) {
+    if (bytes == 0) return CBS_OK;
+    CBS_TRY(check_ptr(workspace, "workspace"));
+    return cuda_check(cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream), "cudaMemsetAsync");
+}
+
+cbs_status cbs_read_device_status(int *status_out, int reset, void *stream) {
+    if (!status_out) return fail(CBS_ERR_INVALID_ARG, "status_out is NULL");
+    return read_and_reset_status(status_out, reset, (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// cbs_internal.cuh -- declarations shared by the library's translation units.
+// Nothing here is part of the public ABI (include/cbs.h is).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/cbs.h"
+
+namespace cbs {
+
+// GB300: 152 SMs on two dies.  cbs_plan is host-only and makes no CUDA call,
+// so it plans for this count; launches size their grids from the plan.
+constexpr int kNumSMs = 152;
+
+// Records a message for the calling thread and returns `s`.
+cbs_status fail(cbs_status s, const char *fmt, ...);
+// Maps a CUDA error to CBS_ERR_CUDA (with message) or CBS_OK.
+cbs_status cuda_check(cudaError_t e, const char *what);
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- SIMT FP32
+// Tile configurations of the CUDA-core kernel (index = plan->block_k slot).
+struct SimtTile { int bm, bn, tm, tn; };
+constexpr int kSimtBK = 8;
+constexpr SimtTile kSimtTiles[] = {
+    {128, 128, 8, 8},  // 0: 256 threads
+    {128, 64, 8, 8},   // 1: 128 threads
+    {64, 64, 4, 4},    // 2: 256 threads
+    {128, 32, 4, 4},   // 3: 256 threads
+    {256, 16, 4, 4},   // 4: 256 threads
+    {64, 128, 4, 8},   // 5: 256 threads
+};
+constexpr int kNumSimtTiles = sizeof(kSimtTiles) / sizeof(kSimtTiles[0]);
+
+struct SimtLaunch {
+    const float *x;
+    const float *w;       // [K][C_out]
+    const float *bias;    // [C_out]
+    float *y;
+    float *partials;      // split-K partial tiles (workspace)
+    unsigned int *counters;  // split-K arrival counters (workspace)
+    int N, C, H, W, Cout, OH, OW, KS, stride, pad;
+    int M, K, k_chunk, split;
+    int out_row_stride;
+    int tile;             // index into kSimtTiles
+    int in_nhwc, out_nhwc;
+    int m_tiles, n_tiles;
+};
+cudaError_t launch_simt(const SimtLaunch &L, cudaStream_t s);
+
+// ---------------------------------------------------------------- misc kernels
+struct FoldLaunch {
+    const float *w;           // [C_out][C_in][k][k]
+    const float *conv_bias;   // nullable
+    const float *gamma, *beta, *mean, *var;
+    float eps, s_x;
+    int C_out, C_in, KS, c_in_pad;
+    int variant;              // cbs_variant
+    void *w_packed;
+    void *bias;               // float or int32
+    float *m_c;               // INT8 only
+};
+cudaError_t launch_fold(const FoldLaunch &L, cudaStream_t s);
+
+// dtype codes for packing: 0 float, 1 bf16, 2 int8 (quantised with s_x)
+cudaError_t launch_pack_input(const float *x_nchw, void *out, int N, int C, int H, int W,
+                              int c_pad, int to_nhwc, int dtype, float s_x, cudaStream_t s);
+
+cudaError_t launch_upsample_concat(const void *a, int ca, const void *b, int cb, void *out,
+                                   int n, int h, int w, int nhwc, int elem_bytes,
+                                   cudaStream_t s);
+
+// Device-side status word (bounded waits that expired set it).
+unsigned int *device_status_word();  // device address for the current device, or nullptr
+cbs_status read_and_reset_status(int *status_out, int reset, cudaStream_t s);
+
+// ---------------------------------------------------------------- tensor-core path
+struct TcLaunch;  // defined in k_tc.cu
+cbs_status launch_tc(const cbs_plan_t &p, const void *x, const void *w_packed,
+                     const void *bias, const float *m_c, float inv_s_y, void *y,
+                     void *workspace, cudaStream_t s);
+// Host-side tile selection for the tensor-core variants (fills the tile
+// fields of the plan); returns CBS_OK or an error.
+cbs_status plan_tc(cbs_plan_t &p);
+
+}  // namespace cbs

@@ -1,0 +1,276 @@
+// k_misc.cu -- setup and glue kernels: BN folding and weight packing, the
+// chain-entry layout conversion, the upsample+concat neck glue, and the
+// device status word that bounded waits report into.
+#include <cuda_bf16.h>
+
+#include "cbs_internal.cuh"
+
+namespace cbs {
+namespace {
+
+// ------------------------------------------------------------------ folding
+// One CTA per output channel.  Float arithmetic is written with explicit
+// round-to-nearest intrinsics so nothing is contracted into an FMA: the INT8
+// codes, bias and scales must come out bit-identical to any other IEEE
+// evaluation of the same steps.
+//   s_c = gamma / sqrt(var + eps);   w' = w * s_c;   b' = beta - mean * s_c
+// (with a conv bias cb:  b' = beta + (cb - mean) * s_c).
+constexpr int kFoldThreads = 256;
+
+__global__ void __launch_bounds__(kFoldThreads) fold_kernel(const FoldLaunch a) {
+    const int co = blockIdx.x;
+    const int KK = a.KS * a.KS;
+    const int kin = a.C_in * KK;                 // OIHW row length
+    const int kpad = KK * a.c_in_pad;            // packed row length (tap-major)
+    const float s_c = __fdiv_rn(a.gamma[co], __fsqrt_rn(__fadd_rn(a.var[co], a.eps)));
+    const float *wrow = a.w + (size_t)co * kin;
+
+    float b_fold;
+    if (a.conv_bias) {
+        b_fold = __fadd_rn(a.beta[co], __fmul_rn(__fsub_rn(a.conv_bias[co], a.mean[co]), s_c));
+    } else {
+        b_fold = __fsub_rn(a.beta[co], __fmul_rn(a.mean[co], s_c));
+    }
+
+    if (a.variant == CBS_VARIANT_SIMT_FP32) {
+        float *out = static_cast<float *>(a.w_packed);
+        for (int k = threadIdx.x; k < kin; k += blockDim.x) {
+            const int tap = k / a.C_in, ci = k - tap * a.C_in;
+            out[(size_t)k * a.C_out + co] = __fmul_rn(wrow[ci * KK + tap], s_c);
+        }
+        if (threadIdx.x == 0) static_cast<float *>(a.bias)[co] = b_fold;
+        return;
+    }
+    if (a.variant == CBS_VARIANT_TC_TF32 || a.variant == CBS_VARIANT_TC_BF16) {
+        for (int k = threadIdx.x; k < kpad; k += blockDim.x) {
+            const int tap = k / a.c_in_pad, ci = k - tap * a.c_in_pad;
+            const float v = ci < a.C_in ? __fmul_rn(wrow[ci * KK + tap], s_c) : 0.0f;
+            if (a.variant == CBS_VARIANT_TC_TF32)
+                static_cast<float *>(a.w_packed)[(size_t)co * kpad + k] = v;
+            else
+                static_cast<__nv_bfloat16 *>(a.w_packed)[(size_t)co * kpad + k] = __float2bfloat16_rn(v);
+        }
+        if (threadIdx.x == 0) static_cast<float *>(a.bias)[co] = b_fold;
+        return;
+    }
+    // INT8: per-channel symmetric scale s_w = max|w'| / 127.
+    __shared__ float red[kFoldThreads / 32];
+    float amax = 0.0f;
+    for (int k = threadIdx.x; k < kin; k += blockDim.x)
+        amax = fmaxf(amax, fabsf(__fmul_rn(wrow[k], s_c)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = 0.0f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, red[i]);
+    float s_w = __fdiv_rn(amax, 127.0f);
+    if (s_w == 0.0f) s_w = 1.0f;
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.w_packed);
+    for (int k = threadIdx.x; k < kpad; k += blockDim.x) {
+        const int tap = k / a.c_in_pad, ci = k - tap * a.c_in_pad;
+        float q = 0.0f;
+        if (ci < a.C_in) {
+            q = rintf(__fdiv_rn(__fmul_rn(wrow[ci * KK + tap], s_c), s_w));
+            q = fminf(fmaxf(q, -127.0f), 127.0f);
+        }
+        out[(size_t)co * kpad + k] = __float2bfloat16_rn(q);  // exact: |q| <= 127
+    }
+    if (threadIdx.x == 0) {
+        const float mc = __fmul_rn(a.s_x, s_w);
+        const float bq = rintf(__fdiv_rn(b_fold, mc));
+        int32_t bi;
+        if (bq >= 2147483648.0f) bi = INT32_MAX;
+        else if (bq < -2147483648.0f) bi = INT32_MIN;
+        else bi = (int32_t)bq;
+        static_cast<int32_t *>(a.bias)[co] = bi;
+        a.m_c[co] = mc;
+    }
+}
+
+// ------------------------------------------------------------ entry packing
+// NCHW float -> NHWC (channels padded to c_pad with zeros) in float, bf16 or
+// int8 (q = rne(clamp(x / s_x, -128, 127))).  32x32 (w, c) tiles through
+// shared memory so both the read and the write are coalesced.
+template <typename T>
+__device__ __forceinline__ T convert_out(float v, float s_x);
+template <>
+__device__ __forceinline__ float convert_out<float>(float v, float) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 convert_out<__nv_bfloat16>(float v, float) {
+    return __float2bfloat16_rn(v);
+}
+template <>
+__device__ __forceinline__ int8_t convert_out<int8_t>(float v, float s_x) {
+    float q = __fdiv_rn(v, s_x);
+    q = fminf(fmaxf(q, -128.0f), 127.0f);
+    return (int8_t)rintf(q);
+}
+
+template <typename T>
+__global__ void pack_nhwc_kernel(const float *__restrict__ x, T *__restrict__ out, int C, int H,
+                                 int W, int c_pad, float s_x) {
+    __shared__ float tile[32][33];
+    const int w0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+    const int nh = blockIdx.z;  // n * H + h
+    const int n = nh / H, h = nh - n * H;
+    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+    for (int i = ty; i < 32; i += 8) {
+        const int c = c0 + i, w = w0 + tx;
+        float v = 0.0f;
+        if (c < C && w < W) v = x[(((size_t)n * C + c) * H + h) * W + w];
+        tile[i][tx] = v;
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+        const int w = w0 + i, c = c0 + tx;
+        if (w < W && c < c_pad) out[(((size_t)n * H + h) * W + w) * c_pad + c] = convert_out<T>(tile[tx][i], s_x);
+    }
+}
+
+template <typename T>
+__global__ void pack_nchw_kernel(const float *__restrict__ x, T *__restrict__ out, size_t count,
+                                 float s_x) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count;
+         i += (size_t)gridDim.x * blockDim.x)
+        out[i] = convert_out<T>(x[i], s_x);
+}
+
+// ------------------------------------------------------------------- glue
+// NHWC, 16-byte vectors: out[n,h,w,:] = [a[n,h/2,w/2,:], b[n,h,w,:]].
+__global__ void upcat_nhwc_vec_kernel(const uint4 *__restrict__ a, int va, const uint4 *__restrict__ b,
+                                      int vb, uint4 *__restrict__ out, int n, int h, int w) {
+    const int vt = va + vb;
+    const size_t total = (size_t)n * h * w * vt;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const int v = (int)(i % vt);
+        const size_t pix = i / vt;
+        const int x = (int)(pix % w);
+        const size_t nhh = pix / w;
+        const int y = (int)(nhh % h);
+        const int img = (int)(nhh / h);
+        uint4 val;
+        if (v < va)
+            val = a[(((size_t)img * (h / 2) + y / 2) * (w / 2) + x / 2) * va + v];
+        else
+            val = b[pix * vb + (v - va)];
+        out[i] = val;
+    }
+}
+
+template <typename T>
+__global__ void upcat_elem_kernel(const T *__restrict__ a, int ca, const T *__restrict__ b, int cb,
+                                  T *__restrict__ out, int n, int h, int w, int nhwc) {
+    const int ct = ca + cb;
+    const size_t total = (size_t)n * h * w * ct;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        int c, x, y, img;
+        if (nhwc) {
+            c = (int)(i % ct);
+            size_t r = i / ct;
+            x = (int)(r % w); r /= w;
+            y = (int)(r % h); img = (int)(r / h);
+        } else {
+            x = (int)(i % w);
+            size_t r = i / w;
+            y = (int)(r % h); r /= h;
+            c = (int)(r % ct); img = (int)(r / ct);
+        }
+        T val;
+        if (c < ca) {
+            const int ys = y / 2, xs = x / 2;
+            val = nhwc ? a[(((size_t)img * (h / 2) + ys) * (w / 2) + xs) * ca + c]
+                       : a[(((size_t)img * ca + c) * (h / 2) + ys) * (w / 2) + xs];
+        } else {
+            const int cc = c - ca;
+            val = nhwc ? b[(((size_t)img * h + y) * w + x) * cb + cc]
+                       : b[(((size_t)img * cb + cc) * h + y) * w + x];
+        }
+        out[i] = val;
+    }
+}
+
+__device__ unsigned int g_cbs_status_word;
+
+int grid_for(size_t count, int threads) {
+    size_t blocks = (count + threads - 1) / threads;
+    const size_t cap = (size_t)kNumSMs * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return (int)blocks;
+}
+
+}  // namespace
+
+cudaError_t launch_fold(const FoldLaunch &L, cudaStream_t s) {
+    fold_kernel<<<L.C_out, kFoldThreads, 0, s>>>(L);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_input(const float *x, void *out, int N, int C, int H, int W, int c_pad,
+                              int to_nhwc, int dtype, float s_x, cudaStream_t s) {
+    if (to_nhwc) {
+        dim3 grid((W + 31) / 32, (c_pad + 31) / 32, N * H), block(32, 8);
+        if (dtype == 0) pack_nhwc_kernel<float><<<grid, block, 0, s>>>(x, (float *)out, C, H, W, c_pad, s_x);
+        else if (dtype == 1) pack_nhwc_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(x, (__nv_bfloat16 *)out, C, H, W, c_pad, s_x);
+        else pack_nhwc_kernel<int8_t><<<grid, block, 0, s>>>(x, (int8_t *)out, C, H, W, c_pad, s_x);
+    } else {
+        const size_t count = (size_t)N * C * H * W;
+        const int g = grid_for(count, 256);
+        if (dtype == 0) pack_nchw_kernel<float><<<g, 256, 0, s>>>(x, (float *)out, count, s_x);
+        else if (dtype == 1) pack_nchw_kernel<__nv_bfloat16><<<g, 256, 0, s>>>(x, (__nv_bfloat16 *)out, count, s_x);
+        else pack_nchw_kernel<int8_t><<<g, 256, 0, s>>>(x, (int8_t *)out, count, s_x);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_upsample_concat(const void *a, int ca, const void *b, int cb, void *out, int n,
+                                   int h, int w, int nhwc, int eb, cudaStream_t s) {
+    const bool vec = nhwc && (ca * eb) % 16 == 0 && (cb * eb) % 16 == 0 &&
+                     aligned16(a) && aligned16(b) && aligned16(out);
+    if (vec) {
+        const int va = ca * eb / 16, vb = cb * eb / 16;
+        const size_t total = (size_t)n * h * w * (va + vb);
+        upcat_nhwc_vec_kernel<<<grid_for(total, 256), 256, 0, s>>>(
+            (const uint4 *)a, va, (const uint4 *)b, vb, (uint4 *)out, n, h, w);
+    } else {
+        const size_t total = (size_t)n * h * w * (ca + cb);
+        const int g = grid_for(total, 256);
+        if (eb == 4) upcat_elem_kernel<uint32_t><<<g, 256, 0, s>>>((const uint32_t *)a, ca, (const uint32_t *)b, cb, (uint32_t *)out, n, h, w, nhwc);
+        else if (eb == 2) upcat_elem_kernel<uint16_t><<<g, 256, 0, s>>>((const uint16_t *)a, ca, (const uint16_t *)b, cb, (uint16_t *)out, n, h, w, nhwc);
+        else upcat_elem_kernel<uint8_t><<<g, 256, 0, s>>>((const uint8_t *)a, ca, (const uint8_t *)b, cb, (uint8_t *)out, n, h, w, nhwc);
+    }
+    return cudaGetLastError();
+}
+
+unsigned int *device_status_word() {
+    // One address per device; looked up once per device.
+    static unsigned int *cache[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!cache[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_cbs_status_word) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<unsigned int *>(p);
+    }
+    return cache[dev];
+}
+
+cbs_status read_and_reset_status(int *status_out, int reset, cudaStream_t s) {
+    unsigned int v = 0;
+    cbs_status st = cuda_check(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+    if (st != CBS_OK) return st;
+    st = cuda_check(cudaMemcpyFromSymbol(&v, g_cbs_status_word, sizeof(v)), "read status word");
+    if (st != CBS_OK) return st;
+    if (reset) {
+        const unsigned int zero = 0;
+        st = cuda_check(cudaMemcpyToSymbol(g_cbs_status_word, &zero, sizeof(zero)), "reset status word");
+        if (st != CBS_OK) return st;
+    }
+    *status_out = v ? (int)CBS_ERR_TIMEOUT : (int)CBS_OK;
+    return CBS_OK;
+}
+
+}  // namespace cbs

@@ -1,0 +1,128 @@
+"""Torch-facing helpers over the C ABI: device buffers from PyTorch's caching
+allocator, the current CUDA stream, and the calls of include/cbs.h.
+
+Nothing here computes: packing, folding and the fused layer all run in
+libcbs.so's kernels.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _binding as B
+
+_TORCH_DTYPE = {B.CBS_FP32: torch.float32, B.CBS_TF32: torch.float32,
+                B.CBS_BF16: torch.bfloat16, B.CBS_INT8: torch.int8}
+
+
+def current_stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def make_desc(n, c_in, h, w, c_out, k, stride, pad=None, prec=B.CBS_FP32, in_layout=None,
+              out_layout=None, force_variant=-1, force_split_k=0, force_block_n=0,
+              out_row_stride=0) -> B.cbs_layer_desc:
+    if pad is None:
+        pad = k // 2
+    if in_layout is None:
+        in_layout = B.CBS_NCHW if prec == B.CBS_FP32 else B.CBS_NHWC
+    if out_layout is None:
+        out_layout = in_layout
+    d = B.cbs_layer_desc()
+    for name, v in dict(n=n, c_in=c_in, h=h, w=w, c_out=c_out, k=k, stride=stride, pad=pad,
+                        in_layout=in_layout, out_layout=out_layout, prec=prec,
+                        force_variant=force_variant, force_split_k=force_split_k,
+                        force_block_n=force_block_n, out_row_stride=out_row_stride).items():
+        setattr(d, name, int(v))
+    return d
+
+
+def _dev_f32(a, device):
+    t = torch.as_tensor(a, dtype=torch.float32)
+    return t.to(device).contiguous()
+
+
+class FusedConvBnSilu:
+    """One planned layer with its folded weights resident on the device."""
+
+    def __init__(self, desc: B.cbs_layer_desc, w, gamma, beta, mean, var, eps: float,
+                 conv_bias=None, s_x: float = 0.0, device="cuda"):
+        self.device = torch.device(device)
+        self.desc = desc
+        self.plan = B.cbs_plan(desc)
+        self.prec = desc.prec
+        self.s_x = float(s_x)
+        p = self.plan
+        self.w_packed = torch.empty(p.w_packed_bytes, dtype=torch.uint8, device=self.device)
+        self.bias = torch.empty(p.bias_bytes, dtype=torch.uint8, device=self.device)
+        self.m_c = (torch.empty(desc.c_out, dtype=torch.float32, device=self.device)
+                    if self.prec == B.CBS_INT8 else None)
+        ws = max(int(p.workspace_bytes), 0)
+        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=self.device) if ws else None
+        s = current_stream()
+        raw = [_dev_f32(a, self.device) for a in (w, gamma, beta, mean, var)]
+        cb = None if conv_bias is None else _dev_f32(conv_bias, self.device)
+        B.cbs_fold_bn(p, raw[0], cb, raw[1], raw[2], raw[3], raw[4], float(eps), self.s_x,
+                      self.w_packed, self.bias, self.m_c, s)
+        if self.workspace is not None:
+            B.cbs_workspace_init(self.workspace, int(p.workspace_bytes), s)
+        self._keep = (raw, cb)  # inputs of the asynchronous fold stay alive
+
+    # ---------------------------------------------------------------- shapes
+    @property
+    def x_dtype(self):
+        return _TORCH_DTYPE[self.prec]
+
+    def x_shape(self):
+        d, p = self.desc, self.plan
+        if p.variant == B.CBS_VARIANT_SIMT_FP32 and d.in_layout == B.CBS_NCHW:
+            return (d.n, d.c_in, d.h, d.w)
+        return (d.n, d.h, d.w, p.c_in_pad)
+
+    def y_shape(self):
+        d, p = self.desc, self.plan
+        if d.out_layout == B.CBS_NCHW:
+            return (d.n, d.c_out, p.oh, p.out_row_stride)
+        return (d.n, p.oh, p.ow, d.c_out)
+
+    def empty_x(self):
+        return torch.empty(self.x_shape(), dtype=self.x_dtype, device=self.device)
+
+    def empty_y(self):
+        return torch.empty(self.y_shape(), dtype=self.x_dtype, device=self.device)
+
+    # ----------------------------------------------------------------- calls
+    def pack_input(self, x_nchw: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+        """NCHW float32 device tensor -> the plan's input format (kernel)."""
+        assert x_nchw.is_cuda and x_nchw.dtype == torch.float32 and x_nchw.is_contiguous()
+        out = self.empty_x() if out is None else out
+        B.cbs_pack_input(self.plan, x_nchw, out, self.s_x, current_stream())
+        return out
+
+    def __call__(self, x: torch.Tensor, y: torch.Tensor | None = None, s_y: float | None = None,
+                 stream: int | None = None) -> torch.Tensor:
+        y = self.empty_y() if y is None else y
+        s = current_stream() if stream is None else stream
+        ws_bytes = int(self.plan.workspace_bytes)
+        if self.prec == B.CBS_INT8:
+            assert s_y is not None
+            B.cbs_conv_bn_silu_i8(self.plan, x, self.w_packed, self.bias, self.m_c, float(s_y), y,
+                                  self.workspace, ws_bytes, s)
+        else:
+            B.cbs_conv_bn_silu_f32(self.plan, x, self.w_packed, self.bias, y, self.workspace,
+                                   ws_bytes, s)
+        return y
+
+
+def upsample2x_concat(a: torch.Tensor, b: torch.Tensor, layout: int, out: torch.Tensor | None = None):
+    """Neck glue: concat(upsample2x(a), b) along channels, in the given layout."""
+    if layout == B.CBS_NHWC:
+        n, h, w, cb = b.shape
+        ca = a.shape[3]
+        shape = (n, h, w, ca + cb)
+    else:
+        n, cb, h, w = b.shape
+        ca = a.shape[1]
+        shape = (n, ca + cb, h, w)
+    out = torch.empty(shape, dtype=b.dtype, device=b.device) if out is None else out
+    B.cbs_upsample2x_concat(a, ca, b, cb, out, n, h, w, layout, b.element_size(), current_stream())
+    return out

@@ -1,0 +1,226 @@
+/*
+ * cbs.h -- C ABI of the fused Conv2d + folded BatchNorm + SiLU library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation (page 1, "YOLO26N Inference Optimisation", sections
+ * "NHWC migration -- What NHWC is and why it matters" and "Improvements",
+ * #2 and #7; page 3, "Edge optimisation of YOLO26", "Design notes"):
+ *
+ *   y[n,co,oh,ow] = SiLU( sum_{r,s,ci} x[n, oh*S-P+r, ow*S-P+s, ci] * w'[co,r,s,ci] + b'[co] )
+ *   w'[co,...] = w[co,...] * gamma[co] / sqrt(var[co] + eps)       (BN folded into the weights)
+ *   b'[co]     = beta[co] - mean[co] * gamma[co] / sqrt(var[co] + eps)
+ *   SiLU(z)    = z / (1 + exp(-z))
+ *
+ * x is zero outside the image.  Seen as a GEMM (page 1, "What NHWC is and why
+ * it matters", item 3): A = [N*OH*OW, k*k*C_in] (the implicit im2col matrix),
+ * B = [k*k*C_in, C_out].
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer argument is a DEVICE pointer unless the comment says host.
+ *    The caller allocates and owns every buffer; the library never allocates,
+ *    frees or synchronises device memory (except cbs_read_device_status,
+ *    which synchronises the given stream by design).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    All GPU work is enqueued on it and is asynchronous to the host.
+ *  - Arguments are checked before anything is enqueued; on error nothing is
+ *    enqueued and a status < 0 is returned.  cbs_last_error() then returns a
+ *    message for the calling thread.
+ *  - Device buffers must be 16-byte aligned (CBS_ERR_MISALIGNED otherwise).
+ *  - All functions are re-entrant; message state is thread-local.
+ */
+#ifndef CBS_H
+#define CBS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CBS_ABI_VERSION 1
+
+/* Exported symbols (the library is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define CBS_API __attribute__((visibility("default")))
+#else
+#define CBS_API
+#endif
+
+typedef enum cbs_status {
+    CBS_OK = 0,
+    CBS_ERR_INVALID_ARG = -1,   /* bad shape, null pointer, unknown enum */
+    CBS_ERR_UNSUPPORTED = -2,   /* valid but not implemented (e.g. layout for a variant) */
+    CBS_ERR_MISALIGNED = -3,    /* a buffer is not 16-byte aligned */
+    CBS_ERR_WORKSPACE = -4,     /* workspace missing or smaller than plan->workspace_bytes */
+    CBS_ERR_CUDA = -5,          /* a CUDA runtime/driver call failed (launch, tensor map) */
+    CBS_ERR_TIMEOUT = -6,       /* a bounded device-side wait expired (see cbs_read_device_status) */
+    CBS_ERR_PLAN_MISMATCH = -7  /* plan is not a plan of this library version */
+} cbs_status;
+
+/* Activation layouts (page 1, "What must change in the kernels"). */
+typedef enum cbs_layout { CBS_NCHW = 0, CBS_NHWC = 1 } cbs_layout;
+
+/* Arithmetic variant.  Storage type of x and y: FP32 and TF32 use float,
+ * BF16 uses bfloat16, INT8 uses int8.  Accumulation: float (FP32 FMA on CUDA
+ * cores; TF32/BF16 tensor cores), exact integer for INT8. */
+typedef enum cbs_precision { CBS_FP32 = 0, CBS_TF32 = 1, CBS_BF16 = 2, CBS_INT8 = 3 } cbs_precision;
+
+/* Kernel family a plan selects. */
+typedef enum cbs_variant {
+    CBS_VARIANT_SIMT_FP32 = 0,  /* CUDA-core implicit GEMM, FP32 FMA */
+    CBS_VARIANT_TC_TF32 = 1,    /* tcgen05 kind::tf32, TMA im2col/tile loads, TMEM accumulator */
+    CBS_VARIANT_TC_BF16 = 2,    /* tcgen05 kind::f16 (bf16 operands) */
+    CBS_VARIANT_TC_INT8 = 3     /* int8 values on tcgen05 kind::f16, exact integer sums */
+} cbs_variant;
+
+/* One layer.  Padding is symmetric; OH = (H + 2*pad - k)/stride + 1. */
+typedef struct cbs_layer_desc {
+    int n, c_in, h, w, c_out, k, stride, pad;
+    int in_layout;       /* cbs_layout of x */
+    int out_layout;      /* cbs_layout of y */
+    int prec;            /* cbs_precision */
+    int force_variant;   /* -1: choose from prec; else a cbs_variant compatible with prec */
+    int force_split_k;   /* 0: choose; else the number of K splits to use (>= 1) */
+    int force_block_n;   /* 0: choose; else the N tile width (must be one the variant supports) */
+    int out_row_stride;  /* NCHW output only: elements between output rows; 0 = OW.
+                            Must be >= OW.  Columns OW..stride-1 are never written. */
+} cbs_layer_desc;
+
+/* A plan: plain data, owned by the caller, filled by cbs_plan. */
+typedef struct cbs_plan_t {
+    uint32_t size;          /* sizeof(cbs_plan_t); checked by every call */
+    uint32_t abi_version;   /* CBS_ABI_VERSION */
+    int variant;            /* cbs_variant */
+    int block_m, block_n, block_k;  /* CTA tile: output pixels x output channels x K step */
+    int stages;             /* shared-memory pipeline depth */
+    int split_k;            /* number of K partitions (>= 1) */
+    int c_in_pad;           /* channels per input pixel as stored (NHWC tensor-core variants
+                               pad C_in to a 16-byte multiple; SIMT: = c_in) */
+    int k_gemm;             /* GEMM K = k*k*c_in_pad: length of one packed weight row */
+    int oh, ow;
+    int out_row_stride;     /* NCHW: elements between output rows (>= ow) */
+    int m_tiles, n_tiles;   /* tile grid */
+    int grid_ctas;          /* CTAs launched */
+    int threads;            /* threads per CTA */
+    int smem_bytes;         /* dynamic shared memory per CTA */
+    size_t x_bytes;         /* bytes of x the kernel reads, in the plan's input format */
+    size_t y_bytes;         /* bytes of y, including row padding */
+    size_t w_packed_bytes;  /* bytes of the packed weight buffer */
+    size_t bias_bytes;      /* bytes of the bias buffer (float or int32 per channel) */
+    size_t workspace_bytes; /* scratch the call needs (0 = none) */
+    cbs_layer_desc desc;    /* copy of the request */
+} cbs_plan_t;
+
+/*
+ * cbs_plan -- choose a kernel variant and tile configuration for one layer
+ * (page 1, "Key observations" 1 and "Improvements" #1: one tile configuration
+ * per call-site shape instead of one for all 40 convolutions).
+ *   d:   host pointer to the layer; out: host pointer, filled on success.
+ * Host only: makes no CUDA call and may be used without a GPU.
+ * Input format the plan expects (see x_bytes):
+ *   SIMT FP32: x in d->in_layout, float, exactly C_in channels.
+ *   TF32/BF16/INT8: x NHWC with c_in_pad channels (extra channels zero).
+ * Errors: CBS_ERR_INVALID_ARG (shape, enum), CBS_ERR_UNSUPPORTED.
+ */
+CBS_API cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out);
+
+/*
+ * cbs_fold_bn -- one-time weight transform (page 1, "Weight layout";
+ * "Improvements" #7; page 3, "Design notes", per-channel weights).
+ * Folds inference BatchNorm into the weights and bias, re-lays the weights
+ * from [C_out][C_in][k][k] to the variant's K-major packed form with k-order
+ * (r, s, ci), and casts or quantises them:
+ *   SIMT FP32: float  [k*k*C_in][C_out]
+ *   TF32:      float  [C_out][k*k*c_in_pad]   (padding channels zero)
+ *   BF16:      bf16   [C_out][k*k*c_in_pad]   (round to nearest even)
+ *   INT8:      int8 codes held exactly as bf16 [C_out][k*k*c_in_pad];
+ *              s_w[c] = max|w'[c,:]| / 127, q = rne(w'/s_w), m_c[c] = s_x * s_w[c],
+ *              bias_i32[c] = rne(b'[c] / m_c[c]) saturated.
+ * Arguments (device): w_oihw float[C_out*C_in*k*k]; conv_bias float[C_out] or
+ * NULL; gamma, beta, mean, var float[C_out]; eps > 0.  s_x: activation scale
+ * (INT8 only, else ignored).  Outputs: w_packed (plan->w_packed_bytes), bias
+ * (float[C_out], or int32[C_out] for INT8), m_c (float[C_out], INT8 only,
+ * may be NULL otherwise).  The float arithmetic uses fixed IEEE operations
+ * (no contraction), so the INT8 codes are reproducible bit for bit.
+ */
+CBS_API cbs_status cbs_fold_bn(const cbs_plan_t *p, const float *w_oihw, const float *conv_bias,
+                       const float *gamma, const float *beta, const float *mean,
+                       const float *var, float eps, float s_x,
+                       void *w_packed, void *bias, float *m_c, void *stream);
+
+/*
+ * cbs_pack_input -- chain-entry layout step (page 1, "The all-or-nothing
+ * constraint", item 1: one NCHW->NHWC conversion at graph entry).
+ * x_nchw: float [N][C_in][H][W].  x_packed: the plan's input format
+ * (plan->x_bytes): SIMT with NCHW input: a copy; SIMT with NHWC input: float
+ * NHWC; TF32: float NHWC padded to c_in_pad with zeros; BF16: bf16 (RNE);
+ * INT8: int8 q = rne(clamp(x / s_x, -128, 127)).
+ */
+CBS_API cbs_status cbs_pack_input(const cbs_plan_t *p, const float *x_nchw, void *x_packed, float s_x,
+                          void *stream);
+
+/*
+ * cbs_conv_bn_silu_f32 -- the fused layer for the FP32, TF32 and BF16
+ * variants.  x: plan input format; w_packed, bias: from cbs_fold_bn; y: output
+ * in d.out_layout, float for FP32/TF32, bf16 for BF16 (plan->y_bytes);
+ * workspace: plan->workspace_bytes bytes (may be NULL when that is 0) which
+ * must have been zeroed once with cbs_workspace_init before its first use;
+ * every call leaves it ready for the next one.  A workspace must not be
+ * shared by calls that may run concurrently.
+ */
+CBS_API cbs_status cbs_conv_bn_silu_f32(const cbs_plan_t *p, const void *x, const void *w_packed,
+                                const float *bias, void *y, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/*
+ * cbs_conv_bn_silu_i8 -- the fused INT8 layer (page 3, "Highlights" and
+ * "Design notes": per-output-channel weight scales, one activation scale).
+ *   acc   = sum q_x * q_w + bias_i32         (exact integer)
+ *   t     = float(acc) * m_c[co]
+ *   u     = t / (1 + e(-t))                   (SiLU in float; e = the library's
+ *                                              Cody-Waite/Taylor exp, bit-specified)
+ *   q_y   = rne(clamp(u * (1/s_y), -128, 127))
+ * x: int8 NHWC with c_in_pad channels; y: int8 in d.out_layout.
+ * Workspace rules as for cbs_conv_bn_silu_f32.
+ */
+CBS_API cbs_status cbs_conv_bn_silu_i8(const cbs_plan_t *p, const int8_t *x, const void *w_packed,
+                               const int32_t *bias_i32, const float *m_c, float s_y,
+                               int8_t *y, void *workspace, size_t workspace_bytes,
+                               void *stream);
+
+/*
+ * cbs_upsample2x_concat -- neck glue between two fused layers (page 1,
+ * "Op-by-op impact", upsample_nearest2d and channel_cat):
+ *   out[n, h, w, :] = concat( a[n, h/2, w/2, 0:ca], b[n, h, w, 0:cb] )
+ * layout: CBS_NHWC or CBS_NCHW for all three tensors; elem_bytes: 1, 2 or 4.
+ * a: [n][h/2][w/2][ca]; b, out: [n][h][w][cb] and [n][h][w][ca+cb] (as NHWC).
+ */
+CBS_API cbs_status cbs_upsample2x_concat(const void *a, int ca, const void *b, int cb, void *out,
+                                 int n, int h, int w, int layout, int elem_bytes,
+                                 void *stream);
+
+/* Zero a workspace before its first use (cudaMemsetAsync on `stream`). */
+CBS_API cbs_status cbs_workspace_init(void *workspace, size_t bytes, void *stream);
+
+/*
+ * cbs_read_device_status -- synchronise `stream`, then report whether any
+ * kernel of this library on the current device gave up a bounded wait since
+ * the last reset: *status_out (host) receives CBS_OK or CBS_ERR_TIMEOUT.
+ * reset != 0 clears the flag.
+ */
+CBS_API cbs_status cbs_read_device_status(int *status_out, int reset, void *stream);
+
+/* Static string for a status code. */
+CBS_API const char *cbs_status_string(cbs_status s);
+
+/* Message for the last failing call on this thread ("" if none). */
+CBS_API const char *cbs_last_error(void);
+
+/* CBS_ABI_VERSION of the loaded library. */
+CBS_API int cbs_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CBS_H */

@@ -1,0 +1,117 @@
+"""Host-side checks of the C ABI: the library loads without a GPU, exports
+every function include/cbs.h declares, and its planner and argument checks
+behave as documented (none of these calls reach the GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conv_bn_silu_gb300 import _binding as B
+from conv_bn_silu_gb300 import workloads as wl
+from conv_bn_silu_gb300.layer import make_desc
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "cbs.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"CBS_API\s+[\w\s\*]+?\b(cbs_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(cuda_lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for name in names:
+        assert hasattr(cuda_lib, name), name
+    assert set(names) == set(B.EXPORTED)
+
+
+def test_abi_version_and_struct_sizes(cuda_lib):
+    assert B.cbs_abi_version() == 1
+    plan = B.cbs_plan(make_desc(1, 16, 40, 40, 32, 3, 1))
+    assert plan.size == ctypes.sizeof(B.cbs_plan_t)
+    assert plan.abi_version == 1
+
+
+def test_status_strings(cuda_lib):
+    for code, name in [(0, "CBS_OK"), (-1, "CBS_ERR_INVALID_ARG"), (-2, "CBS_ERR_UNSUPPORTED"),
+                       (-3, "CBS_ERR_MISALIGNED"), (-4, "CBS_ERR_WORKSPACE"), (-5, "CBS_ERR_CUDA"),
+                       (-6, "CBS_ERR_TIMEOUT"), (-7, "CBS_ERR_PLAN_MISMATCH")]:
+        assert B.cbs_status_string(code) == name
+
+
+@pytest.mark.parametrize("i", range(len(wl.LAYER_LIST)))
+def test_plan_fp32_layer_list(cuda_lib, i):
+    s = wl.LAYER_LIST[i]
+    p = B.cbs_plan(make_desc(1, s.c_in, s.h, s.width, s.c_out, s.k, s.stride))
+    assert p.variant == B.CBS_VARIANT_SIMT_FP32
+    assert (p.oh, p.ow) == (s.oh, s.ow)
+    assert p.out_row_stride == s.ow
+    assert p.x_bytes == s.c_in * s.h * s.width * 4
+    assert p.y_bytes == s.c_out * s.oh * s.ow * 4
+    assert p.w_packed_bytes == s.c_out * s.c_in * s.k * s.k * 4
+    assert p.m_tiles * p.block_m >= s.oh * s.ow
+    assert p.n_tiles * p.block_n >= s.c_out
+    assert p.split_k >= 1 and p.grid_ctas == p.m_tiles * p.n_tiles * p.split_k
+    assert (p.workspace_bytes > 0) == (p.split_k > 1)
+
+
+def test_plan_padded_row_stride(cuda_lib):
+    p = B.cbs_plan(make_desc(1, 16, 40, 40, 32, 3, 1, out_row_stride=48))
+    assert p.out_row_stride == 48 and p.y_bytes == 32 * 40 * 48 * 4
+
+
+def test_plan_forced_split(cuda_lib):
+    for split in (1, 2, 5, 9):
+        p = B.cbs_plan(make_desc(1, 256, 20, 20, 256, 3, 1, force_split_k=split))
+        assert p.split_k == split
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n=-1), B.CBS_ERR_INVALID_ARG),
+    (dict(c_in=0), B.CBS_ERR_INVALID_ARG),
+    (dict(pad=3), B.CBS_ERR_UNSUPPORTED),
+    (dict(prec=7), B.CBS_ERR_INVALID_ARG),
+    (dict(out_row_stride=39), B.CBS_ERR_INVALID_ARG),
+    (dict(out_row_stride=48, out_layout=B.CBS_NHWC), B.CBS_ERR_INVALID_ARG),
+    (dict(force_variant=2), B.CBS_ERR_INVALID_ARG),
+    (dict(in_layout=5), B.CBS_ERR_INVALID_ARG),
+    (dict(h=1, w=1, pad=0), B.CBS_ERR_INVALID_ARG),
+])
+def test_plan_rejects(cuda_lib, kw, status):
+    args = dict(n=1, c_in=16, h=40, w=40, c_out=32, k=3, stride=1, pad=1)
+    args.update(kw)
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_plan(make_desc(**args))
+    assert e.value.status == status
+
+
+def test_call_checks_before_any_launch(cuda_lib):
+    """Argument errors are reported without touching the GPU."""
+    p = B.cbs_plan(make_desc(1, 256, 20, 20, 256, 3, 1, force_split_k=4))
+    ok = 1 << 20
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_conv_bn_silu_f32(p, None, ok, ok, ok, ok, p.workspace_bytes, None)
+    assert e.value.status == B.CBS_ERR_INVALID_ARG
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_conv_bn_silu_f32(p, ok + 4, ok, ok, ok, ok, p.workspace_bytes, None)
+    assert e.value.status == B.CBS_ERR_MISALIGNED
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_conv_bn_silu_f32(p, ok, ok, ok, ok, None, 0, None)
+    assert e.value.status == B.CBS_ERR_WORKSPACE
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_conv_bn_silu_f32(p, ok, ok, ok, ok, ok, p.workspace_bytes - 1, None)
+    assert e.value.status == B.CBS_ERR_WORKSPACE
+    bad = B.cbs_plan_t.from_buffer_copy(p)
+    bad.size = 3
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_conv_bn_silu_f32(bad, ok, ok, ok, ok, ok, p.workspace_bytes, None)
+    assert e.value.status == B.CBS_ERR_PLAN_MISMATCH
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_conv_bn_silu_i8(p, ok, ok, ok, ok, 0.1, ok, ok, p.workspace_bytes, None)
+    assert e.value.status == B.CBS_ERR_INVALID_ARG
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_upsample2x_concat(ok, 4, ok, 4, ok, 1, 5, 4, B.CBS_NHWC, 2, None)
+    assert e.value.status == B.CBS_ERR_INVALID_ARG
+    assert "odd" in B.cbs_last_error() or "shape" in B.cbs_last_error()
