@@ -165,7 +165,8 @@ def run_ours(args, rank: int, world: int):
             for i in range(K):
                 step(i % R, evs[i] if evs is not None else None)
     torch.cuda.synchronize()
-    graph.replay()  # one untimed replay of the instantiated graph
+    with torch.cuda.stream(stream):
+        graph.replay()  # one untimed replay of the instantiated graph
     torch.cuda.synchronize()
 
     if world > 1:
@@ -174,10 +175,19 @@ def run_ours(args, rank: int, world: int):
     time.sleep(0.3)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    graph.replay()
-    t1.record(stream)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        graph.replay()
+        t1.record(stream)
     torch.cuda.synchronize()
+    # Per-launch durations: read the in-graph events of the timed replay now.
+    per_layer_us = None
+    if evs is not None:
+        per_layer_us = np.zeros(len(layers))
+        for i in range(args.steps):
+            for j in range(len(layers)):
+                per_layer_us[j] += evs[i][j].elapsed_time(evs[i][j + 1]) * 1e3
+        per_layer_us /= args.steps
     if world > 1:
         torch.distributed.barrier()
     total_ms = t0.elapsed_time(t1)
@@ -185,7 +195,8 @@ def run_ours(args, rank: int, world: int):
     # sees this load (the timed region itself may be shorter than a sample)
     tend = time.time() + 1.0
     while time.time() < tend:
-        graph.replay()
+        with torch.cuda.stream(stream):
+            graph.replay()
         torch.cuda.synchronize()
     clocks = sampler.stop()
 
@@ -195,14 +206,6 @@ def run_ours(args, rank: int, world: int):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms_step = float(t.item())
 
-    # Per-launch device durations from the in-graph events.
-    per_layer_us = None
-    if evs is not None:
-        per_layer_us = np.zeros(nl)
-        for i in range(K):
-            for j in range(nl):
-                per_layer_us[j] += evs[i][j].elapsed_time(evs[i][j + 1]) * 1e3
-        per_layer_us /= K
 
     flops_step = sum(s.flops(n) for s, _, _ in layers)
     value = flops_step * world / (ms_step * 1e-3) / 1e12

@@ -35,7 +35,7 @@ EXPORTED = (
 class cbs_layer_desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "n", "c_in", "h", "w", "c_out", "k", "stride", "pad", "in_layout", "out_layout", "prec",
-        "force_variant", "force_split_k", "force_block_n", "out_row_stride")]
+        "force_variant", "force_split_k", "force_block_n", "force_block_m", "out_row_stride")]
 
 
 class cbs_plan_t(ctypes.Structure):

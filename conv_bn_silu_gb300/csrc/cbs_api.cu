@@ -39,53 +39,77 @@ size_t elem_bytes(int prec) {
     }
 }
 
-// Pick the CUDA-core tile and split-K by a simple throughput model:
-// time ~ waves * (CTAs per SM) * tile work / (FMA lanes * efficiency),
-// divided by an occupancy factor when too few warps are resident.
+// Pick the CUDA-core tile and split-K with a throughput model of the kernel:
+// per-thread instructions (FMAs, shared-memory loads, gather and loop
+// overhead, epilogue) times warps, issued by 4 schedulers per SM at an
+// occupancy-dependent rate, over the number of CTA waves; plus the split-K
+// partial-tile traffic (written and read back through L2) and a floor set by
+// the layer's own input and output bytes at HBM bandwidth.
+struct SimtCost { int tile, split; double cycles; };
+
+SimtCost simt_cost(const cbs_layer_desc &d, int oh, int ow, int t, int split) {
+    const SimtTile T = kSimtTiles[t];
+    const long long M = (long long)d.n * oh * ow;
+    const int K = d.k * d.k * d.c_in;
+    const int nt = (T.bm / T.tm) * (T.bn / T.tn);
+    const int regs = T.tm * T.tn >= 64 ? 152 : (T.tm * T.tn >= 32 ? 80 : 64);
+    const int kc = round_up(ceil_div(K, split), kSimtBK);
+    const int splits = ceil_div(K, kc);
+    const int smem = simt_smem_bytes(t, kc, d.out_layout == CBS_NHWC) + 1024;
+    int res = 65536 / (nt * regs);
+    if (res > 2048 / nt) res = 2048 / nt;
+    if (res > 228 * 1024 / smem) res = 228 * 1024 / smem;
+    if (res < 1) res = 1;
+    const long long tiles = (long long)ceil_div(M, T.bm) * ceil_div(d.c_out, T.bn);
+    const long long ctas = tiles * splits;
+    const double a_pt = (double)T.bm * kSimtBK / nt, b_pt = (double)T.bn * kSimtBK / nt;
+    const double per_thread = (double)T.tm * T.tn * kc + (double)kc * (T.tm + T.tn) / 4.0 +
+                              (double)kc / kSimtBK * (a_pt * 7 + b_pt * 6 + 12) + T.tm * T.tn * 9.0 + 150.0 +
+                              (splits > 1 ? T.tm * T.tn * (0.5 * splits + 2) : 0.0);
+    const double cta_warp_instr = per_thread * nt / 32.0;
+    const long long slots = (long long)kNumSMs * res;
+    const long long waves = (ctas + slots - 1) / slots;
+    const long long per_sm = (ctas + kNumSMs - 1) / kNumSMs < res ? (ctas + kNumSMs - 1) / kNumSMs : res;
+    const double warps = (double)per_sm * nt / 32.0;
+    const double ipc = 4.0 * 0.7 * (warps >= 24 ? 1.0 : warps / 24.0);
+    double cycles = (double)waves * per_sm * cta_warp_instr / ipc;
+    if (splits > 1) cycles += (double)ctas * T.bm * T.bn * 8.0 / 2600.0;  // partials through L2
+    const double io_bytes = 4.0 * ((double)d.n * d.c_in * d.h * d.w + (double)M * d.c_out);
+    const double mem_cycles = io_bytes / 3100.0;  // ~6 TB/s at ~1.9 GHz
+    if (cycles < mem_cycles) cycles = mem_cycles;
+    cycles += 1500.0;  // launch and fill
+    return {t, splits, cycles};
+}
+
 void plan_simt(cbs_plan_t &p) {
     const cbs_layer_desc &d = p.desc;
     const long long M = (long long)d.n * p.oh * p.ow;
     const int K = d.k * d.k * d.c_in;
-    double best = 1e300;
-    int best_t = 1, best_split = 1;
+    SimtCost best{1, 1, 1e300};
     for (int t = 0; t < kNumSimtTiles; ++t) {
         if (d.force_block_n > 0 && kSimtTiles[t].bn != d.force_block_n) continue;
-        const SimtTile T = kSimtTiles[t];
-        const int nt = (T.bm / T.tm) * (T.bn / T.tn);
-        const int regs = T.tm * T.tn + 48;
-        int res = 65536 / (nt * (regs < 64 ? 64 : regs));
-        if (res > 2048 / nt) res = 2048 / nt;
-        if (res < 1) res = 1;
-        const double eff = (T.tm * T.tn >= 64) ? 0.85 : (T.tm * T.tn >= 32 ? 0.75 : 0.6);
-        const long long tiles = (long long)ceil_div(M, T.bm) * ceil_div(d.c_out, T.bn);
-        int max_split = K / (kSimtBK * 4) > 1 ? K / (kSimtBK * 4) : 1;
+        if (d.force_block_m > 0 && kSimtTiles[t].bm != d.force_block_m) continue;
+        int max_split = K / (kSimtBK * 2) > 1 ? K / (kSimtBK * 2) : 1;
         if (max_split > 32) max_split = 32;
-        if (d.force_split_k > 0) max_split = d.force_split_k;
-        for (int split = 1; split <= max_split; ++split) {
-            if (d.force_split_k > 0 && split != d.force_split_k) continue;
-            const long long kc = (long long)round_up(ceil_div(K, split), kSimtBK);
-            const long long ctas = tiles * split;
-            const long long slots = (long long)kNumSMs * res;
-            const long long waves = (ctas + slots - 1) / slots;
-            double warps = (double)(ctas < slots ? ctas : slots) / kNumSMs * nt / 32.0;
-            const double occ = warps >= 16 ? 1.0 : warps / 16.0;
-            double est = (double)waves * res * T.bm * T.bn * kc / (128.0 * eff) / occ;
-            est *= 1.0 + 0.04 * (split - 1);
-            if (est < best) { best = est; best_t = t; best_split = split; }
+        int lo = 1;
+        if (d.force_split_k > 0) lo = max_split = d.force_split_k;
+        for (int split = lo; split <= max_split; ++split) {
+            const SimtCost c = simt_cost(d, p.oh, p.ow, t, split);
+            if (c.cycles < best.cycles) best = c;
         }
     }
-    const SimtTile T = kSimtTiles[best_t];
+    const SimtTile T = kSimtTiles[best.tile];
     p.block_m = T.bm;
     p.block_n = T.bn;
     p.block_k = kSimtBK;
     p.stages = 2;
     p.threads = (T.bm / T.tm) * (T.bn / T.tn);
-    p.smem_bytes = 0;
     p.m_tiles = ceil_div(M, T.bm);
     p.n_tiles = ceil_div(d.c_out, T.bn);
     // K per split, a multiple of BK; recompute the split so none is empty.
-    const int kc = round_up(ceil_div(K, best_split), kSimtBK);
+    const int kc = round_up(ceil_div(K, d.force_split_k > 0 ? d.force_split_k : best.split), kSimtBK);
     p.split_k = ceil_div(K, kc);
+    p.smem_bytes = simt_smem_bytes(best.tile, kc, d.out_layout == CBS_NHWC);
     p.grid_ctas = p.m_tiles * p.n_tiles * p.split_k;
     p.variant = CBS_VARIANT_SIMT_FP32;
     p.workspace_bytes = 0;
@@ -281,9 +305,9 @@ cbs_status cbs_conv_bn_silu_f32(const cbs_plan_t *p, const void *x, const void *
     CBS_TRY(check_plan(p));
     if (p->variant == CBS_VARIANT_TC_INT8)
         return fail(CBS_ERR_INVALID_ARG, "INT8 plans run through cbs_conv_bn_silu_i8");
-    CBS_TRY(check_conv_common(p, x, w_packed, bias, y, workspace, workspace_bytes));
     const cbs_layer_desc &d = p->desc;
-    if (d.n == 0) return CBS_OK;
+    if (d.n == 0) return CBS_OK;  // empty batch: nothing is read or written
+    CBS_TRY(check_conv_common(p, x, w_packed, bias, y, workspace, workspace_bytes));
     if (p->variant == CBS_VARIANT_SIMT_FP32) {
         SimtLaunch L;
         std::memset(&L, 0, sizeof(L));
@@ -318,6 +342,7 @@ cbs_status cbs_conv_bn_silu_i8(const cbs_plan_t *p, const int8_t *x, const void 
     CBS_TRY(check_plan(p));
     if (p->variant != CBS_VARIANT_TC_INT8)
         return fail(CBS_ERR_INVALID_ARG, "plan is not an INT8 plan");
+    if (p->desc.n == 0) return CBS_OK;  // empty batch: nothing is read or written
     CBS_TRY(check_conv_common(p, x, w_packed, bias_i32, y, workspace, workspace_bytes));
     CBS_TRY(check_ptr(m_c, "m_c"));
     if (!(s_y > 0.0f) || !(s_y < 3.0e38f)) return fail(CBS_ERR_INVALID_ARG, "s_y must be a positive finite float");

@@ -24,7 +24,7 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 // ---------------------------------------------------------------- SIMT FP32
 // Tile configurations of the CUDA-core kernel (index = plan->block_k slot).
 struct SimtTile { int bm, bn, tm, tn; };
-constexpr int kSimtBK = 8;
+constexpr int kSimtBK = 16;
 constexpr SimtTile kSimtTiles[] = {
     {128, 128, 8, 8},  // 0: 256 threads
     {128, 64, 8, 8},   // 1: 128 threads
@@ -50,6 +50,8 @@ struct SimtLaunch {
     int m_tiles, n_tiles;
 };
 cudaError_t launch_simt(const SimtLaunch &L, cudaStream_t s);
+// Dynamic shared memory of one CUDA-core CTA (tiles + k table).
+int simt_smem_bytes(int tile, int k_chunk, int out_nhwc);
 
 // ---------------------------------------------------------------- misc kernels
 struct FoldLaunch {

@@ -5,30 +5,36 @@
 //   B[k, co] = w'[co, r, s, ci]               (packed [K][C_out] by cbs_fold_bn)
 //   y[m, co] = SiLU(sum_k A[m,k] B[k,co] + b'[co])
 // The A tile is gathered straight from x (NCHW or NHWC), zero outside the
-// image, into shared memory; nothing is materialised in global memory.
+// image, into shared memory; nothing is materialised in global memory.  A
+// per-CTA table maps each k of the CTA's K range to its input offset and
+// filter tap, so the gather costs one table read, a bounds test and a load.
 // Each thread accumulates a TM x TN register tile with FP32 fused
-// multiply-adds; the epilogue adds the folded bias and applies SiLU with
-// IEEE float operations, then stores each output element at its exact
-// address (row pitch out_row_stride for NCHW), so no store can reach the
-// padding columns of a row or the next row (page 1, "Bug fixed: TMA overflow
-// in Conv2dBnSiluTiled").
+// multiply-adds.  The epilogue adds the folded bias and applies SiLU, stages
+// the output tile in shared memory and stores it so that consecutive lanes
+// write consecutive addresses, each element at its exact address (row pitch
+// out_row_stride for NCHW): no store reaches the padding columns of a row or
+// the next row (page 1, "Bug fixed: TMA overflow in Conv2dBnSiluTiled").
 //
 // Split-K (small spatial layers at batch 1): CTAs with blockIdx.z = split
 // index write their partial tile to the workspace; the last CTA to arrive on
 // the tile's counter sums the partials in split order (deterministic), runs
 // the epilogue and puts the counter back to zero.  Nothing waits on another
 // CTA, so there is no spin loop.
-#include <cstdio>
-
 #include "cbs_internal.cuh"
 
 namespace cbs {
 namespace {
 
-__device__ __forceinline__ float silu_ieee(float z) {
-    // z * sigmoid(z) = z / (1 + e^-z); IEEE division and accurate expf.
-    return z / (1.0f + expf(-z));
-}
+// z * sigmoid(z) = z / (1 + e^-z).  Hardware exp2 and fast division: the
+// relative error stays near 1e-6 over the output range, far inside the FP32
+// path's 1e-5 relative-L2 bar, at a fraction of the instruction count.
+__device__ __forceinline__ float silu_f32(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+struct KEntry {
+    int off;      // input offset of (r, s, ci) relative to the window corner
+    short r, s;   // filter tap (r = kMaxTap marks k beyond the CTA's range)
+};
+constexpr short kNoTap = 0x3fff;
 
 template <int BM, int BN, int TM, int TN, int BK, bool NHWC_IN, bool NHWC_OUT>
 __global__ void __launch_bounds__((BM / TM) * (BN / TN))
@@ -43,9 +49,19 @@ simt_conv_kernel(const SimtLaunch a) {
     constexpr int B_PT = (BN * BK + NT - 1) / NT;
     constexpr int RG = TM / 4;           // row groups of 4
     constexpr int CG = TN / 4;           // column groups of 4
+    constexpr int MAIN_FLOATS = 2 * BK * (BM + BN);
+    constexpr int CP = BM + 4;           // NCHW output tile: [BN][BM + 4]
+    constexpr int CQ = BN + 4;           // NHWC output tile: [BM][BN + 4]
+    constexpr int OUT_FLOATS = NHWC_OUT ? BM * CQ : BN * CP;
+    constexpr int TILE_FLOATS = MAIN_FLOATS > OUT_FLOATS ? MAIN_FLOATS : OUT_FLOATS;
 
-    __shared__ __align__(16) float As[2][BK][BM];
-    __shared__ __align__(16) float Bs[2][BK][BN];
+    // Dynamic shared memory: [double-buffered A/B tiles | output tile] then
+    // the k table.
+    extern __shared__ float4 smem4[];
+    float *smem = reinterpret_cast<float *>(smem4);
+    float (*As)[BK][BM] = reinterpret_cast<float (*)[BK][BM]>(smem);
+    float (*Bs)[BK][BN] = reinterpret_cast<float (*)[BK][BN]>(smem + 2 * BK * BM);
+    KEntry *ktab = reinterpret_cast<KEntry *>(smem + TILE_FLOATS);
     __shared__ int s_is_last;
 
     const int t = threadIdx.x;
@@ -53,7 +69,28 @@ simt_conv_kernel(const SimtLaunch a) {
     const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
     const int kbeg = blockIdx.z * a.k_chunk;
     const int kend = min(a.K, kbeg + a.k_chunk);
+    const int klen = kend - kbeg;
+    const int klen_pad = (klen + BK - 1) / BK * BK;
     const int OHW = a.OH * a.OW;
+
+    // ---- k table for this CTA's K range
+    for (int kl = t; kl < klen_pad; kl += NT) {
+        KEntry e;
+        if (kl < klen) {
+            const int k = kbeg + kl;
+            const int tap = k / a.C;
+            const int ci = k - tap * a.C;
+            const int r = tap / a.KS, s = tap - (tap / a.KS) * a.KS;
+            e.off = NHWC_IN ? (r * a.W + s) * a.C + ci : (ci * a.H + r) * a.W + s;
+            e.r = (short)r;
+            e.s = (short)s;
+        } else {
+            e.off = 0;
+            e.r = kNoTap;
+            e.s = 0;
+        }
+        ktab[kl] = e;
+    }
 
     // ---- the A row (output pixel) this thread gathers
     const int am = t % BM;
@@ -68,54 +105,32 @@ simt_conv_kernel(const SimtLaunch a) {
         ow = rem - oh * a.OW;
     }
     const int ih0 = oh * a.stride - a.pad, iw0 = ow * a.stride - a.pad;
-    const float *__restrict__ xb = a.x + (size_t)img * a.C * a.H * a.W;
-
-    // Decode state (ci, r, s) of this thread's k indices, advanced by BK per step.
-    int dci[A_PT], dr[A_PT], ds[A_PT];
-#pragma unroll
-    for (int j = 0; j < A_PT; ++j) {
-        const int k = kbeg + ak0 + j * A_KSTEP;
-        const int tap = k / a.C;
-        dci[j] = k - tap * a.C;
-        dr[j] = tap / a.KS;
-        ds[j] = tap - dr[j] * a.KS;
-    }
+    // Rows (ih) and columns (iw) of the window that lie inside the image,
+    // as ranges of the tap index: r in [r_lo, r_hi), s in [s_lo, s_hi).
+    const int r_lo = mvalid ? max(0, -ih0) : kNoTap, r_hi = mvalid ? min(a.KS, a.H - ih0) : 0;
+    const int s_lo = max(0, -iw0), s_hi = min(a.KS, a.W - iw0);
+    const float *__restrict__ xw = a.x + (size_t)img * a.C * a.H * a.W +
+                                   (NHWC_IN ? ((long long)ih0 * a.W + iw0) * a.C : (long long)ih0 * a.W + iw0);
 
     float ra[A_PT], rb[B_PT];
-    auto load_a = [&](int kb) {
+    auto load_a = [&](int kl0) {
 #pragma unroll
         for (int j = 0; j < A_PT; ++j) {
-            const int k = kb + ak0 + j * A_KSTEP;
+            const KEntry e = ktab[kl0 + ak0 + j * A_KSTEP];
             float v = 0.0f;
-            const int ih = ih0 + dr[j], iw = iw0 + ds[j];
-            if (mvalid && k < kend && ih >= 0 && ih < a.H && iw >= 0 && iw < a.W) {
-                if (NHWC_IN)
-                    v = __ldg(xb + ((size_t)ih * a.W + iw) * a.C + dci[j]);
-                else
-                    v = __ldg(xb + ((size_t)dci[j] * a.H + ih) * a.W + iw);
-            }
+            if (e.r >= r_lo && e.r < r_hi && e.s >= s_lo && e.s < s_hi) v = __ldg(xw + e.off);
             ra[j] = v;
         }
     };
-    auto advance_a = [&]() {
-#pragma unroll
-        for (int j = 0; j < A_PT; ++j) {
-            dci[j] += BK;
-            while (dci[j] >= a.C) {
-                dci[j] -= a.C;
-                if (++ds[j] == a.KS) { ds[j] = 0; ++dr[j]; }
-            }
-        }
-    };
-    auto load_b = [&](int kb) {
+    auto load_b = [&](int kl0) {
 #pragma unroll
         for (int j = 0; j < B_PT; ++j) {
             const int idx = t + j * NT;
             float v = 0.0f;
             if (idx < BN * BK) {
-                const int kl = idx / BN, nl = idx - (idx / BN) * BN;
-                const int k = kb + kl, n = n0 + nl;
-                if (k < kend && n < a.Cout) v = __ldg(a.w + (size_t)k * a.Cout + n);
+                const int kl = kl0 + idx / BN, nl = idx % BN;
+                const int n = n0 + nl;
+                if (kl < klen && n < a.Cout) v = __ldg(a.w + (size_t)(kbeg + kl) * a.Cout + n);
             }
             rb[j] = v;
         }
@@ -136,19 +151,19 @@ simt_conv_kernel(const SimtLaunch a) {
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
 
-    if (kbeg < kend) {
-        load_a(kbeg);
-        load_b(kbeg);
+    __syncthreads();  // k table ready
+    if (klen > 0) {
+        load_a(0);
+        load_b(0);
         store_smem(0);
     }
     __syncthreads();
     int buf = 0;
-    for (int kb = kbeg; kb < kend; kb += BK) {
-        const bool more = kb + BK < kend;
+    for (int kl = 0; kl < klen; kl += BK) {
+        const bool more = kl + BK < klen;
         if (more) {
-            advance_a();
-            load_a(kb + BK);
-            load_b(kb + BK);
+            load_a(kl + BK);
+            load_b(kl + BK);
         }
 #pragma unroll
         for (int kk = 0; kk < BK; ++kk) {
@@ -215,52 +230,93 @@ simt_conv_kernel(const SimtLaunch a) {
             }
     }
 
-    // ---- epilogue: + folded bias, SiLU, exact-address stores
+    // ---- epilogue: + folded bias, SiLU into the shared output tile, then
+    // coalesced exact-address stores.
     float bvals[TN];
 #pragma unroll
     for (int j = 0; j < TN; ++j) {
         const int n = n0 + col_of(j);
         bvals[j] = n < a.Cout ? __ldg(a.bias + n) : 0.0f;
     }
+    __syncthreads();  // main-loop tiles are no longer read
+    float *Cs = smem;
 #pragma unroll
-    for (int i = 0; i < TM; ++i) {
-        const int m = m0 + row_of(i);
-        if (m >= a.M) continue;
-        const int im = m / OHW;
-        const int rem = m - im * OHW;
-        const int ohh = rem / a.OW;
-        const int oww = rem - ohh * a.OW;
+    for (int j = 0; j < TN; ++j) {
 #pragma unroll
-        for (int j = 0; j < TN; ++j) {
-            const int n = n0 + col_of(j);
-            if (n >= a.Cout) continue;
-            const float v = silu_ieee(acc[i][j] + bvals[j]);
-            size_t off;
-            if (NHWC_OUT)
-                off = (size_t)m * a.Cout + n;
-            else
-                off = (((size_t)im * a.Cout + n) * a.OH + ohh) * (size_t)a.out_row_stride + oww;
-            a.y[off] = v;
+        for (int g = 0; g < RG; ++g) {
+            float v[4];
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) v[ii] = silu_f32(acc[g * 4 + ii][j] + bvals[j]);
+            const int r0 = row_of(g * 4), c = col_of(j);
+            if (NHWC_OUT) {
+#pragma unroll
+                for (int ii = 0; ii < 4; ++ii) Cs[(r0 + ii) * CQ + c] = v[ii];
+            } else {
+                *reinterpret_cast<float4 *>(&Cs[c * CP + r0]) = make_float4(v[0], v[1], v[2], v[3]);
+            }
+        }
+    }
+    __syncthreads();
+    if (!NHWC_OUT) {
+        const int ml = t % BM;
+        const int m = m0 + ml;
+        if (m < a.M) {
+            const int im = m / OHW;
+            const int rem = m - im * OHW;
+            const int ohh = rem / a.OW;
+            const int oww = rem - ohh * a.OW;
+            float *yb = a.y + ((size_t)im * a.Cout * a.OH + ohh) * (size_t)a.out_row_stride + oww;
+            const size_t plane = (size_t)a.OH * a.out_row_stride;
+            for (int nl = t / BM; nl < BN; nl += NT / BM) {
+                const int n = n0 + nl;
+                if (n < a.Cout) yb[(size_t)n * plane] = Cs[nl * CP + ml];
+            }
+        }
+    } else {
+        for (int idx = t; idx < BM * BN; idx += NT) {
+            const int ml = idx / BN, nl = idx % BN;
+            const int m = m0 + ml, n = n0 + nl;
+            if (m < a.M && n < a.Cout) a.y[(size_t)m * a.Cout + n] = Cs[ml * CQ + nl];
         }
     }
 }
 
-template <int BM, int BN, int TM, int TN>
-cudaError_t launch_cfg(const SimtLaunch &L, cudaStream_t s) {
+template <int BM, int BN, int TM, int TN, bool IN_NHWC, bool OUT_NHWC>
+cudaError_t launch_one(dim3 grid, const SimtLaunch &L, cudaStream_t s) {
     constexpr int NT = (BM / TM) * (BN / TN);
-    dim3 grid(L.m_tiles, L.n_tiles, L.split);
-    if (L.in_nhwc && L.out_nhwc)
-        simt_conv_kernel<BM, BN, TM, TN, kSimtBK, true, true><<<grid, NT, 0, s>>>(L);
-    else if (!L.in_nhwc && !L.out_nhwc)
-        simt_conv_kernel<BM, BN, TM, TN, kSimtBK, false, false><<<grid, NT, 0, s>>>(L);
-    else if (L.in_nhwc)
-        simt_conv_kernel<BM, BN, TM, TN, kSimtBK, true, false><<<grid, NT, 0, s>>>(L);
-    else
-        simt_conv_kernel<BM, BN, TM, TN, kSimtBK, false, true><<<grid, NT, 0, s>>>(L);
+    constexpr int main_floats = 2 * kSimtBK * (BM + BN);
+    constexpr int out_floats = OUT_NHWC ? BM * (BN + 4) : BN * (BM + 4);
+    constexpr int tile_bytes = 4 * (main_floats > out_floats ? main_floats : out_floats);
+    const int kpad = (L.k_chunk + kSimtBK - 1) / kSimtBK * kSimtBK;
+    const int bytes = tile_bytes + kpad * (int)sizeof(KEntry);
+    auto kern = simt_conv_kernel<BM, BN, TM, TN, kSimtBK, IN_NHWC, OUT_NHWC>;
+    if (bytes > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<grid, NT, bytes, s>>>(L);
     return cudaGetLastError();
 }
 
+template <int BM, int BN, int TM, int TN>
+cudaError_t launch_cfg(const SimtLaunch &L, cudaStream_t s) {
+    dim3 grid(L.m_tiles, L.n_tiles, L.split);
+    if (L.in_nhwc && L.out_nhwc) return launch_one<BM, BN, TM, TN, true, true>(grid, L, s);
+    if (!L.in_nhwc && !L.out_nhwc) return launch_one<BM, BN, TM, TN, false, false>(grid, L, s);
+    if (L.in_nhwc) return launch_one<BM, BN, TM, TN, true, false>(grid, L, s);
+    return launch_one<BM, BN, TM, TN, false, true>(grid, L, s);
+}
+
 }  // namespace
+
+int simt_smem_bytes(int tile, int k_chunk, int out_nhwc) {
+    if (tile < 0 || tile >= kNumSimtTiles) return 0;
+    const SimtTile T = kSimtTiles[tile];
+    const int main_floats = 2 * kSimtBK * (T.bm + T.bn);
+    const int out_floats = out_nhwc ? T.bm * (T.bn + 4) : T.bn * (T.bm + 4);
+    const int kpad = (k_chunk + kSimtBK - 1) / kSimtBK * kSimtBK;
+    return 4 * (main_floats > out_floats ? main_floats : out_floats) + kpad * (int)sizeof(KEntry);
+}
 
 cudaError_t launch_simt(const SimtLaunch &L, cudaStream_t s) {
     switch (L.tile) {

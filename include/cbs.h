@@ -83,6 +83,7 @@ typedef struct cbs_layer_desc {
     int force_variant;   /* -1: choose from prec; else a cbs_variant compatible with prec */
     int force_split_k;   /* 0: choose; else the number of K splits to use (>= 1) */
     int force_block_n;   /* 0: choose; else the N tile width (must be one the variant supports) */
+    int force_block_m;   /* 0: choose; else the M tile height (CUDA-core variant: 64, 128 or 256) */
     int out_row_stride;  /* NCHW output only: elements between output rows; 0 = OW.
                             Must be >= OW.  Columns OW..stride-1 are never written. */
 } cbs_layer_desc;

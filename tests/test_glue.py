@@ -19,8 +19,8 @@ def _np_upcat_nhwc(a, b):
 @pytest.mark.parametrize("ca,cb", [(256, 128), (3, 5), (8, 8)])
 def test_upsample_concat_nhwc(cuda_lib, dtype, ca, cb):
     g = torch.Generator().manual_seed(ca * 7 + cb)
-    a = (torch.randn((2, 5, 6, ca), generator=g) * 50).to(dtype)
-    b = (torch.randn((2, 10, 12, cb), generator=g) * 50).to(dtype)
+    a = (torch.randn((2, 5, 6, ca), generator=g, dtype=torch.float32) * 50).to(dtype)
+    b = (torch.randn((2, 10, 12, cb), generator=g, dtype=torch.float32) * 50).to(dtype)
     out = upsample2x_concat(a.cuda(), b.cuda(), B.CBS_NHWC)
     torch.cuda.synchronize()
     ref = _np_upcat_nhwc(a.view(torch.int8 if dtype == torch.int8 else torch.int16 if dtype == torch.bfloat16 else torch.int32).numpy(),
@@ -31,8 +31,8 @@ def test_upsample_concat_nhwc(cuda_lib, dtype, ca, cb):
 
 def test_upsample_concat_nchw(cuda_lib):
     g = torch.Generator().manual_seed(3)
-    a = torch.randn((2, 7, 4, 5), generator=g)
-    b = torch.randn((2, 3, 8, 10), generator=g)
+    a = torch.randn((2, 7, 4, 5), generator=g, dtype=torch.float32)
+    b = torch.randn((2, 3, 8, 10), generator=g, dtype=torch.float32)
     out = upsample2x_concat(a.cuda(), b.cuda(), B.CBS_NCHW).cpu()
     ref = torch.cat([a.repeat_interleave(2, 2).repeat_interleave(2, 3), b], 1)
     assert torch.equal(out, ref)

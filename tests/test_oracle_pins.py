@@ -16,8 +16,6 @@ import torch
 import oracle
 from conv_bn_silu_gb300 import workloads as wl
 
-torch.set_default_dtype(torch.float64)
-
 
 def rng(seed=0):
     return np.random.default_rng(seed)
@@ -143,7 +141,8 @@ def test_bn_matches_torch():
     g, b, m = f32(r.uniform(0.5, 1.5, 6)), f32(r.normal(0, 0.3, 6)), f32(r.normal(0, 0.3, 6))
     v = f32(r.uniform(0.5, 2.0, 6))
     out = oracle.batchnorm(t, g, b, m, v, 1e-3)
-    ref = torch.nn.functional.batch_norm(torch.from_numpy(t), *(torch.from_numpy(a.astype(np.float64)) for a in (m, v, g, b)),
+    ref = torch.nn.functional.batch_norm(torch.from_numpy(t.astype(np.float64)),
+                                         *(torch.from_numpy(a.astype(np.float64)) for a in (m, v, g, b)),
                                          training=False, eps=float(np.float32(1e-3))).numpy()
     np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-13)
 

@@ -103,8 +103,8 @@ def test_empty_batch_is_a_noop(cuda_lib):
     _, p = wl.layer_inputs(spec, 1)
     desc = make_desc(0, 8, 6, 6, 8, 3, 1)
     layer = FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps)
-    x = torch.empty((0, 8, 6, 6), device="cuda")
-    y = layer(x, torch.empty((0, 8, 6, 6), device="cuda"))
+    x = torch.empty((0, 8, 6, 6), dtype=torch.float32, device="cuda")
+    y = layer(x, torch.empty((0, 8, 6, 6), dtype=torch.float32, device="cuda"))
     torch.cuda.synchronize()
     assert y.numel() == 0
 
@@ -120,7 +120,7 @@ def test_padded_rows_and_guard_bands_untouched(cuda_lib, ow_case):
     layer = FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps)
     guard = 4096
     n_el = 2 * 32 * size * pitch
-    buf = torch.full((n_el + guard,), float("nan"), device="cuda")
+    buf = torch.full((n_el + guard,), float("nan"), dtype=torch.float32, device="cuda")
     sentinel_bits = buf[:1].view(torch.int32).item()
     y = buf[:n_el].view(2, 32, size, pitch)
     layer(torch.from_numpy(x).cuda(), y)

@@ -1,0 +1,129 @@
+"""GPU parity of the tcgen05 tensor-core paths (TF32, BF16) against the CPU
+FP32 oracle.
+
+Bar: relative L2 <= 5e-3 over the whole output, and max abs error <= 2e-2
+at unit output scale (max |err| / max(1, |ref|) <= 2e-2).  The
+oracle sees the same float32 input the library receives before the input
+packing step rounds it (TF32 operands are truncated by the tensor cores,
+BF16 inputs and weights are rounded to bfloat16, accumulation is FP32)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conv_bn_silu_gb300 import _binding as B
+from conv_bn_silu_gb300 import workloads as wl
+from conv_bn_silu_gb300.layer import FusedConvBnSilu, make_desc
+from helpers import TOL_TC_MAX_ABS, TOL_TC_REL_L2, max_scaled_err, nhwc_to_nchw, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+PRECS = {"tf32": B.CBS_TF32, "bf16": B.CBS_BF16}
+
+
+def run_tc(spec, x, p, prec, out_layout=B.CBS_NHWC, **kw):
+    n = x.shape[0]
+    desc = make_desc(n, spec.c_in, spec.h, spec.width, spec.c_out, spec.k, spec.stride, spec.pad,
+                     prec=prec, in_layout=B.CBS_NHWC, out_layout=out_layout, **kw)
+    layer = FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps)
+    xp = layer.pack_input(torch.from_numpy(x).cuda())
+    y = layer(xp)
+    torch.cuda.synchronize()
+    y = y.float().cpu().numpy()
+    if out_layout == B.CBS_NHWC:
+        y = nhwc_to_nchw(y)
+    return y, layer
+
+
+def ref_of(spec, x, p):
+    return oracle.conv_bn_silu_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, spec.stride, spec.pad)
+
+
+def check(y, ref, what=""):
+    e, m = rel_l2(y, ref), max_scaled_err(y, ref)
+    assert e <= TOL_TC_REL_L2 and m <= TOL_TC_MAX_ABS, (what, e, m)
+
+
+@pytest.mark.parametrize("prec", ["bf16", "tf32"])
+def test_tiny_first(cuda_lib, prec):
+    """Smallest case: one 128-pixel tile, one K step per tap."""
+    spec = wl.LayerSpec(16, 16, 3, 1, 8)
+    x, p = wl.layer_inputs(spec, 2, layer_index=2)
+    y, _ = run_tc(spec, x, p, PRECS[prec])
+    check(y, ref_of(spec, x, p))
+
+
+@pytest.mark.parametrize("prec", ["bf16", "tf32"])
+def test_single_layer_40x40(cuda_lib, prec):
+    spec = wl.SINGLE_LAYER
+    x, p = wl.layer_inputs(spec, 1)
+    for out_layout in (B.CBS_NHWC, B.CBS_NCHW):
+        y, _ = run_tc(spec, x, p, PRECS[prec], out_layout=out_layout)
+        check(y, ref_of(spec, x, p), out_layout)
+
+
+@pytest.mark.parametrize("prec", ["bf16", "tf32"])
+@pytest.mark.parametrize("i", range(len(wl.LAYER_LIST)))
+def test_layer_list_batch1(cuda_lib, prec, i):
+    spec = wl.LAYER_LIST[i]
+    x, p = wl.layer_inputs(spec, 1, layer_index=i)
+    y, layer = run_tc(spec, x, p, PRECS[prec])
+    check(y, ref_of(spec, x, p), (i, layer.plan.block_n, layer.plan.block_k, layer.plan.stages))
+
+
+@pytest.mark.parametrize("prec", ["bf16", "tf32"])
+@pytest.mark.parametrize("shape", [
+    (3, 16, 48, 3, 2, 13),     # ragged pixels, stride 2, BN = 48
+    (2, 32, 16, 1, 1, 11),     # 1x1, tail tile
+    (1, 64, 272, 3, 1, 6),     # C_out > 256: two N tiles, second ragged
+    (4, 48, 32, 3, 1, 9),      # C_in = 48 (96 B in BF16: 32-byte K steps)
+    (1, 3, 16, 3, 2, 34),      # C_in = 3 padded, stride 2, even size
+    (2, 8, 16, 3, 1, 1),       # 1x1 image with a 3x3 filter
+])
+def test_ragged(cuda_lib, prec, shape):
+    n, c_in, c_out, k, stride, h = shape
+    spec = wl.LayerSpec(c_in, c_out, k, stride, h)
+    x, p = wl.layer_inputs(spec, n, layer_index=9)
+    y, _ = run_tc(spec, x, p, PRECS[prec])
+    check(y, ref_of(spec, x, p), shape)
+
+
+@pytest.mark.parametrize("prec", ["bf16", "tf32"])
+def test_non_square_image(cuda_lib, prec):
+    """H != W pins the order of the im2col corner and offset coordinates."""
+    spec = wl.LayerSpec(32, 32, 3, 1, 12, 20)
+    x, p = wl.layer_inputs(spec, 2, layer_index=3)
+    y, _ = run_tc(spec, x, p, PRECS[prec])
+    check(y, ref_of(spec, x, p))
+    spec2 = wl.LayerSpec(32, 64, 3, 2, 18, 10)
+    x2, p2 = wl.layer_inputs(spec2, 1, layer_index=4)
+    y2, _ = run_tc(spec2, x2, p2, PRECS[prec])
+    check(y2, ref_of(spec2, x2, p2))
+
+
+@pytest.mark.parametrize("prec", ["bf16", "tf32"])
+@pytest.mark.parametrize("bn", [16, 32, 64, 128, 256])
+def test_forced_block_n(cuda_lib, prec, bn):
+    spec = wl.LayerSpec(64, 256, 3, 1, 10)
+    x, p = wl.layer_inputs(spec, 2, layer_index=8)
+    y, layer = run_tc(spec, x, p, PRECS[prec], force_block_n=bn)
+    assert layer.plan.block_n == bn
+    check(y, ref_of(spec, x, p), bn)
+
+
+@pytest.mark.parametrize("prec", ["bf16", "tf32"])
+@pytest.mark.parametrize("i", [1, 5, 7, 10, 11])
+def test_batch16_sampled_images(cuda_lib, prec, i):
+    """Full batch-16 launch; images 0 and 15 checked against the oracle
+    (images are independent, so the oracle computes only those two)."""
+    spec = wl.LAYER_LIST[i]
+    x, p = wl.layer_inputs(spec, 16, layer_index=i)
+    y, _ = run_tc(spec, x, p, PRECS[prec])
+    sel = x[[0, 15]]
+    ref = ref_of(spec, sel, p)
+    check(y[[0, 15]], ref)
+    assert np.isfinite(y).all()
+
+
+def test_no_timeout_reported(cuda_lib):
+    assert B.cbs_read_device_status(True, torch.cuda.current_stream().cuda_stream) == B.CBS_OK
