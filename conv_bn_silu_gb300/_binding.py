@@ -28,7 +28,7 @@ CBS_VARIANT_SIMT_FP32, CBS_VARIANT_TC_TF32, CBS_VARIANT_TC_BF16, CBS_VARIANT_TC_
 EXPORTED = (
     "cbs_plan", "cbs_fold_bn", "cbs_pack_input", "cbs_conv_bn_silu_f32", "cbs_conv_bn_silu_i8",
     "cbs_upsample2x_concat", "cbs_workspace_init", "cbs_read_device_status", "cbs_status_string",
-    "cbs_last_error", "cbs_abi_version",
+    "cbs_last_error", "cbs_abi_version", "cbs_conv_bn_silu_f32_noalloc",
 )
 
 
@@ -71,6 +71,7 @@ def lib():
         L.cbs_conv_bn_silu_f32.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P, Z, P]
         L.cbs_conv_bn_silu_i8.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, F, P, P, Z, P]
         L.cbs_upsample2x_concat.argtypes = [P, I, P, I, P, I, I, I, I, I, P]
+        L.cbs_conv_bn_silu_f32_noalloc.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P]
         L.cbs_workspace_init.argtypes = [P, Z, P]
         L.cbs_read_device_status.argtypes = [ctypes.POINTER(I), I, P]
         L.cbs_status_string.argtypes = [I]
@@ -145,6 +146,13 @@ def cbs_conv_bn_silu_i8(plan, x, w_packed, bias_i32, m_c, s_y, y, workspace, wor
     _check(lib().cbs_conv_bn_silu_i8(ctypes.byref(plan), _p(x), _p(w_packed), _p(bias_i32),
                                      _p(m_c), s_y, _p(y), _p(workspace), workspace_bytes, stream),
            "cbs_conv_bn_silu_i8")
+
+
+def cbs_conv_bn_silu_f32_noalloc(plan, x, w_packed, bias, y, stream):
+    """FP32 CUDA-core layer with the library's built-in split-K scratch (for
+    callers that cannot allocate device memory)."""
+    _check(lib().cbs_conv_bn_silu_f32_noalloc(ctypes.byref(plan), _p(x), _p(w_packed), _p(bias), _p(y),
+                                              stream), "cbs_conv_bn_silu_f32_noalloc")
 
 
 def cbs_upsample2x_concat(a, ca, b, cb, out, n, h, w, layout, elem_bytes, stream):

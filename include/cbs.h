@@ -201,6 +201,28 @@ CBS_API cbs_status cbs_upsample2x_concat(const void *a, int ca, const void *b, i
                                  int n, int h, int w, int layout, int elem_bytes,
                                  void *stream);
 
+/*
+ * cbs_conv_bn_silu_f32_noalloc -- the FP32 CUDA-core fused layer for callers
+ * that cannot allocate device memory.  No passage of the pages has a
+ * counterpart: this is a deployment interface, not part of the method.
+ * Some callers hold only the layer's own buffers: a plugin interface that
+ * passes input and output pointers and no workspace, or a latency-bound
+ * serving loop that must not allocate after start-up (cudaMalloc can
+ * synchronise the device).  This call needs no workspace argument: split-K
+ * scratch comes from a 16 MiB array the library defines in device memory
+ * (present on every GPU that loads the library, until the process exits).
+ *   p: a CBS_VARIANT_SIMT_FP32 plan with workspace_bytes <= 16 MiB (larger
+ *      plans fail with CBS_ERR_WORKSPACE; other variants CBS_ERR_UNSUPPORTED);
+ *   x, w_packed, bias, y: as for cbs_conv_bn_silu_f32 (device, 16-byte aligned).
+ * The first call on a device looks up the array's address with that device
+ * current; make it before any stream capture.  Every call shares the array
+ * and zeroes its split-K counters on `stream` before its kernel; calls whose
+ * kernels may overlap on the GPU race on the array and give wrong results.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+CBS_API cbs_status cbs_conv_bn_silu_f32_noalloc(const cbs_plan_t *p, const float *x, const float *w_packed,
+                                                const float *bias, float *y, void *stream);
+
 /* Zero a workspace before its first use (cudaMemsetAsync on `stream`). */
 CBS_API cbs_status cbs_workspace_init(void *workspace, size_t bytes, void *stream);
 
