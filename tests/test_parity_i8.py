@@ -1,0 +1,137 @@
+"""GPU parity of the INT8 path against the CPU oracle: bit-exact.
+
+Each stage is compared byte for byte with the oracle on the same seeded
+inputs: the activation quantiser (cbs_pack_input), the quantising fold
+(int8 codes, int32 bias, m_c), and the fused INT8 layer (integer sums,
+int32 bias, SiLU in float with the specified exp, round half to even)."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conv_bn_silu_gb300 import _binding as B
+from conv_bn_silu_gb300 import workloads as wl
+from conv_bn_silu_gb300.layer import FusedConvBnSilu, make_desc
+from helpers import nhwc_to_nchw
+
+pytestmark = pytest.mark.gpu
+
+SCALES = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "int8_scales.json")))
+S_X = float(wl.S_X_INT8)
+
+
+def build(spec, n, p, out_layout=B.CBS_NHWC, **kw):
+    desc = make_desc(n, spec.c_in, spec.h, spec.width, spec.c_out, spec.k, spec.stride, spec.pad,
+                     prec=B.CBS_INT8, in_layout=B.CBS_NHWC, out_layout=out_layout, **kw)
+    return FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, s_x=S_X)
+
+
+def gpu_packed_codes(layer, spec):
+    """The fold's packed weights back in OIHW int8 (bf16 codes -> int)."""
+    c_pad = layer.plan.c_in_pad
+    wb = layer.w_packed.view(torch.bfloat16).float().cpu().numpy()
+    wb = wb.reshape(spec.c_out, spec.k, spec.k, c_pad)
+    assert np.all(wb[..., spec.c_in:] == 0)
+    assert np.all(wb == np.round(wb))
+    return wb[..., :spec.c_in].transpose(0, 3, 1, 2).astype(np.int8)
+
+
+def run_layer(spec, x, p, s_y, out_layout=B.CBS_NHWC, **kw):
+    n = x.shape[0]
+    layer = build(spec, n, p, out_layout=out_layout, **kw)
+    qx = layer.pack_input(torch.from_numpy(x).cuda())
+    y = layer(qx, s_y=s_y)
+    torch.cuda.synchronize()
+    y = y.cpu().numpy()
+    if out_layout == B.CBS_NHWC:
+        y = nhwc_to_nchw(y)
+    return layer, qx.cpu().numpy(), y
+
+
+def oracle_layer(spec, x, p, s_y):
+    q_x = oracle.quantize_act(x, S_X)
+    q_w, bias, m_c = oracle.fold_quant_i8(p.w, p.gamma, p.beta, p.mean, p.var, p.eps, S_X)
+    q_y = oracle.conv_i8(q_x, q_w, bias, m_c, s_y, spec.stride, spec.pad)
+    return q_x, q_w, bias, m_c, q_y
+
+
+def assert_bit_exact(spec, x, p, s_y, what="", **kw):
+    layer, qx_gpu, y_gpu = run_layer(spec, x, p, s_y, **kw)
+    q_x, q_w, bias, m_c, q_y = oracle_layer(spec, x, p, s_y)
+    c_pad = layer.plan.c_in_pad
+    qx_gpu = qx_gpu.reshape(x.shape[0], spec.h, spec.width, c_pad)
+    assert np.all(qx_gpu[..., spec.c_in:] == 0)
+    assert np.array_equal(nhwc_to_nchw(qx_gpu[..., :spec.c_in]), q_x), ("quantised input", what)
+    assert np.array_equal(gpu_packed_codes(layer, spec), q_w), ("weight codes", what)
+    assert np.array_equal(layer.bias.view(torch.int32).cpu().numpy(), bias), ("int32 bias", what)
+    assert np.array_equal(layer.m_c.cpu().numpy().view(np.int32), m_c.view(np.int32)), ("m_c", what)
+    mism = int(np.count_nonzero(y_gpu != q_y))
+    assert mism == 0, (what, mism, y_gpu.size)
+    return y_gpu
+
+
+def test_single_layer(cuda_lib):
+    spec = wl.SINGLE_LAYER
+    x, p = wl.layer_inputs(spec, 1)
+    y = assert_bit_exact(spec, x, p, SCALES["single_layer"])
+    assert len(np.unique(y)) > 50  # the scale puts outputs across the code range
+
+
+@pytest.mark.parametrize("i", range(len(wl.LAYER_LIST)))
+def test_layer_list_batch1(cuda_lib, i):
+    spec = wl.LAYER_LIST[i]
+    x, p = wl.layer_inputs(spec, 1, layer_index=i)
+    assert_bit_exact(spec, x, p, SCALES["layer_list"][i], i)
+
+
+@pytest.mark.parametrize("i", [1, 5, 7, 10, 11])
+def test_batch16_sampled_images(cuda_lib, i):
+    """Full batch-16 launch; images 0 and 15 checked against the oracle."""
+    spec = wl.LAYER_LIST[i]
+    x, p = wl.layer_inputs(spec, 16, layer_index=i)
+    s_y = SCALES["layer_list"][i]
+    layer, _, y = run_layer(spec, x, p, s_y)
+    sel = np.ascontiguousarray(x[[0, 15]])
+    q = oracle_layer(spec, sel, p, s_y)[-1]
+    assert np.array_equal(y[[0, 15]], q)
+
+
+@pytest.mark.parametrize("shape", [
+    (3, 16, 48, 3, 2, 13),     # ragged pixels, stride 2
+    (2, 32, 16, 1, 1, 11),     # 1x1, tail tile
+    (1, 64, 272, 3, 1, 6),     # two N tiles, second ragged
+    (2, 48, 32, 3, 1, 9),      # C_in = 48: 16-channel K steps
+    (1, 3, 16, 3, 2, 34),      # C_in = 3 padded to 16
+    (1, 256, 64, 3, 1, 5),     # K = 2304: three exact-sum chunks
+    (1, 384, 32, 1, 1, 7),     # 1x1 with 384 channels
+])
+def test_ragged(cuda_lib, shape):
+    n, c_in, c_out, k, stride, h = shape
+    spec = wl.LayerSpec(c_in, c_out, k, stride, h)
+    x, p = wl.layer_inputs(spec, n, layer_index=11)
+    assert_bit_exact(spec, x, p, 0.05, shape)
+
+
+def test_nchw_output(cuda_lib):
+    spec = wl.LayerSpec(32, 48, 3, 1, 10)
+    x, p = wl.layer_inputs(spec, 2, layer_index=2)
+    assert_bit_exact(spec, x, p, 0.06, out_layout=B.CBS_NCHW)
+
+
+@pytest.mark.parametrize("s_y", [1e-4, 10.0])
+def test_saturation_and_underflow(cuda_lib, s_y):
+    """Tiny s_y saturates most outputs at -128/127; a huge one rounds them to 0."""
+    spec = wl.LayerSpec(16, 32, 3, 1, 12)
+    x, p = wl.layer_inputs(spec, 1, layer_index=4)
+    y = assert_bit_exact(spec, x, p, s_y)
+    if s_y < 1:
+        assert (y == 127).mean() > 0.3
+    else:
+        assert (y == 0).mean() > 0.9
+
+
+def test_no_timeout_reported(cuda_lib):
+    assert B.cbs_read_device_status(True, torch.cuda.current_stream().cuda_stream) == B.CBS_OK
