@@ -91,191 +91,309 @@ class ClockSampler:
 
 # --------------------------------------------------------------- workloads
 WORKLOADS = {
-    "layer_list_fp32_n1": dict(layers=wl.LAYER_LIST, n=1, prec="fp32"),
-    "single_layer_fp32_n1": dict(layers=(wl.SINGLE_LAYER,), n=1, prec="fp32"),
+    "layer_list_fp32_n1": dict(kind="list", layers=wl.LAYER_LIST, n=1, prec="fp32"),
+    "single_layer_fp32_n1": dict(kind="list", layers=(wl.SINGLE_LAYER,), n=1, prec="fp32"),
+    "layer_list_bf16_n16": dict(kind="list", layers=wl.LAYER_LIST, n=16, prec="bf16"),
+    "layer_list_tf32_n16": dict(kind="list", layers=wl.LAYER_LIST, n=16, prec="tf32"),
+    "layer_list_int8_n16": dict(kind="list", layers=wl.LAYER_LIST, n=16, prec="int8"),
+    "chain_fp32_n1": dict(kind="chain", n=1, prec="fp32"),
+    "chain_bf16_n16": dict(kind="chain", n=16, prec="bf16"),
+    "chain_tf32_n16": dict(kind="chain", n=16, prec="tf32"),
 }
+EXTRA_DEFAULT = ("layer_list_bf16_n16", "layer_list_tf32_n16", "layer_list_int8_n16", "chain_fp32_n1",
+                 "chain_bf16_n16")
 
 
 def act_bytes(prec: str) -> int:
     return {"fp32": 4, "tf32": 4, "bf16": 2, "int8": 1}[prec]
 
 
-def build_layers(name: str, device):
-    import torch
-    from conv_bn_silu_gb300 import _binding as B
-    from conv_bn_silu_gb300.layer import FusedConvBnSilu, make_desc
-    cfg = WORKLOADS[name]
-    prec = {"fp32": B.CBS_FP32, "tf32": B.CBS_TF32, "bf16": B.CBS_BF16, "int8": B.CBS_INT8}[cfg["prec"]]
-    layers = []
-    for i, spec in enumerate(cfg["layers"]):
-        x, p = wl.layer_inputs(spec, cfg["n"], seed=0, layer_index=i)
-        desc = make_desc(cfg["n"], spec.c_in, spec.h, spec.width, spec.c_out, spec.k, spec.stride, spec.pad,
-                         prec=prec)
-        layer = FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, device=device)
-        layers.append((spec, layer, x))
-    return cfg, layers
+def peak_for(prec: str, peaks):
+    """(bound-kind peak in TFLOP/s, label) of the arithmetic a variant runs on."""
+    bf16 = float(peaks["bf16_tflops"])
+    if prec == "fp32":
+        return FP32_ALU_PEAK_TFLOPS, "alu: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz"
+    if prec == "tf32":
+        return bf16 * 1.1 / 2.25, "tensor: measured bf16 burst x nominal tf32/bf16 (1.1/2.25)"
+    return bf16, "tensor: measured bf16 burst" + (" (int8 codes on bf16 MMA)" if prec == "int8" else "")
 
 
-def run_ours(args, rank: int, world: int):
-    import torch
-    from conv_bn_silu_gb300 import _binding as B
+def int8_scales():
+    path = os.path.join(ROOT, "tests", "golden", "int8_scales.json")
+    return json.load(open(path))["layer_list"]
 
-    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(device)
-    cfg, layers = build_layers(args.workload, device)
-    n = cfg["n"]
-    peaks, peak_src = load_peaks()
-    ab = act_bytes(cfg["prec"])
 
-    # Resident inputs/outputs, rotated over R copies so the working set per
-    # rotation exceeds L2.
-    step_bytes = sum(s.alg_bytes(n, ab) for s, _, _ in layers)
-    R = max(2, int(np.ceil(2 * L2_BYTES / step_bytes)) + 1)
-    xs = [[torch.from_numpy(x).to(device) for (_, _, x) in layers] for _ in range(R)]
-    ys = [[layer.empty_y() for (_, layer, _) in layers] for _ in range(R)]
-    torch.cuda.synchronize()
+class ListWorkload:
+    """Independent layers, each on its own resident input; inputs and outputs
+    rotate over R copies so one rotation exceeds twice the L2 size."""
 
-    stream = torch.cuda.Stream(device)
-    sid = stream.cuda_stream
+    def __init__(self, cfg, device):
+        import torch
+        from conv_bn_silu_gb300 import _binding as B
+        from conv_bn_silu_gb300.layer import FusedConvBnSilu, make_desc
+        self.cfg, self.n, self.prec = cfg, cfg["n"], cfg["prec"]
+        cp = {"fp32": B.CBS_FP32, "tf32": B.CBS_TF32, "bf16": B.CBS_BF16, "int8": B.CBS_INT8}[self.prec]
+        self.specs = list(cfg["layers"])
+        self.layers, host_x = [], []
+        s_x = float(wl.S_X_INT8) if self.prec == "int8" else 0.0
+        self.s_y = int8_scales() if self.prec == "int8" else [None] * len(self.specs)
+        for i, spec in enumerate(self.specs):
+            x, p = wl.layer_inputs(spec, self.n, seed=0, layer_index=i)
+            desc = make_desc(self.n, spec.c_in, spec.h, spec.width, spec.c_out, spec.k, spec.stride, spec.pad,
+                             prec=cp)
+            self.layers.append(FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, s_x=s_x,
+                                               device=device))
+            host_x.append(x)
+        self.host_x = host_x
+        ab = act_bytes(self.prec)
+        self.step_bytes = sum(s.alg_bytes(self.n, ab) for s in self.specs)
+        self.R = max(2, int(np.ceil(2 * L2_BYTES / self.step_bytes)) + 1)
+        packed = []
+        for layer, x in zip(self.layers, host_x):
+            xd = torch.from_numpy(x).to(device)
+            packed.append(layer.pack_input(xd) if (self.prec != "fp32") else xd)
+        torch.cuda.synchronize()
+        self.xs = [[t.clone() for t in packed] for _ in range(self.R)]
+        self.ys = [[layer.empty_y() for layer in self.layers] for _ in range(self.R)]
+        self.launches_per_step = len(self.layers)
 
-    def step(r, events=None):
-        for j, (_, layer, _) in enumerate(layers):
+    def step(self, r, stream_id, events=None, stream=None):
+        for j, layer in enumerate(self.layers):
             if events is not None:
                 events[j].record(stream)
-            layer(xs[r][j], ys[r][j], stream=sid)
+            layer(self.xs[r % self.R][j], self.ys[r % self.R][j], s_y=self.s_y[j], stream=stream_id)
         if events is not None:
-            events[len(layers)].record(stream)
+            events[len(self.layers)].record(stream)
 
-    # Warm-up: W steps, eager.
+    def rows(self):
+        return [(s, layer) for s, layer in zip(self.specs, self.layers)]
+
+
+class ChainWorkload:
+    """The 40-layer whole-frame chain; one step = one frame batch (frame
+    packing, 40 fused layers, one glue kernel)."""
+
+    def __init__(self, cfg, device):
+        import torch
+        from conv_bn_silu_gb300.chain import Chain
+        self.cfg, self.n, self.prec = cfg, cfg["n"], cfg["prec"]
+        self.chain = Chain(self.prec, self.n, device=device)
+        self.frame = torch.from_numpy(wl.frame(self.n)).to(device)
+        self.specs = [cl.spec for cl in self.chain.specs]
+        self.layers = self.chain.layers
+        ab = act_bytes(self.prec)
+        self.step_bytes = self.chain.alg_bytes(ab)
+        self.R = 1
+        self.launches_per_step = self.chain.launches_per_frame()
+
+    def step(self, r, stream_id, events=None, stream=None):
+        from conv_bn_silu_gb300 import _binding as B
+        c = self.chain
+        B.cbs_pack_input(c.layers[0].plan, self.frame, c.x0, 0.0, stream_id)
+        for i, layer in enumerate(c.layers):
+            src = c.specs[i].src
+            if src[0] == "upcat":
+                a, b = c.outs[src[1]], c.outs[src[2]]
+                if c.layout == B.CBS_NHWC:
+                    n, h, w, cb = b.shape
+                    ca = a.shape[3]
+                else:
+                    n, cb, h, w = b.shape
+                    ca = a.shape[1]
+                B.cbs_upsample2x_concat(a, ca, b, cb, c.glue, n, h, w, c.layout, b.element_size(), stream_id)
+            if events is not None:
+                events[i].record(stream)
+            layer(c.input_of(i), c.outs[i], stream=stream_id)
+        if events is not None:
+            events[len(c.layers)].record(stream)
+
+    def rows(self):
+        return [(s, layer) for s, layer in zip(self.specs, self.layers)]
+
+
+def make_workload(name, device):
+    cfg = WORKLOADS[name]
+    return (ChainWorkload if cfg["kind"] == "chain" else ListWorkload)(cfg, device)
+
+
+def measure(name, steps, warmup, device, peaks, sample_clocks=False):
+    """Capture `steps` steps (events between launches) in one CUDA graph,
+    replay it once untimed, then once timed; returns the summary."""
+    import torch
+    w = make_workload(name, device)
+    stream = torch.cuda.Stream(device)
+    sid = stream.cuda_stream
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            step(i % R)
+        for i in range(warmup):
+            w.step(i, sid)
     torch.cuda.synchronize()
-
-    # Capture exactly K steps (with an event between every launch) in one graph.
-    K = args.steps
-    nl = len(layers)
+    nl = len(w.layers)
     try:
-        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(nl + 1)] for _ in range(K)]
-    except TypeError:  # older torch without external events
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(nl + 1)] for _ in range(steps)]
+    except TypeError:  # torch without external events: per-launch times unavailable
         evs = None
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(graph, stream=stream):
-            for i in range(K):
-                step(i % R, evs[i] if evs is not None else None)
+            for i in range(steps):
+                w.step(i, sid, evs[i] if evs is not None else None, stream)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        graph.replay()  # one untimed replay of the instantiated graph
+        graph.replay()
     torch.cuda.synchronize()
-
-    if world > 1:
-        torch.distributed.barrier()
-    sampler = ClockSampler(device.index)
-    time.sleep(0.3)
-    torch.cuda.synchronize()
+    sampler = ClockSampler(device.index) if sample_clocks else None
+    if sampler:
+        time.sleep(0.3)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t0.record(stream)
         graph.replay()
         t1.record(stream)
     torch.cuda.synchronize()
-    # Per-launch durations: read the in-graph events of the timed replay now.
+    total_ms = t0.elapsed_time(t1)
     per_layer_us = None
     if evs is not None:
-        per_layer_us = np.zeros(len(layers))
-        for i in range(args.steps):
-            for j in range(len(layers)):
+        per_layer_us = np.zeros(nl)
+        for i in range(steps):
+            for j in range(nl):
                 per_layer_us[j] += evs[i][j].elapsed_time(evs[i][j + 1]) * 1e3
-        per_layer_us /= args.steps
+        per_layer_us /= steps
+    clocks = None
+    if sampler:
+        tend = time.time() + 1.0
+        while time.time() < tend:
+            with torch.cuda.stream(stream):
+                graph.replay()
+            torch.cuda.synchronize()
+        clocks = sampler.stop()
+
+    n, prec = w.n, w.prec
+    ab = act_bytes(prec)
+    peak, peak_label = peak_for(prec, peaks)
+    hbm = float(peaks["hbm_gbs"])
+    rows = []
+    for j, (sp, layer) in enumerate(w.rows()):
+        f, by = sp.flops(n), sp.alg_bytes(n, ab)
+        t_c, t_m = f / (peak * 1e12), by / (hbm * 1e9)
+        bound = "compute" if t_c >= t_m else "hbm"
+        row = {"layer": j + 1, "shape": f"{sp.c_in}->{sp.c_out} k{sp.k} s{sp.stride} {sp.h}",
+               "tile": f"{layer.plan.block_m}x{layer.plan.block_n}", "split_k": layer.plan.split_k,
+               "mflop": round(f / 1e6, 2), "alg_mb": round(by / 1e6, 3), "bound": bound,
+               "roofline_us": round(max(t_c, t_m) * 1e6, 3)}
+        if per_layer_us is not None:
+            u = float(per_layer_us[j])
+            row.update(us=round(u, 3), tflops=round(f / (u * 1e-6) / 1e12, 3),
+                       frac_of_roofline=round(max(t_c, t_m) * 1e6 / u, 4),
+                       frac_of_compute_peak=round(t_c * 1e6 / u, 4), frac_of_hbm=round(t_m * 1e6 / u, 4))
+        rows.append(row)
+    flops_step = sum(sp.flops(n) for sp in w.specs)
+    ms_step = total_ms / steps
+    kern_us = float(per_layer_us.sum()) if per_layer_us is not None else ms_step * 1e3
+    out = {"workload": name, "prec": prec, "batch": n, "steps": steps, "ms_per_step": round(ms_step, 5),
+           "tflops": round(flops_step / (ms_step * 1e-3) / 1e12, 4),
+           "sum_layer_us": round(kern_us, 3),
+           "sum_layer_roofline_us": round(sum(r["roofline_us"] for r in rows), 3),
+           "frac_of_layer_roofline_sum": round(sum(r["roofline_us"] for r in rows) / kern_us, 4),
+           "peak_tflops": round(peak, 2), "peak": peak_label, "hbm_gbs": hbm,
+           "l2": (f"inputs larger than L2: {w.R} rotating copies of the step's {w.step_bytes / 1e6:.1f} MB"
+                  if w.R > 1 else f"chain activations, {w.step_bytes / 1e6:.1f} MB algorithmic per frame batch"),
+           "launches_per_step": w.launches_per_step, "layers": rows}
+    if per_layer_us is not None and name.startswith("layer_list") and n == 16:
+        k3 = [r for r in rows if " k3 " in r["shape"] and r["bound"] == "compute"]
+        mem = [r for r in rows if r not in k3]
+        if k3:
+            out["k3_compute_bound_frac_of_tensor_peak"] = round(
+                sum(r["mflop"] for r in k3) * 1e6 / (sum(r["us"] for r in k3) * 1e-6) / (peak * 1e12), 4)
+        if mem:
+            out["hbm_bound_frac_of_hbm"] = round(
+                sum(r["alg_mb"] for r in mem) * 1e6 / (sum(r["us"] for r in mem) * 1e-6) / (hbm * 1e9), 4)
+    return out, w, clocks
+
+
+def run_ours(args, rank: int, world: int):
+    import torch
+    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(device)
+    peaks, peak_src = load_peaks()
     if world > 1:
         torch.distributed.barrier()
-    total_ms = t0.elapsed_time(t1)
-    # keep the GPU busy with the same workload for >= 1 s so the clock sampler
-    # sees this load (the timed region itself may be shorter than a sample)
-    tend = time.time() + 1.0
-    while time.time() < tend:
-        with torch.cuda.stream(stream):
-            graph.replay()
-        torch.cuda.synchronize()
-    clocks = sampler.stop()
-
-    ms_step = total_ms / K
+    head, w, clocks = measure(args.workload, args.steps, args.warmup, device, peaks, sample_clocks=True)
+    if world > 1:
+        torch.distributed.barrier()
+    ms_step = head["ms_per_step"]
     if world > 1:
         t = torch.tensor([ms_step], device=device)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms_step = float(t.item())
-
-
-    flops_step = sum(s.flops(n) for s, _, _ in layers)
+    n = w.n
+    flops_step = sum(sp.flops(n) for sp in w.specs)
     value = flops_step * world / (ms_step * 1e-3) / 1e12
-
-    # Roofline of the dominant kernel (the FP32 CUDA-core conv kernel: every
-    # launch of this workload) and per layer.
-    hbm = float(peaks["hbm_gbs"])
-    layer_rows = []
-    for j, (s, layer, _) in enumerate(layers):
-        f, by = s.flops(n), s.alg_bytes(n, ab)
-        t_roof_us = max(f / (FP32_ALU_PEAK_TFLOPS * 1e12), by / (hbm * 1e9)) * 1e6
-        row = {"layer": j + 1, "shape": f"{s.c_in}->{s.c_out} k{s.k} s{s.stride} {s.h}",
-               "tile": f"{layer.plan.block_m}x{layer.plan.block_n}", "split_k": layer.plan.split_k,
-               "mflop": round(f / 1e6, 2), "alg_mb": round(by / 1e6, 3), "roofline_us": round(t_roof_us, 3)}
-        if per_layer_us is not None:
-            row["us"] = round(float(per_layer_us[j]), 3)
-            row["tflops"] = round(f / (per_layer_us[j] * 1e-6) / 1e12, 3)
-            row["frac_of_roofline"] = round(t_roof_us / per_layer_us[j], 4)
-        layer_rows.append(row)
-    if per_layer_us is not None:
-        kern_us = float(per_layer_us.sum())
-    else:
-        kern_us = ms_step * 1e3
+    rows = head["layers"]
+    kern_us = head["sum_layer_us"]
     achieved = flops_step / (kern_us * 1e-6) / 1e12
-    roofline = {"bound": "alu", "kernel": "simt_conv_kernel (FP32 FMA, all launches)",
-                "achieved": round(achieved, 3), "peak": round(FP32_ALU_PEAK_TFLOPS, 2), "unit": "TFLOP/s",
-                "frac": round(achieved / FP32_ALU_PEAK_TFLOPS, 4),
-                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz",
+    peak = head["peak_tflops"]
+    kernel = {"fp32": "simt_conv_kernel (FP32 FMA)", "tf32": "tc_conv_kernel<TF32>",
+              "bf16": "tc_conv_kernel<BF16>", "int8": "tc_conv_i8_kernel"}[w.prec]
+    roofline = {"bound": "alu" if w.prec == "fp32" else "tensor", "kernel": kernel + ", all launches",
+                "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "peak_source": head["peak"] + f" ({peak_src})",
                 "traffic": None,
-                "sum_layer_roofline_us": round(sum(r["roofline_us"] for r in layer_rows), 2),
-                "frac_of_layer_roofline_sum": (round(sum(r["roofline_us"] for r in layer_rows) / kern_us, 4)
-                                               if kern_us > 0 else None)}
-
-    e2e = run_e2e(layers, n, device, stream, args, flops_step, world)
+                "sum_layer_roofline_us": head["sum_layer_roofline_us"],
+                "frac_of_layer_roofline_sum": head["frac_of_layer_roofline_sum"]}
+    e2e = run_e2e(w, device, args, flops_step, world)
     out = {
         "metric": "fused conv+BN+SiLU TFLOP/s & us/frame over the layer list; % of roofline",
-        "value": round(value, 4), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "value": round(value, 4), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "us_per_frame": round(ms_step * 1e3 / n, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded N(0,1) inputs, He-init weights, random BN statistics)",
-        "config": {"workload": args.workload, "layers": len(layers), "batch": n, "layout": "NCHW",
-                   "l2": f"inputs larger than L2: {R} rotating copies of the step's {step_bytes / 1e6:.1f} MB",
-                   "timing": "K steps captured in one CUDA graph, events on the launching stream",
+        "dtype": {"fp32": "f32", "tf32": "tf32", "bf16": "bf16", "int8": "int8"}[w.prec],
+        "data": "synthetic (seeded N(0,1) inputs, He-init weights, random BN statistics)",
+        "config": {"workload": args.workload, "layers": len(rows), "batch": n,
+                   "layout": "NCHW" if w.prec == "fp32" else "NHWC", "l2": head["l2"],
+                   "timing": "K steps captured in one CUDA graph, events between launches on the launching stream",
                    "parallelism": f"replicas x{world}"},
-        "roofline": roofline, "layers": layer_rows,
-        "gpu_launches": K * len(layers),
+        "roofline": roofline, "layers": rows,
+        "gpu_launches": args.steps * w.launches_per_step,
         "e2e": e2e, "clocks": clocks, "peaks_source": peak_src,
     }
+    if rank == 0 and not args.no_extra:
+        extra = {}
+        for name in EXTRA_DEFAULT:
+            if name == args.workload:
+                continue
+            try:
+                summ, _, _ = measure(name, min(args.steps, 20), 3, device, peaks)
+                extra[name] = summ
+            except Exception as exc:  # report, do not hide, a failing extra workload
+                extra[name] = {"error": f"{type(exc).__name__}: {exc}"}
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+        out["extra"] = extra
     if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(cfg, layers)
+        out["cpu_baseline"] = cpu_baseline(w)
     return out
 
 
-def run_e2e(layers, n, device, stream, args, flops_step, world):
+def run_e2e(w, device, args, flops_step, world):
     """Same metric through the public API with host buffers: each step copies
-    its inputs from pinned host memory, runs the layers and reads every
-    output back; the host waits for the result."""
+    its inputs from pinned host memory (FP32 activations for the FP32 list;
+    the packed input format otherwise), runs the layers and reads every output
+    back; the host waits for the result."""
     import torch
-    xs_h = [torch.from_numpy(x).pin_memory() for (_, _, x) in layers]
-    ys_h = [torch.empty(layer.y_shape(), dtype=layer.x_dtype).pin_memory() for (_, layer, _) in layers]
-    xs_d = [torch.empty_like(x, device=device) for x in xs_h]
-    ys_d = [layer.empty_y() for (_, layer, _) in layers]
+    stream = torch.cuda.Stream(device)
     sid = stream.cuda_stream
+    xs_d = w.xs[0] if hasattr(w, "xs") else [w.frame]
+    ys_d = w.ys[0] if hasattr(w, "ys") else [w.chain.outs[-1]]
+    xs_h = [x.cpu().pin_memory() for x in xs_d]
+    ys_h = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys_d]
     steps = max(3, min(args.steps, 50))
 
     def one():
         with torch.cuda.stream(stream):
-            for j, (_, layer, _) in enumerate(layers):
+            for j in range(len(xs_d)):
                 xs_d[j].copy_(xs_h[j], non_blocking=True)
-                layer(xs_d[j], ys_d[j], stream=sid)
+            w.step(0, sid)
+            for j in range(len(ys_d)):
                 ys_h[j].copy_(ys_d[j], non_blocking=True)
         stream.synchronize()
 
@@ -292,23 +410,25 @@ def run_e2e(layers, n, device, stream, args, flops_step, world):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
-def cpu_baseline(cfg, layers, budget_s: float = 20.0):
+def cpu_baseline(w, budget_s: float = 10.0):
     """The CPU oracle as it stands, on the host cores, on a bounded sample of
-    the same workload: layers of the list in order until the budget is
-    spent (the last one included)."""
+    the same workload: passes over the list's layers (full size) until about
+    `budget_s` seconds of CPU work are done."""
     import oracle
-    done_flops, t0, used = 0, time.perf_counter(), []
-    for i, (spec, _, x) in enumerate(layers):
-        _, p = wl.layer_inputs(spec, cfg["n"], seed=0, layer_index=i)
-        oracle.conv_bn_silu_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, spec.stride, spec.pad)
-        done_flops += spec.flops(cfg["n"])
-        used.append(i + 1)
-        if time.perf_counter() - t0 > budget_s:
-            break
+    specs = list(WORKLOADS["layer_list_fp32_n1"]["layers"]) if not hasattr(w, "host_x") else w.specs
+    n = w.n if hasattr(w, "host_x") else 1
+    inputs = [wl.layer_inputs(s, n, seed=0, layer_index=i) for i, s in enumerate(specs)]
+    done_flops, layers_done, t0 = 0, 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        for spec, (x, p) in zip(specs, inputs):
+            oracle.conv_bn_silu_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, spec.stride, spec.pad)
+            done_flops += spec.flops(n)
+            layers_done += 1
     dt = time.perf_counter() - t0
     return {"value": round(done_flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle", "seconds": round(dt, 2),
-            "sample": f"layers {used[0]}..{used[-1]} of the list at batch {cfg['n']}, one pass, double arithmetic"}
+            "sample": f"{layers_done} full-size layers of the list at batch {n} "
+                      f"({layers_done / len(specs):.0f} passes), double arithmetic"}
 
 
 def run_reference(args, rank: int, world: int):
@@ -318,7 +438,7 @@ def run_reference(args, rank: int, world: int):
         return None
     import oracle
     cfg = WORKLOADS[args.workload]
-    specs = cfg["layers"]
+    specs = cfg["layers"] if cfg["kind"] == "list" else [cl.spec for cl in wl.chain_layers()]
     inputs = [wl.layer_inputs(s, cfg["n"], seed=0, layer_index=i) for i, s in enumerate(specs)]
 
     def step(i):
@@ -353,6 +473,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="layer_list_fp32_n1", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other configs' summaries")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

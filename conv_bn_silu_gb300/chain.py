@@ -1,0 +1,91 @@
+"""The 40-layer whole-frame chain of fused layers (YOLO26n-scale shapes).
+
+Layers and their sources are those of `workloads.chain_layers()`: the list's
+first eleven layers from the frame, the 384->128 1x1 layer on
+concat(upsample2x(layer 10), layer 7), and 28 stride-1 repeats at 80/40/20.
+Every computation runs in libcbs.so: the chain-entry layout step
+(cbs_pack_input), the fused layers and the neck glue.
+
+FP32 runs the CUDA-core variant in NCHW; TF32, BF16 and INT8 run the
+tensor-core variants in NHWC, where only the frame needs packing.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import _binding as B
+from . import workloads as wl
+from .layer import FusedConvBnSilu, current_stream, make_desc
+
+PRECS = {"fp32": B.CBS_FP32, "tf32": B.CBS_TF32, "bf16": B.CBS_BF16}
+
+
+class Chain:
+    def __init__(self, prec: str, n: int, seed: int = 0, device="cuda"):
+        self.prec = prec
+        self.n = n
+        self.device = torch.device(device)
+        self.specs = wl.chain_layers()
+        cp = PRECS[prec]
+        self.layout = B.CBS_NCHW if prec == "fp32" else B.CBS_NHWC
+        self.layers = []
+        for i, cl in enumerate(self.specs):
+            s = cl.spec
+            p = wl.layer_params(s, seed=seed, layer_index=100 + i)
+            desc = make_desc(n, s.c_in, s.h, s.width, s.c_out, s.k, s.stride, s.pad, prec=cp,
+                             in_layout=self.layout, out_layout=self.layout)
+            self.layers.append(FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps,
+                                               device=self.device))
+        self.outs = [layer.empty_y() for layer in self.layers]
+        self.x0 = self.layers[0].empty_x()
+        s11 = self.specs[11].spec
+        if self.layout == B.CBS_NHWC:
+            glue_shape = (n, s11.h, s11.width, s11.c_in)
+        else:
+            glue_shape = (n, s11.c_in, s11.h, s11.width)
+        self.glue = torch.empty(glue_shape, dtype=self.layers[11].x_dtype, device=self.device)
+
+    def params(self, i: int, seed: int = 0):
+        return wl.layer_params(self.specs[i].spec, seed=seed, layer_index=100 + i)
+
+    def input_of(self, i: int):
+        """The device tensor layer i reads (after its source has run)."""
+        src = self.specs[i].src
+        if src[0] == "frame":
+            return self.x0
+        if src[0] == "layer":
+            return self.outs[src[1]]
+        return self.glue
+
+    def launches_per_frame(self) -> int:
+        return len(self.layers) + 2  # 40 fused layers, frame packing, one glue kernel
+
+    def run(self, frame_nchw: torch.Tensor, stream: int | None = None):
+        """One frame batch: pack the frame, then the 40 layers in order."""
+        s = current_stream() if stream is None else stream
+        B.cbs_pack_input(self.layers[0].plan, frame_nchw, self.x0, 0.0, s)
+        for i, layer in enumerate(self.layers):
+            src = self.specs[i].src
+            if src[0] == "upcat":
+                a, b = self.outs[src[1]], self.outs[src[2]]
+                if self.layout == B.CBS_NHWC:
+                    n, h, w, cb = b.shape
+                    ca = a.shape[3]
+                else:
+                    n, cb, h, w = b.shape
+                    ca = a.shape[1]
+                B.cbs_upsample2x_concat(a, ca, b, cb, self.glue, n, h, w, self.layout, b.element_size(), s)
+            layer(self.input_of(i), self.outs[i], stream=s)
+        return self.outs
+
+    def flops(self) -> int:
+        return sum(cl.spec.flops(self.n) for cl in self.specs)
+
+    def alg_bytes(self, act_bytes: int) -> int:
+        return sum(cl.spec.alg_bytes(self.n, act_bytes) for cl in self.specs)
+
+
+def to_nchw_numpy(t: torch.Tensor, layout: int) -> np.ndarray:
+    a = t.float().cpu().numpy()
+    return np.ascontiguousarray(a.transpose(0, 3, 1, 2)) if layout == B.CBS_NHWC else a

@@ -1,0 +1,86 @@
+"""The 40-layer whole-frame chain on the GPU against the CPU oracle.
+
+Pass/fail is teacher-forced: every GPU layer is fed the oracle's input for
+that layer (packed into the layer's format by cbs_pack_input) and its output
+is compared with the oracle's, with the bars of its variant (FP32: relative
+L2 <= 1e-5; TF32/BF16: relative L2 <= 5e-3, scaled max abs <= 2e-2 on the
+values the kernel reads).  The free-running chain (each GPU layer on the GPU
+output before it) is checked for finiteness and its drift is printed.
+
+FP32 runs at batch 1 (the frame config); TF32 and BF16 at batch 16, the
+launch configuration of the throughput config, checked on images 0 and 15
+(the oracle computes only those two; the other images repeat them)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conv_bn_silu_gb300 import _binding as B
+from conv_bn_silu_gb300 import workloads as wl
+from conv_bn_silu_gb300.chain import Chain, to_nchw_numpy
+from helpers import TOL_FP32_REL_L2, TOL_TC_MAX_ABS, TOL_TC_REL_L2, max_scaled_err, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def upcat(a, b):
+    """Neck glue on NCHW arrays: concat(upsample2x(a), b) along channels."""
+    return np.concatenate([a.repeat(2, axis=2).repeat(2, axis=3), b], axis=1)
+
+
+def oracle_chain(chain, frame):
+    """Oracle inputs and outputs of every layer (NCHW float32)."""
+    ins, outs = [], []
+    for i, cl in enumerate(chain.specs):
+        s, src = cl.spec, cl.src
+        x = frame if src[0] == "frame" else outs[src[1]] if src[0] == "layer" else upcat(outs[src[1]], outs[src[2]])
+        p = chain.params(i)
+        ins.append(x)
+        outs.append(oracle.conv_bn_silu_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, s.stride, s.pad))
+    return ins, outs
+
+
+def bf16_round(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).float().numpy()
+
+
+@pytest.mark.parametrize("prec,n", [("fp32", 1), ("tf32", 16), ("bf16", 16)])
+def test_chain_teacher_forced(cuda_lib, prec, n):
+    chain = Chain(prec, n)
+    frame = wl.frame(n)
+    sel = [0] if n == 1 else [0, n - 1]
+    ins, outs = oracle_chain(chain, np.ascontiguousarray(frame[sel]))
+    k = len(sel)
+    tile = lambda a: np.ascontiguousarray(a[[j % k for j in range(n)]])  # noqa: E731
+    s = torch.cuda.current_stream().cuda_stream
+    worst = []
+    for i, layer in enumerate(chain.layers):
+        x_dev = torch.from_numpy(tile(ins[i])).cuda()
+        xin = layer.empty_x()
+        B.cbs_pack_input(layer.plan, x_dev, xin, 0.0, s)
+        y = to_nchw_numpy(layer(xin), chain.layout)
+        got = y[[0] if n == 1 else [0, n - 1]]
+        e = rel_l2(got, outs[i])
+        if prec == "fp32":
+            assert e <= TOL_FP32_REL_L2, (i, e)
+        else:
+            xr = ins[i] if prec == "tf32" else bf16_round(ins[i])
+            p = chain.params(i)
+            sp = chain.specs[i].spec
+            ref_read = oracle.conv_bn_silu_f32(xr, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, sp.stride, sp.pad)
+            m = max_scaled_err(got, ref_read)
+            assert e <= TOL_TC_REL_L2 and m <= TOL_TC_MAX_ABS, (i, e, m)
+        worst.append(e)
+    print(f"{prec} n={n}: teacher-forced worst rel L2 {max(worst):.3e}")
+
+    # Free-running chain from the frame.
+    frame_dev = torch.from_numpy(frame).cuda()
+    chain.run(frame_dev)
+    torch.cuda.synchronize()
+    drift = []
+    for i in range(len(chain.layers)):
+        y = to_nchw_numpy(chain.outs[i], chain.layout)[[0] if n == 1 else [0, n - 1]]
+        assert np.isfinite(y).all(), i
+        drift.append(rel_l2(y, outs[i]))
+    print(f"{prec} n={n}: free-running drift, last layer {drift[-1]:.3e}, max {max(drift):.3e}")
+    assert max(drift) < 0.2
