@@ -24,6 +24,7 @@ CBS_ERR_PLAN_MISMATCH = -7
 CBS_NCHW, CBS_NHWC = 0, 1
 CBS_FP32, CBS_TF32, CBS_BF16, CBS_INT8 = 0, 1, 2, 3
 CBS_VARIANT_SIMT_FP32, CBS_VARIANT_TC_TF32, CBS_VARIANT_TC_BF16, CBS_VARIANT_TC_INT8 = 0, 1, 2, 3
+CBS_VARIANT_STEM = 4
 
 EXPORTED = (
     "cbs_plan", "cbs_fold_bn", "cbs_pack_input", "cbs_conv_bn_silu_f32", "cbs_conv_bn_silu_i8",

@@ -146,6 +146,20 @@ cbs_status check_ptr(const void *ptr, const char *name, bool nullable = false) {
         if (_s != CBS_OK) return _s;       \
     } while (0)
 
+StemLaunch stem_launch(const cbs_plan_t &p, const void *x, const void *w, const void *bias, const float *m_c,
+                       float inv_s_y, void *y) {
+    const cbs_layer_desc &d = p.desc;
+    StemLaunch L{};
+    L.x = x; L.w = w; L.bias = bias; L.m_c = m_c; L.inv_s_y = inv_s_y; L.y = y;
+    L.N = d.n; L.C = d.c_in; L.c_pad = p.c_in_pad; L.H = d.h; L.W = d.w; L.Cout = d.c_out;
+    L.OH = p.oh; L.OW = p.ow; L.KS = d.k; L.stride = d.stride; L.pad = d.pad;
+    L.in_nhwc = d.in_layout == CBS_NHWC;
+    L.out_nhwc = d.out_layout == CBS_NHWC;
+    L.out_row_stride = p.out_row_stride;
+    L.kind = d.prec == CBS_INT8 ? 2 : (d.prec == CBS_BF16 ? 1 : 0);
+    return L;
+}
+
 }  // namespace
 }  // namespace cbs
 
@@ -199,11 +213,18 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
     if (M > 0x7fffffffLL || (long long)D.n * D.c_in * D.h * D.w > (1LL << 40))
         return fail(CBS_ERR_UNSUPPORTED, "problem too large for 32-bit pixel indexing");
 
+    const bool stem_fits = D.c_in <= kStemMaxCin && D.c_out <= kStemMaxCout && D.k <= kStemMaxK;
     int variant = D.force_variant;
-    if (variant < 0) variant = D.prec;  // enum values line up: FP32->SIMT, TF32, BF16, INT8
-    const int need_prec[] = {CBS_FP32, CBS_TF32, CBS_BF16, CBS_INT8};
-    if (variant < 0 || variant > 3 || need_prec[variant] != D.prec)
-        return fail(CBS_ERR_INVALID_ARG, "variant %d does not compute precision %d", variant, D.prec);
+    if (variant < 0) variant = stem_fits ? (int)CBS_VARIANT_STEM : D.prec;  // FP32->SIMT, TF32, BF16, INT8
+    if (variant == CBS_VARIANT_STEM) {
+        if (!stem_fits)
+            return fail(CBS_ERR_UNSUPPORTED, "stem variant needs C_in <= %d, C_out <= %d, k <= %d", kStemMaxCin,
+                        kStemMaxCout, kStemMaxK);
+    } else {
+        const int need_prec[] = {CBS_FP32, CBS_TF32, CBS_BF16, CBS_INT8};
+        if (variant < 0 || variant > 3 || need_prec[variant] != D.prec)
+            return fail(CBS_ERR_INVALID_ARG, "variant %d does not compute precision %d", variant, D.prec);
+    }
     p.variant = variant;
 
     if (D.out_row_stride != 0) {
@@ -215,7 +236,9 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
     p.out_row_stride = D.out_row_stride ? D.out_row_stride : p.ow;
 
     const size_t eb = elem_bytes(D.prec);
-    if (variant == CBS_VARIANT_SIMT_FP32) {
+    if (variant == CBS_VARIANT_STEM) {
+        p.c_in_pad = (D.in_layout == CBS_NHWC && D.prec != CBS_FP32) ? 4 : D.c_in;
+    } else if (variant == CBS_VARIANT_SIMT_FP32) {
         p.c_in_pad = D.c_in;
     } else {
         if (D.in_layout != CBS_NHWC)
@@ -228,10 +251,23 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
         p.y_bytes = (size_t)D.n * D.c_out * p.oh * p.out_row_stride * eb;
     else
         p.y_bytes = (size_t)M * D.c_out * eb;
-    p.w_packed_bytes = (size_t)D.c_out * p.k_gemm * (variant == CBS_VARIANT_SIMT_FP32 || variant == CBS_VARIANT_TC_TF32 ? 4 : 2);
+    p.w_packed_bytes = (size_t)D.c_out * p.k_gemm * (D.prec == CBS_FP32 || D.prec == CBS_TF32 ? 4 : 2);
     p.bias_bytes = (size_t)D.c_out * 4;
 
-    if (variant == CBS_VARIANT_SIMT_FP32) {
+    if (variant == CBS_VARIANT_STEM) {
+        const int cout_t = D.c_out <= 16 ? 16 : (D.c_out <= 32 ? 32 : 64);
+        p.block_m = 256;  // output pixels per CTA, one per thread
+        p.block_n = cout_t;
+        p.block_k = D.k * D.k * p.c_in_pad;
+        p.stages = 1;
+        p.split_k = 1;
+        p.m_tiles = (int)((M + 255) / 256);
+        p.n_tiles = 1;
+        p.grid_ctas = p.m_tiles;
+        p.threads = 256;
+        p.smem_bytes = D.k * D.k * p.c_in_pad * cout_t * 4;
+        p.workspace_bytes = 0;
+    } else if (variant == CBS_VARIANT_SIMT_FP32) {
         plan_simt(p);
     } else {
         CBS_TRY(plan_tc(p));
@@ -253,7 +289,7 @@ cbs_status cbs_fold_bn(const cbs_plan_t *p, const float *w_oihw, const float *co
     CBS_TRY(check_ptr(w_packed, "w_packed"));
     CBS_TRY(check_ptr(bias, "bias"));
     if (!(eps > 0.0f)) return fail(CBS_ERR_INVALID_ARG, "eps must be > 0");
-    if (p->variant == CBS_VARIANT_TC_INT8) {
+    if (p->desc.prec == CBS_INT8) {
         CBS_TRY(check_ptr(m_c, "m_c"));
         if (!(s_x > 0.0f)) return fail(CBS_ERR_INVALID_ARG, "s_x must be > 0 for INT8");
     }
@@ -261,7 +297,12 @@ cbs_status cbs_fold_bn(const cbs_plan_t *p, const float *w_oihw, const float *co
     L.w = w_oihw; L.conv_bias = conv_bias; L.gamma = gamma; L.beta = beta; L.mean = mean; L.var = var;
     L.eps = eps; L.s_x = s_x;
     L.C_out = p->desc.c_out; L.C_in = p->desc.c_in; L.KS = p->desc.k; L.c_in_pad = p->c_in_pad;
-    L.variant = p->variant; L.w_packed = w_packed; L.bias = bias; L.m_c = m_c;
+    L.variant = p->variant;
+    if (p->variant == CBS_VARIANT_STEM) {  // stem weights use the tensor-core layouts of its precision
+        const int by_prec[] = {CBS_VARIANT_TC_TF32, CBS_VARIANT_TC_TF32, CBS_VARIANT_TC_BF16, CBS_VARIANT_TC_INT8};
+        L.variant = by_prec[p->desc.prec];
+    }
+    L.w_packed = w_packed; L.bias = bias; L.m_c = m_c;
     return cuda_check(launch_fold(L, (cudaStream_t)stream), "fold kernel launch");
 }
 
@@ -303,11 +344,15 @@ cbs_status cbs_conv_bn_silu_f32(const cbs_plan_t *p, const void *x, const void *
                                 const float *bias, void *y, void *workspace, size_t workspace_bytes,
                                 void *stream) {
     CBS_TRY(check_plan(p));
-    if (p->variant == CBS_VARIANT_TC_INT8)
+    if (p->desc.prec == CBS_INT8)
         return fail(CBS_ERR_INVALID_ARG, "INT8 plans run through cbs_conv_bn_silu_i8");
     const cbs_layer_desc &d = p->desc;
     if (d.n == 0) return CBS_OK;  // empty batch: nothing is read or written
     CBS_TRY(check_conv_common(p, x, w_packed, bias, y, workspace, workspace_bytes));
+    if (p->variant == CBS_VARIANT_STEM) {
+        const StemLaunch L = stem_launch(*p, x, w_packed, bias, nullptr, 0.0f, y);
+        return cuda_check(launch_stem(L, (cudaStream_t)stream), "stem kernel launch");
+    }
     if (p->variant == CBS_VARIANT_SIMT_FP32) {
         SimtLaunch L;
         std::memset(&L, 0, sizeof(L));
@@ -340,7 +385,7 @@ cbs_status cbs_conv_bn_silu_i8(const cbs_plan_t *p, const int8_t *x, const void 
                                const int32_t *bias_i32, const float *m_c, float s_y, int8_t *y,
                                void *workspace, size_t workspace_bytes, void *stream) {
     CBS_TRY(check_plan(p));
-    if (p->variant != CBS_VARIANT_TC_INT8)
+    if (p->desc.prec != CBS_INT8)
         return fail(CBS_ERR_INVALID_ARG, "plan is not an INT8 plan");
     if (p->desc.n == 0) return CBS_OK;  // empty batch: nothing is read or written
     CBS_TRY(check_conv_common(p, x, w_packed, bias_i32, y, workspace, workspace_bytes));
@@ -348,6 +393,10 @@ cbs_status cbs_conv_bn_silu_i8(const cbs_plan_t *p, const int8_t *x, const void 
     if (!(s_y > 0.0f) || !(s_y < 3.0e38f)) return fail(CBS_ERR_INVALID_ARG, "s_y must be a positive finite float");
     if (p->desc.n == 0) return CBS_OK;
     const float inv_s_y = 1.0f / s_y;
+    if (p->variant == CBS_VARIANT_STEM) {
+        const StemLaunch L = stem_launch(*p, x, w_packed, bias_i32, m_c, inv_s_y, y);
+        return cuda_check(launch_stem(L, (cudaStream_t)stream), "stem kernel launch");
+    }
     return launch_tc(*p, x, w_packed, bias_i32, m_c, inv_s_y, y, workspace, (cudaStream_t)stream);
 }
 

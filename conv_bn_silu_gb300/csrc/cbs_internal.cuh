@@ -53,6 +53,19 @@ cudaError_t launch_simt(const SimtLaunch &L, cudaStream_t s);
 // Dynamic shared memory of one CUDA-core CTA (tiles + k table).
 int simt_smem_bytes(int tile, int k_chunk, int out_nhwc);
 
+// ---------------------------------------------------------------- stem
+struct StemLaunch {
+    const void *x, *w, *bias;  // w: [C_out][KS*KS*c_pad] float (kind 0) or bf16 (kinds 1, 2)
+    const float *m_c;          // INT8 only
+    float inv_s_y;             // INT8 only
+    void *y;
+    int N, C, c_pad, H, W, Cout, OH, OW, KS, stride, pad;
+    int in_nhwc, out_nhwc, out_row_stride;
+    int kind;                  // 0 float, 1 bf16, 2 int8
+};
+cudaError_t launch_stem(const StemLaunch &L, cudaStream_t s);
+constexpr int kStemMaxCin = 4, kStemMaxCout = 64, kStemMaxK = 7;
+
 // ---------------------------------------------------------------- misc kernels
 struct FoldLaunch {
     const float *w;           // [C_out][C_in][k][k]

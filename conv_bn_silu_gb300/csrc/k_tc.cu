@@ -26,13 +26,16 @@
 #include <mutex>
 
 #include "cbs_internal.cuh"
+#include "requant.cuh"
 #include "tc_ptx.cuh"
 
 namespace cbs {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;     // TF32/BF16: producer, MMA, 8 epilogue warps (2..9)
+constexpr int kThreadsI8 = 448;   // INT8: + four converter warps (10..13)
+constexpr int kEpiWarps = 8;      // two per TMEM lane quadrant, splitting the columns
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kSmemBudget = 200 * 1024;
 
@@ -46,6 +49,8 @@ struct TcParams {
     int BN, stages, a_bytes, b_bytes, stage_bytes;
     int im2col, out_nhwc, out_row_stride;
     uint32_t idesc, swz, tmem_cols;
+    int acc_stride;            // TMEM columns of one accumulator buffer
+    int m_tiles, n_tiles;      // tile grid walked by the persistent CTAs
     const float *bias;
     void *y;
     unsigned int *status;
@@ -54,13 +59,107 @@ struct TcParams {
     const float *m_c;
     float inv_s_y;
     int nchunks, kpc;          // exact-sum K chunks and K steps per chunk
+    int chunk_stride;          // TMEM columns between chunk accumulators (power of two)
     int stg_bytes;             // int8 staging tile of one stage (128 x CB bytes)
     uint32_t stg_mask;         // staging swizzle mask (bits 7.. -> bits 4..)
     uint32_t op_mask;          // operand swizzle mask
 };
 
-__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+// SiLU(z) = z * sigmoid(z) = h + h * tanh(h) with h = z / 2: one MUFU
+// operation per output (tanh.approx, relative error ~2^-11, far below the
+// TF32/BF16 tolerances and the bfloat16 output rounding).
+__device__ __forceinline__ float silu_fast(float z) {
+    const float h = 0.5f * z;
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+    return fmaf(h, t, h);
+}
 
+// Bias + SiLU + store of 16 consecutive output channels of one pixel.
+template <int KIND>
+__device__ __forceinline__ void epi_store16(const TcParams &p, int m, int img, int oh, int ow, int nbase,
+                                            const uint32_t (&v)[16]) {
+    float bv[16];
+    const bool full = nbase + 16 <= p.C_out;
+    if (full) {
+#pragma unroll
+        for (int jj = 0; jj < 16; jj += 4) {
+            const float4 b4 = __ldg(reinterpret_cast<const float4 *>(p.bias + nbase + jj));
+            bv[jj] = b4.x; bv[jj + 1] = b4.y; bv[jj + 2] = b4.z; bv[jj + 3] = b4.w;
+        }
+    } else {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) bv[jj] = nbase + jj < p.C_out ? __ldg(p.bias + nbase + jj) : 0.0f;
+    }
+    float o[16];
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) o[jj] = silu_fast(__uint_as_float(v[jj]) + bv[jj]);
+    if (p.out_nhwc) {
+        if (KIND == kTF32) {
+            float *yr = static_cast<float *>(p.y) + (size_t)m * p.C_out + nbase;
+            if (full && (p.C_out & 3) == 0) {
+#pragma unroll
+                for (int jj = 0; jj < 16; jj += 4)
+                    *reinterpret_cast<float4 *>(yr + jj) = make_float4(o[jj], o[jj + 1], o[jj + 2], o[jj + 3]);
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                    if (nbase + jj < p.C_out) yr[jj] = o[jj];
+            }
+        } else {
+            __nv_bfloat16 *yr = static_cast<__nv_bfloat16 *>(p.y) + (size_t)m * p.C_out + nbase;
+            if (full && (p.C_out & 7) == 0) {
+                uint32_t w[8];
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * jj], o[2 * jj + 1]);
+                    w[jj] = *reinterpret_cast<uint32_t *>(&h2);
+                }
+                *reinterpret_cast<uint4 *>(yr) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(yr + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                    if (nbase + jj < p.C_out) yr[jj] = __float2bfloat16_rn(o[jj]);
+            }
+        }
+    } else {
+        // NCHW: lanes hold consecutive pixels, so each channel's store is
+        // contiguous across the warp.
+        const size_t plane = (size_t)p.OH * p.out_row_stride;
+        const size_t pix = (size_t)oh * p.out_row_stride + ow;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            if (nbase + jj >= p.C_out) continue;
+            const size_t off = ((size_t)img * p.C_out + nbase + jj) * plane + pix;
+            if (KIND == kTF32)
+                static_cast<float *>(p.y)[off] = o[jj];
+            else
+                static_cast<__nv_bfloat16 *>(p.y)[off] = __float2bfloat16_rn(o[jj]);
+        }
+    }
+}
+
+// Tile t of the persistent walk: M-tile major, N-tile minor, so CTAs that
+// run at the same time share A rows through L2.
+__device__ __forceinline__ void tile_coords(int t, int n_tiles, int &m0, int &n0, int BN) {
+    const int mt = t / n_tiles;
+    m0 = mt * kBM;
+    n0 = (t - mt * n_tiles) * BN;
+}
+
+__device__ __forceinline__ void abort_now(const TcParams &p, int *abort_flag) {
+    atomicOr(p.status, 1u);
+    *(volatile int *)abort_flag = 1;
+}
+
+__device__ __forceinline__ bool aborted(int *abort_flag) { return *(volatile int *)abort_flag != 0; }
+
+// Persistent tensor-core kernel (TF32 / BF16).  Each CTA walks the tiles
+// t = blockIdx.x, blockIdx.x + gridDim.x, ...; the producer's stage ring and
+// the MMA issuer run ahead across tile boundaries, and the accumulator is
+// double-buffered in TMEM so the epilogue of tile j overlaps the MMAs of
+// tile j+1.
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcParams p) {
@@ -71,27 +170,32 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t *base_ptr = smem_raw + (base - raw_addr);
     const int S = p.stages;
-    const uint32_t bars = base + S * p.stage_bytes;           // full[S], empty[S], acc_full
+    // Barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain.
+    const uint32_t bars = base + S * p.stage_bytes;
     uint64_t *bar_ptr = reinterpret_cast<uint64_t *>(base_ptr + S * p.stage_bytes);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_ptr + 2 * S + 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_ptr + 2 * S + 5);
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
-    float *bias_s = reinterpret_cast<float *>(tmem_slot + 4);
 
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
-    const uint32_t acc_bar = bars + 8u * (2 * S);
+    auto accf_bar = [&](int a) { return bars + 8u * (2 * S + a); };
+    auto acce_bar = [&](int a) { return bars + 8u * (2 * S + 2 + a); };
+    const uint32_t drain_bar = bars + 8u * (2 * S + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * kBM;
-    const int n0 = blockIdx.y * p.BN;
     const int nk = p.ksteps;
+    const int num_tiles = p.m_tiles * p.n_tiles;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(full_bar(s), 1);
             ptx::mbar_init(empty_bar(s), 1);
         }
-        ptx::mbar_init(acc_bar, 1);
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(accf_bar(a), 1);
+            ptx::mbar_init(acce_bar(a), kEpiWarps);   // one arrive per epilogue warp
+        }
+        ptx::mbar_init(drain_bar, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmA);
@@ -101,153 +205,141 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), p.tmem_cols);
         ptx::tmem_relinquish();
     }
-    for (int i = threadIdx.x; i < p.BN; i += blockDim.x) {
-        const int n = n0 + i;
-        bias_s[i] = n < p.C_out ? p.bias[n] : 0.0f;
-    }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    int issued = 0;  // producer: K steps whose loads were issued
+    int issued = 0;  // producer: K steps whose loads were issued (global count)
     if (warp == 0) {
         if (lane == 0) {
-            // Window corner of the tile's first output pixel.
-            const int img = m0 / p.OHW;
-            const int rem = m0 - img * p.OHW;
-            const int oh = rem / p.OW, ow = rem - (rem / p.OW) * p.OW;
-            const int wc = ow * p.stride - p.pad, hc = oh * p.stride - p.pad;
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % S, u = i / S;
-                if (!ptx::mbar_wait_bounded(empty_bar(s), (u & 1) ^ 1, kWaitLimitNs)) {
-                    atomicOr(p.status, 1u);
-                    *(volatile int *)abort_flag = 1;
-                    break;
+            int g = 0;
+            for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
+                int m0, n0;
+                tile_coords(t, p.n_tiles, m0, n0, p.BN);
+                // Window corner of the tile's first output pixel.
+                const int img = m0 / p.OHW;
+                const int rem = m0 - img * p.OHW;
+                const int oh = rem / p.OW, ow = rem - (rem / p.OW) * p.OW;
+                const int wc = ow * p.stride - p.pad, hc = oh * p.stride - p.pad;
+                for (int i = 0; i < nk; ++i, ++g) {
+                    const int s = g % S, u = g / S;
+                    if (!ptx::mbar_wait_bounded(empty_bar(s), (u & 1) ^ 1, kWaitLimitNs)) {
+                        abort_now(p, abort_flag);
+                        break;
+                    }
+                    if (aborted(abort_flag)) break;
+                    const int tap = i / p.cblocks, cb = i - tap * p.cblocks;
+                    const int r = tap / p.ks, tt = tap - r * p.ks;
+                    const uint32_t a_dst = base + s * p.stage_bytes;
+                    const uint32_t b_dst = a_dst + p.a_bytes;
+                    ptx::mbar_arrive_expect_tx(full_bar(s), (uint32_t)(p.a_bytes + p.b_bytes));
+                    if (p.im2col)
+                        ptx::tma_load_im2col_4d(a_dst, &tmA, full_bar(s), cb * p.CB, wc, hc, img, (uint16_t)tt,
+                                                (uint16_t)r);
+                    else
+                        ptx::tma_load_2d(a_dst, &tmA, full_bar(s), cb * p.CB, m0);
+                    ptx::tma_load_2d(b_dst, &tmB, full_bar(s), tap * p.c_in_pad + cb * p.CB, n0);
+                    issued = g + 1;
                 }
-                if (*(volatile int *)abort_flag) break;
-                const int tap = i / p.cblocks, cb = i - tap * p.cblocks;
-                const int r = tap / p.ks, t = tap - r * p.ks;
-                const uint32_t a_dst = base + s * p.stage_bytes;
-                const uint32_t b_dst = a_dst + p.a_bytes;
-                ptx::mbar_arrive_expect_tx(full_bar(s), (uint32_t)(p.a_bytes + p.b_bytes));
-                if (p.im2col)
-                    ptx::tma_load_im2col_4d(a_dst, &tmA, full_bar(s), cb * p.CB, wc, hc, img, (uint16_t)t,
-                                            (uint16_t)r);
-                else
-                    ptx::tma_load_2d(a_dst, &tmA, full_bar(s), cb * p.CB, m0);
-                ptx::tma_load_2d(b_dst, &tmB, full_bar(s), tap * p.c_in_pad + cb * p.CB, n0);
-                issued = i + 1;
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t sbo = 8u * p.RB;
             const int kslices = p.RB / 32;
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % S, u = i / S;
-                if (!ptx::mbar_wait_bounded(full_bar(s), u & 1, kWaitLimitNs)) {
-                    atomicOr(p.status, 1u);
-                    *(volatile int *)abort_flag = 1;
+            int g = 0, j = 0;
+            for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x, ++j) {
+                const int acc = j & 1, ua = j >> 1;
+                if (!ptx::mbar_wait_bounded(acce_bar(acc), (ua & 1) ^ 1, kWaitLimitNs)) {
+                    abort_now(p, abort_flag);
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t a_addr = base + s * p.stage_bytes;
-                const uint32_t b_addr = a_addr + p.a_bytes;
-                for (int j = 0; j < kslices; ++j) {
-                    const uint64_t ad = ptx::smem_desc(a_addr + 32u * j, 16u, sbo, p.swz);
-                    const uint64_t bd = ptx::smem_desc(b_addr + 32u * j, 16u, sbo, p.swz);
-                    if (KIND == kTF32)
-                        ptx::mma_tf32(tmem_base, ad, bd, p.idesc, (i > 0 || j > 0) ? 1u : 0u);
-                    else
-                        ptx::mma_f16(tmem_base, ad, bd, p.idesc, (i > 0 || j > 0) ? 1u : 0u);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_stride);
+                bool ok = true;
+                for (int i = 0; i < nk; ++i, ++g) {
+                    const int s = g % S, u = g / S;
+                    if (!ptx::mbar_wait_bounded(full_bar(s), u & 1, kWaitLimitNs)) {
+                        abort_now(p, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t a_addr = base + s * p.stage_bytes;
+                    const uint32_t b_addr = a_addr + p.a_bytes;
+                    for (int k = 0; k < kslices; ++k) {
+                        const uint64_t ad = ptx::smem_desc(a_addr + 32u * k, 16u, sbo, p.swz);
+                        const uint64_t bd = ptx::smem_desc(b_addr + 32u * k, 16u, sbo, p.swz);
+                        if (KIND == kTF32)
+                            ptx::mma_tf32(d_tmem, ad, bd, p.idesc, (i > 0 || k > 0) ? 1u : 0u);
+                        else
+                            ptx::mma_f16(d_tmem, ad, bd, p.idesc, (i > 0 || k > 0) ? 1u : 0u);
+                    }
+                    ptx::mma_commit(empty_bar(s));
                 }
-                ptx::mma_commit(empty_bar(s));
+                if (!ok) break;
+                ptx::mma_commit(accf_bar(acc));  // fires once this tile's MMAs have completed
             }
-            ptx::mma_commit(acc_bar);  // fires once every MMA above has completed
+            ptx::mma_commit(drain_bar);          // fires once every MMA issued here completed
         }
     } else {
-        // Epilogue warps 2..5.
+        // Epilogue warps 2..9: warp w reads TMEM lanes 32*(w%4) .. +31, and
+        // the two warps of a lane quadrant take alternate 32-column groups.
         const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int row = 32 * q + lane;
-        const int m = m0 + row;
-        const bool ok = ptx::mbar_wait_bounded(acc_bar, 0, kWaitLimitNs);
-        if (!ok) {
-            atomicOr(p.status, 1u);
-            *(volatile int *)abort_flag = 1;
-        }
-        ptx::tc_fence_after();
-        int img = 0, oh = 0, ow = 0;
-        if (m < p.M) {
-            img = m / p.OHW;
-            const int rem = m - img * p.OHW;
-            oh = rem / p.OW;
-            ow = rem - oh * p.OW;
-        }
-        const bool valid = ok && m < p.M && !*(volatile int *)abort_flag;
-        for (int c0 = 0; c0 < p.BN; c0 += 16) {
-            uint32_t v[16];
-            ptx::tmem_ld16(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
-            ptx::tmem_ld_wait();
-            if (!valid) continue;
-            float o[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) o[j] = silu_fast(__uint_as_float(v[j]) + bias_s[c0 + j]);
-            const int nbase = n0 + c0;
-            if (p.out_nhwc) {
-                if (KIND == kTF32) {
-                    float *yr = static_cast<float *>(p.y) + (size_t)m * p.C_out + nbase;
-                    if (nbase + 16 <= p.C_out && (p.C_out & 3) == 0) {
-#pragma unroll
-                        for (int j = 0; j < 16; j += 4)
-                            *reinterpret_cast<float4 *>(yr + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
-                    } else {
-                        for (int j = 0; j < 16 && nbase + j < p.C_out; ++j) yr[j] = o[j];
-                    }
-                } else {
-                    __nv_bfloat16 *yr = static_cast<__nv_bfloat16 *>(p.y) + (size_t)m * p.C_out + nbase;
-                    if (nbase + 16 <= p.C_out && (p.C_out & 7) == 0) {
-                        uint32_t w[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
-                            w[j] = *reinterpret_cast<uint32_t *>(&h2);
-                        }
-                        *reinterpret_cast<uint4 *>(yr) = make_uint4(w[0], w[1], w[2], w[3]);
-                        *reinterpret_cast<uint4 *>(yr + 8) = make_uint4(w[4], w[5], w[6], w[7]);
-                    } else {
-                        for (int j = 0; j < 16 && nbase + j < p.C_out; ++j) yr[j] = __float2bfloat16_rn(o[j]);
-                    }
-                }
-            } else {
-                // NCHW: lanes hold consecutive pixels, so each channel's
-                // store is contiguous across the warp.
-                const size_t plane = (size_t)p.OH * p.out_row_stride;
-                const size_t pix = (size_t)oh * p.out_row_stride + ow;
-                for (int j = 0; j < 16; ++j) {
-                    const int n = nbase + j;
-                    if (n >= p.C_out) break;
-                    const size_t off = ((size_t)img * p.C_out + n) * plane + pix;
-                    if (KIND == kTF32)
-                        static_cast<float *>(p.y)[off] = o[j];
-                    else
-                        static_cast<__nv_bfloat16 *>(p.y)[off] = __float2bfloat16_rn(o[j]);
+        int j = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++j) {
+            const int acc = j & 1, ua = j >> 1;
+            // Warp-uniform decision: tcgen05.ld below needs the whole warp.
+            bool ok = !aborted(abort_flag) && ptx::mbar_wait_bounded(accf_bar(acc), ua & 1, kWaitLimitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0 && !aborted(abort_flag)) abort_now(p, abort_flag);
+                break;
+            }
+            ptx::tc_fence_after();
+            int m0, n0;
+            tile_coords(t, p.n_tiles, m0, n0, p.BN);
+            const int m = m0 + row;
+            int img = 0, oh = 0, ow = 0;
+            if (m < p.M) {
+                img = m / p.OHW;
+                const int rem = m - img * p.OHW;
+                oh = rem / p.OW;
+                ow = rem - oh * p.OW;
+            }
+            const uint32_t t_row = tmem_base + (uint32_t)(acc * p.acc_stride) + ((uint32_t)(32 * q) << 16);
+            for (int c0 = 32 * half; c0 < p.BN; c0 += 64) {
+                // Two loads, one wait: 32 columns in flight per thread.
+                uint32_t v0[16], v1[16];
+                const bool two = c0 + 16 < p.BN;
+                ptx::tmem_ld16(t_row + (uint32_t)c0, v0);
+                if (two) ptx::tmem_ld16(t_row + (uint32_t)(c0 + 16), v1);
+                ptx::tmem_ld_wait();
+                if (m < p.M) {
+                    if (n0 + c0 < p.C_out) epi_store16<KIND>(p, m, img, oh, ow, n0 + c0, v0);
+                    if (two && n0 + c0 + 16 < p.C_out) epi_store16<KIND>(p, m, img, oh, ow, n0 + c0 + 16, v1);
                 }
             }
+            // This accumulator has been read: hand it back to the MMA issuer.
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(acce_bar(acc));
         }
     }
 
-    // ---- teardown: all tensor-memory reads done, all copies landed.
-    ptx::tc_fence_before();
+    // ---- teardown: all MMAs complete, loads landed, TMEM freed.
     __syncthreads();
-    if (warp == 0 && lane == 0 && *(volatile int *)abort_flag) {
-        // Drain loads still in flight after an abort (bounded).
-        for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
-            ptx::mbar_wait_bounded(full_bar(i % S), (i / S) & 1, kWaitLimitNs);
+    if (warp == 0 && lane == 0 && aborted(abort_flag)) {
+        for (int g = (issued > S ? issued - S : 0); g < issued; ++g)
+            ptx::mbar_wait_bounded(full_bar(g % S), (g / S) & 1, kWaitLimitNs);
     }
-    if (warp == 1 && *(volatile int *)abort_flag && lane == 0) {
-        ptx::mbar_wait_bounded(acc_bar, 0, kWaitLimitNs);
+    if (warp == 1 && lane == 0) {
+        if (!ptx::mbar_wait_bounded(drain_bar, 0, kWaitLimitNs)) atomicOr(p.status, 1u);
     }
+    ptx::tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         ptx::tc_fence_after();
@@ -269,38 +361,6 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // (swizzled, then fence.proxy.async) -> one thread issues the MMAs.  The same
 // four warps run the requantising epilogue after the last K step.
 
-// Our exp for the requantising epilogue, specified bit for bit:
-// Cody-Waite reduction with a 16-bit head of ln 2, degree-7 Taylor
-// polynomial in Horner form with fused multiply-adds, scaling by 2^k through
-// the exponent field; +inf above 88, +0 below -87.
-__device__ __forceinline__ float cw_exp(float x) {
-    if (x > 88.0f) return __int_as_float(0x7f800000);
-    if (x < -87.0f) return 0.0f;
-    const float kf = rintf(__fmul_rn(x, 0x1.715476p+0f));
-    float r = __fmaf_rn(-kf, 0x1.62e4p-1f, x);
-    r = __fmaf_rn(-kf, 0x1.7f7d1cp-20f, r);
-    float p = 0x1.a01a02p-13f;
-    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);
-    p = __fmaf_rn(p, r, 0x1.111112p-7f);
-    p = __fmaf_rn(p, r, 0x1.555556p-5f);
-    p = __fmaf_rn(p, r, 0x1.555556p-3f);
-    p = __fmaf_rn(p, r, 0.5f);
-    p = __fmaf_rn(p, r, 1.0f);
-    p = __fmaf_rn(p, r, 1.0f);
-    const int k = (int)kf;
-    return __fmul_rn(p, __int_as_float((k + 127) << 23));
-}
-
-// q = rne(clamp(SiLU(float(acc) * m_c) * inv_s_y, -128, 127)), IEEE steps.
-__device__ __forceinline__ int requant_i8(int acc, float m_c, float inv_s_y) {
-    const float t = __fmul_rn(__int2float_rn(acc), m_c);
-    const float e = cw_exp(-t);
-    const float u = __fdiv_rn(t, __fadd_rn(1.0f, e));
-    float v = __fmul_rn(u, inv_s_y);
-    v = fminf(fmaxf(v, -128.0f), 127.0f);
-    return (int)rintf(v);
-}
-
 // Address swizzle of the TMA/UMMA shared-memory layouts: 16-byte chunk bits
 // [4, 4+b) XOR row bits [7, 7+b), b = 1, 2, 3 for 32-, 64-, 128-byte spans.
 __device__ __forceinline__ uint32_t swz(uint32_t addr, uint32_t mask) {
@@ -315,7 +375,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t u_lo, uint32_t u_hi) {
     return (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+
+// Persistent INT8 kernel.  Warp 0: TMA producer; warp 1: TMEM + MMA issuer;
+// warps 2-9: epilogue; warps 10-13: int8 -> bf16 converters.
+__global__ void __launch_bounds__(kThreadsI8, 1)
 tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -323,24 +386,24 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     uint8_t *base_ptr = smem_raw + (base - raw_addr);
     const int S = p.stages;
     // Stage s: [operand A bf16 | operand B bf16 | staging A int8], each 1024-aligned.
-    const uint32_t bars = base + S * p.stage_bytes;   // raw_full[S], conv_done[S], free[S], acc_full
+    // Barriers: raw_full[S], conv_done[S], free[S], acc_full[2], acc_empty[2], drain.
+    const uint32_t bars = base + S * p.stage_bytes;
     uint64_t *bar_ptr = reinterpret_cast<uint64_t *>(base_ptr + S * p.stage_bytes);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_ptr + 3 * S + 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_ptr + 3 * S + 5);
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
-    int *bias_s = reinterpret_cast<int *>(tmem_slot + 4);
-    float *mc_s = reinterpret_cast<float *>(bias_s + p.BN);
 
     auto raw_bar = [&](int s) { return bars + 8u * s; };
     auto conv_bar = [&](int s) { return bars + 8u * (S + s); };
     auto free_bar = [&](int s) { return bars + 8u * (2 * S + s); };
-    const uint32_t acc_bar = bars + 8u * (3 * S);
+    auto accf_bar = [&](int a) { return bars + 8u * (3 * S + a); };
+    auto acce_bar = [&](int a) { return bars + 8u * (3 * S + 2 + a); };
+    const uint32_t drain_bar = bars + 8u * (3 * S + 4);
     const int op_b_off = p.a_bytes;
     const int stg_off = (p.a_bytes + p.b_bytes + 1023) & ~1023;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * kBM;
-    const int n0 = blockIdx.y * p.BN;
     const int nk = p.ksteps;
+    const int num_tiles = p.m_tiles * p.n_tiles;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -348,7 +411,11 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             ptx::mbar_init(conv_bar(s), 4);   // one arrive per converter warp
             ptx::mbar_init(free_bar(s), 1);
         }
-        ptx::mbar_init(acc_bar, 1);
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(accf_bar(a), 1);
+            ptx::mbar_init(acce_bar(a), kEpiWarps);   // one arrive per epilogue warp
+        }
+        ptx::mbar_init(drain_bar, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmA);
@@ -358,11 +425,6 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), p.tmem_cols);
         ptx::tmem_relinquish();
     }
-    for (int i = threadIdx.x; i < p.BN; i += blockDim.x) {
-        const int n = n0 + i;
-        bias_s[i] = n < p.C_out ? p.bias_i32[n] : 0;
-        mc_s[i] = n < p.C_out ? p.m_c[n] : 0.0f;
-    }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -371,166 +433,199 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     int issued = 0;
     if (warp == 0) {
         if (lane == 0) {
-            const int img = m0 / p.OHW;
-            const int rem = m0 - img * p.OHW;
-            const int oh = rem / p.OW, ow = rem - (rem / p.OW) * p.OW;
-            const int wc = ow * p.stride - p.pad, hc = oh * p.stride - p.pad;
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % S, u = i / S;
-                if (!ptx::mbar_wait_bounded(free_bar(s), (u & 1) ^ 1, kWaitLimitNs)) {
-                    atomicOr(p.status, 1u);
-                    *(volatile int *)abort_flag = 1;
-                    break;
+            int g = 0;
+            for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
+                int m0, n0;
+                tile_coords(t, p.n_tiles, m0, n0, p.BN);
+                const int img = m0 / p.OHW;
+                const int rem = m0 - img * p.OHW;
+                const int oh = rem / p.OW, ow = rem - (rem / p.OW) * p.OW;
+                const int wc = ow * p.stride - p.pad, hc = oh * p.stride - p.pad;
+                for (int i = 0; i < nk; ++i, ++g) {
+                    const int s = g % S, u = g / S;
+                    if (!ptx::mbar_wait_bounded(free_bar(s), (u & 1) ^ 1, kWaitLimitNs)) {
+                        abort_now(p, abort_flag);
+                        break;
+                    }
+                    if (aborted(abort_flag)) break;
+                    const int tap = i / p.cblocks, cb = i - tap * p.cblocks;
+                    const int r = tap / p.ks, tt = tap - r * p.ks;
+                    const uint32_t st = base + s * p.stage_bytes;
+                    ptx::mbar_arrive_expect_tx(raw_bar(s), (uint32_t)(p.stg_bytes + p.b_bytes));
+                    if (p.im2col)
+                        ptx::tma_load_im2col_4d(st + stg_off, &tmA, raw_bar(s), cb * p.CB, wc, hc, img, (uint16_t)tt,
+                                                (uint16_t)r);
+                    else
+                        ptx::tma_load_2d(st + stg_off, &tmA, raw_bar(s), cb * p.CB, m0);
+                    ptx::tma_load_2d(st + op_b_off, &tmB, raw_bar(s), tap * p.c_in_pad + cb * p.CB, n0);
+                    issued = g + 1;
                 }
-                if (*(volatile int *)abort_flag) break;
-                const int tap = i / p.cblocks, cb = i - tap * p.cblocks;
-                const int r = tap / p.ks, t = tap - r * p.ks;
-                const uint32_t st = base + s * p.stage_bytes;
-                ptx::mbar_arrive_expect_tx(raw_bar(s), (uint32_t)(p.stg_bytes + p.b_bytes));
-                if (p.im2col)
-                    ptx::tma_load_im2col_4d(st + stg_off, &tmA, raw_bar(s), cb * p.CB, wc, hc, img, (uint16_t)t,
-                                            (uint16_t)r);
-                else
-                    ptx::tma_load_2d(st + stg_off, &tmA, raw_bar(s), cb * p.CB, m0);
-                ptx::tma_load_2d(st + op_b_off, &tmB, raw_bar(s), tap * p.c_in_pad + cb * p.CB, n0);
-                issued = i + 1;
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t sbo = 8u * p.RB;
             const int kslices = p.RB / 32;
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % S, u = i / S;
-                if (!ptx::mbar_wait_bounded(conv_bar(s), u & 1, kWaitLimitNs) ||
-                    !ptx::mbar_wait_bounded(raw_bar(s), u & 1, kWaitLimitNs)) {
-                    atomicOr(p.status, 1u);
-                    *(volatile int *)abort_flag = 1;
+            int g = 0, j = 0;
+            for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x, ++j) {
+                const int acc = j & 1, ua = j >> 1;
+                if (!ptx::mbar_wait_bounded(acce_bar(acc), (ua & 1) ^ 1, kWaitLimitNs)) {
+                    abort_now(p, abort_flag);
                     break;
                 }
                 ptx::tc_fence_after();
-                const int chunk = i / p.kpc;
-                const bool first_of_chunk = (i % p.kpc) == 0;
-                const uint32_t d_tmem = tmem_base + (uint32_t)(chunk * p.BN);
-                const uint32_t a_addr = base + s * p.stage_bytes;
-                const uint32_t b_addr = a_addr + op_b_off;
-                for (int j = 0; j < kslices; ++j) {
-                    const uint64_t ad = ptx::smem_desc(a_addr + 32u * j, 16u, sbo, p.swz);
-                    const uint64_t bd = ptx::smem_desc(b_addr + 32u * j, 16u, sbo, p.swz);
-                    ptx::mma_f16(d_tmem, ad, bd, p.idesc, (first_of_chunk && j == 0) ? 0u : 1u);
+                bool ok = true;
+                for (int i = 0; i < nk; ++i, ++g) {
+                    const int s = g % S, u = g / S;
+                    if (!ptx::mbar_wait_bounded(conv_bar(s), u & 1, kWaitLimitNs) ||
+                        !ptx::mbar_wait_bounded(raw_bar(s), u & 1, kWaitLimitNs)) {
+                        abort_now(p, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const int chunk = i / p.kpc;
+                    const bool first_of_chunk = (i % p.kpc) == 0;
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_stride + chunk * p.chunk_stride);
+                    const uint32_t a_addr = base + s * p.stage_bytes;
+                    const uint32_t b_addr = a_addr + op_b_off;
+                    for (int k = 0; k < kslices; ++k) {
+                        const uint64_t ad = ptx::smem_desc(a_addr + 32u * k, 16u, sbo, p.swz);
+                        const uint64_t bd = ptx::smem_desc(b_addr + 32u * k, 16u, sbo, p.swz);
+                        ptx::mma_f16(d_tmem, ad, bd, p.idesc, (first_of_chunk && k == 0) ? 0u : 1u);
+                    }
+                    ptx::mma_commit(free_bar(s));
                 }
-                ptx::mma_commit(free_bar(s));
+                if (!ok) break;
+                ptx::mma_commit(accf_bar(acc));
             }
-            ptx::mma_commit(acc_bar);
+            ptx::mma_commit(drain_bar);
+        }
+    } else if (warp >= 10) {
+        // Converters: thread (warp - 10) * 32 + lane widens row `row` of every
+        // staging tile into the swizzled bf16 operand.
+        const int row = (warp - 10) * 32 + lane;
+        const int in_bytes = p.CB;
+        int g = 0;
+        for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
+            bool ok = true;
+            for (int i = 0; i < nk; ++i, ++g) {
+                const int s = g % S, u = g / S;
+                if (!ptx::mbar_wait_bounded(raw_bar(s), u & 1, kWaitLimitNs)) {
+                    abort_now(p, abort_flag);
+                    ok = false;
+                    break;
+                }
+                const uint32_t st = base + s * p.stage_bytes;
+                const uint32_t src_row = st + stg_off + row * in_bytes;
+                const uint32_t dst_row = st + row * p.RB;
+                for (int c = 0; c < in_bytes; c += 16) {
+                    uint32_t w0, w1, w2, w3;
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                                 : "r"(swz(src_row + c, p.stg_mask)));
+                    uint32_t o[8];
+                    const uint32_t ws[4] = {w0 ^ 0x80808080u, w1 ^ 0x80808080u, w2 ^ 0x80808080u, w3 ^ 0x80808080u};
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        o[2 * qq] = pack_bf16x2(ws[qq] & 0xFF, (ws[qq] >> 8) & 0xFF);
+                        o[2 * qq + 1] = pack_bf16x2((ws[qq] >> 16) & 0xFF, ws[qq] >> 24);
+                    }
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(swz(dst_row + 2 * c, p.op_mask)),
+                                 "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(swz(dst_row + 2 * c + 16, p.op_mask)),
+                                 "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                                 : "memory");
+                }
+                // Make the generic-proxy writes visible to the tensor cores.
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(conv_bar(s));
+            }
+            if (!ok) break;
         }
     } else {
-        // Warps 2..5: widen int8 staging rows to bf16 operand rows, then the
-        // requantising epilogue.  Thread (warp - 2) * 32 + lane owns row
-        // `row` of every staging tile.
-        const int row = (warp - 2) * 32 + lane;
-        const int in_bytes = p.CB;            // int8 bytes per row
-        bool ok = true;
-        for (int i = 0; i < nk && ok; ++i) {
-            const int s = i % S, u = i / S;
-            if (!ptx::mbar_wait_bounded(raw_bar(s), u & 1, kWaitLimitNs)) {
-                atomicOr(p.status, 1u);
-                *(volatile int *)abort_flag = 1;
-                ok = false;
+        // Epilogue warps 2..9: quadrant warp % 4, alternate 16-column groups.
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int erow = 32 * q + lane;
+        int j = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++j) {
+            const int acc = j & 1, ua = j >> 1;
+            bool ok = !aborted(abort_flag) && ptx::mbar_wait_bounded(accf_bar(acc), ua & 1, kWaitLimitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0 && !aborted(abort_flag)) abort_now(p, abort_flag);
                 break;
             }
-            const uint32_t st = base + s * p.stage_bytes;
-            const uint32_t src_row = st + stg_off + row * in_bytes;
-            const uint32_t dst_row = st + row * p.RB;
-            for (int c = 0; c < in_bytes; c += 16) {
-                uint32_t w0, w1, w2, w3;
-                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                             : "r"(swz(src_row + c, p.stg_mask)));
-                uint32_t o[8];
-                const uint32_t ws[4] = {w0 ^ 0x80808080u, w1 ^ 0x80808080u, w2 ^ 0x80808080u, w3 ^ 0x80808080u};
+            ptx::tc_fence_after();
+            int m0, n0;
+            tile_coords(t, p.n_tiles, m0, n0, p.BN);
+            const int m = m0 + erow;
+            int img = 0, oh = 0, ow = 0;
+            if (m < p.M) {
+                img = m / p.OHW;
+                const int rem = m - img * p.OHW;
+                oh = rem / p.OW;
+                ow = rem - oh * p.OW;
+            }
+            const uint32_t t_row = tmem_base + (uint32_t)(acc * p.acc_stride) + ((uint32_t)(32 * q) << 16);
+            for (int c0 = 16 * half; c0 < p.BN; c0 += 32) {
+                const int nbase = n0 + c0;
+                int accv[16];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    o[2 * q] = pack_bf16x2(ws[q] & 0xFF, (ws[q] >> 8) & 0xFF);
-                    o[2 * q + 1] = pack_bf16x2((ws[q] >> 16) & 0xFF, ws[q] >> 24);
+                for (int jj = 0; jj < 16; ++jj) accv[jj] = nbase + jj < p.C_out ? __ldg(p.bias_i32 + nbase + jj) : 0;
+                for (int ch = 0; ch < p.nchunks; ++ch) {
+                    uint32_t v[16];
+                    ptx::tmem_ld16(t_row + (uint32_t)(ch * p.chunk_stride + c0), v);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) accv[jj] += __float2int_rn(__uint_as_float(v[jj]));
                 }
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(swz(dst_row + 2 * c, p.op_mask)),
-                             "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
-                             : "memory");
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(swz(dst_row + 2 * c + 16, p.op_mask)),
-                             "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
-                             : "memory");
-            }
-            // Make the generic-proxy writes visible to the tensor cores.
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(conv_bar(s));
-        }
-        const int q = warp & 3;
-        const int erow = 32 * q + lane;       // TMEM lane this thread reads
-        const int m = m0 + erow;
-        ok = ok && ptx::mbar_wait_bounded(acc_bar, 0, kWaitLimitNs);
-        if (!ok) {
-            atomicOr(p.status, 1u);
-            *(volatile int *)abort_flag = 1;
-        }
-        ptx::tc_fence_after();
-        int img = 0, oh = 0, ow = 0;
-        if (m < p.M) {
-            img = m / p.OHW;
-            const int rem = m - img * p.OHW;
-            oh = rem / p.OW;
-            ow = rem - oh * p.OW;
-        }
-        const bool valid = ok && m < p.M && !*(volatile int *)abort_flag;
-        for (int c0 = 0; c0 < p.BN; c0 += 16) {
-            int acc[16];
+                if (m >= p.M || nbase >= p.C_out) continue;
+                uint32_t qw[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = bias_s[c0 + j];
-            for (int ch = 0; ch < p.nchunks; ++ch) {
-                uint32_t v[16];
-                ptx::tmem_ld16(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(ch * p.BN + c0), v);
-                ptx::tmem_ld_wait();
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int qv = requant_i8(accv[jj], nbase + jj < p.C_out ? __ldg(p.m_c + nbase + jj) : 0.0f,
+                                              p.inv_s_y);
+                    qw[jj >> 2] |= (uint32_t)(uint8_t)(int8_t)qv << (8 * (jj & 3));
+                }
+                if (p.out_nhwc) {
+                    int8_t *yr = static_cast<int8_t *>(p.y) + (size_t)m * p.C_out + nbase;
+                    if (nbase + 16 <= p.C_out && (p.C_out & 15) == 0) {
+                        *reinterpret_cast<uint4 *>(yr) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+                    } else {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc[j] += __float2int_rn(__uint_as_float(v[j]));
-            }
-            if (!valid) continue;
-            int8_t qv[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) qv[j] = (int8_t)requant_i8(acc[j], mc_s[c0 + j], p.inv_s_y);
-            const int nbase = n0 + c0;
-            if (p.out_nhwc) {
-                int8_t *yr = static_cast<int8_t *>(p.y) + (size_t)m * p.C_out + nbase;
-                if (nbase + 16 <= p.C_out && (p.C_out & 15) == 0) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        w[j] = (uint32_t)(uint8_t)qv[4 * j] | ((uint32_t)(uint8_t)qv[4 * j + 1] << 8) |
-                               ((uint32_t)(uint8_t)qv[4 * j + 2] << 16) | ((uint32_t)(uint8_t)qv[4 * j + 3] << 24);
-                    *reinterpret_cast<uint4 *>(yr) = make_uint4(w[0], w[1], w[2], w[3]);
+                        for (int jj = 0; jj < 16; ++jj)
+                            if (nbase + jj < p.C_out) yr[jj] = (int8_t)(qw[jj >> 2] >> (8 * (jj & 3)));
+                    }
                 } else {
-                    for (int j = 0; j < 16 && nbase + j < p.C_out; ++j) yr[j] = qv[j];
-                }
-            } else {
-                const size_t plane = (size_t)p.OH * p.out_row_stride;
-                const size_t pix = (size_t)oh * p.out_row_stride + ow;
-                for (int j = 0; j < 16; ++j) {
-                    const int n = nbase + j;
-                    if (n >= p.C_out) break;
-                    static_cast<int8_t *>(p.y)[((size_t)img * p.C_out + n) * plane + pix] = qv[j];
+                    const size_t plane = (size_t)p.OH * p.out_row_stride;
+                    const size_t pix = (size_t)oh * p.out_row_stride + ow;
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        if (nbase + jj >= p.C_out) continue;
+                        static_cast<int8_t *>(p.y)[((size_t)img * p.C_out + nbase + jj) * plane + pix] =
+                            (int8_t)(qw[jj >> 2] >> (8 * (jj & 3)));
+                    }
                 }
             }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(acce_bar(acc));
         }
     }
 
-    ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 0 && lane == 0 && *(volatile int *)abort_flag) {
-        for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
-            ptx::mbar_wait_bounded(raw_bar(i % S), (i / S) & 1, kWaitLimitNs);
+    if (warp == 0 && lane == 0 && aborted(abort_flag)) {
+        for (int g = (issued > S ? issued - S : 0); g < issued; ++g)
+            ptx::mbar_wait_bounded(raw_bar(g % S), (g / S) & 1, kWaitLimitNs);
     }
-    if (warp == 1 && *(volatile int *)abort_flag && lane == 0) {
-        ptx::mbar_wait_bounded(acc_bar, 0, kWaitLimitNs);
+    if (warp == 1 && lane == 0) {
+        if (!ptx::mbar_wait_bounded(drain_bar, 0, kWaitLimitNs)) atomicOr(p.status, 1u);
     }
+    ptx::tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         ptx::tc_fence_after();
@@ -595,9 +690,25 @@ int elem_bytes_of(int variant) { return variant == CBS_VARIANT_TC_TF32 ? 4 : 2; 
 // Channels per K step for the INT8 variant (int8 bytes per staging row).
 int i8_channel_block(int c_in_pad) { return c_in_pad % 64 == 0 ? 64 : (c_in_pad % 32 == 0 ? 32 : 16); }
 
+// Estimated cycles of one layer on the persistent kernel for a given N tile:
+// tiles are spread over the SMs in waves; a tile costs the larger of its MMA
+// time and its shared-memory fill (A and B re-read from L2 for every tile),
+// and the epilogue overlaps the next tile's main loop.
+double tc_cycles(long long m_tiles, int c_out, int BN, int K, int eb_x, int eb_w, bool tf32) {
+    const long long tiles = m_tiles * ((c_out + BN - 1) / BN);
+    const long long waves = (tiles + kNumSMs - 1) / kNumSMs;
+    const double macs_per_clk = tf32 ? 2048.0 : 4096.0;       // per SM, dense
+    const double l2_bytes_per_clk = 64.0;                      // per SM, all SMs loading
+    const double mma = (double)kBM * BN * K / macs_per_clk;
+    const double load = ((double)kBM * K * eb_x + (double)BN * K * eb_w) / l2_bytes_per_clk;
+    const double per_tile = (mma > load ? mma : load) + 150.0;
+    return (double)waves * per_tile + 2500.0;  // + pipeline fill and the last epilogue
+}
+
 cbs_status plan_tc(cbs_plan_t &p) {
     const cbs_layer_desc &d = p.desc;
     const bool i8 = p.variant == CBS_VARIANT_TC_INT8;
+    const bool tf32 = p.variant == CBS_VARIANT_TC_TF32;
     const int eb = i8 ? 1 : elem_bytes_of(p.variant);
     int RB, CB, nchunks = 1;
     if (i8) {
@@ -617,23 +728,34 @@ cbs_status plan_tc(cbs_plan_t &p) {
     }
     p.k_gemm = d.k * d.k * p.c_in_pad;
     p.x_bytes = (size_t)d.n * d.h * d.w * p.c_in_pad * eb;
-    p.w_packed_bytes = (size_t)d.c_out * p.k_gemm * (p.variant == CBS_VARIANT_TC_TF32 ? 4 : 2);
+    p.w_packed_bytes = (size_t)d.c_out * p.k_gemm * (tf32 ? 4 : 2);
     if (d.pad > 127 || (p.oh - 1) * d.stride - d.pad - d.h + 1 < -128 || (p.ow - 1) * d.stride - d.pad - d.w + 1 < -128)
         return fail(CBS_ERR_UNSUPPORTED, "padding outside the im2col corner range");
     const long long M = (long long)d.n * p.oh * p.ow;
     p.m_tiles = ceil_div(M, kBM);
+    // TMEM holds two accumulator buffers of nchunks * next_pow2(BN) columns
+    // (rounded to a power of two): nchunks * next_pow2(BN) <= 256.
+    int max_bn = 256;
+    while (max_bn >= 16 && nchunks * max_bn > 256) max_bn /= 2;
     int BN;
     if (d.force_block_n > 0) {
         BN = d.force_block_n;
         if (BN % 16 || BN < 16 || BN > 256) return fail(CBS_ERR_INVALID_ARG, "block_n %d: 16..256, multiple of 16", BN);
+        if (BN > max_bn)
+            return fail(CBS_ERR_UNSUPPORTED, "block_n %d with %d exact-sum chunks exceeds TMEM", BN, nchunks);
     } else {
-        BN = d.c_out <= 256 ? round_up(d.c_out, 16) : 256;
-        // Prefer more CTAs when the tile grid cannot fill the SMs.
-        while (BN > 32 && (BN % 32) == 0 && (long long)p.m_tiles * ceil_div(d.c_out, BN) < kNumSMs) BN /= 2;
-        while (nchunks * BN > 512) BN = round_up(BN / 2, 16);
+        const int full = round_up(d.c_out, 16) < max_bn ? round_up(d.c_out, 16) : max_bn;
+        if (full < 16) return fail(CBS_ERR_UNSUPPORTED, "INT8: %d exact-sum chunks exceed TMEM", nchunks);
+        const int cands[] = {full, 256, 192, 128, 96, 64, 48, 32, 16};
+        const int K = p.k_gemm;
+        double best = 1e300;
+        BN = full;
+        for (int c : cands) {
+            if (c > full || c < 16) continue;
+            const double cyc = tc_cycles(p.m_tiles, d.c_out, c, K, eb, tf32 ? 4 : 2, tf32);
+            if (cyc < best * 0.98) { best = cyc; BN = c; }
+        }
     }
-    if (nchunks * BN > 512)
-        return fail(CBS_ERR_UNSUPPORTED, "INT8: %d exact-sum chunks x block_n %d exceed 512 TMEM columns", nchunks, BN);
     if (d.force_split_k > 1) return fail(CBS_ERR_UNSUPPORTED, "split-K not built for the tensor-core path yet");
     p.block_m = kBM;
     p.block_n = BN;
@@ -642,13 +764,16 @@ cbs_status plan_tc(cbs_plan_t &p) {
     p.split_k = 1;
     int stage = round_up(kBM * RB + BN * RB, 1024);  // stages stay 1024-byte aligned
     if (i8) stage += round_up(kBM * CB, 1024);       // int8 staging tile
+    // As many stages as the budget holds (small-channel layers move little
+    // per K step and need many loads in flight to cover L2 latency).
     int stages = kSmemBudget / stage;
-    if (stages > 8) stages = 8;
+    if (stages > 32) stages = 32;
     if (stages < 2) stages = 2;
     p.stages = stages;
-    p.threads = kThreads;
-    p.smem_bytes = 1024 + stages * stage + 8 * ((i8 ? 3 : 2) * stages + 1) + 16 + BN * (i8 ? 8 : 4);
-    p.grid_ctas = p.m_tiles * p.n_tiles;
+    p.threads = i8 ? kThreadsI8 : kThreads;
+    p.smem_bytes = 1024 + stages * stage + 8 * ((i8 ? 3 : 2) * stages + 5) + 16;
+    const long long tiles = (long long)p.m_tiles * p.n_tiles;
+    p.grid_ctas = (int)(tiles < kNumSMs ? tiles : kNumSMs);
     p.workspace_bytes = 0;
     return CBS_OK;
 }
@@ -682,6 +807,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     P.cblocks = pl.c_in_pad / CB;
     P.ksteps = d.k * d.k * P.cblocks;
     P.BN = BN; P.stages = pl.stages;
+    P.m_tiles = pl.m_tiles; P.n_tiles = pl.n_tiles;
     P.a_bytes = kBM * RB; P.b_bytes = BN * RB;
     P.stage_bytes = round_up(P.a_bytes + P.b_bytes, 1024);
     if (i8) {
@@ -704,11 +830,16 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     const uint32_t fmt = pl.variant == CBS_VARIANT_TC_TF32 ? 2u : 1u;  // TF32 : BF16 operands
     P.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
     P.swz = desc_swizzle_code(RB);
-    const int cols = next_pow2(P.nchunks * BN);
-    P.tmem_cols = (uint32_t)(cols < 32 ? 32 : cols);
+    // Two accumulator buffers (double buffering across tiles); INT8 chunks
+    // sit at power-of-two column offsets inside a buffer.
+    P.chunk_stride = next_pow2(BN);
+    P.acc_stride = next_pow2(P.nchunks * P.chunk_stride) < 16 ? 16 : next_pow2(P.nchunks * P.chunk_stride);
+    P.tmem_cols = (uint32_t)(2 * P.acc_stride < 32 ? 32 : 2 * P.acc_stride);
+    if (P.tmem_cols > 512) return fail(CBS_ERR_UNSUPPORTED, "accumulators need %u TMEM columns", P.tmem_cols);
     P.y = y;
     P.status = device_status_word();
     if (!P.status) return fail(CBS_ERR_CUDA, "cannot resolve the device status word");
+    if (pl.grid_ctas <= 0) return CBS_OK;
 
     alignas(64) CUtensorMap tmA, tmB;
     CUresult r;
@@ -744,7 +875,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
         if (r != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuTensorMapEncodeTiled (B) failed (%d)", (int)r);
     }
 
-    dim3 grid(pl.m_tiles, pl.n_tiles, 1);
+    dim3 grid(pl.grid_ctas, 1, 1);  // persistent: each CTA walks tiles blockIdx.x + i * gridDim.x
     cudaError_t e;
     if (pl.variant == CBS_VARIANT_TC_TF32) {
         e = cudaFuncSetAttribute(tc_conv_kernel<kTF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
@@ -754,7 +885,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
         if (e == cudaSuccess) tc_conv_kernel<kBF16><<<grid, kThreads, pl.smem_bytes, s>>>(tmA, tmB, P);
     } else {
         e = cudaFuncSetAttribute(tc_conv_i8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
-        if (e == cudaSuccess) tc_conv_i8_kernel<<<grid, kThreads, pl.smem_bytes, s>>>(tmA, tmB, P);
+        if (e == cudaSuccess) tc_conv_i8_kernel<<<grid, kThreadsI8, pl.smem_bytes, s>>>(tmA, tmB, P);
     }
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute");
     return cuda_check(cudaGetLastError(), "tensor-core kernel launch");

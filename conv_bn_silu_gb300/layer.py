@@ -75,7 +75,7 @@ class FusedConvBnSilu:
 
     def x_shape(self):
         d, p = self.desc, self.plan
-        if p.variant == B.CBS_VARIANT_SIMT_FP32 and d.in_layout == B.CBS_NCHW:
+        if d.in_layout == B.CBS_NCHW:
             return (d.n, d.c_in, d.h, d.w)
         return (d.n, d.h, d.w, p.c_in_pad)
 

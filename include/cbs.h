@@ -71,7 +71,8 @@ typedef enum cbs_variant {
     CBS_VARIANT_SIMT_FP32 = 0,  /* CUDA-core implicit GEMM, FP32 FMA */
     CBS_VARIANT_TC_TF32 = 1,    /* tcgen05 kind::tf32, TMA im2col/tile loads, TMEM accumulator */
     CBS_VARIANT_TC_BF16 = 2,    /* tcgen05 kind::f16 (bf16 operands) */
-    CBS_VARIANT_TC_INT8 = 3     /* int8 values on tcgen05 kind::f16, exact integer sums */
+    CBS_VARIANT_TC_INT8 = 3,    /* int8 values on tcgen05 kind::f16, exact integer sums */
+    CBS_VARIANT_STEM = 4        /* direct CUDA-core convolution for C_in <= 4 (any precision) */
 } cbs_variant;
 
 /* One layer.  Padding is symmetric; OH = (H + 2*pad - k)/stride + 1. */
@@ -122,6 +123,8 @@ typedef struct cbs_plan_t {
  * Input format the plan expects (see x_bytes):
  *   SIMT FP32: x in d->in_layout, float, exactly C_in channels.
  *   TF32/BF16/INT8: x NHWC with c_in_pad channels (extra channels zero).
+ *   STEM (chosen for C_in <= 4, C_out <= 64, k <= 7): x in d->in_layout;
+ *   NHWC pixels hold c_in_pad = 4 channels for TF32/BF16/INT8, C_in for FP32.
  * Errors: CBS_ERR_INVALID_ARG (shape, enum), CBS_ERR_UNSUPPORTED.
  */
 CBS_API cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out);
@@ -133,7 +136,7 @@ CBS_API cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out);
  * from [C_out][C_in][k][k] to the variant's K-major packed form with k-order
  * (r, s, ci), and casts or quantises them:
  *   SIMT FP32: float  [k*k*C_in][C_out]
- *   TF32:      float  [C_out][k*k*c_in_pad]   (padding channels zero)
+ *   TF32, STEM with FP32/TF32: float [C_out][k*k*c_in_pad] (padding channels zero)
  *   BF16:      bf16   [C_out][k*k*c_in_pad]   (round to nearest even)
  *   INT8:      int8 codes held exactly as bf16 [C_out][k*k*c_in_pad];
  *              s_w[c] = max|w'[c,:]| / 127, q = rne(w'/s_w), m_c[c] = s_x * s_w[c],

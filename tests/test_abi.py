@@ -45,7 +45,8 @@ def test_status_strings(cuda_lib):
 def test_plan_fp32_layer_list(cuda_lib, i):
     s = wl.LAYER_LIST[i]
     p = B.cbs_plan(make_desc(1, s.c_in, s.h, s.width, s.c_out, s.k, s.stride))
-    assert p.variant == B.CBS_VARIANT_SIMT_FP32
+    # three-channel stems take the direct CUDA-core kernel, the rest the implicit GEMM
+    assert p.variant == (B.CBS_VARIANT_STEM if s.c_in <= 4 else B.CBS_VARIANT_SIMT_FP32)
     assert (p.oh, p.ow) == (s.oh, s.ow)
     assert p.out_row_stride == s.ow
     assert p.x_bytes == s.c_in * s.h * s.width * 4
@@ -55,6 +56,18 @@ def test_plan_fp32_layer_list(cuda_lib, i):
     assert p.n_tiles * p.block_n >= s.c_out
     assert p.split_k >= 1 and p.grid_ctas == p.m_tiles * p.n_tiles * p.split_k
     assert (p.workspace_bytes > 0) == (p.split_k > 1)
+
+
+def test_plan_stem_rules(cuda_lib):
+    for prec, c_pad in ((B.CBS_FP32, 3), (B.CBS_TF32, 4), (B.CBS_BF16, 4), (B.CBS_INT8, 4)):
+        p = B.cbs_plan(make_desc(2, 3, 64, 64, 16, 3, 2, prec=prec, in_layout=B.CBS_NHWC))
+        assert p.variant == B.CBS_VARIANT_STEM and p.c_in_pad == c_pad
+    # forcing the implicit GEMM for a small-channel FP32 layer stays possible
+    p = B.cbs_plan(make_desc(1, 3, 64, 64, 16, 3, 2, force_variant=B.CBS_VARIANT_SIMT_FP32))
+    assert p.variant == B.CBS_VARIANT_SIMT_FP32
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_plan(make_desc(1, 8, 64, 64, 16, 3, 2, force_variant=B.CBS_VARIANT_STEM))
+    assert e.value.status == B.CBS_ERR_UNSUPPORTED
 
 
 def test_plan_padded_row_stride(cuda_lib):

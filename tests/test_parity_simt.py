@@ -98,6 +98,20 @@ def test_ragged_and_degenerate(cuda_lib, shape):
     assert rel_l2(y, ref_of(spec, x, p)) <= TOL_FP32_REL_L2
 
 
+@pytest.mark.parametrize("variant", [B.CBS_VARIANT_SIMT_FP32, B.CBS_VARIANT_STEM])
+@pytest.mark.parametrize("layouts", [(B.CBS_NCHW, B.CBS_NCHW), (B.CBS_NHWC, B.CBS_NHWC), (B.CBS_NCHW, B.CBS_NHWC)])
+def test_small_channel_layers_both_kernels(cuda_lib, variant, layouts):
+    """The stem shape through the implicit GEMM and through the direct
+    kernel, with ragged sizes and both layouts."""
+    for shape in ((2, 3, 16, 3, 2, 37), (1, 4, 24, 3, 1, 19), (3, 1, 5, 1, 1, 9), (1, 2, 64, 5, 2, 23)):
+        n, c_in, c_out, k, stride, h = shape
+        spec = wl.LayerSpec(c_in, c_out, k, stride, h)
+        x, p = wl.layer_inputs(spec, n, layer_index=12)
+        y, layer = run_simt(spec, x, p, in_layout=layouts[0], out_layout=layouts[1], force_variant=variant)
+        assert layer.plan.variant == variant
+        assert rel_l2(y, ref_of(spec, x, p)) <= TOL_FP32_REL_L2, (shape, variant)
+
+
 def test_empty_batch_is_a_noop(cuda_lib):
     spec = wl.LayerSpec(8, 8, 3, 1, 6)
     _, p = wl.layer_inputs(spec, 1)
