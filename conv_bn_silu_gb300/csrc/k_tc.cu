@@ -33,9 +33,20 @@ namespace cbs {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kThreads = 320;     // TF32/BF16: producer, MMA, 8 epilogue warps (2..9)
-constexpr int kThreadsI8 = 448;   // INT8: + four converter warps (10..13)
-constexpr int kEpiWarps = 8;      // two per TMEM lane quadrant, splitting the columns
+// Warp roles.  One warp issuing TMA tensor copies gets about one copy
+// through every ~0.3 us whatever the box size (measured on GB300: 8.4 TB/s
+// from L2 for 16 KB boxes with one issuing warp per SM, 13 TB/s with two),
+// so several producer warps take interleaved K steps.
+constexpr int kMaxProducers = 4;                 // warps 0..3
+constexpr int kMmaWarp = kMaxProducers;          // warp 4: TMEM + MMA issuer
+constexpr int kEpiFirst = kMmaWarp + 1;          // warps 5..12: epilogue
+constexpr int kEpiWarps = 8;                     // two per TMEM lane quadrant, splitting the columns
+constexpr int kThreads = 32 * (kEpiFirst + kEpiWarps);        // TF32/BF16: 416
+constexpr int kMaxProducersI8 = 2;               // INT8: warps 0..1
+constexpr int kMmaWarpI8 = kMaxProducersI8;      // warp 2
+constexpr int kEpiFirstI8 = kMmaWarpI8 + 1;      // warps 3..10
+constexpr int kConvFirstI8 = kEpiFirstI8 + kEpiWarps;  // warps 11..14: int8 -> bf16 converters
+constexpr int kThreadsI8 = 32 * (kConvFirstI8 + 4);    // 480
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kSmemBudget = 200 * 1024;
 
@@ -58,6 +69,7 @@ struct TcParams {
     const int32_t *bias_i32;
     const float *m_c;
     float inv_s_y;
+    int nprod;                 // producer warps in use (divides stages)
     int nchunks, kpc;          // exact-sum K chunks and K steps per chunk
     int chunk_stride;          // TMEM columns between chunk accumulators (power of two)
     int stg_bytes;             // int8 staging tile of one stage (128 x CB bytes)
@@ -201,7 +213,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmB);
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), p.tmem_cols);
         ptx::tmem_relinquish();
     }
@@ -210,9 +222,12 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    int issued = 0;  // producer: K steps whose loads were issued (global count)
-    if (warp == 0) {
-        if (lane == 0) {
+    int last_g = -1;  // producer: last K step (global count) whose loads this warp issued
+    if (warp < kMaxProducers) {
+        // Producer warp `warp` takes the K steps g with g % nprod == warp;
+        // nprod divides the stage count, so a stage is always refilled by
+        // the same warp and its empty-barrier parity cannot alias.
+        if (lane == 0 && warp < p.nprod) {
             int g = 0;
             for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
                 int m0, n0;
@@ -222,13 +237,16 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const int rem = m0 - img * p.OHW;
                 const int oh = rem / p.OW, ow = rem - (rem / p.OW) * p.OW;
                 const int wc = ow * p.stride - p.pad, hc = oh * p.stride - p.pad;
+                bool ok = true;
                 for (int i = 0; i < nk; ++i, ++g) {
+                    if (g % p.nprod != warp) continue;
                     const int s = g % S, u = g / S;
                     if (!ptx::mbar_wait_bounded(empty_bar(s), (u & 1) ^ 1, kWaitLimitNs)) {
                         abort_now(p, abort_flag);
+                        ok = false;
                         break;
                     }
-                    if (aborted(abort_flag)) break;
+                    if (aborted(abort_flag)) { ok = false; break; }
                     const int tap = i / p.cblocks, cb = i - tap * p.cblocks;
                     const int r = tap / p.ks, tt = tap - r * p.ks;
                     const uint32_t a_dst = base + s * p.stage_bytes;
@@ -240,11 +258,12 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     else
                         ptx::tma_load_2d(a_dst, &tmA, full_bar(s), cb * p.CB, m0);
                     ptx::tma_load_2d(b_dst, &tmB, full_bar(s), tap * p.c_in_pad + cb * p.CB, n0);
-                    issued = g + 1;
+                    last_g = g;
                 }
+                if (!ok) break;
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         if (lane == 0) {
             const uint32_t sbo = 8u * p.RB;
             const int kslices = p.RB / 32;
@@ -284,10 +303,10 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ptx::mma_commit(drain_bar);          // fires once every MMA issued here completed
         }
     } else {
-        // Epilogue warps 2..9: warp w reads TMEM lanes 32*(w%4) .. +31, and
-        // the two warps of a lane quadrant take alternate 32-column groups.
+        // Epilogue warps: warp w reads TMEM lanes 32*(w%4) .. +31, and the
+        // two warps of a lane quadrant take alternate 32-column groups.
         const int q = warp & 3;
-        const int half = (warp - 2) >> 2;
+        const int half = (warp - kEpiFirst) >> 2;
         const int row = 32 * q + lane;
         int j = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++j) {
@@ -332,16 +351,17 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     // ---- teardown: all MMAs complete, loads landed, TMEM freed.
     __syncthreads();
-    if (warp == 0 && lane == 0 && aborted(abort_flag)) {
-        for (int g = (issued > S ? issued - S : 0); g < issued; ++g)
+    if (warp < kMaxProducers && lane == 0 && aborted(abort_flag)) {
+        // Drain this warp's loads that may still be in flight (bounded).
+        for (int g = last_g; g >= 0 && g > last_g - S; g -= p.nprod)
             ptx::mbar_wait_bounded(full_bar(g % S), (g / S) & 1, kWaitLimitNs);
     }
-    if (warp == 1 && lane == 0) {
+    if (warp == kMmaWarp && lane == 0) {
         if (!ptx::mbar_wait_bounded(drain_bar, 0, kWaitLimitNs)) atomicOr(p.status, 1u);
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, p.tmem_cols);
     }
@@ -376,8 +396,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t u_lo, uint32_t u_hi) {
 }
 
 
-// Persistent INT8 kernel.  Warp 0: TMA producer; warp 1: TMEM + MMA issuer;
-// warps 2-9: epilogue; warps 10-13: int8 -> bf16 converters.
+// Persistent INT8 kernel.  Warps 0-1: TMA producers; warp 2: TMEM + MMA
+// issuer; warps 3-10: epilogue; warps 11-14: int8 -> bf16 converters.
 __global__ void __launch_bounds__(kThreadsI8, 1)
 tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -421,7 +441,7 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmB);
     }
-    if (warp == 1) {
+    if (warp == kMmaWarpI8) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), p.tmem_cols);
         ptx::tmem_relinquish();
     }
@@ -430,9 +450,11 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    int issued = 0;
-    if (warp == 0) {
-        if (lane == 0) {
+    int last_g = -1;
+    if (warp < kMaxProducersI8) {
+        // Producer warp `warp` takes the K steps g with g % nprod == warp
+        // (nprod divides the stage count: one warp per stage, no aliasing).
+        if (lane == 0 && warp < p.nprod) {
             int g = 0;
             for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
                 int m0, n0;
@@ -441,13 +463,16 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const int rem = m0 - img * p.OHW;
                 const int oh = rem / p.OW, ow = rem - (rem / p.OW) * p.OW;
                 const int wc = ow * p.stride - p.pad, hc = oh * p.stride - p.pad;
+                bool ok = true;
                 for (int i = 0; i < nk; ++i, ++g) {
+                    if (g % p.nprod != warp) continue;
                     const int s = g % S, u = g / S;
                     if (!ptx::mbar_wait_bounded(free_bar(s), (u & 1) ^ 1, kWaitLimitNs)) {
                         abort_now(p, abort_flag);
+                        ok = false;
                         break;
                     }
-                    if (aborted(abort_flag)) break;
+                    if (aborted(abort_flag)) { ok = false; break; }
                     const int tap = i / p.cblocks, cb = i - tap * p.cblocks;
                     const int r = tap / p.ks, tt = tap - r * p.ks;
                     const uint32_t st = base + s * p.stage_bytes;
@@ -458,11 +483,12 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     else
                         ptx::tma_load_2d(st + stg_off, &tmA, raw_bar(s), cb * p.CB, m0);
                     ptx::tma_load_2d(st + op_b_off, &tmB, raw_bar(s), tap * p.c_in_pad + cb * p.CB, n0);
-                    issued = g + 1;
+                    last_g = g;
                 }
+                if (!ok) break;
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarpI8) {
         if (lane == 0) {
             const uint32_t sbo = 8u * p.RB;
             const int kslices = p.RB / 32;
@@ -501,10 +527,10 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
             ptx::mma_commit(drain_bar);
         }
-    } else if (warp >= 10) {
-        // Converters: thread (warp - 10) * 32 + lane widens row `row` of every
-        // staging tile into the swizzled bf16 operand.
-        const int row = (warp - 10) * 32 + lane;
+    } else if (warp >= kConvFirstI8) {
+        // Converters: thread (warp - kConvFirstI8) * 32 + lane widens row `row`
+        // of every staging tile into the swizzled bf16 operand.
+        const int row = (warp - kConvFirstI8) * 32 + lane;
         const int in_bytes = p.CB;
         int g = 0;
         for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
@@ -546,9 +572,9 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             if (!ok) break;
         }
     } else {
-        // Epilogue warps 2..9: quadrant warp % 4, alternate 16-column groups.
+        // Epilogue warps 3..10: quadrant warp % 4, alternate 16-column groups.
         const int q = warp & 3;
-        const int half = (warp - 2) >> 2;
+        const int half = (warp - kEpiFirstI8) >> 2;
         const int erow = 32 * q + lane;
         int j = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++j) {
@@ -618,16 +644,16 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
 
     __syncthreads();
-    if (warp == 0 && lane == 0 && aborted(abort_flag)) {
-        for (int g = (issued > S ? issued - S : 0); g < issued; ++g)
+    if (warp < kMaxProducersI8 && lane == 0 && aborted(abort_flag)) {
+        for (int g = last_g; g >= 0 && g > last_g - S; g -= p.nprod)
             ptx::mbar_wait_bounded(raw_bar(g % S), (g / S) & 1, kWaitLimitNs);
     }
-    if (warp == 1 && lane == 0) {
+    if (warp == kMmaWarpI8 && lane == 0) {
         if (!ptx::mbar_wait_bounded(drain_bar, 0, kWaitLimitNs)) atomicOr(p.status, 1u);
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarpI8) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, p.tmem_cols);
     }
@@ -769,6 +795,12 @@ cbs_status plan_tc(cbs_plan_t &p) {
     int stages = kSmemBudget / stage;
     if (stages > 32) stages = 32;
     if (stages < 2) stages = 2;
+    // Producer warps take interleaved K steps; their count divides the
+    // stage count (so each stage is refilled by one warp).
+    const int max_prod = i8 ? kMaxProducersI8 : kMaxProducers;
+    int nprod = max_prod;
+    while (nprod > 1 && (stages < 2 * nprod)) nprod /= 2;
+    stages = stages / nprod * nprod;
     p.stages = stages;
     p.threads = i8 ? kThreadsI8 : kThreads;
     p.smem_bytes = 1024 + stages * stage + 8 * ((i8 ? 3 : 2) * stages + 5) + 16;
@@ -808,6 +840,12 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     P.ksteps = d.k * d.k * P.cblocks;
     P.BN = BN; P.stages = pl.stages;
     P.m_tiles = pl.m_tiles; P.n_tiles = pl.n_tiles;
+    {
+        const int max_prod = i8 ? kMaxProducersI8 : kMaxProducers;
+        int nprod = max_prod;
+        while (nprod > 1 && (pl.stages < 2 * nprod || pl.stages % nprod != 0)) nprod /= 2;
+        P.nprod = nprod;
+    }
     P.a_bytes = kBM * RB; P.b_bytes = BN * RB;
     P.stage_bytes = round_up(P.a_bytes + P.b_bytes, 1024);
     if (i8) {
