@@ -36,13 +36,15 @@ EXPORTED = (
 class cbs_layer_desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "n", "c_in", "h", "w", "c_out", "k", "stride", "pad", "in_layout", "out_layout", "prec",
-        "force_variant", "force_split_k", "force_block_n", "force_block_m", "out_row_stride")]
+        "force_variant", "force_split_k", "force_block_n", "force_block_m", "out_row_stride",
+        "force_k_group", "force_b_resident")]
 
 
 class cbs_plan_t(ctypes.Structure):
     _fields_ = [("size", ctypes.c_uint32), ("abi_version", ctypes.c_uint32)] + \
         [(n, ctypes.c_int) for n in (
-            "variant", "block_m", "block_n", "block_k", "stages", "split_k", "c_in_pad", "k_gemm",
+            "variant", "block_m", "block_n", "block_k", "stages", "split_k", "k_group", "b_resident",
+            "c_in_pad", "k_gemm",
             "oh", "ow", "out_row_stride", "m_tiles", "n_tiles", "grid_ctas", "threads",
             "smem_bytes")] + \
         [(n, ctypes.c_size_t) for n in (

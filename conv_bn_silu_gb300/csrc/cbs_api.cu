@@ -207,6 +207,7 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
     p.size = sizeof(cbs_plan_t);
     p.abi_version = CBS_ABI_VERSION;
     p.desc = D;
+    p.k_group = 1;
     p.oh = (D.h + 2 * D.pad - D.k) / D.stride + 1;
     p.ow = (D.w + 2 * D.pad - D.k) / D.stride + 1;
     const long long M = (long long)D.n * p.oh * p.ow;

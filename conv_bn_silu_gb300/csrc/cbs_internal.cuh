@@ -13,6 +13,11 @@ namespace cbs {
 // GB300: 152 SMs on two dies.  cbs_plan is host-only and makes no CUDA call,
 // so it plans for this count; launches size their grids from the plan.
 constexpr int kNumSMs = 152;
+// Dynamic shared memory ceiling set once on every kernel that opts in above
+// 48 KB (the sm_100-family per-block maximum).  Each launch asks for its own
+// size below it; a fixed ceiling means a launch recorded in a CUDA graph stays
+// valid whatever other launches set afterwards.
+constexpr int kMaxDynSmem = 227 * 1024;
 
 // Records a message for the calling thread and returns `s`.
 cbs_status fail(cbs_status s, const char *fmt, ...);

@@ -191,6 +191,15 @@ cudaError_t launch_kind(const StemLaunch &L, cudaStream_t s) {
     const long long total = (long long)L.N * L.OH * L.OW;
     const int grid = (int)((total + 255) / 256);
     const int smem = L.KS * L.KS * L.c_pad * COUT * (int)sizeof(float);
+    if (smem > 48 * 1024) {  // 7x7 filters with 64 output channels need 49 KB of weights
+        if (smem > kMaxDynSmem) return cudaErrorInvalidValue;
+        cudaError_t e = cudaSuccess;
+        if (L.in_nhwc && L.out_nhwc) e = cudaFuncSetAttribute(stem_kernel<KIND, COUT, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        else if (L.in_nhwc) e = cudaFuncSetAttribute(stem_kernel<KIND, COUT, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        else if (L.out_nhwc) e = cudaFuncSetAttribute(stem_kernel<KIND, COUT, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        else e = cudaFuncSetAttribute(stem_kernel<KIND, COUT, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        if (e != cudaSuccess) return e;
+    }
     if (L.in_nhwc && L.out_nhwc) stem_kernel<KIND, COUT, true, true><<<grid, 256, smem, s>>>(L);
     else if (L.in_nhwc) stem_kernel<KIND, COUT, true, false><<<grid, 256, smem, s>>>(L);
     else if (L.out_nhwc) stem_kernel<KIND, COUT, false, true><<<grid, 256, smem, s>>>(L);

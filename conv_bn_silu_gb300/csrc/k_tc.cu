@@ -2,21 +2,33 @@
 // BN + SiLU layer on sm_103a.
 //
 // Implicit GEMM (page 1, "What NHWC is and why it matters", item 3 and the
-// tensor-core plan of "Improvements" #2): the output tile is 128 consecutive
-// output pixels (n, oh, ow flattened) x BN output channels.  K is walked as
+// tensor-core plan of "Improvements" #2): a tile is 128 * mmul consecutive
+// output pixels (n, oh, ow flattened) x BN output channels, computed as mmul
+// M=128 accumulators side by side in tensor memory.  K is walked as
 // (filter tap, channel block); each K step brings
-//   A: 128 pixels x RB bytes of channels for one tap, loaded by TMA in im2col
-//      mode (the hardware forms the shifted, zero-padded window; no im2col
-//      matrix exists in memory), or by a 2-D tiled TMA for 1x1 stride-1
+//   A: 128 * mmul pixels x RB bytes of channels for one tap in ONE TMA box,
+//      in im2col mode (the hardware forms the shifted, zero-padded window; no
+//      im2col matrix exists in memory), or as a 2-D tile for 1x1 stride-1
 //      layers, where A is the NHWC activation matrix itself;
-//   B: BN packed weight rows x RB bytes (2-D tiled TMA);
-// into a ring of shared-memory stages guarded by mbarriers.  One thread
-// issues tcgen05.mma (M=128, N=BN, accumulator in tensor memory); four
-// epilogue warps read the accumulator with tcgen05.ld, add the folded bias,
-// apply SiLU and store NHWC or NCHW output at exact addresses.
+//   B: BN packed weight rows x RB bytes (2-D tiled TMA), either with every
+//      K step or, when the layer's weight tile fits, once per CTA into a
+//      resident region that every tile of the launch reuses;
+// into a ring of shared-memory stages guarded by mbarriers; one stage carries
+// k_group K steps.  One thread issues tcgen05.mma (M=128, N=BN, accumulators
+// in tensor memory); eight epilogue warps read the accumulators with
+// tcgen05.ld, add the folded bias, apply SiLU and store NHWC or NCHW output at
+// exact addresses.
 //
-// Warp roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
-// warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
+// The shape of the pipeline follows what GB300 measures: a warp issuing TMA
+// copies gets about one box through every ~570 cycles whatever its size (up
+// to ~75 B/cycle per SM in total), and an MMA costs ~90 cycles whenever its
+// operands change (N <= 128), plus a few hundred cycles for each barrier the
+// issuing thread waits on.  So the kernel moves few, large boxes (tall A
+// tiles, resident B) from several producer warps and waits once per stage of
+// several K steps.
+//
+// Warp roles: warps 0-3 = TMA producers, warp 4 = TMEM allocator + MMA issuer,
+// warps 5-12 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
 // Every mbarrier wait is bounded by wall time; on expiry the kernel records
 // a timeout in the library's status word, drains what it issued (again
 // bounded), frees its tensor memory and returns.
@@ -32,15 +44,11 @@
 namespace cbs {
 namespace {
 
-constexpr int kBM = 128;
-// Warp roles.  One warp issuing TMA tensor copies gets about one copy
-// through every ~0.3 us whatever the box size (measured on GB300: 8.4 TB/s
-// from L2 for 16 KB boxes with one issuing warp per SM, 13 TB/s with two),
-// so several producer warps take interleaved K steps.
+constexpr int kBM = 128;                         // rows of one MMA (one TMEM lane per pixel)
 constexpr int kMaxProducers = 4;                 // warps 0..3
 constexpr int kMmaWarp = kMaxProducers;          // warp 4: TMEM + MMA issuer
 constexpr int kEpiFirst = kMmaWarp + 1;          // warps 5..12: epilogue
-constexpr int kEpiWarps = 8;                     // two per TMEM lane quadrant, splitting the columns
+constexpr int kEpiWarps = 8;                     // two per TMEM lane quadrant
 constexpr int kThreads = 32 * (kEpiFirst + kEpiWarps);        // TF32/BF16: 416
 constexpr int kMaxProducersI8 = 2;               // INT8: warps 0..1
 constexpr int kMmaWarpI8 = kMaxProducersI8;      // warp 2
@@ -48,7 +56,7 @@ constexpr int kEpiFirstI8 = kMmaWarpI8 + 1;      // warps 3..10
 constexpr int kConvFirstI8 = kEpiFirstI8 + kEpiWarps;  // warps 11..14: int8 -> bf16 converters
 constexpr int kThreadsI8 = 32 * (kConvFirstI8 + 4);    // 480
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSmemBudget = 222 * 1024;           // stages + resident weights + barriers
 
 enum TcKind { kTF32 = 0, kBF16 = 1 };
 
@@ -75,6 +83,14 @@ struct TcParams {
     int stg_bytes;             // int8 staging tile of one stage (128 x CB bytes)
     uint32_t stg_mask;         // staging swizzle mask (bits 7.. -> bits 4..)
     uint32_t op_mask;          // operand swizzle mask
+    // TF32/BF16 tall tiles, grouped K steps, resident weights
+    int mmul;                  // 128-pixel sub-tiles per tile (one A box of 128*mmul rows)
+    int kg;                    // K steps per stage (divides ksteps)
+    int b_res;                 // weights resident for the whole launch
+    int bnp;                   // TMEM columns between sub-tile accumulators (power of two >= BN)
+    int b_tile_stride;         // bytes between B tiles (1024-aligned)
+    int b_region;              // bytes of the resident weight region (0 if none)
+    int a_box_bytes;           // one A box: 128 * mmul * RB
 };
 
 // SiLU(z) = z * sigmoid(z) = h + h * tanh(h) with h = z / 2: one MUFU
@@ -153,10 +169,11 @@ __device__ __forceinline__ void epi_store16(const TcParams &p, int m, int img, i
 }
 
 // Tile t of the persistent walk: M-tile major, N-tile minor, so CTAs that
-// run at the same time share A rows through L2.
-__device__ __forceinline__ void tile_coords(int t, int n_tiles, int &m0, int &n0, int BN) {
+// run at the same time share A rows through L2.  When the grid is a multiple
+// of n_tiles, every tile of a CTA has the same N tile (resident weights).
+__device__ __forceinline__ void tile_coords(int t, int n_tiles, int tile_m, int &m0, int &n0, int BN) {
     const int mt = t / n_tiles;
-    m0 = mt * kBM;
+    m0 = mt * tile_m;
     n0 = (t - mt * n_tiles) * BN;
 }
 
@@ -168,24 +185,26 @@ __device__ __forceinline__ void abort_now(const TcParams &p, int *abort_flag) {
 __device__ __forceinline__ bool aborted(int *abort_flag) { return *(volatile int *)abort_flag != 0; }
 
 // Persistent tensor-core kernel (TF32 / BF16).  Each CTA walks the tiles
-// t = blockIdx.x, blockIdx.x + gridDim.x, ...; the producer's stage ring and
-// the MMA issuer run ahead across tile boundaries, and the accumulator is
+// t = blockIdx.x, blockIdx.x + gridDim.x, ...; the producers' stage ring and
+// the MMA issuer run ahead across tile boundaries, and the accumulators are
 // double-buffered in TMEM so the epilogue of tile j overlaps the MMAs of
 // tile j+1.
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // Stage buffers start on a 1024-byte boundary of the shared window (the
+    // Buffers start on a 1024-byte boundary of the shared window (the
     // swizzle atoms of TMA and of the MMA descriptors are address based).
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t *base_ptr = smem_raw + (base - raw_addr);
     const int S = p.stages;
-    // Barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain.
-    const uint32_t bars = base + S * p.stage_bytes;
-    uint64_t *bar_ptr = reinterpret_cast<uint64_t *>(base_ptr + S * p.stage_bytes);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_ptr + 2 * S + 5);
+    // [resident B][S stages][barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain, b_full]
+    const uint32_t b_base = base;
+    const uint32_t stage0 = base + p.b_region;
+    const uint32_t bars = stage0 + S * p.stage_bytes;
+    uint64_t *bar_ptr = reinterpret_cast<uint64_t *>(base_ptr + p.b_region + S * p.stage_bytes);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_ptr + 2 * S + 6);
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
     auto full_bar = [&](int s) { return bars + 8u * s; };
@@ -193,10 +212,14 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     auto accf_bar = [&](int a) { return bars + 8u * (2 * S + a); };
     auto acce_bar = [&](int a) { return bars + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = bars + 8u * (2 * S + 4);
+    const uint32_t bfull_bar = bars + 8u * (2 * S + 5);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = p.ksteps;
+    const int nstage = nk / p.kg;                 // stages per tile
+    const int tile_m = kBM * p.mmul;
     const int num_tiles = p.m_tiles * p.n_tiles;
+    const int b_step_bytes = p.BN * p.RB;         // bytes of one B tile as loaded
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -208,6 +231,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ptx::mbar_init(acce_bar(a), kEpiWarps);   // one arrive per epilogue warp
         }
         ptx::mbar_init(drain_bar, 1);
+        ptx::mbar_init(bfull_bar, p.nprod);           // one arrive per producer warp
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmA);
@@ -222,23 +246,37 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    int last_g = -1;  // producer: last K step (global count) whose loads this warp issued
+    int last_g = -1;  // producer: last stage (global count) whose loads this warp issued
+    bool b_issued = false;
     if (warp < kMaxProducers) {
-        // Producer warp `warp` takes the K steps g with g % nprod == warp;
-        // nprod divides the stage count, so a stage is always refilled by
-        // the same warp and its empty-barrier parity cannot alias.
         if (lane == 0 && warp < p.nprod) {
+            if (p.b_res && blockIdx.x < num_tiles) {
+                // This CTA's N tile never changes: load its weight tile once.
+                int m0, n0;
+                tile_coords(blockIdx.x, p.n_tiles, tile_m, m0, n0, p.BN);
+                int mine = 0;
+                for (int i = warp; i < nk; i += p.nprod) ++mine;
+                ptx::mbar_arrive_expect_tx(bfull_bar, (uint32_t)(mine * b_step_bytes));
+                for (int i = warp; i < nk; i += p.nprod) {
+                    const int tap = i / p.cblocks, cb = i - tap * p.cblocks;
+                    ptx::tma_load_2d(b_base + i * p.b_tile_stride, &tmB, bfull_bar, tap * p.c_in_pad + cb * p.CB, n0);
+                }
+                b_issued = true;
+            }
+            // Producer warp `warp` takes the stages g with g % nprod == warp;
+            // nprod divides the stage count, so a stage is always refilled by
+            // the same warp and its empty-barrier parity cannot alias.
             int g = 0;
             for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
                 int m0, n0;
-                tile_coords(t, p.n_tiles, m0, n0, p.BN);
+                tile_coords(t, p.n_tiles, tile_m, m0, n0, p.BN);
                 // Window corner of the tile's first output pixel.
                 const int img = m0 / p.OHW;
                 const int rem = m0 - img * p.OHW;
                 const int oh = rem / p.OW, ow = rem - (rem / p.OW) * p.OW;
                 const int wc = ow * p.stride - p.pad, hc = oh * p.stride - p.pad;
                 bool ok = true;
-                for (int i = 0; i < nk; ++i, ++g) {
+                for (int st = 0; st < nstage; ++st, ++g) {
                     if (g % p.nprod != warp) continue;
                     const int s = g % S, u = g / S;
                     if (!ptx::mbar_wait_bounded(empty_bar(s), (u & 1) ^ 1, kWaitLimitNs)) {
@@ -247,17 +285,22 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         break;
                     }
                     if (aborted(abort_flag)) { ok = false; break; }
-                    const int tap = i / p.cblocks, cb = i - tap * p.cblocks;
-                    const int r = tap / p.ks, tt = tap - r * p.ks;
-                    const uint32_t a_dst = base + s * p.stage_bytes;
-                    const uint32_t b_dst = a_dst + p.a_bytes;
-                    ptx::mbar_arrive_expect_tx(full_bar(s), (uint32_t)(p.a_bytes + p.b_bytes));
-                    if (p.im2col)
-                        ptx::tma_load_im2col_4d(a_dst, &tmA, full_bar(s), cb * p.CB, wc, hc, img, (uint16_t)tt,
-                                                (uint16_t)r);
-                    else
-                        ptx::tma_load_2d(a_dst, &tmA, full_bar(s), cb * p.CB, m0);
-                    ptx::tma_load_2d(b_dst, &tmB, full_bar(s), tap * p.c_in_pad + cb * p.CB, n0);
+                    const uint32_t sbase = stage0 + s * p.stage_bytes;
+                    ptx::mbar_arrive_expect_tx(full_bar(s), (uint32_t)(p.kg * (p.a_box_bytes + (p.b_res ? 0 : b_step_bytes))));
+                    for (int kk = 0; kk < p.kg; ++kk) {
+                        const int i = st * p.kg + kk;
+                        const int tap = i / p.cblocks, cb = i - tap * p.cblocks;
+                        const int r = tap / p.ks, tt = tap - r * p.ks;
+                        const uint32_t a_dst = sbase + kk * p.a_box_bytes;
+                        if (p.im2col)
+                            ptx::tma_load_im2col_4d(a_dst, &tmA, full_bar(s), cb * p.CB, wc, hc, img, (uint16_t)tt,
+                                                    (uint16_t)r);
+                        else
+                            ptx::tma_load_2d(a_dst, &tmA, full_bar(s), cb * p.CB, m0);
+                        if (!p.b_res)
+                            ptx::tma_load_2d(sbase + p.kg * p.a_box_bytes + kk * p.b_tile_stride, &tmB, full_bar(s),
+                                             tap * p.c_in_pad + cb * p.CB, n0);
+                    }
                     last_g = g;
                 }
                 if (!ok) break;
@@ -267,8 +310,14 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (lane == 0) {
             const uint32_t sbo = 8u * p.RB;
             const int kslices = p.RB / 32;
+            const uint32_t sub_bytes = (uint32_t)(kBM * p.RB);   // one 128-row sub-tile of an A box
+            bool ok = true;
+            if (p.b_res && blockIdx.x < num_tiles && !ptx::mbar_wait_bounded(bfull_bar, 0, kWaitLimitNs)) {
+                abort_now(p, abort_flag);
+                ok = false;
+            }
             int g = 0, j = 0;
-            for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x, ++j) {
+            for (int t = blockIdx.x; ok && t < num_tiles && !aborted(abort_flag); t += gridDim.x, ++j) {
                 const int acc = j & 1, ua = j >> 1;
                 if (!ptx::mbar_wait_bounded(acce_bar(acc), (ua & 1) ^ 1, kWaitLimitNs)) {
                     abort_now(p, abort_flag);
@@ -276,8 +325,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_stride);
-                bool ok = true;
-                for (int i = 0; i < nk; ++i, ++g) {
+                for (int st = 0; st < nstage; ++st, ++g) {
                     const int s = g % S, u = g / S;
                     if (!ptx::mbar_wait_bounded(full_bar(s), u & 1, kWaitLimitNs)) {
                         abort_now(p, abort_flag);
@@ -285,15 +333,23 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t a_addr = base + s * p.stage_bytes;
-                    const uint32_t b_addr = a_addr + p.a_bytes;
-                    for (int k = 0; k < kslices; ++k) {
-                        const uint64_t ad = ptx::smem_desc(a_addr + 32u * k, 16u, sbo, p.swz);
-                        const uint64_t bd = ptx::smem_desc(b_addr + 32u * k, 16u, sbo, p.swz);
-                        if (KIND == kTF32)
-                            ptx::mma_tf32(d_tmem, ad, bd, p.idesc, (i > 0 || k > 0) ? 1u : 0u);
-                        else
-                            ptx::mma_f16(d_tmem, ad, bd, p.idesc, (i > 0 || k > 0) ? 1u : 0u);
+                    const uint32_t sbase = stage0 + s * p.stage_bytes;
+                    for (int kk = 0; kk < p.kg; ++kk) {
+                        const int i = st * p.kg + kk;
+                        const uint32_t a_addr = sbase + kk * p.a_box_bytes;
+                        const uint32_t b_addr = p.b_res ? b_base + i * p.b_tile_stride
+                                                        : sbase + p.kg * p.a_box_bytes + kk * p.b_tile_stride;
+                        for (int mi = 0; mi < p.mmul; ++mi) {
+                            const uint32_t d = d_tmem + (uint32_t)(mi * p.bnp);
+                            for (int k = 0; k < kslices; ++k) {
+                                const uint64_t ad = ptx::smem_desc(a_addr + mi * sub_bytes + 32u * k, 16u, sbo, p.swz);
+                                const uint64_t bd = ptx::smem_desc(b_addr + 32u * k, 16u, sbo, p.swz);
+                                if (KIND == kTF32)
+                                    ptx::mma_tf32(d, ad, bd, p.idesc, (i > 0 || k > 0) ? 1u : 0u);
+                                else
+                                    ptx::mma_f16(d, ad, bd, p.idesc, (i > 0 || k > 0) ? 1u : 0u);
+                            }
+                        }
                     }
                     ptx::mma_commit(empty_bar(s));
                 }
@@ -303,11 +359,15 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ptx::mma_commit(drain_bar);          // fires once every MMA issued here completed
         }
     } else {
-        // Epilogue warps: warp w reads TMEM lanes 32*(w%4) .. +31, and the
-        // two warps of a lane quadrant take alternate 32-column groups.
+        // Epilogue warps: warp w reads TMEM lanes 32*(w%4) .. +31.  With two
+        // sub-tiles the two warps of a lane quadrant take one sub-tile each;
+        // with one they take alternate 16-column groups.
         const int q = warp & 3;
-        const int half = (warp - kEpiFirst) >> 2;
-        const int row = 32 * q + lane;
+        const int h = (warp - kEpiFirst) >> 2;
+        const int sub = p.mmul == 2 ? h : 0;
+        const int cstart = p.mmul == 2 ? 0 : 16 * h;
+        const int cstep = p.mmul == 2 ? 16 : 32;
+        const int row = sub * kBM + 32 * q + lane;
         int j = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++j) {
             const int acc = j & 1, ua = j >> 1;
@@ -320,7 +380,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             ptx::tc_fence_after();
             int m0, n0;
-            tile_coords(t, p.n_tiles, m0, n0, p.BN);
+            tile_coords(t, p.n_tiles, tile_m, m0, n0, p.BN);
             const int m = m0 + row;
             int img = 0, oh = 0, ow = 0;
             if (m < p.M) {
@@ -329,17 +389,17 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 oh = rem / p.OW;
                 ow = rem - oh * p.OW;
             }
-            const uint32_t t_row = tmem_base + (uint32_t)(acc * p.acc_stride) + ((uint32_t)(32 * q) << 16);
-            for (int c0 = 32 * half; c0 < p.BN; c0 += 64) {
+            const uint32_t t_row = tmem_base + (uint32_t)(acc * p.acc_stride + sub * p.bnp) + ((uint32_t)(32 * q) << 16);
+            for (int c0 = cstart; c0 < p.BN; c0 += 2 * cstep) {
                 // Two loads, one wait: 32 columns in flight per thread.
                 uint32_t v0[16], v1[16];
-                const bool two = c0 + 16 < p.BN;
+                const bool two = c0 + cstep < p.BN;
                 ptx::tmem_ld16(t_row + (uint32_t)c0, v0);
-                if (two) ptx::tmem_ld16(t_row + (uint32_t)(c0 + 16), v1);
+                if (two) ptx::tmem_ld16(t_row + (uint32_t)(c0 + cstep), v1);
                 ptx::tmem_ld_wait();
                 if (m < p.M) {
                     if (n0 + c0 < p.C_out) epi_store16<KIND>(p, m, img, oh, ow, n0 + c0, v0);
-                    if (two && n0 + c0 + 16 < p.C_out) epi_store16<KIND>(p, m, img, oh, ow, n0 + c0 + 16, v1);
+                    if (two && n0 + c0 + cstep < p.C_out) epi_store16<KIND>(p, m, img, oh, ow, n0 + c0 + cstep, v1);
                 }
             }
             // This accumulator has been read: hand it back to the MMA issuer.
@@ -355,6 +415,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // Drain this warp's loads that may still be in flight (bounded).
         for (int g = last_g; g >= 0 && g > last_g - S; g -= p.nprod)
             ptx::mbar_wait_bounded(full_bar(g % S), (g / S) & 1, kWaitLimitNs);
+        if (b_issued) ptx::mbar_wait_bounded(bfull_bar, 0, kWaitLimitNs);
     }
     if (warp == kMmaWarp && lane == 0) {
         if (!ptx::mbar_wait_bounded(drain_bar, 0, kWaitLimitNs)) atomicOr(p.status, 1u);
@@ -458,7 +519,7 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             int g = 0;
             for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
                 int m0, n0;
-                tile_coords(t, p.n_tiles, m0, n0, p.BN);
+                tile_coords(t, p.n_tiles, kBM, m0, n0, p.BN);
                 const int img = m0 / p.OHW;
                 const int rem = m0 - img * p.OHW;
                 const int oh = rem / p.OW, ow = rem - (rem / p.OW) * p.OW;
@@ -587,7 +648,7 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
             ptx::tc_fence_after();
             int m0, n0;
-            tile_coords(t, p.n_tiles, m0, n0, p.BN);
+            tile_coords(t, p.n_tiles, kBM, m0, n0, p.BN);
             const int m = m0 + erow;
             int img = 0, oh = 0, ow = 0;
             if (m < p.M) {
@@ -716,19 +777,78 @@ int elem_bytes_of(int variant) { return variant == CBS_VARIANT_TC_TF32 ? 4 : 2; 
 // Channels per K step for the INT8 variant (int8 bytes per staging row).
 int i8_channel_block(int c_in_pad) { return c_in_pad % 64 == 0 ? 64 : (c_in_pad % 32 == 0 ? 32 : 16); }
 
-// Estimated cycles of one layer on the persistent kernel for a given N tile:
-// tiles are spread over the SMs in waves; a tile costs the larger of its MMA
-// time and its shared-memory fill (A and B re-read from L2 for every tile),
-// and the epilogue overlaps the next tile's main loop.
-double tc_cycles(long long m_tiles, int c_out, int BN, int K, int eb_x, int eb_w, bool tf32) {
-    const long long tiles = m_tiles * ((c_out + BN - 1) / BN);
-    const long long waves = (tiles + kNumSMs - 1) / kNumSMs;
-    const double macs_per_clk = tf32 ? 2048.0 : 4096.0;       // per SM, dense
-    const double l2_bytes_per_clk = 64.0;                      // per SM, all SMs loading
-    const double mma = (double)kBM * BN * K / macs_per_clk;
-    const double load = ((double)kBM * K * eb_x + (double)BN * K * eb_w) / l2_bytes_per_clk;
-    const double per_tile = (mma > load ? mma : load) + 150.0;
-    return (double)waves * per_tile + 2500.0;  // + pipeline fill and the last epilogue
+// Producer warps for a stage count: the largest of 4, 3, 2 that divides it
+// (each stage is then always refilled by the same warp).
+int tc_producers(int stages) {
+    for (int np = kMaxProducers; np >= 2; --np)
+        if (stages >= np && stages % np == 0) return np;
+    return 1;
+}
+
+// GB300 costs the planner works from (SM cycles, measured with single-SM
+// probes): a warp issuing TMA copies gets one box through every ~570 cycles
+// whatever its size, and all SMs loading at once fill from L2 at ~70 B/cycle
+// each; an MMA with fresh operands costs ~95 cycles for N <= 128 (a commit
+// per stage included) and N/2 beyond (TF32: twice that), and the issuing
+// thread loses ~270 cycles per stage barrier it waits on.
+constexpr double kClkPerBox = 570.0, kFillBytesPerClk = 70.0, kClkPerStageWait = 270.0;
+
+double tc_mma_clk(int N, bool tf32) {
+    const double c = tf32 ? (double)N : 0.5 * N;
+    return c > 95.0 ? c : 95.0;
+}
+
+struct TcConfig {
+    int BN, mmul, b_res, kg, stages, nprod;
+    int m_tiles, n_tiles, grid;
+    int stage_bytes, b_region, b_tile_stride, a_box_bytes;
+    double cycles;
+};
+
+// Shared-memory layout and cost of one configuration (false if it does not fit).
+bool tc_config(const cbs_layer_desc &d, long long M, int RB, int ksteps, bool tf32, int BN, int mmul, int b_res,
+               int kg, TcConfig &c) {
+    c.BN = BN; c.mmul = mmul; c.b_res = b_res; c.kg = kg;
+    c.a_box_bytes = kBM * mmul * RB;
+    const int b_bytes = BN * RB;
+    c.b_tile_stride = (b_bytes + 1023) / 1024 * 1024;
+    c.b_region = b_res ? ksteps * c.b_tile_stride : 0;
+    c.stage_bytes = kg * c.a_box_bytes + (b_res ? 0 : kg * c.b_tile_stride);
+    const int barrier_bytes = 8 * (2 * 16 + 6) + 16;
+    int cap = (kSmemBudget - c.b_region - barrier_bytes) / c.stage_bytes;
+    if (cap > 16) cap = 16;
+    if (cap < 2) return false;
+    c.stages = cap >= 4 ? cap - cap % 4 : cap;
+    c.nprod = tc_producers(c.stages);
+    c.m_tiles = (int)((M + kBM * mmul - 1) / (kBM * mmul));
+    c.n_tiles = (d.c_out + BN - 1) / BN;
+    const long long tiles = (long long)c.m_tiles * c.n_tiles;
+    if (b_res && c.n_tiles > 1) {
+        // Every CTA keeps one N tile: the grid is a multiple of n_tiles.
+        const long long g = tiles < kNumSMs ? tiles : (long long)(kNumSMs / c.n_tiles) * c.n_tiles;
+        if (g <= 0) return false;
+        c.grid = (int)g;
+    } else {
+        c.grid = (int)(tiles < kNumSMs ? tiles : kNumSMs);
+    }
+    const double tpc = (double)((tiles + c.grid - 1) / c.grid);   // tiles of the busiest CTA
+    const int kslices = RB / 32;
+    const double mma = tpc * ((double)ksteps * kslices * mmul * tc_mma_clk(BN, tf32) + (double)(ksteps / kg) * kClkPerStageWait);
+    const double boxes = tpc * ksteps * (b_res ? 1.0 : 2.0) + (b_res ? (double)ksteps : 0.0);
+    const double bytes = tpc * ksteps * (double)(c.a_box_bytes + (b_res ? 0 : b_bytes)) + (b_res ? (double)ksteps * b_bytes : 0.0);
+    const double t_box = boxes * kClkPerBox / c.nprod, t_fill = bytes / kFillBytesPerClk;
+    const double tma = t_box > t_fill ? t_box : t_fill;
+    // Epilogue: one thread per pixel and 16-column group; eight warps cover
+    // two sub-tiles, or split one sub-tile's columns.
+    const double vals = mmul == 2 ? (double)BN : 0.5 * BN;
+    const double epi = tpc * (250.0 + 45.0 * vals);
+    double cyc = mma > tma ? mma : tma;
+    if (epi > cyc) cyc = epi;
+    // Pipeline fill: the first stage's loads (and a resident weight tile)
+    // arrive before any MMA, and the last tile's epilogue follows the last.
+    cyc += 1500.0 + (b_res ? kClkPerBox + (double)ksteps * b_bytes / kFillBytesPerClk / c.nprod : 0.0) + 250.0 + 45.0 * vals;
+    c.cycles = cyc;
+    return true;
 }
 
 cbs_status plan_tc(cbs_plan_t &p) {
@@ -757,56 +877,96 @@ cbs_status plan_tc(cbs_plan_t &p) {
     p.w_packed_bytes = (size_t)d.c_out * p.k_gemm * (tf32 ? 4 : 2);
     if (d.pad > 127 || (p.oh - 1) * d.stride - d.pad - d.h + 1 < -128 || (p.ow - 1) * d.stride - d.pad - d.w + 1 < -128)
         return fail(CBS_ERR_UNSUPPORTED, "padding outside the im2col corner range");
+    if (d.force_split_k > 1) return fail(CBS_ERR_UNSUPPORTED, "split-K not built for the tensor-core path yet");
     const long long M = (long long)d.n * p.oh * p.ow;
-    p.m_tiles = ceil_div(M, kBM);
-    // TMEM holds two accumulator buffers of nchunks * next_pow2(BN) columns
-    // (rounded to a power of two): nchunks * next_pow2(BN) <= 256.
-    int max_bn = 256;
-    while (max_bn >= 16 && nchunks * max_bn > 256) max_bn /= 2;
-    int BN;
+    const int ksteps = d.k * d.k * (p.c_in_pad / CB);
+    p.block_k = CB;
+    p.split_k = 1;
+    p.workspace_bytes = 0;
+
+    if (i8) {
+        p.m_tiles = ceil_div(M, kBM);
+        // TMEM holds two accumulator buffers of nchunks * next_pow2(BN)
+        // columns (rounded to a power of two): nchunks * next_pow2(BN) <= 256.
+        int max_bn = 256;
+        while (max_bn >= 16 && nchunks * max_bn > 256) max_bn /= 2;
+        int BN;
+        if (d.force_block_n > 0) {
+            BN = d.force_block_n;
+            if (BN % 16 || BN < 16 || BN > 256) return fail(CBS_ERR_INVALID_ARG, "block_n %d: 16..256, multiple of 16", BN);
+            if (BN > max_bn)
+                return fail(CBS_ERR_UNSUPPORTED, "block_n %d with %d exact-sum chunks exceeds TMEM", BN, nchunks);
+        } else {
+            BN = round_up(d.c_out, 16) < max_bn ? round_up(d.c_out, 16) : max_bn;
+            if (BN < 16) return fail(CBS_ERR_UNSUPPORTED, "INT8: %d exact-sum chunks exceed TMEM", nchunks);
+        }
+        p.block_m = kBM;
+        p.block_n = BN;
+        p.n_tiles = ceil_div(d.c_out, BN);
+        p.k_group = 1;
+        p.b_resident = 0;
+        int stage = round_up(kBM * RB + BN * RB, 1024) + round_up(kBM * CB, 1024);  // + int8 staging tile
+        int stages = (200 * 1024) / stage;
+        if (stages > 32) stages = 32;
+        if (stages < 2) stages = 2;
+        int nprod = kMaxProducersI8;
+        while (nprod > 1 && (stages < 2 * nprod)) nprod /= 2;
+        stages = stages / nprod * nprod;
+        p.stages = stages;
+        p.threads = kThreadsI8;
+        p.smem_bytes = 1024 + stages * stage + 8 * (3 * stages + 5) + 16;
+        const long long tiles = (long long)p.m_tiles * p.n_tiles;
+        p.grid_ctas = (int)(tiles < kNumSMs ? tiles : kNumSMs);
+        return CBS_OK;
+    }
+
+    // TF32 / BF16: search N tile, sub-tiles per tile, resident weights and
+    // K steps per stage with the cost model above.
+    int bn_list[12], nbn = 0;
     if (d.force_block_n > 0) {
-        BN = d.force_block_n;
+        const int BN = d.force_block_n;
         if (BN % 16 || BN < 16 || BN > 256) return fail(CBS_ERR_INVALID_ARG, "block_n %d: 16..256, multiple of 16", BN);
-        if (BN > max_bn)
-            return fail(CBS_ERR_UNSUPPORTED, "block_n %d with %d exact-sum chunks exceeds TMEM", BN, nchunks);
+        bn_list[nbn++] = BN;
     } else {
-        const int full = round_up(d.c_out, 16) < max_bn ? round_up(d.c_out, 16) : max_bn;
-        if (full < 16) return fail(CBS_ERR_UNSUPPORTED, "INT8: %d exact-sum chunks exceed TMEM", nchunks);
+        const int full = round_up(d.c_out, 16) < 256 ? round_up(d.c_out, 16) : 256;
         const int cands[] = {full, 256, 192, 128, 96, 64, 48, 32, 16};
-        const int K = p.k_gemm;
-        double best = 1e300;
-        BN = full;
-        for (int c : cands) {
-            if (c > full || c < 16) continue;
-            const double cyc = tc_cycles(p.m_tiles, d.c_out, c, K, eb, tf32 ? 4 : 2, tf32);
-            if (cyc < best * 0.98) { best = cyc; BN = c; }
+        for (int c : cands)
+            if (c <= full) {
+                bool dup = false;
+                for (int k = 0; k < nbn; ++k) dup |= bn_list[k] == c;
+                if (!dup) bn_list[nbn++] = c;
+            }
+    }
+    TcConfig best{};
+    best.cycles = 1e300;
+    for (int bi = 0; bi < nbn; ++bi) {
+        const int BN = bn_list[bi];
+        for (int mmul = 1; mmul <= 2; ++mmul) {
+            if (mmul * next_pow2(BN) > 256) continue;           // two buffers of mmul * BN columns in TMEM
+            if (d.force_block_m > 0 && d.force_block_m != kBM * mmul) continue;
+            for (int b_res = 0; b_res <= 1; ++b_res) {
+                if ((d.force_b_resident > 0 && !b_res) || (d.force_b_resident < 0 && b_res)) continue;
+                for (int kg = 1; kg <= (d.force_k_group > 4 ? d.force_k_group : 4); ++kg) {
+                    if (ksteps % kg) continue;
+                    if (d.force_k_group > 0 && kg != d.force_k_group) continue;
+                    TcConfig c;
+                    if (!tc_config(d, M, RB, ksteps, tf32, BN, mmul, b_res, kg, c)) continue;
+                    if (c.cycles < best.cycles * 0.99) best = c;
+                }
+            }
         }
     }
-    if (d.force_split_k > 1) return fail(CBS_ERR_UNSUPPORTED, "split-K not built for the tensor-core path yet");
-    p.block_m = kBM;
-    p.block_n = BN;
-    p.block_k = CB;
-    p.n_tiles = ceil_div(d.c_out, BN);
-    p.split_k = 1;
-    int stage = round_up(kBM * RB + BN * RB, 1024);  // stages stay 1024-byte aligned
-    if (i8) stage += round_up(kBM * CB, 1024);       // int8 staging tile
-    // As many stages as the budget holds (small-channel layers move little
-    // per K step and need many loads in flight to cover L2 latency).
-    int stages = kSmemBudget / stage;
-    if (stages > 32) stages = 32;
-    if (stages < 2) stages = 2;
-    // Producer warps take interleaved K steps; their count divides the
-    // stage count (so each stage is refilled by one warp).
-    const int max_prod = i8 ? kMaxProducersI8 : kMaxProducers;
-    int nprod = max_prod;
-    while (nprod > 1 && (stages < 2 * nprod)) nprod /= 2;
-    stages = stages / nprod * nprod;
-    p.stages = stages;
-    p.threads = i8 ? kThreadsI8 : kThreads;
-    p.smem_bytes = 1024 + stages * stage + 8 * ((i8 ? 3 : 2) * stages + 5) + 16;
-    const long long tiles = (long long)p.m_tiles * p.n_tiles;
-    p.grid_ctas = (int)(tiles < kNumSMs ? tiles : kNumSMs);
-    p.workspace_bytes = 0;
+    if (best.cycles >= 1e299) return fail(CBS_ERR_UNSUPPORTED, "no tensor-core tile configuration fits shared memory");
+    p.block_m = kBM * best.mmul;
+    p.block_n = best.BN;
+    p.k_group = best.kg;
+    p.b_resident = best.b_res;
+    p.stages = best.stages;
+    p.m_tiles = best.m_tiles;
+    p.n_tiles = best.n_tiles;
+    p.grid_ctas = best.grid;
+    p.threads = kThreads;
+    p.smem_bytes = 1024 + best.b_region + best.stages * best.stage_bytes + 8 * (2 * best.stages + 6) + 16;
     return CBS_OK;
 }
 
@@ -840,14 +1000,30 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     P.ksteps = d.k * d.k * P.cblocks;
     P.BN = BN; P.stages = pl.stages;
     P.m_tiles = pl.m_tiles; P.n_tiles = pl.n_tiles;
-    {
-        const int max_prod = i8 ? kMaxProducersI8 : kMaxProducers;
-        int nprod = max_prod;
+    const int mmul = i8 ? 1 : pl.block_m / kBM;
+    if (pl.block_m != kBM * mmul || mmul < 1 || mmul > 2) return fail(CBS_ERR_PLAN_MISMATCH, "block_m %d", pl.block_m);
+    P.mmul = mmul;
+    P.kg = i8 ? 1 : pl.k_group;
+    P.b_res = i8 ? 0 : pl.b_resident;
+    if (P.kg < 1 || P.ksteps % P.kg) return fail(CBS_ERR_PLAN_MISMATCH, "k_group %d", pl.k_group);
+    P.bnp = next_pow2(BN);
+    P.a_bytes = kBM * RB; P.b_bytes = BN * RB;
+    P.a_box_bytes = kBM * mmul * RB;
+    P.b_tile_stride = round_up(P.b_bytes, 1024);
+    P.b_region = P.b_res ? P.ksteps * P.b_tile_stride : 0;
+    if (i8) {
+        int nprod = kMaxProducersI8;
         while (nprod > 1 && (pl.stages < 2 * nprod || pl.stages % nprod != 0)) nprod /= 2;
         P.nprod = nprod;
+        P.stage_bytes = round_up(P.a_bytes + P.b_bytes, 1024);
+    } else {
+        P.nprod = tc_producers(pl.stages);
+        P.stage_bytes = P.kg * P.a_box_bytes + (P.b_res ? 0 : P.kg * P.b_tile_stride);
+        if (1024 + P.b_region + pl.stages * P.stage_bytes + 8 * (2 * pl.stages + 6) + 16 > pl.smem_bytes)
+            return fail(CBS_ERR_PLAN_MISMATCH, "plan's shared memory does not hold its stages");
+        if (P.b_res && P.n_tiles > 1 && pl.grid_ctas % P.n_tiles)
+            return fail(CBS_ERR_PLAN_MISMATCH, "resident weights need a grid that is a multiple of the N tiles");
     }
-    P.a_bytes = kBM * RB; P.b_bytes = BN * RB;
-    P.stage_bytes = round_up(P.a_bytes + P.b_bytes, 1024);
     if (i8) {
         P.stg_bytes = kBM * CB;
         P.stage_bytes += round_up(P.stg_bytes, 1024);
@@ -871,7 +1047,10 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     // Two accumulator buffers (double buffering across tiles); INT8 chunks
     // sit at power-of-two column offsets inside a buffer.
     P.chunk_stride = next_pow2(BN);
-    P.acc_stride = next_pow2(P.nchunks * P.chunk_stride) < 16 ? 16 : next_pow2(P.nchunks * P.chunk_stride);
+    {
+        const int cols = i8 ? P.nchunks * P.chunk_stride : mmul * P.bnp;
+        P.acc_stride = next_pow2(cols) < 16 ? 16 : next_pow2(cols);
+    }
     P.tmem_cols = (uint32_t)(2 * P.acc_stride < 32 ? 32 : 2 * P.acc_stride);
     if (P.tmem_cols > 512) return fail(CBS_ERR_UNSUPPORTED, "accumulators need %u TMEM columns", P.tmem_cols);
     P.y = y;
@@ -891,14 +1070,15 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
         const int lower[2] = {-d.pad, -d.pad};
         const int upper[2] = {(pl.ow - 1) * d.stride - d.pad - (d.w - 1), (pl.oh - 1) * d.stride - d.pad - (d.h - 1)};
         const cuuint32_t estr[4] = {1, (cuuint32_t)d.stride, (cuuint32_t)d.stride, 1};
-        r = fns.im2col(&tmA, dt_x, 4, const_cast<void *>(x), dims, strides, lower, upper, (cuuint32_t)CB, kBM, estr,
+        r = fns.im2col(&tmA, dt_x, 4, const_cast<void *>(x), dims, strides, lower, upper, (cuuint32_t)CB,
+                       (cuuint32_t)(kBM * mmul), estr,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz_x, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuTensorMapEncodeIm2col failed (%d)", (int)r);
     } else {
         const cuuint64_t dims[2] = {(cuuint64_t)pl.c_in_pad, (cuuint64_t)P.M};
         const cuuint64_t strides[1] = {(cuuint64_t)pl.c_in_pad * eb_x};
-        const cuuint32_t box[2] = {(cuuint32_t)CB, (cuuint32_t)kBM};
+        const cuuint32_t box[2] = {(cuuint32_t)CB, (cuuint32_t)(kBM * mmul)};
         r = fns.tiled(&tmA, dt_x, 2, const_cast<void *>(x), dims, strides, box, estr1, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       swz_x, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuTensorMapEncodeTiled (A) failed (%d)", (int)r);
@@ -914,15 +1094,16 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     }
 
     dim3 grid(pl.grid_ctas, 1, 1);  // persistent: each CTA walks tiles blockIdx.x + i * gridDim.x
+    if (pl.smem_bytes > kMaxDynSmem) return fail(CBS_ERR_UNSUPPORTED, "plan needs %d bytes of shared memory", pl.smem_bytes);
     cudaError_t e;
     if (pl.variant == CBS_VARIANT_TC_TF32) {
-        e = cudaFuncSetAttribute(tc_conv_kernel<kTF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
+        e = cudaFuncSetAttribute(tc_conv_kernel<kTF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
         if (e == cudaSuccess) tc_conv_kernel<kTF32><<<grid, kThreads, pl.smem_bytes, s>>>(tmA, tmB, P);
     } else if (pl.variant == CBS_VARIANT_TC_BF16) {
-        e = cudaFuncSetAttribute(tc_conv_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
+        e = cudaFuncSetAttribute(tc_conv_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
         if (e == cudaSuccess) tc_conv_kernel<kBF16><<<grid, kThreads, pl.smem_bytes, s>>>(tmA, tmB, P);
     } else {
-        e = cudaFuncSetAttribute(tc_conv_i8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
+        e = cudaFuncSetAttribute(tc_conv_i8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
         if (e == cudaSuccess) tc_conv_i8_kernel<<<grid, kThreadsI8, pl.smem_bytes, s>>>(tmA, tmB, P);
     }
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute");

@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define CBS_ABI_VERSION 1
+#define CBS_ABI_VERSION 2
 
 /* Exported symbols (the library is built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -84,9 +84,14 @@ typedef struct cbs_layer_desc {
     int force_variant;   /* -1: choose from prec; else a cbs_variant compatible with prec */
     int force_split_k;   /* 0: choose; else the number of K splits to use (>= 1) */
     int force_block_n;   /* 0: choose; else the N tile width (must be one the variant supports) */
-    int force_block_m;   /* 0: choose; else the M tile height (CUDA-core variant: 64, 128 or 256) */
+    int force_block_m;   /* 0: choose; else the M tile height (CUDA-core variant: 64, 128 or 256;
+                            TF32/BF16 tensor-core variants: 128 or 256) */
     int out_row_stride;  /* NCHW output only: elements between output rows; 0 = OW.
                             Must be >= OW.  Columns OW..stride-1 are never written. */
+    int force_k_group;   /* TF32/BF16: 0 = choose; else K steps per pipeline stage (divides the
+                            layer's K steps) */
+    int force_b_resident;/* TF32/BF16: 0 = choose; 1 = keep weights resident in shared memory;
+                            -1 = stream them with every K step */
 } cbs_layer_desc;
 
 /* A plan: plain data, owned by the caller, filled by cbs_plan. */
@@ -97,6 +102,9 @@ typedef struct cbs_plan_t {
     int block_m, block_n, block_k;  /* CTA tile: output pixels x output channels x K step */
     int stages;             /* shared-memory pipeline depth */
     int split_k;            /* number of K partitions (>= 1) */
+    int k_group;            /* tensor-core variants: K steps carried by one pipeline stage */
+    int b_resident;         /* tensor-core variants: 1 = each CTA loads its weight tile once
+                               and keeps it in shared memory for the whole launch */
     int c_in_pad;           /* channels per input pixel as stored (NHWC tensor-core variants
                                pad C_in to a 16-byte multiple; SIMT: = c_in) */
     int k_gemm;             /* GEMM K = k*k*c_in_pad: length of one packed weight row */

@@ -28,10 +28,10 @@ def test_library_exports_every_declared_symbol(cuda_lib):
 
 
 def test_abi_version_and_struct_sizes(cuda_lib):
-    assert B.cbs_abi_version() == 1
+    assert B.cbs_abi_version() == 2
     plan = B.cbs_plan(make_desc(1, 16, 40, 40, 32, 3, 1))
     assert plan.size == ctypes.sizeof(B.cbs_plan_t)
-    assert plan.abi_version == 1
+    assert plan.abi_version == 2
 
 
 def test_status_strings(cuda_lib):

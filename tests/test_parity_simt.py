@@ -103,7 +103,8 @@ def test_ragged_and_degenerate(cuda_lib, shape):
 def test_small_channel_layers_both_kernels(cuda_lib, variant, layouts):
     """The stem shape through the implicit GEMM and through the direct
     kernel, with ragged sizes and both layouts."""
-    for shape in ((2, 3, 16, 3, 2, 37), (1, 4, 24, 3, 1, 19), (3, 1, 5, 1, 1, 9), (1, 2, 64, 5, 2, 23)):
+    for shape in ((2, 3, 16, 3, 2, 37), (1, 4, 24, 3, 1, 19), (3, 1, 5, 1, 1, 9), (1, 2, 64, 5, 2, 23),
+                  (1, 4, 64, 7, 2, 29)):  # 7x7 x 4 x 64 weights: 49 KB of shared memory
         n, c_in, c_out, k, stride, h = shape
         spec = wl.LayerSpec(c_in, c_out, k, stride, h)
         x, p = wl.layer_inputs(spec, n, layer_index=12)

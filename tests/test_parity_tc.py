@@ -93,6 +93,7 @@ def test_layer_list_batch1(cuda_lib, prec, i):
     (4, 48, 32, 3, 1, 9),      # C_in = 48 (96 B in BF16: 32-byte K steps)
     (1, 3, 16, 3, 2, 34),      # C_in = 3 padded, stride 2, even size
     (2, 8, 16, 3, 1, 1),       # 1x1 image with a 3x3 filter
+    (1, 4, 64, 7, 2, 21),      # direct small-channel kernel, 7x7: 49 KB of weights
 ])
 def test_ragged(cuda_lib, prec, shape):
     n, c_in, c_out, k, stride, h = shape
@@ -136,6 +137,47 @@ def test_batch16_sampled_images(cuda_lib, prec, i):
     sel = np.ascontiguousarray(x[[0, 15]])
     check(y[[0, 15]], spec, sel, p, prec)
     assert np.isfinite(y).all()
+
+
+CONFIGS = [(prec, bm, kg, bres) for prec in ("bf16", "tf32")
+           for bm, kg, bres in ((128, 1, -1), (128, 3, 1), (256, 1, 1), (256, 3, -1), (256, 3, 1), (128, 1, 1))]
+CONFIGS.append(("bf16", 128, 9, -1))   # a whole 3x3 window per stage
+
+
+@pytest.mark.parametrize("prec,bm,kg,bres", CONFIGS)
+@pytest.mark.parametrize("shape", [
+    (2, 32, 64, 3, 1, 20, 64),     # several 256-pixel tiles with a ragged tail
+    (3, 32, 48, 3, 2, 17, 48),     # stride 2, BN = 48 (B tiles not a multiple of 1 KB)
+    (2, 32, 272, 3, 1, 9, 96),     # several N tiles, the last ragged: resident weights pin one N tile per CTA
+])
+def test_tile_height_k_group_resident_weights(cuda_lib, prec, bm, kg, bres, shape):
+    """Every combination of tile height (one or two 128-pixel sub-tiles per
+    TMA box), K steps per pipeline stage and resident or streamed weights.
+    The N tile is forced where shared memory holds it, else chosen."""
+    n, c_in, c_out, k, stride, h, bn = shape
+    spec = wl.LayerSpec(c_in, c_out, k, stride, h)
+    x, p = wl.layer_inputs(spec, n, layer_index=11)
+    kw = dict(force_block_m=bm, force_k_group=kg, force_b_resident=bres)
+    try:
+        B.cbs_plan(make_desc(n, c_in, h, h, c_out, k, stride, prec=PRECS[prec], force_block_n=bn, **kw))
+        kw["force_block_n"] = bn
+    except B.CbsError as e:
+        assert e.status == B.CBS_ERR_UNSUPPORTED
+    y, layer = run_tc(spec, x, p, PRECS[prec], **kw)
+    pl = layer.plan
+    assert (pl.block_m, pl.k_group, pl.b_resident) == (bm, kg, 1 if bres > 0 else 0)
+    check(y, spec, x, p, prec, (shape, bm, kg, bres, pl.block_n, pl.stages))
+
+
+@pytest.mark.parametrize("prec", ["bf16", "tf32"])
+@pytest.mark.parametrize("bm,bres", [(128, -1), (128, 1), (256, -1), (256, 1)])
+def test_pointwise_tall_tiles(cuda_lib, prec, bm, bres):
+    """1x1 layer (A loaded as a 2-D tile of 128 or 256 rows), ragged pixel count."""
+    spec = wl.LayerSpec(64, 96, 1, 1, 13)
+    x, p = wl.layer_inputs(spec, 4, layer_index=12)
+    y, layer = run_tc(spec, x, p, PRECS[prec], force_block_m=bm, force_b_resident=bres, force_k_group=1)
+    assert (layer.plan.block_m, layer.plan.b_resident) == (bm, 1 if bres > 0 else 0)
+    check(y, spec, x, p, prec, (bm, bres))
 
 
 def test_no_timeout_reported(cuda_lib):
