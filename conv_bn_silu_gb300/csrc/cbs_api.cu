@@ -257,12 +257,16 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
 
     if (variant == CBS_VARIANT_STEM) {
         const int cout_t = D.c_out <= 16 ? 16 : (D.c_out <= 32 ? 32 : 64);
-        p.block_m = 256;  // output pixels per CTA, one per thread
+        // pixels per thread, as the direct kernel picks them (k_stem.cu)
+        const int px_per_thread = (D.prec == CBS_FP32 || D.prec == CBS_TF32) ? 1
+                                  : D.prec == CBS_INT8 ? (cout_t == 16 ? 4 : (cout_t == 32 ? 2 : 1))
+                                                       : (cout_t <= 32 ? 2 : 1);
+        p.block_m = 256 * px_per_thread;  // output pixels per CTA: 256 threads, px_per_thread each
         p.block_n = cout_t;
         p.block_k = D.k * D.k * p.c_in_pad;
         p.stages = 1;
         p.split_k = 1;
-        p.m_tiles = (int)((M + 255) / 256);
+        p.m_tiles = (int)((M + p.block_m - 1) / p.block_m);
         p.n_tiles = 1;
         p.grid_ctas = p.m_tiles;
         p.threads = 256;

@@ -28,117 +28,20 @@ __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return _
 template <>
 __device__ __forceinline__ float to_f<int8_t>(int8_t v) { return (float)v; }
 
-// KIND: 0 float in/out, 1 bf16 in/out, 2 int8 in/out (requantised).
-template <int KIND, int COUT, bool IN_NHWC, bool OUT_NHWC>
-__global__ void __launch_bounds__(256) stem_kernel(const StemLaunch a) {
-    using Tin = typename std::conditional<KIND == 0, float, typename std::conditional<KIND == 1, __nv_bfloat16, int8_t>::type>::type;
-    extern __shared__ float4 wsm4[];  // [KK * c_pad][COUT] floats
-    float *wsm = reinterpret_cast<float *>(wsm4);
-    const int KK = a.KS * a.KS;
-    const int kpad = KK * a.c_pad;
-    // Folded weights: packed [C_out][KK * c_pad] (float, or bf16 holding
-    // bf16 values / int8 codes) -> [tap * c_pad + ci][co] as float.
-    for (int idx = threadIdx.x; idx < kpad * COUT; idx += blockDim.x) {
-        const int co = idx / kpad, k = idx - co * kpad;
-        float v = 0.0f;
-        if (co < a.Cout) {
-            if (KIND == 0)
-                v = static_cast<const float *>(a.w)[(size_t)co * kpad + k];
-            else
-                v = __bfloat162float(static_cast<const __nv_bfloat16 *>(a.w)[(size_t)co * kpad + k]);
-        }
-        wsm[k * COUT + co] = v;
-    }
-    __syncthreads();
+// Output pixels per thread: every weight read from shared memory feeds
+// P x 4 multiply-adds.  Measured on GB300 for the 3 -> 16 stem: FP32 is
+// fastest at one pixel per thread (more warps hide the scalar NCHW loads),
+// BF16 at two, INT8 (integer multiply-adds) at four.
+template <int KIND, int COUT>
+struct StemTile {
+    static constexpr int P = KIND == 0 ? 1 : KIND == 1 ? (COUT <= 32 ? 2 : 1) : (COUT <= 16 ? 4 : (COUT <= 32 ? 2 : 1));
+};
 
-    const long long pix = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long total = (long long)a.N * a.OH * a.OW;
-    if (pix >= total) return;
-    const int ohw = a.OH * a.OW;
-    const int img = (int)(pix / ohw);
-    const int rem = (int)(pix - (long long)img * ohw);
-    const int oh = rem / a.OW, ow = rem - (rem / a.OW) * a.OW;
-    const Tin *x = static_cast<const Tin *>(a.x);
-
-    float accf[COUT];
-    int acci[COUT];
-#pragma unroll
-    for (int c = 0; c < COUT; ++c) { accf[c] = 0.0f; acci[c] = 0; }
-
-    const bool vec_in = IN_NHWC && a.c_pad == 4;  // one 4-channel vector load per tap
-    for (int r = 0; r < a.KS; ++r) {
-        const int ih = oh * a.stride - a.pad + r;
-        if (ih < 0 || ih >= a.H) continue;
-        for (int s = 0; s < a.KS; ++s) {
-            const int iw = ow * a.stride - a.pad + s;
-            if (iw < 0 || iw >= a.W) continue;
-            const float *wt = wsm + (r * a.KS + s) * a.c_pad * COUT;
-            Tin xv[4];
-            if (vec_in) {
-                const Tin *src = x + (((size_t)img * a.H + ih) * a.W + iw) * 4;
-                if (KIND == 0) {
-                    const float4 q = *reinterpret_cast<const float4 *>(src);
-                    xv[0] = q.x; xv[1] = q.y; xv[2] = q.z; xv[3] = q.w;
-                } else if (KIND == 1) {
-                    const uint2 q = *reinterpret_cast<const uint2 *>(src);
-                    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&q.x);
-                    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&q.y);
-                    xv[0] = lo.x; xv[1] = lo.y; xv[2] = hi.x; xv[3] = hi.y;
-                } else {
-                    const int q = *reinterpret_cast<const int *>(src);
-                    xv[0] = (int8_t)(q & 0xff); xv[1] = (int8_t)((q >> 8) & 0xff);
-                    xv[2] = (int8_t)((q >> 16) & 0xff); xv[3] = (int8_t)(q >> 24);
-                }
-            }
-#pragma unroll
-            for (int ci = 0; ci < 4; ++ci) {
-                if (ci >= a.C) break;
-                Tin v;
-                if (vec_in)
-                    v = xv[ci];
-                else if (IN_NHWC)
-                    v = x[(((size_t)img * a.H + ih) * a.W + iw) * a.c_pad + ci];
-                else
-                    v = x[(((size_t)img * a.C + ci) * a.H + ih) * a.W + iw];
-                const float4 *w4 = reinterpret_cast<const float4 *>(wt + ci * COUT);
-                if (KIND == 2) {
-                    const int xi = (int)v;
-#pragma unroll
-                    for (int c = 0; c < COUT / 4; ++c) {
-                        const float4 w = w4[c];
-                        acci[4 * c] += xi * (int)w.x; acci[4 * c + 1] += xi * (int)w.y;
-                        acci[4 * c + 2] += xi * (int)w.z; acci[4 * c + 3] += xi * (int)w.w;
-                    }
-                } else {
-                    const float xf = to_f<Tin>(v);
-#pragma unroll
-                    for (int c = 0; c < COUT / 4; ++c) {
-                        const float4 w = w4[c];
-                        accf[4 * c] = fmaf(xf, w.x, accf[4 * c]);
-                        accf[4 * c + 1] = fmaf(xf, w.y, accf[4 * c + 1]);
-                        accf[4 * c + 2] = fmaf(xf, w.z, accf[4 * c + 2]);
-                        accf[4 * c + 3] = fmaf(xf, w.w, accf[4 * c + 3]);
-                    }
-                }
-            }
-        }
-    }
-
-    // Epilogue: + bias, SiLU (or the INT8 requantisation), then stores; an
-    // NHWC pixel whose channel count is the register tile's is written with
-    // 16-byte vector stores.
-    float of[COUT];
-    int oq[COUT];
-#pragma unroll
-    for (int c = 0; c < COUT; ++c) {
-        const bool live = c < a.Cout;
-        if (KIND == 2) {
-            const int acc = acci[c] + (live ? static_cast<const int32_t *>(a.bias)[c] : 0);
-            oq[c] = live ? requant_i8(acc, a.m_c[c], a.inv_s_y) : 0;
-        } else {
-            of[c] = silu_fast(accf[c] + (live ? static_cast<const float *>(a.bias)[c] : 0.0f));
-        }
-    }
+// Stores one output pixel: 16-byte vectors when an NHWC pixel holds exactly
+// the register tile's channels, else one element per channel.
+template <int KIND, int COUT, bool OUT_NHWC>
+__device__ __forceinline__ void store_pixel(const StemLaunch &a, long long pix, int img, int oh, int ow,
+                                            const float (&of)[COUT], const int (&oq)[COUT]) {
     if (OUT_NHWC && a.Cout == COUT) {
         if (KIND == 0) {
             float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.y) + (size_t)pix * COUT);
@@ -186,10 +89,164 @@ __global__ void __launch_bounds__(256) stem_kernel(const StemLaunch a) {
     }
 }
 
+// KIND: 0 float in/out, 1 bf16 in/out, 2 int8 in/out (requantised).
+template <int KIND, int COUT, bool IN_NHWC, bool OUT_NHWC>
+__global__ void __launch_bounds__(256) stem_kernel(const StemLaunch a) {
+    using Tin = typename std::conditional<KIND == 0, float, typename std::conditional<KIND == 1, __nv_bfloat16, int8_t>::type>::type;
+    constexpr int P = StemTile<KIND, COUT>::P;
+    extern __shared__ float4 wsm4[];  // [KK * c_pad][COUT] floats
+    float *wsm = reinterpret_cast<float *>(wsm4);
+    const int KK = a.KS * a.KS;
+    const int kpad = KK * a.c_pad;
+    // Folded weights: packed [C_out][KK * c_pad] (float, or bf16 holding
+    // bf16 values / int8 codes) -> [tap * c_pad + ci][co] as float.
+    for (int idx = threadIdx.x; idx < kpad * COUT; idx += blockDim.x) {
+        const int co = idx / kpad, k = idx - co * kpad;
+        float v = 0.0f;
+        if (co < a.Cout) {
+            if (KIND == 0)
+                v = static_cast<const float *>(a.w)[(size_t)co * kpad + k];
+            else
+                v = __bfloat162float(static_cast<const __nv_bfloat16 *>(a.w)[(size_t)co * kpad + k]);
+        }
+        wsm[k * COUT + co] = v;
+    }
+    __syncthreads();
+
+    const long long total = (long long)a.N * a.OH * a.OW;
+    const long long pix0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * P;
+    if (pix0 >= total) return;
+    const int ohw = a.OH * a.OW;
+    int img[P], oh[P], ow[P];
+    bool live[P];
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+        const long long pix = pix0 + j;
+        live[j] = pix < total;
+        const long long pc = live[j] ? pix : pix0;
+        img[j] = (int)(pc / ohw);
+        const int rem = (int)(pc - (long long)img[j] * ohw);
+        oh[j] = rem / a.OW;
+        ow[j] = rem - oh[j] * a.OW;
+    }
+    const Tin *x = static_cast<const Tin *>(a.x);
+
+    float accf[P][COUT];
+    int acci[P][COUT];
+#pragma unroll
+    for (int j = 0; j < P; ++j)
+#pragma unroll
+        for (int c = 0; c < COUT; ++c) { accf[j][c] = 0.0f; acci[j][c] = 0; }
+
+    const bool vec_in = IN_NHWC && a.c_pad == 4;  // one 4-channel vector load per tap
+    for (int r = 0; r < a.KS; ++r) {
+        for (int s = 0; s < a.KS; ++s) {
+            const float *wt = wsm + (r * a.KS + s) * a.c_pad * COUT;
+            // The tap's input channels of each pixel (zero outside the image).
+            float xf[P][4];
+            int xi[P][4];
+#pragma unroll
+            for (int j = 0; j < P; ++j) {
+                const int ih = oh[j] * a.stride - a.pad + r;
+                const int iw = ow[j] * a.stride - a.pad + s;
+                const bool in = live[j] && ih >= 0 && ih < a.H && iw >= 0 && iw < a.W;
+                Tin xv[4];
+#pragma unroll
+                for (int ci = 0; ci < 4; ++ci) xv[ci] = Tin(0);
+                if (in) {
+                    if (vec_in) {
+                        const Tin *src = x + (((size_t)img[j] * a.H + ih) * a.W + iw) * 4;
+                        if (KIND == 0) {
+                            const float4 q = *reinterpret_cast<const float4 *>(src);
+                            xv[0] = q.x; xv[1] = q.y; xv[2] = q.z; xv[3] = q.w;
+                        } else if (KIND == 1) {
+                            const uint2 q = *reinterpret_cast<const uint2 *>(src);
+                            const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&q.x);
+                            const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&q.y);
+                            xv[0] = lo.x; xv[1] = lo.y; xv[2] = hi.x; xv[3] = hi.y;
+                        } else {
+                            const int q = *reinterpret_cast<const int *>(src);
+                            xv[0] = (int8_t)(q & 0xff); xv[1] = (int8_t)((q >> 8) & 0xff);
+                            xv[2] = (int8_t)((q >> 16) & 0xff); xv[3] = (int8_t)(q >> 24);
+                        }
+                    } else {
+#pragma unroll
+                        for (int ci = 0; ci < 4; ++ci) {
+                            if (ci >= a.C) break;
+                            xv[ci] = IN_NHWC ? x[(((size_t)img[j] * a.H + ih) * a.W + iw) * a.c_pad + ci]
+                                             : x[(((size_t)img[j] * a.C + ci) * a.H + ih) * a.W + iw];
+                        }
+                    }
+                }
+#pragma unroll
+                for (int ci = 0; ci < 4; ++ci) {
+                    xf[j][ci] = to_f<Tin>(xv[ci]);
+                    xi[j][ci] = (int)xv[ci];
+                }
+            }
+#pragma unroll
+            for (int ci = 0; ci < 4; ++ci) {
+                if (ci >= a.C) break;
+                const float4 *w4 = reinterpret_cast<const float4 *>(wt + ci * COUT);
+#pragma unroll
+                for (int c = 0; c < COUT / 4; ++c) {
+                    const float4 w = w4[c];
+                    if (KIND == 2) {
+                        const int w0 = (int)w.x, w1 = (int)w.y, w2 = (int)w.z, w3 = (int)w.w;
+#pragma unroll
+                        for (int j = 0; j < P; ++j) {
+                            acci[j][4 * c] += xi[j][ci] * w0; acci[j][4 * c + 1] += xi[j][ci] * w1;
+                            acci[j][4 * c + 2] += xi[j][ci] * w2; acci[j][4 * c + 3] += xi[j][ci] * w3;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < P; ++j) {
+                            accf[j][4 * c] = fmaf(xf[j][ci], w.x, accf[j][4 * c]);
+                            accf[j][4 * c + 1] = fmaf(xf[j][ci], w.y, accf[j][4 * c + 1]);
+                            accf[j][4 * c + 2] = fmaf(xf[j][ci], w.z, accf[j][4 * c + 2]);
+                            accf[j][4 * c + 3] = fmaf(xf[j][ci], w.w, accf[j][4 * c + 3]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // Epilogue: + bias, SiLU (or the INT8 requantisation), then stores; an
+    // NHWC pixel whose channel count is the register tile's is written with
+    // 16-byte vector stores (the P pixels of a thread are contiguous).
+    float bias_f[COUT];
+    int bias_i[COUT];
+    float mc[COUT];
+#pragma unroll
+    for (int c = 0; c < COUT; ++c) {
+        const bool lc = c < a.Cout;
+        bias_f[c] = (KIND != 2 && lc) ? static_cast<const float *>(a.bias)[c] : 0.0f;
+        bias_i[c] = (KIND == 2 && lc) ? static_cast<const int32_t *>(a.bias)[c] : 0;
+        mc[c] = (KIND == 2 && lc) ? a.m_c[c] : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+        if (!live[j]) continue;
+        const long long pix = pix0 + j;
+        float of[COUT];
+        int oq[COUT];
+#pragma unroll
+        for (int c = 0; c < COUT; ++c) {
+            if (KIND == 2)
+                oq[c] = c < a.Cout ? requant_i8(acci[j][c] + bias_i[c], mc[c], a.inv_s_y) : 0;
+            else
+                of[c] = silu_fast(accf[j][c] + bias_f[c]);
+        }
+        store_pixel<KIND, COUT, OUT_NHWC>(a, pix, img[j], oh[j], ow[j], of, oq);
+    }
+}
+
 template <int KIND, int COUT>
 cudaError_t launch_kind(const StemLaunch &L, cudaStream_t s) {
     const long long total = (long long)L.N * L.OH * L.OW;
-    const int grid = (int)((total + 255) / 256);
+    constexpr int P = StemTile<KIND, COUT>::P;
+    const int grid = (int)((total + 256 * P - 1) / (256 * P));
     const int smem = L.KS * L.KS * L.c_pad * COUT * (int)sizeof(float);
     if (smem > 48 * 1024) {  // 7x7 filters with 64 output channels need 49 KB of weights
         if (smem > kMaxDynSmem) return cudaErrorInvalidValue;

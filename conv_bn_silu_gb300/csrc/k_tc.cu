@@ -35,6 +35,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "cbs_internal.cuh"
@@ -91,7 +92,14 @@ struct TcParams {
     int b_tile_stride;         // bytes between B tiles (1024-aligned)
     int b_region;              // bytes of the resident weight region (0 if none)
     int a_box_bytes;           // one A box: 128 * mmul * RB
+    int st_mode;               // 1: NHWC output staged in shared memory and written by TMA stores
+    int cbw;                   // columns of one staged store block (128 bytes of output)
+    int stg_bytes_total;       // bytes of the staging region (8 warps x 4 KB) when st_mode
+    int bias_smem;             // 1: the folded bias is copied to shared memory at start
+    int bias_bytes_smem;       // bytes reserved for it
 };
+
+constexpr int kStageBlockBytes = 4096;            // one warp's staged store block: 32 rows x 128 B
 
 // SiLU(z) = z * sigmoid(z) = h + h * tanh(h) with h = z / 2: one MUFU
 // operation per output (tanh.approx, relative error ~2^-11, far below the
@@ -104,21 +112,62 @@ __device__ __forceinline__ float silu_fast(float z) {
 }
 
 // Bias + SiLU + store of 16 consecutive output channels of one pixel.
-template <int KIND>
-__device__ __forceinline__ void epi_store16(const TcParams &p, int m, int img, int oh, int ow, int nbase,
-                                            const uint32_t (&v)[16]) {
-    float bv[16];
-    const bool full = nbase + 16 <= p.C_out;
-    if (full) {
+// The 16 folded-bias values of channels nbase.. (zero past C_out).
+__device__ __forceinline__ void load_bias16(const TcParams &p, const float *bias, int nbase, float (&bv)[16]) {
+    if (nbase + 16 <= p.C_out) {
 #pragma unroll
         for (int jj = 0; jj < 16; jj += 4) {
-            const float4 b4 = __ldg(reinterpret_cast<const float4 *>(p.bias + nbase + jj));
+            const float4 b4 = *reinterpret_cast<const float4 *>(bias + nbase + jj);
             bv[jj] = b4.x; bv[jj + 1] = b4.y; bv[jj + 2] = b4.z; bv[jj + 3] = b4.w;
         }
     } else {
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) bv[jj] = nbase + jj < p.C_out ? __ldg(p.bias + nbase + jj) : 0.0f;
+        for (int jj = 0; jj < 16; ++jj) bv[jj] = nbase + jj < p.C_out ? bias[nbase + jj] : 0.0f;
     }
+}
+
+// Bias + SiLU of 16 accumulator columns, written into row `row` of a staged
+// store block (32 rows x 128 bytes, 128-byte swizzle: 16-byte chunk j of a
+// row sits at chunk j ^ (row % 8)).  c is the block column of the first value.
+template <int KIND>
+__device__ __forceinline__ void stage16(uint32_t blk, int row, int c, const float (&bv)[16], const uint32_t (&v)[16]) {
+    float o[16];
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) o[jj] = silu_fast(__uint_as_float(v[jj]) + bv[jj]);
+    const uint32_t rbase = blk + (uint32_t)row * 128u;
+    if (KIND == kTF32) {
+        const int j0 = c >> 2;   // 4 floats per chunk
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t a = rbase + ((uint32_t)((j0 + q) ^ (row & 7)) << 4);
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(o[4 * q]), "f"(o[4 * q + 1]),
+                         "f"(o[4 * q + 2]), "f"(o[4 * q + 3])
+                         : "memory");
+        }
+    } else {
+        const int j0 = c >> 3;   // 8 bf16 per chunk
+        uint32_t w[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * jj], o[2 * jj + 1]);
+            w[jj] = *reinterpret_cast<uint32_t *>(&h2);
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const uint32_t a = rbase + ((uint32_t)((j0 + q) ^ (row & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[4 * q]), "r"(w[4 * q + 1]),
+                         "r"(w[4 * q + 2]), "r"(w[4 * q + 3])
+                         : "memory");
+        }
+    }
+}
+
+template <int KIND>
+__device__ __forceinline__ void epi_store16(const TcParams &p, const float *bias, int m, int img, int oh, int ow,
+                                            int nbase, const uint32_t (&v)[16]) {
+    float bv[16];
+    const bool full = nbase + 16 <= p.C_out;
+    load_bias16(p, bias, nbase, bv);
     float o[16];
 #pragma unroll
     for (int jj = 0; jj < 16; ++jj) o[jj] = silu_fast(__uint_as_float(v[jj]) + bv[jj]);
@@ -191,7 +240,8 @@ __device__ __forceinline__ bool aborted(int *abort_flag) { return *(volatile int
 // tile j+1.
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
-tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmY, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Buffers start on a 1024-byte boundary of the shared window (the
     // swizzle atoms of TMA and of the MMA descriptors are address based).
@@ -199,11 +249,15 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t *base_ptr = smem_raw + (base - raw_addr);
     const int S = p.stages;
-    // [resident B][S stages][barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain, b_full]
+    // [resident B][S stages][store staging][bias][barriers: full[S], empty[S],
+    //  acc_full[2], acc_empty[2], drain, b_full]
     const uint32_t b_base = base;
     const uint32_t stage0 = base + p.b_region;
-    const uint32_t bars = stage0 + S * p.stage_bytes;
-    uint64_t *bar_ptr = reinterpret_cast<uint64_t *>(base_ptr + p.b_region + S * p.stage_bytes);
+    const uint32_t stg_base = stage0 + S * p.stage_bytes;
+    float *bias_sm = reinterpret_cast<float *>(base_ptr + p.b_region + S * p.stage_bytes + p.stg_bytes_total);
+    const uint32_t bars = stg_base + p.stg_bytes_total + p.bias_bytes_smem;
+    uint64_t *bar_ptr = reinterpret_cast<uint64_t *>(base_ptr + p.b_region + S * p.stage_bytes + p.stg_bytes_total +
+                                                     p.bias_bytes_smem);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_ptr + 2 * S + 6);
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
@@ -231,12 +285,15 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ptx::mbar_init(acce_bar(a), kEpiWarps);   // one arrive per epilogue warp
         }
         ptx::mbar_init(drain_bar, 1);
-        ptx::mbar_init(bfull_bar, p.nprod);           // one arrive per producer warp
+        ptx::mbar_init(bfull_bar, 1);                 // producer warp 0 loads the resident weights
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmB);
+        if (p.st_mode) ptx::prefetch_tmap(&tmY);
     }
+    if (p.bias_smem)
+        for (int i = threadIdx.x; i < p.C_out; i += blockDim.x) bias_sm[i] = p.bias[i];
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), p.tmem_cols);
         ptx::tmem_relinquish();
@@ -245,19 +302,23 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    const float *bias = p.bias_smem ? bias_sm : p.bias;
 
     int last_g = -1;  // producer: last stage (global count) whose loads this warp issued
     bool b_issued = false;
     if (warp < kMaxProducers) {
-        if (lane == 0 && warp < p.nprod) {
-            if (p.b_res && blockIdx.x < num_tiles) {
+        // A TMA box takes an issuing thread ~570 cycles whatever its size,
+        // and lanes issue in parallel: lane l of a producer warp issues box l
+        // of the stage (A boxes first, then B boxes).
+        const int nbox = p.kg * (p.b_res ? 1 : 2);
+        if (warp < p.nprod) {
+            if (p.b_res && warp == 0 && blockIdx.x < num_tiles) {
                 // This CTA's N tile never changes: load its weight tile once.
                 int m0, n0;
                 tile_coords(blockIdx.x, p.n_tiles, tile_m, m0, n0, p.BN);
-                int mine = 0;
-                for (int i = warp; i < nk; i += p.nprod) ++mine;
-                ptx::mbar_arrive_expect_tx(bfull_bar, (uint32_t)(mine * b_step_bytes));
-                for (int i = warp; i < nk; i += p.nprod) {
+                if (lane == 0) ptx::mbar_arrive_expect_tx(bfull_bar, (uint32_t)(nk * b_step_bytes));
+                __syncwarp();
+                for (int i = lane; i < nk; i += 32) {
                     const int tap = i / p.cblocks, cb = i - tap * p.cblocks;
                     ptx::tma_load_2d(b_base + i * p.b_tile_stride, &tmB, bfull_bar, tap * p.c_in_pad + cb * p.CB, n0);
                 }
@@ -279,27 +340,36 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 for (int st = 0; st < nstage; ++st, ++g) {
                     if (g % p.nprod != warp) continue;
                     const int s = g % S, u = g / S;
-                    if (!ptx::mbar_wait_bounded(empty_bar(s), (u & 1) ^ 1, kWaitLimitNs)) {
-                        abort_now(p, abort_flag);
+                    bool got = true;
+                    if (lane == 0) got = ptx::mbar_wait_bounded(empty_bar(s), (u & 1) ^ 1, kWaitLimitNs) && !aborted(abort_flag);
+                    got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                    if (!got) {
+                        if (lane == 0 && !aborted(abort_flag)) abort_now(p, abort_flag);
                         ok = false;
                         break;
                     }
-                    if (aborted(abort_flag)) { ok = false; break; }
                     const uint32_t sbase = stage0 + s * p.stage_bytes;
-                    ptx::mbar_arrive_expect_tx(full_bar(s), (uint32_t)(p.kg * (p.a_box_bytes + (p.b_res ? 0 : b_step_bytes))));
-                    for (int kk = 0; kk < p.kg; ++kk) {
+                    if (lane == 0)
+                        ptx::mbar_arrive_expect_tx(full_bar(s),
+                                                   (uint32_t)(p.kg * (p.a_box_bytes + (p.b_res ? 0 : b_step_bytes))));
+                    __syncwarp();
+                    if (lane < nbox) {
+                        const bool is_a = lane < p.kg;
+                        const int kk = is_a ? lane : lane - p.kg;
                         const int i = st * p.kg + kk;
                         const int tap = i / p.cblocks, cb = i - tap * p.cblocks;
-                        const int r = tap / p.ks, tt = tap - r * p.ks;
-                        const uint32_t a_dst = sbase + kk * p.a_box_bytes;
-                        if (p.im2col)
-                            ptx::tma_load_im2col_4d(a_dst, &tmA, full_bar(s), cb * p.CB, wc, hc, img, (uint16_t)tt,
-                                                    (uint16_t)r);
-                        else
-                            ptx::tma_load_2d(a_dst, &tmA, full_bar(s), cb * p.CB, m0);
-                        if (!p.b_res)
+                        if (is_a) {
+                            const uint32_t a_dst = sbase + kk * p.a_box_bytes;
+                            const int r = tap / p.ks, tt = tap - r * p.ks;
+                            if (p.im2col)
+                                ptx::tma_load_im2col_4d(a_dst, &tmA, full_bar(s), cb * p.CB, wc, hc, img, (uint16_t)tt,
+                                                        (uint16_t)r);
+                            else
+                                ptx::tma_load_2d(a_dst, &tmA, full_bar(s), cb * p.CB, m0);
+                        } else {
                             ptx::tma_load_2d(sbase + p.kg * p.a_box_bytes + kk * p.b_tile_stride, &tmB, full_bar(s),
                                              tap * p.c_in_pad + cb * p.CB, n0);
+                        }
                     }
                     last_g = g;
                 }
@@ -390,16 +460,52 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 ow = rem - oh * p.OW;
             }
             const uint32_t t_row = tmem_base + (uint32_t)(acc * p.acc_stride + sub * p.bnp) + ((uint32_t)(32 * q) << 16);
-            for (int c0 = cstart; c0 < p.BN; c0 += 2 * cstep) {
-                // Two loads, one wait: 32 columns in flight per thread.
-                uint32_t v0[16], v1[16];
-                const bool two = c0 + cstep < p.BN;
-                ptx::tmem_ld16(t_row + (uint32_t)c0, v0);
-                if (two) ptx::tmem_ld16(t_row + (uint32_t)(c0 + cstep), v1);
-                ptx::tmem_ld_wait();
-                if (m < p.M) {
-                    if (n0 + c0 < p.C_out) epi_store16<KIND>(p, m, img, oh, ow, n0 + c0, v0);
-                    if (two && n0 + c0 + cstep < p.C_out) epi_store16<KIND>(p, m, img, oh, ow, n0 + c0 + cstep, v1);
+            if (p.st_mode) {
+                // Staged NHWC store: the warp's 32 pixels x one block of
+                // 128 output bytes go to shared memory, then out with one TMA
+                // store (coalesced, asynchronous; rows past M and columns
+                // past C_out are clipped by the tensor bounds).
+                const uint32_t blk = stg_base + (uint32_t)((warp - kEpiFirst) * kStageBlockBytes);
+                const int nblk = (p.BN + p.cbw - 1) / p.cbw;
+                for (int b = p.mmul == 2 ? 0 : h; b < nblk; b += p.mmul == 2 ? 1 : 2) {
+                    const int bc0 = b * p.cbw;
+                    const int bcols = p.BN - bc0 < p.cbw ? p.BN - bc0 : p.cbw;
+                    if (lane == 0) ptx::bulk_wait_read0();   // the block's previous store has read it
+                    __syncwarp();
+                    for (int c = 0; c < bcols; c += 32) {
+                        uint32_t v0[16], v1[16];
+                        const bool two = c + 16 < bcols;
+                        ptx::tmem_ld16(t_row + (uint32_t)(bc0 + c), v0);
+                        if (two) ptx::tmem_ld16(t_row + (uint32_t)(bc0 + c + 16), v1);
+                        ptx::tmem_ld_wait();
+                        float bv[16];
+                        load_bias16(p, bias, n0 + bc0 + c, bv);
+                        stage16<KIND>(blk, lane, c, bv, v0);
+                        if (two) {
+                            load_bias16(p, bias, n0 + bc0 + c + 16, bv);
+                            stage16<KIND>(blk, lane, c + 16, bv, v1);
+                        }
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(&tmY, blk, n0 + bc0, m0 + sub * kBM + 32 * q);
+                        ptx::bulk_commit();
+                    }
+                }
+            } else {
+                for (int c0 = cstart; c0 < p.BN; c0 += 2 * cstep) {
+                    // Two loads, one wait: 32 columns in flight per thread.
+                    uint32_t v0[16], v1[16];
+                    const bool two = c0 + cstep < p.BN;
+                    ptx::tmem_ld16(t_row + (uint32_t)c0, v0);
+                    if (two) ptx::tmem_ld16(t_row + (uint32_t)(c0 + cstep), v1);
+                    ptx::tmem_ld_wait();
+                    if (m < p.M) {
+                        if (n0 + c0 < p.C_out) epi_store16<KIND>(p, bias, m, img, oh, ow, n0 + c0, v0);
+                        if (two && n0 + c0 + cstep < p.C_out)
+                            epi_store16<KIND>(p, bias, m, img, oh, ow, n0 + c0 + cstep, v1);
+                    }
                 }
             }
             // This accumulator has been read: hand it back to the MMA issuer.
@@ -407,6 +513,9 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(acce_bar(acc));
         }
+        // Staged stores must finish reading shared memory (and land) before
+        // the CTA exits.
+        if (p.st_mode && lane == 0) ptx::bulk_wait0();
     }
 
     // ---- teardown: all MMAs complete, loads landed, TMEM freed.
@@ -798,8 +907,22 @@ double tc_mma_clk(int N, bool tf32) {
     return c > 95.0 ? c : 95.0;
 }
 
+// Output bytes per element of a TF32/BF16 layer (float or bfloat16).
+int tc_out_bytes(bool tf32) { return tf32 ? 4 : 2; }
+
+// NHWC output goes through staged TMA stores when the output rows are
+// 16-byte multiples and no store block can spill into another CTA's N tile.
+int tc_store_mode(const cbs_layer_desc &d, int BN, int n_tiles, bool tf32) {
+    const int eb = tc_out_bytes(tf32);
+    const int cbw = 128 / eb;
+    if (d.out_layout != CBS_NHWC || (d.c_out * eb) % 16 != 0) return 0;
+    return (n_tiles == 1 || BN % cbw == 0) ? 1 : 0;
+}
+
+int tc_bias_smem_bytes(const cbs_layer_desc &d) { return d.c_out <= 1024 ? (d.c_out * 4 + 15) / 16 * 16 : 0; }
+
 struct TcConfig {
-    int BN, mmul, b_res, kg, stages, nprod;
+    int BN, mmul, b_res, kg, stages, nprod, st_mode, extra_bytes;
     int m_tiles, n_tiles, grid;
     int stage_bytes, b_region, b_tile_stride, a_box_bytes;
     double cycles;
@@ -809,19 +932,22 @@ struct TcConfig {
 bool tc_config(const cbs_layer_desc &d, long long M, int RB, int ksteps, bool tf32, int BN, int mmul, int b_res,
                int kg, TcConfig &c) {
     c.BN = BN; c.mmul = mmul; c.b_res = b_res; c.kg = kg;
+    if (kg * (b_res ? 1 : 2) > 32) return false;   // one issuing lane per box of a stage
     c.a_box_bytes = kBM * mmul * RB;
     const int b_bytes = BN * RB;
     c.b_tile_stride = (b_bytes + 1023) / 1024 * 1024;
     c.b_region = b_res ? ksteps * c.b_tile_stride : 0;
     c.stage_bytes = kg * c.a_box_bytes + (b_res ? 0 : kg * c.b_tile_stride);
+    c.m_tiles = (int)((M + kBM * mmul - 1) / (kBM * mmul));
+    c.n_tiles = (d.c_out + BN - 1) / BN;
+    c.st_mode = tc_store_mode(d, BN, c.n_tiles, tf32);
+    c.extra_bytes = (c.st_mode ? kEpiWarps * kStageBlockBytes : 0) + tc_bias_smem_bytes(d);
     const int barrier_bytes = 8 * (2 * 16 + 6) + 16;
-    int cap = (kSmemBudget - c.b_region - barrier_bytes) / c.stage_bytes;
+    int cap = (kSmemBudget - c.b_region - c.extra_bytes - barrier_bytes) / c.stage_bytes;
     if (cap > 16) cap = 16;
     if (cap < 2) return false;
     c.stages = cap >= 4 ? cap - cap % 4 : cap;
     c.nprod = tc_producers(c.stages);
-    c.m_tiles = (int)((M + kBM * mmul - 1) / (kBM * mmul));
-    c.n_tiles = (d.c_out + BN - 1) / BN;
     const long long tiles = (long long)c.m_tiles * c.n_tiles;
     if (b_res && c.n_tiles > 1) {
         // Every CTA keeps one N tile: the grid is a multiple of n_tiles.
@@ -836,12 +962,14 @@ bool tc_config(const cbs_layer_desc &d, long long M, int RB, int ksteps, bool tf
     const double mma = tpc * ((double)ksteps * kslices * mmul * tc_mma_clk(BN, tf32) + (double)(ksteps / kg) * kClkPerStageWait);
     const double boxes = tpc * ksteps * (b_res ? 1.0 : 2.0) + (b_res ? (double)ksteps : 0.0);
     const double bytes = tpc * ksteps * (double)(c.a_box_bytes + (b_res ? 0 : b_bytes)) + (b_res ? (double)ksteps * b_bytes : 0.0);
-    const double t_box = boxes * kClkPerBox / c.nprod, t_fill = bytes / kFillBytesPerClk;
+    // Boxes of one stage go out from parallel lanes; the SM's TMA engine
+    // still takes ~140 cycles per box.
+    const double t_box = boxes * 140.0, t_fill = bytes / kFillBytesPerClk;
     const double tma = t_box > t_fill ? t_box : t_fill;
     // Epilogue: one thread per pixel and 16-column group; eight warps cover
     // two sub-tiles, or split one sub-tile's columns.
     const double vals = mmul == 2 ? (double)BN : 0.5 * BN;
-    const double epi = tpc * (250.0 + 45.0 * vals);
+    const double epi = tpc * (250.0 + (c.st_mode ? 25.0 : 45.0) * vals);
     double cyc = mma > tma ? mma : tma;
     if (epi > cyc) cyc = epi;
     // Pipeline fill: the first stage's loads (and a resident weight tile)
@@ -966,7 +1094,7 @@ cbs_status plan_tc(cbs_plan_t &p) {
     p.n_tiles = best.n_tiles;
     p.grid_ctas = best.grid;
     p.threads = kThreads;
-    p.smem_bytes = 1024 + best.b_region + best.stages * best.stage_bytes + 8 * (2 * best.stages + 6) + 16;
+    p.smem_bytes = 1024 + best.b_region + best.stages * best.stage_bytes + best.extra_bytes + 8 * (2 * best.stages + 6) + 16;
     return CBS_OK;
 }
 
@@ -1019,7 +1147,14 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     } else {
         P.nprod = tc_producers(pl.stages);
         P.stage_bytes = P.kg * P.a_box_bytes + (P.b_res ? 0 : P.kg * P.b_tile_stride);
-        if (1024 + P.b_region + pl.stages * P.stage_bytes + 8 * (2 * pl.stages + 6) + 16 > pl.smem_bytes)
+        const bool tf32 = pl.variant == CBS_VARIANT_TC_TF32;
+        P.st_mode = tc_store_mode(d, BN, pl.n_tiles, tf32);
+        P.cbw = 128 / tc_out_bytes(tf32);
+        P.stg_bytes_total = P.st_mode ? kEpiWarps * kStageBlockBytes : 0;
+        P.bias_bytes_smem = tc_bias_smem_bytes(d);
+        P.bias_smem = P.bias_bytes_smem > 0;
+        if (1024 + P.b_region + pl.stages * P.stage_bytes + P.stg_bytes_total + P.bias_bytes_smem +
+                8 * (2 * pl.stages + 6) + 16 > pl.smem_bytes)
             return fail(CBS_ERR_PLAN_MISMATCH, "plan's shared memory does not hold its stages");
         if (P.b_res && P.n_tiles > 1 && pl.grid_ctas % P.n_tiles)
             return fail(CBS_ERR_PLAN_MISMATCH, "resident weights need a grid that is a multiple of the N tiles");
@@ -1058,8 +1193,19 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     if (!P.status) return fail(CBS_ERR_CUDA, "cannot resolve the device status word");
     if (pl.grid_ctas <= 0) return CBS_OK;
 
-    alignas(64) CUtensorMap tmA, tmB;
+    alignas(64) CUtensorMap tmA, tmB, tmY;
+    std::memset(&tmY, 0, sizeof(tmY));
     CUresult r;
+    if (P.st_mode) {
+        const int eb_y = eb_w;   // output element: float (TF32) or bfloat16 (BF16)
+        const cuuint64_t dims[2] = {(cuuint64_t)d.c_out, (cuuint64_t)P.M};
+        const cuuint64_t strides[1] = {(cuuint64_t)d.c_out * eb_y};
+        const cuuint32_t box[2] = {(cuuint32_t)P.cbw, 32u};
+        const cuuint32_t es[2] = {1, 1};
+        r = fns.tiled(&tmY, dt_w, 2, y, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuTensorMapEncodeTiled (y) failed (%d)", (int)r);
+    }
     const cuuint32_t estr1[2] = {1, 1};
     const CUtensorMapSwizzle swz_x = XB == 16 ? CU_TENSOR_MAP_SWIZZLE_NONE : swizzle_for(XB);
     if (P.im2col) {
@@ -1098,10 +1244,10 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     cudaError_t e;
     if (pl.variant == CBS_VARIANT_TC_TF32) {
         e = cudaFuncSetAttribute(tc_conv_kernel<kTF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
-        if (e == cudaSuccess) tc_conv_kernel<kTF32><<<grid, kThreads, pl.smem_bytes, s>>>(tmA, tmB, P);
+        if (e == cudaSuccess) tc_conv_kernel<kTF32><<<grid, kThreads, pl.smem_bytes, s>>>(tmA, tmB, tmY, P);
     } else if (pl.variant == CBS_VARIANT_TC_BF16) {
         e = cudaFuncSetAttribute(tc_conv_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
-        if (e == cudaSuccess) tc_conv_kernel<kBF16><<<grid, kThreads, pl.smem_bytes, s>>>(tmA, tmB, P);
+        if (e == cudaSuccess) tc_conv_kernel<kBF16><<<grid, kThreads, pl.smem_bytes, s>>>(tmA, tmB, tmY, P);
     } else {
         e = cudaFuncSetAttribute(tc_conv_i8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
         if (e == cudaSuccess) tc_conv_i8_kernel<<<grid, kThreadsI8, pl.smem_bytes, s>>>(tmA, tmB, P);

@@ -94,6 +94,8 @@ def test_layer_list_batch1(cuda_lib, prec, i):
     (1, 3, 16, 3, 2, 34),      # C_in = 3 padded, stride 2, even size
     (2, 8, 16, 3, 1, 1),       # 1x1 image with a 3x3 filter
     (1, 4, 64, 7, 2, 21),      # direct small-channel kernel, 7x7: 49 KB of weights
+    (2, 16, 20, 3, 1, 9),      # BF16 rows of 40 bytes: direct stores; TF32 rows of 80: staged stores
+    (1, 32, 36, 1, 1, 7),      # C_out = 36: ragged channel block in both store paths
 ])
 def test_ragged(cuda_lib, prec, shape):
     n, c_in, c_out, k, stride, h = shape
