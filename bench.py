@@ -104,6 +104,37 @@ EXTRA_DEFAULT = ("layer_list_bf16_n16", "layer_list_tf32_n16", "layer_list_int8_
                  "chain_bf16_n16")
 
 
+# DRAM traffic of the dominant kernel over one step of a workload, from one
+# ncu capture of the default bench command's first warm-up step
+# (dram__bytes_read.sum + dram__bytes_write.sum summed over that kernel's
+# launches; the summary and command are in profiles/).  A figure is reported
+# only while the kernel's sources are the ones the counters were taken from.
+TRAFFIC = {
+    "layer_list_fp32_n1": {"kernel": "simt_conv_kernel", "launches": 11, "bytes": 28535040,
+                           "sources": ("k_simt.cu", "cbs_internal.cuh"), "digest": "f3beafd128ff54cb",
+                           "profile": "profiles/launches_layer_list_fp32_n1.md"},
+}
+# Variant of the dominant kernel per precision (the direct small-channel
+# kernel runs the stem and is reported per layer, not here).
+DOMINANT_VARIANT = {"fp32": 0, "tf32": 1, "bf16": 2, "int8": 3}
+
+
+def sources_digest(files) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "conv_bn_silu_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(workload: str):
+    t = TRAFFIC.get(workload)
+    if t is None or sources_digest(t["sources"]) != t["digest"]:
+        return None
+    return t["bytes"]
+
+
 def act_bytes(prec: str) -> int:
     return {"fp32": 4, "tf32": 4, "bf16": 2, "int8": 1}[prec]
 
@@ -329,15 +360,23 @@ def run_ours(args, rank: int, world: int):
     flops_step = sum(sp.flops(n) for sp in w.specs)
     value = flops_step * world / (ms_step * 1e-3) / 1e12
     rows = head["layers"]
-    kern_us = head["sum_layer_us"]
-    achieved = flops_step / (kern_us * 1e-6) / 1e12
     peak = head["peak_tflops"]
     kernel = {"fp32": "simt_conv_kernel (FP32 FMA)", "tf32": "tc_conv_kernel<TF32>",
               "bf16": "tc_conv_kernel<BF16>", "int8": "tc_conv_i8_kernel"}[w.prec]
-    roofline = {"bound": "alu" if w.prec == "fp32" else "tensor", "kernel": kernel + ", all launches",
+    # The dominant kernel: every layer the plan gives to it (all but the stem).
+    dom = [(sp, r) for (sp, layer), r in zip(w.rows(), rows) if layer.plan.variant == DOMINANT_VARIANT[w.prec]]
+    dom_flops = sum(sp.flops(n) for sp, _ in dom)
+    dom_us = sum(r["us"] for _, r in dom)
+    achieved = dom_flops / (dom_us * 1e-6) / 1e12
+    traffic = traffic_for(args.workload)
+    roofline = {"bound": "alu" if w.prec == "fp32" else "tensor",
+                "kernel": f"{kernel}, the {len(dom)} launches of one step",
                 "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "peak_source": head["peak"] + f" ({peak_src})",
-                "traffic": None,
+                "traffic": traffic,
+                "traffic_note": ("DRAM bytes of those launches in one step (ncu, cold cache)" if traffic is not None
+                                 else "no capture of the current kernel sources"),
+                "algorithmic_bytes": sum(sp.alg_bytes(n, act_bytes(w.prec)) for sp, _ in dom),
                 "sum_layer_roofline_us": head["sum_layer_roofline_us"],
                 "frac_of_layer_roofline_sum": head["frac_of_layer_roofline_sum"]}
     e2e = run_e2e(w, device, args, flops_step, world)

@@ -37,13 +37,13 @@ class cbs_layer_desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "n", "c_in", "h", "w", "c_out", "k", "stride", "pad", "in_layout", "out_layout", "prec",
         "force_variant", "force_split_k", "force_block_n", "force_block_m", "out_row_stride",
-        "force_k_group", "force_b_resident")]
+        "force_k_group", "force_b_resident", "force_window")]
 
 
 class cbs_plan_t(ctypes.Structure):
     _fields_ = [("size", ctypes.c_uint32), ("abi_version", ctypes.c_uint32)] + \
         [(n, ctypes.c_int) for n in (
-            "variant", "block_m", "block_n", "block_k", "stages", "split_k", "k_group", "b_resident",
+            "variant", "block_m", "block_n", "block_k", "stages", "split_k", "k_group", "b_resident", "window",
             "c_in_pad", "k_gemm",
             "oh", "ow", "out_row_stride", "m_tiles", "n_tiles", "grid_ctas", "threads",
             "smem_bytes")] + \

@@ -97,6 +97,14 @@ struct TcParams {
     int stg_bytes_total;       // bytes of the staging region (8 warps x 4 KB) when st_mode
     int bias_smem;             // 1: the folded bias is copied to shared memory at start
     int bias_bytes_smem;       // bytes reserved for it
+    // Windowed A (stride 1, pad k/2): tiles are runs of padded positions
+    // q = oh * Wp + ow' of one image (ow' < Wp = W + 2 pad; columns ow' >= OW
+    // are computed and dropped), and one TMA box brings the zero-padded input
+    // window of a tile and channel block; tap (r, s) is the window viewed from
+    // row r * Wp + s on.
+    int win;
+    int Wp, tiles_per_img, R_box;
+    int SB;                    // weight-ring stages when the weights are streamed (windowed)
 };
 
 constexpr int kStageBlockBytes = 4096;            // one warp's staged store block: 32 rows x 128 B
@@ -249,8 +257,9 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t *base_ptr = smem_raw + (base - raw_addr);
     const int S = p.stages;
-    // [resident B][S stages][store staging][bias][barriers: full[S], empty[S],
-    //  acc_full[2], acc_empty[2], drain, b_full]
+    // [resident B or weight ring][S stages][store staging][bias][barriers:
+    //  full[S], empty[S], acc_full[2], acc_empty[2], drain, b_full,
+    //  wring_full[SB], wring_empty[SB]]
     const uint32_t b_base = base;
     const uint32_t stage0 = base + p.b_region;
     const uint32_t stg_base = stage0 + S * p.stage_bytes;
@@ -258,7 +267,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const uint32_t bars = stg_base + p.stg_bytes_total + p.bias_bytes_smem;
     uint64_t *bar_ptr = reinterpret_cast<uint64_t *>(base_ptr + p.b_region + S * p.stage_bytes + p.stg_bytes_total +
                                                      p.bias_bytes_smem);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_ptr + 2 * S + 6);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_ptr + 2 * S + 6 + 2 * p.SB);
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
     auto full_bar = [&](int s) { return bars + 8u * s; };
@@ -267,10 +276,13 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     auto acce_bar = [&](int a) { return bars + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = bars + 8u * (2 * S + 4);
     const uint32_t bfull_bar = bars + 8u * (2 * S + 5);
+    auto wfull_bar = [&](int b) { return bars + 8u * (2 * S + 6 + b); };
+    auto wempty_bar = [&](int b) { return bars + 8u * (2 * S + 6 + p.SB + b); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = p.ksteps;
-    const int nstage = nk / p.kg;                 // stages per tile
+    const int nstage = p.win ? p.cblocks : nk / p.kg;   // stages per tile
+    const int kk2 = p.ks * p.ks;
     const int tile_m = kBM * p.mmul;
     const int num_tiles = p.m_tiles * p.n_tiles;
     const int b_step_bytes = p.BN * p.RB;         // bytes of one B tile as loaded
@@ -286,6 +298,10 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         ptx::mbar_init(drain_bar, 1);
         ptx::mbar_init(bfull_bar, 1);                 // producer warp 0 loads the resident weights
+        for (int b = 0; b < p.SB; ++b) {
+            ptx::mbar_init(wfull_bar(b), 1);
+            ptx::mbar_init(wempty_bar(b), 1);
+        }
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmA);
@@ -305,17 +321,44 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const float *bias = p.bias_smem ? bias_sm : p.bias;
 
     int last_g = -1;  // producer: last stage (global count) whose loads this warp issued
+    int last_w = -1;  // weight-ring lane: last weight load (global count) it issued
     bool b_issued = false;
-    if (warp < kMaxProducers) {
+    // Windowed mode with streamed weights: warp 3 keeps the weight ring full
+    // (lane b owns ring slot b) and warps 0..nprod-1 (nprod <= 3) load windows.
+    const bool wring = p.win && !p.b_res;
+    if (wring && warp == kMaxProducers - 1) {
+        if (lane < p.SB) {
+            int gw = 0;
+            for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
+                const int n0 = (t % p.n_tiles) * p.BN;
+                bool ok = true;
+                for (int cb = 0; cb < p.cblocks && ok; ++cb) {
+                    for (int tap = 0; tap < kk2; ++tap, ++gw) {
+                        if (gw % p.SB != lane) continue;
+                        const int u = gw / p.SB;
+                        if (!ptx::mbar_wait_bounded(wempty_bar(lane), (u & 1) ^ 1, kWaitLimitNs) || aborted(abort_flag)) {
+                            if (!aborted(abort_flag)) abort_now(p, abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        ptx::mbar_arrive_expect_tx(wfull_bar(lane), (uint32_t)b_step_bytes);
+                        ptx::tma_load_2d(b_base + lane * p.b_tile_stride, &tmB, wfull_bar(lane),
+                                         tap * p.c_in_pad + cb * p.CB, n0);
+                        last_w = gw;
+                    }
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (warp < kMaxProducers) {
         // A TMA box takes an issuing thread ~570 cycles whatever its size,
         // and lanes issue in parallel: lane l of a producer warp issues box l
         // of the stage (A boxes first, then B boxes).
-        const int nbox = p.kg * (p.b_res ? 1 : 2);
+        const int nbox = p.win ? 1 : p.kg * (p.b_res ? 1 : 2);
         if (warp < p.nprod) {
             if (p.b_res && warp == 0 && blockIdx.x < num_tiles) {
                 // This CTA's N tile never changes: load its weight tile once.
-                int m0, n0;
-                tile_coords(blockIdx.x, p.n_tiles, tile_m, m0, n0, p.BN);
+                const int n0 = (blockIdx.x % p.n_tiles) * p.BN;
                 if (lane == 0) ptx::mbar_arrive_expect_tx(bfull_bar, (uint32_t)(nk * b_step_bytes));
                 __syncwarp();
                 for (int i = lane; i < nk; i += 32) {
@@ -331,11 +374,23 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
                 int m0, n0;
                 tile_coords(t, p.n_tiles, tile_m, m0, n0, p.BN);
-                // Window corner of the tile's first output pixel.
-                const int img = m0 / p.OHW;
-                const int rem = m0 - img * p.OHW;
-                const int oh = rem / p.OW, ow = rem - (rem / p.OW) * p.OW;
-                const int wc = ow * p.stride - p.pad, hc = oh * p.stride - p.pad;
+                int img, wc, hc;
+                if (p.win) {
+                    // Window of the tile: padded columns -pad .. W+pad-1 of the
+                    // input rows from (first output row) - pad on.
+                    const int mt = t / p.n_tiles;
+                    img = mt / p.tiles_per_img;
+                    const int q0 = (mt - img * p.tiles_per_img) * tile_m;
+                    wc = -p.pad;
+                    hc = q0 / p.Wp - p.pad;
+                } else {
+                    // Window corner of the tile's first output pixel.
+                    img = m0 / p.OHW;
+                    const int rem = m0 - img * p.OHW;
+                    const int oh = rem / p.OW, ow = rem - (rem / p.OW) * p.OW;
+                    wc = ow * p.stride - p.pad;
+                    hc = oh * p.stride - p.pad;
+                }
                 bool ok = true;
                 for (int st = 0; st < nstage; ++st, ++g) {
                     if (g % p.nprod != warp) continue;
@@ -350,10 +405,12 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     const uint32_t sbase = stage0 + s * p.stage_bytes;
                     if (lane == 0)
-                        ptx::mbar_arrive_expect_tx(full_bar(s),
-                                                   (uint32_t)(p.kg * (p.a_box_bytes + (p.b_res ? 0 : b_step_bytes))));
+                        ptx::mbar_arrive_expect_tx(full_bar(s), p.win ? (uint32_t)p.a_box_bytes
+                                                                      : (uint32_t)(p.kg * (p.a_box_bytes + (p.b_res ? 0 : b_step_bytes))));
                     __syncwarp();
-                    if (lane < nbox) {
+                    if (p.win) {
+                        if (lane == 0) ptx::tma_load_4d(sbase, &tmA, full_bar(s), st * p.CB, wc, hc, img);
+                    } else if (lane < nbox) {
                         const bool is_a = lane < p.kg;
                         const int kk = is_a ? lane : lane - p.kg;
                         const int i = st * p.kg + kk;
@@ -386,7 +443,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 abort_now(p, abort_flag);
                 ok = false;
             }
-            int g = 0, j = 0;
+            int g = 0, j = 0, gw = 0;
             for (int t = blockIdx.x; ok && t < num_tiles && !aborted(abort_flag); t += gridDim.x, ++j) {
                 const int acc = j & 1, ua = j >> 1;
                 if (!ptx::mbar_wait_bounded(acce_bar(acc), (ua & 1) ^ 1, kWaitLimitNs)) {
@@ -395,6 +452,61 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_stride);
+                if (p.win) {
+                    // Row of the window that holds the tile's first position.
+                    const int mt = t / p.n_tiles;
+                    const int q0 = (mt - (mt / p.tiles_per_img) * p.tiles_per_img) * tile_m;
+                    const int row0 = q0 - (q0 / p.Wp) * p.Wp;
+                    for (int cb = 0; cb < p.cblocks; ++cb, ++g) {
+                        const int s = g % S, u = g / S;
+                        if (!ptx::mbar_wait_bounded(full_bar(s), u & 1, kWaitLimitNs)) {
+                            abort_now(p, abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const uint32_t window = stage0 + s * p.stage_bytes;
+                        for (int tap = 0; tap < kk2 && ok; ++tap) {
+                            const int r = tap / p.ks, c = tap - r * p.ks;
+                            uint32_t b_addr;
+                            int ws = 0;
+                            if (p.b_res) {
+                                b_addr = b_base + (tap * p.cblocks + cb) * p.b_tile_stride;
+                            } else {
+                                ws = gw % p.SB;
+                                if (!ptx::mbar_wait_bounded(wfull_bar(ws), (gw / p.SB) & 1, kWaitLimitNs)) {
+                                    abort_now(p, abort_flag);
+                                    ok = false;
+                                    break;
+                                }
+                                ptx::tc_fence_after();
+                                b_addr = b_base + ws * p.b_tile_stride;
+                            }
+                            for (int mi = 0; mi < p.mmul; ++mi) {
+                                const uint32_t d = d_tmem + (uint32_t)(mi * p.bnp);
+                                const uint32_t a_addr = window + (uint32_t)(row0 + mi * kBM + r * p.Wp + c) * p.RB;
+                                for (int k = 0; k < kslices; ++k) {
+                                    const uint64_t ad = ptx::smem_desc_offset(a_addr + 32u * k, 16u, sbo, p.swz);
+                                    const uint64_t bd = ptx::smem_desc(b_addr + 32u * k, 16u, sbo, p.swz);
+                                    const uint32_t accum = (cb > 0 || tap > 0 || k > 0) ? 1u : 0u;
+                                    if (KIND == kTF32)
+                                        ptx::mma_tf32(d, ad, bd, p.idesc, accum);
+                                    else
+                                        ptx::mma_f16(d, ad, bd, p.idesc, accum);
+                                }
+                            }
+                            if (!p.b_res) {
+                                ptx::mma_commit(wempty_bar(ws));   // weight slot free once these MMAs are done
+                                ++gw;
+                            }
+                        }
+                        if (!ok) break;
+                        ptx::mma_commit(empty_bar(s));
+                    }
+                    if (!ok) break;
+                    ptx::mma_commit(accf_bar(acc));
+                    continue;
+                }
                 for (int st = 0; st < nstage; ++st, ++g) {
                     const int s = g % S, u = g / S;
                     if (!ptx::mbar_wait_bounded(full_bar(s), u & 1, kWaitLimitNs)) {
@@ -451,13 +563,26 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ptx::tc_fence_after();
             int m0, n0;
             tile_coords(t, p.n_tiles, tile_m, m0, n0, p.BN);
-            const int m = m0 + row;
+            int m = m0 + row;
             int img = 0, oh = 0, ow = 0;
-            if (m < p.M) {
-                img = m / p.OHW;
-                const int rem = m - img * p.OHW;
-                oh = rem / p.OW;
-                ow = rem - oh * p.OW;
+            bool valid;
+            if (p.win) {
+                // Position q of the padded grid: keep it when ow' < OW.
+                const int mt = t / p.n_tiles;
+                img = mt / p.tiles_per_img;
+                const int q = (mt - img * p.tiles_per_img) * tile_m + row;
+                oh = q / p.Wp;
+                ow = q - oh * p.Wp;
+                valid = oh < p.OH && ow < p.OW;
+                m = (img * p.OH + oh) * p.OW + ow;
+            } else {
+                valid = m < p.M;
+                if (valid) {
+                    img = m / p.OHW;
+                    const int rem = m - img * p.OHW;
+                    oh = rem / p.OW;
+                    ow = rem - oh * p.OW;
+                }
             }
             const uint32_t t_row = tmem_base + (uint32_t)(acc * p.acc_stride + sub * p.bnp) + ((uint32_t)(32 * q) << 16);
             if (p.st_mode) {
@@ -501,7 +626,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     ptx::tmem_ld16(t_row + (uint32_t)c0, v0);
                     if (two) ptx::tmem_ld16(t_row + (uint32_t)(c0 + cstep), v1);
                     ptx::tmem_ld_wait();
-                    if (m < p.M) {
+                    if (valid) {
                         if (n0 + c0 < p.C_out) epi_store16<KIND>(p, bias, m, img, oh, ow, n0 + c0, v0);
                         if (two && n0 + c0 + cstep < p.C_out)
                             epi_store16<KIND>(p, bias, m, img, oh, ow, n0 + c0 + cstep, v1);
@@ -526,6 +651,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ptx::mbar_wait_bounded(full_bar(g % S), (g / S) & 1, kWaitLimitNs);
         if (b_issued) ptx::mbar_wait_bounded(bfull_bar, 0, kWaitLimitNs);
     }
+    if (warp == kMaxProducers - 1 && lane < p.SB && last_w >= 0 && aborted(abort_flag))
+        ptx::mbar_wait_bounded(wfull_bar(lane), (last_w / p.SB) & 1, kWaitLimitNs);
     if (warp == kMmaWarp && lane == 0) {
         if (!ptx::mbar_wait_bounded(drain_bar, 0, kWaitLimitNs)) atomicOr(p.status, 1u);
     }
@@ -921,17 +1048,94 @@ int tc_store_mode(const cbs_layer_desc &d, int BN, int n_tiles, bool tf32) {
 
 int tc_bias_smem_bytes(const cbs_layer_desc &d) { return d.c_out <= 1024 ? (d.c_out * 4 + 15) / 16 * 16 : 0; }
 
+// Producer warps for a stage count, at most maxp.
+int tc_producers_max(int stages, int maxp) {
+    for (int np = maxp; np >= 2; --np)
+        if (stages >= np && stages % np == 0) return np;
+    return 1;
+}
+
+// Window geometry of the windowed A path (stride 1, odd k, pad k/2, 128-byte
+// channel blocks): padded row width and input rows of one window box.
+struct TcWindow {
+    int Wp, R_box, tiles_per_img;
+};
+bool tc_window_geometry(const cbs_layer_desc &d, int oh, int RB, int tile_m, TcWindow &w) {
+    if (d.stride != 1 || d.k % 2 == 0 || d.pad != d.k / 2 || RB != 128) return false;
+    w.Wp = d.w + 2 * d.pad;
+    w.R_box = (tile_m - 1) / w.Wp + 2 + 2 * d.pad;
+    if (w.Wp > 256 || w.R_box > 256) return false;
+    w.tiles_per_img = (oh * w.Wp + tile_m - 1) / tile_m;
+    return true;
+}
+
 struct TcConfig {
-    int BN, mmul, b_res, kg, stages, nprod, st_mode, extra_bytes;
+    int BN, mmul, b_res, kg, stages, nprod, st_mode, extra_bytes, win, SB;
+    TcWindow wg;
     int m_tiles, n_tiles, grid;
     int stage_bytes, b_region, b_tile_stride, a_box_bytes;
     double cycles;
 };
 
+// Windowed configuration: one window box per tile and channel block (kept
+// for all k*k taps), weights resident or in a ring of SB single-tile slots.
+bool tc_config_window(const cbs_layer_desc &d, int oh, int RB, int ksteps, bool tf32, TcConfig &c) {
+    const int tile_m = kBM * c.mmul;
+    if (!tc_window_geometry(d, oh, RB, tile_m, c.wg)) return false;
+    const int cblocks = ksteps / (d.k * d.k);
+    c.kg = 1;
+    c.a_box_bytes = c.wg.R_box * c.wg.Wp * RB;
+    // The last taps of the last (dropped) columns read up to k-2 rows past the
+    // box: the stage keeps 8 spare rows.
+    c.stage_bytes = ((c.wg.R_box * c.wg.Wp + 8) * RB + 1023) / 1024 * 1024;
+    const int b_bytes = c.BN * RB;
+    c.b_tile_stride = (b_bytes + 1023) / 1024 * 1024;
+    c.m_tiles = d.n * c.wg.tiles_per_img;
+    c.n_tiles = (d.c_out + c.BN - 1) / c.BN;
+    c.st_mode = 0;
+    c.extra_bytes = tc_bias_smem_bytes(d);
+    int cap = 0;
+    for (int sb : {8, 4}) {
+        c.SB = c.b_res ? 0 : sb;
+        c.b_region = c.b_res ? ksteps * c.b_tile_stride : c.SB * c.b_tile_stride;
+        const int barrier_bytes = 8 * (2 * 16 + 6 + 2 * c.SB) + 16;
+        cap = (kSmemBudget - c.b_region - c.extra_bytes - barrier_bytes) / c.stage_bytes;
+        if (cap >= 2 || c.b_res) break;
+    }
+    if (cap > 6) cap = 6;
+    if (cap < 2) return false;
+    c.stages = cap;
+    c.nprod = tc_producers_max(c.stages, c.b_res ? kMaxProducers : kMaxProducers - 1);
+    const long long tiles = (long long)c.m_tiles * c.n_tiles;
+    if (c.b_res && c.n_tiles > 1) {
+        const long long g = tiles < kNumSMs ? tiles : (long long)(kNumSMs / c.n_tiles) * c.n_tiles;
+        if (g <= 0) return false;
+        c.grid = (int)g;
+    } else {
+        c.grid = (int)(tiles < kNumSMs ? tiles : kNumSMs);
+    }
+    const double tpc = (double)((tiles + c.grid - 1) / c.grid);
+    const int kslices = RB / 32;
+    const double mma = tpc * ((double)ksteps * kslices * c.mmul * tc_mma_clk(c.BN, tf32) +
+                              (double)cblocks * kClkPerStageWait + (c.b_res ? 0.0 : (double)ksteps * 100.0));
+    const double boxes = tpc * cblocks + (c.b_res ? (double)ksteps : tpc * ksteps);
+    const double bytes = tpc * cblocks * (double)c.a_box_bytes + (c.b_res ? (double)ksteps : tpc * ksteps) * b_bytes;
+    const double t_box = boxes * 140.0, t_fill = bytes / kFillBytesPerClk;
+    const double tma = t_box > t_fill ? t_box : t_fill;
+    const double vals = c.mmul == 2 ? (double)c.BN : 0.5 * c.BN;
+    const double epi = tpc * (250.0 + 45.0 * vals);
+    double cyc = mma > tma ? mma : tma;
+    if (epi > cyc) cyc = epi;
+    cyc += 1500.0 + (double)c.a_box_bytes / kFillBytesPerClk + 250.0 + 45.0 * vals;
+    c.cycles = cyc;
+    return true;
+}
+
 // Shared-memory layout and cost of one configuration (false if it does not fit).
-bool tc_config(const cbs_layer_desc &d, long long M, int RB, int ksteps, bool tf32, int BN, int mmul, int b_res,
-               int kg, TcConfig &c) {
-    c.BN = BN; c.mmul = mmul; c.b_res = b_res; c.kg = kg;
+bool tc_config(const cbs_layer_desc &d, long long M, int oh, int RB, int ksteps, bool tf32, int BN, int mmul,
+               int b_res, int kg, int win, TcConfig &c) {
+    c.BN = BN; c.mmul = mmul; c.b_res = b_res; c.kg = kg; c.win = win; c.SB = 0;
+    if (win) return tc_config_window(d, oh, RB, ksteps, tf32, c);
     if (kg * (b_res ? 1 : 2) > 32) return false;   // one issuing lane per box of a stage
     c.a_box_bytes = kBM * mmul * RB;
     const int b_bytes = BN * RB;
@@ -1074,12 +1278,20 @@ cbs_status plan_tc(cbs_plan_t &p) {
             if (d.force_block_m > 0 && d.force_block_m != kBM * mmul) continue;
             for (int b_res = 0; b_res <= 1; ++b_res) {
                 if ((d.force_b_resident > 0 && !b_res) || (d.force_b_resident < 0 && b_res)) continue;
-                for (int kg = 1; kg <= (d.force_k_group > 4 ? d.force_k_group : 4); ++kg) {
-                    if (ksteps % kg) continue;
-                    if (d.force_k_group > 0 && kg != d.force_k_group) continue;
-                    TcConfig c;
-                    if (!tc_config(d, M, RB, ksteps, tf32, BN, mmul, b_res, kg, c)) continue;
-                    if (c.cycles < best.cycles * 0.99) best = c;
+                for (int win = 0; win <= 1; ++win) {
+                    // Windowed A moves ~4x fewer bytes from L2 but measured no
+                    // faster on GB300 (the MMA rate bounds these layers): it is
+                    // used when asked for.
+                    if ((d.force_window <= 0 && win) || (d.force_window > 0 && !win)) continue;
+                    if (win && d.force_k_group > 0) continue;     // K groups belong to the im2col path
+                    for (int kg = 1; kg <= (d.force_k_group > 4 ? d.force_k_group : 4); ++kg) {
+                        if (ksteps % kg) continue;
+                        if (win && kg > 1) break;                  // a window stage is one channel block
+                        if (d.force_k_group > 0 && kg != d.force_k_group) continue;
+                        TcConfig c;
+                        if (!tc_config(d, M, p.oh, RB, ksteps, tf32, BN, mmul, b_res, kg, win, c)) continue;
+                        if (c.cycles < best.cycles * 0.99) best = c;
+                    }
                 }
             }
         }
@@ -1087,14 +1299,16 @@ cbs_status plan_tc(cbs_plan_t &p) {
     if (best.cycles >= 1e299) return fail(CBS_ERR_UNSUPPORTED, "no tensor-core tile configuration fits shared memory");
     p.block_m = kBM * best.mmul;
     p.block_n = best.BN;
-    p.k_group = best.kg;
+    p.k_group = best.win ? best.SB : best.kg;   // windowed plans: weight-ring slots
     p.b_resident = best.b_res;
+    p.window = best.win;
     p.stages = best.stages;
     p.m_tiles = best.m_tiles;
     p.n_tiles = best.n_tiles;
     p.grid_ctas = best.grid;
     p.threads = kThreads;
-    p.smem_bytes = 1024 + best.b_region + best.stages * best.stage_bytes + best.extra_bytes + 8 * (2 * best.stages + 6) + 16;
+    p.smem_bytes = 1024 + best.b_region + best.stages * best.stage_bytes + best.extra_bytes +
+                   8 * (2 * best.stages + 6 + 2 * best.SB) + 16;
     return CBS_OK;
 }
 
@@ -1131,30 +1345,44 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     const int mmul = i8 ? 1 : pl.block_m / kBM;
     if (pl.block_m != kBM * mmul || mmul < 1 || mmul > 2) return fail(CBS_ERR_PLAN_MISMATCH, "block_m %d", pl.block_m);
     P.mmul = mmul;
-    P.kg = i8 ? 1 : pl.k_group;
+    P.win = i8 ? 0 : pl.window;
+    P.kg = (i8 || P.win) ? 1 : pl.k_group;
     P.b_res = i8 ? 0 : pl.b_resident;
+    P.SB = (P.win && !P.b_res) ? pl.k_group : 0;
     if (P.kg < 1 || P.ksteps % P.kg) return fail(CBS_ERR_PLAN_MISMATCH, "k_group %d", pl.k_group);
+    if (P.win && !P.b_res && (P.SB < 1 || P.SB > 32)) return fail(CBS_ERR_PLAN_MISMATCH, "weight ring %d", P.SB);
     P.bnp = next_pow2(BN);
     P.a_bytes = kBM * RB; P.b_bytes = BN * RB;
     P.a_box_bytes = kBM * mmul * RB;
     P.b_tile_stride = round_up(P.b_bytes, 1024);
-    P.b_region = P.b_res ? P.ksteps * P.b_tile_stride : 0;
+    P.b_region = P.b_res ? P.ksteps * P.b_tile_stride : P.SB * P.b_tile_stride;
+    if (P.win) {
+        TcWindow wg;
+        if (!tc_window_geometry(d, pl.oh, RB, kBM * mmul, wg)) return fail(CBS_ERR_PLAN_MISMATCH, "window geometry");
+        P.Wp = wg.Wp;
+        P.R_box = wg.R_box;
+        P.tiles_per_img = wg.tiles_per_img;
+        P.a_box_bytes = wg.R_box * wg.Wp * RB;
+        if (pl.m_tiles != d.n * wg.tiles_per_img) return fail(CBS_ERR_PLAN_MISMATCH, "window tiles");
+    }
     if (i8) {
         int nprod = kMaxProducersI8;
         while (nprod > 1 && (pl.stages < 2 * nprod || pl.stages % nprod != 0)) nprod /= 2;
         P.nprod = nprod;
         P.stage_bytes = round_up(P.a_bytes + P.b_bytes, 1024);
     } else {
-        P.nprod = tc_producers(pl.stages);
-        P.stage_bytes = P.kg * P.a_box_bytes + (P.b_res ? 0 : P.kg * P.b_tile_stride);
+        P.nprod = P.win ? tc_producers_max(pl.stages, P.b_res ? kMaxProducers : kMaxProducers - 1)
+                        : tc_producers(pl.stages);
+        P.stage_bytes = P.win ? round_up((P.R_box * P.Wp + 8) * RB, 1024)
+                              : P.kg * P.a_box_bytes + (P.b_res ? 0 : P.kg * P.b_tile_stride);
         const bool tf32 = pl.variant == CBS_VARIANT_TC_TF32;
-        P.st_mode = tc_store_mode(d, BN, pl.n_tiles, tf32);
+        P.st_mode = P.win ? 0 : tc_store_mode(d, BN, pl.n_tiles, tf32);
         P.cbw = 128 / tc_out_bytes(tf32);
         P.stg_bytes_total = P.st_mode ? kEpiWarps * kStageBlockBytes : 0;
         P.bias_bytes_smem = tc_bias_smem_bytes(d);
         P.bias_smem = P.bias_bytes_smem > 0;
         if (1024 + P.b_region + pl.stages * P.stage_bytes + P.stg_bytes_total + P.bias_bytes_smem +
-                8 * (2 * pl.stages + 6) + 16 > pl.smem_bytes)
+                8 * (2 * pl.stages + 6 + 2 * P.SB) + 16 > pl.smem_bytes)
             return fail(CBS_ERR_PLAN_MISMATCH, "plan's shared memory does not hold its stages");
         if (P.b_res && P.n_tiles > 1 && pl.grid_ctas % P.n_tiles)
             return fail(CBS_ERR_PLAN_MISMATCH, "resident weights need a grid that is a multiple of the N tiles");
@@ -1208,7 +1436,16 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     }
     const cuuint32_t estr1[2] = {1, 1};
     const CUtensorMapSwizzle swz_x = XB == 16 ? CU_TENSOR_MAP_SWIZZLE_NONE : swizzle_for(XB);
-    if (P.im2col) {
+    if (P.win) {
+        const cuuint64_t dims[4] = {(cuuint64_t)pl.c_in_pad, (cuuint64_t)d.w, (cuuint64_t)d.h, (cuuint64_t)d.n};
+        const cuuint64_t strides[3] = {(cuuint64_t)pl.c_in_pad * eb_x, (cuuint64_t)d.w * pl.c_in_pad * eb_x,
+                                       (cuuint64_t)d.h * d.w * pl.c_in_pad * eb_x};
+        const cuuint32_t box[4] = {(cuuint32_t)CB, (cuuint32_t)P.Wp, (cuuint32_t)P.R_box, 1u};
+        const cuuint32_t es4[4] = {1, 1, 1, 1};
+        r = fns.tiled(&tmA, dt_x, 4, const_cast<void *>(x), dims, strides, box, es4, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      swz_x, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuTensorMapEncodeTiled (window) failed (%d)", (int)r);
+    } else if (P.im2col) {
         const cuuint64_t dims[4] = {(cuuint64_t)pl.c_in_pad, (cuuint64_t)d.w, (cuuint64_t)d.h, (cuuint64_t)d.n};
         const cuuint64_t strides[3] = {(cuuint64_t)pl.c_in_pad * eb_x, (cuuint64_t)d.w * pl.c_in_pad * eb_x,
                                        (cuuint64_t)d.h * d.w * pl.c_in_pad * eb_x};

@@ -74,6 +74,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// Tiled 4-D load (NHWC activations: {c, w, h, n}); coordinates may be
+// negative or past the end, where the box is zero-filled.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, uint32_t bar, int c0, int c1, int c2,
+                                            int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
 // im2col load of a 4-D NHWC tensor: coordinates {c, w, h, n} of the first
 // output pixel's window corner, filter-tap offsets {w_off, h_off}.
 __device__ __forceinline__ void tma_load_im2col_4d(uint32_t dst, const void *tmap, uint32_t bar, int c, int w,
@@ -188,6 +199,17 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
     d |= (uint64_t)1 << 46;
     d |= (uint64_t)(swizzle_code & 7u) << 61;
     return d;
+}
+
+// Same, for a matrix that starts inside a swizzle pattern (any 128-byte row
+// of a 128-byte-swizzled buffer, not only a 1024-byte repeat).  The tensor
+// cores apply the swizzle to the absolute shared-memory address, the same way
+// TMA wrote the data, so the start address alone places the view; the
+// base-offset field stays zero (measured on GB300: setting it to address bits
+// 7-9 of the start shifts the pattern and corrupts the operand).
+__device__ __forceinline__ uint64_t smem_desc_offset(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                                     uint32_t swizzle_code) {
+    return smem_desc(saddr, lbo_bytes, sbo_bytes, swizzle_code);
 }
 
 }  // namespace ptx

@@ -92,6 +92,8 @@ typedef struct cbs_layer_desc {
                             layer's K steps) */
     int force_b_resident;/* TF32/BF16: 0 = choose; 1 = keep weights resident in shared memory;
                             -1 = stream them with every K step */
+    int force_window;    /* TF32/BF16: 1 = windowed A (stride 1, odd k, pad k/2, channel blocks of
+                            128 bytes); 0 or -1 = im2col A */
 } cbs_layer_desc;
 
 /* A plan: plain data, owned by the caller, filled by cbs_plan. */
@@ -102,9 +104,14 @@ typedef struct cbs_plan_t {
     int block_m, block_n, block_k;  /* CTA tile: output pixels x output channels x K step */
     int stages;             /* shared-memory pipeline depth */
     int split_k;            /* number of K partitions (>= 1) */
-    int k_group;            /* tensor-core variants: K steps carried by one pipeline stage */
+    int k_group;            /* tensor-core variants: K steps carried by one pipeline stage
+                               (windowed plans: slots of the weight ring, 0 if resident) */
     int b_resident;         /* tensor-core variants: 1 = each CTA loads its weight tile once
                                and keeps it in shared memory for the whole launch */
+    int window;             /* TF32/BF16, stride 1: 1 = each tile loads its zero-padded input
+                               window once per channel block and every filter tap reads a
+                               shifted view of it (block_m positions of the padded grid
+                               oh * (W + 2 pad) + ow'); 0 = one im2col box per tap */
     int c_in_pad;           /* channels per input pixel as stored (NHWC tensor-core variants
                                pad C_in to a 16-byte multiple; SIMT: = c_in) */
     int k_gemm;             /* GEMM K = k*k*c_in_pad: length of one packed weight row */

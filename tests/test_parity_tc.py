@@ -182,5 +182,43 @@ def test_pointwise_tall_tiles(cuda_lib, prec, bm, bres):
     check(y, spec, x, p, prec, (bm, bres))
 
 
+
+WINDOW_SHAPES = [  # (n, c_in, c_out, k, h, w, N tile tried first)
+    (2, 64, 64, 3, 20, 20, 64),      # several tiles per image, last one ragged
+    (1, 128, 96, 3, 13, 17, 96),     # non-square, window rows of 19 positions
+    (1, 64, 32, 5, 11, 11, 32),      # 5x5 filter, pad 2
+    (3, 64, 48, 1, 9, 9, 48),        # 1x1 through the window path
+    (1, 192, 272, 3, 7, 7, 128),     # three channel blocks (BF16), several N tiles, the last ragged
+]
+
+
+@pytest.mark.parametrize("prec", ["bf16", "tf32"])
+@pytest.mark.parametrize("bm,bres", [(128, -1), (256, -1), (128, 1), (256, 1)])
+@pytest.mark.parametrize("shape", WINDOW_SHAPES)
+def test_windowed_a(cuda_lib, prec, bm, bres, shape):
+    """Stride-1 layers with the windowed A operand: one zero-padded input
+    window per tile and channel block, every tap a shifted view of it, weights
+    resident or streamed through the weight ring.  Resident weights that do
+    not fit fall back to the ring."""
+    n, c_in, c_out, k, h, w, bn = shape
+    spec = wl.LayerSpec(c_in, c_out, k, 1, h, w)
+    x, p = wl.layer_inputs(spec, n, layer_index=13)
+    kw = None
+    for cand in (dict(force_block_n=bn, force_b_resident=bres), dict(force_b_resident=bres),
+                 dict(force_block_n=bn, force_b_resident=-1), dict(force_b_resident=-1)):
+        cand.update(force_window=1, force_block_m=bm)
+        try:
+            B.cbs_plan(make_desc(n, c_in, h, w, c_out, k, 1, prec=PRECS[prec], **cand))
+            kw = cand
+            break
+        except B.CbsError as e:
+            assert e.status == B.CBS_ERR_UNSUPPORTED
+    assert kw is not None
+    y, layer = run_tc(spec, x, p, PRECS[prec], **kw)
+    pl = layer.plan
+    assert pl.window == 1 and pl.block_m == bm
+    check(y, spec, x, p, prec, (shape, bm, pl.b_resident, pl.block_n, pl.stages, pl.k_group))
+
+
 def test_no_timeout_reported(cuda_lib):
     assert B.cbs_read_device_status(True, torch.cuda.current_stream().cuda_stream) == B.CBS_OK
