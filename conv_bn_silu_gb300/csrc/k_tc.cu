@@ -234,6 +234,37 @@ __device__ __forceinline__ void tile_coords(int t, int n_tiles, int tile_m, int 
     n0 = (t - mt * n_tiles) * BN;
 }
 
+// The MMAs of one K step for one accumulator: kslices K=16 (bf16) / K=8
+// (tf32) slices, 32 bytes apart along both operands' rows.  Descriptors are
+// built once per launch (dhi: every field but the start address); a slice
+// adds 2 to the start-address field (32 bytes >> 4).  The issuing thread does
+// little else between MMAs: the tensor pipe's queue is short, and any slack
+// in this thread shows up as idle tensor cycles.
+template <int KIND>
+__device__ __forceinline__ void issue_kstep(uint32_t d, uint64_t dhi, uint32_t a_addr, uint32_t b_addr, uint32_t idesc,
+                                            int kslices, bool first) {
+    const uint64_t ad = dhi | (uint64_t)((a_addr & 0x3FFFFu) >> 4);
+    const uint64_t bd = dhi | (uint64_t)((b_addr & 0x3FFFFu) >> 4);
+    if (kslices == 4) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t acc = (first && k == 0) ? 0u : 1u;
+            if (KIND == kTF32)
+                ptx::mma_tf32(d, ad + 2u * k, bd + 2u * k, idesc, acc);
+            else
+                ptx::mma_f16(d, ad + 2u * k, bd + 2u * k, idesc, acc);
+        }
+    } else {
+        for (int k = 0; k < kslices; ++k) {
+            const uint32_t acc = (first && k == 0) ? 0u : 1u;
+            if (KIND == kTF32)
+                ptx::mma_tf32(d, ad + 2u * k, bd + 2u * k, idesc, acc);
+            else
+                ptx::mma_f16(d, ad + 2u * k, bd + 2u * k, idesc, acc);
+        }
+    }
+}
+
 __device__ __forceinline__ void abort_now(const TcParams &p, int *abort_flag) {
     atomicOr(p.status, 1u);
     *(volatile int *)abort_flag = 1;
@@ -438,6 +469,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t sbo = 8u * p.RB;
             const int kslices = p.RB / 32;
             const uint32_t sub_bytes = (uint32_t)(kBM * p.RB);   // one 128-row sub-tile of an A box
+            const uint64_t dhi = ptx::smem_desc(0u, 16u, sbo, p.swz);
             bool ok = true;
             if (p.b_res && blockIdx.x < num_tiles && !ptx::mbar_wait_bounded(bfull_bar, 0, kWaitLimitNs)) {
                 abort_now(p, abort_flag);
@@ -482,19 +514,12 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                 ptx::tc_fence_after();
                                 b_addr = b_base + ws * p.b_tile_stride;
                             }
-                            for (int mi = 0; mi < p.mmul; ++mi) {
-                                const uint32_t d = d_tmem + (uint32_t)(mi * p.bnp);
-                                const uint32_t a_addr = window + (uint32_t)(row0 + mi * kBM + r * p.Wp + c) * p.RB;
-                                for (int k = 0; k < kslices; ++k) {
-                                    const uint64_t ad = ptx::smem_desc_offset(a_addr + 32u * k, 16u, sbo, p.swz);
-                                    const uint64_t bd = ptx::smem_desc(b_addr + 32u * k, 16u, sbo, p.swz);
-                                    const uint32_t accum = (cb > 0 || tap > 0 || k > 0) ? 1u : 0u;
-                                    if (KIND == kTF32)
-                                        ptx::mma_tf32(d, ad, bd, p.idesc, accum);
-                                    else
-                                        ptx::mma_f16(d, ad, bd, p.idesc, accum);
-                                }
-                            }
+                            // A view starting at any 128-byte row: the descriptor's
+                            // start address alone places it (absolute swizzle).
+                            const uint32_t a0 = window + (uint32_t)(row0 + r * p.Wp + c) * p.RB;
+                            for (int mi = 0; mi < p.mmul; ++mi)
+                                issue_kstep<KIND>(d_tmem + (uint32_t)(mi * p.bnp), dhi, a0 + mi * sub_bytes, b_addr, p.idesc,
+                                                  kslices, cb == 0 && tap == 0);
                             if (!p.b_res) {
                                 ptx::mma_commit(wempty_bar(ws));   // weight slot free once these MMAs are done
                                 ++gw;
@@ -521,17 +546,9 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         const uint32_t a_addr = sbase + kk * p.a_box_bytes;
                         const uint32_t b_addr = p.b_res ? b_base + i * p.b_tile_stride
                                                         : sbase + p.kg * p.a_box_bytes + kk * p.b_tile_stride;
-                        for (int mi = 0; mi < p.mmul; ++mi) {
-                            const uint32_t d = d_tmem + (uint32_t)(mi * p.bnp);
-                            for (int k = 0; k < kslices; ++k) {
-                                const uint64_t ad = ptx::smem_desc(a_addr + mi * sub_bytes + 32u * k, 16u, sbo, p.swz);
-                                const uint64_t bd = ptx::smem_desc(b_addr + 32u * k, 16u, sbo, p.swz);
-                                if (KIND == kTF32)
-                                    ptx::mma_tf32(d, ad, bd, p.idesc, (i > 0 || k > 0) ? 1u : 0u);
-                                else
-                                    ptx::mma_f16(d, ad, bd, p.idesc, (i > 0 || k > 0) ? 1u : 0u);
-                            }
-                        }
+                        for (int mi = 0; mi < p.mmul; ++mi)
+                            issue_kstep<KIND>(d_tmem + (uint32_t)(mi * p.bnp), dhi, a_addr + mi * sub_bytes, b_addr, p.idesc,
+                                              kslices, i == 0);
                     }
                     ptx::mma_commit(empty_bar(s));
                 }
