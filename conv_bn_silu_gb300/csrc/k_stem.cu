@@ -132,11 +132,10 @@ __global__ void __launch_bounds__(256) stem_kernel(const StemLaunch a) {
     const Tin *x = static_cast<const Tin *>(a.x);
 
     float accf[P][COUT];
-    int acci[P][COUT];
 #pragma unroll
     for (int j = 0; j < P; ++j)
 #pragma unroll
-        for (int c = 0; c < COUT; ++c) { accf[j][c] = 0.0f; acci[j][c] = 0; }
+        for (int c = 0; c < COUT; ++c) accf[j][c] = 0.0f;
 
     const bool vec_in = IN_NHWC && a.c_pad == 4;  // one 4-channel vector load per tap
     for (int r = 0; r < a.KS; ++r) {
@@ -144,7 +143,6 @@ __global__ void __launch_bounds__(256) stem_kernel(const StemLaunch a) {
             const float *wt = wsm + (r * a.KS + s) * a.c_pad * COUT;
             // The tap's input channels of each pixel (zero outside the image).
             float xf[P][4];
-            int xi[P][4];
 #pragma unroll
             for (int j = 0; j < P; ++j) {
                 const int ih = oh[j] * a.stride - a.pad + r;
@@ -179,10 +177,7 @@ __global__ void __launch_bounds__(256) stem_kernel(const StemLaunch a) {
                     }
                 }
 #pragma unroll
-                for (int ci = 0; ci < 4; ++ci) {
-                    xf[j][ci] = to_f<Tin>(xv[ci]);
-                    xi[j][ci] = (int)xv[ci];
-                }
+                for (int ci = 0; ci < 4; ++ci) xf[j][ci] = to_f<Tin>(xv[ci]);
             }
 #pragma unroll
             for (int ci = 0; ci < 4; ++ci) {
@@ -191,21 +186,16 @@ __global__ void __launch_bounds__(256) stem_kernel(const StemLaunch a) {
 #pragma unroll
                 for (int c = 0; c < COUT / 4; ++c) {
                     const float4 w = w4[c];
-                    if (KIND == 2) {
-                        const int w0 = (int)w.x, w1 = (int)w.y, w2 = (int)w.z, w3 = (int)w.w;
+                    // INT8 too: codes are exact in float, every product
+                    // |q_x q_w| <= 16256 and a sum of at most 7*7*4 = 196 of
+                    // them stays below 2^24, so the float accumulation is the
+                    // exact integer sum (and runs at the FMA rate, twice IMAD's).
 #pragma unroll
-                        for (int j = 0; j < P; ++j) {
-                            acci[j][4 * c] += xi[j][ci] * w0; acci[j][4 * c + 1] += xi[j][ci] * w1;
-                            acci[j][4 * c + 2] += xi[j][ci] * w2; acci[j][4 * c + 3] += xi[j][ci] * w3;
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < P; ++j) {
-                            accf[j][4 * c] = fmaf(xf[j][ci], w.x, accf[j][4 * c]);
-                            accf[j][4 * c + 1] = fmaf(xf[j][ci], w.y, accf[j][4 * c + 1]);
-                            accf[j][4 * c + 2] = fmaf(xf[j][ci], w.z, accf[j][4 * c + 2]);
-                            accf[j][4 * c + 3] = fmaf(xf[j][ci], w.w, accf[j][4 * c + 3]);
-                        }
+                    for (int j = 0; j < P; ++j) {
+                        accf[j][4 * c] = fmaf(xf[j][ci], w.x, accf[j][4 * c]);
+                        accf[j][4 * c + 1] = fmaf(xf[j][ci], w.y, accf[j][4 * c + 1]);
+                        accf[j][4 * c + 2] = fmaf(xf[j][ci], w.z, accf[j][4 * c + 2]);
+                        accf[j][4 * c + 3] = fmaf(xf[j][ci], w.w, accf[j][4 * c + 3]);
                     }
                 }
             }
@@ -234,7 +224,7 @@ __global__ void __launch_bounds__(256) stem_kernel(const StemLaunch a) {
 #pragma unroll
         for (int c = 0; c < COUT; ++c) {
             if (KIND == 2)
-                oq[c] = c < a.Cout ? requant_i8(acci[j][c] + bias_i[c], mc[c], a.inv_s_y) : 0;
+                oq[c] = c < a.Cout ? requant_i8(__float2int_rn(accf[j][c]) + bias_i[c], mc[c], a.inv_s_y) : 0;
             else
                 of[c] = silu_fast(accf[j][c] + bias_f[c]);
         }
