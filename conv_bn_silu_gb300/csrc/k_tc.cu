@@ -719,7 +719,8 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t *base_ptr = smem_raw + (base - raw_addr);
     const int S = p.stages;
-    // Stage s: [operand A bf16 | operand B bf16 | staging A int8], each 1024-aligned.
+    // Stage s holds kg K steps: [kg x operand A bf16 | kg x operand B bf16 |
+    // kg x staging A int8], each block 1024-aligned.
     // Barriers: raw_full[S], conv_done[S], free[S], acc_full[2], acc_empty[2], drain.
     const uint32_t bars = base + S * p.stage_bytes;
     uint64_t *bar_ptr = reinterpret_cast<uint64_t *>(base_ptr + S * p.stage_bytes);
@@ -732,11 +733,13 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     auto accf_bar = [&](int a) { return bars + 8u * (3 * S + a); };
     auto acce_bar = [&](int a) { return bars + 8u * (3 * S + 2 + a); };
     const uint32_t drain_bar = bars + 8u * (3 * S + 4);
-    const int op_b_off = p.a_bytes;
-    const int stg_off = (p.a_bytes + p.b_bytes + 1023) & ~1023;
+    const int kg = p.kg;
+    const int op_b_off = kg * p.a_bytes;                              // a_bytes = 128 x RB: 1 KB multiple
+    const int stg_off = op_b_off + kg * p.b_tile_stride;
+    const int stg_stride = (p.stg_bytes + 1023) & ~1023;
+    const int nstage = p.ksteps / kg;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nk = p.ksteps;
     const int num_tiles = p.m_tiles * p.n_tiles;
 
     if (threadIdx.x == 0) {
@@ -766,9 +769,11 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     int last_g = -1;
     if (warp < kMaxProducersI8) {
-        // Producer warp `warp` takes the K steps g with g % nprod == warp
+        // Producer warp `warp` takes the stages g with g % nprod == warp
         // (nprod divides the stage count: one warp per stage, no aliasing).
-        if (lane == 0 && warp < p.nprod) {
+        // Lane l issues box l of the stage: A boxes (int8 staging) first,
+        // then B boxes; TMA issue throughput scales with issuing lanes.
+        if (warp < p.nprod) {
             int g = 0;
             for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
                 int m0, n0;
@@ -778,25 +783,38 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const int oh = rem / p.OW, ow = rem - (rem / p.OW) * p.OW;
                 const int wc = ow * p.stride - p.pad, hc = oh * p.stride - p.pad;
                 bool ok = true;
-                for (int i = 0; i < nk; ++i, ++g) {
+                for (int st = 0; st < nstage; ++st, ++g) {
                     if (g % p.nprod != warp) continue;
                     const int s = g % S, u = g / S;
-                    if (!ptx::mbar_wait_bounded(free_bar(s), (u & 1) ^ 1, kWaitLimitNs)) {
-                        abort_now(p, abort_flag);
+                    bool got = true;
+                    if (lane == 0) got = ptx::mbar_wait_bounded(free_bar(s), (u & 1) ^ 1, kWaitLimitNs) && !aborted(abort_flag);
+                    got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                    if (!got) {
+                        if (lane == 0 && !aborted(abort_flag)) abort_now(p, abort_flag);
                         ok = false;
                         break;
                     }
-                    if (aborted(abort_flag)) { ok = false; break; }
-                    const int tap = i / p.cblocks, cb = i - tap * p.cblocks;
-                    const int r = tap / p.ks, tt = tap - r * p.ks;
-                    const uint32_t st = base + s * p.stage_bytes;
-                    ptx::mbar_arrive_expect_tx(raw_bar(s), (uint32_t)(p.stg_bytes + p.b_bytes));
-                    if (p.im2col)
-                        ptx::tma_load_im2col_4d(st + stg_off, &tmA, raw_bar(s), cb * p.CB, wc, hc, img, (uint16_t)tt,
-                                                (uint16_t)r);
-                    else
-                        ptx::tma_load_2d(st + stg_off, &tmA, raw_bar(s), cb * p.CB, m0);
-                    ptx::tma_load_2d(st + op_b_off, &tmB, raw_bar(s), tap * p.c_in_pad + cb * p.CB, n0);
+                    const uint32_t sb = base + s * p.stage_bytes;
+                    if (lane == 0) ptx::mbar_arrive_expect_tx(raw_bar(s), (uint32_t)(kg * (p.stg_bytes + p.b_bytes)));
+                    __syncwarp();
+                    if (lane < 2 * kg) {
+                        const bool is_a = lane < kg;
+                        const int kk = is_a ? lane : lane - kg;
+                        const int i = st * kg + kk;
+                        const int tap = i / p.cblocks, cb = i - tap * p.cblocks;
+                        if (is_a) {
+                            const int r = tap / p.ks, tt = tap - r * p.ks;
+                            const uint32_t dst = sb + stg_off + kk * stg_stride;
+                            if (p.im2col)
+                                ptx::tma_load_im2col_4d(dst, &tmA, raw_bar(s), cb * p.CB, wc, hc, img, (uint16_t)tt,
+                                                        (uint16_t)r);
+                            else
+                                ptx::tma_load_2d(dst, &tmA, raw_bar(s), cb * p.CB, m0);
+                        } else {
+                            ptx::tma_load_2d(sb + op_b_off + kk * p.b_tile_stride, &tmB, raw_bar(s),
+                                             tap * p.c_in_pad + cb * p.CB, n0);
+                        }
+                    }
                     last_g = g;
                 }
                 if (!ok) break;
@@ -806,6 +824,7 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         if (lane == 0) {
             const uint32_t sbo = 8u * p.RB;
             const int kslices = p.RB / 32;
+            const uint64_t dhi = ptx::smem_desc(0u, 16u, sbo, p.swz);
             int g = 0, j = 0;
             for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x, ++j) {
                 const int acc = j & 1, ua = j >> 1;
@@ -815,8 +834,10 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
                 ptx::tc_fence_after();
                 bool ok = true;
-                for (int i = 0; i < nk; ++i, ++g) {
+                for (int st = 0; st < nstage; ++st, ++g) {
                     const int s = g % S, u = g / S;
+                    // conv_done follows raw_full (the converters waited on it),
+                    // and raw_full also carries the B tiles.
                     if (!ptx::mbar_wait_bounded(conv_bar(s), u & 1, kWaitLimitNs) ||
                         !ptx::mbar_wait_bounded(raw_bar(s), u & 1, kWaitLimitNs)) {
                         abort_now(p, abort_flag);
@@ -824,15 +845,13 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         break;
                     }
                     ptx::tc_fence_after();
-                    const int chunk = i / p.kpc;
-                    const bool first_of_chunk = (i % p.kpc) == 0;
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_stride + chunk * p.chunk_stride);
-                    const uint32_t a_addr = base + s * p.stage_bytes;
-                    const uint32_t b_addr = a_addr + op_b_off;
-                    for (int k = 0; k < kslices; ++k) {
-                        const uint64_t ad = ptx::smem_desc(a_addr + 32u * k, 16u, sbo, p.swz);
-                        const uint64_t bd = ptx::smem_desc(b_addr + 32u * k, 16u, sbo, p.swz);
-                        ptx::mma_f16(d_tmem, ad, bd, p.idesc, (first_of_chunk && k == 0) ? 0u : 1u);
+                    const uint32_t sb = base + s * p.stage_bytes;
+                    for (int kk = 0; kk < kg; ++kk) {
+                        const int i = st * kg + kk;
+                        const int chunk = i / p.kpc;
+                        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_stride + chunk * p.chunk_stride);
+                        issue_kstep<kBF16>(d_tmem, dhi, sb + kk * p.a_bytes, sb + op_b_off + kk * p.b_tile_stride, p.idesc,
+                                           kslices, (i % p.kpc) == 0);
                     }
                     ptx::mma_commit(free_bar(s));
                 }
@@ -849,16 +868,17 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         int g = 0;
         for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
             bool ok = true;
-            for (int i = 0; i < nk; ++i, ++g) {
+            for (int st = 0; st < nstage; ++st, ++g) {
                 const int s = g % S, u = g / S;
                 if (!ptx::mbar_wait_bounded(raw_bar(s), u & 1, kWaitLimitNs)) {
                     abort_now(p, abort_flag);
                     ok = false;
                     break;
                 }
-                const uint32_t st = base + s * p.stage_bytes;
-                const uint32_t src_row = st + stg_off + row * in_bytes;
-                const uint32_t dst_row = st + row * p.RB;
+                const uint32_t sb = base + s * p.stage_bytes;
+                for (int kk = 0; kk < kg; ++kk) {
+                const uint32_t src_row = sb + stg_off + kk * stg_stride + row * in_bytes;
+                const uint32_t dst_row = sb + kk * p.a_bytes + row * p.RB;
                 for (int c = 0; c < in_bytes; c += 16) {
                     uint32_t w0, w1, w2, w3;
                     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -877,6 +897,7 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(swz(dst_row + 2 * c + 16, p.op_mask)),
                                  "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
                                  : "memory");
+                }
                 }
                 // Make the generic-proxy writes visible to the tensor cores.
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1246,18 +1267,46 @@ cbs_status plan_tc(cbs_plan_t &p) {
             if (BN > max_bn)
                 return fail(CBS_ERR_UNSUPPORTED, "block_n %d with %d exact-sum chunks exceeds TMEM", BN, nchunks);
         } else {
-            BN = round_up(d.c_out, 16) < max_bn ? round_up(d.c_out, 16) : max_bn;
-            if (BN < 16) return fail(CBS_ERR_UNSUPPORTED, "INT8: %d exact-sum chunks exceed TMEM", nchunks);
+            const int full = round_up(d.c_out, 16) < max_bn ? round_up(d.c_out, 16) : max_bn;
+            if (full < 16) return fail(CBS_ERR_UNSUPPORTED, "INT8: %d exact-sum chunks exceed TMEM", nchunks);
+            // Waves of tiles over the SMs x the MMA cost of a tile (flat below
+            // N = 64): fewer, wider tiles unless they leave SMs idle.
+            BN = full;
+            double best = 1e300;
+            for (int c : {full, 256, 192, 128, 96, 64}) {
+                if (c > full || c < 16) continue;
+                const long long tiles = (long long)p.m_tiles * ((d.c_out + c - 1) / c);
+                const double cost = (double)((tiles + kNumSMs - 1) / kNumSMs) * (c > 64 ? c : 64);
+                if (cost < best * 0.99) { best = cost; BN = c; }
+            }
         }
         p.block_m = kBM;
         p.block_n = BN;
         p.n_tiles = ceil_div(d.c_out, BN);
-        p.k_group = 1;
         p.b_resident = 0;
-        int stage = round_up(kBM * RB + BN * RB, 1024) + round_up(kBM * CB, 1024);  // + int8 staging tile
+        // One K step: bf16 operand A, bf16 weights, int8 staging tile.  The
+        // MMA issuer waits twice per stage, so a stage carries the most K
+        // steps (up to 4, dividing the K steps) that still leave 3 stages.
+        const int kstep_bytes = kBM * RB + round_up(BN * RB, 1024) + round_up(kBM * CB, 1024);
+        int kg = 1;
+        for (int c = 4; c >= 1; --c) {
+            if (d.force_k_group > 0 && c != d.force_k_group) continue;
+            if (ksteps % c == 0 && ((200 * 1024) / (c * kstep_bytes) >= 2 || c == 1 || d.force_k_group > 0)) {
+                kg = c;
+                break;
+            }
+        }
+        if (d.force_k_group > 0 && kg != d.force_k_group)
+            return fail(CBS_ERR_UNSUPPORTED, "INT8: k_group %d does not divide %d K steps", d.force_k_group, ksteps);
+        p.k_group = kg;
+        const int stage = kg * kstep_bytes;
         int stages = (200 * 1024) / stage;
         if (stages > 32) stages = 32;
-        if (stages < 2) stages = 2;
+        if (stages < 2) {
+            if (2 * stage > kSmemBudget)
+                return fail(CBS_ERR_UNSUPPORTED, "INT8: two stages of %d K steps do not fit shared memory", kg);
+            stages = 2;
+        }
         int nprod = kMaxProducersI8;
         while (nprod > 1 && (stages < 2 * nprod)) nprod /= 2;
         stages = stages / nprod * nprod;
@@ -1363,7 +1412,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     if (pl.block_m != kBM * mmul || mmul < 1 || mmul > 2) return fail(CBS_ERR_PLAN_MISMATCH, "block_m %d", pl.block_m);
     P.mmul = mmul;
     P.win = i8 ? 0 : pl.window;
-    P.kg = (i8 || P.win) ? 1 : pl.k_group;
+    P.kg = P.win ? 1 : pl.k_group;
     P.b_res = i8 ? 0 : pl.b_resident;
     P.SB = (P.win && !P.b_res) ? pl.k_group : 0;
     if (P.kg < 1 || P.ksteps % P.kg) return fail(CBS_ERR_PLAN_MISMATCH, "k_group %d", pl.k_group);
@@ -1386,7 +1435,9 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
         int nprod = kMaxProducersI8;
         while (nprod > 1 && (pl.stages < 2 * nprod || pl.stages % nprod != 0)) nprod /= 2;
         P.nprod = nprod;
-        P.stage_bytes = round_up(P.a_bytes + P.b_bytes, 1024);
+        P.stage_bytes = P.kg * (P.a_bytes + P.b_tile_stride + round_up(kBM * CB, 1024));
+        if (1024 + pl.stages * P.stage_bytes + 8 * (3 * pl.stages + 5) + 16 > pl.smem_bytes)
+            return fail(CBS_ERR_PLAN_MISMATCH, "plan's shared memory does not hold its stages");
     } else {
         P.nprod = P.win ? tc_producers_max(pl.stages, P.b_res ? kMaxProducers : kMaxProducers - 1)
                         : tc_producers(pl.stages);
@@ -1406,7 +1457,6 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     }
     if (i8) {
         P.stg_bytes = kBM * CB;
-        P.stage_bytes += round_up(P.stg_bytes, 1024);
         P.kpc = 1024 / CB;
         P.nchunks = ceil_div(P.ksteps, P.kpc);
         P.stg_mask = XB == 64 ? 3u : XB == 32 ? 1u : 0u;

@@ -115,6 +115,32 @@ def test_ragged(cuda_lib, shape):
     assert_bit_exact(spec, x, p, 0.05, shape)
 
 
+
+@pytest.mark.parametrize("kg", [1, 2, 3, 4])
+@pytest.mark.parametrize("shape,bn", [
+    ((1, 128, 64, 3, 1, 9), 64),     # 18 K steps, two exact-sum chunks: a 3-step stage spans the boundary
+    ((1, 256, 96, 3, 1, 5), 48),     # 36 K steps, three chunks, two N tiles
+    ((2, 32, 32, 3, 2, 13), 32),     # 9 K steps of 32 channels
+])
+def test_k_steps_per_stage(cuda_lib, shape, bn, kg):
+    """Several K steps per pipeline stage, including stages that straddle an
+    exact-sum chunk boundary (each K step picks its chunk's accumulator)."""
+    n, c_in, c_out, k, stride, h = shape
+    spec = wl.LayerSpec(c_in, c_out, k, stride, h)
+    x, p = wl.layer_inputs(spec, n, layer_index=14)
+    ksteps = k * k * (c_in // (64 if c_in % 64 == 0 else 32))
+    if ksteps % kg:
+        with pytest.raises(B.CbsError):
+            build(spec, n, p, force_k_group=kg, force_block_n=bn)
+        return
+    try:
+        layer = build(spec, n, p, force_k_group=kg, force_block_n=bn)
+    except B.CbsError as e:   # two stages of kg K steps exceed shared memory
+        assert e.status == B.CBS_ERR_UNSUPPORTED and kg == 4
+        return
+    assert layer.plan.k_group == kg and layer.plan.block_n == bn
+    assert_bit_exact(spec, x, p, 0.05, (shape, kg), force_k_group=kg, force_block_n=bn)
+
 def test_nchw_output(cuda_lib):
     spec = wl.LayerSpec(32, 48, 3, 1, 10)
     x, p = wl.layer_inputs(spec, 2, layer_index=2)
