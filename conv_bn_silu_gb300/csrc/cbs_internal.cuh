@@ -19,6 +19,18 @@ constexpr int kNumSMs = 152;
 // valid whatever other launches set afterwards.
 constexpr int kMaxDynSmem = 227 * 1024;
 
+// Raises `kern`'s dynamic shared memory ceiling to the per-block maximum less
+// its static shared memory, and checks that `bytes` fit under it.
+template <typename F>
+cudaError_t set_max_dyn_smem(F *kern, int bytes) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    const int cap = kMaxDynSmem - (int)fa.sharedSizeBytes;
+    if (bytes > cap) return cudaErrorInvalidValue;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cap);
+}
+
 // Records a message for the calling thread and returns `s`.
 cbs_status fail(cbs_status s, const char *fmt, ...);
 // Maps a CUDA error to CBS_ERR_CUDA (with message) or CBS_OK.

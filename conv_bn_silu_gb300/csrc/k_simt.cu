@@ -291,8 +291,7 @@ cudaError_t launch_one(dim3 grid, const SimtLaunch &L, cudaStream_t s) {
     const int bytes = tile_bytes + kpad * (int)sizeof(KEntry);
     auto kern = simt_conv_kernel<BM, BN, TM, TN, kSimtBK, IN_NHWC, OUT_NHWC>;
     if (bytes > 48 * 1024) {
-        if (bytes > kMaxDynSmem) return cudaErrorInvalidValue;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        cudaError_t e = set_max_dyn_smem(kern, bytes);
         if (e != cudaSuccess) return e;
     }
     kern<<<grid, NT, bytes, s>>>(L);

@@ -239,12 +239,11 @@ cudaError_t launch_kind(const StemLaunch &L, cudaStream_t s) {
     const int grid = (int)((total + 256 * P - 1) / (256 * P));
     const int smem = L.KS * L.KS * L.c_pad * COUT * (int)sizeof(float);
     if (smem > 48 * 1024) {  // 7x7 filters with 64 output channels need 49 KB of weights
-        if (smem > kMaxDynSmem) return cudaErrorInvalidValue;
-        cudaError_t e = cudaSuccess;
-        if (L.in_nhwc && L.out_nhwc) e = cudaFuncSetAttribute(stem_kernel<KIND, COUT, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
-        else if (L.in_nhwc) e = cudaFuncSetAttribute(stem_kernel<KIND, COUT, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
-        else if (L.out_nhwc) e = cudaFuncSetAttribute(stem_kernel<KIND, COUT, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
-        else e = cudaFuncSetAttribute(stem_kernel<KIND, COUT, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        cudaError_t e;
+        if (L.in_nhwc && L.out_nhwc) e = set_max_dyn_smem(stem_kernel<KIND, COUT, true, true>, smem);
+        else if (L.in_nhwc) e = set_max_dyn_smem(stem_kernel<KIND, COUT, true, false>, smem);
+        else if (L.out_nhwc) e = set_max_dyn_smem(stem_kernel<KIND, COUT, false, true>, smem);
+        else e = set_max_dyn_smem(stem_kernel<KIND, COUT, false, false>, smem);
         if (e != cudaSuccess) return e;
     }
     if (L.in_nhwc && L.out_nhwc) stem_kernel<KIND, COUT, true, true><<<grid, 256, smem, s>>>(L);

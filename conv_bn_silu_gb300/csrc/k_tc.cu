@@ -1547,13 +1547,13 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     if (pl.smem_bytes > kMaxDynSmem) return fail(CBS_ERR_UNSUPPORTED, "plan needs %d bytes of shared memory", pl.smem_bytes);
     cudaError_t e;
     if (pl.variant == CBS_VARIANT_TC_TF32) {
-        e = cudaFuncSetAttribute(tc_conv_kernel<kTF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        e = set_max_dyn_smem(tc_conv_kernel<kTF32>, pl.smem_bytes);
         if (e == cudaSuccess) tc_conv_kernel<kTF32><<<grid, kThreads, pl.smem_bytes, s>>>(tmA, tmB, tmY, P);
     } else if (pl.variant == CBS_VARIANT_TC_BF16) {
-        e = cudaFuncSetAttribute(tc_conv_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        e = set_max_dyn_smem(tc_conv_kernel<kBF16>, pl.smem_bytes);
         if (e == cudaSuccess) tc_conv_kernel<kBF16><<<grid, kThreads, pl.smem_bytes, s>>>(tmA, tmB, tmY, P);
     } else {
-        e = cudaFuncSetAttribute(tc_conv_i8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        e = set_max_dyn_smem(tc_conv_i8_kernel, pl.smem_bytes);
         if (e == cudaSuccess) tc_conv_i8_kernel<<<grid, kThreadsI8, pl.smem_bytes, s>>>(tmA, tmB, P);
     }
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute");

@@ -9,6 +9,7 @@ from __future__ import annotations
 import torch
 
 from . import _binding as B
+from . import tuning
 
 _TORCH_DTYPE = {B.CBS_FP32: torch.float32, B.CBS_TF32: torch.float32,
                 B.CBS_BF16: torch.bfloat16, B.CBS_INT8: torch.int8}
@@ -48,9 +49,12 @@ class FusedConvBnSilu:
     """One planned layer with its folded weights resident on the device."""
 
     def __init__(self, desc: B.cbs_layer_desc, w, gamma, beta, mean, var, eps: float,
-                 conv_bias=None, s_x: float = 0.0, device="cuda"):
+                 conv_bias=None, s_x: float = 0.0, device="cuda", tuned: bool = True):
+        """tuned: take the measured configuration of tuning.py's table when
+        the shape is in it and `desc` forces nothing."""
         self.device = torch.device(device)
-        self.desc = desc
+        self.desc = tuning.tuned_desc(desc) if tuned else desc
+        desc = self.desc
         self.plan = B.cbs_plan(desc)
         self.prec = desc.prec
         self.s_x = float(s_x)

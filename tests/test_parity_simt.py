@@ -75,6 +75,19 @@ def test_forced_tiles(cuda_lib, bn):
     assert rel_l2(y, ref_of(spec, x, p)) <= TOL_FP32_REL_L2
 
 
+@pytest.mark.parametrize("bm,bn,split", [(128, 128, 1), (128, 128, 4), (128, 64, 2), (256, 16, 3)])
+@pytest.mark.parametrize("layouts", [(B.CBS_NCHW, B.CBS_NCHW), (B.CBS_NHWC, B.CBS_NHWC)])
+def test_forced_large_tiles(cuda_lib, bm, bn, split, layouts):
+    """Tiles whose shared memory exceeds 48 KB (128x128: the staged output
+    tile alone is 67 KB) run with the raised dynamic shared-memory ceiling."""
+    spec = wl.LayerSpec(64, 160, 3, 1, 21)
+    x, p = wl.layer_inputs(spec, 2, layer_index=5)
+    y, layer = run_simt(spec, x, p, in_layout=layouts[0], out_layout=layouts[1], force_block_m=bm,
+                        force_block_n=bn, force_split_k=split)
+    assert (layer.plan.block_m, layer.plan.block_n, layer.plan.split_k) == (bm, bn, split)
+    assert rel_l2(y, ref_of(spec, x, p)) <= TOL_FP32_REL_L2
+
+
 @pytest.mark.parametrize("layouts", [(B.CBS_NHWC, B.CBS_NHWC), (B.CBS_NCHW, B.CBS_NHWC), (B.CBS_NHWC, B.CBS_NCHW)])
 def test_layouts(cuda_lib, layouts):
     spec = wl.LayerSpec(24, 40, 3, 1, 17)

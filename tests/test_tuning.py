@@ -1,0 +1,48 @@
+"""The measured plan table: lookup rules, and every entry plans on the host."""
+import json
+
+import pytest
+
+from conv_bn_silu_gb300 import _binding as B
+from conv_bn_silu_gb300 import tuning
+from conv_bn_silu_gb300.layer import make_desc
+
+
+def test_key_and_copy_rules(cuda_lib):
+    d = make_desc(16, 64, 80, 80, 64, 3, 1, prec=B.CBS_BF16)
+    key = tuning.shape_key(d)
+    table = {key: {"force": {"force_block_m": 256, "force_k_group": 1, "force_block_n": 64}}}
+    t = tuning.tuned_desc(d, table)
+    assert (t.force_block_m, t.force_k_group, t.force_block_n) == (256, 1, 64)
+    assert d.force_block_m == 0                      # the caller's descriptor is not modified
+    # a descriptor that forces anything is left as it is
+    f = make_desc(16, 64, 80, 80, 64, 3, 1, prec=B.CBS_BF16, force_block_n=32)
+    assert tuning.tuned_desc(f, table) is f
+    # other shapes (batch, layout, precision) do not match
+    for other in (make_desc(1, 64, 80, 80, 64, 3, 1, prec=B.CBS_BF16),
+                  make_desc(16, 64, 80, 80, 64, 3, 1, prec=B.CBS_TF32),
+                  make_desc(16, 64, 80, 80, 64, 3, 1, prec=B.CBS_BF16, out_layout=B.CBS_NCHW)):
+        assert tuning.shape_key(other) != key
+        assert tuning.tuned_desc(other, table) is other
+    with pytest.raises(ValueError):
+        tuning.tuned_desc(d, {key: {"force": {"block_m": 1}}})
+
+
+def test_every_table_entry_plans(cuda_lib):
+    """The committed table's configurations are valid plans for their shapes."""
+    table = tuning.load_table()
+    for key, entry in table.items():
+        prec, n, c_in, c_out, k, s, pad, h, w, il, ol = (int(v) for v in key.split(":"))
+        d = make_desc(n, c_in, h, w, c_out, k, s, pad, prec=prec, in_layout=il, out_layout=ol)
+        t = tuning.tuned_desc(d, table)
+        p = B.cbs_plan(t)
+        assert entry["us"] <= entry["auto_us"], key
+        if "force_block_m" in entry["force"]:
+            assert p.block_m == entry["force"]["force_block_m"], key
+
+
+def test_table_file_is_well_formed():
+    with open(tuning.TABLE_PATH) as f:
+        meta = json.load(f)
+    assert meta["created_by"] == "conv_bn_silu_gb300/autotune.py"
+    assert isinstance(meta["plans"], dict)
