@@ -99,9 +99,12 @@ WORKLOADS = {
     "chain_fp32_n1": dict(kind="chain", n=1, prec="fp32"),
     "chain_bf16_n16": dict(kind="chain", n=16, prec="bf16"),
     "chain_tf32_n16": dict(kind="chain", n=16, prec="tf32"),
+    # The list with the residual form of the epilogue, y = SiLU(BN(conv)) + r, on every
+    # stride-1 layer whose input and output shapes match (a bottleneck's skip add).
+    "layer_list_bf16_n16_residual": dict(kind="list", layers=wl.LAYER_LIST, n=16, prec="bf16", residual=True),
 }
 EXTRA_DEFAULT = ("layer_list_bf16_n16", "layer_list_tf32_n16", "layer_list_int8_n16", "chain_fp32_n1",
-                 "chain_bf16_n16")
+                 "chain_bf16_n16", "layer_list_bf16_n16_residual")
 
 
 # DRAM traffic of the dominant kernel over one step of a workload, from one
@@ -168,16 +171,19 @@ class ListWorkload:
         self.layers, host_x = [], []
         s_x = float(wl.S_X_INT8) if self.prec == "int8" else 0.0
         self.s_y = int8_scales() if self.prec == "int8" else [None] * len(self.specs)
+        self.res = [bool(cfg.get("residual")) and s.c_in == s.c_out and s.stride == 1 for s in self.specs]
         for i, spec in enumerate(self.specs):
             x, p = wl.layer_inputs(spec, self.n, seed=0, layer_index=i)
             desc = make_desc(self.n, spec.c_in, spec.h, spec.width, spec.c_out, spec.k, spec.stride, spec.pad,
-                             prec=cp)
+                             prec=cp, residual=int(self.res[i]))
             self.layers.append(FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, s_x=s_x,
                                                device=device))
             host_x.append(x)
         self.host_x = host_x
         ab = act_bytes(self.prec)
-        self.step_bytes = sum(s.alg_bytes(self.n, ab) for s in self.specs)
+        # a residual layer also reads r (the output's size)
+        self.extra_bytes = [self.n * s.c_out * s.oh * s.ow * ab if r else 0 for s, r in zip(self.specs, self.res)]
+        self.step_bytes = sum(s.alg_bytes(self.n, ab) for s in self.specs) + sum(self.extra_bytes)
         self.R = max(2, int(np.ceil(2 * L2_BYTES / self.step_bytes)) + 1)
         packed = []
         for layer, x in zip(self.layers, host_x):
@@ -186,13 +192,16 @@ class ListWorkload:
         torch.cuda.synchronize()
         self.xs = [[t.clone() for t in packed] for _ in range(self.R)]
         self.ys = [[layer.empty_y() for layer in self.layers] for _ in range(self.R)]
+        self.rs = [[layer.empty_y().normal_() if r else None for layer, r in zip(self.layers, self.res)]
+                   for _ in range(self.R)]
         self.launches_per_step = len(self.layers)
 
     def step(self, r, stream_id, events=None, stream=None):
         for j, layer in enumerate(self.layers):
             if events is not None:
                 events[j].record(stream)
-            layer(self.xs[r % self.R][j], self.ys[r % self.R][j], s_y=self.s_y[j], stream=stream_id)
+            layer(self.xs[r % self.R][j], self.ys[r % self.R][j], s_y=self.s_y[j], stream=stream_id,
+                  residual=self.rs[r % self.R][j])
         if events is not None:
             events[len(self.layers)].record(stream)
 
@@ -303,11 +312,12 @@ def measure(name, steps, warmup, device, peaks, sample_clocks=False):
     peak, peak_label = peak_for(prec, peaks)
     hbm = float(peaks["hbm_gbs"])
     rows = []
+    extra = getattr(w, "extra_bytes", None) or [0] * len(w.layers)
     for j, (sp, layer) in enumerate(w.rows()):
-        f, by = sp.flops(n), sp.alg_bytes(n, ab)
+        f, by = sp.flops(n), sp.alg_bytes(n, ab) + extra[j]
         t_c, t_m = f / (peak * 1e12), by / (hbm * 1e9)
         bound = "compute" if t_c >= t_m else "hbm"
-        row = {"layer": j + 1, "shape": f"{sp.c_in}->{sp.c_out} k{sp.k} s{sp.stride} {sp.h}",
+        row = {"layer": j + 1, "shape": f"{sp.c_in}->{sp.c_out} k{sp.k} s{sp.stride} {sp.h}" + (" +r" if extra[j] else ""),
                "tile": f"{layer.plan.block_m}x{layer.plan.block_n}", "split_k": layer.plan.split_k,
                "mflop": round(f / 1e6, 2), "alg_mb": round(by / 1e6, 3), "bound": bound,
                "roofline_us": round(max(t_c, t_m) * 1e6, 3)}

@@ -25,11 +25,12 @@ CBS_NCHW, CBS_NHWC = 0, 1
 CBS_FP32, CBS_TF32, CBS_BF16, CBS_INT8 = 0, 1, 2, 3
 CBS_VARIANT_SIMT_FP32, CBS_VARIANT_TC_TF32, CBS_VARIANT_TC_BF16, CBS_VARIANT_TC_INT8 = 0, 1, 2, 3
 CBS_VARIANT_STEM = 4
+CBS_ACT_SILU, CBS_ACT_IDENTITY = 0, 1
 
 EXPORTED = (
     "cbs_plan", "cbs_fold_bn", "cbs_pack_input", "cbs_conv_bn_silu_f32", "cbs_conv_bn_silu_i8",
     "cbs_upsample2x_concat", "cbs_workspace_init", "cbs_read_device_status", "cbs_status_string",
-    "cbs_last_error", "cbs_abi_version", "cbs_conv_bn_silu_f32_noalloc",
+    "cbs_last_error", "cbs_abi_version", "cbs_conv_bn_silu_f32_noalloc", "cbs_conv_bn_act",
 )
 
 
@@ -37,7 +38,7 @@ class cbs_layer_desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "n", "c_in", "h", "w", "c_out", "k", "stride", "pad", "in_layout", "out_layout", "prec",
         "force_variant", "force_split_k", "force_block_n", "force_block_m", "out_row_stride",
-        "force_k_group", "force_b_resident", "force_window")]
+        "force_k_group", "force_b_resident", "force_window", "activation", "residual")]
 
 
 class cbs_plan_t(ctypes.Structure):
@@ -72,6 +73,7 @@ def lib():
         L.cbs_fold_bn.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P, P, F, F, P, P, P, P]
         L.cbs_pack_input.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, F, P]
         L.cbs_conv_bn_silu_f32.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P, Z, P]
+        L.cbs_conv_bn_act.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P, P, Z, P]
         L.cbs_conv_bn_silu_i8.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, F, P, P, Z, P]
         L.cbs_upsample2x_concat.argtypes = [P, I, P, I, P, I, I, I, I, I, P]
         L.cbs_conv_bn_silu_f32_noalloc.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P]
@@ -142,6 +144,11 @@ def cbs_conv_bn_silu_f32(plan, x, w_packed, bias, y, workspace, workspace_bytes,
     _check(lib().cbs_conv_bn_silu_f32(ctypes.byref(plan), _p(x), _p(w_packed), _p(bias), _p(y),
                                       _p(workspace), workspace_bytes, stream),
            "cbs_conv_bn_silu_f32")
+
+
+def cbs_conv_bn_act(plan, x, w_packed, bias, residual, y, workspace, workspace_bytes, stream):
+    _check(lib().cbs_conv_bn_act(ctypes.byref(plan), _p(x), _p(w_packed), _p(bias), _p(residual), _p(y),
+                                 _p(workspace), workspace_bytes, stream), "cbs_conv_bn_act")
 
 
 def cbs_conv_bn_silu_i8(plan, x, w_packed, bias_i32, m_c, s_y, y, workspace, workspace_bytes,

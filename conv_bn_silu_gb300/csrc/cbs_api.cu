@@ -157,6 +157,8 @@ StemLaunch stem_launch(const cbs_plan_t &p, const void *x, const void *w, const 
     L.out_nhwc = d.out_layout == CBS_NHWC;
     L.out_row_stride = p.out_row_stride;
     L.kind = d.prec == CBS_INT8 ? 2 : (d.prec == CBS_BF16 ? 1 : 0);
+    L.act = d.activation;
+    L.residual = nullptr;
     return L;
 }
 
@@ -201,6 +203,11 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
         (D.out_layout != CBS_NCHW && D.out_layout != CBS_NHWC))
         return fail(CBS_ERR_INVALID_ARG, "unknown layout");
     if (D.prec < CBS_FP32 || D.prec > CBS_INT8) return fail(CBS_ERR_INVALID_ARG, "unknown precision %d", D.prec);
+    if (D.activation != CBS_ACT_SILU && D.activation != CBS_ACT_IDENTITY)
+        return fail(CBS_ERR_INVALID_ARG, "unknown activation %d", D.activation);
+    if (D.residual != 0 && D.residual != 1) return fail(CBS_ERR_INVALID_ARG, "residual must be 0 or 1");
+    if (D.prec == CBS_INT8 && (D.activation != CBS_ACT_SILU || D.residual))
+        return fail(CBS_ERR_UNSUPPORTED, "INT8: the specified requantising SiLU epilogue only");
 
     cbs_plan_t p;
     std::memset(&p, 0, sizeof(p));
@@ -345,17 +352,21 @@ static cbs_status check_conv_common(const cbs_plan_t *p, const void *x, const vo
     return CBS_OK;
 }
 
-cbs_status cbs_conv_bn_silu_f32(const cbs_plan_t *p, const void *x, const void *w_packed,
-                                const float *bias, void *y, void *workspace, size_t workspace_bytes,
-                                void *stream) {
-    CBS_TRY(check_plan(p));
-    if (p->desc.prec == CBS_INT8)
-        return fail(CBS_ERR_INVALID_ARG, "INT8 plans run through cbs_conv_bn_silu_i8");
+}  // extern "C"
+
+namespace {
+
+// The FP32 / TF32 / BF16 layer with the plan's activation and an optional
+// residual (already checked against the plan by the caller).
+cbs_status conv_act_impl(const cbs_plan_t *p, const void *x, const void *w_packed, const float *bias,
+                         const void *residual, void *y, void *workspace, size_t workspace_bytes, void *stream) {
     const cbs_layer_desc &d = p->desc;
     if (d.n == 0) return CBS_OK;  // empty batch: nothing is read or written
     CBS_TRY(check_conv_common(p, x, w_packed, bias, y, workspace, workspace_bytes));
+    if (residual && !aligned16(residual)) return fail(CBS_ERR_MISALIGNED, "residual is not 16-byte aligned");
     if (p->variant == CBS_VARIANT_STEM) {
-        const StemLaunch L = stem_launch(*p, x, w_packed, bias, nullptr, 0.0f, y);
+        StemLaunch L = stem_launch(*p, x, w_packed, bias, nullptr, 0.0f, y);
+        L.residual = residual;
         return cuda_check(launch_stem(L, (cudaStream_t)stream), "stem kernel launch");
     }
     if (p->variant == CBS_VARIANT_SIMT_FP32) {
@@ -375,6 +386,8 @@ cbs_status cbs_conv_bn_silu_f32(const cbs_plan_t *p, const void *x, const void *
         L.in_nhwc = d.in_layout == CBS_NHWC;
         L.out_nhwc = d.out_layout == CBS_NHWC;
         L.m_tiles = p->m_tiles; L.n_tiles = p->n_tiles;
+        L.act = d.activation;
+        L.residual = (const float *)residual;
         if (L.split > 1) {
             const size_t tiles = (size_t)p->m_tiles * p->n_tiles;
             const size_t counters = (tiles * sizeof(unsigned) + 255) / 256 * 256;
@@ -383,7 +396,34 @@ cbs_status cbs_conv_bn_silu_f32(const cbs_plan_t *p, const void *x, const void *
         }
         return cuda_check(launch_simt(L, (cudaStream_t)stream), "SIMT kernel launch");
     }
-    return launch_tc(*p, x, w_packed, bias, nullptr, 0.0f, y, workspace, (cudaStream_t)stream);
+    return launch_tc(*p, x, w_packed, bias, nullptr, 0.0f, residual, y, workspace, (cudaStream_t)stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+cbs_status cbs_conv_bn_silu_f32(const cbs_plan_t *p, const void *x, const void *w_packed,
+                                const float *bias, void *y, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+    CBS_TRY(check_plan(p));
+    if (p->desc.prec == CBS_INT8)
+        return fail(CBS_ERR_INVALID_ARG, "INT8 plans run through cbs_conv_bn_silu_i8");
+    if (p->desc.activation != CBS_ACT_SILU || p->desc.residual)
+        return fail(CBS_ERR_INVALID_ARG, "plan asks for another activation or a residual: call cbs_conv_bn_act");
+    return conv_act_impl(p, x, w_packed, bias, nullptr, y, workspace, workspace_bytes, stream);
+}
+
+cbs_status cbs_conv_bn_act(const cbs_plan_t *p, const void *x, const void *w_packed, const float *bias,
+                           const void *residual, void *y, void *workspace, size_t workspace_bytes, void *stream) {
+    CBS_TRY(check_plan(p));
+    if (p->desc.prec == CBS_INT8)
+        return fail(CBS_ERR_INVALID_ARG, "INT8 plans run through cbs_conv_bn_silu_i8");
+    if (p->desc.residual && !residual && p->desc.n > 0)
+        return fail(CBS_ERR_INVALID_ARG, "residual is NULL for a plan with a residual");
+    if (!p->desc.residual && residual)
+        return fail(CBS_ERR_INVALID_ARG, "residual given for a plan without one");
+    return conv_act_impl(p, x, w_packed, bias, residual, y, workspace, workspace_bytes, stream);
 }
 
 cbs_status cbs_conv_bn_silu_i8(const cbs_plan_t *p, const int8_t *x, const void *w_packed,
@@ -402,7 +442,7 @@ cbs_status cbs_conv_bn_silu_i8(const cbs_plan_t *p, const int8_t *x, const void 
         const StemLaunch L = stem_launch(*p, x, w_packed, bias_i32, m_c, inv_s_y, y);
         return cuda_check(launch_stem(L, (cudaStream_t)stream), "stem kernel launch");
     }
-    return launch_tc(*p, x, w_packed, bias_i32, m_c, inv_s_y, y, workspace, (cudaStream_t)stream);
+    return launch_tc(*p, x, w_packed, bias_i32, m_c, inv_s_y, nullptr, y, workspace, (cudaStream_t)stream);
 }
 
 cbs_status cbs_upsample2x_concat(const void *a, int ca, const void *b, int cb, void *out, int n, int h,

@@ -65,6 +65,8 @@ struct SimtLaunch {
     int tile;             // index into kSimtTiles
     int in_nhwc, out_nhwc;
     int m_tiles, n_tiles;
+    int act;                 // cbs_activation
+    const float *residual;   // nullable: added after the activation (same layout as y)
 };
 cudaError_t launch_simt(const SimtLaunch &L, cudaStream_t s);
 // Dynamic shared memory of one CUDA-core CTA (tiles + k table).
@@ -79,6 +81,8 @@ struct StemLaunch {
     int N, C, c_pad, H, W, Cout, OH, OW, KS, stride, pad;
     int in_nhwc, out_nhwc, out_row_stride;
     int kind;                  // 0 float, 1 bf16, 2 int8
+    int act;                   // cbs_activation (float kinds)
+    const void *residual;      // nullable, element type and layout of y (float kinds)
 };
 cudaError_t launch_stem(const StemLaunch &L, cudaStream_t s);
 constexpr int kStemMaxCin = 4, kStemMaxCout = 64, kStemMaxK = 7;
@@ -112,7 +116,7 @@ cbs_status read_and_reset_status(int *status_out, int reset, cudaStream_t s);
 // ---------------------------------------------------------------- tensor-core path
 struct TcLaunch;  // defined in k_tc.cu
 cbs_status launch_tc(const cbs_plan_t &p, const void *x, const void *w_packed,
-                     const void *bias, const float *m_c, float inv_s_y, void *y,
+                     const void *bias, const float *m_c, float inv_s_y, const void *residual, void *y,
                      void *workspace, cudaStream_t s);
 // Host-side tile selection for the tensor-core variants (fills the tile
 // fields of the plan); returns CBS_OK or an error.

@@ -72,6 +72,8 @@ cbs_status cbs_conv_bn_silu_f32_noalloc(const cbs_plan_t *p, const float *x, con
         return fail(CBS_ERR_PLAN_MISMATCH, "plan was not made by cbs_plan of this library");
     if (p->variant != CBS_VARIANT_SIMT_FP32)
         return fail(CBS_ERR_UNSUPPORTED, "the allocation-free entry point runs FP32 CUDA-core plans only");
+    if (p->desc.activation != CBS_ACT_SILU || p->desc.residual)
+        return fail(CBS_ERR_UNSUPPORTED, "the allocation-free entry point runs SiLU plans without a residual");
     if (p->workspace_bytes > kNoAllocScratchBytes)
         return fail(CBS_ERR_WORKSPACE, "plan needs %zu bytes of split-K scratch; the built-in scratch holds %zu",
                     p->workspace_bytes, kNoAllocScratchBytes);

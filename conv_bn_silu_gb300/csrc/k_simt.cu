@@ -246,7 +246,10 @@ simt_conv_kernel(const SimtLaunch a) {
         for (int g = 0; g < RG; ++g) {
             float v[4];
 #pragma unroll
-            for (int ii = 0; ii < 4; ++ii) v[ii] = silu_f32(acc[g * 4 + ii][j] + bvals[j]);
+            for (int ii = 0; ii < 4; ++ii) {
+                const float z = acc[g * 4 + ii][j] + bvals[j];
+                v[ii] = a.act == CBS_ACT_IDENTITY ? z : silu_f32(z);
+            }
             const int r0 = row_of(g * 4), c = col_of(j);
             if (NHWC_OUT) {
 #pragma unroll
@@ -265,18 +268,23 @@ simt_conv_kernel(const SimtLaunch a) {
             const int rem = m - im * OHW;
             const int ohh = rem / a.OW;
             const int oww = rem - ohh * a.OW;
-            float *yb = a.y + ((size_t)im * a.Cout * a.OH + ohh) * (size_t)a.out_row_stride + oww;
+            const size_t pix = ((size_t)im * a.Cout * a.OH + ohh) * (size_t)a.out_row_stride + oww;
+            float *yb = a.y + pix;
+            const float *rb = a.residual ? a.residual + pix : nullptr;
             const size_t plane = (size_t)a.OH * a.out_row_stride;
             for (int nl = t / BM; nl < BN; nl += NT / BM) {
                 const int n = n0 + nl;
-                if (n < a.Cout) yb[(size_t)n * plane] = Cs[nl * CP + ml];
+                if (n < a.Cout) yb[(size_t)n * plane] = Cs[nl * CP + ml] + (rb ? rb[(size_t)n * plane] : 0.0f);
             }
         }
     } else {
         for (int idx = t; idx < BM * BN; idx += NT) {
             const int ml = idx / BN, nl = idx % BN;
             const int m = m0 + ml, n = n0 + nl;
-            if (m < a.M && n < a.Cout) a.y[(size_t)m * a.Cout + n] = Cs[ml * CQ + nl];
+            if (m < a.M && n < a.Cout) {
+                const size_t off = (size_t)m * a.Cout + n;
+                a.y[off] = Cs[ml * CQ + nl] + (a.residual ? a.residual[off] : 0.0f);
+            }
         }
     }
 }

@@ -41,7 +41,19 @@ struct StemTile {
 // the register tile's channels, else one element per channel.
 template <int KIND, int COUT, bool OUT_NHWC>
 __device__ __forceinline__ void store_pixel(const StemLaunch &a, long long pix, int img, int oh, int ow,
-                                            const float (&of)[COUT], const int (&oq)[COUT]) {
+                                            float (&of)[COUT], const int (&oq)[COUT]) {
+    // Residual (float kinds): the same element of r, added after the activation.
+    const size_t plane = (size_t)a.OH * a.out_row_stride;
+    const size_t opix = (size_t)oh * a.out_row_stride + ow;
+    if (KIND != 2 && a.residual) {
+#pragma unroll
+        for (int c = 0; c < COUT; ++c) {
+            if (c >= a.Cout) break;
+            const size_t off = OUT_NHWC ? (size_t)pix * a.Cout + c : ((size_t)img * a.Cout + c) * plane + opix;
+            of[c] += KIND == 0 ? static_cast<const float *>(a.residual)[off]
+                               : __bfloat162float(static_cast<const __nv_bfloat16 *>(a.residual)[off]);
+        }
+    }
     if (OUT_NHWC && a.Cout == COUT) {
         if (KIND == 0) {
             float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.y) + (size_t)pix * COUT);
@@ -74,8 +86,6 @@ __device__ __forceinline__ void store_pixel(const StemLaunch &a, long long pix, 
         }
         return;
     }
-    const size_t plane = (size_t)a.OH * a.out_row_stride;
-    const size_t opix = (size_t)oh * a.out_row_stride + ow;
 #pragma unroll
     for (int c = 0; c < COUT; ++c) {
         if (c >= a.Cout) break;
@@ -226,7 +236,7 @@ __global__ void __launch_bounds__(256) stem_kernel(const StemLaunch a) {
             if (KIND == 2)
                 oq[c] = c < a.Cout ? requant_i8(__float2int_rn(accf[j][c]) + bias_i[c], mc[c], a.inv_s_y) : 0;
             else
-                of[c] = silu_fast(accf[j][c] + bias_f[c]);
+                of[c] = a.act == CBS_ACT_IDENTITY ? accf[j][c] + bias_f[c] : silu_fast(accf[j][c] + bias_f[c]);
         }
         store_pixel<KIND, COUT, OUT_NHWC>(a, pix, img[j], oh[j], ow[j], of, oq);
     }

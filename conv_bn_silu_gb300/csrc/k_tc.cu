@@ -105,6 +105,8 @@ struct TcParams {
     int win;
     int Wp, tiles_per_img, R_box;
     int SB;                    // weight-ring stages when the weights are streamed (windowed)
+    int act;                   // cbs_activation
+    const void *residual;      // nullable: added after the activation (y's layout and element type)
 };
 
 constexpr int kStageBlockBytes = 4096;            // one warp's staged store block: 32 rows x 128 B
@@ -120,6 +122,47 @@ __device__ __forceinline__ float silu_fast(float z) {
 }
 
 // Bias + SiLU + store of 16 consecutive output channels of one pixel.
+__device__ __forceinline__ float activate(const TcParams &p, float z) {
+    return p.act == CBS_ACT_IDENTITY ? z : silu_fast(z);
+}
+
+// Adds the residual of 16 consecutive channels nbase.. of one output element
+// run (NHWC: pixel m; contiguous), channels past C_out excluded.
+template <int KIND>
+__device__ __forceinline__ void add_residual16_nhwc(const TcParams &p, int m, int nbase, float (&o)[16]) {
+    const size_t off = (size_t)m * p.C_out + nbase;
+    if (nbase + 16 <= p.C_out && ((p.C_out & (KIND == kTF32 ? 3 : 7)) == 0)) {
+        if (KIND == kTF32) {
+            const float4 *r = reinterpret_cast<const float4 *>(static_cast<const float *>(p.residual) + off);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v = r[q];
+                o[4 * q] += v.x; o[4 * q + 1] += v.y; o[4 * q + 2] += v.z; o[4 * q + 3] += v.w;
+            }
+        } else {
+            const uint4 *r = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.residual) + off);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const uint4 v = r[q];
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[k]);
+                    o[8 * q + 2 * k] += __low2float(h2);
+                    o[8 * q + 2 * k + 1] += __high2float(h2);
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            if (nbase + jj >= p.C_out) break;
+            o[jj] += KIND == kTF32 ? static_cast<const float *>(p.residual)[off + jj]
+                                   : __bfloat162float(static_cast<const __nv_bfloat16 *>(p.residual)[off + jj]);
+        }
+    }
+}
+
 // The 16 folded-bias values of channels nbase.. (zero past C_out).
 __device__ __forceinline__ void load_bias16(const TcParams &p, const float *bias, int nbase, float (&bv)[16]) {
     if (nbase + 16 <= p.C_out) {
@@ -138,10 +181,12 @@ __device__ __forceinline__ void load_bias16(const TcParams &p, const float *bias
 // store block (32 rows x 128 bytes, 128-byte swizzle: 16-byte chunk j of a
 // row sits at chunk j ^ (row % 8)).  c is the block column of the first value.
 template <int KIND>
-__device__ __forceinline__ void stage16(uint32_t blk, int row, int c, const float (&bv)[16], const uint32_t (&v)[16]) {
+__device__ __forceinline__ void stage16(const TcParams &p, uint32_t blk, int row, int c, const float (&bv)[16],
+                                        const uint32_t (&v)[16], int m, int nbase) {
     float o[16];
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj) o[jj] = silu_fast(__uint_as_float(v[jj]) + bv[jj]);
+    for (int jj = 0; jj < 16; ++jj) o[jj] = activate(p, __uint_as_float(v[jj]) + bv[jj]);
+    if (p.residual && m < p.M) add_residual16_nhwc<KIND>(p, m, nbase, o);
     const uint32_t rbase = blk + (uint32_t)row * 128u;
     if (KIND == kTF32) {
         const int j0 = c >> 2;   // 4 floats per chunk
@@ -178,7 +223,22 @@ __device__ __forceinline__ void epi_store16(const TcParams &p, const float *bias
     load_bias16(p, bias, nbase, bv);
     float o[16];
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj) o[jj] = silu_fast(__uint_as_float(v[jj]) + bv[jj]);
+    for (int jj = 0; jj < 16; ++jj) o[jj] = activate(p, __uint_as_float(v[jj]) + bv[jj]);
+    if (p.residual) {
+        if (p.out_nhwc) {
+            add_residual16_nhwc<KIND>(p, m, nbase, o);
+        } else {
+            const size_t plane = (size_t)p.OH * p.out_row_stride;
+            const size_t pix = (size_t)oh * p.out_row_stride + ow;
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                if (nbase + jj >= p.C_out) break;
+                const size_t off = ((size_t)img * p.C_out + nbase + jj) * plane + pix;
+                o[jj] += KIND == kTF32 ? static_cast<const float *>(p.residual)[off]
+                                       : __bfloat162float(static_cast<const __nv_bfloat16 *>(p.residual)[off]);
+            }
+        }
+    }
     if (p.out_nhwc) {
         if (KIND == kTF32) {
             float *yr = static_cast<float *>(p.y) + (size_t)m * p.C_out + nbase;
@@ -622,10 +682,10 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         ptx::tmem_ld_wait();
                         float bv[16];
                         load_bias16(p, bias, n0 + bc0 + c, bv);
-                        stage16<KIND>(blk, lane, c, bv, v0);
+                        stage16<KIND>(p, blk, lane, c, bv, v0, m, n0 + bc0 + c);
                         if (two) {
                             load_bias16(p, bias, n0 + bc0 + c + 16, bv);
-                            stage16<KIND>(blk, lane, c + 16, bv, v1);
+                            stage16<KIND>(p, blk, lane, c + 16, bv, v1, m, n0 + bc0 + c + 16);
                         }
                     }
                     ptx::fence_proxy_async_smem();
@@ -1379,7 +1439,8 @@ cbs_status plan_tc(cbs_plan_t &p) {
 }
 
 cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, const void *bias,
-                     const float *m_c, float inv_s_y, void *y, void *workspace, cudaStream_t s) {
+                     const float *m_c, float inv_s_y, const void *residual, void *y, void *workspace,
+                     cudaStream_t s) {
     (void)workspace;
     const cbs_layer_desc &d = pl.desc;
     const DriverFns &fns = driver_fns();
@@ -1484,6 +1545,8 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     P.tmem_cols = (uint32_t)(2 * P.acc_stride < 32 ? 32 : 2 * P.acc_stride);
     if (P.tmem_cols > 512) return fail(CBS_ERR_UNSUPPORTED, "accumulators need %u TMEM columns", P.tmem_cols);
     P.y = y;
+    P.act = d.activation;
+    P.residual = residual;
     P.status = device_status_word();
     if (!P.status) return fail(CBS_ERR_CUDA, "cannot resolve the device status word");
     if (pl.grid_ctas <= 0) return CBS_OK;

@@ -22,7 +22,7 @@ def current_stream() -> int:
 def make_desc(n, c_in, h, w, c_out, k, stride, pad=None, prec=B.CBS_FP32, in_layout=None,
               out_layout=None, force_variant=-1, force_split_k=0, force_block_n=0,
               force_block_m=0, out_row_stride=0, force_k_group=0, force_b_resident=0,
-              force_window=0) -> B.cbs_layer_desc:
+              force_window=0, activation=B.CBS_ACT_SILU, residual=0) -> B.cbs_layer_desc:
     if pad is None:
         pad = k // 2
     if in_layout is None:
@@ -35,7 +35,8 @@ def make_desc(n, c_in, h, w, c_out, k, stride, pad=None, prec=B.CBS_FP32, in_lay
                         force_variant=force_variant, force_split_k=force_split_k,
                         force_block_n=force_block_n, force_block_m=force_block_m,
                         out_row_stride=out_row_stride, force_k_group=force_k_group,
-                        force_b_resident=force_b_resident, force_window=force_window).items():
+                        force_b_resident=force_b_resident, force_window=force_window,
+                        activation=activation, residual=residual).items():
         setattr(d, name, int(v))
     return d
 
@@ -106,10 +107,15 @@ class FusedConvBnSilu:
         return out
 
     def __call__(self, x: torch.Tensor, y: torch.Tensor | None = None, s_y: float | None = None,
-                 stream: int | None = None) -> torch.Tensor:
+                 stream: int | None = None, residual: torch.Tensor | None = None) -> torch.Tensor:
+        """residual: for descriptors with residual=1, a tensor shaped and typed
+        like y, added after the activation (may be y itself)."""
         y = self.empty_y() if y is None else y
         s = current_stream() if stream is None else stream
         ws_bytes = int(self.plan.workspace_bytes)
+        if self.desc.residual or self.desc.activation != B.CBS_ACT_SILU:
+            B.cbs_conv_bn_act(self.plan, x, self.w_packed, self.bias, residual, y, self.workspace, ws_bytes, s)
+            return y
         if self.prec == B.CBS_INT8:
             assert s_y is not None
             B.cbs_conv_bn_silu_i8(self.plan, x, self.w_packed, self.bias, self.m_c, float(s_y), y,

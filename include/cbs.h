@@ -66,6 +66,11 @@ typedef enum cbs_layout { CBS_NCHW = 0, CBS_NHWC = 1 } cbs_layout;
  * cores; TF32/BF16 tensor cores), exact integer for INT8. */
 typedef enum cbs_precision { CBS_FP32 = 0, CBS_TF32 = 1, CBS_BF16 = 2, CBS_INT8 = 3 } cbs_precision;
 
+/* Activation after the folded BatchNorm.  SiLU is the fused layer of the
+ * pages; identity gives the plain convolution + bias that page 1's kernel
+ * profile also runs ("conv2d_forward").  FP32, TF32 and BF16 only. */
+typedef enum cbs_activation { CBS_ACT_SILU = 0, CBS_ACT_IDENTITY = 1 } cbs_activation;
+
 /* Kernel family a plan selects. */
 typedef enum cbs_variant {
     CBS_VARIANT_SIMT_FP32 = 0,  /* CUDA-core implicit GEMM, FP32 FMA */
@@ -94,6 +99,10 @@ typedef struct cbs_layer_desc {
                             -1 = stream them with every K step */
     int force_window;    /* TF32/BF16: 1 = windowed A (stride 1, odd k, pad k/2, channel blocks of
                             128 bytes); 0 or -1 = im2col A */
+    int activation;      /* cbs_activation (0 = SiLU) */
+    int residual;        /* 1: add a residual tensor to the activated output, y = act(z) + r
+                            (page 1's profile: the element-wise adds beside the convolutions);
+                            the layer is then called through cbs_conv_bn_act.  FP32/TF32/BF16. */
 } cbs_layer_desc;
 
 /* A plan: plain data, owned by the caller, filled by cbs_plan. */
@@ -191,6 +200,22 @@ CBS_API cbs_status cbs_pack_input(const cbs_plan_t *p, const float *x_nchw, void
 CBS_API cbs_status cbs_conv_bn_silu_f32(const cbs_plan_t *p, const void *x, const void *w_packed,
                                 const float *bias, void *y, void *workspace,
                                 size_t workspace_bytes, void *stream);
+
+/*
+ * cbs_conv_bn_act -- the same layer with the descriptor's activation and an
+ * optional residual add, fused into the epilogue:
+ *   y = act(conv(x) * s + b') + r
+ * (the residual and plain-bias forms of page 1's kernel profile:
+ * "conv2d_forward", "elemwise_add").  residual: device pointer, NULL unless
+ * p->desc.residual; same layout, element type and row pitch as y.  It may be
+ * y itself (in-place add).  Other arguments, ownership and errors as for
+ * cbs_conv_bn_silu_f32, which accepts only SiLU plans without a residual.
+ * CBS_ERR_INVALID_ARG if residual is NULL for a residual plan, or non-NULL
+ * for one without.
+ */
+CBS_API cbs_status cbs_conv_bn_act(const cbs_plan_t *p, const void *x, const void *w_packed, const float *bias,
+                                   const void *residual, void *y, void *workspace, size_t workspace_bytes,
+                                   void *stream);
 
 /*
  * cbs_conv_bn_silu_i8 -- the fused INT8 layer (page 3, "Highlights" and

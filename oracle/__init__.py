@@ -10,6 +10,7 @@ from .oracle import (  # noqa: F401
     batchnorm,
     silu,
     conv_bn_silu_f32,
+    conv_bn_act_f32,
     spec_exp,
     quantize_act,
     fold_quant_i8,

@@ -119,6 +119,30 @@ ORACLE_API void oracle_conv_bn_silu_f32(const float *x, const float *w, const fl
     for (size_t i = 0; i < total; ++i) y[i] = (float)work[i];
 }
 
+/* Conv -> BN -> activation -> + residual, the plain conv + bias and residual
+ * forms beside the fused layer in the kernel profile of "YOLO26N Inference
+ * Optimisation" (conv2d_forward, elemwise_add):
+ *   y = act(BN(conv(x))) + r,   act = SiLU (act == 0) or identity (act == 1),
+ * r an NCHW float tensor shaped like y, or NULL for none.  Same order of
+ * steps as oracle_conv_bn_silu_f32, double arithmetic, rounded once. */
+ORACLE_API void oracle_conv_bn_act_f32(const float *x, const float *w, const float *conv_bias,
+                                       const float *gamma, const float *beta,
+                                       const float *mean, const float *var, float eps,
+                                       int N, int C_in, int H, int W, int C_out, int k,
+                                       int stride, int pad, int act, const float *residual,
+                                       double *work, float *y)
+{
+    const int OH = oracle_out_dim(H, k, stride, pad);
+    const int OW = oracle_out_dim(W, k, stride, pad);
+    const size_t total = (size_t)N * C_out * OH * OW;
+    oracle_conv2d(x, w, conv_bias, N, C_in, H, W, C_out, k, stride, pad, work);
+    oracle_batchnorm(work, gamma, beta, mean, var, eps, N, C_out, (size_t)OH * OW);
+    if (act == 0) oracle_silu(work, total);
+    if (residual)
+        for (size_t i = 0; i < total; ++i) work[i] += (double)residual[i];
+    for (size_t i = 0; i < total; ++i) y[i] = (float)work[i];
+}
+
 /* ---------------------------------------------------------------------- */
 /* INT8 path.                                                              */
 /* ---------------------------------------------------------------------- */

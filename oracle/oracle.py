@@ -32,6 +32,7 @@ def _load():
         lib.oracle_batchnorm.argtypes = [P, P, P, P, P, F, I, I, Z]
         lib.oracle_silu.argtypes = [P, Z]
         lib.oracle_conv_bn_silu_f32.argtypes = [P, P, P, P, P, P, P, F, I, I, I, I, I, I, I, I, P, P]
+        lib.oracle_conv_bn_act_f32.argtypes = [P, P, P, P, P, P, P, F, I, I, I, I, I, I, I, I, I, P, P, P]
         lib.oracle_spec_exp.argtypes = [F]
         lib.oracle_spec_exp.restype = F
         lib.oracle_spec_exp_array.argtypes = [P, P, Z]
@@ -105,6 +106,27 @@ def conv_bn_silu_f32(x, w, gamma, beta, mean, var, eps: float, stride: int, pad:
     cb = None if conv_bias is None else _f32(conv_bias)
     _load().oracle_conv_bn_silu_f32(_ptr(x), _ptr(w), _ptr(cb), _ptr(g), _ptr(b), _ptr(m), _ptr(v),
                                     eps, N, C_in, H, W, C_out, k, stride, pad, _ptr(work), _ptr(y))
+    return (y, work) if return_f64 else y
+
+
+def conv_bn_act_f32(x, w, gamma, beta, mean, var, eps: float, stride: int, pad: int, act: int = 0,
+                    residual=None, conv_bias=None, return_f64: bool = False):
+    """y = act(BN(conv(x))) + residual (act 0: SiLU, 1: identity), double
+    arithmetic, rounded once to float32; residual: NCHW, y's shape, or None."""
+    x, w = _f32(x), _f32(w)
+    N, C_in, H, W = x.shape
+    C_out, _, k, _ = w.shape
+    OH, OW = out_dim(H, k, stride, pad), out_dim(W, k, stride, pad)
+    work = np.empty((N, C_out, OH, OW), np.float64)
+    y = np.empty((N, C_out, OH, OW), np.float32)
+    g, b, m, v = (_f32(a) for a in (gamma, beta, mean, var))
+    cb = None if conv_bias is None else _f32(conv_bias)
+    r = None
+    if residual is not None:
+        r = _f32(residual)
+        assert r.shape == y.shape
+    _load().oracle_conv_bn_act_f32(_ptr(x), _ptr(w), _ptr(cb), _ptr(g), _ptr(b), _ptr(m), _ptr(v), eps, N,
+                                   C_in, H, W, C_out, k, stride, pad, int(act), _ptr(r), _ptr(work), _ptr(y))
     return (y, work) if return_f64 else y
 
 

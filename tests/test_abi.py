@@ -128,3 +128,34 @@ def test_call_checks_before_any_launch(cuda_lib):
         B.cbs_upsample2x_concat(ok, 4, ok, 4, ok, 1, 5, 4, B.CBS_NHWC, 2, None)
     assert e.value.status == B.CBS_ERR_INVALID_ARG
     assert "odd" in B.cbs_last_error() or "shape" in B.cbs_last_error()
+
+
+def test_activation_and_residual_argument_rules(cuda_lib):
+    """Host-side checks of the activation / residual plans (no launch)."""
+    ok = 1 << 20
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_plan(make_desc(1, 16, 40, 40, 32, 3, 1, activation=2))
+    assert e.value.status == B.CBS_ERR_INVALID_ARG
+    for kw in (dict(activation=B.CBS_ACT_IDENTITY), dict(residual=1)):
+        with pytest.raises(B.CbsError) as e:
+            B.cbs_plan(make_desc(1, 16, 40, 40, 32, 3, 1, prec=B.CBS_INT8, in_layout=B.CBS_NHWC, **kw))
+        assert e.value.status == B.CBS_ERR_UNSUPPORTED
+    ident = B.cbs_plan(make_desc(1, 16, 40, 40, 32, 3, 1, activation=B.CBS_ACT_IDENTITY))
+    resid = B.cbs_plan(make_desc(1, 16, 40, 40, 32, 3, 1, residual=1))
+    plain = B.cbs_plan(make_desc(1, 16, 40, 40, 32, 3, 1))
+    for p in (ident, resid):   # the SiLU entry point refuses them
+        with pytest.raises(B.CbsError) as e:
+            B.cbs_conv_bn_silu_f32(p, ok, ok, ok, ok, ok, p.workspace_bytes, None)
+        assert e.value.status == B.CBS_ERR_INVALID_ARG
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_conv_bn_act(resid, ok, ok, ok, None, ok, ok, resid.workspace_bytes, None)
+    assert e.value.status == B.CBS_ERR_INVALID_ARG
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_conv_bn_act(plain, ok, ok, ok, ok, ok, ok, plain.workspace_bytes, None)
+    assert e.value.status == B.CBS_ERR_INVALID_ARG
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_conv_bn_act(resid, ok, ok, ok, ok + 8, ok, ok, resid.workspace_bytes, None)
+    assert e.value.status == B.CBS_ERR_MISALIGNED
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_conv_bn_silu_f32_noalloc(ident, ok, ok, ok, ok, None)
+    assert e.value.status == B.CBS_ERR_UNSUPPORTED

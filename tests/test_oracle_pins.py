@@ -222,6 +222,75 @@ def test_conv_bias_path_vs_torch():
     np.testing.assert_allclose(z, ref, rtol=1e-13, atol=1e-13)
 
 
+
+# ------------------------------------------ activation and residual (plain conv + bias, residual add)
+def _identity_bn(c):
+    """BN that is exactly the identity: var + eps == 1 in float32 (eps = 2^-10)."""
+    eps = 2.0 ** -10
+    return (np.ones(c, np.float32), np.zeros(c, np.float32), np.zeros(c, np.float32),
+            np.full(c, 1.0 - eps, np.float32), eps)
+
+
+def _delta_kernel(c, k):
+    w = np.zeros((c, c, k, k), np.float32)
+    for i in range(c):
+        w[i, i, k // 2, k // 2] = 1.0
+    return w
+
+
+def test_act_silu_without_residual_is_the_fused_layer():
+    spec = wl.LayerSpec(8, 12, 3, 2, 11)
+    x, p = wl.layer_inputs(spec, 2, layer_index=3)
+    a = oracle.conv_bn_silu_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, 2, 1)
+    b = oracle.conv_bn_act_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, 2, 1, act=0)
+    assert np.array_equal(a.view(np.int32), b.view(np.int32))
+
+
+@pytest.mark.parametrize("k", [1, 3, 5])
+def test_identity_act_delta_kernel_identity_bn_returns_input(k):
+    r = rng(11)
+    x = f32(r.standard_normal((2, 5, 7, 9)))
+    g, b, m, v, eps = _identity_bn(5)
+    y = oracle.conv_bn_act_f32(x, _delta_kernel(5, k), g, b, m, v, eps, 1, k // 2, act=1)
+    assert np.array_equal(y, x)
+    # the same with SiLU is SiLU of the input (closed form, double)
+    ys = oracle.conv_bn_act_f32(x, _delta_kernel(5, k), g, b, m, v, eps, 1, k // 2, act=0)
+    xd = x.astype(np.float64)
+    np.testing.assert_array_equal(ys, (xd / (1.0 + np.exp(-xd))).astype(np.float32))
+
+
+def test_residual_is_added_after_the_activation():
+    r = rng(12)
+    x = f32(r.standard_normal((1, 4, 6, 6)))
+    res = f32(r.standard_normal((1, 4, 6, 6)))
+    g, b, m, v, eps = _identity_bn(4)
+    # identity everything: y = x + r, rounded once (exactly numpy's float32 add)
+    y = oracle.conv_bn_act_f32(x, _delta_kernel(4, 3), g, b, m, v, eps, 1, 1, act=1, residual=res)
+    assert np.array_equal(y, x + res)
+    # a real layer: y = float(SiLU(BN(conv)) in double + r)
+    spec = wl.LayerSpec(6, 10, 3, 1, 8)
+    x2, p = wl.layer_inputs(spec, 2, layer_index=5)
+    r2 = f32(r.standard_normal((2, 10, 8, 8)))
+    _, work = oracle.conv_bn_silu_f32(x2, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, 1, 1, return_f64=True)
+    y2 = oracle.conv_bn_act_f32(x2, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, 1, 1, act=0, residual=r2)
+    assert np.array_equal(y2, (work + r2.astype(np.float64)).astype(np.float32))
+
+
+def test_identity_act_vs_torch():
+    """Plain conv + BN (no SiLU) against torch float64 conv2d + batch_norm."""
+    spec = wl.LayerSpec(16, 24, 3, 2, 13)
+    x, p = wl.layer_inputs(spec, 2, layer_index=6)
+    y, work = oracle.conv_bn_act_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, 2, 1, act=1, return_f64=True)
+    t = torch.nn.functional.conv2d(torch.from_numpy(x.astype(np.float64)), torch.from_numpy(p.w.astype(np.float64)),
+                                   stride=2, padding=1)
+    ref = torch.nn.functional.batch_norm(t, torch.from_numpy(p.mean.astype(np.float64)),
+                                         torch.from_numpy(p.var.astype(np.float64)),
+                                         torch.from_numpy(p.gamma.astype(np.float64)),
+                                         torch.from_numpy(p.beta.astype(np.float64)), False, 0.0,
+                                         float(np.float32(p.eps))).numpy()
+    np.testing.assert_allclose(work, ref, rtol=1e-12, atol=1e-12)
+
+
 # ------------------------------------------------------------------------ INT8
 def _ulp_distance(a, b):
     ia = a.view(np.int32).astype(np.int64)
