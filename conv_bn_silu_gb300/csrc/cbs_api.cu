@@ -1,5 +1,6 @@
 // cbs_api.cu -- the C ABI (include/cbs.h): planning, argument checks and
 // dispatch to the kernels.  Planning is pure host code with no CUDA call.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -269,15 +270,19 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
                                   : D.prec == CBS_INT8 ? (cout_t == 16 ? 4 : (cout_t == 32 ? 2 : 1))
                                                        : (cout_t <= 32 ? 2 : 1);
         p.block_m = 256 * px_per_thread;  // output pixels per CTA: 256 threads, px_per_thread each
+        const bool tc = stem_uses_tensor_cores(D.prec == CBS_BF16 ? 1 : 0, D.in_layout == CBS_NHWC, p.c_in_pad,
+                                               D.k, D.c_out, M);
+        if (tc) p.block_m = 128;           // tensor-core stem: 128 pixels (one M=128 MMA) per CTA
         p.block_n = cout_t;
         p.block_k = D.k * D.k * p.c_in_pad;
         p.stages = 1;
         p.split_k = 1;
         p.m_tiles = (int)((M + p.block_m - 1) / p.block_m);
         p.n_tiles = 1;
-        p.grid_ctas = p.m_tiles;
+        // the tensor-core stem is persistent: kStemTcCtasPerSm CTAs per SM walk the tiles
+        p.grid_ctas = tc ? std::min(p.m_tiles, kNumSMs * kStemTcCtasPerSm) : p.m_tiles;
         p.threads = 256;
-        p.smem_bytes = D.k * D.k * p.c_in_pad * cout_t * 4;
+        p.smem_bytes = tc ? kStemTcSmemBytes : D.k * D.k * p.c_in_pad * cout_t * 4;
         p.workspace_bytes = 0;
     } else if (variant == CBS_VARIANT_SIMT_FP32) {
         plan_simt(p);

@@ -85,6 +85,15 @@ struct StemLaunch {
     const void *residual;      // nullable, element type and layout of y (float kinds)
 };
 cudaError_t launch_stem(const StemLaunch &L, cudaStream_t s);
+// BF16 stems (4-channel NHWC input, k <= 3, C_out <= 64) run on the tensor
+// cores (when there are fewer than kStemTcMaxPixels output pixels, for 32-bit
+// pixel indices): persistent CTAs of 256 threads, 128 output pixels per tile,
+// a ring of kStemTcStages A tiles; the others on the CUDA cores.
+bool stem_uses_tensor_cores(int kind, int in_nhwc, int c_pad, int ks, int cout, long long pixels);
+constexpr int kStemTcStages = 4, kStemTcCtasPerSm = 3;
+constexpr long long kStemTcMaxPixels = (1ll << 31) - 256;
+// A ring + B (64 rows x 128 B) + bias + two mbarriers + TMEM slot + 1 KB for alignment
+constexpr int kStemTcSmemBytes = kStemTcStages * 16384 + 8192 + 64 * 4 + 16 + 16 + 1024;
 constexpr int kStemMaxCin = 4, kStemMaxCout = 64, kStemMaxK = 7;
 
 // ---------------------------------------------------------------- misc kernels

@@ -9,10 +9,12 @@
 // folded weights from shared memory, with FP32 fused multiply-adds (exact
 // integer sums for INT8).  The epilogue is the same as the other variants':
 // + folded bias, SiLU, store (or the specified INT8 requantisation).
+#include <algorithm>
 #include <cuda_bf16.h>
 
 #include "cbs_internal.cuh"
 #include "requant.cuh"
+#include "tc_ptx.cuh"
 
 namespace cbs {
 namespace {
@@ -272,8 +274,316 @@ cudaError_t launch_cout(const StemLaunch &L, cudaStream_t s) {
 
 }  // namespace
 
+namespace {
+
+// ------------------------------------------------------ tensor-core stem
+// BF16 stems with 4-channel NHWC pixels and k <= 3: the contraction is an
+// M x 16..64 x K<=48 GEMM, one M=128 tile per 128 output pixels.  Persistent
+// CTAs of 256 threads each keep the weights (B) in shared memory and walk
+// their tiles with a ring of kStemTcStages A tiles.  Threads t and t + 128
+// share output pixel t of a tile (TMEM lane t):
+//   - each gathers half of the pixel's taps into row t of a 128-byte-swizzled
+//     A tile with cp.async (zero-filled outside the image), kStemTcStages - 1
+//     tiles ahead of the MMA;
+//   - one thread issues the tile's MMAs into one of two TMEM accumulators
+//     and commits them to that accumulator's mbarrier;
+//   - while tile i's MMAs run, each thread reads alternate 8-channel groups of
+//     tile i-1's accumulator back for bias, activation, residual and stores.
+// K layout.  In general row t holds tap s (4 channels, 8 bytes) at byte 8s.
+// For 3x3, stride 2, pad 1 and an even input width the row instead holds, for
+// each kernel row r, the two 16-byte pixel pairs starting at input column
+// 2*ow-2: four pixels of which the first is unused (its slot is zeroed after
+// the copy lands and its weights are zero), so each pixel takes six aligned
+// 16-byte copies instead of nine 8-byte ones.
+constexpr uint64_t kStemWaitNs = 2000000000ull;
+
+// n / d for 0 <= n < 2^31 as (umulhi(n, m) + n) >> l, the round-up
+// multiplier of Granlund and Montgomery, "Division by invariant integers
+// using multiplication" (PLDI 1994): l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1.
+struct FastDiv {
+    uint32_t m, l;
+};
+
+FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    const uint64_t m = ((1ull << 32) * ((1ull << l) - d)) / d + 1;
+    return FastDiv{(uint32_t)m, l};
+}
+
+__device__ __forceinline__ int fast_div(int n, FastDiv f) {
+    return (int)((__umulhi((uint32_t)n, f.m) + (uint32_t)n) >> f.l);
+}
+
+struct StemTcGeom {
+    int total;          // output pixels (< 2^31 - 128)
+    int n_tiles;        // 128-pixel tiles
+    FastDiv div_ohw;    // by OH * OW
+    FastDiv div_ow;     // by OW
+};
+
+// SiLU as h + h tanh(h), h = z / 2 (sigma(z) = (1 + tanh(z / 2)) / 2).
+__device__ __forceinline__ float silu_tanh(float h) {
+    float th;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(h));
+    return fmaf(h, th, h);
+}
+
+// Two floats rounded to bf16 (lo in the low half).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
+    return (uint32_t)__bfloat16_as_ushort(h2.x) | ((uint32_t)__bfloat16_as_ushort(h2.y) << 16);
+}
+
+template <bool OUT_NHWC, bool PAIRS>
+__global__ void __launch_bounds__(256) stem_tc_bf16_kernel(const StemLaunch a, int n_mma, StemTcGeom g,
+                                                           unsigned int *status) {
+    constexpr int S = kStemTcStages;
+    extern __shared__ uint8_t stem_smem_raw[];
+    const uint32_t raw = ptx::smem_u32(stem_smem_raw);
+    uint8_t *base = stem_smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t *sA = base;                                           // S x 128 rows x 128 B
+    uint8_t *sB = base + S * 16384;                               // 64 rows x 128 B
+    float *sBias = reinterpret_cast<float *>(sB + 8192);          // 64
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sBias + 64);    // 2
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
+
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int row = t & 127, half = t >> 7;
+    const int KK = a.KS * a.KS;
+    const int kslices = PAIRS ? 3 : (KK + 3) / 4;    // 16-value K slices: 4 taps (or 2 pairs) each
+    const uint32_t ncols = 2 * n_mma <= 32 ? 32u : (2 * n_mma <= 64 ? 64u : 128u);
+    const bool silu = a.act != CBS_ACT_IDENTITY;
+    if (warp == 0) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), ncols);
+        ptx::tmem_relinquish();
+    }
+    if (t == 0) {
+        ptx::mbar_init(ptx::smem_u32(&bars[0]), 1);
+        ptx::mbar_init(ptx::smem_u32(&bars[1]), 1);
+        ptx::fence_mbar_init();
+    }
+    // B row co: the folded weights of output channel co in the K layout above,
+    // zero for co >= C_out; 16-byte chunk q stored at q ^ (co % 8).
+    const uint2 *w2 = static_cast<const uint2 *>(a.w);   // [C_out][KK] taps of 4 bf16
+    for (int idx = t; idx < n_mma * 8; idx += 256) {
+        const int co = idx >> 3, q = idx & 7;
+        uint2 lo = make_uint2(0u, 0u), hi = make_uint2(0u, 0u);
+        if (co < a.Cout) {
+            const uint2 *wr = w2 + (size_t)co * KK;
+            if (PAIRS) {
+                if (q < 6) {
+                    const int r = q >> 1;
+                    if ((q & 1) == 0) {
+                        hi = wr[r * 3];
+                    } else {
+                        lo = wr[r * 3 + 1];
+                        hi = wr[r * 3 + 2];
+                    }
+                }
+            } else {
+                if (2 * q < KK) lo = wr[2 * q];
+                if (2 * q + 1 < KK) hi = wr[2 * q + 1];
+            }
+        }
+        *reinterpret_cast<uint4 *>(sB + co * 128 + ((q ^ (co & 7)) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+    // Bias, halved for the tanh form of SiLU.
+    if (t < 64) {
+        const float b = t < a.Cout ? static_cast<const float *>(a.bias)[t] : 0.0f;
+        sBias[t] = silu ? 0.5f * b : b;
+    }
+
+    const int n_local = (int)blockIdx.x < g.n_tiles ? (g.n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int ohw = a.OH * a.OW;
+    const uint2 *x2 = static_cast<const uint2 *>(a.x);   // one 4-channel bf16 pixel
+    const uint32_t sA_u32 = ptx::smem_u32(sA);
+    const uint32_t swz = (uint32_t)(row & 7);
+
+    // Issue this thread's copies of local tile i into stage i % S (an empty
+    // group past the last tile).
+    auto gather = [&](int i) {
+        if (i < n_local) {
+            const int pix = ((int)blockIdx.x + i * (int)gridDim.x) * 128 + row;
+            const bool valid = pix < g.total;
+            const int img = fast_div(pix, g.div_ohw);
+            const int rem = pix - img * ohw;
+            const int oh = fast_div(rem, g.div_ow);
+            const int ow = rem - oh * a.OW;
+            const uint32_t dst = sA_u32 + (uint32_t)((i % S) * 16384 + row * 128);
+            if (PAIRS) {
+#pragma unroll
+                for (int qq = 0; qq < 3; ++qq) {
+                    const int q = 3 * half + qq, r = q >> 1;
+                    const int ih = 2 * oh - 1 + r, col = 2 * ow - 2 + 2 * (q & 1);
+                    const bool in = valid && (unsigned)ih < (unsigned)a.H && col >= 0 && col + 1 < a.W;
+                    const void *src = in ? (const void *)(x2 + (size_t)(img * a.H + ih) * a.W + col) : a.x;
+                    ptx::cp_async_16(dst + (((uint32_t)q ^ swz) << 4), src, in ? 16u : 0u);
+                }
+            } else {
+#pragma unroll
+                for (int ss = 0; ss < 6; ++ss) {
+                    const int s = 6 * half + ss;
+                    if (s >= kslices * 4) break;
+                    const int r = s / a.KS, c = s - (s / a.KS) * a.KS;
+                    const int ih = oh * a.stride - a.pad + r, iw = ow * a.stride - a.pad + c;
+                    const bool in = valid && s < KK && (unsigned)ih < (unsigned)a.H && (unsigned)iw < (unsigned)a.W;
+                    const void *src = in ? (const void *)(x2 + (size_t)(img * a.H + ih) * a.W + iw) : a.x;
+                    ptx::cp_async_8(dst + (((uint32_t)(s >> 1) ^ swz) << 4) + (uint32_t)((s & 1) * 8), src,
+                                    in ? 8u : 0u);
+                }
+            }
+        }
+        ptx::cp_async_commit();
+    };
+
+    // Bias, activation, residual and stores of this thread's 8-channel groups
+    // (half, half + 2, ...) of local tile i, from its accumulator.
+    auto epilogue = [&](int i, uint32_t tmem) {
+        const int pix = ((int)blockIdx.x + i * (int)gridDim.x) * 128 + row;
+        const bool valid = pix < g.total;
+        const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((i & 1) * n_mma);
+        __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(a.y);
+        const __nv_bfloat16 *res = static_cast<const __nv_bfloat16 *>(a.residual);
+        for (int c0 = 8 * half; c0 < n_mma; c0 += 16) {
+            uint32_t v[8];
+            ptx::tmem_ld8(t_row + (uint32_t)c0, v);
+            ptx::tmem_ld_wait();
+            if (!valid) continue;
+            float o[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+                o[jj] = silu ? silu_tanh(fmaf(__uint_as_float(v[jj]), 0.5f, sBias[c0 + jj]))
+                             : __uint_as_float(v[jj]) + sBias[c0 + jj];
+            if (OUT_NHWC && c0 + 8 <= a.Cout && (a.Cout & 7) == 0) {
+                const size_t off = (size_t)pix * a.Cout + c0;
+                if (res) {   // bf16 -> float is a 16-bit shift
+                    const uint4 rv = *reinterpret_cast<const uint4 *>(res + off);
+                    o[0] += __uint_as_float(rv.x << 16), o[1] += __uint_as_float(rv.x & 0xffff0000u);
+                    o[2] += __uint_as_float(rv.y << 16), o[3] += __uint_as_float(rv.y & 0xffff0000u);
+                    o[4] += __uint_as_float(rv.z << 16), o[5] += __uint_as_float(rv.z & 0xffff0000u);
+                    o[6] += __uint_as_float(rv.w << 16), o[7] += __uint_as_float(rv.w & 0xffff0000u);
+                }
+                *reinterpret_cast<uint4 *>(y + off) = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                                                                 pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+            } else {
+                const int img = fast_div(pix, g.div_ohw);
+                const int rem = pix - img * ohw;
+                const int oh = fast_div(rem, g.div_ow);
+                const int ow = rem - oh * a.OW;
+                const size_t plane = (size_t)a.OH * a.out_row_stride;
+                const size_t opix = (size_t)oh * a.out_row_stride + ow;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int c = c0 + jj;
+                    if (c >= a.Cout) break;
+                    const size_t off = OUT_NHWC ? (size_t)pix * a.Cout + c : ((size_t)img * a.Cout + c) * plane + opix;
+                    const float r = res ? __bfloat162float(res[off]) : 0.0f;
+                    y[off] = __float2bfloat16_rn(o[jj] + r);
+                }
+            }
+        }
+    };
+
+#pragma unroll 1
+    for (int i = 0; i < S - 1; ++i) gather(i);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint64_t dhi = ptx::smem_desc(0u, 16u, 1024u, 2u);
+    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n_mma >> 3) << 17) |
+                           ((uint32_t)(128 >> 4) << 24);
+    const uint64_t bd = dhi | (uint64_t)((ptx::smem_u32(sB) & 0x3FFFFu) >> 4);
+    bool failed = false;
+#pragma unroll 1
+    for (int i = 0; i <= n_local; ++i) {
+        if (i < n_local) {
+            ptx::cp_async_wait<S - 2>();   // this thread's copies of tile i have landed
+            if (PAIRS) {                   // zero the unused first pixel of each pair this thread copied
+                uint8_t *rp = sA + (i % S) * 16384 + row * 128;
+                *reinterpret_cast<uint2 *>(rp + ((uint32_t)(half ? 4 : 0) ^ swz) * 16) = make_uint2(0u, 0u);
+                if (!half) *reinterpret_cast<uint2 *>(rp + (2u ^ swz) * 16) = make_uint2(0u, 0u);
+            }
+            ptx::fence_proxy_async_smem();
+        }
+        ptx::tc_fence_before();
+        if (__syncthreads_or(failed)) break;
+        ptx::tc_fence_after();
+        if (i < n_local && t == 0) {
+            const uint64_t ad = dhi | (uint64_t)(((sA_u32 + (uint32_t)((i % S) * 16384)) & 0x3FFFFu) >> 4);
+            const uint32_t acc = tmem + (uint32_t)((i & 1) * n_mma);
+            for (int k = 0; k < kslices; ++k) ptx::mma_f16(acc, ad + 2u * k, bd + 2u * k, idesc, k > 0 ? 1u : 0u);
+            ptx::mma_commit(ptx::smem_u32(&bars[i & 1]));
+        }
+        if (i > 0) {
+            const int j = i - 1;
+            bool ok = ptx::mbar_wait_bounded(ptx::smem_u32(&bars[j & 1]), (uint32_t)((j >> 1) & 1), kStemWaitNs);
+            ok = __all_sync(0xffffffffu, ok);   // warp-uniform before .sync.aligned loads
+            if (!ok) {
+                failed = true;
+                if (lane == 0) atomicOr(status, 1u);
+            } else {
+                ptx::tc_fence_after();
+                epilogue(j, tmem);
+            }
+        }
+        // Stage (i - 1) % S is free: its MMAs completed before the wait above.
+        if (i < n_local) gather(i + S - 1);
+    }
+    ptx::cp_async_wait<0>();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, ncols);
+    }
+}
+
+}  // namespace
+
+bool stem_uses_tensor_cores(int kind, int in_nhwc, int c_pad, int ks, int cout, long long pixels) {
+    return kind == 1 && in_nhwc && c_pad == 4 && ks <= 3 && cout <= 64 && pixels < kStemTcMaxPixels;
+}
+
+namespace {
+
+template <bool OUT_NHWC, bool PAIRS>
+cudaError_t launch_stem_tc_as(const StemLaunch &L, int n_mma, StemTcGeom g, int grid, cudaStream_t s,
+                              unsigned int *status) {
+    auto kern = stem_tc_bf16_kernel<OUT_NHWC, PAIRS>;
+    const cudaError_t e = set_max_dyn_smem(kern, kStemTcSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, 256, kStemTcSmemBytes, s>>>(L, n_mma, g, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stem_tc(const StemLaunch &L, cudaStream_t s) {
+    unsigned int *status = device_status_word();
+    if (!status) return cudaErrorInvalidValue;
+    const long long total = (long long)L.N * L.OH * L.OW;
+    if (total >= kStemTcMaxPixels) return cudaErrorInvalidValue;
+    StemTcGeom g;
+    g.total = (int)total;
+    g.n_tiles = (int)((total + 127) / 128);
+    g.div_ohw = make_fastdiv((uint32_t)(L.OH * L.OW));
+    g.div_ow = make_fastdiv((uint32_t)L.OW);
+    const int grid = std::min(g.n_tiles, kNumSMs * kStemTcCtasPerSm);
+    const int n_mma = (L.Cout + 15) / 16 * 16;
+    const bool pairs = L.KS == 3 && L.stride == 2 && L.pad == 1 && (L.W & 1) == 0;
+    if (L.out_nhwc)
+        return pairs ? launch_stem_tc_as<true, true>(L, n_mma, g, grid, s, status)
+                     : launch_stem_tc_as<true, false>(L, n_mma, g, grid, s, status);
+    return pairs ? launch_stem_tc_as<false, true>(L, n_mma, g, grid, s, status)
+                 : launch_stem_tc_as<false, false>(L, n_mma, g, grid, s, status);
+}
+
+}  // namespace
+
 cudaError_t launch_stem(const StemLaunch &L, cudaStream_t s) {
     if (L.N == 0) return cudaSuccess;
+    if (stem_uses_tensor_cores(L.kind, L.in_nhwc, L.c_pad, L.KS, L.Cout, (long long)L.N * L.OH * L.OW))
+        return launch_stem_tc(L, s);
     switch (L.kind) {
         case 0: return launch_cout<0>(L, s);
         case 1: return launch_cout<1>(L, s);

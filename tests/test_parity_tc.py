@@ -105,6 +105,30 @@ def test_ragged(cuda_lib, prec, shape):
     check(y, spec, x, p, prec, shape)
 
 
+@pytest.mark.parametrize("out_layout", [B.CBS_NHWC, B.CBS_NCHW])
+@pytest.mark.parametrize("shape", [
+    (2, 3, 16, 3, 2, 38, 38),      # 3x3 s2 with an even width: pixel-pair copies, ragged last tile
+    (2, 3, 16, 3, 2, 37, 37),      # odd width: one copy per tap
+    (1, 4, 32, 3, 1, 19, 19),      # stride 1
+    (3, 1, 48, 1, 1, 9, 9),        # 1x1 filter: one K slice, C_out 48
+    (1, 2, 64, 3, 2, 50, 34),      # C_out 64, non-square
+    (1, 3, 40, 3, 2, 30, 30),      # C_out 40: a ragged 16-channel block
+    (1, 3, 20, 3, 2, 22, 22),      # C_out 20: per-channel stores
+    (8, 3, 16, 3, 2, 256, 256),    # 1024 tiles: several per persistent CTA, through the whole ring
+])
+def test_tensor_core_stem(cuda_lib, out_layout, shape):
+    """BF16 layers with at most 4 input channels and k <= 3 run on the
+    tensor-core stem kernel."""
+    n, c_in, c_out, k, stride, h, w = shape
+    spec = wl.LayerSpec(c_in, c_out, k, stride, h, w)
+    x, p = wl.layer_inputs(spec, n, layer_index=4)
+    y, layer = run_tc(spec, x, p, B.CBS_BF16, out_layout=out_layout)
+    pl = layer.plan
+    assert pl.variant == B.CBS_VARIANT_STEM and pl.block_m == 128 and pl.threads == 256
+    assert pl.grid_ctas == min(pl.m_tiles, 152 * 3)
+    check(y, spec, x, p, "bf16", shape)
+
+
 @pytest.mark.parametrize("prec", ["bf16", "tf32"])
 def test_non_square_image(cuda_lib, prec):
     """H != W pins the order of the im2col corner and offset coordinates."""
@@ -129,7 +153,7 @@ def test_forced_block_n(cuda_lib, prec, bn):
 
 
 @pytest.mark.parametrize("prec", ["bf16", "tf32"])
-@pytest.mark.parametrize("i", [1, 5, 7, 10, 11])
+@pytest.mark.parametrize("i", [0, 1, 5, 7, 10, 11])
 def test_batch16_sampled_images(cuda_lib, prec, i):
     """Full batch-16 launch; images 0 and 15 checked against the oracle
     (images are independent, so the oracle computes only those two)."""
