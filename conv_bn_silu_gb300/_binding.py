@@ -31,6 +31,7 @@ EXPORTED = (
     "cbs_plan", "cbs_fold_bn", "cbs_pack_input", "cbs_conv_bn_silu_f32", "cbs_conv_bn_silu_i8",
     "cbs_upsample2x_concat", "cbs_workspace_init", "cbs_read_device_status", "cbs_status_string",
     "cbs_last_error", "cbs_abi_version", "cbs_conv_bn_silu_f32_noalloc", "cbs_conv_bn_act",
+    "cbs_conv_bn_act_cat",
 )
 
 
@@ -38,7 +39,7 @@ class cbs_layer_desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "n", "c_in", "h", "w", "c_out", "k", "stride", "pad", "in_layout", "out_layout", "prec",
         "force_variant", "force_split_k", "force_block_n", "force_block_m", "out_row_stride",
-        "force_k_group", "force_b_resident", "force_window", "activation", "residual")]
+        "force_k_group", "force_b_resident", "force_window", "activation", "residual", "c_in_b")]
 
 
 class cbs_plan_t(ctypes.Structure):
@@ -49,7 +50,7 @@ class cbs_plan_t(ctypes.Structure):
             "oh", "ow", "out_row_stride", "m_tiles", "n_tiles", "grid_ctas", "threads",
             "smem_bytes")] + \
         [(n, ctypes.c_size_t) for n in (
-            "x_bytes", "y_bytes", "w_packed_bytes", "bias_bytes", "workspace_bytes")] + \
+            "x_bytes", "y_bytes", "w_packed_bytes", "bias_bytes", "workspace_bytes", "x_b_bytes")] + \
         [("desc", cbs_layer_desc)]
 
 
@@ -74,6 +75,7 @@ def lib():
         L.cbs_pack_input.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, F, P]
         L.cbs_conv_bn_silu_f32.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P, Z, P]
         L.cbs_conv_bn_act.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P, P, Z, P]
+        L.cbs_conv_bn_act_cat.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P, P, P, Z, P]
         L.cbs_conv_bn_silu_i8.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, F, P, P, Z, P]
         L.cbs_upsample2x_concat.argtypes = [P, I, P, I, P, I, I, I, I, I, P]
         L.cbs_conv_bn_silu_f32_noalloc.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P]
@@ -149,6 +151,11 @@ def cbs_conv_bn_silu_f32(plan, x, w_packed, bias, y, workspace, workspace_bytes,
 def cbs_conv_bn_act(plan, x, w_packed, bias, residual, y, workspace, workspace_bytes, stream):
     _check(lib().cbs_conv_bn_act(ctypes.byref(plan), _p(x), _p(w_packed), _p(bias), _p(residual), _p(y),
                                  _p(workspace), workspace_bytes, stream), "cbs_conv_bn_act")
+
+
+def cbs_conv_bn_act_cat(plan, x, x_b, w_packed, bias, residual, y, workspace, workspace_bytes, stream):
+    _check(lib().cbs_conv_bn_act_cat(ctypes.byref(plan), _p(x), _p(x_b), _p(w_packed), _p(bias), _p(residual),
+                                     _p(y), _p(workspace), workspace_bytes, stream), "cbs_conv_bn_act_cat")
 
 
 def cbs_conv_bn_silu_i8(plan, x, w_packed, bias_i32, m_c, s_y, y, workspace, workspace_bytes,

@@ -4,7 +4,10 @@ Layers and their sources are those of `workloads.chain_layers()`: the list's
 first eleven layers from the frame, the 384->128 1x1 layer on
 concat(upsample2x(layer 10), layer 7), and 28 stride-1 repeats at 80/40/20.
 Every computation runs in libcbs.so: the chain-entry layout step
-(cbs_pack_input), the fused layers and the neck glue.
+(cbs_pack_input), the fused layers and the neck glue.  Layer 11 is a
+two-input layer: it reads the upsampled layer 10 and layer 7 straight from
+their buffers (the channel concatenation happens in its input loads), so the
+only glue kernel is the 2x upsample.
 
 FP32 runs the CUDA-core variant in NCHW; TF32, BF16 and INT8 run the
 tensor-core variants in NHWC, where only the frame needs packing.
@@ -33,24 +36,20 @@ class Chain:
         for i, cl in enumerate(self.specs):
             s = cl.spec
             p = wl.layer_params(s, seed=seed, layer_index=100 + i)
+            c_in_b = self.specs[cl.src[2]].spec.c_out if cl.src[0] == "upcat" else 0
             desc = make_desc(n, s.c_in, s.h, s.width, s.c_out, s.k, s.stride, s.pad, prec=cp,
-                             in_layout=self.layout, out_layout=self.layout)
+                             in_layout=self.layout, out_layout=self.layout, c_in_b=c_in_b)
             self.layers.append(FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps,
                                                device=self.device))
         self.outs = [layer.empty_y() for layer in self.layers]
         self.x0 = self.layers[0].empty_x()
-        s11 = self.specs[11].spec
-        if self.layout == B.CBS_NHWC:
-            glue_shape = (n, s11.h, s11.width, s11.c_in)
-        else:
-            glue_shape = (n, s11.c_in, s11.h, s11.width)
-        self.glue = torch.empty(glue_shape, dtype=self.layers[11].x_dtype, device=self.device)
+        self.glue = self.layers[11].empty_x()   # upsample2x(layer 10): the first input of layer 11
 
     def params(self, i: int, seed: int = 0):
         return wl.layer_params(self.specs[i].spec, seed=seed, layer_index=100 + i)
 
     def input_of(self, i: int):
-        """The device tensor layer i reads (after its source has run)."""
+        """The device tensor layer i reads (its first input; after its source has run)."""
         src = self.specs[i].src
         if src[0] == "frame":
             return self.x0
@@ -58,8 +57,13 @@ class Chain:
             return self.outs[src[1]]
         return self.glue
 
+    def second_input_of(self, i: int):
+        """The second input of a two-input layer, else None."""
+        src = self.specs[i].src
+        return self.outs[src[2]] if src[0] == "upcat" else None
+
     def launches_per_frame(self) -> int:
-        return len(self.layers) + 2  # 40 fused layers, frame packing, one glue kernel
+        return len(self.layers) + 2  # 40 fused layers, frame packing, one upsample kernel
 
     def run(self, frame_nchw: torch.Tensor, stream: int | None = None):
         """One frame batch: pack the frame, then the 40 layers in order."""
@@ -68,15 +72,13 @@ class Chain:
         for i, layer in enumerate(self.layers):
             src = self.specs[i].src
             if src[0] == "upcat":
-                a, b = self.outs[src[1]], self.outs[src[2]]
+                a = self.outs[src[1]]
                 if self.layout == B.CBS_NHWC:
-                    n, h, w, cb = b.shape
-                    ca = a.shape[3]
+                    n, h, w, ca = a.shape
                 else:
-                    n, cb, h, w = b.shape
-                    ca = a.shape[1]
-                B.cbs_upsample2x_concat(a, ca, b, cb, self.glue, n, h, w, self.layout, b.element_size(), s)
-            layer(self.input_of(i), self.outs[i], stream=s)
+                    n, ca, h, w = a.shape
+                B.cbs_upsample2x_concat(a, ca, None, 0, self.glue, n, 2 * h, 2 * w, self.layout, a.element_size(), s)
+            layer(self.input_of(i), self.outs[i], stream=s, x_b=self.second_input_of(i))
         return self.outs
 
     def flops(self) -> int:

@@ -141,11 +141,6 @@ cbs_status check_ptr(const void *ptr, const char *name, bool nullable = false) {
     return CBS_OK;
 }
 
-#define CBS_TRY(expr)                      \
-    do {                                   \
-        cbs_status _s = (expr);            \
-        if (_s != CBS_OK) return _s;       \
-    } while (0)
 
 StemLaunch stem_launch(const cbs_plan_t &p, const void *x, const void *w, const void *bias, const float *m_c,
                        float inv_s_y, void *y) {
@@ -209,6 +204,10 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
     if (D.residual != 0 && D.residual != 1) return fail(CBS_ERR_INVALID_ARG, "residual must be 0 or 1");
     if (D.prec == CBS_INT8 && (D.activation != CBS_ACT_SILU || D.residual))
         return fail(CBS_ERR_UNSUPPORTED, "INT8: the specified requantising SiLU epilogue only");
+    if (D.c_in_b < 0 || D.c_in_b >= D.c_in)
+        return fail(CBS_ERR_INVALID_ARG, "c_in_b %d: 0 (one input) or 1..c_in-1 (c_in = %d)", D.c_in_b, D.c_in);
+    if (D.c_in_b > 0 && D.prec == CBS_INT8)
+        return fail(CBS_ERR_UNSUPPORTED, "INT8: two-input (channel concatenation) layers are not built");
 
     cbs_plan_t p;
     std::memset(&p, 0, sizeof(p));
@@ -222,13 +221,13 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
     if (M > 0x7fffffffLL || (long long)D.n * D.c_in * D.h * D.w > (1LL << 40))
         return fail(CBS_ERR_UNSUPPORTED, "problem too large for 32-bit pixel indexing");
 
-    const bool stem_fits = D.c_in <= kStemMaxCin && D.c_out <= kStemMaxCout && D.k <= kStemMaxK;
+    const bool stem_fits = D.c_in <= kStemMaxCin && D.c_out <= kStemMaxCout && D.k <= kStemMaxK && D.c_in_b == 0;
     int variant = D.force_variant;
     if (variant < 0) variant = stem_fits ? (int)CBS_VARIANT_STEM : D.prec;  // FP32->SIMT, TF32, BF16, INT8
     if (variant == CBS_VARIANT_STEM) {
         if (!stem_fits)
-            return fail(CBS_ERR_UNSUPPORTED, "stem variant needs C_in <= %d, C_out <= %d, k <= %d", kStemMaxCin,
-                        kStemMaxCout, kStemMaxK);
+            return fail(CBS_ERR_UNSUPPORTED, "stem variant needs one input with C_in <= %d, C_out <= %d, k <= %d",
+                        kStemMaxCin, kStemMaxCout, kStemMaxK);
     } else {
         const int need_prec[] = {CBS_FP32, CBS_TF32, CBS_BF16, CBS_INT8};
         if (variant < 0 || variant > 3 || need_prec[variant] != D.prec)
@@ -253,6 +252,10 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
         if (D.in_layout != CBS_NHWC)
             return fail(CBS_ERR_UNSUPPORTED, "tensor-core variants read NHWC input (use cbs_pack_input)");
         p.c_in_pad = round_up(D.c_in, (int)(16 / eb));
+        if (D.c_in_b > 0 && (((size_t)(D.c_in - D.c_in_b) * eb) % 32 || ((size_t)D.c_in_b * eb) % 16))
+            return fail(CBS_ERR_UNSUPPORTED,
+                        "two-input tensor-core layers need the first input's pixels to be a multiple of 32 bytes "
+                        "and the second's of 16 bytes (c_in %d, c_in_b %d)", D.c_in, D.c_in_b);
     }
     p.k_gemm = D.k * D.k * p.c_in_pad;
     p.x_bytes = (size_t)D.n * D.h * D.w * p.c_in_pad * eb;
@@ -288,6 +291,12 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
         plan_simt(p);
     } else {
         CBS_TRY(plan_tc(p));
+    }
+    if (D.c_in_b > 0) {   // x holds the first c_in - c_in_b channels, x_b the rest (plus padding)
+        const int c_a = D.c_in - D.c_in_b;
+        const size_t pixels = (size_t)D.n * D.h * D.w;
+        p.x_bytes = pixels * c_a * eb;
+        p.x_b_bytes = pixels * (size_t)(p.c_in_pad - c_a) * eb;
     }
     *out = p;
     return CBS_OK;
@@ -329,6 +338,8 @@ cbs_status cbs_pack_input(const cbs_plan_t *p, const float *x_nchw, void *x_pack
     CBS_TRY(check_ptr(x_nchw, "x_nchw"));
     CBS_TRY(check_ptr(x_packed, "x_packed"));
     const cbs_layer_desc &d = p->desc;
+    if (d.c_in_b > 0)
+        return fail(CBS_ERR_UNSUPPORTED, "two-input plan: pack each input with a one-input plan of its own channels");
     if (d.n == 0) return CBS_OK;
     int dtype = 0;
     if (d.prec == CBS_BF16) dtype = 1;
@@ -363,11 +374,13 @@ namespace {
 
 // The FP32 / TF32 / BF16 layer with the plan's activation and an optional
 // residual (already checked against the plan by the caller).
-cbs_status conv_act_impl(const cbs_plan_t *p, const void *x, const void *w_packed, const float *bias,
-                         const void *residual, void *y, void *workspace, size_t workspace_bytes, void *stream) {
+cbs_status conv_act_impl(const cbs_plan_t *p, const void *x, const void *x_b, const void *w_packed,
+                         const float *bias, const void *residual, void *y, void *workspace, size_t workspace_bytes,
+                         void *stream) {
     const cbs_layer_desc &d = p->desc;
     if (d.n == 0) return CBS_OK;  // empty batch: nothing is read or written
     CBS_TRY(check_conv_common(p, x, w_packed, bias, y, workspace, workspace_bytes));
+    if (d.c_in_b > 0) CBS_TRY(check_ptr(x_b, "x_b"));
     if (residual && !aligned16(residual)) return fail(CBS_ERR_MISALIGNED, "residual is not 16-byte aligned");
     if (p->variant == CBS_VARIANT_STEM) {
         StemLaunch L = stem_launch(*p, x, w_packed, bias, nullptr, 0.0f, y);
@@ -378,6 +391,8 @@ cbs_status conv_act_impl(const cbs_plan_t *p, const void *x, const void *w_packe
         SimtLaunch L;
         std::memset(&L, 0, sizeof(L));
         L.x = (const float *)x; L.w = (const float *)w_packed; L.bias = bias; L.y = (float *)y;
+        L.x_b = d.c_in_b > 0 ? (const float *)x_b : nullptr;
+        L.C_a = d.c_in - d.c_in_b;
         L.N = d.n; L.C = d.c_in; L.H = d.h; L.W = d.w; L.Cout = d.c_out; L.OH = p->oh; L.OW = p->ow;
         L.KS = d.k; L.stride = d.stride; L.pad = d.pad;
         L.M = d.n * p->oh * p->ow;
@@ -401,7 +416,19 @@ cbs_status conv_act_impl(const cbs_plan_t *p, const void *x, const void *w_packe
         }
         return cuda_check(launch_simt(L, (cudaStream_t)stream), "SIMT kernel launch");
     }
-    return launch_tc(*p, x, w_packed, bias, nullptr, 0.0f, residual, y, workspace, (cudaStream_t)stream);
+    return launch_tc(*p, x, d.c_in_b > 0 ? x_b : nullptr, w_packed, bias, nullptr, 0.0f, residual, y, workspace,
+                     (cudaStream_t)stream);
+}
+
+// Activation/residual agreement between a plan and the call's arguments.
+cbs_status check_act_call(const cbs_plan_t *p, const void *residual) {
+    if (p->desc.prec == CBS_INT8)
+        return fail(CBS_ERR_INVALID_ARG, "INT8 plans run through cbs_conv_bn_silu_i8");
+    if (p->desc.residual && !residual && p->desc.n > 0)
+        return fail(CBS_ERR_INVALID_ARG, "residual is NULL for a plan with a residual");
+    if (!p->desc.residual && residual)
+        return fail(CBS_ERR_INVALID_ARG, "residual given for a plan without one");
+    return CBS_OK;
 }
 
 }  // namespace
@@ -416,19 +443,25 @@ cbs_status cbs_conv_bn_silu_f32(const cbs_plan_t *p, const void *x, const void *
         return fail(CBS_ERR_INVALID_ARG, "INT8 plans run through cbs_conv_bn_silu_i8");
     if (p->desc.activation != CBS_ACT_SILU || p->desc.residual)
         return fail(CBS_ERR_INVALID_ARG, "plan asks for another activation or a residual: call cbs_conv_bn_act");
-    return conv_act_impl(p, x, w_packed, bias, nullptr, y, workspace, workspace_bytes, stream);
+    if (p->desc.c_in_b > 0) return fail(CBS_ERR_INVALID_ARG, "two-input plan: call cbs_conv_bn_act_cat");
+    return conv_act_impl(p, x, nullptr, w_packed, bias, nullptr, y, workspace, workspace_bytes, stream);
 }
 
 cbs_status cbs_conv_bn_act(const cbs_plan_t *p, const void *x, const void *w_packed, const float *bias,
                            const void *residual, void *y, void *workspace, size_t workspace_bytes, void *stream) {
     CBS_TRY(check_plan(p));
-    if (p->desc.prec == CBS_INT8)
-        return fail(CBS_ERR_INVALID_ARG, "INT8 plans run through cbs_conv_bn_silu_i8");
-    if (p->desc.residual && !residual && p->desc.n > 0)
-        return fail(CBS_ERR_INVALID_ARG, "residual is NULL for a plan with a residual");
-    if (!p->desc.residual && residual)
-        return fail(CBS_ERR_INVALID_ARG, "residual given for a plan without one");
-    return conv_act_impl(p, x, w_packed, bias, residual, y, workspace, workspace_bytes, stream);
+    CBS_TRY(check_act_call(p, residual));
+    if (p->desc.c_in_b > 0) return fail(CBS_ERR_INVALID_ARG, "two-input plan: call cbs_conv_bn_act_cat");
+    return conv_act_impl(p, x, nullptr, w_packed, bias, residual, y, workspace, workspace_bytes, stream);
+}
+
+cbs_status cbs_conv_bn_act_cat(const cbs_plan_t *p, const void *x, const void *x_b, const void *w_packed,
+                               const float *bias, const void *residual, void *y, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+    CBS_TRY(check_plan(p));
+    CBS_TRY(check_act_call(p, residual));
+    if (p->desc.c_in_b <= 0) return fail(CBS_ERR_INVALID_ARG, "one-input plan: call cbs_conv_bn_act");
+    return conv_act_impl(p, x, x_b, w_packed, bias, residual, y, workspace, workspace_bytes, stream);
 }
 
 cbs_status cbs_conv_bn_silu_i8(const cbs_plan_t *p, const int8_t *x, const void *w_packed,
@@ -447,15 +480,15 @@ cbs_status cbs_conv_bn_silu_i8(const cbs_plan_t *p, const int8_t *x, const void 
         const StemLaunch L = stem_launch(*p, x, w_packed, bias_i32, m_c, inv_s_y, y);
         return cuda_check(launch_stem(L, (cudaStream_t)stream), "stem kernel launch");
     }
-    return launch_tc(*p, x, w_packed, bias_i32, m_c, inv_s_y, nullptr, y, workspace, (cudaStream_t)stream);
+    return launch_tc(*p, x, nullptr, w_packed, bias_i32, m_c, inv_s_y, nullptr, y, workspace, (cudaStream_t)stream);
 }
 
 cbs_status cbs_upsample2x_concat(const void *a, int ca, const void *b, int cb, void *out, int n, int h,
                                  int w, int layout, int elem_bytes, void *stream) {
     CBS_TRY(check_ptr(a, "a"));
-    CBS_TRY(check_ptr(b, "b"));
+    CBS_TRY(check_ptr(b, "b", cb == 0));
     CBS_TRY(check_ptr(out, "out"));
-    if (ca < 1 || cb < 1 || n < 0 || h < 2 || w < 2 || (h & 1) || (w & 1))
+    if (ca < 1 || cb < 0 || n < 0 || h < 2 || w < 2 || (h & 1) || (w & 1))
         return fail(CBS_ERR_INVALID_ARG, "bad upsample/concat shape (ca=%d cb=%d n=%d h=%d w=%d; h, w even)",
                     ca, cb, n, h, w);
     if (layout != CBS_NCHW && layout != CBS_NHWC) return fail(CBS_ERR_INVALID_ARG, "unknown layout %d", layout);

@@ -38,6 +38,13 @@ cbs_status cuda_check(cudaError_t e, const char *what);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Returns the status of `expr` from the calling function unless it is CBS_OK.
+#define CBS_TRY(expr)                      \
+    do {                                   \
+        cbs_status _s = (expr);            \
+        if (_s != CBS_OK) return _s;       \
+    } while (0)
+
 // ---------------------------------------------------------------- SIMT FP32
 // Tile configurations of the CUDA-core kernel (index = plan->block_k slot).
 struct SimtTile { int bm, bn, tm, tn; };
@@ -54,6 +61,8 @@ constexpr int kNumSimtTiles = sizeof(kSimtTiles) / sizeof(kSimtTiles[0]);
 
 struct SimtLaunch {
     const float *x;
+    const float *x_b;     // nullable: second input, channels C_a..C-1 (channel concatenation)
+    int C_a;              // channels held by x (= C without x_b)
     const float *w;       // [K][C_out]
     const float *bias;    // [C_out]
     float *y;
@@ -124,7 +133,7 @@ cbs_status read_and_reset_status(int *status_out, int reset, cudaStream_t s);
 
 // ---------------------------------------------------------------- tensor-core path
 struct TcLaunch;  // defined in k_tc.cu
-cbs_status launch_tc(const cbs_plan_t &p, const void *x, const void *w_packed,
+cbs_status launch_tc(const cbs_plan_t &p, const void *x, const void *x_b, const void *w_packed,
                      const void *bias, const float *m_c, float inv_s_y, const void *residual, void *y,
                      void *workspace, cudaStream_t s);
 // Host-side tile selection for the tensor-core variants (fills the tile

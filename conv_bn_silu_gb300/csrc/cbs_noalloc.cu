@@ -72,8 +72,9 @@ cbs_status cbs_conv_bn_silu_f32_noalloc(const cbs_plan_t *p, const float *x, con
         return fail(CBS_ERR_PLAN_MISMATCH, "plan was not made by cbs_plan of this library");
     if (p->variant != CBS_VARIANT_SIMT_FP32)
         return fail(CBS_ERR_UNSUPPORTED, "the allocation-free entry point runs FP32 CUDA-core plans only");
-    if (p->desc.activation != CBS_ACT_SILU || p->desc.residual)
-        return fail(CBS_ERR_UNSUPPORTED, "the allocation-free entry point runs SiLU plans without a residual");
+    if (p->desc.activation != CBS_ACT_SILU || p->desc.residual || p->desc.c_in_b)
+        return fail(CBS_ERR_UNSUPPORTED,
+                    "the allocation-free entry point runs one-input SiLU plans without a residual");
     if (p->workspace_bytes > kNoAllocScratchBytes)
         return fail(CBS_ERR_WORKSPACE, "plan needs %zu bytes of split-K scratch; the built-in scratch holds %zu",
                     p->workspace_bytes, kNoAllocScratchBytes);
@@ -92,6 +93,7 @@ cbs_status cbs_conv_bn_silu_f32_noalloc(const cbs_plan_t *p, const float *x, con
 
     SimtLaunch L{};
     L.x = x; L.w = w_packed; L.bias = bias; L.y = y;
+    L.x_b = nullptr; L.C_a = d.c_in;
     L.N = d.n; L.C = d.c_in; L.H = d.h; L.W = d.w; L.Cout = d.c_out; L.OH = p->oh; L.OW = p->ow;
     L.KS = d.k; L.stride = d.stride; L.pad = d.pad;
     L.M = d.n * p->oh * p->ow;

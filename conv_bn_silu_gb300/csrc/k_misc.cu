@@ -128,6 +128,54 @@ __global__ void pack_nhwc_kernel(const float *__restrict__ x, T *__restrict__ ou
     }
 }
 
+// Few channels (c_pad <= 8, e.g. a 3-channel frame padded to 4): one thread
+// per pixel, each block a run of 128 pixels of a row, rows walked by a
+// grid-stride loop.  Reads are coalesced per channel plane; a pixel's 4
+// channels leave as one vector store.
+template <typename T>
+__device__ __forceinline__ void store4(T *dst, const T (&v)[8]);
+template <>
+__device__ __forceinline__ void store4<float>(float *dst, const float (&v)[8]) {
+    *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *dst, const __nv_bfloat16 (&v)[8]) {
+    const uint32_t lo = (uint32_t)__bfloat16_as_ushort(v[0]) | ((uint32_t)__bfloat16_as_ushort(v[1]) << 16);
+    const uint32_t hi = (uint32_t)__bfloat16_as_ushort(v[2]) | ((uint32_t)__bfloat16_as_ushort(v[3]) << 16);
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(lo, hi);
+}
+template <>
+__device__ __forceinline__ void store4<int8_t>(int8_t *dst, const int8_t (&v)[8]) {
+    *reinterpret_cast<uint32_t *>(dst) = (uint32_t)(uint8_t)v[0] | ((uint32_t)(uint8_t)v[1] << 8) |
+                                         ((uint32_t)(uint8_t)v[2] << 16) | ((uint32_t)(uint8_t)v[3] << 24);
+}
+
+constexpr int kPackSmallThreads = 128;
+
+template <typename T>
+__global__ void __launch_bounds__(kPackSmallThreads) pack_nhwc_small_kernel(const float *__restrict__ x,
+                                                                            T *__restrict__ out, int C, int H, int W,
+                                                                            int rows, int c_pad, float s_x) {
+    const int w = blockIdx.x * kPackSmallThreads + threadIdx.x;
+    if (w >= W) return;
+    const size_t hw = (size_t)H * W;
+    for (int row = blockIdx.y; row < rows; row += gridDim.y) {   // row = n * H + h
+        const int n = row / H, h = row - n * H;
+        const float *src = x + (size_t)n * C * hw + (size_t)h * W + w;
+        T v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) v[c] = convert_out<T>(c < C ? __ldg(src + c * hw) : 0.0f, s_x);
+        T *dst = out + ((size_t)row * W + w) * c_pad;
+        if (c_pad == 4) {
+            store4<T>(dst, v);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                if (c < c_pad) dst[c] = v[c];
+        }
+    }
+}
+
 template <typename T>
 __global__ void pack_nchw_kernel(const float *__restrict__ x, T *__restrict__ out, size_t count,
                                  float s_x) {
@@ -211,7 +259,16 @@ cudaError_t launch_fold(const FoldLaunch &L, cudaStream_t s) {
 
 cudaError_t launch_pack_input(const float *x, void *out, int N, int C, int H, int W, int c_pad,
                               int to_nhwc, int dtype, float s_x, cudaStream_t s) {
-    if (to_nhwc) {
+    if (to_nhwc && c_pad <= 8) {
+        const int gx = (W + kPackSmallThreads - 1) / kPackSmallThreads;
+        const int rows = N * H;
+        int gy = kNumSMs * 32 / gx;
+        gy = gy < 1 ? 1 : (gy > rows ? rows : (gy > 65535 ? 65535 : gy));
+        const dim3 grid(gx, gy);
+        if (dtype == 0) pack_nhwc_small_kernel<float><<<grid, kPackSmallThreads, 0, s>>>(x, (float *)out, C, H, W, rows, c_pad, s_x);
+        else if (dtype == 1) pack_nhwc_small_kernel<__nv_bfloat16><<<grid, kPackSmallThreads, 0, s>>>(x, (__nv_bfloat16 *)out, C, H, W, rows, c_pad, s_x);
+        else pack_nhwc_small_kernel<int8_t><<<grid, kPackSmallThreads, 0, s>>>(x, (int8_t *)out, C, H, W, rows, c_pad, s_x);
+    } else if (to_nhwc) {
         dim3 grid((W + 31) / 32, (c_pad + 31) / 32, N * H), block(32, 8);
         if (dtype == 0) pack_nhwc_kernel<float><<<grid, block, 0, s>>>(x, (float *)out, C, H, W, c_pad, s_x);
         else if (dtype == 1) pack_nhwc_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(x, (__nv_bfloat16 *)out, C, H, W, c_pad, s_x);

@@ -31,7 +31,8 @@ namespace {
 __device__ __forceinline__ float silu_f32(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 struct KEntry {
-    int off;      // input offset of (r, s, ci) relative to the window corner
+    int off;      // input offset of (r, s, ci) relative to the window corner in x; for a
+                  // channel of the second input x_b, ~(its offset in x_b) (offsets are >= 0)
     short r, s;   // filter tap (r = kMaxTap marks k beyond the CTA's range)
 };
 constexpr short kNoTap = 0x3fff;
@@ -81,7 +82,12 @@ simt_conv_kernel(const SimtLaunch a) {
             const int tap = k / a.C;
             const int ci = k - tap * a.C;
             const int r = tap / a.KS, s = tap - (tap / a.KS) * a.KS;
-            e.off = NHWC_IN ? (r * a.W + s) * a.C + ci : (ci * a.H + r) * a.W + s;
+            if (ci < a.C_a) {
+                e.off = NHWC_IN ? (r * a.W + s) * a.C_a + ci : (ci * a.H + r) * a.W + s;
+            } else {   // channel concatenation: the rest come from x_b
+                const int cj = ci - a.C_a, cb = a.C - a.C_a;
+                e.off = ~(NHWC_IN ? (r * a.W + s) * cb + cj : (cj * a.H + r) * a.W + s);
+            }
             e.r = (short)r;
             e.s = (short)s;
         } else {
@@ -109,8 +115,13 @@ simt_conv_kernel(const SimtLaunch a) {
     // as ranges of the tap index: r in [r_lo, r_hi), s in [s_lo, s_hi).
     const int r_lo = mvalid ? max(0, -ih0) : kNoTap, r_hi = mvalid ? min(a.KS, a.H - ih0) : 0;
     const int s_lo = max(0, -iw0), s_hi = min(a.KS, a.W - iw0);
-    const float *__restrict__ xw = a.x + (size_t)img * a.C * a.H * a.W +
-                                   (NHWC_IN ? ((long long)ih0 * a.W + iw0) * a.C : (long long)ih0 * a.W + iw0);
+    const float *__restrict__ xw = a.x + (size_t)img * a.C_a * a.H * a.W +
+                                   (NHWC_IN ? ((long long)ih0 * a.W + iw0) * a.C_a : (long long)ih0 * a.W + iw0);
+    const int c_b = a.C - a.C_a;
+    const float *__restrict__ xw_b =
+        a.x_b ? a.x_b + (size_t)img * c_b * a.H * a.W +
+                    (NHWC_IN ? ((long long)ih0 * a.W + iw0) * c_b : (long long)ih0 * a.W + iw0)
+              : xw;
 
     float ra[A_PT], rb[B_PT];
     auto load_a = [&](int kl0) {
@@ -118,7 +129,7 @@ simt_conv_kernel(const SimtLaunch a) {
         for (int j = 0; j < A_PT; ++j) {
             const KEntry e = ktab[kl0 + ak0 + j * A_KSTEP];
             float v = 0.0f;
-            if (e.r >= r_lo && e.r < r_hi && e.s >= s_lo && e.s < s_hi) v = __ldg(xw + e.off);
+            if (e.r >= r_lo && e.r < r_hi && e.s >= s_lo && e.s < s_hi) v = __ldg(e.off >= 0 ? xw + e.off : xw_b + ~e.off);
             ra[j] = v;
         }
     };

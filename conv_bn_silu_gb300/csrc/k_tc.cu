@@ -107,6 +107,10 @@ struct TcParams {
     int SB;                    // weight-ring stages when the weights are streamed (windowed)
     int act;                   // cbs_activation
     const void *residual;      // nullable: added after the activation (y's layout and element type)
+    // Channel concatenation: channel blocks 0..ca_blocks-1 come from the first
+    // input (tensor map A), the rest from the second (tensor map A2, block
+    // cb - ca_blocks).  ca_blocks = cblocks with one input.
+    int ca_blocks;
 };
 
 constexpr int kStageBlockBytes = 4096;            // one warp's staged store block: 32 rows x 128 B
@@ -339,8 +343,8 @@ __device__ __forceinline__ bool aborted(int *abort_flag) { return *(volatile int
 // tile j+1.
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
-tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmY, const TcParams p) {
+tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+               const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Buffers start on a 1024-byte boundary of the shared window (the
     // swizzle atoms of TMA and of the MMA descriptors are address based).
@@ -396,6 +400,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmA);
+        if (p.ca_blocks < p.cblocks) ptx::prefetch_tmap(&tmA2);
         ptx::prefetch_tmap(&tmB);
         if (p.st_mode) ptx::prefetch_tmap(&tmY);
     }
@@ -500,7 +505,11 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                                                       : (uint32_t)(p.kg * (p.a_box_bytes + (p.b_res ? 0 : b_step_bytes))));
                     __syncwarp();
                     if (p.win) {
-                        if (lane == 0) ptx::tma_load_4d(sbase, &tmA, full_bar(s), st * p.CB, wc, hc, img);
+                        // A window stage is channel block st of the first or the second input.
+                        const bool second = st >= p.ca_blocks;
+                        if (lane == 0)
+                            ptx::tma_load_4d(sbase, second ? &tmA2 : &tmA, full_bar(s),
+                                             (second ? st - p.ca_blocks : st) * p.CB, wc, hc, img);
                     } else if (lane < nbox) {
                         const bool is_a = lane < p.kg;
                         const int kk = is_a ? lane : lane - p.kg;
@@ -509,11 +518,14 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         if (is_a) {
                             const uint32_t a_dst = sbase + kk * p.a_box_bytes;
                             const int r = tap / p.ks, tt = tap - r * p.ks;
+                            const bool second = cb >= p.ca_blocks;   // channel block of the second input
+                            const CUtensorMap *tm = second ? &tmA2 : &tmA;
+                            const int c0 = (second ? cb - p.ca_blocks : cb) * p.CB;
                             if (p.im2col)
-                                ptx::tma_load_im2col_4d(a_dst, &tmA, full_bar(s), cb * p.CB, wc, hc, img, (uint16_t)tt,
+                                ptx::tma_load_im2col_4d(a_dst, tm, full_bar(s), c0, wc, hc, img, (uint16_t)tt,
                                                         (uint16_t)r);
                             else
-                                ptx::tma_load_2d(a_dst, &tmA, full_bar(s), cb * p.CB, m0);
+                                ptx::tma_load_2d(a_dst, tm, full_bar(s), c0, m0);
                         } else {
                             ptx::tma_load_2d(sbase + p.kg * p.a_box_bytes + kk * p.b_tile_stride, &tmB, full_bar(s),
                                              tap * p.c_in_pad + cb * p.CB, n0);
@@ -1298,8 +1310,11 @@ cbs_status plan_tc(cbs_plan_t &p) {
         // One K step carries RB bytes of channels (32, 64 or 128: a TMA
         // swizzle span); C_in is padded so a pixel holds a multiple of 32 bytes.
         p.c_in_pad = round_up(d.c_in, 32 / eb);
+        // Two inputs: a channel block must not straddle them, so RB also
+        // divides the first input's pixel bytes (a multiple of 32).
         const int cbytes = p.c_in_pad * eb;
-        RB = (cbytes % 128 == 0) ? 128 : (cbytes % 64 == 0) ? 64 : 32;
+        const int abytes = d.c_in_b > 0 ? (d.c_in - d.c_in_b) * eb : cbytes;
+        RB = (cbytes % 128 == 0 && abytes % 128 == 0) ? 128 : (cbytes % 64 == 0 && abytes % 64 == 0) ? 64 : 32;
         CB = RB / eb;
     }
     p.k_gemm = d.k * d.k * p.c_in_pad;
@@ -1438,7 +1453,7 @@ cbs_status plan_tc(cbs_plan_t &p) {
     return CBS_OK;
 }
 
-cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, const void *bias,
+cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const void *w_packed, const void *bias,
                      const float *m_c, float inv_s_y, const void *residual, void *y, void *workspace,
                      cudaStream_t s) {
     (void)workspace;
@@ -1467,6 +1482,13 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     P.c_in_pad = pl.c_in_pad; P.CB = CB; P.RB = RB;
     P.cblocks = pl.c_in_pad / CB;
     P.ksteps = d.k * d.k * P.cblocks;
+    const int c_a = d.c_in - d.c_in_b;             // channels of the first input (all of them with one)
+    if (d.c_in_b > 0) {
+        if (i8 || !x_b || c_a % CB) return fail(CBS_ERR_PLAN_MISMATCH, "two-input plan: channel blocks");
+        P.ca_blocks = c_a / CB;
+    } else {
+        P.ca_blocks = P.cblocks;
+    }
     P.BN = BN; P.stages = pl.stages;
     P.m_tiles = pl.m_tiles; P.n_tiles = pl.n_tiles;
     const int mmul = i8 ? 1 : pl.block_m / kBM;
@@ -1566,35 +1588,48 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     }
     const cuuint32_t estr1[2] = {1, 1};
     const CUtensorMapSwizzle swz_x = XB == 16 ? CU_TENSOR_MAP_SWIZZLE_NONE : swizzle_for(XB);
-    if (P.win) {
-        const cuuint64_t dims[4] = {(cuuint64_t)pl.c_in_pad, (cuuint64_t)d.w, (cuuint64_t)d.h, (cuuint64_t)d.n};
-        const cuuint64_t strides[3] = {(cuuint64_t)pl.c_in_pad * eb_x, (cuuint64_t)d.w * pl.c_in_pad * eb_x,
-                                       (cuuint64_t)d.h * d.w * pl.c_in_pad * eb_x};
-        const cuuint32_t box[4] = {(cuuint32_t)CB, (cuuint32_t)P.Wp, (cuuint32_t)P.R_box, 1u};
-        const cuuint32_t es4[4] = {1, 1, 1, 1};
-        r = fns.tiled(&tmA, dt_x, 4, const_cast<void *>(x), dims, strides, box, es4, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      swz_x, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuTensorMapEncodeTiled (window) failed (%d)", (int)r);
-    } else if (P.im2col) {
-        const cuuint64_t dims[4] = {(cuuint64_t)pl.c_in_pad, (cuuint64_t)d.w, (cuuint64_t)d.h, (cuuint64_t)d.n};
-        const cuuint64_t strides[3] = {(cuuint64_t)pl.c_in_pad * eb_x, (cuuint64_t)d.w * pl.c_in_pad * eb_x,
-                                       (cuuint64_t)d.h * d.w * pl.c_in_pad * eb_x};
-        // Bounding box of the window corners: from -pad to (O-1)*stride - pad.
-        const int lower[2] = {-d.pad, -d.pad};
-        const int upper[2] = {(pl.ow - 1) * d.stride - d.pad - (d.w - 1), (pl.oh - 1) * d.stride - d.pad - (d.h - 1)};
-        const cuuint32_t estr[4] = {1, (cuuint32_t)d.stride, (cuuint32_t)d.stride, 1};
-        r = fns.im2col(&tmA, dt_x, 4, const_cast<void *>(x), dims, strides, lower, upper, (cuuint32_t)CB,
-                       (cuuint32_t)(kBM * mmul), estr,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, swz_x, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuTensorMapEncodeIm2col failed (%d)", (int)r);
+    // A map of one input tensor holding `chans` channels per pixel (NHWC).
+    auto make_a_map = [&](CUtensorMap *tm, const void *ptr, int chans, const char *what) -> cbs_status {
+        CUresult res;
+        void *gptr = const_cast<void *>(ptr);
+        if (P.win) {
+            const cuuint64_t dims[4] = {(cuuint64_t)chans, (cuuint64_t)d.w, (cuuint64_t)d.h, (cuuint64_t)d.n};
+            const cuuint64_t strides[3] = {(cuuint64_t)chans * eb_x, (cuuint64_t)d.w * chans * eb_x,
+                                           (cuuint64_t)d.h * d.w * chans * eb_x};
+            const cuuint32_t box[4] = {(cuuint32_t)CB, (cuuint32_t)P.Wp, (cuuint32_t)P.R_box, 1u};
+            const cuuint32_t es4[4] = {1, 1, 1, 1};
+            res = fns.tiled(tm, dt_x, 4, gptr, dims, strides, box, es4, CU_TENSOR_MAP_INTERLEAVE_NONE, swz_x,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (res != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuTensorMapEncodeTiled (%s window) failed (%d)", what, (int)res);
+        } else if (P.im2col) {
+            const cuuint64_t dims[4] = {(cuuint64_t)chans, (cuuint64_t)d.w, (cuuint64_t)d.h, (cuuint64_t)d.n};
+            const cuuint64_t strides[3] = {(cuuint64_t)chans * eb_x, (cuuint64_t)d.w * chans * eb_x,
+                                           (cuuint64_t)d.h * d.w * chans * eb_x};
+            // Bounding box of the window corners: from -pad to (O-1)*stride - pad.
+            const int lower[2] = {-d.pad, -d.pad};
+            const int upper[2] = {(pl.ow - 1) * d.stride - d.pad - (d.w - 1), (pl.oh - 1) * d.stride - d.pad - (d.h - 1)};
+            const cuuint32_t estr[4] = {1, (cuuint32_t)d.stride, (cuuint32_t)d.stride, 1};
+            res = fns.im2col(tm, dt_x, 4, gptr, dims, strides, lower, upper, (cuuint32_t)CB, (cuuint32_t)(kBM * mmul),
+                             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz_x, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (res != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuTensorMapEncodeIm2col (%s) failed (%d)", what, (int)res);
+        } else {
+            const cuuint64_t dims[2] = {(cuuint64_t)chans, (cuuint64_t)P.M};
+            const cuuint64_t strides[1] = {(cuuint64_t)chans * eb_x};
+            const cuuint32_t box[2] = {(cuuint32_t)CB, (cuuint32_t)(kBM * mmul)};
+            res = fns.tiled(tm, dt_x, 2, gptr, dims, strides, box, estr1, CU_TENSOR_MAP_INTERLEAVE_NONE, swz_x,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (res != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuTensorMapEncodeTiled (%s) failed (%d)", what, (int)res);
+        }
+        return CBS_OK;
+    };
+    alignas(64) CUtensorMap tmA2;
+    if (d.c_in_b > 0) {
+        CBS_TRY(make_a_map(&tmA, x, c_a, "A"));
+        CBS_TRY(make_a_map(&tmA2, x_b, pl.c_in_pad - c_a, "A of x_b"));
     } else {
-        const cuuint64_t dims[2] = {(cuuint64_t)pl.c_in_pad, (cuuint64_t)P.M};
-        const cuuint64_t strides[1] = {(cuuint64_t)pl.c_in_pad * eb_x};
-        const cuuint32_t box[2] = {(cuuint32_t)CB, (cuuint32_t)(kBM * mmul)};
-        r = fns.tiled(&tmA, dt_x, 2, const_cast<void *>(x), dims, strides, box, estr1, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      swz_x, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuTensorMapEncodeTiled (A) failed (%d)", (int)r);
+        CBS_TRY(make_a_map(&tmA, x, pl.c_in_pad, "A"));
+        std::memcpy(&tmA2, &tmA, sizeof(tmA));
     }
     {
         const cuuint64_t dims[2] = {(cuuint64_t)pl.k_gemm, (cuuint64_t)d.c_out};
@@ -1611,10 +1646,10 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *w_packed, 
     cudaError_t e;
     if (pl.variant == CBS_VARIANT_TC_TF32) {
         e = set_max_dyn_smem(tc_conv_kernel<kTF32>, pl.smem_bytes);
-        if (e == cudaSuccess) tc_conv_kernel<kTF32><<<grid, kThreads, pl.smem_bytes, s>>>(tmA, tmB, tmY, P);
+        if (e == cudaSuccess) tc_conv_kernel<kTF32><<<grid, kThreads, pl.smem_bytes, s>>>(tmA, tmA2, tmB, tmY, P);
     } else if (pl.variant == CBS_VARIANT_TC_BF16) {
         e = set_max_dyn_smem(tc_conv_kernel<kBF16>, pl.smem_bytes);
-        if (e == cudaSuccess) tc_conv_kernel<kBF16><<<grid, kThreads, pl.smem_bytes, s>>>(tmA, tmB, tmY, P);
+        if (e == cudaSuccess) tc_conv_kernel<kBF16><<<grid, kThreads, pl.smem_bytes, s>>>(tmA, tmA2, tmB, tmY, P);
     } else {
         e = set_max_dyn_smem(tc_conv_i8_kernel, pl.smem_bytes);
         if (e == cudaSuccess) tc_conv_i8_kernel<<<grid, kThreadsI8, pl.smem_bytes, s>>>(tmA, tmB, P);

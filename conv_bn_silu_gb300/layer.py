@@ -22,7 +22,7 @@ def current_stream() -> int:
 def make_desc(n, c_in, h, w, c_out, k, stride, pad=None, prec=B.CBS_FP32, in_layout=None,
               out_layout=None, force_variant=-1, force_split_k=0, force_block_n=0,
               force_block_m=0, out_row_stride=0, force_k_group=0, force_b_resident=0,
-              force_window=0, activation=B.CBS_ACT_SILU, residual=0) -> B.cbs_layer_desc:
+              force_window=0, activation=B.CBS_ACT_SILU, residual=0, c_in_b=0) -> B.cbs_layer_desc:
     if pad is None:
         pad = k // 2
     if in_layout is None:
@@ -36,7 +36,7 @@ def make_desc(n, c_in, h, w, c_out, k, stride, pad=None, prec=B.CBS_FP32, in_lay
                         force_block_n=force_block_n, force_block_m=force_block_m,
                         out_row_stride=out_row_stride, force_k_group=force_k_group,
                         force_b_resident=force_b_resident, force_window=force_window,
-                        activation=activation, residual=residual).items():
+                        activation=activation, residual=residual, c_in_b=c_in_b).items():
         setattr(d, name, int(v))
     return d
 
@@ -81,10 +81,20 @@ class FusedConvBnSilu:
         return _TORCH_DTYPE[self.prec]
 
     def x_shape(self):
+        """Shape of x (of the first input, for a two-input layer)."""
         d, p = self.desc, self.plan
+        c_a = d.c_in - d.c_in_b
         if d.in_layout == B.CBS_NCHW:
-            return (d.n, d.c_in, d.h, d.w)
-        return (d.n, d.h, d.w, p.c_in_pad)
+            return (d.n, c_a, d.h, d.w)
+        return (d.n, d.h, d.w, c_a if d.c_in_b else p.c_in_pad)
+
+    def x_b_shape(self):
+        """Shape of x_b, the second input of a two-input layer."""
+        d, p = self.desc, self.plan
+        assert d.c_in_b > 0
+        if d.in_layout == B.CBS_NCHW:
+            return (d.n, d.c_in_b, d.h, d.w)
+        return (d.n, d.h, d.w, p.c_in_pad - (d.c_in - d.c_in_b))
 
     def y_shape(self):
         d, p = self.desc, self.plan
@@ -106,13 +116,33 @@ class FusedConvBnSilu:
         B.cbs_pack_input(self.plan, x_nchw, out, self.s_x, current_stream())
         return out
 
+    def pack_inputs(self, x_nchw: torch.Tensor, x_b_nchw: torch.Tensor):
+        """Two-input layer: each NCHW float32 input -> its input format, each
+        through a one-input plan of its own channel count (kernel)."""
+        d = self.desc
+        out = []
+        for t, shape in ((x_nchw, self.x_shape()), (x_b_nchw, self.x_b_shape())):
+            assert t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()
+            one = make_desc(d.n, t.shape[1], d.h, d.w, 16, 1, 1, 0, prec=d.prec, in_layout=d.in_layout,
+                            force_variant=self.plan.variant)
+            o = torch.empty(shape, dtype=self.x_dtype, device=self.device)
+            B.cbs_pack_input(B.cbs_plan(one), t, o, self.s_x, current_stream())
+            out.append(o)
+        return tuple(out)
+
     def __call__(self, x: torch.Tensor, y: torch.Tensor | None = None, s_y: float | None = None,
-                 stream: int | None = None, residual: torch.Tensor | None = None) -> torch.Tensor:
+                 stream: int | None = None, residual: torch.Tensor | None = None,
+                 x_b: torch.Tensor | None = None) -> torch.Tensor:
         """residual: for descriptors with residual=1, a tensor shaped and typed
-        like y, added after the activation (may be y itself)."""
+        like y, added after the activation (may be y itself).  x_b: the second
+        input of a two-input (channel concatenation) layer."""
         y = self.empty_y() if y is None else y
         s = current_stream() if stream is None else stream
         ws_bytes = int(self.plan.workspace_bytes)
+        if self.desc.c_in_b:
+            B.cbs_conv_bn_act_cat(self.plan, x, x_b, self.w_packed, self.bias, residual, y, self.workspace,
+                                  ws_bytes, s)
+            return y
         if self.desc.residual or self.desc.activation != B.CBS_ACT_SILU:
             B.cbs_conv_bn_act(self.plan, x, self.w_packed, self.bias, residual, y, self.workspace, ws_bytes, s)
             return y
@@ -124,6 +154,19 @@ class FusedConvBnSilu:
             B.cbs_conv_bn_silu_f32(self.plan, x, self.w_packed, self.bias, y, self.workspace,
                                    ws_bytes, s)
         return y
+
+
+def upsample2x(a: torch.Tensor, layout: int, out: torch.Tensor | None = None):
+    """Nearest 2x upsample (the glue in front of a two-input layer)."""
+    if layout == B.CBS_NHWC:
+        n, h, w, ca = a.shape
+        shape = (n, 2 * h, 2 * w, ca)
+    else:
+        n, ca, h, w = a.shape
+        shape = (n, ca, 2 * h, 2 * w)
+    out = torch.empty(shape, dtype=a.dtype, device=a.device) if out is None else out
+    B.cbs_upsample2x_concat(a, ca, None, 0, out, n, 2 * h, 2 * w, layout, a.element_size(), current_stream())
+    return out
 
 
 def upsample2x_concat(a: torch.Tensor, b: torch.Tensor, layout: int, out: torch.Tensor | None = None):

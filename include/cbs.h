@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define CBS_ABI_VERSION 2
+#define CBS_ABI_VERSION 3
 
 /* Exported symbols (the library is built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -103,6 +103,14 @@ typedef struct cbs_layer_desc {
     int residual;        /* 1: add a residual tensor to the activated output, y = act(z) + r
                             (page 1's profile: the element-wise adds beside the convolutions);
                             the layer is then called through cbs_conv_bn_act.  FP32/TF32/BF16. */
+    int c_in_b;          /* 0: one input tensor x.  > 0: the layer's input is the channel
+                            concatenation of two tensors (page 1, "Improvements" #6, channel_cat
+                            fused into the convolution's input loads): channels 0..c_in-c_in_b-1
+                            come from x and the last c_in_b from x_b, both with the same N, H, W
+                            and layout; the layer is then called through cbs_conv_bn_act_cat.
+                            FP32 (CUDA-core variant), TF32 and BF16; the tensor-core variants
+                            need c_in - c_in_b to be a multiple of 16 (BF16) or 8 (TF32) channels
+                            and c_in_b a multiple of 8 (BF16) or 4 (TF32). */
 } cbs_layer_desc;
 
 /* A plan: plain data, owned by the caller, filled by cbs_plan. */
@@ -135,6 +143,8 @@ typedef struct cbs_plan_t {
     size_t w_packed_bytes;  /* bytes of the packed weight buffer */
     size_t bias_bytes;      /* bytes of the bias buffer (float or int32 per channel) */
     size_t workspace_bytes; /* scratch the call needs (0 = none) */
+    size_t x_b_bytes;       /* two-input plans: bytes of x_b the kernel reads (x_bytes is then
+                               x's share); 0 for one-input plans */
     cbs_layer_desc desc;    /* copy of the request */
 } cbs_plan_t;
 
@@ -149,6 +159,9 @@ typedef struct cbs_plan_t {
  *   TF32/BF16/INT8: x NHWC with c_in_pad channels (extra channels zero).
  *   STEM (chosen for C_in <= 4, C_out <= 64, k <= 7): x in d->in_layout;
  *   NHWC pixels hold c_in_pad = 4 channels for TF32/BF16/INT8, C_in for FP32.
+ *   Two-input plans (d->c_in_b > 0): x holds the first c_in - c_in_b channels
+ *   exactly; x_b the other c_in_b (SIMT FP32) or c_in_pad - (c_in - c_in_b)
+ *   (TF32/BF16, extra channels zero).
  * Errors: CBS_ERR_INVALID_ARG (shape, enum), CBS_ERR_UNSUPPORTED.
  */
 CBS_API cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out);
@@ -183,7 +196,9 @@ CBS_API cbs_status cbs_fold_bn(const cbs_plan_t *p, const float *w_oihw, const f
  * x_nchw: float [N][C_in][H][W].  x_packed: the plan's input format
  * (plan->x_bytes): SIMT with NCHW input: a copy; SIMT with NHWC input: float
  * NHWC; TF32: float NHWC padded to c_in_pad with zeros; BF16: bf16 (RNE);
- * INT8: int8 q = rne(clamp(x / s_x, -128, 127)).
+ * INT8: int8 q = rne(clamp(x / s_x, -128, 127)).  Two-input plans:
+ * CBS_ERR_UNSUPPORTED (each input is an earlier layer's output, or is packed
+ * with a one-input plan of its own channel count).
  */
 CBS_API cbs_status cbs_pack_input(const cbs_plan_t *p, const float *x_nchw, void *x_packed, float s_x,
                           void *stream);
@@ -218,6 +233,19 @@ CBS_API cbs_status cbs_conv_bn_act(const cbs_plan_t *p, const void *x, const voi
                                    void *stream);
 
 /*
+ * cbs_conv_bn_act_cat -- cbs_conv_bn_act for a two-input plan (d.c_in_b > 0):
+ * the convolution's input is concat(x, x_b) along channels, read straight from
+ * the two tensors (no concatenated copy is made).  x: the plan's input format
+ * with c_in - c_in_b channels; x_b: the same format with the remaining
+ * channels (see cbs_plan).  Other arguments, ownership and errors as for
+ * cbs_conv_bn_act.  The one-input entry points reject two-input plans
+ * (CBS_ERR_INVALID_ARG), and this one rejects one-input plans.
+ */
+CBS_API cbs_status cbs_conv_bn_act_cat(const cbs_plan_t *p, const void *x, const void *x_b, const void *w_packed,
+                                       const float *bias, const void *residual, void *y, void *workspace,
+                                       size_t workspace_bytes, void *stream);
+
+/*
  * cbs_conv_bn_silu_i8 -- the fused INT8 layer (page 3, "Highlights" and
  * "Design notes": per-output-channel weight scales, one activation scale).
  *   acc   = sum q_x * q_w + bias_i32         (exact integer)
@@ -239,6 +267,8 @@ CBS_API cbs_status cbs_conv_bn_silu_i8(const cbs_plan_t *p, const int8_t *x, con
  *   out[n, h, w, :] = concat( a[n, h/2, w/2, 0:ca], b[n, h, w, 0:cb] )
  * layout: CBS_NHWC or CBS_NCHW for all three tensors; elem_bytes: 1, 2 or 4.
  * a: [n][h/2][w/2][ca]; b, out: [n][h][w][cb] and [n][h][w][ca+cb] (as NHWC).
+ * cb = 0 (b may then be NULL) gives the plain nearest 2x upsample of a, the
+ * form that feeds a two-input layer (cbs_conv_bn_act_cat) directly.
  */
 CBS_API cbs_status cbs_upsample2x_concat(const void *a, int ca, const void *b, int cb, void *out,
                                  int n, int h, int w, int layout, int elem_bytes,

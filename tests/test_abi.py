@@ -28,10 +28,10 @@ def test_library_exports_every_declared_symbol(cuda_lib):
 
 
 def test_abi_version_and_struct_sizes(cuda_lib):
-    assert B.cbs_abi_version() == 2
+    assert B.cbs_abi_version() == 3
     plan = B.cbs_plan(make_desc(1, 16, 40, 40, 32, 3, 1))
     assert plan.size == ctypes.sizeof(B.cbs_plan_t)
-    assert plan.abi_version == 2
+    assert plan.abi_version == 3
 
 
 def test_status_strings(cuda_lib):
@@ -159,3 +159,57 @@ def test_activation_and_residual_argument_rules(cuda_lib):
     with pytest.raises(B.CbsError) as e:
         B.cbs_conv_bn_silu_f32_noalloc(ident, ok, ok, ok, ok, None)
     assert e.value.status == B.CBS_ERR_UNSUPPORTED
+
+
+def test_two_input_plans(cuda_lib):
+    """Channel-concatenation layers: what each variant accepts, the per-input
+    byte counts, and the entry points that refuse them (no launch)."""
+    ok = 1 << 20
+    # CUDA-core FP32, both layouts: x holds c_in - c_in_b channels, x_b the rest
+    for lay in (B.CBS_NCHW, B.CBS_NHWC):
+        p = B.cbs_plan(make_desc(2, 384, 40, 40, 128, 1, 1, in_layout=lay, c_in_b=128))
+        assert p.variant == B.CBS_VARIANT_SIMT_FP32
+        assert p.x_bytes == 2 * 40 * 40 * 256 * 4 and p.x_b_bytes == 2 * 40 * 40 * 128 * 4
+    # tensor cores: a channel block never straddles the two inputs
+    for prec, eb in ((B.CBS_BF16, 2), (B.CBS_TF32, 4)):
+        p = B.cbs_plan(make_desc(2, 384, 40, 40, 128, 1, 1, prec=prec, c_in_b=128))
+        assert (256 * eb) % (p.block_k * eb) == 0
+        assert p.x_bytes == 2 * 40 * 40 * 256 * eb and p.x_b_bytes == 2 * 40 * 40 * 128 * eb
+        p = B.cbs_plan(make_desc(1, 48, 20, 20, 64, 3, 1, prec=prec, c_in_b=16))
+        assert (32 % p.block_k) == 0 and p.x_b_bytes == 20 * 20 * (p.c_in_pad - 32) * eb
+    assert B.cbs_plan(make_desc(1, 24, 20, 20, 64, 3, 1, prec=B.CBS_BF16, c_in_b=8)).c_in_pad == 32
+    rejects = [
+        (dict(c_in=16, c_in_b=16), B.CBS_ERR_INVALID_ARG),                      # c_in_b must be < c_in
+        (dict(c_in=16, c_in_b=-1), B.CBS_ERR_INVALID_ARG),
+        (dict(c_in=32, c_in_b=16, prec=B.CBS_INT8), B.CBS_ERR_UNSUPPORTED),
+        (dict(c_in=24, c_in_b=16, prec=B.CBS_BF16), B.CBS_ERR_UNSUPPORTED),     # first input 8 bf16 = 16 B
+        (dict(c_in=36, c_in_b=4, prec=B.CBS_BF16), B.CBS_ERR_UNSUPPORTED),      # second input 4 bf16 = 8 B
+        (dict(c_in=4, c_in_b=2, force_variant=B.CBS_VARIANT_STEM), B.CBS_ERR_UNSUPPORTED),
+    ]
+    for kw, status in rejects:
+        prec = kw.pop("prec", B.CBS_FP32)
+        c_in = kw.pop("c_in")
+        lay = B.CBS_NHWC if prec != B.CBS_FP32 else B.CBS_NCHW
+        with pytest.raises(B.CbsError) as e:
+            B.cbs_plan(make_desc(1, c_in, 20, 20, 32, 3, 1, prec=prec, in_layout=lay, **kw))
+        assert e.value.status == status, (c_in, kw)
+    # a small-channel two-input layer takes the implicit GEMM, not the stem
+    assert B.cbs_plan(make_desc(1, 4, 20, 20, 16, 3, 1, c_in_b=2)).variant == B.CBS_VARIANT_SIMT_FP32
+    two = B.cbs_plan(make_desc(1, 64, 20, 20, 32, 3, 1, c_in_b=32))
+    one = B.cbs_plan(make_desc(1, 64, 20, 20, 32, 3, 1))
+    ws = two.workspace_bytes
+    for call in (lambda: B.cbs_conv_bn_silu_f32(two, ok, ok, ok, ok, ok, ws, None),
+                 lambda: B.cbs_conv_bn_act(two, ok, ok, ok, None, ok, ok, ws, None),
+                 lambda: B.cbs_conv_bn_act_cat(one, ok, ok, ok, ok, None, ok, ok, one.workspace_bytes, None),
+                 lambda: B.cbs_conv_bn_act_cat(two, ok, None, ok, ok, None, ok, ok, ws, None)):
+        with pytest.raises(B.CbsError) as e:
+            call()
+        assert e.value.status == B.CBS_ERR_INVALID_ARG
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_conv_bn_act_cat(two, ok, ok + 8, ok, ok, None, ok, ok, ws, None)
+    assert e.value.status == B.CBS_ERR_MISALIGNED
+    for call, status in ((lambda: B.cbs_pack_input(two, ok, ok, 0.0, None), B.CBS_ERR_UNSUPPORTED),
+                         (lambda: B.cbs_conv_bn_silu_f32_noalloc(two, ok, ok, ok, ok, None), B.CBS_ERR_UNSUPPORTED)):
+        with pytest.raises(B.CbsError) as e:
+            call()
+        assert e.value.status == status

@@ -55,10 +55,17 @@ def test_chain_teacher_forced(cuda_lib, prec, n):
     s = torch.cuda.current_stream().cuda_stream
     worst = []
     for i, layer in enumerate(chain.layers):
-        x_dev = torch.from_numpy(tile(ins[i])).cuda()
-        xin = layer.empty_x()
-        B.cbs_pack_input(layer.plan, x_dev, xin, 0.0, s)
-        y = to_nchw_numpy(layer(xin), chain.layout)
+        x_full = tile(ins[i])
+        c_b = layer.desc.c_in_b
+        if c_b:   # two-input layer: its inputs are the two parts of the concatenation
+            c_a = x_full.shape[1] - c_b
+            xa, xb = layer.pack_inputs(torch.from_numpy(np.ascontiguousarray(x_full[:, :c_a])).cuda(),
+                                       torch.from_numpy(np.ascontiguousarray(x_full[:, c_a:])).cuda())
+            y = to_nchw_numpy(layer(xa, x_b=xb), chain.layout)
+        else:
+            xin = layer.empty_x()
+            B.cbs_pack_input(layer.plan, torch.from_numpy(x_full).cuda(), xin, 0.0, s)
+            y = to_nchw_numpy(layer(xin), chain.layout)
         got = y[[0] if n == 1 else [0, n - 1]]
         e = rel_l2(got, outs[i])
         if prec == "fp32":

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 from conv_bn_silu_gb300 import _binding as B
-from conv_bn_silu_gb300.layer import FusedConvBnSilu, make_desc, upsample2x_concat
+from conv_bn_silu_gb300.layer import FusedConvBnSilu, make_desc, upsample2x, upsample2x_concat
 from conv_bn_silu_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -38,6 +38,18 @@ def test_upsample_concat_nchw(cuda_lib):
     assert torch.equal(out, ref)
 
 
+@pytest.mark.parametrize("layout", [B.CBS_NHWC, B.CBS_NCHW])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_upsample_only(cuda_lib, layout, dtype):
+    """cb = 0: the plain upsample that feeds a two-input layer."""
+    g = torch.Generator().manual_seed(11)
+    shape = (2, 5, 6, 24) if layout == B.CBS_NHWC else (2, 24, 5, 6)
+    a = (torch.randn(shape, generator=g) * 10).to(dtype)
+    out = upsample2x(a.cuda(), layout).cpu()
+    hw = (1, 2) if layout == B.CBS_NHWC else (2, 3)
+    assert torch.equal(out, a.repeat_interleave(2, hw[0]).repeat_interleave(2, hw[1]))
+
+
 def test_pack_input_fp32_nhwc(cuda_lib):
     spec = wl.LayerSpec(3, 16, 3, 2, 37)
     x, p = wl.layer_inputs(spec, 2)
@@ -46,3 +58,28 @@ def test_pack_input_fp32_nhwc(cuda_lib):
     xp = layer.pack_input(torch.from_numpy(x).cuda())
     torch.cuda.synchronize()
     assert np.array_equal(xp.cpu().numpy(), x.transpose(0, 2, 3, 1))
+
+
+@pytest.mark.parametrize("prec", [B.CBS_BF16, B.CBS_INT8, B.CBS_TF32])
+@pytest.mark.parametrize("c_in", [3, 8, 24])
+def test_pack_input_nhwc_exact(cuda_lib, prec, c_in):
+    """Entry packing to NHWC, padded channels zero: bf16 round-to-nearest-even,
+    int8 q = rne(clamp(x / s_x, -128, 127)), float copied; few channels take
+    the one-thread-per-pixel kernel, more the tiled transpose."""
+    n, h, w = 2, 19, 21
+    spec = wl.LayerSpec(c_in, 32, 3, 1, h, w)
+    x, p = wl.layer_inputs(spec, n)
+    s_x = 0.0125
+    desc = make_desc(n, c_in, h, w, 32, 3, 1, prec=prec, in_layout=B.CBS_NHWC, out_layout=B.CBS_NHWC)
+    layer = FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, s_x=s_x)
+    got = layer.pack_input(torch.from_numpy(x).cuda()).cpu()
+    c_pad = layer.plan.c_in_pad
+    xt = torch.zeros((n, h, w, c_pad), dtype=torch.float32)
+    xt[..., :c_in] = torch.from_numpy(x).permute(0, 2, 3, 1)
+    if prec == B.CBS_BF16:
+        assert torch.equal(got.view(torch.int16), xt.to(torch.bfloat16).view(torch.int16))
+    elif prec == B.CBS_INT8:
+        q = np.rint(np.clip(xt.numpy() / np.float32(s_x), -128, 127)).astype(np.int8)
+        assert np.array_equal(got.numpy(), q)
+    else:
+        assert torch.equal(got, xt)
