@@ -1,0 +1,76 @@
+"""Layers on host-resident tensors, with the copies overlapped with the kernels.
+
+For a run of independent layers whose inputs and outputs live in pinned host
+memory, `HostPipeline.run` enqueues
+  - every host-to-device input copy, back to back, on a copy stream;
+  - layer j on the compute stream, after an event that marks its own input
+    as landed (not after all inputs);
+  - layer j's device-to-host output copy on a second copy stream, as soon as
+    an event marks the layer as finished;
+so the host link carries inputs and outputs in both directions while the
+kernels run, instead of copy-all / compute-all / copy-all.  The copies are
+cudaMemcpyAsync calls (torch's copy_ on pinned memory) and every layer is a
+library kernel: nothing is computed on the host.
+"""
+from __future__ import annotations
+
+from typing import Callable, Sequence
+
+import torch
+
+
+class HostPipeline:
+    def __init__(self, n_layers: int, device="cuda"):
+        device = torch.device(device)
+        self.h2d = torch.cuda.Stream(device)
+        self.compute = torch.cuda.Stream(device)
+        self.d2h = torch.cuda.Stream(device)
+        self.ev_in = [torch.cuda.Event() for _ in range(n_layers)]
+        self.ev_out = [torch.cuda.Event() for _ in range(n_layers)]
+
+    def _enqueue(self, calls, xs_h, xs_d, ys_d, ys_h, origin) -> None:
+        n = len(calls)
+        assert n <= len(self.ev_in) and len(xs_h) == len(xs_d) == n and len(ys_d) == len(ys_h) == n
+        # Work already queued on `origin` may still use these buffers.
+        self.h2d.wait_stream(origin)
+        self.compute.wait_stream(origin)
+        self.d2h.wait_stream(origin)
+        with torch.cuda.stream(self.h2d):
+            for j in range(n):
+                xs_d[j].copy_(xs_h[j], non_blocking=True)
+                self.ev_in[j].record(self.h2d)
+        sid = self.compute.cuda_stream
+        for j in range(n):
+            self.compute.wait_event(self.ev_in[j])
+            calls[j](sid)
+            self.ev_out[j].record(self.compute)
+            self.d2h.wait_event(self.ev_out[j])
+            with torch.cuda.stream(self.d2h):
+                ys_h[j].copy_(ys_d[j], non_blocking=True)
+
+    def run(self, calls: Sequence[Callable[[int], None]], xs_h, xs_d, ys_d, ys_h) -> None:
+        """calls[j](stream) launches layer j on `stream` (a cudaStream_t as
+        int), reading xs_d[j] and writing ys_d[j].  xs_h / ys_h: pinned host
+        tensors of the same shapes.  Returns once every output is in ys_h."""
+        self._enqueue(calls, xs_h, xs_d, ys_d, ys_h, torch.cuda.current_stream())
+        self.d2h.synchronize()
+
+    def capture(self, calls: Sequence[Callable[[int], None]], xs_h, xs_d, ys_d, ys_h) -> Callable[[], None]:
+        """The same work recorded once as a CUDA graph (copies, kernels and
+        the events between the three streams become graph nodes and edges),
+        so a step costs one launch on the host.  Returns a function that
+        replays it and returns once every output is in ys_h."""
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(self.compute.device)
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(graph, stream=cap):
+            self._enqueue(calls, xs_h, xs_d, ys_d, ys_h, cap)   # fork from the capture stream
+            cap.wait_stream(self.h2d)                          # join every stream back
+            cap.wait_stream(self.compute)
+            cap.wait_stream(self.d2h)
+
+        def replay() -> None:
+            with torch.cuda.stream(cap):
+                graph.replay()
+            cap.synchronize()
+        return replay

@@ -1,0 +1,44 @@
+"""GPU check of the host-I/O pipeline: layers run on pinned host tensors
+(copies overlapped with the kernels on separate streams) give exactly the
+outputs of the same layers run on device-resident tensors, run after run."""
+import pytest
+import torch
+
+from conv_bn_silu_gb300 import _binding as B
+from conv_bn_silu_gb300 import workloads as wl
+from conv_bn_silu_gb300.host_io import HostPipeline
+from conv_bn_silu_gb300.layer import FusedConvBnSilu, make_desc
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("prec", [B.CBS_FP32, B.CBS_BF16])
+def test_pipeline_matches_device_runs(cuda_lib, prec):
+    specs = [wl.LayerSpec(16, 32, 3, 2, 64), wl.LayerSpec(32, 32, 1, 1, 40), wl.LayerSpec(64, 128, 3, 1, 20)]
+    layers, xs_d = [], []
+    for i, s in enumerate(specs):
+        x, p = wl.layer_inputs(s, 2, layer_index=30 + i)
+        layer = FusedConvBnSilu(make_desc(2, s.c_in, s.h, s.width, s.c_out, s.k, s.stride, s.pad, prec=prec),
+                                p.w, p.gamma, p.beta, p.mean, p.var, p.eps)
+        xd = torch.from_numpy(x).cuda()
+        xs_d.append(layer.pack_input(xd) if prec != B.CBS_FP32 else xd)
+        layers.append(layer)
+    want = [layer(x).cpu() for layer, x in zip(layers, xs_d)]
+    xs_h = [x.cpu().pin_memory() for x in xs_d]
+    ys_d = [layer.empty_y() for layer in layers]
+    ys_h = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys_d]
+    pipe = HostPipeline(len(layers))
+    calls = [(lambda st, j=j: layers[j](xs_d[j], ys_d[j], stream=st)) for j in range(len(layers))]
+    replay = pipe.capture(calls, xs_h, xs_d, ys_d, ys_h)
+    for run in range(6):
+        for y in ys_h:
+            y.zero_()
+        for x in xs_d:          # the pipeline must bring the inputs in itself
+            x.zero_()
+        torch.cuda.synchronize()
+        if run % 2:
+            replay()            # the CUDA-graph form
+        else:
+            pipe.run(calls, xs_h, xs_d, ys_d, ys_h)
+        for j in range(len(layers)):
+            assert torch.equal(ys_h[j], want[j]), (run, j)
