@@ -113,8 +113,8 @@ EXTRA_DEFAULT = ("layer_list_bf16_n16", "layer_list_tf32_n16", "layer_list_int8_
 # launches; the summary and command are in profiles/).  A figure is reported
 # only while the kernel's sources are the ones the counters were taken from.
 TRAFFIC = {
-    "layer_list_fp32_n1": {"kernel": "simt_conv_kernel", "launches": 11, "bytes": 28537088,
-                           "sources": ("k_simt.cu", "cbs_internal.cuh"), "digest": "7aa0dc9fa486c979",
+    "layer_list_fp32_n1": {"kernel": "simt_conv_kernel", "launches": 11, "bytes": 28574208,
+                           "sources": ("k_simt.cu", "cbs_internal.cuh"), "digest": "e5c884f3d10d7f17",
                            "profile": "profiles/launches_layer_list_fp32_n1.md"},
 }
 # Variant of the dominant kernel per precision (the direct small-channel
@@ -256,8 +256,12 @@ def make_workload(name, device):
 
 
 def measure(name, steps, warmup, device, peaks, sample_clocks=False):
-    """Capture `steps` steps (events between launches) in one CUDA graph,
-    replay it once untimed, then once timed; returns the summary."""
+    """Capture `steps` steps in one CUDA graph of plain launches (with the
+    library's default programmatic dependent launch, consecutive kernels
+    overlap their set-up), replay it once untimed, then once timed for the
+    step time.  The same steps captured a second time with an external event
+    between launches give each launch's duration (an event node between two
+    kernels also orders them fully, so that replay is not the timed one)."""
     import torch
     w = make_workload(name, device)
     stream = torch.cuda.Stream(device)
@@ -271,15 +275,20 @@ def measure(name, steps, warmup, device, peaks, sample_clocks=False):
         evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(nl + 1)] for _ in range(steps)]
     except TypeError:  # torch without external events: per-launch times unavailable
         evs = None
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(steps):
-                w.step(i, sid, evs[i] if evs is not None else None, stream)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        graph.replay()
-    torch.cuda.synchronize()
+    def capture(events):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(steps):
+                    w.step(i, sid, events[i] if events is not None else None, stream)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    graph = capture(None)
+    graph_ev = capture(evs) if evs is not None else None
     sampler = ClockSampler(device.index) if sample_clocks else None
     if sampler:
         time.sleep(0.3)
@@ -292,6 +301,9 @@ def measure(name, steps, warmup, device, peaks, sample_clocks=False):
     total_ms = t0.elapsed_time(t1)
     per_layer_us = None
     if evs is not None:
+        with torch.cuda.stream(stream):
+            graph_ev.replay()
+        torch.cuda.synchronize()
         per_layer_us = np.zeros(nl)
         for i in range(steps):
             for j in range(nl):
@@ -355,6 +367,8 @@ def run_ours(args, rank: int, world: int):
     device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(device)
     peaks, peak_src = load_peaks()
+    from conv_bn_silu_gb300 import _binding as B
+    B.cbs_set_launch_options(0 if args.no_pdl else B.CBS_LAUNCH_PDL)
     if world > 1:
         torch.distributed.barrier()
     head, w, clocks = measure(args.workload, args.steps, args.warmup, device, peaks, sample_clocks=True)
@@ -398,8 +412,11 @@ def run_ours(args, rank: int, world: int):
         "data": "synthetic (seeded N(0,1) inputs, He-init weights, random BN statistics)",
         "config": {"workload": args.workload, "layers": len(rows), "batch": n,
                    "layout": "NCHW" if w.prec == "fp32" else "NHWC", "l2": head["l2"],
-                   "timing": "K steps captured in one CUDA graph, events between launches on the launching stream",
-                   "parallelism": f"replicas x{world}"},
+                   "timing": ("K steps captured in one CUDA graph of programmatic dependent launches, CUDA events around "
+                              "its replay on the launching stream; per-launch durations from a replay of the same K steps "
+                              "captured with an event between launches"),
+                   "parallelism": f"replicas x{world}",
+                   "launch": "plain" if args.no_pdl else "programmatic dependent launch"},
         "roofline": roofline, "layers": rows,
         "gpu_launches": args.steps * w.launches_per_step,
         "e2e": e2e, "clocks": clocks, "peaks_source": peak_src,
@@ -533,6 +550,8 @@ def main():
     ap.add_argument("--workload", default="layer_list_fp32_n1", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the other configs' summaries")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="plain launches instead of programmatic dependent launches (for comparison)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

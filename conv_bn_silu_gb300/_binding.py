@@ -26,12 +26,13 @@ CBS_FP32, CBS_TF32, CBS_BF16, CBS_INT8 = 0, 1, 2, 3
 CBS_VARIANT_SIMT_FP32, CBS_VARIANT_TC_TF32, CBS_VARIANT_TC_BF16, CBS_VARIANT_TC_INT8 = 0, 1, 2, 3
 CBS_VARIANT_STEM = 4
 CBS_ACT_SILU, CBS_ACT_IDENTITY = 0, 1
+CBS_LAUNCH_PDL = 1
 
 EXPORTED = (
     "cbs_plan", "cbs_fold_bn", "cbs_pack_input", "cbs_conv_bn_silu_f32", "cbs_conv_bn_silu_i8",
     "cbs_upsample2x_concat", "cbs_workspace_init", "cbs_read_device_status", "cbs_status_string",
     "cbs_last_error", "cbs_abi_version", "cbs_conv_bn_silu_f32_noalloc", "cbs_conv_bn_act",
-    "cbs_conv_bn_act_cat",
+    "cbs_conv_bn_act_cat", "cbs_set_launch_options", "cbs_launch_options",
 )
 
 
@@ -87,8 +88,11 @@ def lib():
         L.cbs_last_error.restype = ctypes.c_char_p
         L.cbs_abi_version.argtypes = []
         L.cbs_abi_version.restype = I
+        L.cbs_set_launch_options.argtypes = [I]
+        L.cbs_launch_options.argtypes = []
+        L.cbs_launch_options.restype = I
         for name in EXPORTED:
-            if name not in ("cbs_status_string", "cbs_last_error", "cbs_abi_version"):
+            if name not in ("cbs_status_string", "cbs_last_error", "cbs_abi_version", "cbs_launch_options"):
                 getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -151,6 +155,14 @@ def cbs_conv_bn_silu_f32(plan, x, w_packed, bias, y, workspace, workspace_bytes,
 def cbs_conv_bn_act(plan, x, w_packed, bias, residual, y, workspace, workspace_bytes, stream):
     _check(lib().cbs_conv_bn_act(ctypes.byref(plan), _p(x), _p(w_packed), _p(bias), _p(residual), _p(y),
                                  _p(workspace), workspace_bytes, stream), "cbs_conv_bn_act")
+
+
+def cbs_set_launch_options(flags: int):
+    _check(lib().cbs_set_launch_options(int(flags)), "cbs_set_launch_options")
+
+
+def cbs_launch_options() -> int:
+    return int(lib().cbs_launch_options())
 
 
 def cbs_conv_bn_act_cat(plan, x, x_b, w_packed, bias, residual, y, workspace, workspace_bytes, stream):

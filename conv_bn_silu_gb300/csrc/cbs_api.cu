@@ -1,6 +1,7 @@
 // cbs_api.cu -- the C ABI (include/cbs.h): planning, argument checks and
 // dispatch to the kernels.  Planning is pure host code with no CUDA call.
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -26,6 +27,12 @@ cbs_status cuda_check(cudaError_t e, const char *what) {
     if (e == cudaSuccess) return CBS_OK;
     return fail(CBS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
+
+namespace {
+std::atomic<int> g_launch_options{CBS_LAUNCH_PDL};
+}
+
+int launch_options() { return g_launch_options.load(std::memory_order_relaxed); }
 
 namespace {
 
@@ -166,6 +173,14 @@ using namespace cbs;
 extern "C" {
 
 int cbs_abi_version(void) { return CBS_ABI_VERSION; }
+
+cbs_status cbs_set_launch_options(int flags) {
+    if (flags & ~CBS_LAUNCH_PDL) return fail(CBS_ERR_INVALID_ARG, "unknown launch option bits 0x%x", flags);
+    g_launch_options.store(flags);
+    return CBS_OK;
+}
+
+int cbs_launch_options(void) { return g_launch_options.load(); }
 
 const char *cbs_last_error(void) { return g_msg; }
 

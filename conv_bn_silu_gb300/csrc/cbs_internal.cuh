@@ -31,6 +31,29 @@ cudaError_t set_max_dyn_smem(F *kern, int bytes) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cap);
 }
 
+// Launch options set by cbs_set_launch_options (CBS_LAUNCH_* bits).
+int launch_options();
+
+// Launches `kern` on `s`; with CBS_LAUNCH_PDL set, as a programmatic
+// dependent launch (it may be scheduled before the preceding kernel in the
+// stream completes; the kernel itself waits for that kernel before it
+// touches global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (launch_options() & CBS_LAUNCH_PDL) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // Records a message for the calling thread and returns `s`.
 cbs_status fail(cbs_status s, const char *fmt, ...);
 // Maps a CUDA error to CBS_ERR_CUDA (with message) or CBS_OK.

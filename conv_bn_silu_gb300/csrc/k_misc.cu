@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 
 #include "cbs_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace cbs {
 namespace {
@@ -111,6 +112,8 @@ template <typename T>
 __global__ void pack_nhwc_kernel(const float *__restrict__ x, T *__restrict__ out, int C, int H,
                                  int W, int c_pad, float s_x) {
     __shared__ float tile[32][33];
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     const int w0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
     const int nh = blockIdx.z;  // n * H + h
     const int n = nh / H, h = nh - n * H;
@@ -156,6 +159,8 @@ template <typename T>
 __global__ void __launch_bounds__(kPackSmallThreads) pack_nhwc_small_kernel(const float *__restrict__ x,
                                                                             T *__restrict__ out, int C, int H, int W,
                                                                             int rows, int c_pad, float s_x) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     const int w = blockIdx.x * kPackSmallThreads + threadIdx.x;
     if (w >= W) return;
     const size_t hw = (size_t)H * W;
@@ -179,6 +184,8 @@ __global__ void __launch_bounds__(kPackSmallThreads) pack_nhwc_small_kernel(cons
 template <typename T>
 __global__ void pack_nchw_kernel(const float *__restrict__ x, T *__restrict__ out, size_t count,
                                  float s_x) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count;
          i += (size_t)gridDim.x * blockDim.x)
         out[i] = convert_out<T>(x[i], s_x);
@@ -188,6 +195,8 @@ __global__ void pack_nchw_kernel(const float *__restrict__ x, T *__restrict__ ou
 // NHWC, 16-byte vectors: out[n,h,w,:] = [a[n,h/2,w/2,:], b[n,h,w,:]].
 __global__ void upcat_nhwc_vec_kernel(const uint4 *__restrict__ a, int va, const uint4 *__restrict__ b,
                                       int vb, uint4 *__restrict__ out, int n, int h, int w) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     const int vt = va + vb;
     const size_t total = (size_t)n * h * w * vt;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
@@ -210,6 +219,8 @@ __global__ void upcat_nhwc_vec_kernel(const uint4 *__restrict__ a, int va, const
 template <typename T>
 __global__ void upcat_elem_kernel(const T *__restrict__ a, int ca, const T *__restrict__ b, int cb,
                                   T *__restrict__ out, int n, int h, int w, int nhwc) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     const int ct = ca + cb;
     const size_t total = (size_t)n * h * w * ct;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
@@ -253,7 +264,7 @@ int grid_for(size_t count, int threads) {
 }  // namespace
 
 cudaError_t launch_fold(const FoldLaunch &L, cudaStream_t s) {
-    fold_kernel<<<L.C_out, kFoldThreads, 0, s>>>(L);
+    fold_kernel<<<L.C_out, kFoldThreads, 0, s>>>(L);   // set-up: a plain launch, fully ordered
     return cudaGetLastError();
 }
 
@@ -265,20 +276,20 @@ cudaError_t launch_pack_input(const float *x, void *out, int N, int C, int H, in
         int gy = kNumSMs * 32 / gx;
         gy = gy < 1 ? 1 : (gy > rows ? rows : (gy > 65535 ? 65535 : gy));
         const dim3 grid(gx, gy);
-        if (dtype == 0) pack_nhwc_small_kernel<float><<<grid, kPackSmallThreads, 0, s>>>(x, (float *)out, C, H, W, rows, c_pad, s_x);
-        else if (dtype == 1) pack_nhwc_small_kernel<__nv_bfloat16><<<grid, kPackSmallThreads, 0, s>>>(x, (__nv_bfloat16 *)out, C, H, W, rows, c_pad, s_x);
-        else pack_nhwc_small_kernel<int8_t><<<grid, kPackSmallThreads, 0, s>>>(x, (int8_t *)out, C, H, W, rows, c_pad, s_x);
+        if (dtype == 0) launch_kernel(pack_nhwc_small_kernel<float>, grid, kPackSmallThreads, 0, s, x, (float *)out, C, H, W, rows, c_pad, s_x);
+        else if (dtype == 1) launch_kernel(pack_nhwc_small_kernel<__nv_bfloat16>, grid, kPackSmallThreads, 0, s, x, (__nv_bfloat16 *)out, C, H, W, rows, c_pad, s_x);
+        else launch_kernel(pack_nhwc_small_kernel<int8_t>, grid, kPackSmallThreads, 0, s, x, (int8_t *)out, C, H, W, rows, c_pad, s_x);
     } else if (to_nhwc) {
         dim3 grid((W + 31) / 32, (c_pad + 31) / 32, N * H), block(32, 8);
-        if (dtype == 0) pack_nhwc_kernel<float><<<grid, block, 0, s>>>(x, (float *)out, C, H, W, c_pad, s_x);
-        else if (dtype == 1) pack_nhwc_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(x, (__nv_bfloat16 *)out, C, H, W, c_pad, s_x);
-        else pack_nhwc_kernel<int8_t><<<grid, block, 0, s>>>(x, (int8_t *)out, C, H, W, c_pad, s_x);
+        if (dtype == 0) launch_kernel(pack_nhwc_kernel<float>, grid, block, 0, s, x, (float *)out, C, H, W, c_pad, s_x);
+        else if (dtype == 1) launch_kernel(pack_nhwc_kernel<__nv_bfloat16>, grid, block, 0, s, x, (__nv_bfloat16 *)out, C, H, W, c_pad, s_x);
+        else launch_kernel(pack_nhwc_kernel<int8_t>, grid, block, 0, s, x, (int8_t *)out, C, H, W, c_pad, s_x);
     } else {
         const size_t count = (size_t)N * C * H * W;
         const int g = grid_for(count, 256);
-        if (dtype == 0) pack_nchw_kernel<float><<<g, 256, 0, s>>>(x, (float *)out, count, s_x);
-        else if (dtype == 1) pack_nchw_kernel<__nv_bfloat16><<<g, 256, 0, s>>>(x, (__nv_bfloat16 *)out, count, s_x);
-        else pack_nchw_kernel<int8_t><<<g, 256, 0, s>>>(x, (int8_t *)out, count, s_x);
+        if (dtype == 0) launch_kernel(pack_nchw_kernel<float>, g, 256, 0, s, x, (float *)out, count, s_x);
+        else if (dtype == 1) launch_kernel(pack_nchw_kernel<__nv_bfloat16>, g, 256, 0, s, x, (__nv_bfloat16 *)out, count, s_x);
+        else launch_kernel(pack_nchw_kernel<int8_t>, g, 256, 0, s, x, (int8_t *)out, count, s_x);
     }
     return cudaGetLastError();
 }
@@ -290,14 +301,14 @@ cudaError_t launch_upsample_concat(const void *a, int ca, const void *b, int cb,
     if (vec) {
         const int va = ca * eb / 16, vb = cb * eb / 16;
         const size_t total = (size_t)n * h * w * (va + vb);
-        upcat_nhwc_vec_kernel<<<grid_for(total, 256), 256, 0, s>>>(
+        launch_kernel(upcat_nhwc_vec_kernel, grid_for(total, 256), 256, 0, s, 
             (const uint4 *)a, va, (const uint4 *)b, vb, (uint4 *)out, n, h, w);
     } else {
         const size_t total = (size_t)n * h * w * (ca + cb);
         const int g = grid_for(total, 256);
-        if (eb == 4) upcat_elem_kernel<uint32_t><<<g, 256, 0, s>>>((const uint32_t *)a, ca, (const uint32_t *)b, cb, (uint32_t *)out, n, h, w, nhwc);
-        else if (eb == 2) upcat_elem_kernel<uint16_t><<<g, 256, 0, s>>>((const uint16_t *)a, ca, (const uint16_t *)b, cb, (uint16_t *)out, n, h, w, nhwc);
-        else upcat_elem_kernel<uint8_t><<<g, 256, 0, s>>>((const uint8_t *)a, ca, (const uint8_t *)b, cb, (uint8_t *)out, n, h, w, nhwc);
+        if (eb == 4) launch_kernel(upcat_elem_kernel<uint32_t>, g, 256, 0, s, (const uint32_t *)a, ca, (const uint32_t *)b, cb, (uint32_t *)out, n, h, w, nhwc);
+        else if (eb == 2) launch_kernel(upcat_elem_kernel<uint16_t>, g, 256, 0, s, (const uint16_t *)a, ca, (const uint16_t *)b, cb, (uint16_t *)out, n, h, w, nhwc);
+        else launch_kernel(upcat_elem_kernel<uint8_t>, g, 256, 0, s, (const uint8_t *)a, ca, (const uint8_t *)b, cb, (uint8_t *)out, n, h, w, nhwc);
     }
     return cudaGetLastError();
 }

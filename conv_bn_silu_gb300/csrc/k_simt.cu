@@ -21,6 +21,7 @@
 // the epilogue and puts the counter back to zero.  Nothing waits on another
 // CTA, so there is no spin loop.
 #include "cbs_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace cbs {
 namespace {
@@ -64,6 +65,9 @@ simt_conv_kernel(const SimtLaunch a) {
     float (*Bs)[BK][BN] = reinterpret_cast<float (*)[BK][BN]>(smem + 2 * BK * BM);
     KEntry *ktab = reinterpret_cast<KEntry *>(smem + TILE_FLOATS);
     __shared__ int s_is_last;
+    // The next grid may be scheduled now: it waits for this one before it
+    // touches global memory.
+    ptx::griddep_launch_dependents();
 
     const int t = threadIdx.x;
     const int tx = t % TX, ty = t / TX;
@@ -162,6 +166,9 @@ simt_conv_kernel(const SimtLaunch a) {
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
 
+    // The k table and the window above come from the launch parameters only;
+    // the previous grid in the stream must be complete before any load.
+    ptx::griddep_wait();
     __syncthreads();  // k table ready
     if (klen > 0) {
         load_a(0);
@@ -313,6 +320,11 @@ cudaError_t launch_one(dim3 grid, const SimtLaunch &L, cudaStream_t s) {
         cudaError_t e = set_max_dyn_smem(kern, bytes);
         if (e != cudaSuccess) return e;
     }
+    // A plain launch: measured on GB300, programmatic dependent launch made
+    // the batch-1 list 20% slower with these kernels.  Their grids are one
+    // partial wave of small CTAs, and CTAs scheduled early pile onto the SMs
+    // that have room while the previous kernel runs, instead of spreading
+    // over all 152.
     kern<<<grid, NT, bytes, s>>>(L);
     return cudaGetLastError();
 }

@@ -108,6 +108,8 @@ __global__ void __launch_bounds__(256) stem_kernel(const StemLaunch a) {
     constexpr int P = StemTile<KIND, COUT>::P;
     extern __shared__ float4 wsm4[];  // [KK * c_pad][COUT] floats
     float *wsm = reinterpret_cast<float *>(wsm4);
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     const int KK = a.KS * a.KS;
     const int kpad = KK * a.c_pad;
     // Folded weights: packed [C_out][KK * c_pad] (float, or bf16 holding
@@ -258,6 +260,7 @@ cudaError_t launch_kind(const StemLaunch &L, cudaStream_t s) {
         else e = set_max_dyn_smem(stem_kernel<KIND, COUT, false, false>, smem);
         if (e != cudaSuccess) return e;
     }
+    // Plain launches, as for the CUDA-core implicit GEMM (see k_simt.cu).
     if (L.in_nhwc && L.out_nhwc) stem_kernel<KIND, COUT, true, true><<<grid, 256, smem, s>>>(L);
     else if (L.in_nhwc) stem_kernel<KIND, COUT, true, false><<<grid, 256, smem, s>>>(L);
     else if (L.out_nhwc) stem_kernel<KIND, COUT, false, true><<<grid, 256, smem, s>>>(L);
@@ -363,6 +366,11 @@ __global__ void __launch_bounds__(256) stem_tc_bf16_kernel(const StemLaunch a, i
         ptx::mbar_init(ptx::smem_u32(&bars[1]), 1);
         ptx::fence_mbar_init();
     }
+    // This CTA holds its tensor memory: the next grid may be scheduled.  Then
+    // wait for the previous one before touching global memory.
+    __syncthreads();
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
     // B row co: the folded weights of output channel co in the K layout above,
     // zero for co >= C_out; 16-byte chunk q stored at q ^ (co % 8).
     const uint2 *w2 = static_cast<const uint2 *>(a.w);   // [C_out][KK] taps of 4 bf16
@@ -554,8 +562,7 @@ cudaError_t launch_stem_tc_as(const StemLaunch &L, int n_mma, StemTcGeom g, int 
     auto kern = stem_tc_bf16_kernel<OUT_NHWC, PAIRS>;
     const cudaError_t e = set_max_dyn_smem(kern, kStemTcSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, 256, kStemTcSmemBytes, s>>>(L, n_mma, g, status);
-    return cudaGetLastError();
+    return launch_kernel(kern, grid, 256, kStemTcSmemBytes, s, L, n_mma, g, status);
 }
 
 cudaError_t launch_stem_tc(const StemLaunch &L, cudaStream_t s) {

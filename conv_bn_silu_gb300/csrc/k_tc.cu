@@ -404,8 +404,6 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         ptx::prefetch_tmap(&tmB);
         if (p.st_mode) ptx::prefetch_tmap(&tmY);
     }
-    if (p.bias_smem)
-        for (int i = threadIdx.x; i < p.C_out; i += blockDim.x) bias_sm[i] = p.bias[i];
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), p.tmem_cols);
         ptx::tmem_relinquish();
@@ -413,6 +411,14 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    // This CTA holds its tensor memory: the next grid may be scheduled.  Then
+    // wait for the previous one before touching global memory.
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
+    if (p.bias_smem) {
+        for (int i = threadIdx.x; i < p.C_out; i += blockDim.x) bias_sm[i] = p.bias[i];
+        __syncthreads();
+    }
     const uint32_t tmem_base = *tmem_slot;
     const float *bias = p.bias_smem ? bias_sm : p.bias;
 
@@ -837,6 +843,8 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    ptx::griddep_launch_dependents();   // after this CTA's TMEM allocation
+    ptx::griddep_wait();
     const uint32_t tmem_base = *tmem_slot;
 
     int last_g = -1;
@@ -1646,16 +1654,15 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     cudaError_t e;
     if (pl.variant == CBS_VARIANT_TC_TF32) {
         e = set_max_dyn_smem(tc_conv_kernel<kTF32>, pl.smem_bytes);
-        if (e == cudaSuccess) tc_conv_kernel<kTF32><<<grid, kThreads, pl.smem_bytes, s>>>(tmA, tmA2, tmB, tmY, P);
+        if (e == cudaSuccess) e = launch_kernel(tc_conv_kernel<kTF32>, grid, kThreads, pl.smem_bytes, s, tmA, tmA2, tmB, tmY, P);
     } else if (pl.variant == CBS_VARIANT_TC_BF16) {
         e = set_max_dyn_smem(tc_conv_kernel<kBF16>, pl.smem_bytes);
-        if (e == cudaSuccess) tc_conv_kernel<kBF16><<<grid, kThreads, pl.smem_bytes, s>>>(tmA, tmA2, tmB, tmY, P);
+        if (e == cudaSuccess) e = launch_kernel(tc_conv_kernel<kBF16>, grid, kThreads, pl.smem_bytes, s, tmA, tmA2, tmB, tmY, P);
     } else {
         e = set_max_dyn_smem(tc_conv_i8_kernel, pl.smem_bytes);
-        if (e == cudaSuccess) tc_conv_i8_kernel<<<grid, kThreadsI8, pl.smem_bytes, s>>>(tmA, tmB, P);
+        if (e == cudaSuccess) e = launch_kernel(tc_conv_i8_kernel, grid, kThreadsI8, pl.smem_bytes, s, tmA, tmB, P);
     }
-    if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute");
-    return cuda_check(cudaGetLastError(), "tensor-core kernel launch");
+    return cuda_check(e, "tensor-core kernel launch");
 }
 
 }  // namespace cbs

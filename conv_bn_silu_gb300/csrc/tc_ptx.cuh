@@ -136,6 +136,23 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// --------------------------------------- programmatic dependent launch
+// Both are no-ops for a kernel launched without the programmatic
+// stream-serialisation attribute.
+// Wait until the preceding grid in the stream has completed and its memory
+// operations are visible.  Every global read or write of a kernel in this
+// library comes after this wait.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next grid in the stream to be scheduled (its CTAs then run their
+// prologue and block in griddep_wait until this grid completes).  Kernels
+// that allocate tensor memory signal only after their allocation: a
+// dependent CTA that took the columns first would wait on this grid while
+// this grid waited for the columns.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------- per-thread async copies
 // Copy 8 or 16 bytes global -> shared; bytes past src_bytes (0 or the full
 // size) are written as zero, so src_bytes = 0 zero-fills without reading.

@@ -296,6 +296,27 @@ CBS_API cbs_status cbs_upsample2x_concat(const void *a, int ca, const void *b, i
 CBS_API cbs_status cbs_conv_bn_silu_f32_noalloc(const cbs_plan_t *p, const float *x, const float *w_packed,
                                                 const float *bias, float *y, void *stream);
 
+/*
+ * cbs_set_launch_options -- process-wide launch options for every kernel
+ * the library enqueues afterwards (a bit set, CBS_LAUNCH_*):
+ *   CBS_LAUNCH_PDL  programmatic dependent launch (default on) of the
+ *                   tensor-core kernels, the tensor-core stem and the
+ *                   packing and glue kernels: a kernel may be scheduled while
+ *                   the previous kernel in the stream finishes, runs its
+ *                   set-up (barriers, tensor memory, tensor-map prefetch)
+ *                   meanwhile, and waits for that kernel before it reads or
+ *                   writes global memory.  The CUDA-core kernels always use
+ *                   plain launches (measured faster).  Results are the same
+ *                   with the bit clear; only the gap between kernels changes.
+ *                   Inside a CUDA graph capture the dependency becomes a
+ *                   programmatic edge.
+ * Not synchronised with launches in flight on other threads.
+ * Errors: CBS_ERR_INVALID_ARG for unknown bits.
+ */
+#define CBS_LAUNCH_PDL 1
+CBS_API cbs_status cbs_set_launch_options(int flags);
+CBS_API int cbs_launch_options(void);
+
 /* Zero a workspace before its first use (cudaMemsetAsync on `stream`). */
 CBS_API cbs_status cbs_workspace_init(void *workspace, size_t bytes, void *stream);
 

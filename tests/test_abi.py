@@ -213,3 +213,17 @@ def test_two_input_plans(cuda_lib):
         with pytest.raises(B.CbsError) as e:
             call()
         assert e.value.status == status
+
+
+def test_launch_options(cuda_lib):
+    """Programmatic dependent launch is on by default and can be switched."""
+    assert B.cbs_launch_options() == B.CBS_LAUNCH_PDL
+    try:
+        B.cbs_set_launch_options(0)
+        assert B.cbs_launch_options() == 0
+        with pytest.raises(B.CbsError) as e:
+            B.cbs_set_launch_options(6)
+        assert e.value.status == B.CBS_ERR_INVALID_ARG
+        assert B.cbs_launch_options() == 0
+    finally:
+        B.cbs_set_launch_options(B.CBS_LAUNCH_PDL)
