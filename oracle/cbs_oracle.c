@@ -21,8 +21,9 @@
  *
  * The INT8 oracle follows the quantised scheme step by step in float
  * arithmetic with a fixed operation order (per-output-channel symmetric weight
- * scales, one symmetric activation scale, integer accumulation, bias folded in
- * int32, SiLU in float, round-half-even back to int8).  Its exp is our own
+ * scales, one activation scale, symmetric or with a zero point, integer
+ * accumulation, bias folded in int32, SiLU in float, round-half-even back to
+ * int8).  Its exp is our own
  * Cody-Waite range reduction (W. J. Cody and W. Waite, "Software Manual for
  * the Elementary Functions", 1980) followed by a degree-7 Taylor polynomial,
  * so that the result does not depend on any libm.  Build with
@@ -199,6 +200,22 @@ ORACLE_API void oracle_quantize_act(const float *x, size_t count, float s_x, int
     }
 }
 
+/* Asymmetric activation quantisation ("Edge optimisation of YOLO26", Design
+ * notes: asymmetric activations, symmetric weights; the affine scheme of
+ * Jacob et al., CVPR 2018, r = s (q - z)), on signed 8-bit codes:
+ *   q = clamp(rne(x / s_x) + z_x, -128, 127),   z_x in [-128, 127].
+ * A uint8 code u with zero point z_u is the same value as q = u - 128 with
+ * z = z_u - 128.  With z_x = 0 this is oracle_quantize_act. */
+ORACLE_API void oracle_quantize_act_zp(const float *x, size_t count, float s_x, int z_x, int8_t *q)
+{
+#pragma omp parallel for
+    for (size_t i = 0; i < count; ++i) {
+        float v = rne(x[i] / s_x) + (float)z_x;
+        v = v < -128.0f ? -128.0f : (v > 127.0f ? 127.0f : v);
+        q[i] = (int8_t)v;
+    }
+}
+
 /* Fold BN into the weights and quantise them per output channel.
  *   s_c   = gamma / sqrtf(var + eps)
  *   w'    = w * s_c                      b' = beta - mean * s_c
@@ -253,6 +270,20 @@ ORACLE_API int8_t oracle_requant(int32_t acc, float m_c, float inv_s_y)
     return (int8_t)rne(v);
 }
 
+/* Requantisation to an asymmetric output code:
+ *   t = float(acc) * m_c;  u = t / (1 + exp(-t));  v = u * (1 / s_y);
+ *   q = clamp(rne(v) + z_y, -128, 127).
+ * With z_y = 0 this is oracle_requant (the bounds are integers). */
+ORACLE_API int8_t oracle_requant_zp(int32_t acc, float m_c, float inv_s_y, int z_y)
+{
+    const float t = (float)acc * m_c;
+    const float e = oracle_spec_exp(-t);
+    const float u = t / (1.0f + e);
+    float v = rne(u * inv_s_y) + (float)z_y;
+    v = v < -128.0f ? -128.0f : (v > 127.0f ? 127.0f : v);
+    return (int8_t)v;
+}
+
 /* INT8 layer: integer convolution (int64 accumulation; the sum must fit in
  * int32, which the function checks), plus the int32 bias, then the epilogue.
  * q_x: [N][C_in][H][W], q_w: [C_out][C_in][k][k], q_y: [N][C_out][OH][OW].
@@ -288,6 +319,49 @@ ORACLE_API int oracle_conv_i8(const int8_t *q_x, const int8_t *q_w, const int32_
                     const size_t o = (((size_t)n * C_out + co) * OH + oh) * OW + ow;
                     if (acc_out) acc_out[o] = (int32_t)acc;
                     q_y[o] = oracle_requant((int32_t)acc, m_c[co], inv_s_y);
+                }
+            }
+        }
+    }
+    return bad ? -1 : 0;
+}
+
+/* The INT8 layer with asymmetric activations: input codes q_x with zero point
+ * z_x, output codes with zero point z_y, symmetric per-channel weights.
+ *   acc = bias_i32 + sum over the taps inside the image of (q_x - z_x) * q_w
+ * (a tap outside the image is a real zero and adds nothing), then
+ * oracle_requant_zp.  Layouts, acc_out and the return value as for
+ * oracle_conv_i8; with z_x = z_y = 0 the two functions agree. */
+ORACLE_API int oracle_conv_i8_zp(const int8_t *q_x, const int8_t *q_w, const int32_t *bias_i32,
+                                 const float *m_c, float s_y, int z_x, int z_y, int N, int C_in, int H, int W,
+                                 int C_out, int k, int stride, int pad, int8_t *q_y, int32_t *acc_out)
+{
+    const int OH = oracle_out_dim(H, k, stride, pad);
+    const int OW = oracle_out_dim(W, k, stride, pad);
+    const float inv_s_y = 1.0f / s_y;
+    int bad = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic) reduction(|:bad)
+    for (int n = 0; n < N; ++n) {
+        for (int co = 0; co < C_out; ++co) {
+            for (int oh = 0; oh < OH; ++oh) {
+                for (int ow = 0; ow < OW; ++ow) {
+                    int64_t acc = bias_i32[co];
+                    for (int ci = 0; ci < C_in; ++ci) {
+                        for (int r = 0; r < k; ++r) {
+                            const int ih = oh * stride - pad + r;
+                            if (ih < 0 || ih >= H) continue;
+                            for (int s = 0; s < k; ++s) {
+                                const int iw = ow * stride - pad + s;
+                                if (iw < 0 || iw >= W) continue;
+                                const int64_t xv = (int64_t)q_x[(((size_t)n * C_in + ci) * H + ih) * W + iw] - z_x;
+                                acc += xv * (int64_t)q_w[(((size_t)co * C_in + ci) * k + r) * k + s];
+                            }
+                        }
+                    }
+                    if (acc > INT32_MAX || acc < INT32_MIN) bad = 1;
+                    const size_t o = (((size_t)n * C_out + co) * OH + oh) * OW + ow;
+                    if (acc_out) acc_out[o] = (int32_t)acc;
+                    q_y[o] = oracle_requant_zp((int32_t)acc, m_c[co], inv_s_y, z_y);
                 }
             }
         }

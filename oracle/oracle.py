@@ -42,6 +42,11 @@ def _load():
         lib.oracle_requant.restype = ctypes.c_int8
         lib.oracle_conv_i8.argtypes = [P, P, P, P, F, I, I, I, I, I, I, I, I, P, P]
         lib.oracle_conv_i8.restype = I
+        lib.oracle_quantize_act_zp.argtypes = [P, Z, F, I, P]
+        lib.oracle_requant_zp.argtypes = [ctypes.c_int32, F, F, I]
+        lib.oracle_requant_zp.restype = ctypes.c_int8
+        lib.oracle_conv_i8_zp.argtypes = [P, P, P, P, F, I, I, I, I, I, I, I, I, I, I, P, P]
+        lib.oracle_conv_i8_zp.restype = I
         _lib = lib
     return _lib
 
@@ -138,10 +143,15 @@ def spec_exp(x) -> np.ndarray:
     return y
 
 
-def quantize_act(x, s_x: float) -> np.ndarray:
+def quantize_act(x, s_x: float, z_x: int = 0) -> np.ndarray:
+    """q = clamp(rne(x / s_x), -128, 127); with a zero point z_x (asymmetric
+    activations), q = clamp(rne(x / s_x) + z_x, -128, 127)."""
     x = _f32(x)
     q = np.empty(x.shape, np.int8)
-    _load().oracle_quantize_act(_ptr(x), x.size, s_x, _ptr(q))
+    if z_x:
+        _load().oracle_quantize_act_zp(_ptr(x), x.size, s_x, int(z_x), _ptr(q))
+    else:
+        _load().oracle_quantize_act(_ptr(x), x.size, s_x, _ptr(q))
     return q
 
 
@@ -159,12 +169,16 @@ def fold_quant_i8(w, gamma, beta, mean, var, eps: float, s_x: float):
     return q_w, bias, m_c
 
 
-def requant(acc: int, m_c: float, inv_s_y: float) -> int:
+def requant(acc: int, m_c: float, inv_s_y: float, z_y: int = 0) -> int:
+    if z_y:
+        return int(_load().oracle_requant_zp(int(acc), float(m_c), float(inv_s_y), int(z_y)))
     return int(_load().oracle_requant(int(acc), float(m_c), float(inv_s_y)))
 
 
-def conv_i8(q_x, q_w, bias_i32, m_c, s_y: float, stride: int, pad: int, return_acc: bool = False):
-    """INT8 layer; returns q_y int8 [N, C_out, OH, OW] (and the int32 accumulators)."""
+def conv_i8(q_x, q_w, bias_i32, m_c, s_y: float, stride: int, pad: int, return_acc: bool = False,
+            z_x: int = 0, z_y: int = 0):
+    """INT8 layer; returns q_y int8 [N, C_out, OH, OW] (and the int32 accumulators).
+    z_x, z_y: zero points of asymmetric input and output codes (0: symmetric)."""
     q_x = np.ascontiguousarray(q_x, np.int8)
     q_w = np.ascontiguousarray(q_w, np.int8)
     bias_i32 = np.ascontiguousarray(bias_i32, np.int32)
@@ -174,8 +188,12 @@ def conv_i8(q_x, q_w, bias_i32, m_c, s_y: float, stride: int, pad: int, return_a
     OH, OW = out_dim(H, k, stride, pad), out_dim(W, k, stride, pad)
     q_y = np.empty((N, C_out, OH, OW), np.int8)
     acc = np.empty((N, C_out, OH, OW), np.int32) if return_acc else None
-    rc = _load().oracle_conv_i8(_ptr(q_x), _ptr(q_w), _ptr(bias_i32), _ptr(m_c), s_y,
-                                N, C_in, H, W, C_out, k, stride, pad, _ptr(q_y), _ptr(acc))
+    if z_x or z_y:
+        rc = _load().oracle_conv_i8_zp(_ptr(q_x), _ptr(q_w), _ptr(bias_i32), _ptr(m_c), s_y, int(z_x), int(z_y),
+                                       N, C_in, H, W, C_out, k, stride, pad, _ptr(q_y), _ptr(acc))
+    else:
+        rc = _load().oracle_conv_i8(_ptr(q_x), _ptr(q_w), _ptr(bias_i32), _ptr(m_c), s_y,
+                                    N, C_in, H, W, C_out, k, stride, pad, _ptr(q_y), _ptr(acc))
     if rc != 0:
         raise OverflowError("INT8 accumulator left the int32 range")
     return (q_y, acc) if return_acc else q_y

@@ -411,3 +411,72 @@ def test_int8_layer_tracks_fp32_layer():
     q_y = oracle.conv_i8(q_x, q_w, bias, m_c, s_y, 1, 1)
     err = np.abs(q_y.astype(np.float64) * s_y - y32)
     assert err.mean() < 1.0 * s_y and err.max() < 6 * s_y
+
+
+# ------------------------------------------------- asymmetric INT8 activations
+# ("Edge optimisation of YOLO26", Design notes: asymmetric activations,
+# symmetric per-channel weights; the affine scheme r = s (q - z).)
+
+@pytest.mark.parametrize("k,stride,z_x", [(3, 1, -37), (3, 2, 90), (1, 1, -128), (5, 2, 127)])
+def test_int8_zero_point_accumulation_exact(k, stride, z_x):
+    """acc = bias + conv(q_x - z_x, q_w) with zero padding in the (q - z)
+    domain: a padded tap is a real zero and adds nothing.  PyTorch float64
+    conv2d (exact on these integers) is the independent sum."""
+    r = rng(40 + k + stride)
+    q_x = r.integers(-128, 128, size=(2, 6, 9, 11)).astype(np.int8)
+    q_w = r.integers(-127, 128, size=(4, 6, k, k)).astype(np.int8)
+    bias = r.integers(-10**5, 10**5, size=4).astype(np.int32)
+    m_c = np.full(4, 1e-4, np.float32)
+    _, acc = oracle.conv_i8(q_x, q_w, bias, m_c, 0.05, stride, k // 2, return_acc=True, z_x=z_x, z_y=3)
+    xs = torch.from_numpy(q_x.astype(np.float64) - z_x)
+    ref = torch.nn.functional.conv2d(xs, torch.from_numpy(q_w.astype(np.float64)), stride=stride,
+                                     padding=k // 2).numpy()
+    assert np.array_equal(acc.astype(np.int64), ref.astype(np.int64) + bias[None, :, None, None])
+
+
+def test_quantize_zero_point():
+    """q = clamp(rne(x / s) + z): x = 0 maps to z, the dequantised value
+    s (q - z) is within s/2 of x inside the range, and the ends saturate."""
+    s = 0.02
+    for z in (-128, -61, 0, 44, 127):
+        lo, hi = (-128 - z) * s, (127 - z) * s
+        x = np.linspace(lo + s, hi - s, 4001, dtype=np.float32)
+        q = oracle.quantize_act(np.concatenate([x, [0.0, lo - 1, hi + 1]]).astype(np.float32), s, z)
+        assert q[-3] == z and q[-2] == -128 and q[-1] == 127
+        err = np.abs(s * (q[:-3].astype(np.float64) - z) - x)
+        assert err.max() <= 0.5 * s * (1 + 1e-4)
+
+
+def test_requant_zero_point_against_float64():
+    r = rng(11)
+    accs = r.integers(-200000, 200000, size=20000)
+    m_c, s_y = 1.7e-4, 0.031
+    inv = float(np.float32(1.0) / np.float32(s_y))
+    for z_y in (-100, 57):
+        got = np.array([oracle.requant(int(a), m_c, inv, z_y) for a in accs])
+        t = accs.astype(np.float64) * np.float64(np.float32(m_c))
+        v = t / (1 + np.exp(-t)) * inv
+        want = np.clip(np.round(v) + z_y, -128, 127)   # numpy rounds half to even
+        near_tie = np.abs(v - np.floor(v) - 0.5) < 1e-4
+        assert np.all(np.abs(got - want) <= 1)
+        assert np.all(got[~near_tie] == want[~near_tie])
+        assert oracle.requant(0, m_c, inv, z_y) == z_y
+
+
+def test_asymmetric_int8_layer_tracks_fp32_layer():
+    """Post-SiLU-like activations (mostly positive) quantised with a zero
+    point near the bottom of the code range: the dequantised output of the
+    asymmetric layer follows the FP32 layer within a few output steps."""
+    spec = wl.LayerSpec(16, 8, 3, 1, 12)
+    x, p = wl.layer_inputs(spec, 2, layer_index=6)
+    x = (x / (1 + np.exp(-x))).astype(np.float32)          # SiLU(x): in [-0.28, ...)
+    s_x = float(np.float32((x.max() - x.min()) / 255))
+    z_x = int(-128 - round(float(x.min()) / s_x))
+    y32 = oracle.conv_bn_silu_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, 1, 1)
+    s_y = float(np.float32((y32.max() - y32.min()) / 255))
+    z_y = int(-128 - round(float(y32.min()) / s_y))
+    q_x = oracle.quantize_act(x, s_x, z_x)
+    q_w, bias, m_c = oracle.fold_quant_i8(p.w, p.gamma, p.beta, p.mean, p.var, p.eps, s_x)
+    q_y = oracle.conv_i8(q_x, q_w, bias, m_c, s_y, 1, 1, z_x=z_x, z_y=z_y)
+    err = np.abs((q_y.astype(np.float64) - z_y) * s_y - y32)
+    assert err.mean() < 1.0 * s_y and err.max() < 6 * s_y
