@@ -102,9 +102,11 @@ WORKLOADS = {
     # The list with the residual form of the epilogue, y = SiLU(BN(conv)) + r, on every
     # stride-1 layer whose input and output shapes match (a bottleneck's skip add).
     "layer_list_bf16_n16_residual": dict(kind="list", layers=wl.LAYER_LIST, n=16, prec="bf16", residual=True),
+    # asymmetric activations: input codes with zero point -20, outputs with -100
+    "layer_list_int8_n16_asym": dict(kind="list", layers=wl.LAYER_LIST, n=16, prec="int8", zero_points=(-20, -100)),
 }
 EXTRA_DEFAULT = ("layer_list_bf16_n16", "layer_list_tf32_n16", "layer_list_int8_n16", "chain_fp32_n1",
-                 "chain_bf16_n16", "layer_list_bf16_n16_residual")
+                 "chain_bf16_n16", "layer_list_bf16_n16_residual", "layer_list_int8_n16_asym")
 
 
 # DRAM traffic of the dominant kernel over one step of a workload, from one
@@ -172,10 +174,11 @@ class ListWorkload:
         s_x = float(wl.S_X_INT8) if self.prec == "int8" else 0.0
         self.s_y = int8_scales() if self.prec == "int8" else [None] * len(self.specs)
         self.res = [bool(cfg.get("residual")) and s.c_in == s.c_out and s.stride == 1 for s in self.specs]
+        z_x, z_y = cfg.get("zero_points", (0, 0))
         for i, spec in enumerate(self.specs):
             x, p = wl.layer_inputs(spec, self.n, seed=0, layer_index=i)
             desc = make_desc(self.n, spec.c_in, spec.h, spec.width, spec.c_out, spec.k, spec.stride, spec.pad,
-                             prec=cp, residual=int(self.res[i]))
+                             prec=cp, residual=int(self.res[i]), zero_point_x=z_x, zero_point_y=z_y)
             self.layers.append(FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, s_x=s_x,
                                                device=device))
             host_x.append(x)

@@ -40,7 +40,8 @@ class cbs_layer_desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "n", "c_in", "h", "w", "c_out", "k", "stride", "pad", "in_layout", "out_layout", "prec",
         "force_variant", "force_split_k", "force_block_n", "force_block_m", "out_row_stride",
-        "force_k_group", "force_b_resident", "force_window", "activation", "residual", "c_in_b")]
+        "force_k_group", "force_b_resident", "force_window", "activation", "residual", "c_in_b",
+        "zero_point_x", "zero_point_y")]
 
 
 class cbs_plan_t(ctypes.Structure):

@@ -162,6 +162,8 @@ StemLaunch stem_launch(const cbs_plan_t &p, const void *x, const void *w, const 
     L.kind = d.prec == CBS_INT8 ? 2 : (d.prec == CBS_BF16 ? 1 : 0);
     L.act = d.activation;
     L.residual = nullptr;
+    L.zp_x = d.prec == CBS_INT8 ? d.zero_point_x : 0;
+    L.zp_y = d.prec == CBS_INT8 ? d.zero_point_y : 0;
     return L;
 }
 
@@ -223,6 +225,11 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
         return fail(CBS_ERR_INVALID_ARG, "c_in_b %d: 0 (one input) or 1..c_in-1 (c_in = %d)", D.c_in_b, D.c_in);
     if (D.c_in_b > 0 && D.prec == CBS_INT8)
         return fail(CBS_ERR_UNSUPPORTED, "INT8: two-input (channel concatenation) layers are not built");
+    if (D.prec != CBS_INT8 && (D.zero_point_x || D.zero_point_y))
+        return fail(CBS_ERR_INVALID_ARG, "zero points apply to INT8 plans only");
+    if (D.zero_point_x < -128 || D.zero_point_x > 127 || D.zero_point_y < -128 || D.zero_point_y > 127)
+        return fail(CBS_ERR_INVALID_ARG, "zero points must lie in [-128, 127] (z_x %d, z_y %d)", D.zero_point_x,
+                    D.zero_point_y);
 
     cbs_plan_t p;
     std::memset(&p, 0, sizeof(p));
@@ -344,6 +351,7 @@ cbs_status cbs_fold_bn(const cbs_plan_t *p, const float *w_oihw, const float *co
         L.variant = by_prec[p->desc.prec];
     }
     L.w_packed = w_packed; L.bias = bias; L.m_c = m_c;
+    L.z_x = p->desc.prec == CBS_INT8 ? p->desc.zero_point_x : 0;
     return cuda_check(launch_fold(L, (cudaStream_t)stream), "fold kernel launch");
 }
 
@@ -364,7 +372,7 @@ cbs_status cbs_pack_input(const cbs_plan_t *p, const float *x_nchw, void *x_pack
     }
     const int to_nhwc = d.in_layout == CBS_NHWC;
     return cuda_check(launch_pack_input(x_nchw, x_packed, d.n, d.c_in, d.h, d.w, p->c_in_pad, to_nhwc,
-                                        dtype, s_x, (cudaStream_t)stream),
+                                        dtype, s_x, d.prec == CBS_INT8 ? d.zero_point_x : 0, (cudaStream_t)stream),
                       "pack kernel launch");
 }
 

@@ -115,6 +115,7 @@ struct StemLaunch {
     int kind;                  // 0 float, 1 bf16, 2 int8
     int act;                   // cbs_activation (float kinds)
     const void *residual;      // nullable, element type and layout of y (float kinds)
+    int zp_x, zp_y;            // INT8 zero points of input and output codes
 };
 cudaError_t launch_stem(const StemLaunch &L, cudaStream_t s);
 // BF16 stems (4-channel NHWC input, k <= 3, C_out <= 64) run on the tensor
@@ -139,12 +140,13 @@ struct FoldLaunch {
     void *w_packed;
     void *bias;               // float or int32
     float *m_c;               // INT8 only
+    int z_x;                  // INT8: input zero point (0 = symmetric)
 };
 cudaError_t launch_fold(const FoldLaunch &L, cudaStream_t s);
 
 // dtype codes for packing: 0 float, 1 bf16, 2 int8 (quantised with s_x)
 cudaError_t launch_pack_input(const float *x_nchw, void *out, int N, int C, int H, int W,
-                              int c_pad, int to_nhwc, int dtype, float s_x, cudaStream_t s);
+                              int c_pad, int to_nhwc, int dtype, float s_x, int zp, cudaStream_t s);
 
 cudaError_t launch_upsample_concat(const void *a, int ca, const void *b, int cb, void *out,
                                    int n, int h, int w, int nhwc, int elem_bytes,

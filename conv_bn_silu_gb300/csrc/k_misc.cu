@@ -77,6 +77,24 @@ __global__ void __launch_bounds__(kFoldThreads) fold_kernel(const FoldLaunch a) 
         }
         out[(size_t)co * kpad + k] = __float2bfloat16_rn(q);  // exact: |q| <= 127
     }
+    // Input zero point: the bias becomes bias_i32 - z_x * sum(q_w[c, :]),
+    // in two's-complement int32 arithmetic (the kernels' sums are exact
+    // modulo 2^32, so they are exact whenever the true accumulator fits).
+    __shared__ unsigned int qsum_red[kFoldThreads / 32];
+    unsigned int qsum = 0u;
+    if (a.z_x != 0) {
+        for (int k = threadIdx.x; k < kin; k += blockDim.x) {
+            float q = rintf(__fdiv_rn(__fmul_rn(wrow[k], s_c), s_w));
+            q = fminf(fmaxf(q, -127.0f), 127.0f);
+            qsum += (unsigned int)(int)q;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) qsum += __shfl_xor_sync(0xffffffffu, qsum, o);
+        if ((threadIdx.x & 31) == 0) qsum_red[threadIdx.x >> 5] = qsum;
+        __syncthreads();
+        qsum = 0u;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) qsum += qsum_red[i];
+    }
     if (threadIdx.x == 0) {
         const float mc = __fmul_rn(a.s_x, s_w);
         const float bq = rintf(__fdiv_rn(b_fold, mc));
@@ -84,6 +102,7 @@ __global__ void __launch_bounds__(kFoldThreads) fold_kernel(const FoldLaunch a) 
         if (bq >= 2147483648.0f) bi = INT32_MAX;
         else if (bq < -2147483648.0f) bi = INT32_MIN;
         else bi = (int32_t)bq;
+        if (a.z_x != 0) bi = (int32_t)((unsigned int)bi - (unsigned int)a.z_x * qsum);
         static_cast<int32_t *>(a.bias)[co] = bi;
         a.m_c[co] = mc;
     }
@@ -94,23 +113,28 @@ __global__ void __launch_bounds__(kFoldThreads) fold_kernel(const FoldLaunch a) 
 // int8 (q = rne(clamp(x / s_x, -128, 127))).  32x32 (w, c) tiles through
 // shared memory so both the read and the write are coalesced.
 template <typename T>
-__device__ __forceinline__ T convert_out(float v, float s_x);
+__device__ __forceinline__ T convert_out(float v, float s_x, int zp);
 template <>
-__device__ __forceinline__ float convert_out<float>(float v, float) { return v; }
+__device__ __forceinline__ float convert_out<float>(float v, float, int) { return v; }
 template <>
-__device__ __forceinline__ __nv_bfloat16 convert_out<__nv_bfloat16>(float v, float) {
+__device__ __forceinline__ __nv_bfloat16 convert_out<__nv_bfloat16>(float v, float, int) {
     return __float2bfloat16_rn(v);
 }
+// q = clamp(rne(x / s_x) + zp, -128, 127); with zp = 0 the same as
+// rne(clamp(x / s_x, -128, 127)) (integer bounds).
 template <>
-__device__ __forceinline__ int8_t convert_out<int8_t>(float v, float s_x) {
-    float q = __fdiv_rn(v, s_x);
+__device__ __forceinline__ int8_t convert_out<int8_t>(float v, float s_x, int zp) {
+    float q = __fadd_rn(rintf(__fdiv_rn(v, s_x)), (float)zp);
     q = fminf(fmaxf(q, -128.0f), 127.0f);
-    return (int8_t)rintf(q);
+    return (int8_t)q;
 }
+// Padding channels hold code 0 in every format.
+template <typename T>
+__device__ __forceinline__ T zero_code() { return convert_out<T>(0.0f, 1.0f, 0); }
 
 template <typename T>
 __global__ void pack_nhwc_kernel(const float *__restrict__ x, T *__restrict__ out, int C, int H,
-                                 int W, int c_pad, float s_x) {
+                                 int W, int c_pad, float s_x, int zp) {
     __shared__ float tile[32][33];
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
@@ -127,7 +151,8 @@ __global__ void pack_nhwc_kernel(const float *__restrict__ x, T *__restrict__ ou
     __syncthreads();
     for (int i = ty; i < 32; i += 8) {
         const int w = w0 + i, c = c0 + tx;
-        if (w < W && c < c_pad) out[(((size_t)n * H + h) * W + w) * c_pad + c] = convert_out<T>(tile[tx][i], s_x);
+        if (w < W && c < c_pad)
+            out[(((size_t)n * H + h) * W + w) * c_pad + c] = c < C ? convert_out<T>(tile[tx][i], s_x, zp) : zero_code<T>();
     }
 }
 
@@ -158,7 +183,7 @@ constexpr int kPackSmallThreads = 128;
 template <typename T>
 __global__ void __launch_bounds__(kPackSmallThreads) pack_nhwc_small_kernel(const float *__restrict__ x,
                                                                             T *__restrict__ out, int C, int H, int W,
-                                                                            int rows, int c_pad, float s_x) {
+                                                                            int rows, int c_pad, float s_x, int zp) {
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
     const int w = blockIdx.x * kPackSmallThreads + threadIdx.x;
@@ -169,7 +194,7 @@ __global__ void __launch_bounds__(kPackSmallThreads) pack_nhwc_small_kernel(cons
         const float *src = x + (size_t)n * C * hw + (size_t)h * W + w;
         T v[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) v[c] = convert_out<T>(c < C ? __ldg(src + c * hw) : 0.0f, s_x);
+        for (int c = 0; c < 8; ++c) v[c] = c < C ? convert_out<T>(__ldg(src + c * hw), s_x, zp) : zero_code<T>();
         T *dst = out + ((size_t)row * W + w) * c_pad;
         if (c_pad == 4) {
             store4<T>(dst, v);
@@ -183,12 +208,12 @@ __global__ void __launch_bounds__(kPackSmallThreads) pack_nhwc_small_kernel(cons
 
 template <typename T>
 __global__ void pack_nchw_kernel(const float *__restrict__ x, T *__restrict__ out, size_t count,
-                                 float s_x) {
+                                 float s_x, int zp) {
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count;
          i += (size_t)gridDim.x * blockDim.x)
-        out[i] = convert_out<T>(x[i], s_x);
+        out[i] = convert_out<T>(x[i], s_x, zp);
 }
 
 // ------------------------------------------------------------------- glue
@@ -269,27 +294,27 @@ cudaError_t launch_fold(const FoldLaunch &L, cudaStream_t s) {
 }
 
 cudaError_t launch_pack_input(const float *x, void *out, int N, int C, int H, int W, int c_pad,
-                              int to_nhwc, int dtype, float s_x, cudaStream_t s) {
+                              int to_nhwc, int dtype, float s_x, int zp, cudaStream_t s) {
     if (to_nhwc && c_pad <= 8) {
         const int gx = (W + kPackSmallThreads - 1) / kPackSmallThreads;
         const int rows = N * H;
         int gy = kNumSMs * 32 / gx;
         gy = gy < 1 ? 1 : (gy > rows ? rows : (gy > 65535 ? 65535 : gy));
         const dim3 grid(gx, gy);
-        if (dtype == 0) launch_kernel(pack_nhwc_small_kernel<float>, grid, kPackSmallThreads, 0, s, x, (float *)out, C, H, W, rows, c_pad, s_x);
-        else if (dtype == 1) launch_kernel(pack_nhwc_small_kernel<__nv_bfloat16>, grid, kPackSmallThreads, 0, s, x, (__nv_bfloat16 *)out, C, H, W, rows, c_pad, s_x);
-        else launch_kernel(pack_nhwc_small_kernel<int8_t>, grid, kPackSmallThreads, 0, s, x, (int8_t *)out, C, H, W, rows, c_pad, s_x);
+        if (dtype == 0) launch_kernel(pack_nhwc_small_kernel<float>, grid, kPackSmallThreads, 0, s, x, (float *)out, C, H, W, rows, c_pad, s_x, zp);
+        else if (dtype == 1) launch_kernel(pack_nhwc_small_kernel<__nv_bfloat16>, grid, kPackSmallThreads, 0, s, x, (__nv_bfloat16 *)out, C, H, W, rows, c_pad, s_x, zp);
+        else launch_kernel(pack_nhwc_small_kernel<int8_t>, grid, kPackSmallThreads, 0, s, x, (int8_t *)out, C, H, W, rows, c_pad, s_x, zp);
     } else if (to_nhwc) {
         dim3 grid((W + 31) / 32, (c_pad + 31) / 32, N * H), block(32, 8);
-        if (dtype == 0) launch_kernel(pack_nhwc_kernel<float>, grid, block, 0, s, x, (float *)out, C, H, W, c_pad, s_x);
-        else if (dtype == 1) launch_kernel(pack_nhwc_kernel<__nv_bfloat16>, grid, block, 0, s, x, (__nv_bfloat16 *)out, C, H, W, c_pad, s_x);
-        else launch_kernel(pack_nhwc_kernel<int8_t>, grid, block, 0, s, x, (int8_t *)out, C, H, W, c_pad, s_x);
+        if (dtype == 0) launch_kernel(pack_nhwc_kernel<float>, grid, block, 0, s, x, (float *)out, C, H, W, c_pad, s_x, zp);
+        else if (dtype == 1) launch_kernel(pack_nhwc_kernel<__nv_bfloat16>, grid, block, 0, s, x, (__nv_bfloat16 *)out, C, H, W, c_pad, s_x, zp);
+        else launch_kernel(pack_nhwc_kernel<int8_t>, grid, block, 0, s, x, (int8_t *)out, C, H, W, c_pad, s_x, zp);
     } else {
         const size_t count = (size_t)N * C * H * W;
         const int g = grid_for(count, 256);
-        if (dtype == 0) launch_kernel(pack_nchw_kernel<float>, g, 256, 0, s, x, (float *)out, count, s_x);
-        else if (dtype == 1) launch_kernel(pack_nchw_kernel<__nv_bfloat16>, g, 256, 0, s, x, (__nv_bfloat16 *)out, count, s_x);
-        else launch_kernel(pack_nchw_kernel<int8_t>, g, 256, 0, s, x, (int8_t *)out, count, s_x);
+        if (dtype == 0) launch_kernel(pack_nchw_kernel<float>, g, 256, 0, s, x, (float *)out, count, s_x, zp);
+        else if (dtype == 1) launch_kernel(pack_nchw_kernel<__nv_bfloat16>, g, 256, 0, s, x, (__nv_bfloat16 *)out, count, s_x, zp);
+        else launch_kernel(pack_nchw_kernel<int8_t>, g, 256, 0, s, x, (int8_t *)out, count, s_x, zp);
     }
     return cudaGetLastError();
 }

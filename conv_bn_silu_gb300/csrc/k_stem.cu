@@ -162,9 +162,13 @@ __global__ void __launch_bounds__(256) stem_kernel(const StemLaunch a) {
                 const int ih = oh[j] * a.stride - a.pad + r;
                 const int iw = ow[j] * a.stride - a.pad + s;
                 const bool in = live[j] && ih >= 0 && ih < a.H && iw >= 0 && iw < a.W;
+                // Outside the image the input is a real zero: code 0, or for
+                // INT8 the code of zero, z_x.  (With an input zero point the
+                // fold's bias is bias_i32 - z_x * sum(q_w), so every tap then
+                // contributes (q - z_x) * q_w, inside the image or not.)
                 Tin xv[4];
 #pragma unroll
-                for (int ci = 0; ci < 4; ++ci) xv[ci] = Tin(0);
+                for (int ci = 0; ci < 4; ++ci) xv[ci] = KIND == 2 ? Tin(a.zp_x) : Tin(0);
                 if (in) {
                     if (vec_in) {
                         const Tin *src = x + (((size_t)img[j] * a.H + ih) * a.W + iw) * 4;
@@ -238,7 +242,9 @@ __global__ void __launch_bounds__(256) stem_kernel(const StemLaunch a) {
 #pragma unroll
         for (int c = 0; c < COUT; ++c) {
             if (KIND == 2)
-                oq[c] = c < a.Cout ? requant_i8(__float2int_rn(accf[j][c]) + bias_i[c], mc[c], a.inv_s_y) : 0;
+                oq[c] = c < a.Cout ? requant_i8((int)((unsigned)__float2int_rn(accf[j][c]) + (unsigned)bias_i[c]),
+                                                mc[c], a.inv_s_y, a.zp_y)
+                                   : 0;
             else
                 of[c] = a.act == CBS_ACT_IDENTITY ? accf[j][c] + bias_f[c] : silu_fast(accf[j][c] + bias_f[c]);
         }

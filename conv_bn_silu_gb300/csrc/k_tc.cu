@@ -111,6 +111,13 @@ struct TcParams {
     // input (tensor map A), the rest from the second (tensor map A2, block
     // cb - ca_blocks).  ca_blocks = cblocks with one input.
     int ca_blocks;
+    // INT8 zero points (asymmetric activations).  Outside the image the
+    // input is a real zero, code zp_x: the converters write that code for
+    // the taps of a pixel's window that leave the image (TMA fills 0), and
+    // the fold's bias carries -zp_x * sum(q_w), so every tap contributes
+    // (q - zp_x) * q_w.
+    int zp_x, zp_y;
+    int in_h, in_w;
 };
 
 constexpr int kStageBlockBytes = 4096;            // one warp's staged store block: 32 rows x 128 B
@@ -945,9 +952,32 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // of every staging tile into the swizzled bf16 operand.
         const int row = (warp - kConvFirstI8) * 32 + lane;
         const int in_bytes = p.CB;
+        // With an input zero point: the code of a real zero, as a bf16 pair.
+        const uint32_t zcode = p.zp_x ? pack_bf16x2((uint32_t)(p.zp_x + 128), (uint32_t)(p.zp_x + 128)) : 0u;
         int g = 0;
         for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
             bool ok = true;
+            // With a zero point: bit tap of `oob` marks a tap of this row's
+            // pixel window outside the image (k <= 5: at most 25 taps; larger
+            // filters test each tap as it comes).
+            int ih0 = 0, iw0 = 0;
+            uint32_t oob = 0u;
+            if (p.zp_x) {
+                int m0, n0;
+                tile_coords(t, p.n_tiles, kBM, m0, n0, p.BN);
+                const int m = m0 + row < p.M ? m0 + row : m0;
+                const int img = m / p.OHW;
+                const int rem = m - img * p.OHW;
+                const int oh = rem / p.OW;
+                ih0 = oh * p.stride - p.pad;
+                iw0 = (rem - oh * p.OW) * p.stride - p.pad;
+                if (p.ks <= 5)
+                    for (int r = 0; r < p.ks; ++r)
+                        for (int c2 = 0; c2 < p.ks; ++c2)
+                            if ((unsigned)(ih0 + r) >= (unsigned)p.in_h || (unsigned)(iw0 + c2) >= (unsigned)p.in_w)
+                                oob |= 1u << (r * p.ks + c2);
+            }
+            int tap = 0, cbk = 0;   // tap and channel block of the next K step
             for (int st = 0; st < nstage; ++st, ++g) {
                 const int s = g % S, u = g / S;
                 if (!ptx::mbar_wait_bounded(raw_bar(s), u & 1, kWaitLimitNs)) {
@@ -959,6 +989,28 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 for (int kk = 0; kk < kg; ++kk) {
                 const uint32_t src_row = sb + stg_off + kk * stg_stride + row * in_bytes;
                 const uint32_t dst_row = sb + kk * p.a_bytes + row * p.RB;
+                const int ktap = tap;
+                if (++cbk == p.cblocks) {
+                    cbk = 0;
+                    ++tap;
+                }
+                if (p.zp_x) {
+                    bool out;
+                    if (p.ks <= 5) {
+                        out = (oob >> ktap) & 1u;
+                    } else {
+                        const int r = ktap / p.ks, c2 = ktap - r * p.ks;
+                        out = (unsigned)(ih0 + r) >= (unsigned)p.in_h || (unsigned)(iw0 + c2) >= (unsigned)p.in_w;
+                    }
+                    if (out) {
+                        // A tap outside the image: every channel is the code of zero.
+                        for (int c = 0; c < in_bytes; c += 8)
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(swz(dst_row + 2 * c, p.op_mask)),
+                                         "r"(zcode)
+                                         : "memory");
+                        continue;
+                    }
+                }
                 for (int c = 0; c < in_bytes; c += 16) {
                     uint32_t w0, w1, w2, w3;
                     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -1029,7 +1081,7 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
                     const int qv = requant_i8(accv[jj], nbase + jj < p.C_out ? __ldg(p.m_c + nbase + jj) : 0.0f,
-                                              p.inv_s_y);
+                                              p.inv_s_y, p.zp_y);
                     qw[jj >> 2] |= (uint32_t)(uint8_t)(int8_t)qv << (8 * (jj & 3));
                 }
                 if (p.out_nhwc) {
@@ -1555,6 +1607,10 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
         P.bias_i32 = static_cast<const int32_t *>(bias);
         P.m_c = m_c;
         P.inv_s_y = inv_s_y;
+        P.zp_x = d.zero_point_x;
+        P.zp_y = d.zero_point_y;
+        P.in_h = d.h;
+        P.in_w = d.w;
     } else {
         P.nchunks = 1;
         P.bias = static_cast<const float *>(bias);

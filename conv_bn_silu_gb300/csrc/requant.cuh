@@ -27,14 +27,16 @@ static __device__ __forceinline__ float cw_exp(float x) {
     return __fmul_rn(p, __int_as_float((k + 127) << 23));
 }
 
-// q = rne(clamp(SiLU(float(acc) * m_c) * inv_s_y, -128, 127)), IEEE steps.
-static __device__ __forceinline__ int requant_i8(int acc, float m_c, float inv_s_y) {
+// q = clamp(rne(SiLU(float(acc) * m_c) * inv_s_y) + z_y, -128, 127), IEEE
+// steps.  With z_y = 0 this is rne(clamp(v, -128, 127)): the bounds are
+// integers, so rounding and clamping commute.
+static __device__ __forceinline__ int requant_i8(int acc, float m_c, float inv_s_y, int z_y = 0) {
     const float t = __fmul_rn(__int2float_rn(acc), m_c);
     const float e = cw_exp(-t);
     const float u = __fdiv_rn(t, __fadd_rn(1.0f, e));
-    float v = __fmul_rn(u, inv_s_y);
+    float v = __fadd_rn(rintf(__fmul_rn(u, inv_s_y)), (float)z_y);
     v = fminf(fmaxf(v, -128.0f), 127.0f);
-    return (int)rintf(v);
+    return (int)v;
 }
 
 }  // namespace cbs

@@ -22,7 +22,8 @@ def current_stream() -> int:
 def make_desc(n, c_in, h, w, c_out, k, stride, pad=None, prec=B.CBS_FP32, in_layout=None,
               out_layout=None, force_variant=-1, force_split_k=0, force_block_n=0,
               force_block_m=0, out_row_stride=0, force_k_group=0, force_b_resident=0,
-              force_window=0, activation=B.CBS_ACT_SILU, residual=0, c_in_b=0) -> B.cbs_layer_desc:
+              force_window=0, activation=B.CBS_ACT_SILU, residual=0, c_in_b=0, zero_point_x=0,
+              zero_point_y=0) -> B.cbs_layer_desc:
     if pad is None:
         pad = k // 2
     if in_layout is None:
@@ -36,7 +37,8 @@ def make_desc(n, c_in, h, w, c_out, k, stride, pad=None, prec=B.CBS_FP32, in_lay
                         force_block_n=force_block_n, force_block_m=force_block_m,
                         out_row_stride=out_row_stride, force_k_group=force_k_group,
                         force_b_resident=force_b_resident, force_window=force_window,
-                        activation=activation, residual=residual, c_in_b=c_in_b).items():
+                        activation=activation, residual=residual, c_in_b=c_in_b, zero_point_x=zero_point_x,
+                        zero_point_y=zero_point_y).items():
         setattr(d, name, int(v))
     return d
 

@@ -111,6 +111,11 @@ typedef struct cbs_layer_desc {
                             FP32 (CUDA-core variant), TF32 and BF16; the tensor-core variants
                             need c_in - c_in_b to be a multiple of 16 (BF16) or 8 (TF32) channels
                             and c_in_b a multiple of 8 (BF16) or 4 (TF32). */
+    int zero_point_x;    /* INT8: zero point z_x in [-128, 127] of the input codes (asymmetric
+                            activations, page 3 "Design notes": a code q stands for s_x (q - z_x);
+                            a uint8 code u with zero point z_u is q = u - 128, z_x = z_u - 128).
+                            0 = symmetric.  Must be 0 for the other precisions. */
+    int zero_point_y;    /* INT8: zero point z_y in [-128, 127] of the output codes. */
 } cbs_layer_desc;
 
 /* A plan: plain data, owned by the caller, filled by cbs_plan. */
@@ -177,7 +182,10 @@ CBS_API cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out);
  *   BF16:      bf16   [C_out][k*k*c_in_pad]   (round to nearest even)
  *   INT8:      int8 codes held exactly as bf16 [C_out][k*k*c_in_pad];
  *              s_w[c] = max|w'[c,:]| / 127, q = rne(w'/s_w), m_c[c] = s_x * s_w[c],
- *              bias_i32[c] = rne(b'[c] / m_c[c]) saturated.
+ *              bias_i32[c] = rne(b'[c] / m_c[c]) saturated.  With an input zero
+ *              point z_x != 0 the bias written is bias_i32[c] - z_x * sum q[c, :]
+ *              (two's-complement int32): the kernels read the code z_x (a real
+ *              zero) for every tap outside the image.
  * Arguments (device): w_oihw float[C_out*C_in*k*k]; conv_bias float[C_out] or
  * NULL; gamma, beta, mean, var float[C_out]; eps > 0.  s_x: activation scale
  * (INT8 only, else ignored).  Outputs: w_packed (plan->w_packed_bytes), bias
@@ -196,7 +204,8 @@ CBS_API cbs_status cbs_fold_bn(const cbs_plan_t *p, const float *w_oihw, const f
  * x_nchw: float [N][C_in][H][W].  x_packed: the plan's input format
  * (plan->x_bytes): SIMT with NCHW input: a copy; SIMT with NHWC input: float
  * NHWC; TF32: float NHWC padded to c_in_pad with zeros; BF16: bf16 (RNE);
- * INT8: int8 q = rne(clamp(x / s_x, -128, 127)).  Two-input plans:
+ * INT8: int8 q = clamp(rne(x / s_x) + z_x, -128, 127) with the plan's zero
+ * point z_x (0: symmetric); padding channels hold code 0.  Two-input plans:
  * CBS_ERR_UNSUPPORTED (each input is an earlier layer's output, or is packed
  * with a one-input plan of its own channel count).
  */
@@ -248,11 +257,14 @@ CBS_API cbs_status cbs_conv_bn_act_cat(const cbs_plan_t *p, const void *x, const
 /*
  * cbs_conv_bn_silu_i8 -- the fused INT8 layer (page 3, "Highlights" and
  * "Design notes": per-output-channel weight scales, one activation scale).
- *   acc   = sum q_x * q_w + bias_i32         (exact integer)
+ *   acc   = sum over the taps inside the image of (q_x - z_x) * q_w
+ *           + bias_i32                        (exact integer; z_x = 0: symmetric)
  *   t     = float(acc) * m_c[co]
  *   u     = t / (1 + e(-t))                   (SiLU in float; e = the library's
  *                                              Cody-Waite/Taylor exp, bit-specified)
- *   q_y   = rne(clamp(u * (1/s_y), -128, 127))
+ *   q_y   = clamp(rne(u * (1/s_y)) + z_y, -128, 127)
+ * z_x, z_y: the plan's zero points.  w_packed and bias_i32 as written by
+ * cbs_fold_bn for this plan.
  * x: int8 NHWC with c_in_pad channels; y: int8 in d.out_layout.
  * Workspace rules as for cbs_conv_bn_silu_f32.
  */

@@ -227,3 +227,20 @@ def test_launch_options(cuda_lib):
         assert B.cbs_launch_options() == 0
     finally:
         B.cbs_set_launch_options(B.CBS_LAUNCH_PDL)
+
+
+def test_zero_point_plans(cuda_lib):
+    """INT8 zero points: range checks, INT8 only; the plan's buffers do not
+    change."""
+    sym = B.cbs_plan(make_desc(2, 32, 20, 20, 48, 3, 1, prec=B.CBS_INT8))
+    asym = B.cbs_plan(make_desc(2, 32, 20, 20, 48, 3, 1, prec=B.CBS_INT8, zero_point_x=-7, zero_point_y=100))
+    assert asym.w_packed_bytes == sym.w_packed_bytes == 48 * sym.k_gemm * 2
+    assert (asym.block_n, asym.stages, asym.k_group) == (sym.block_n, sym.stages, sym.k_group)
+    stem = B.cbs_plan(make_desc(1, 3, 64, 64, 16, 3, 2, prec=B.CBS_INT8, zero_point_x=12))
+    assert stem.variant == B.CBS_VARIANT_STEM
+    for kw, prec in ((dict(zero_point_x=128), B.CBS_INT8), (dict(zero_point_y=-129), B.CBS_INT8),
+                     (dict(zero_point_x=1), B.CBS_BF16), (dict(zero_point_y=1), B.CBS_FP32)):
+        lay = B.CBS_NCHW if prec == B.CBS_FP32 else B.CBS_NHWC
+        with pytest.raises(B.CbsError) as e:
+            B.cbs_plan(make_desc(1, 32, 20, 20, 48, 3, 1, prec=prec, in_layout=lay, **kw))
+        assert e.value.status == B.CBS_ERR_INVALID_ARG

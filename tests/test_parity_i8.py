@@ -161,3 +161,42 @@ def test_saturation_and_underflow(cuda_lib, s_y):
 
 def test_no_timeout_reported(cuda_lib):
     assert B.cbs_read_device_status(True, torch.cuda.current_stream().cuda_stream) == B.CBS_OK
+
+
+@pytest.mark.parametrize("shape,z", [
+    ((2, 3, 16, 3, 2, 34), (-61, 17)),       # stem (direct kernel), pixel windows leave the image at every edge
+    ((1, 4, 32, 7, 2, 23), (90, -128)),      # 7x7 stem: many out-of-image taps
+    ((2, 16, 32, 3, 2, 21), (-128, 127)),    # tensor cores, stride 2, ragged pixel tiles
+    ((1, 32, 48, 3, 1, 9), (45, -100)),      # small image: most windows touch a border
+    ((2, 48, 64, 1, 1, 11), (-20, 3)),       # 1x1: no padding, only the zero point itself
+    ((1, 64, 32, 5, 1, 13), (127, 0)),       # 5x5, output symmetric
+])
+def test_asymmetric_zero_points(cuda_lib, shape, z):
+    """Asymmetric activations (input and output zero points) bit for bit
+    against the oracle: the quantiser, the fold's bias, and the layer, for
+    the direct small-channel kernel and the tensor-core kernel."""
+    n, c_in, c_out, k, stride, h = shape
+    z_x, z_y = z
+    spec = wl.LayerSpec(c_in, c_out, k, stride, h)
+    x, p = wl.layer_inputs(spec, n, layer_index=13)
+    x = (x / (1 + np.exp(-x)) * 3).astype(np.float32)   # mostly positive, like activations after SiLU
+    y32 = oracle.conv_bn_silu_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, stride, spec.pad)
+    s_y = float(np.float32(np.abs(y32).max() / 200))
+    desc = make_desc(n, c_in, h, h, c_out, k, stride, spec.pad, prec=B.CBS_INT8, in_layout=B.CBS_NHWC,
+                     out_layout=B.CBS_NHWC, zero_point_x=z_x, zero_point_y=z_y)
+    layer = FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, s_x=S_X)
+    qx = layer.pack_input(torch.from_numpy(x).cuda())
+    y = nhwc_to_nchw(layer(qx, s_y=s_y).cpu().numpy())
+    q_x = oracle.quantize_act(x, S_X, z_x)
+    q_w, bias, m_c = oracle.fold_quant_i8(p.w, p.gamma, p.beta, p.mean, p.var, p.eps, S_X)
+    want = oracle.conv_i8(q_x, q_w, bias, m_c, s_y, stride, spec.pad, z_x=z_x, z_y=z_y)
+    c_pad = layer.plan.c_in_pad
+    qg = qx.cpu().numpy().reshape(n, h, h, c_pad)
+    assert np.array_equal(nhwc_to_nchw(qg[..., :c_in]), q_x) and np.all(qg[..., c_in:] == 0)
+    qsum = q_w.astype(np.int64).reshape(c_out, -1).sum(axis=1)
+    want_bias = ((bias.astype(np.int64) - z_x * qsum + 2**31) % 2**32 - 2**31).astype(np.int32)
+    assert np.array_equal(layer.bias.view(torch.int32).cpu().numpy(), want_bias)
+    mism = int(np.count_nonzero(y != want))
+    assert mism == 0, (layer.plan.variant, mism, y.size)
+    if abs(z_y) < 100:   # (an output zero point at an end of the code range saturates half the outputs)
+        assert len(np.unique(y)) > 20
