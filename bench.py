@@ -365,6 +365,21 @@ def measure(name, steps, warmup, device, peaks, sample_clocks=False):
     return out, w, clocks
 
 
+def max_over_ranks(ms_step: float, device) -> float:
+    """The job's step time: the slowest replica's (all_reduce MAX over the
+    process group; NCCL on the GPUs, gloo in the CPU tests)."""
+    import torch
+    t = torch.tensor([ms_step], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_step: float, world: int, ms_step: float) -> float:
+    """Whole-job throughput: every replica runs the same step (weak scaling),
+    so the job does world x flops_step in the slowest replica's time."""
+    return flops_step * world / (ms_step * 1e-3) / 1e12
+
+
 def run_ours(args, rank: int, world: int):
     import torch
     device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
@@ -379,12 +394,10 @@ def run_ours(args, rank: int, world: int):
         torch.distributed.barrier()
     ms_step = head["ms_per_step"]
     if world > 1:
-        t = torch.tensor([ms_step], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+        ms_step = max_over_ranks(ms_step, device)
     n = w.n
     flops_step = sum(sp.flops(n) for sp in w.specs)
-    value = flops_step * world / (ms_step * 1e-3) / 1e12
+    value = job_tflops(flops_step, world, ms_step)
     rows = head["layers"]
     peak = head["peak_tflops"]
     kernel = {"fp32": "simt_conv_kernel (FP32 FMA)", "tf32": "tc_conv_kernel<TF32>",
