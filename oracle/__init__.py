@@ -11,6 +11,7 @@ from .oracle import (  # noqa: F401
     silu,
     conv_bn_silu_f32,
     conv_bn_act_f32,
+    maxpool2d_f32,
     spec_exp,
     quantize_act,
     fold_quant_i8,

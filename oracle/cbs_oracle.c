@@ -145,6 +145,41 @@ ORACLE_API void oracle_conv_bn_act_f32(const float *x, const float *w, const flo
 }
 
 /* ---------------------------------------------------------------------- */
+/* Glue beside the convolutions: max pooling.                              */
+/* ---------------------------------------------------------------------- */
+
+/* 2-D max pooling ("YOLO26N Inference Optimisation", kernel profile and "Op-by-op
+ * impact": maxpool2d, three per frame): y[n,c,oh,ow] = max over the k x k
+ * window at (oh*S-P, ow*S-P) of the positions inside the image (padding
+ * takes no part); OH = (H + 2P - k)/S + 1 (floor).  A NaN in the window
+ * gives NaN.  x, y: NCHW float. */
+ORACLE_API void oracle_maxpool2d_f32(const float *x, int N, int C, int H, int W, int k, int stride, int pad,
+                                     float *y)
+{
+    const int OH = oracle_out_dim(H, k, stride, pad);
+    const int OW = oracle_out_dim(W, k, stride, pad);
+    for (int n = 0; n < N; ++n)
+        for (int c = 0; c < C; ++c)
+            for (int oh = 0; oh < OH; ++oh)
+                for (int ow = 0; ow < OW; ++ow) {
+                    float m = -INFINITY;
+                    int nan = 0;
+                    for (int r = 0; r < k; ++r) {
+                        const int ih = oh * stride - pad + r;
+                        if (ih < 0 || ih >= H) continue;
+                        for (int s = 0; s < k; ++s) {
+                            const int iw = ow * stride - pad + s;
+                            if (iw < 0 || iw >= W) continue;
+                            const float v = x[(((size_t)n * C + c) * H + ih) * W + iw];
+                            if (v != v) nan = 1;
+                            else if (v > m) m = v;
+                        }
+                    }
+                    y[(((size_t)n * C + c) * OH + oh) * OW + ow] = nan ? NAN : m;
+                }
+}
+
+/* ---------------------------------------------------------------------- */
 /* INT8 path.                                                              */
 /* ---------------------------------------------------------------------- */
 

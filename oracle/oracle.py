@@ -42,6 +42,7 @@ def _load():
         lib.oracle_requant.restype = ctypes.c_int8
         lib.oracle_conv_i8.argtypes = [P, P, P, P, F, I, I, I, I, I, I, I, I, P, P]
         lib.oracle_conv_i8.restype = I
+        lib.oracle_maxpool2d_f32.argtypes = [P, I, I, I, I, I, I, I, P]
         lib.oracle_quantize_act_zp.argtypes = [P, Z, F, I, P]
         lib.oracle_requant_zp.argtypes = [ctypes.c_int32, F, F, I]
         lib.oracle_requant_zp.restype = ctypes.c_int8
@@ -133,6 +134,16 @@ def conv_bn_act_f32(x, w, gamma, beta, mean, var, eps: float, stride: int, pad: 
     _load().oracle_conv_bn_act_f32(_ptr(x), _ptr(w), _ptr(cb), _ptr(g), _ptr(b), _ptr(m), _ptr(v), eps, N,
                                    C_in, H, W, C_out, k, stride, pad, int(act), _ptr(r), _ptr(work), _ptr(y))
     return (y, work) if return_f64 else y
+
+
+def maxpool2d_f32(x, k: int, stride: int, pad: int) -> np.ndarray:
+    """Max pooling of an NCHW float32 array; padding takes no part, floor
+    output size, NaN propagates."""
+    x = _f32(x)
+    N, C, H, W = x.shape
+    y = np.empty((N, C, out_dim(H, k, stride, pad), out_dim(W, k, stride, pad)), np.float32)
+    _load().oracle_maxpool2d_f32(_ptr(x), N, C, H, W, k, stride, pad, _ptr(y))
+    return y
 
 
 def spec_exp(x) -> np.ndarray:

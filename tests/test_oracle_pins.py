@@ -480,3 +480,22 @@ def test_asymmetric_int8_layer_tracks_fp32_layer():
     q_y = oracle.conv_i8(q_x, q_w, bias, m_c, s_y, 1, 1, z_x=z_x, z_y=z_y)
     err = np.abs((q_y.astype(np.float64) - z_y) * s_y - y32)
     assert err.mean() < 1.0 * s_y and err.max() < 6 * s_y
+
+
+# ------------------------------------------------------------ max pooling glue
+
+@pytest.mark.parametrize("k,stride,pad,hw", [(5, 1, 2, (13, 17)), (3, 2, 1, (12, 9)), (2, 2, 0, (8, 10)),
+                                             (3, 1, 0, (5, 5)), (5, 1, 2, (1, 1))])
+def test_maxpool_vs_torch(k, stride, pad, hw):
+    """Against PyTorch's max_pool2d (padding takes no part, floor size)."""
+    x = rng(50 + k).standard_normal((2, 5) + hw).astype(np.float32)
+    got = oracle.maxpool2d_f32(x, k, stride, pad)
+    want = torch.nn.functional.max_pool2d(torch.from_numpy(x), k, stride, pad).numpy()
+    assert got.shape == want.shape and np.array_equal(got, want)
+
+
+def test_maxpool_padding_takes_no_part_and_nan_propagates():
+    x = -np.ones((1, 1, 3, 3), np.float32) * 5      # all negative: a zero-padded window would give 0
+    assert np.all(oracle.maxpool2d_f32(x, 3, 1, 1) == -5)
+    x[0, 0, 1, 1] = np.nan
+    assert np.isnan(oracle.maxpool2d_f32(x, 3, 1, 1)).all()
