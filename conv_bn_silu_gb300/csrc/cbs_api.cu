@@ -506,6 +506,22 @@ cbs_status cbs_conv_bn_silu_i8(const cbs_plan_t *p, const int8_t *x, const void 
     return launch_tc(*p, x, nullptr, w_packed, bias_i32, m_c, inv_s_y, nullptr, y, workspace, (cudaStream_t)stream);
 }
 
+cbs_status cbs_maxpool2d(const void *x, void *y, int n, int c, int h, int w, int k, int stride, int pad,
+                         int layout, int prec, void *stream) {
+    CBS_TRY(check_ptr(x, "x"));
+    CBS_TRY(check_ptr(y, "y"));
+    if (n < 0 || c < 1 || h < 1 || w < 1 || k < 1 || stride < 1 || pad < 0 || 2 * pad > k || h + 2 * pad < k ||
+        w + 2 * pad < k)
+        return fail(CBS_ERR_INVALID_ARG, "bad max-pool shape (n=%d c=%d h=%d w=%d k=%d stride=%d pad=%d; pad <= k/2)",
+                    n, c, h, w, k, stride, pad);
+    if (layout != CBS_NCHW && layout != CBS_NHWC) return fail(CBS_ERR_INVALID_ARG, "unknown layout %d", layout);
+    if (prec < CBS_FP32 || prec > CBS_INT8) return fail(CBS_ERR_INVALID_ARG, "unknown precision %d", prec);
+    if (n == 0) return CBS_OK;
+    const int eb = prec == CBS_BF16 ? 2 : (prec == CBS_INT8 ? 1 : 4);
+    return cuda_check(launch_maxpool(x, y, n, c, h, w, k, stride, pad, layout == CBS_NHWC, eb, (cudaStream_t)stream),
+                      "max-pool launch");
+}
+
 cbs_status cbs_upsample2x_concat(const void *a, int ca, const void *b, int cb, void *out, int n, int h,
                                  int w, int layout, int elem_bytes, void *stream) {
     CBS_TRY(check_ptr(a, "a"));

@@ -152,6 +152,9 @@ cudaError_t launch_upsample_concat(const void *a, int ca, const void *b, int cb,
                                    int n, int h, int w, int nhwc, int elem_bytes,
                                    cudaStream_t s);
 
+cudaError_t launch_maxpool(const void *x, void *y, int n, int c, int h, int w, int k, int stride, int pad, int nhwc,
+                           int elem_bytes, cudaStream_t s);
+
 // Device-side status word (bounded waits that expired set it).
 unsigned int *device_status_word();  // device address for the current device, or nullptr
 cbs_status read_and_reset_status(int *status_out, int reset, cudaStream_t s);

@@ -276,6 +276,71 @@ __global__ void upcat_elem_kernel(const T *__restrict__ a, int ca, const T *__re
     }
 }
 
+// 2-D max pooling ("YOLO26N Inference Optimisation": maxpool2d, three per
+// frame in SPPF): the window's positions inside the image only, floor output
+// size, a NaN in the window gives NaN.  One thread per output element in the
+// tensor's own order, so NHWC reads of a window position are coalesced over
+// channels.  int8 codes compare like their values (the scale is positive).
+template <typename T>
+__device__ __forceinline__ bool pool_is_nan(T v) { return false; }
+template <>
+__device__ __forceinline__ bool pool_is_nan<float>(float v) { return v != v; }
+template <>
+__device__ __forceinline__ bool pool_is_nan<__nv_bfloat16>(__nv_bfloat16 v) {
+    return (__bfloat16_as_ushort(v) & 0x7fffu) > 0x7f80u;
+}
+template <typename T>
+__device__ __forceinline__ bool pool_greater(T a, T b) { return a > b; }
+template <>
+__device__ __forceinline__ bool pool_greater<__nv_bfloat16>(__nv_bfloat16 a, __nv_bfloat16 b) {
+    return __bfloat162float(a) > __bfloat162float(b);
+}
+
+template <typename T>
+__global__ void maxpool_kernel(const T *__restrict__ x, T *__restrict__ y, int N, int C, int H, int W, int OH,
+                               int OW, int k, int stride, int pad, int nhwc) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+    const size_t total = (size_t)N * C * OH * OW;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        int n, c, oh, ow;
+        if (nhwc) {
+            c = (int)(i % C);
+            size_t r = i / C;
+            ow = (int)(r % OW);
+            r /= OW;
+            oh = (int)(r % OH);
+            n = (int)(r / OH);
+        } else {
+            ow = (int)(i % OW);
+            size_t r = i / OW;
+            oh = (int)(r % OH);
+            r /= OH;
+            c = (int)(r % C);
+            n = (int)(r / C);
+        }
+        T m = T(0), nanv = T(0);
+        bool any = false, nan = false;
+        for (int r = 0; r < k; ++r) {
+            const int ih = oh * stride - pad + r;
+            if (ih < 0 || ih >= H) continue;
+            for (int s = 0; s < k; ++s) {
+                const int iw = ow * stride - pad + s;
+                if (iw < 0 || iw >= W) continue;
+                const T v = nhwc ? x[(((size_t)n * H + ih) * W + iw) * C + c] : x[(((size_t)n * C + c) * H + ih) * W + iw];
+                if (pool_is_nan<T>(v)) {
+                    nan = true;
+                    nanv = v;
+                } else if (!any || pool_greater<T>(v, m)) {
+                    m = v;
+                    any = true;
+                }
+            }
+        }
+        y[i] = nan ? nanv : m;
+    }
+}
+
 __device__ unsigned int g_cbs_status_word;
 
 int grid_for(size_t count, int threads) {
@@ -336,6 +401,20 @@ cudaError_t launch_upsample_concat(const void *a, int ca, const void *b, int cb,
         else launch_kernel(upcat_elem_kernel<uint8_t>, g, 256, 0, s, (const uint8_t *)a, ca, (const uint8_t *)b, cb, (uint8_t *)out, n, h, w, nhwc);
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_maxpool(const void *x, void *y, int n, int c, int h, int w, int k, int stride, int pad, int nhwc,
+                           int eb, cudaStream_t s) {
+    const int oh = (h + 2 * pad - k) / stride + 1, ow = (w + 2 * pad - k) / stride + 1;
+    const int g = grid_for((size_t)n * c * oh * ow, 256);
+    if (eb == 4)
+        return launch_kernel(maxpool_kernel<float>, g, 256, 0, s, (const float *)x, (float *)y, n, c, h, w, oh, ow, k,
+                             stride, pad, nhwc);
+    if (eb == 2)
+        return launch_kernel(maxpool_kernel<__nv_bfloat16>, g, 256, 0, s, (const __nv_bfloat16 *)x, (__nv_bfloat16 *)y,
+                             n, c, h, w, oh, ow, k, stride, pad, nhwc);
+    return launch_kernel(maxpool_kernel<int8_t>, g, 256, 0, s, (const int8_t *)x, (int8_t *)y, n, c, h, w, oh, ow, k,
+                         stride, pad, nhwc);
 }
 
 unsigned int *device_status_word() {

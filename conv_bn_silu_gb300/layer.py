@@ -158,6 +158,22 @@ class FusedConvBnSilu:
         return y
 
 
+_PREC_OF_DTYPE = {torch.float32: B.CBS_FP32, torch.bfloat16: B.CBS_BF16, torch.int8: B.CBS_INT8}
+
+
+def maxpool2d(x: torch.Tensor, k: int, stride: int, pad: int, layout: int, out: torch.Tensor | None = None):
+    """Max pooling (the SPPF glue), in the given layout (kernel)."""
+    if layout == B.CBS_NHWC:
+        n, h, w, c = x.shape
+    else:
+        n, c, h, w = x.shape
+    oh, ow = (h + 2 * pad - k) // stride + 1, (w + 2 * pad - k) // stride + 1
+    shape = (n, oh, ow, c) if layout == B.CBS_NHWC else (n, c, oh, ow)
+    out = torch.empty(shape, dtype=x.dtype, device=x.device) if out is None else out
+    B.cbs_maxpool2d(x, out, n, c, h, w, k, stride, pad, layout, _PREC_OF_DTYPE[x.dtype], current_stream())
+    return out
+
+
 def upsample2x(a: torch.Tensor, layout: int, out: torch.Tensor | None = None):
     """Nearest 2x upsample (the glue in front of a two-input layer)."""
     if layout == B.CBS_NHWC:

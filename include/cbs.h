@@ -287,6 +287,21 @@ CBS_API cbs_status cbs_upsample2x_concat(const void *a, int ca, const void *b, i
                                  void *stream);
 
 /*
+ * cbs_maxpool2d -- max pooling beside the convolutions (page 1, "YOLO26N
+ * Inference Optimisation", kernel profile and "Op-by-op impact": maxpool2d,
+ * the SPPF block's 5x5 stride-1 pools):
+ *   y[n,c,oh,ow] = max of x over the k x k window at (oh*stride-pad,
+ *                  ow*stride-pad), positions outside the image taking no part
+ * OH = (h + 2 pad - k)/stride + 1 (floor), likewise OW; 0 <= pad <= k/2.  A
+ * NaN in the window gives NaN.  x: [n][c][h][w] (NCHW) or [n][h][w][c]
+ * (NHWC); y the same layout with OH x OW.  prec: the element type as for a
+ * layer (FP32/TF32 float, BF16 bfloat16, INT8 int8 codes, which compare like
+ * their values).  Errors: CBS_ERR_INVALID_ARG for shapes and enums.
+ */
+CBS_API cbs_status cbs_maxpool2d(const void *x, void *y, int n, int c, int h, int w, int k, int stride, int pad,
+                                 int layout, int prec, void *stream);
+
+/*
  * cbs_conv_bn_silu_f32_noalloc -- the FP32 CUDA-core fused layer for callers
  * that cannot allocate device memory.  No passage of the pages has a
  * counterpart: this is a deployment interface, not part of the method.

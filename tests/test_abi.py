@@ -244,3 +244,19 @@ def test_zero_point_plans(cuda_lib):
         with pytest.raises(B.CbsError) as e:
             B.cbs_plan(make_desc(1, 32, 20, 20, 48, 3, 1, prec=prec, in_layout=lay, **kw))
         assert e.value.status == B.CBS_ERR_INVALID_ARG
+
+
+def test_maxpool_argument_rules(cuda_lib):
+    ok = 1 << 20
+    for args in ((1, 8, 10, 10, 3, 1, 2), (1, 8, 10, 10, 0, 1, 0), (1, 8, 2, 2, 5, 1, 1), (1, 0, 10, 10, 3, 1, 1),
+                 (1, 8, 10, 10, 3, 0, 1)):
+        with pytest.raises(B.CbsError) as e:
+            B.cbs_maxpool2d(ok, ok, *args, B.CBS_NHWC, B.CBS_FP32, None)
+        assert e.value.status == B.CBS_ERR_INVALID_ARG, args
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_maxpool2d(ok, ok, 1, 8, 10, 10, 5, 1, 2, 7, B.CBS_FP32, None)
+    assert e.value.status == B.CBS_ERR_INVALID_ARG
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_maxpool2d(ok + 4, ok, 1, 8, 10, 10, 5, 1, 2, B.CBS_NHWC, B.CBS_FP32, None)
+    assert e.value.status == B.CBS_ERR_MISALIGNED
+    B.cbs_maxpool2d(ok, ok, 0, 8, 10, 10, 5, 1, 2, B.CBS_NHWC, B.CBS_FP32, None)   # empty batch: nothing enqueued

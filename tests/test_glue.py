@@ -83,3 +83,45 @@ def test_pack_input_nhwc_exact(cuda_lib, prec, c_in):
         assert np.array_equal(got.numpy(), q)
     else:
         assert torch.equal(got, xt)
+
+
+def _pool_ref(x_nchw_f32, k, stride, pad):
+    import oracle
+    return oracle.maxpool2d_f32(x_nchw_f32, k, stride, pad)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.int8])
+@pytest.mark.parametrize("layout", [B.CBS_NHWC, B.CBS_NCHW])
+@pytest.mark.parametrize("k,stride,pad,hw,c", [(5, 1, 2, (20, 20), 128), (3, 2, 1, (17, 13), 24), (2, 2, 0, (9, 11), 7),
+                                               (5, 1, 2, (1, 3), 16)])
+def test_maxpool(cuda_lib, dtype, layout, k, stride, pad, hw, c):
+    """Max pooling against the oracle, bit for bit (a max is exact)."""
+    from conv_bn_silu_gb300.layer import maxpool2d
+    g = torch.Generator().manual_seed(k * 100 + c)
+    x = torch.randn((2, c) + hw, generator=g) * 30
+    x = x.to(dtype) if dtype != torch.int8 else x.round().clamp(-128, 127).to(torch.int8)
+    want = _pool_ref(x.float().numpy(), k, stride, pad)
+    xd = x.cuda() if layout == B.CBS_NCHW else x.permute(0, 2, 3, 1).contiguous().cuda()
+    y = maxpool2d(xd, k, stride, pad, layout).cpu()
+    if layout == B.CBS_NHWC:
+        y = y.permute(0, 3, 1, 2)
+    assert np.array_equal(y.float().numpy(), want)
+
+
+def test_maxpool_sppf_chain_and_nan(cuda_lib):
+    """SPPF's three 5x5 stride-1 pools in sequence (NHWC bf16), and NaN
+    propagation (float)."""
+    from conv_bn_silu_gb300.layer import maxpool2d
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn((2, 256, 20, 20), generator=g).to(torch.bfloat16)
+    xd = x.permute(0, 2, 3, 1).contiguous().cuda()
+    ref = x.float().numpy()
+    for _ in range(3):
+        xd = maxpool2d(xd, 5, 1, 2, B.CBS_NHWC)
+        ref = _pool_ref(ref, 5, 1, 2)
+    assert np.array_equal(xd.permute(0, 3, 1, 2).float().cpu().numpy(), ref)
+    xf = torch.randn((1, 3, 6, 6), generator=g)
+    xf[0, 1, 2, 2] = float("nan")
+    y = maxpool2d(xf.cuda(), 3, 1, 1, B.CBS_NCHW).cpu().numpy()
+    want = _pool_ref(xf.numpy(), 3, 1, 1)
+    assert np.array_equal(np.isnan(y), np.isnan(want)) and np.array_equal(y[~np.isnan(y)], want[~np.isnan(want)])
