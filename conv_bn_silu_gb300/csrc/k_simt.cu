@@ -233,15 +233,27 @@ simt_conv_kernel(const SimtLaunch a) {
         if (!s_is_last) return;
         __threadfence();
         const float *base = a.partials + (size_t)tile_id * a.split * (BM * BN);
+        // The sum runs in split order.  Its loads go out eight splits at a
+        // time: one CTA reads every partial of the tile, so a load-add-load
+        // chain would pay the L2 latency once per split.
+        constexpr int kRedBatch = 8;
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
             for (int g = 0; g < CG; ++g) {
+                const float *src = base + row_of(i) * BN + col_of(g * 4);
                 float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int sidx = 0; sidx < a.split; ++sidx) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-                        base + (size_t)sidx * (BM * BN) + row_of(i) * BN + col_of(g * 4)));
-                    sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+                for (int s0 = 0; s0 < a.split; s0 += kRedBatch) {
+                    float4 v[kRedBatch];
+#pragma unroll
+                    for (int b = 0; b < kRedBatch; ++b)
+                        if (s0 + b < a.split)
+                            v[b] = __ldcg(reinterpret_cast<const float4 *>(src + (size_t)(s0 + b) * (BM * BN)));
+#pragma unroll
+                    for (int b = 0; b < kRedBatch; ++b)
+                        if (s0 + b < a.split) {
+                            sum.x += v[b].x; sum.y += v[b].y; sum.z += v[b].z; sum.w += v[b].w;
+                        }
                 }
                 acc[i][g * 4 + 0] = sum.x; acc[i][g * 4 + 1] = sum.y;
                 acc[i][g * 4 + 2] = sum.z; acc[i][g * 4 + 3] = sum.w;
