@@ -33,6 +33,7 @@ EXPORTED = (
     "cbs_upsample2x_concat", "cbs_workspace_init", "cbs_read_device_status", "cbs_status_string",
     "cbs_last_error", "cbs_abi_version", "cbs_conv_bn_silu_f32_noalloc", "cbs_conv_bn_act",
     "cbs_conv_bn_act_cat", "cbs_set_launch_options", "cbs_launch_options", "cbs_maxpool2d",
+    "cbs_conv_bn_silu_i8_cat",
 )
 
 
@@ -79,6 +80,7 @@ def lib():
         L.cbs_conv_bn_act.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P, P, Z, P]
         L.cbs_conv_bn_act_cat.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P, P, P, Z, P]
         L.cbs_conv_bn_silu_i8.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, F, P, P, Z, P]
+        L.cbs_conv_bn_silu_i8_cat.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P, F, P, P, Z, P]
         L.cbs_upsample2x_concat.argtypes = [P, I, P, I, P, I, I, I, I, I, P]
         L.cbs_maxpool2d.argtypes = [P, P, I, I, I, I, I, I, I, I, I, P]
         L.cbs_conv_bn_silu_f32_noalloc.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P]
@@ -157,6 +159,11 @@ def cbs_conv_bn_silu_f32(plan, x, w_packed, bias, y, workspace, workspace_bytes,
 def cbs_conv_bn_act(plan, x, w_packed, bias, residual, y, workspace, workspace_bytes, stream):
     _check(lib().cbs_conv_bn_act(ctypes.byref(plan), _p(x), _p(w_packed), _p(bias), _p(residual), _p(y),
                                  _p(workspace), workspace_bytes, stream), "cbs_conv_bn_act")
+
+
+def cbs_conv_bn_silu_i8_cat(plan, x, x_b, w_packed, bias_i32, m_c, s_y, y, workspace, workspace_bytes, stream):
+    _check(lib().cbs_conv_bn_silu_i8_cat(ctypes.byref(plan), _p(x), _p(x_b), _p(w_packed), _p(bias_i32), _p(m_c),
+                                         s_y, _p(y), _p(workspace), workspace_bytes, stream), "cbs_conv_bn_silu_i8_cat")
 
 
 def cbs_maxpool2d(x, y, n, c, h, w, k, stride, pad, layout, prec, stream):

@@ -223,8 +223,6 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
         return fail(CBS_ERR_UNSUPPORTED, "INT8: the specified requantising SiLU epilogue only");
     if (D.c_in_b < 0 || D.c_in_b >= D.c_in)
         return fail(CBS_ERR_INVALID_ARG, "c_in_b %d: 0 (one input) or 1..c_in-1 (c_in = %d)", D.c_in_b, D.c_in);
-    if (D.c_in_b > 0 && D.prec == CBS_INT8)
-        return fail(CBS_ERR_UNSUPPORTED, "INT8: two-input (channel concatenation) layers are not built");
     if (D.prec != CBS_INT8 && (D.zero_point_x || D.zero_point_y))
         return fail(CBS_ERR_INVALID_ARG, "zero points apply to INT8 plans only");
     if (D.zero_point_x < -128 || D.zero_point_x > 127 || D.zero_point_y < -128 || D.zero_point_y > 127)
@@ -274,10 +272,12 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
         if (D.in_layout != CBS_NHWC)
             return fail(CBS_ERR_UNSUPPORTED, "tensor-core variants read NHWC input (use cbs_pack_input)");
         p.c_in_pad = round_up(D.c_in, (int)(16 / eb));
-        if (D.c_in_b > 0 && (((size_t)(D.c_in - D.c_in_b) * eb) % 32 || ((size_t)D.c_in_b * eb) % 16))
+        // First input: whole channel blocks (32 bytes, INT8: 16 channels); second: TMA strides.
+        const size_t a_unit = D.prec == CBS_INT8 ? 16 : 32;
+        if (D.c_in_b > 0 && (((size_t)(D.c_in - D.c_in_b) * eb) % a_unit || ((size_t)D.c_in_b * eb) % 16))
             return fail(CBS_ERR_UNSUPPORTED,
-                        "two-input tensor-core layers need the first input's pixels to be a multiple of 32 bytes "
-                        "and the second's of 16 bytes (c_in %d, c_in_b %d)", D.c_in, D.c_in_b);
+                        "two-input tensor-core layers need the first input's pixels to be a multiple of %zu bytes "
+                        "and the second's of 16 bytes (c_in %d, c_in_b %d)", a_unit, D.c_in, D.c_in_b);
     }
     p.k_gemm = D.k * D.k * p.c_in_pad;
     p.x_bytes = (size_t)D.n * D.h * D.w * p.c_in_pad * eb;
@@ -487,23 +487,50 @@ cbs_status cbs_conv_bn_act_cat(const cbs_plan_t *p, const void *x, const void *x
     return conv_act_impl(p, x, x_b, w_packed, bias, residual, y, workspace, workspace_bytes, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// The INT8 layer, one or two inputs (checked against the plan by the caller).
+cbs_status conv_i8_impl(const cbs_plan_t *p, const int8_t *x, const int8_t *x_b, const void *w_packed,
+                        const int32_t *bias_i32, const float *m_c, float s_y, int8_t *y, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+    if (p->desc.n == 0) return CBS_OK;  // empty batch: nothing is read or written
+    CBS_TRY(check_conv_common(p, x, w_packed, bias_i32, y, workspace, workspace_bytes));
+    if (p->desc.c_in_b > 0) CBS_TRY(check_ptr(x_b, "x_b"));
+    CBS_TRY(check_ptr(m_c, "m_c"));
+    if (!(s_y > 0.0f) || !(s_y < 3.0e38f)) return fail(CBS_ERR_INVALID_ARG, "s_y must be a positive finite float");
+    const float inv_s_y = 1.0f / s_y;
+    if (p->variant == CBS_VARIANT_STEM) {
+        const StemLaunch L = stem_launch(*p, x, w_packed, bias_i32, m_c, inv_s_y, y);
+        return cuda_check(launch_stem(L, (cudaStream_t)stream), "stem kernel launch");
+    }
+    return launch_tc(*p, x, p->desc.c_in_b > 0 ? x_b : nullptr, w_packed, bias_i32, m_c, inv_s_y, nullptr, y,
+                     workspace, (cudaStream_t)stream);
+}
+
+}  // namespace
+
+extern "C" {
+
 cbs_status cbs_conv_bn_silu_i8(const cbs_plan_t *p, const int8_t *x, const void *w_packed,
                                const int32_t *bias_i32, const float *m_c, float s_y, int8_t *y,
                                void *workspace, size_t workspace_bytes, void *stream) {
     CBS_TRY(check_plan(p));
     if (p->desc.prec != CBS_INT8)
         return fail(CBS_ERR_INVALID_ARG, "plan is not an INT8 plan");
-    if (p->desc.n == 0) return CBS_OK;  // empty batch: nothing is read or written
-    CBS_TRY(check_conv_common(p, x, w_packed, bias_i32, y, workspace, workspace_bytes));
-    CBS_TRY(check_ptr(m_c, "m_c"));
-    if (!(s_y > 0.0f) || !(s_y < 3.0e38f)) return fail(CBS_ERR_INVALID_ARG, "s_y must be a positive finite float");
-    if (p->desc.n == 0) return CBS_OK;
-    const float inv_s_y = 1.0f / s_y;
-    if (p->variant == CBS_VARIANT_STEM) {
-        const StemLaunch L = stem_launch(*p, x, w_packed, bias_i32, m_c, inv_s_y, y);
-        return cuda_check(launch_stem(L, (cudaStream_t)stream), "stem kernel launch");
-    }
-    return launch_tc(*p, x, nullptr, w_packed, bias_i32, m_c, inv_s_y, nullptr, y, workspace, (cudaStream_t)stream);
+    if (p->desc.c_in_b > 0) return fail(CBS_ERR_INVALID_ARG, "two-input plan: call cbs_conv_bn_silu_i8_cat");
+    return conv_i8_impl(p, x, nullptr, w_packed, bias_i32, m_c, s_y, y, workspace, workspace_bytes, stream);
+}
+
+cbs_status cbs_conv_bn_silu_i8_cat(const cbs_plan_t *p, const int8_t *x, const int8_t *x_b, const void *w_packed,
+                                   const int32_t *bias_i32, const float *m_c, float s_y, int8_t *y,
+                                   void *workspace, size_t workspace_bytes, void *stream) {
+    CBS_TRY(check_plan(p));
+    if (p->desc.prec != CBS_INT8)
+        return fail(CBS_ERR_INVALID_ARG, "plan is not an INT8 plan");
+    if (p->desc.c_in_b <= 0) return fail(CBS_ERR_INVALID_ARG, "one-input plan: call cbs_conv_bn_silu_i8");
+    return conv_i8_impl(p, x, x_b, w_packed, bias_i32, m_c, s_y, y, workspace, workspace_bytes, stream);
 }
 
 cbs_status cbs_maxpool2d(const void *x, void *y, int n, int c, int h, int w, int k, int stride, int pad,

@@ -798,7 +798,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t u_lo, uint32_t u_hi) {
 // Persistent INT8 kernel.  Warps 0-1: TMA producers; warp 2: TMEM + MMA
 // issuer; warps 3-10: epilogue; warps 11-14: int8 -> bf16 converters.
 __global__ void __launch_bounds__(kThreadsI8, 1)
-tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                  const __grid_constant__ CUtensorMap tmB, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -841,6 +842,7 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmA);
+        if (p.ca_blocks < p.cblocks) ptx::prefetch_tmap(&tmA2);
         ptx::prefetch_tmap(&tmB);
     }
     if (warp == kMmaWarpI8) {
@@ -892,11 +894,14 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         if (is_a) {
                             const int r = tap / p.ks, tt = tap - r * p.ks;
                             const uint32_t dst = sb + stg_off + kk * stg_stride;
+                            const bool second = cb >= p.ca_blocks;   // channel block of the second input
+                            const CUtensorMap *tm = second ? &tmA2 : &tmA;
+                            const int c0 = (second ? cb - p.ca_blocks : cb) * p.CB;
                             if (p.im2col)
-                                ptx::tma_load_im2col_4d(dst, &tmA, raw_bar(s), cb * p.CB, wc, hc, img, (uint16_t)tt,
+                                ptx::tma_load_im2col_4d(dst, tm, raw_bar(s), c0, wc, hc, img, (uint16_t)tt,
                                                         (uint16_t)r);
                             else
-                                ptx::tma_load_2d(dst, &tmA, raw_bar(s), cb * p.CB, m0);
+                                ptx::tma_load_2d(dst, tm, raw_bar(s), c0, m0);
                         } else {
                             ptx::tma_load_2d(sb + op_b_off + kk * p.b_tile_stride, &tmB, raw_bar(s),
                                              tap * p.c_in_pad + cb * p.CB, n0);
@@ -1181,7 +1186,14 @@ int elem_bytes_of(int variant) { return variant == CBS_VARIANT_TC_TF32 ? 4 : 2; 
 }  // namespace
 
 // Channels per K step for the INT8 variant (int8 bytes per staging row).
-int i8_channel_block(int c_in_pad) { return c_in_pad % 64 == 0 ? 64 : (c_in_pad % 32 == 0 ? 32 : 16); }
+// Channels per INT8 K step: the largest of 64, 32, 16 dividing the padded
+// channel count and, for two inputs, the first input's channels (a channel
+// block never straddles the two tensors).
+int i8_channel_block(int c_in_pad, int c_a) {
+    for (int cb : {64, 32})
+        if (c_in_pad % cb == 0 && c_a % cb == 0) return cb;
+    return 16;
+}
 
 // Producer warps for a stage count: the largest of 4, 3, 2 that divides it
 // (each stage is then always refilled by the same warp).
@@ -1362,7 +1374,7 @@ cbs_status plan_tc(cbs_plan_t &p) {
     if (i8) {
         // int8 codes in memory, widened to bf16 operands in shared memory.
         p.c_in_pad = round_up(d.c_in, 16);
-        CB = i8_channel_block(p.c_in_pad);
+        CB = i8_channel_block(p.c_in_pad, d.c_in_b > 0 ? d.c_in - d.c_in_b : p.c_in_pad);
         RB = 2 * CB;
         const int ksteps = d.k * d.k * (p.c_in_pad / CB);
         nchunks = ceil_div(ksteps, 1024 / CB);
@@ -1544,7 +1556,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     P.ksteps = d.k * d.k * P.cblocks;
     const int c_a = d.c_in - d.c_in_b;             // channels of the first input (all of them with one)
     if (d.c_in_b > 0) {
-        if (i8 || !x_b || c_a % CB) return fail(CBS_ERR_PLAN_MISMATCH, "two-input plan: channel blocks");
+        if (!x_b || c_a % CB) return fail(CBS_ERR_PLAN_MISMATCH, "two-input plan: channel blocks");
         P.ca_blocks = c_a / CB;
     } else {
         P.ca_blocks = P.cblocks;
@@ -1716,7 +1728,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
         if (e == cudaSuccess) e = launch_kernel(tc_conv_kernel<kBF16>, grid, kThreads, pl.smem_bytes, s, tmA, tmA2, tmB, tmY, P);
     } else {
         e = set_max_dyn_smem(tc_conv_i8_kernel, pl.smem_bytes);
-        if (e == cudaSuccess) e = launch_kernel(tc_conv_i8_kernel, grid, kThreadsI8, pl.smem_bytes, s, tmA, tmB, P);
+        if (e == cudaSuccess) e = launch_kernel(tc_conv_i8_kernel, grid, kThreadsI8, pl.smem_bytes, s, tmA, tmA2, tmB, P);
     }
     return cuda_check(e, "tensor-core kernel launch");
 }

@@ -126,7 +126,7 @@ class FusedConvBnSilu:
         for t, shape in ((x_nchw, self.x_shape()), (x_b_nchw, self.x_b_shape())):
             assert t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()
             one = make_desc(d.n, t.shape[1], d.h, d.w, 16, 1, 1, 0, prec=d.prec, in_layout=d.in_layout,
-                            force_variant=self.plan.variant)
+                            force_variant=self.plan.variant, zero_point_x=d.zero_point_x)
             o = torch.empty(shape, dtype=self.x_dtype, device=self.device)
             B.cbs_pack_input(B.cbs_plan(one), t, o, self.s_x, current_stream())
             out.append(o)
@@ -141,6 +141,11 @@ class FusedConvBnSilu:
         y = self.empty_y() if y is None else y
         s = current_stream() if stream is None else stream
         ws_bytes = int(self.plan.workspace_bytes)
+        if self.desc.c_in_b and self.prec == B.CBS_INT8:
+            assert s_y is not None
+            B.cbs_conv_bn_silu_i8_cat(self.plan, x, x_b, self.w_packed, self.bias, self.m_c, float(s_y), y,
+                                      self.workspace, ws_bytes, s)
+            return y
         if self.desc.c_in_b:
             B.cbs_conv_bn_act_cat(self.plan, x, x_b, self.w_packed, self.bias, residual, y, self.workspace,
                                   ws_bytes, s)

@@ -108,9 +108,11 @@ typedef struct cbs_layer_desc {
                             fused into the convolution's input loads): channels 0..c_in-c_in_b-1
                             come from x and the last c_in_b from x_b, both with the same N, H, W
                             and layout; the layer is then called through cbs_conv_bn_act_cat.
-                            FP32 (CUDA-core variant), TF32 and BF16; the tensor-core variants
-                            need c_in - c_in_b to be a multiple of 16 (BF16) or 8 (TF32) channels
-                            and c_in_b a multiple of 8 (BF16) or 4 (TF32). */
+                            FP32 (CUDA-core variant), TF32, BF16 and INT8 (both inputs with the
+                            same scale and zero point; called through cbs_conv_bn_silu_i8_cat);
+                            the tensor-core variants need c_in - c_in_b to be a multiple of 16
+                            (BF16, INT8) or 8 (TF32) channels and c_in_b a multiple of 16 (INT8),
+                            8 (BF16) or 4 (TF32). */
     int zero_point_x;    /* INT8: zero point z_x in [-128, 127] of the input codes (asymmetric
                             activations, page 3 "Design notes": a code q stands for s_x (q - z_x);
                             a uint8 code u with zero point z_u is q = u - 128, z_x = z_u - 128).
@@ -272,6 +274,19 @@ CBS_API cbs_status cbs_conv_bn_silu_i8(const cbs_plan_t *p, const int8_t *x, con
                                const int32_t *bias_i32, const float *m_c, float s_y,
                                int8_t *y, void *workspace, size_t workspace_bytes,
                                void *stream);
+
+/*
+ * cbs_conv_bn_silu_i8_cat -- cbs_conv_bn_silu_i8 for a two-input plan: the
+ * input is concat(x, x_b) along channels, read straight from the two int8
+ * tensors (same scale s_x and zero point z_x).  x: NHWC int8 with
+ * c_in - c_in_b channels; x_b: NHWC int8 with c_in_pad - (c_in - c_in_b)
+ * channels (extra channels 0).  Other arguments and errors as for
+ * cbs_conv_bn_silu_i8, which rejects two-input plans (and this one-input ones).
+ */
+CBS_API cbs_status cbs_conv_bn_silu_i8_cat(const cbs_plan_t *p, const int8_t *x, const int8_t *x_b,
+                                           const void *w_packed, const int32_t *bias_i32, const float *m_c,
+                                           float s_y, int8_t *y, void *workspace, size_t workspace_bytes,
+                                           void *stream);
 
 /*
  * cbs_upsample2x_concat -- neck glue between two fused layers (page 1,

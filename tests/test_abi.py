@@ -178,10 +178,14 @@ def test_two_input_plans(cuda_lib):
         p = B.cbs_plan(make_desc(1, 48, 20, 20, 64, 3, 1, prec=prec, c_in_b=16))
         assert (32 % p.block_k) == 0 and p.x_b_bytes == 20 * 20 * (p.c_in_pad - 32) * eb
     assert B.cbs_plan(make_desc(1, 24, 20, 20, 64, 3, 1, prec=B.CBS_BF16, c_in_b=8)).c_in_pad == 32
+    # INT8: channel blocks of 64/32/16 codes that also divide the first input
+    p8 = B.cbs_plan(make_desc(2, 96, 20, 20, 64, 3, 1, prec=B.CBS_INT8, c_in_b=32))
+    assert p8.variant == B.CBS_VARIANT_TC_INT8 and 64 % p8.block_k == 0 and p8.block_k == 32
+    assert p8.x_bytes == 2 * 400 * 64 and p8.x_b_bytes == 2 * 400 * 32
     rejects = [
         (dict(c_in=16, c_in_b=16), B.CBS_ERR_INVALID_ARG),                      # c_in_b must be < c_in
         (dict(c_in=16, c_in_b=-1), B.CBS_ERR_INVALID_ARG),
-        (dict(c_in=32, c_in_b=16, prec=B.CBS_INT8), B.CBS_ERR_UNSUPPORTED),
+        (dict(c_in=40, c_in_b=16, prec=B.CBS_INT8), B.CBS_ERR_UNSUPPORTED),     # first input 24 codes: not 16-aligned
         (dict(c_in=24, c_in_b=16, prec=B.CBS_BF16), B.CBS_ERR_UNSUPPORTED),     # first input 8 bf16 = 16 B
         (dict(c_in=36, c_in_b=4, prec=B.CBS_BF16), B.CBS_ERR_UNSUPPORTED),      # second input 4 bf16 = 8 B
         (dict(c_in=4, c_in_b=2, force_variant=B.CBS_VARIANT_STEM), B.CBS_ERR_UNSUPPORTED),

@@ -2,10 +2,11 @@
 read straight from the two tensors (page 1, "Improvements" #6: channel_cat
 fused into the convolution's input loads).  The oracle convolves the
 concatenated array.  Covered: the CUDA-core implicit GEMM in both layouts
-(with split-K), and the TF32/BF16 tensor-core kernel on each A path (2-D
-tiles for 1x1, im2col boxes, windowed A) with the channel block boundary at
-the junction of the two inputs and a second input padded with zero channels.
-Bars as for the one-input layer."""
+(with split-K), the TF32/BF16 tensor-core kernel on each A path (2-D tiles
+for 1x1, im2col boxes, windowed A) with the channel block boundary at the
+junction of the two inputs and a second input padded with zero channels, and
+the INT8 kernel (bit-exact, symmetric and with zero points).  Bars as for the
+one-input layer."""
 import numpy as np
 import pytest
 import torch
@@ -111,3 +112,30 @@ def test_two_input_residual_identity(cuda_lib):
     want = oracle.conv_bn_act_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, 1, 1,
                                   act=B.CBS_ACT_IDENTITY, residual=r)
     assert rel_l2(y.cpu().numpy(), want) <= TOL_FP32_REL_L2
+
+
+@pytest.mark.parametrize("case", [
+    ((2, 64, 64, 64, 3, 1, 17, 17), (0, 0)),        # symmetric, 3x3, the junction between channel blocks
+    ((1, 96, 32, 48, 3, 2, 21, 19), (-30, 12)),     # asymmetric, stride 2, channel block 32
+    ((2, 128, 48, 64, 1, 1, 12, 12), (5, -90)),     # 1x1: 2-D tile boxes, second input padded to 64 codes
+])
+def test_int8_two_inputs(cuda_lib, case):
+    """INT8 two-input layers bit for bit against the oracle on the
+    concatenated, quantised input (both inputs share the scale and zero point)."""
+    (n, c_a, c_b, c_out, k, stride, h, w), (z_x, z_y) = case
+    spec = wl.LayerSpec(c_a + c_b, c_out, k, stride, h, w)
+    x, p = wl.layer_inputs(spec, n, layer_index=23)
+    s_x = float(wl.S_X_INT8)
+    y32 = oracle.conv_bn_silu_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, stride, spec.pad)
+    s_y = float(np.float32(np.abs(y32).max() / 120))
+    desc = make_desc(n, c_a + c_b, h, w, c_out, k, stride, spec.pad, prec=B.CBS_INT8, c_in_b=c_b,
+                     zero_point_x=z_x, zero_point_y=z_y)
+    layer = FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, s_x=s_x)
+    assert layer.plan.variant == B.CBS_VARIANT_TC_INT8
+    xa, xb = layer.pack_inputs(torch.from_numpy(np.ascontiguousarray(x[:, :c_a])).cuda(),
+                               torch.from_numpy(np.ascontiguousarray(x[:, c_a:])).cuda())
+    y = nhwc_to_nchw(layer(xa, s_y=s_y, x_b=xb).cpu().numpy())
+    q_x = oracle.quantize_act(x, s_x, z_x)
+    q_w, bias, m_c = oracle.fold_quant_i8(p.w, p.gamma, p.beta, p.mean, p.var, p.eps, s_x)
+    want = oracle.conv_i8(q_x, q_w, bias, m_c, s_y, stride, spec.pad, z_x=z_x, z_y=z_y)
+    assert int(np.count_nonzero(y != want)) == 0
