@@ -8,7 +8,9 @@ memory, `HostPipeline.run` enqueues
   - layer j's device-to-host output copy on a second copy stream, as soon as
     an event marks the layer as finished;
 so the host link carries inputs and outputs in both directions while the
-kernels run, instead of copy-all / compute-all / copy-all.  The copies are
+kernels run, instead of copy-all / compute-all / copy-all.
+`DoubleBufferedRunner` alternates two such steps on two buffer sets, so one
+step's copies also overlap the neighbouring step's kernels.  The copies are
 cudaMemcpyAsync calls (torch's copy_ on pinned memory) and every layer is a
 library kernel: nothing is computed on the host.
 """
@@ -69,8 +71,29 @@ class HostPipeline:
             cap.wait_stream(self.compute)
             cap.wait_stream(self.d2h)
 
-        def replay() -> None:
+        def replay(wait: bool = True) -> None:
             with torch.cuda.stream(cap):
                 graph.replay()
-            cap.synchronize()
+            if wait:
+                cap.synchronize()
+        replay.stream = cap
         return replay
+
+
+class DoubleBufferedRunner:
+    """Back-to-back steps with two sets of buffers: step i uses set i % 2, and
+    each set's captured step (HostPipeline.capture) replays on its own stream,
+    so step i + 1's input copies run while step i computes and its outputs
+    are read back.  A set's next step starts only after its previous one has
+    finished (same stream), so no buffer is overwritten while in use."""
+
+    def __init__(self, replays):
+        assert len(replays) == 2
+        self.replays = replays
+
+    def run(self, steps: int) -> None:
+        """Enqueue `steps` steps, then wait until every output is on the host."""
+        for i in range(steps):
+            self.replays[i % 2](wait=False)
+        for r in self.replays:
+            r.stream.synchronize()

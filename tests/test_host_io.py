@@ -42,3 +42,28 @@ def test_pipeline_matches_device_runs(cuda_lib, prec):
             pipe.run(calls, xs_h, xs_d, ys_d, ys_h)
         for j in range(len(layers)):
             assert torch.equal(ys_h[j], want[j]), (run, j)
+
+
+def test_double_buffered_runner(cuda_lib):
+    """Two buffer sets, two steps in flight: every step's outputs reach the
+    host and equal a device-resident run."""
+    from conv_bn_silu_gb300.host_io import DoubleBufferedRunner
+    s = wl.LayerSpec(32, 64, 3, 1, 40)
+    x, p = wl.layer_inputs(s, 2, layer_index=40)
+    layer = FusedConvBnSilu(make_desc(2, s.c_in, s.h, s.width, s.c_out, s.k, s.stride, s.pad), p.w, p.gamma,
+                            p.beta, p.mean, p.var, p.eps)
+    want = layer(torch.from_numpy(x).cuda()).cpu()
+    replays, hosts = [], []
+    for r in range(2):
+        xd, yd = [torch.from_numpy(x).cuda()], [layer.empty_y()]
+        xh, yh = [torch.from_numpy(x).pin_memory()], [torch.empty(yd[0].shape).pin_memory()]
+        calls = [lambda st, xd=xd, yd=yd: layer(xd[0], yd[0], stream=st)]
+        replays.append(HostPipeline(1).capture(calls, xh, xd, yd, yh))
+        hosts.append(yh[0])
+    runner = DoubleBufferedRunner(replays)
+    for steps in (1, 2, 7):
+        for h in hosts:
+            h.zero_()
+        runner.run(steps)
+        for r in range(min(steps, 2)):
+            assert torch.equal(hosts[r], want), (steps, r)
