@@ -17,6 +17,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import subprocess
 import sys
 import time
@@ -558,10 +559,34 @@ def cpu_baseline(w, budget_s: float = 10.0):
             done_flops += spec.flops(n)
             layers_done += 1
     dt = time.perf_counter() - t0
-    return {"value": round(done_flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "seconds": round(dt, 2),
-            "sample": f"{layers_done} full-size layers of the list at batch {n} "
-                      f"({layers_done / len(specs):.0f} passes), double arithmetic"}
+    cores = oracle.num_threads()
+    out = {"value": round(done_flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+           "kind": "oracle", "seconds": round(dt, 2), "machine": platform.machine(),
+           "sample": f"{layers_done} full-size layers of the list at batch {n} "
+                     f"({layers_done / len(specs):.0f} passes), double arithmetic"}
+    # The same oracle on one core: the single layer (config 1) and one pass
+    # over the batch-1 list, per layer.
+    oracle.set_threads(1)
+    try:
+        s1 = wl.SINGLE_LAYER
+        x1, p1 = wl.layer_inputs(s1, 1)
+        t = time.perf_counter()
+        for _ in range(3):
+            oracle.conv_bn_silu_f32(x1, p1.w, p1.gamma, p1.beta, p1.mean, p1.var, p1.eps, s1.stride, s1.pad)
+        single_ms = (time.perf_counter() - t) / 3 * 1e3
+        list_specs = list(WORKLOADS["layer_list_fp32_n1"]["layers"])
+        per_layer = []
+        for i, s in enumerate(list_specs):
+            x, p = wl.layer_inputs(s, 1, seed=0, layer_index=i)
+            t = time.perf_counter()
+            oracle.conv_bn_silu_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, s.stride, s.pad)
+            per_layer.append(round((time.perf_counter() - t) * 1e3, 2))
+        out["single_core"] = {"single_layer_ms": round(single_ms, 2), "list_batch1_layer_ms": per_layer,
+                              "list_batch1_tflops": round(sum(sp.flops(1) for sp in list_specs)
+                                                          / (sum(per_layer) * 1e-3) / 1e12, 6)}
+    finally:
+        oracle.set_threads(cores)
+    return out
 
 
 def run_reference(args, rank: int, world: int):

@@ -18,4 +18,5 @@ from .oracle import (  # noqa: F401
     requant,
     conv_i8,
     num_threads,
+    set_threads,
 )

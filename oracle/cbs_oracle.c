@@ -32,6 +32,7 @@
  * Parity status: every function here is pinned by tests/test_oracle_pins.py.
  */
 #include <math.h>
+#include <omp.h>
 #include <stddef.h>
 #include <stdint.h>
 #include <string.h>
@@ -42,6 +43,11 @@ ORACLE_API int oracle_out_dim(int in, int k, int stride, int pad)
 {
     return (in + 2 * pad - k) / stride + 1;
 }
+
+/* Threads of the OpenMP loops below (for timing the oracle on one core or
+ * on all of them). */
+ORACLE_API void oracle_set_threads(int n) { omp_set_num_threads(n > 0 ? n : 1); }
+ORACLE_API int oracle_max_threads(void) { return omp_get_max_threads(); }
 
 /* ---------------------------------------------------------------------- */
 /* FP32 path: conv -> BN -> SiLU, each its own step, all in double.        */

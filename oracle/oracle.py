@@ -43,6 +43,9 @@ def _load():
         lib.oracle_conv_i8.argtypes = [P, P, P, P, F, I, I, I, I, I, I, I, I, P, P]
         lib.oracle_conv_i8.restype = I
         lib.oracle_maxpool2d_f32.argtypes = [P, I, I, I, I, I, I, I, P]
+        lib.oracle_set_threads.argtypes = [I]
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_max_threads.restype = I
         lib.oracle_quantize_act_zp.argtypes = [P, Z, F, I, P]
         lib.oracle_requant_zp.argtypes = [ctypes.c_int32, F, F, I]
         lib.oracle_requant_zp.restype = ctypes.c_int8
@@ -61,9 +64,13 @@ def _f32(a):
 
 
 def num_threads() -> int:
-    """Threads the OpenMP runtime will use (OMP_NUM_THREADS, else all cores)."""
-    env = os.environ.get("OMP_NUM_THREADS")
-    return int(env) if env else (os.cpu_count() or 1)
+    """Threads the oracle's OpenMP loops use."""
+    return int(_load().oracle_max_threads())
+
+
+def set_threads(n: int) -> None:
+    """Run the oracle's OpenMP loops on n threads (1: single core)."""
+    _load().oracle_set_threads(int(n))
 
 
 def out_dim(size: int, k: int, stride: int, pad: int) -> int:
