@@ -28,8 +28,11 @@ _table = None
 
 
 def shape_key(d: B.cbs_layer_desc) -> str:
-    return ":".join(str(int(v)) for v in (d.prec, d.n, d.c_in, d.c_out, d.k, d.stride, d.pad, d.h, d.w,
-                                          d.in_layout, d.out_layout))
+    key = ":".join(str(int(v)) for v in (d.prec, d.n, d.c_in, d.c_out, d.k, d.stride, d.pad, d.h, d.w,
+                                         d.in_layout, d.out_layout))
+    # A two-input layer plans its channel blocks around the junction of its
+    # inputs: it is a shape of its own.
+    return key + (f":b{int(d.c_in_b)}" if d.c_in_b else "")
 
 
 def load_table(path: str = TABLE_PATH) -> dict:

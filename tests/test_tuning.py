@@ -46,3 +46,15 @@ def test_table_file_is_well_formed():
         meta = json.load(f)
     assert meta["created_by"] == "conv_bn_silu_gb300/autotune.py"
     assert isinstance(meta["plans"], dict)
+
+
+def test_two_input_layers_are_keyed_apart():
+    from conv_bn_silu_gb300 import _binding as B
+    from conv_bn_silu_gb300.layer import make_desc
+    from conv_bn_silu_gb300.tuning import shape_key, tuned_desc
+    one = make_desc(16, 384, 40, 40, 128, 1, 1, prec=B.CBS_BF16)
+    two = make_desc(16, 384, 40, 40, 128, 1, 1, prec=B.CBS_BF16, c_in_b=128)
+    assert shape_key(one) != shape_key(two) and shape_key(two).endswith(":b128")
+    table = {shape_key(one): {"force": {"force_block_n": 64}}}
+    assert tuned_desc(one, table).force_block_n == 64
+    assert tuned_desc(two, table).force_block_n == 0
