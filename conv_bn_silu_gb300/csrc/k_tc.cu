@@ -118,7 +118,18 @@ struct TcParams {
     // (q - zp_x) * q_w.
     int zp_x, zp_y;
     int in_h, in_w;
+    // Split-K (TF32/BF16, im2col or 2-D A, streamed weights, direct stores):
+    // unit u = tile * split + part covers stages [part * nstage / split,
+    // (part + 1) * nstage / split) of its tile.  Each epilogue warp writes
+    // its region of the FP32 partial tile, column-major ([part][col][row]),
+    // and the warp that arrives last for that region (counters[tile][warp])
+    // sums the parts in order and runs the epilogue.
+    int split;
+    float *partials;           // [tiles][split][tile_m * BN]
+    unsigned int *counters;    // [tiles][kEpiWarps], zero between launches
 };
+
+constexpr int kSplitCounterSlots = 8;   // one per epilogue warp
 
 constexpr int kStageBlockBytes = 4096;            // one warp's staged store block: 32 rows x 128 B
 
@@ -305,6 +316,20 @@ __device__ __forceinline__ void tile_coords(int t, int n_tiles, int tile_m, int 
     n0 = (t - mt * n_tiles) * BN;
 }
 
+// Work unit u of a launch: its tile and its range of pipeline stages.
+__device__ __forceinline__ void unit_range(int u, int split, int nstage, int &t, int &st0, int &st1) {
+    if (split == 1) {
+        t = u;
+        st0 = 0;
+        st1 = nstage;
+        return;
+    }
+    t = u / split;
+    const int part = u - t * split;
+    st0 = (part * nstage) / split;
+    st1 = ((part + 1) * nstage) / split;
+}
+
 // The MMAs of one K step for one accumulator: kslices K=16 (bf16) / K=8
 // (tf32) slices, 32 bytes apart along both operands' rows.  Descriptors are
 // built once per launch (dhi: every field but the start address); a slice
@@ -387,6 +412,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int kk2 = p.ks * p.ks;
     const int tile_m = kBM * p.mmul;
     const int num_tiles = p.m_tiles * p.n_tiles;
+    const int num_units = num_tiles * p.split;    // split-K: (tile, K part) units
     const int b_step_bytes = p.BN * p.RB;         // bytes of one B tile as loaded
 
     if (threadIdx.x == 0) {
@@ -480,7 +506,9 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // nprod divides the stage count, so a stage is always refilled by
             // the same warp and its empty-barrier parity cannot alias.
             int g = 0;
-            for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
+            for (int u = blockIdx.x; u < num_units && !aborted(abort_flag); u += gridDim.x) {
+                int t, st0, st1;
+                unit_range(u, p.split, nstage, t, st0, st1);
                 int m0, n0;
                 tile_coords(t, p.n_tiles, tile_m, m0, n0, p.BN);
                 int img, wc, hc;
@@ -501,7 +529,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     hc = oh * p.stride - p.pad;
                 }
                 bool ok = true;
-                for (int st = 0; st < nstage; ++st, ++g) {
+                for (int st = st0; st < st1; ++st, ++g) {
                     if (g % p.nprod != warp) continue;
                     const int s = g % S, u = g / S;
                     bool got = true;
@@ -561,7 +589,9 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 ok = false;
             }
             int g = 0, j = 0, gw = 0;
-            for (int t = blockIdx.x; ok && t < num_tiles && !aborted(abort_flag); t += gridDim.x, ++j) {
+            for (int u = blockIdx.x; ok && u < num_units && !aborted(abort_flag); u += gridDim.x, ++j) {
+                int t, st0, st1;
+                unit_range(u, p.split, nstage, t, st0, st1);
                 const int acc = j & 1, ua = j >> 1;
                 if (!ptx::mbar_wait_bounded(acce_bar(acc), (ua & 1) ^ 1, kWaitLimitNs)) {
                     abort_now(p, abort_flag);
@@ -617,9 +647,9 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     ptx::mma_commit(accf_bar(acc));
                     continue;
                 }
-                for (int st = 0; st < nstage; ++st, ++g) {
-                    const int s = g % S, u = g / S;
-                    if (!ptx::mbar_wait_bounded(full_bar(s), u & 1, kWaitLimitNs)) {
+                for (int st = st0; st < st1; ++st, ++g) {
+                    const int s = g % S, us = g / S;
+                    if (!ptx::mbar_wait_bounded(full_bar(s), us & 1, kWaitLimitNs)) {
                         abort_now(p, abort_flag);
                         ok = false;
                         break;
@@ -633,7 +663,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                                         : sbase + p.kg * p.a_box_bytes + kk * p.b_tile_stride;
                         for (int mi = 0; mi < p.mmul; ++mi)
                             issue_kstep<KIND>(d_tmem + (uint32_t)(mi * p.bnp), dhi, a_addr + mi * sub_bytes, b_addr, p.idesc,
-                                              kslices, i == 0);
+                                              kslices, i == st0 * p.kg);
                     }
                     ptx::mma_commit(empty_bar(s));
                 }
@@ -653,7 +683,9 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int cstep = p.mmul == 2 ? 16 : 32;
         const int row = sub * kBM + 32 * q + lane;
         int j = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++j) {
+        for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++j) {
+            int t, st0, st1;
+            unit_range(u, p.split, nstage, t, st0, st1);
             const int acc = j & 1, ua = j >> 1;
             // Warp-uniform decision: tcgen05.ld below needs the whole warp.
             bool ok = !aborted(abort_flag) && ptx::mbar_wait_bounded(accf_bar(acc), ua & 1, kWaitLimitNs);
@@ -687,6 +719,52 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
             }
             const uint32_t t_row = tmem_base + (uint32_t)(acc * p.acc_stride + sub * p.bnp) + ((uint32_t)(32 * q) << 16);
+            if (p.split > 1) {
+                // This warp's region of the partial tile: rows `row`, columns
+                // cstart, cstart + cstep, ... (16 each); column-major, so a
+                // warp's 32 rows of one column are 128 contiguous bytes.
+                const int part = u - t * p.split;
+                float *mine = p.partials + ((size_t)t * p.split + part) * (size_t)(tile_m * p.BN);
+                for (int c0 = cstart; c0 < p.BN; c0 += cstep) {
+                    uint32_t v[16];
+                    ptx::tmem_ld16(t_row + (uint32_t)c0, v);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) __stcg(mine + (size_t)(c0 + jj) * tile_m + row, __uint_as_float(v[jj]));
+                }
+                // The accumulator has been read: hand it back to the MMA issuer.
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(acce_bar(acc));
+                __threadfence();
+                __syncwarp();
+                unsigned int prev = 0u;
+                unsigned int *counter = p.counters + (size_t)t * kSplitCounterSlots + (warp - kEpiFirst);
+                if (lane == 0) prev = atomicAdd(counter, 1u);
+                prev = __shfl_sync(0xffffffffu, prev, 0);
+                if (prev != (unsigned int)(p.split - 1)) continue;
+                // Last part of this region: sum the parts in order, then the epilogue.
+                if (lane == 0) *counter = 0u;   // ready for the next launch
+                __threadfence();
+                const float *parts = p.partials + (size_t)t * p.split * (size_t)(tile_m * p.BN);
+                for (int c0 = cstart; c0 < p.BN; c0 += cstep) {
+                    float sum[16];
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) sum[jj] = 0.0f;
+                    for (int k2 = 0; k2 < p.split; ++k2) {
+                        const float *src = parts + (size_t)k2 * (tile_m * p.BN) + (size_t)c0 * tile_m + row;
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) sum[jj] += __ldcg(src + (size_t)jj * tile_m);
+                    }
+                    if (valid && n0 + c0 < p.C_out) {
+                        uint32_t v[16];
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) v[jj] = __float_as_uint(sum[jj]);
+                        epi_store16<KIND>(p, bias, m, img, oh, ow, n0 + c0, v);
+                    }
+                }
+                continue;
+            }
             if (p.st_mode) {
                 // Staged NHWC store: the warp's 32 pixels x one block of
                 // 128 output bytes go to shared memory, then out with one TMA
@@ -1394,7 +1472,7 @@ cbs_status plan_tc(cbs_plan_t &p) {
     p.w_packed_bytes = (size_t)d.c_out * p.k_gemm * (tf32 ? 4 : 2);
     if (d.pad > 127 || (p.oh - 1) * d.stride - d.pad - d.h + 1 < -128 || (p.ow - 1) * d.stride - d.pad - d.w + 1 < -128)
         return fail(CBS_ERR_UNSUPPORTED, "padding outside the im2col corner range");
-    if (d.force_split_k > 1) return fail(CBS_ERR_UNSUPPORTED, "split-K not built for the tensor-core path yet");
+    if (d.force_split_k > 1 && i8) return fail(CBS_ERR_UNSUPPORTED, "split-K is not built for the INT8 kernel");
     const long long M = (long long)d.n * p.oh * p.ow;
     const int ksteps = d.k * d.k * (p.c_in_pad / CB);
     p.block_k = CB;
@@ -1491,6 +1569,7 @@ cbs_status plan_tc(cbs_plan_t &p) {
             if (d.force_block_m > 0 && d.force_block_m != kBM * mmul) continue;
             for (int b_res = 0; b_res <= 1; ++b_res) {
                 if ((d.force_b_resident > 0 && !b_res) || (d.force_b_resident < 0 && b_res)) continue;
+                if (b_res && d.force_split_k > 1 && d.force_b_resident <= 0) continue;   // split-K streams weights
                 for (int win = 0; win <= 1; ++win) {
                     // Windowed A moves ~4x fewer bytes from L2 but measured no
                     // faster on GB300 (the MMA rate bounds these layers): it is
@@ -1499,6 +1578,8 @@ cbs_status plan_tc(cbs_plan_t &p) {
                     if (win && d.force_k_group > 0) continue;     // K groups belong to the im2col path
                     for (int kg = 1; kg <= (d.force_k_group > 4 ? d.force_k_group : 4); ++kg) {
                         if (ksteps % kg) continue;
+                        // a forced split needs at least that many stages per tile
+                        if (d.force_split_k > 1 && d.force_k_group <= 0 && ksteps / kg < d.force_split_k) continue;
                         if (win && kg > 1) break;                  // a window stage is one channel block
                         if (d.force_k_group > 0 && kg != d.force_k_group) continue;
                         TcConfig c;
@@ -1510,6 +1591,29 @@ cbs_status plan_tc(cbs_plan_t &p) {
         }
     }
     if (best.cycles >= 1e299) return fail(CBS_ERR_UNSUPPORTED, "no tensor-core tile configuration fits shared memory");
+    // Split-K on request only.  A launch with fewer tiles than SMs leaves
+    // SMs idle, and splitting K over S parts balances the MMAs (e.g. 100
+    // tiles of 256x128 over 152 SMs: 288 -> 192 MMAs on the busiest SM at
+    // S = 3), but on GB300 the partial tiles cost more than that: the last
+    // warp of each region reads every part back at the end of the kernel,
+    // and the 128->128 3x3 40x40 BF16 layer at batch 16 went from 24.6 us to
+    // 46.2 us.  So the cost model keeps S = 1.
+    const int tiles = best.m_tiles * best.n_tiles;
+    const int nstage = best.win ? 0 : ksteps / best.kg;
+    int split = 1;
+    if (d.force_split_k > 1) {
+        if (best.win || best.b_res)
+            return fail(CBS_ERR_UNSUPPORTED, "split-K needs im2col A and streamed weights (force_window/b_resident)");
+        if (d.force_split_k > nstage)
+            return fail(CBS_ERR_UNSUPPORTED, "split-K %d exceeds the %d pipeline stages of a tile", d.force_split_k, nstage);
+        split = d.force_split_k;
+    }
+    p.split_k = split;
+    if (split > 1) {
+        best.grid = tiles * split < kNumSMs ? tiles * split : kNumSMs;
+        p.workspace_bytes = (size_t)round_up(tiles * kSplitCounterSlots * 4, 256) +
+                            (size_t)tiles * split * (kBM * best.mmul) * best.BN * 4;
+    }
     p.block_m = kBM * best.mmul;
     p.block_n = best.BN;
     p.k_group = best.win ? best.SB : best.kg;   // windowed plans: weight-ring slots
@@ -1528,7 +1632,6 @@ cbs_status plan_tc(cbs_plan_t &p) {
 cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const void *w_packed, const void *bias,
                      const float *m_c, float inv_s_y, const void *residual, void *y, void *workspace,
                      cudaStream_t s) {
-    (void)workspace;
     const cbs_layer_desc &d = pl.desc;
     const DriverFns &fns = driver_fns();
     if (!fns.ok) return fail(CBS_ERR_CUDA, "cannot resolve cuTensorMapEncode* from the driver");
@@ -1567,6 +1670,14 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     if (pl.block_m != kBM * mmul || mmul < 1 || mmul > 2) return fail(CBS_ERR_PLAN_MISMATCH, "block_m %d", pl.block_m);
     P.mmul = mmul;
     P.win = i8 ? 0 : pl.window;
+    P.split = pl.split_k < 1 ? 1 : pl.split_k;
+    if (P.split > 1) {
+        if (i8 || pl.window || pl.b_resident) return fail(CBS_ERR_PLAN_MISMATCH, "split-K plan with windowed A or resident weights");
+        if (!workspace) return fail(CBS_ERR_WORKSPACE, "split-K plan without a workspace");
+        const size_t counter_bytes = (size_t)round_up(pl.m_tiles * pl.n_tiles * kSplitCounterSlots * 4, 256);
+        P.counters = static_cast<unsigned int *>(workspace);
+        P.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + counter_bytes);
+    }
     P.kg = P.win ? 1 : pl.k_group;
     P.b_res = i8 ? 0 : pl.b_resident;
     P.SB = (P.win && !P.b_res) ? pl.k_group : 0;
@@ -1599,7 +1710,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
         P.stage_bytes = P.win ? round_up((P.R_box * P.Wp + 8) * RB, 1024)
                               : P.kg * P.a_box_bytes + (P.b_res ? 0 : P.kg * P.b_tile_stride);
         const bool tf32 = pl.variant == CBS_VARIANT_TC_TF32;
-        P.st_mode = P.win ? 0 : tc_store_mode(d, BN, pl.n_tiles, tf32);
+        P.st_mode = (P.win || P.split > 1) ? 0 : tc_store_mode(d, BN, pl.n_tiles, tf32);
         P.cbw = 128 / tc_out_bytes(tf32);
         P.stg_bytes_total = P.st_mode ? kEpiWarps * kStageBlockBytes : 0;
         P.bias_bytes_smem = tc_bias_smem_bytes(d);

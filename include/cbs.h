@@ -87,7 +87,9 @@ typedef struct cbs_layer_desc {
     int out_layout;      /* cbs_layout of y */
     int prec;            /* cbs_precision */
     int force_variant;   /* -1: choose from prec; else a cbs_variant compatible with prec */
-    int force_split_k;   /* 0: choose; else the number of K splits to use (>= 1) */
+    int force_split_k;   /* 0: choose; else the number of K splits to use (>= 1).  Tensor-core
+                            variants (TF32/BF16): on request only, with im2col or 2-D A and
+                            streamed weights; the plan then needs a workspace */
     int force_block_n;   /* 0: choose; else the N tile width (must be one the variant supports) */
     int force_block_m;   /* 0: choose; else the M tile height (CUDA-core variant: 64, 128 or 256;
                             TF32/BF16 tensor-core variants: 128 or 256) */

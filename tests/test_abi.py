@@ -264,3 +264,18 @@ def test_maxpool_argument_rules(cuda_lib):
         B.cbs_maxpool2d(ok + 4, ok, 1, 8, 10, 10, 5, 1, 2, B.CBS_NHWC, B.CBS_FP32, None)
     assert e.value.status == B.CBS_ERR_MISALIGNED
     B.cbs_maxpool2d(ok, ok, 0, 8, 10, 10, 5, 1, 2, B.CBS_NHWC, B.CBS_FP32, None)   # empty batch: nothing enqueued
+
+
+def test_split_k_plan_rules(cuda_lib):
+    """Tensor-core split-K on request (the cost model keeps one part); it
+    needs im2col A and streamed weights."""
+    auto = B.cbs_plan(make_desc(16, 128, 40, 40, 128, 3, 1, prec=B.CBS_BF16, force_block_m=256, force_block_n=128))
+    assert auto.split_k == 1 and auto.workspace_bytes == 0
+    forced = B.cbs_plan(make_desc(16, 128, 40, 40, 128, 3, 1, prec=B.CBS_BF16, force_block_m=256, force_block_n=128,
+                                  force_split_k=3))
+    assert forced.split_k == 3 and forced.grid_ctas == 152
+    assert forced.workspace_bytes == 3328 + 100 * 3 * 256 * 128 * 4   # counters [tile][8 warps], then partials
+    for kw in ({"force_window": 1}, {"force_b_resident": 1}):
+        with pytest.raises(B.CbsError) as e:
+            B.cbs_plan(make_desc(2, 64, 16, 16, 64, 3, 1, prec=B.CBS_BF16, force_split_k=2, **kw))
+        assert e.value.status == B.CBS_ERR_UNSUPPORTED

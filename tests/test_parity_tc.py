@@ -246,3 +246,45 @@ def test_windowed_a(cuda_lib, prec, bm, bres, shape):
 
 def test_no_timeout_reported(cuda_lib):
     assert B.cbs_read_device_status(True, torch.cuda.current_stream().cuda_stream) == B.CBS_OK
+
+
+@pytest.mark.parametrize("prec", ["bf16", "tf32"])
+@pytest.mark.parametrize("case", [
+    ((2, 64, 64, 3, 1, 20), 2, {}),                        # two K parts
+    ((2, 64, 64, 3, 1, 20), 3, {"force_block_m": 256}),    # tall tiles: each warp owns a whole sub-tile
+    ((1, 64, 40, 3, 2, 17), 5, {"force_k_group": 1}),      # ragged pixels and channels; 5 parts over 9 stages
+    ((2, 128, 96, 1, 1, 9), 2, {"force_block_n": 48}),     # 1x1, several N tiles
+])
+def test_split_k(cuda_lib, prec, case):
+    """K split over parts whose partial tiles the last-arriving epilogue warp
+    of each region sums in order (NHWC and NCHW outputs)."""
+    (n, c_in, c_out, k, stride, h), split, kw = case
+    spec = wl.LayerSpec(c_in, c_out, k, stride, h)
+    x, p = wl.layer_inputs(spec, n, layer_index=17)
+    for out_layout in (B.CBS_NHWC, B.CBS_NCHW):
+        y, layer = run_tc(spec, x, p, PRECS[prec], out_layout=out_layout, force_split_k=split, **kw)
+        assert layer.plan.split_k == split and layer.plan.workspace_bytes > 0
+        check(y, spec, x, p, prec, (split, out_layout))
+        y2, _ = run_tc(spec, x, p, PRECS[prec], out_layout=out_layout, force_split_k=split, **kw)
+        assert np.array_equal(y, y2)     # the parts are summed in a fixed order
+
+
+def test_split_k_with_residual_and_two_inputs(cuda_lib):
+    """Split-K beside the residual add and the channel concatenation."""
+    spec = wl.LayerSpec(96, 64, 3, 1, 14)
+    x, p = wl.layer_inputs(spec, 2, layer_index=18)
+    r = np.random.default_rng(4).standard_normal((2, 64, 14, 14)).astype(np.float32)
+    desc = make_desc(2, 96, 14, 14, 64, 3, 1, prec=B.CBS_BF16, force_split_k=3, residual=1, c_in_b=32)
+    layer = FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps)
+    assert layer.plan.split_k == 3
+    xa, xb = layer.pack_inputs(torch.from_numpy(np.ascontiguousarray(x[:, :64])).cuda(),
+                               torch.from_numpy(np.ascontiguousarray(x[:, 64:])).cuda())
+    rr = torch.from_numpy(np.ascontiguousarray(r.transpose(0, 2, 3, 1))).cuda().to(torch.bfloat16)
+    y = nhwc_to_nchw(layer(xa, residual=rr, x_b=xb).float().cpu().numpy())
+    want = oracle.conv_bn_act_f32(as_read(x, "bf16"), p.w, p.gamma, p.beta, p.mean, p.var, p.eps, 1, 1,
+                                  residual=as_read(r, "bf16"))
+    assert rel_l2(y, want) <= TOL_TC_REL_L2 and max_scaled_err(y, want) <= TOL_TC_MAX_ABS
+    for _ in range(3):   # the arrival counters are back at zero after every call
+        again = nhwc_to_nchw(layer(xa, residual=rr, x_b=xb).float().cpu().numpy())
+        assert np.array_equal(again, y)
+
