@@ -295,7 +295,8 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
                                   : D.prec == CBS_INT8 ? (cout_t == 16 ? 4 : (cout_t == 32 ? 2 : 1))
                                                        : (cout_t <= 32 ? 2 : 1);
         p.block_m = 256 * px_per_thread;  // output pixels per CTA: 256 threads, px_per_thread each
-        const bool tc = stem_uses_tensor_cores(D.prec == CBS_BF16 ? 1 : 0, D.in_layout == CBS_NHWC, p.c_in_pad,
+        const bool tc = stem_uses_tensor_cores(D.prec == CBS_BF16 ? 1 : (D.prec == CBS_INT8 ? 2 : 0),
+                                               D.in_layout == CBS_NHWC, p.c_in_pad,
                                                D.k, D.c_out, M);
         if (tc) p.block_m = 128;           // tensor-core stem: 128 pixels (one M=128 MMA) per CTA
         p.block_n = cout_t;
@@ -305,7 +306,7 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
         p.m_tiles = (int)((M + p.block_m - 1) / p.block_m);
         p.n_tiles = 1;
         // the tensor-core stem is persistent: kStemTcCtasPerSm CTAs per SM walk the tiles
-        p.grid_ctas = tc ? std::min(p.m_tiles, kNumSMs * kStemTcCtasPerSm) : p.m_tiles;
+        p.grid_ctas = tc ? std::min(p.m_tiles, kNumSMs * stem_tc_ctas_per_sm(D.c_out)) : p.m_tiles;
         p.threads = 256;
         p.smem_bytes = tc ? kStemTcSmemBytes : D.k * D.k * p.c_in_pad * cout_t * 4;
         p.workspace_bytes = 0;

@@ -125,6 +125,14 @@ cudaError_t launch_stem(const StemLaunch &L, cudaStream_t s);
 bool stem_uses_tensor_cores(int kind, int in_nhwc, int c_pad, int ks, int cout, long long pixels);
 constexpr int kStemTcStages = 2, kStemTcCtasPerSm = 5;   // measured: 55.6 us vs 57.3 (4 stages, 3 CTAs) for the 640x640 stem at batch 16
 constexpr long long kStemTcMaxPixels = (1ll << 31) - 256;
+// CTAs of the tensor-core stem per SM: kStemTcCtasPerSm, fewer when their
+// two accumulators (n_mma columns each, allocated as a power of two >= 32)
+// would not fit the SM's 512 TMEM columns together.
+inline int stem_tc_ctas_per_sm(int cout) {
+    const int n_mma = (cout + 15) / 16 * 16;
+    const int cols = 2 * n_mma <= 32 ? 32 : (2 * n_mma <= 64 ? 64 : 128);
+    return kStemTcCtasPerSm < 512 / cols ? kStemTcCtasPerSm : 512 / cols;
+}
 // A ring + B (64 rows x 128 B) + bias + two mbarriers + TMEM slot + 1 KB for alignment
 constexpr int kStemTcSmemBytes = kStemTcStages * 16384 + 8192 + 64 * 4 + 16 + 16 + 1024;
 constexpr int kStemMaxCin = 4, kStemMaxCout = 64, kStemMaxK = 7;

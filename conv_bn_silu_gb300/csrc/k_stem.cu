@@ -554,10 +554,238 @@ __global__ void __launch_bounds__(256) stem_tc_bf16_kernel(const StemLaunch a, i
     }
 }
 
+// INT8 codes widened to bfloat16 (exact for |q| <= 128: the float has at most
+// 8 significant bits, so its top 16 bits are the bfloat16).
+__device__ __forceinline__ uint32_t codes_to_bf16x2(int lo, int hi) {
+    return (__float_as_uint((float)lo) >> 16) | (__float_as_uint((float)hi) & 0xffff0000u);
+}
+
+// Four int8 codes (one pixel, 4 channels) -> four bfloat16.
+__device__ __forceinline__ uint2 pixel_codes_to_bf16(uint32_t w) {
+    const int c0 = (int)(w << 24) >> 24, c1 = (int)(w << 16) >> 24, c2 = (int)(w << 8) >> 24, c3 = (int)w >> 24;
+    return make_uint2(codes_to_bf16x2(c0, c1), codes_to_bf16x2(c2, c3));
+}
+
+// INT8 stem on the tensor cores: the BF16 kernel's layout and pipeline, with
+// the gather through registers (codes are widened to bfloat16 on their way
+// into the A tile, one tile ahead of the MMA; a tap outside the image reads
+// the code of zero, z_x) and the specified requantising epilogue.  The sums
+// are exact: at most 48 products of magnitude <= 16256 per output.
+template <bool OUT_NHWC, bool PAIRS>
+__global__ void __launch_bounds__(256) stem_tc_i8_kernel(const StemLaunch a, int n_mma, StemTcGeom g,
+                                                         unsigned int *status) {
+    static_assert(kStemTcStages >= 2, "the INT8 stem uses two A stages");
+    extern __shared__ uint8_t stem_smem_raw[];
+    const uint32_t raw = ptx::smem_u32(stem_smem_raw);
+    uint8_t *base = stem_smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t *sA = base;                                           // 2 x 128 rows x 128 B
+    uint8_t *sB = base + kStemTcStages * 16384;                   // 64 rows x 128 B
+    int32_t *sBias = reinterpret_cast<int32_t *>(sB + 8192);      // 64: int32 bias (with the zero point)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sBias + 64);    // 2
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
+    __shared__ float sMc[64];
+
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int row = t & 127, half = t >> 7;
+    const int KK = a.KS * a.KS;
+    const int kslices = PAIRS ? 3 : (KK + 3) / 4;
+    const uint32_t ncols = 2 * n_mma <= 32 ? 32u : (2 * n_mma <= 64 ? 64u : 128u);
+    if (warp == 0) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), ncols);
+        ptx::tmem_relinquish();
+    }
+    if (t == 0) {
+        ptx::mbar_init(ptx::smem_u32(&bars[0]), 1);
+        ptx::mbar_init(ptx::smem_u32(&bars[1]), 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    ptx::griddep_launch_dependents();   // after this CTA's TMEM allocation
+    ptx::griddep_wait();
+    // B: the weight codes (bf16) in the BF16 stem's K layout.
+    const uint2 *w2 = static_cast<const uint2 *>(a.w);
+    for (int idx = t; idx < n_mma * 8; idx += 256) {
+        const int co = idx >> 3, q = idx & 7;
+        uint2 lo = make_uint2(0u, 0u), hi = make_uint2(0u, 0u);
+        if (co < a.Cout) {
+            const uint2 *wr = w2 + (size_t)co * KK;
+            if (PAIRS) {
+                if (q < 6) {
+                    const int r = q >> 1;
+                    if ((q & 1) == 0) {
+                        hi = wr[r * 3];
+                    } else {
+                        lo = wr[r * 3 + 1];
+                        hi = wr[r * 3 + 2];
+                    }
+                }
+            } else {
+                if (2 * q < KK) lo = wr[2 * q];
+                if (2 * q + 1 < KK) hi = wr[2 * q + 1];
+            }
+        }
+        *reinterpret_cast<uint4 *>(sB + co * 128 + ((q ^ (co & 7)) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+    if (t < 64) {
+        sBias[t] = t < a.Cout ? static_cast<const int32_t *>(a.bias)[t] : 0;
+        sMc[t] = t < a.Cout ? a.m_c[t] : 0.0f;
+    }
+
+    const int n_local = (int)blockIdx.x < g.n_tiles ? (g.n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int ohw = a.OH * a.OW;
+    const uint32_t *x4 = static_cast<const uint32_t *>(a.x);   // one 4-channel int8 pixel
+    const uint32_t zfill = (uint32_t)(uint8_t)(int8_t)a.zp_x * 0x01010101u;
+    const uint32_t swz = (uint32_t)(row & 7);
+
+    // This thread's share of one tile's taps, as raw codes (PAIRS: three
+    // 2-pixel chunks; otherwise six single taps).
+    uint32_t reg[6];
+    auto load = [&](int i) {
+        const int pix = ((int)blockIdx.x + i * (int)gridDim.x) * 128 + row;
+        const bool valid = pix < g.total;
+        const int img = fast_div(pix, g.div_ohw);
+        const int rem = pix - img * ohw;
+        const int oh = fast_div(rem, g.div_ow);
+        const int ow = rem - oh * a.OW;
+        if (PAIRS) {
+#pragma unroll
+            for (int qq = 0; qq < 3; ++qq) {
+                const int q = 3 * half + qq, r = q >> 1;
+                const int ih = 2 * oh - 1 + r, col = 2 * ow - 2 + 2 * (q & 1);
+                const bool in = valid && (unsigned)ih < (unsigned)a.H && col >= 0 && col + 1 < a.W;
+                uint2 v = make_uint2(zfill, zfill);
+                if (in) v = __ldg(reinterpret_cast<const uint2 *>(x4 + (size_t)(img * a.H + ih) * a.W + col));
+                reg[2 * qq] = v.x;
+                reg[2 * qq + 1] = v.y;
+            }
+        } else {
+#pragma unroll
+            for (int ss = 0; ss < 6; ++ss) {
+                const int s2 = 6 * half + ss;
+                const int r = s2 / a.KS, c = s2 - (s2 / a.KS) * a.KS;
+                const int ih = oh * a.stride - a.pad + r, iw = ow * a.stride - a.pad + c;
+                const bool in = valid && s2 < KK && (unsigned)ih < (unsigned)a.H && (unsigned)iw < (unsigned)a.W;
+                reg[ss] = in ? __ldg(x4 + (size_t)(img * a.H + ih) * a.W + iw) : zfill;
+            }
+        }
+    };
+    // Widen the loaded codes into stage st of A.
+    auto store = [&](int st) {
+        uint8_t *rp = sA + st * 16384 + row * 128;
+        if (PAIRS) {
+#pragma unroll
+            for (int qq = 0; qq < 3; ++qq) {
+                const int q = 3 * half + qq;
+                const uint2 lo = pixel_codes_to_bf16(reg[2 * qq]), hi = pixel_codes_to_bf16(reg[2 * qq + 1]);
+                *reinterpret_cast<uint4 *>(rp + (((uint32_t)q ^ swz) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+            }
+        } else {
+#pragma unroll
+            for (int ss = 0; ss < 6; ++ss) {
+                const int s2 = 6 * half + ss;
+                if (s2 >= kslices * 4) break;
+                *reinterpret_cast<uint2 *>(rp + (((uint32_t)(s2 >> 1) ^ swz) << 4) + (s2 & 1) * 8) =
+                    pixel_codes_to_bf16(reg[ss]);
+            }
+        }
+    };
+    // Requantising epilogue of this thread's 8-channel groups of local tile i.
+    auto epilogue = [&](int i, uint32_t tmem) {
+        const int pix = ((int)blockIdx.x + i * (int)gridDim.x) * 128 + row;
+        const bool valid = pix < g.total;
+        const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((i & 1) * n_mma);
+        int8_t *y = static_cast<int8_t *>(a.y);
+        for (int c0 = 8 * half; c0 < n_mma; c0 += 16) {
+            uint32_t v[8];
+            ptx::tmem_ld8(t_row + (uint32_t)c0, v);
+            ptx::tmem_ld_wait();
+            if (!valid) continue;
+            int q[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int acc = (int)((unsigned)__float2int_rn(__uint_as_float(v[jj])) + (unsigned)sBias[c0 + jj]);
+                q[jj] = requant_i8(acc, sMc[c0 + jj], a.inv_s_y, a.zp_y);
+            }
+            if (OUT_NHWC && c0 + 8 <= a.Cout && (a.Cout & 7) == 0) {
+                uint32_t lo = 0u, hi = 0u;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    lo |= (uint32_t)(uint8_t)(int8_t)q[jj] << (8 * jj);
+                    hi |= (uint32_t)(uint8_t)(int8_t)q[jj + 4] << (8 * jj);
+                }
+                *reinterpret_cast<uint2 *>(y + (size_t)pix * a.Cout + c0) = make_uint2(lo, hi);
+            } else {
+                const int img = fast_div(pix, g.div_ohw);
+                const int rem = pix - img * ohw;
+                const int oh = fast_div(rem, g.div_ow);
+                const int ow = rem - oh * a.OW;
+                const size_t plane = (size_t)a.OH * a.out_row_stride;
+                const size_t opix = (size_t)oh * a.out_row_stride + ow;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int c = c0 + jj;
+                    if (c >= a.Cout) break;
+                    const size_t off = OUT_NHWC ? (size_t)pix * a.Cout + c : ((size_t)img * a.Cout + c) * plane + opix;
+                    y[off] = (int8_t)q[jj];
+                }
+            }
+        }
+    };
+
+    if (n_local > 0) {
+        load(0);
+        store(0);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint64_t dhi = ptx::smem_desc(0u, 16u, 1024u, 2u);
+    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n_mma >> 3) << 17) |
+                           ((uint32_t)(128 >> 4) << 24);
+    const uint64_t bd = dhi | (uint64_t)((ptx::smem_u32(sB) & 0x3FFFFu) >> 4);
+    const uint32_t sA_u32 = ptx::smem_u32(sA);
+    bool failed = false;
+#pragma unroll 1
+    for (int i = 0; i <= n_local; ++i) {
+        if (i + 1 < n_local) load(i + 1);   // in flight during this tile's MMA and the last tile's epilogue
+        ptx::fence_proxy_async_smem();       // stage i % 2 written through the generic proxy
+        ptx::tc_fence_before();
+        if (__syncthreads_or(failed)) break;
+        ptx::tc_fence_after();
+        if (i < n_local && t == 0) {
+            const uint64_t ad = dhi | (uint64_t)(((sA_u32 + (uint32_t)((i & 1) * 16384)) & 0x3FFFFu) >> 4);
+            const uint32_t acc = tmem + (uint32_t)((i & 1) * n_mma);
+            for (int k = 0; k < kslices; ++k) ptx::mma_f16(acc, ad + 2u * k, bd + 2u * k, idesc, k > 0 ? 1u : 0u);
+            ptx::mma_commit(ptx::smem_u32(&bars[i & 1]));
+        }
+        if (i > 0) {
+            const int j = i - 1;
+            bool ok = ptx::mbar_wait_bounded(ptx::smem_u32(&bars[j & 1]), (uint32_t)((j >> 1) & 1), kStemWaitNs);
+            ok = __all_sync(0xffffffffu, ok);   // warp-uniform before .sync.aligned loads
+            if (!ok) {
+                failed = true;
+                if (lane == 0) atomicOr(status, 1u);
+            } else {
+                ptx::tc_fence_after();
+                epilogue(j, tmem);
+            }
+        }
+        // Stage (i + 1) % 2 was read by the MMAs of tile i - 1, complete above.
+        if (i + 1 < n_local && !failed) store((i + 1) & 1);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, ncols);
+    }
+}
+
 }  // namespace
 
 bool stem_uses_tensor_cores(int kind, int in_nhwc, int c_pad, int ks, int cout, long long pixels) {
-    return kind == 1 && in_nhwc && c_pad == 4 && ks <= 3 && cout <= 64 && pixels < kStemTcMaxPixels;
+    return (kind == 1 || kind == 2) && in_nhwc && c_pad == 4 && ks <= 3 && cout <= 64 && pixels < kStemTcMaxPixels;
 }
 
 namespace {
@@ -565,7 +793,7 @@ namespace {
 template <bool OUT_NHWC, bool PAIRS>
 cudaError_t launch_stem_tc_as(const StemLaunch &L, int n_mma, StemTcGeom g, int grid, cudaStream_t s,
                               unsigned int *status) {
-    auto kern = stem_tc_bf16_kernel<OUT_NHWC, PAIRS>;
+    auto kern = L.kind == 2 ? stem_tc_i8_kernel<OUT_NHWC, PAIRS> : stem_tc_bf16_kernel<OUT_NHWC, PAIRS>;
     const cudaError_t e = set_max_dyn_smem(kern, kStemTcSmemBytes);
     if (e != cudaSuccess) return e;
     return launch_kernel(kern, grid, 256, kStemTcSmemBytes, s, L, n_mma, g, status);
@@ -581,7 +809,7 @@ cudaError_t launch_stem_tc(const StemLaunch &L, cudaStream_t s) {
     g.n_tiles = (int)((total + 127) / 128);
     g.div_ohw = make_fastdiv((uint32_t)(L.OH * L.OW));
     g.div_ow = make_fastdiv((uint32_t)L.OW);
-    const int grid = std::min(g.n_tiles, kNumSMs * kStemTcCtasPerSm);
+    const int grid = std::min(g.n_tiles, kNumSMs * stem_tc_ctas_per_sm(L.Cout));
     const int n_mma = (L.Cout + 15) / 16 * 16;
     const bool pairs = L.KS == 3 && L.stride == 2 && L.pad == 1 && (L.W & 1) == 0;
     if (L.out_nhwc)

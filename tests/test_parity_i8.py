@@ -200,3 +200,36 @@ def test_asymmetric_zero_points(cuda_lib, shape, z):
     assert mism == 0, (layer.plan.variant, mism, y.size)
     if abs(z_y) < 100:   # (an output zero point at an end of the code range saturates half the outputs)
         assert len(np.unique(y)) > 20
+
+
+@pytest.mark.parametrize("out_layout", [B.CBS_NHWC, B.CBS_NCHW])
+@pytest.mark.parametrize("shape,z", [
+    ((2, 3, 16, 3, 2, 38, 38), (0, 0)),        # 3x3 s2, even width: pixel-pair loads
+    ((2, 3, 16, 3, 2, 37, 37), (-40, 9)),      # odd width: one load per tap
+    ((1, 4, 32, 3, 1, 19, 19), (17, -3)),      # stride 1
+    ((3, 1, 48, 1, 1, 9, 9), (5, 60)),         # 1x1, C_out 48: 4 CTAs per SM (TMEM)
+    ((1, 2, 64, 3, 2, 50, 34), (-128, 127)),   # C_out 64, non-square, zero points at the ends
+    ((1, 3, 20, 3, 2, 22, 22), (3, -7)),       # C_out 20: per-channel stores
+    ((4, 3, 16, 3, 2, 160, 160), (-20, -100)), # 1600 tiles: several per persistent CTA
+])
+def test_tensor_core_stem_i8(cuda_lib, out_layout, shape, z):
+    """INT8 layers with at most 4 input channels and k <= 3 run on the
+    tensor-core stem: bit for bit against the oracle."""
+    n, c_in, c_out, k, stride, h, w = shape
+    z_x, z_y = z
+    spec = wl.LayerSpec(c_in, c_out, k, stride, h, w)
+    x, p = wl.layer_inputs(spec, n, layer_index=19)
+    y32 = oracle.conv_bn_silu_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, stride, spec.pad)
+    s_y = float(np.float32(np.abs(y32).max() / 110))
+    desc = make_desc(n, c_in, h, w, c_out, k, stride, spec.pad, prec=B.CBS_INT8, in_layout=B.CBS_NHWC,
+                     out_layout=out_layout, zero_point_x=z_x, zero_point_y=z_y)
+    layer = FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, s_x=S_X)
+    pl = layer.plan
+    assert pl.variant == B.CBS_VARIANT_STEM and pl.block_m == 128 and pl.threads == 256
+    y = layer(layer.pack_input(torch.from_numpy(x).cuda()), s_y=s_y).cpu().numpy()
+    if out_layout == B.CBS_NHWC:
+        y = nhwc_to_nchw(y)
+    q_w, bias, m_c = oracle.fold_quant_i8(p.w, p.gamma, p.beta, p.mean, p.var, p.eps, S_X)
+    want = oracle.conv_i8(oracle.quantize_act(x, S_X, z_x), q_w, bias, m_c, s_y, stride, spec.pad,
+                          z_x=z_x, z_y=z_y)
+    assert int(np.count_nonzero(y != want)) == 0, shape
