@@ -160,6 +160,7 @@ StemLaunch stem_launch(const cbs_plan_t &p, const void *x, const void *w, const 
     L.out_nhwc = d.out_layout == CBS_NHWC;
     L.out_row_stride = p.out_row_stride;
     L.kind = d.prec == CBS_INT8 ? 2 : (d.prec == CBS_BF16 ? 1 : 0);
+    L.tf32 = d.prec == CBS_TF32;
     L.act = d.activation;
     L.residual = nullptr;
     L.zp_x = d.prec == CBS_INT8 ? d.zero_point_x : 0;
@@ -295,9 +296,8 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
                                   : D.prec == CBS_INT8 ? (cout_t == 16 ? 4 : (cout_t == 32 ? 2 : 1))
                                                        : (cout_t <= 32 ? 2 : 1);
         p.block_m = 256 * px_per_thread;  // output pixels per CTA: 256 threads, px_per_thread each
-        const bool tc = stem_uses_tensor_cores(D.prec == CBS_BF16 ? 1 : (D.prec == CBS_INT8 ? 2 : 0),
-                                               D.in_layout == CBS_NHWC, p.c_in_pad,
-                                               D.k, D.c_out, M);
+        const int tc_kind = D.prec == CBS_BF16 ? 1 : (D.prec == CBS_INT8 ? 2 : (D.prec == CBS_TF32 ? 3 : 0));
+        const bool tc = stem_uses_tensor_cores(tc_kind, D.in_layout == CBS_NHWC, p.c_in_pad, D.k, D.c_out, M);
         if (tc) p.block_m = 128;           // tensor-core stem: 128 pixels (one M=128 MMA) per CTA
         p.block_n = cout_t;
         p.block_k = D.k * D.k * p.c_in_pad;
@@ -306,9 +306,9 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
         p.m_tiles = (int)((M + p.block_m - 1) / p.block_m);
         p.n_tiles = 1;
         // the tensor-core stem is persistent: kStemTcCtasPerSm CTAs per SM walk the tiles
-        p.grid_ctas = tc ? std::min(p.m_tiles, kNumSMs * stem_tc_ctas_per_sm(D.c_out)) : p.m_tiles;
+        p.grid_ctas = tc ? std::min(p.m_tiles, kNumSMs * stem_tc_ctas_per_sm(D.c_out, tc_kind == 3)) : p.m_tiles;
         p.threads = 256;
-        p.smem_bytes = tc ? kStemTcSmemBytes : D.k * D.k * p.c_in_pad * cout_t * 4;
+        p.smem_bytes = tc ? (tc_kind == 3 ? kStemTf32SmemBytes : kStemTcSmemBytes) : D.k * D.k * p.c_in_pad * cout_t * 4;
         p.workspace_bytes = 0;
     } else if (variant == CBS_VARIANT_SIMT_FP32) {
         plan_simt(p);

@@ -113,25 +113,32 @@ struct StemLaunch {
     int N, C, c_pad, H, W, Cout, OH, OW, KS, stride, pad;
     int in_nhwc, out_nhwc, out_row_stride;
     int kind;                  // 0 float, 1 bf16, 2 int8
+    int tf32;                  // float kind: 1 = the TF32 precision (tensor cores allowed), 0 = FP32
     int act;                   // cbs_activation (float kinds)
     const void *residual;      // nullable, element type and layout of y (float kinds)
     int zp_x, zp_y;            // INT8 zero points of input and output codes
 };
 cudaError_t launch_stem(const StemLaunch &L, cudaStream_t s);
-// BF16 stems (4-channel NHWC input, k <= 3, C_out <= 64) run on the tensor
+// TF32, BF16 and INT8 stems (4-channel NHWC input, k <= 3, C_out <= 64;
+// kind 3 = TF32, 1 = BF16, 2 = INT8) run on the tensor
 // cores (when there are fewer than kStemTcMaxPixels output pixels, for 32-bit
 // pixel indices): persistent CTAs of 256 threads, 128 output pixels per tile,
 // a ring of kStemTcStages A tiles; the others on the CUDA cores.
 bool stem_uses_tensor_cores(int kind, int in_nhwc, int c_pad, int ks, int cout, long long pixels);
 constexpr int kStemTcStages = 2, kStemTcCtasPerSm = 5;   // measured: 55.6 us vs 57.3 (4 stages, 3 CTAs) for the 640x640 stem at batch 16
 constexpr long long kStemTcMaxPixels = (1ll << 31) - 256;
+// TF32: a row of 9 taps x 16 bytes spans two 128-byte panels (A and B), two stages.
+constexpr int kStemTf32CtasPerSm = 4;
+// Two A stages of 5 x 4 KB, B of 5 x 2 KB, bias, mbarriers, TMEM slot, alignment.
+constexpr int kStemTf32SmemBytes = 2 * 20480 + 10240 + 64 * 4 + 16 + 16 + 1024;
 // CTAs of the tensor-core stem per SM: kStemTcCtasPerSm, fewer when their
 // two accumulators (n_mma columns each, allocated as a power of two >= 32)
 // would not fit the SM's 512 TMEM columns together.
-inline int stem_tc_ctas_per_sm(int cout) {
+inline int stem_tc_ctas_per_sm(int cout, int tf32 = 0) {
     const int n_mma = (cout + 15) / 16 * 16;
     const int cols = 2 * n_mma <= 32 ? 32 : (2 * n_mma <= 64 ? 64 : 128);
-    return kStemTcCtasPerSm < 512 / cols ? kStemTcCtasPerSm : 512 / cols;
+    const int want = tf32 ? kStemTf32CtasPerSm : kStemTcCtasPerSm;
+    return want < 512 / cols ? want : 512 / cols;
 }
 // A ring + B (64 rows x 128 B) + bias + two mbarriers + TMEM slot + 1 KB for alignment
 constexpr int kStemTcSmemBytes = kStemTcStages * 16384 + 8192 + 64 * 4 + 16 + 16 + 1024;

@@ -782,10 +782,194 @@ __global__ void __launch_bounds__(256) stem_tc_i8_kernel(const StemLaunch a, int
     }
 }
 
+// TF32 stem on the tensor cores.  An fp32 pixel of 4 channels is 16 bytes,
+// so each tap is one 16-byte cp.async straight into the A tile (no
+// conversion), and a tcgen05 kind::tf32 K slice (8 values, 32 bytes) holds two
+// taps.  Nine taps (+ one zero slot) are five K slices, each its own
+// 32-byte-swizzled block (128 rows x 32 B for A, 64 rows x 32 B for B), so no
+// byte of shared memory is padding: 20 KB per A stage, two stages, four CTAs
+// per SM.  Otherwise the BF16 kernel's pipeline (ring one tile ahead,
+// double-buffered accumulators).
+template <bool OUT_NHWC>
+__global__ void __launch_bounds__(256) stem_tc_tf32_kernel(const StemLaunch a, int n_mma, StemTcGeom g,
+                                                           unsigned int *status) {
+    constexpr int S = 2, kSliceA = 4096, kSliceB = 2048, kStage = 5 * kSliceA;
+    extern __shared__ uint8_t stem_smem_raw[];
+    const uint32_t raw = ptx::smem_u32(stem_smem_raw);
+    uint8_t *base = stem_smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t *sA = base;                                             // S stages x 5 slices x 128 rows x 32 B
+    uint8_t *sB = base + S * kStage;                                // 5 slices x 64 rows x 32 B
+    float *sBias = reinterpret_cast<float *>(sB + 5 * kSliceB);     // 64
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sBias + 64);      // 2
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
+
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int row = t & 127, half = t >> 7;
+    const int KK = a.KS * a.KS;
+    const int kslices = (KK + 1) / 2;                 // two taps per K slice
+    const uint32_t ncols = 2 * n_mma <= 32 ? 32u : (2 * n_mma <= 64 ? 64u : 128u);
+    const bool silu = a.act != CBS_ACT_IDENTITY;
+    if (warp == 0) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), ncols);
+        ptx::tmem_relinquish();
+    }
+    if (t == 0) {
+        ptx::mbar_init(ptx::smem_u32(&bars[0]), 1);
+        ptx::mbar_init(ptx::smem_u32(&bars[1]), 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    ptx::griddep_launch_dependents();   // after this CTA's TMEM allocation
+    ptx::griddep_wait();
+    // B row co, slot s: tap s's four folded weights (zero past KK and for
+    // co >= C_out), slice s / 2, 16-byte chunk s % 2 stored at (s % 2) ^ bit 2 of co.
+    const float4 *w4 = static_cast<const float4 *>(a.w);   // [C_out][KK] taps of 4 floats
+    for (int idx = t; idx < n_mma * 10; idx += 256) {
+        const int co = idx / 10, sl = idx - co * 10;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (co < a.Cout && sl < KK) v = w4[(size_t)co * KK + sl];
+        *reinterpret_cast<float4 *>(sB + (sl >> 1) * kSliceB + co * 32 + (((sl & 1) ^ ((co >> 2) & 1)) << 4)) = v;
+    }
+    if (t < 64) {   // halved for the tanh form of SiLU
+        const float b = t < a.Cout ? static_cast<const float *>(a.bias)[t] : 0.0f;
+        sBias[t] = silu ? 0.5f * b : b;
+    }
+
+    const int n_local = (int)blockIdx.x < g.n_tiles ? (g.n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int ohw = a.OH * a.OW;
+    const float4 *x4 = static_cast<const float4 *>(a.x);   // one 4-channel fp32 pixel
+    const uint32_t sA_u32 = ptx::smem_u32(sA);
+    const uint32_t swz = (uint32_t)((row >> 2) & 1);
+
+    // This thread's five tap slots (5 * half ..) of local tile i into stage i % 2.
+    auto gather = [&](int i) {
+        if (i < n_local) {
+            const int pix = ((int)blockIdx.x + i * (int)gridDim.x) * 128 + row;
+            const bool valid = pix < g.total;
+            const int img = fast_div(pix, g.div_ohw);
+            const int rem = pix - img * ohw;
+            const int oh = fast_div(rem, g.div_ow);
+            const int ow = rem - oh * a.OW;
+            const uint32_t dst = sA_u32 + (uint32_t)((i & 1) * kStage + row * 32);
+#pragma unroll
+            for (int ss = 0; ss < 5; ++ss) {
+                const int sl = 5 * half + ss;
+                if (sl >= 2 * kslices) break;
+                const int r = sl / a.KS, c = sl - (sl / a.KS) * a.KS;
+                const int ih = oh * a.stride - a.pad + r, iw = ow * a.stride - a.pad + c;
+                const bool in = valid && sl < KK && (unsigned)ih < (unsigned)a.H && (unsigned)iw < (unsigned)a.W;
+                const void *src = in ? (const void *)(x4 + (size_t)(img * a.H + ih) * a.W + iw) : a.x;
+                ptx::cp_async_16(dst + (uint32_t)((sl >> 1) * kSliceA) + (((uint32_t)(sl & 1) ^ swz) << 4), src,
+                                 in ? 16u : 0u);
+            }
+        }
+        ptx::cp_async_commit();
+    };
+
+    // Bias, activation, residual and float stores of this thread's 8-channel
+    // groups (half, half + 2, ...) of local tile i.
+    auto epilogue = [&](int i, uint32_t tmem) {
+        const int pix = ((int)blockIdx.x + i * (int)gridDim.x) * 128 + row;
+        const bool valid = pix < g.total;
+        const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((i & 1) * n_mma);
+        float *y = static_cast<float *>(a.y);
+        const float *res = static_cast<const float *>(a.residual);
+        for (int c0 = 8 * half; c0 < n_mma; c0 += 16) {
+            uint32_t v[8];
+            ptx::tmem_ld8(t_row + (uint32_t)c0, v);
+            ptx::tmem_ld_wait();
+            if (!valid) continue;
+            float o[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+                o[jj] = silu ? silu_tanh(fmaf(__uint_as_float(v[jj]), 0.5f, sBias[c0 + jj]))
+                             : __uint_as_float(v[jj]) + sBias[c0 + jj];
+            if (OUT_NHWC && c0 + 8 <= a.Cout && (a.Cout & 3) == 0) {
+                const size_t off = (size_t)pix * a.Cout + c0;
+                if (res) {
+                    const float4 r0 = *reinterpret_cast<const float4 *>(res + off);
+                    const float4 r1 = *reinterpret_cast<const float4 *>(res + off + 4);
+                    o[0] += r0.x, o[1] += r0.y, o[2] += r0.z, o[3] += r0.w;
+                    o[4] += r1.x, o[5] += r1.y, o[6] += r1.z, o[7] += r1.w;
+                }
+                *reinterpret_cast<float4 *>(y + off) = make_float4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<float4 *>(y + off + 4) = make_float4(o[4], o[5], o[6], o[7]);
+            } else {
+                const int img = fast_div(pix, g.div_ohw);
+                const int rem = pix - img * ohw;
+                const int oh = fast_div(rem, g.div_ow);
+                const int ow = rem - oh * a.OW;
+                const size_t plane = (size_t)a.OH * a.out_row_stride;
+                const size_t opix = (size_t)oh * a.out_row_stride + ow;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int c = c0 + jj;
+                    if (c >= a.Cout) break;
+                    const size_t off = OUT_NHWC ? (size_t)pix * a.Cout + c : ((size_t)img * a.Cout + c) * plane + opix;
+                    y[off] = o[jj] + (res ? res[off] : 0.0f);
+                }
+            }
+        }
+    };
+
+    gather(0);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint64_t dhi = ptx::smem_desc(0u, 16u, 256u, 6u);   // 32-byte swizzle, 8-row groups 256 B apart
+    const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n_mma >> 3) << 17) |
+                           ((uint32_t)(128 >> 4) << 24);
+    const uint32_t sB_u32 = ptx::smem_u32(sB);
+    bool failed = false;
+#pragma unroll 1
+    for (int i = 0; i <= n_local; ++i) {
+        if (i < n_local) {
+            ptx::cp_async_wait<0>();   // this thread's copies of tile i have landed
+            ptx::fence_proxy_async_smem();
+        }
+        ptx::tc_fence_before();
+        if (__syncthreads_or(failed)) break;
+        ptx::tc_fence_after();
+        if (i < n_local && t == 0) {
+            const uint32_t stage = sA_u32 + (uint32_t)((i & 1) * kStage);
+            const uint32_t acc = tmem + (uint32_t)((i & 1) * n_mma);
+            for (int k = 0; k < kslices; ++k) {
+                const uint64_t ad = dhi | (uint64_t)(((stage + (uint32_t)(k * kSliceA)) & 0x3FFFFu) >> 4);
+                const uint64_t bd = dhi | (uint64_t)(((sB_u32 + (uint32_t)(k * kSliceB)) & 0x3FFFFu) >> 4);
+                ptx::mma_tf32(acc, ad, bd, idesc, k > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(ptx::smem_u32(&bars[i & 1]));
+        }
+        if (i > 0) {
+            const int j = i - 1;
+            bool ok = ptx::mbar_wait_bounded(ptx::smem_u32(&bars[j & 1]), (uint32_t)((j >> 1) & 1), kStemWaitNs);
+            ok = __all_sync(0xffffffffu, ok);   // warp-uniform before .sync.aligned loads
+            if (!ok) {
+                failed = true;
+                if (lane == 0) atomicOr(status, 1u);
+            } else {
+                ptx::tc_fence_after();
+                epilogue(j, tmem);
+            }
+        }
+        // Stage (i + 1) % 2 was read by the MMAs of tile i - 1, complete above.
+        if (i < n_local) gather(i + 1);
+    }
+    ptx::cp_async_wait<0>();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, ncols);
+    }
+}
+
 }  // namespace
 
 bool stem_uses_tensor_cores(int kind, int in_nhwc, int c_pad, int ks, int cout, long long pixels) {
-    return (kind == 1 || kind == 2) && in_nhwc && c_pad == 4 && ks <= 3 && cout <= 64 && pixels < kStemTcMaxPixels;
+    return (kind == 1 || kind == 2 || kind == 3) && in_nhwc && c_pad == 4 && ks <= 3 && cout <= 64 &&
+           pixels < kStemTcMaxPixels;
 }
 
 namespace {
@@ -799,6 +983,15 @@ cudaError_t launch_stem_tc_as(const StemLaunch &L, int n_mma, StemTcGeom g, int 
     return launch_kernel(kern, grid, 256, kStemTcSmemBytes, s, L, n_mma, g, status);
 }
 
+template <bool OUT_NHWC>
+cudaError_t launch_stem_tf32(const StemLaunch &L, int n_mma, StemTcGeom g, int grid, cudaStream_t s,
+                             unsigned int *status) {
+    auto kern = stem_tc_tf32_kernel<OUT_NHWC>;
+    const cudaError_t e = set_max_dyn_smem(kern, kStemTf32SmemBytes);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(kern, grid, 256, kStemTf32SmemBytes, s, L, n_mma, g, status);
+}
+
 cudaError_t launch_stem_tc(const StemLaunch &L, cudaStream_t s) {
     unsigned int *status = device_status_word();
     if (!status) return cudaErrorInvalidValue;
@@ -809,8 +1002,11 @@ cudaError_t launch_stem_tc(const StemLaunch &L, cudaStream_t s) {
     g.n_tiles = (int)((total + 127) / 128);
     g.div_ohw = make_fastdiv((uint32_t)(L.OH * L.OW));
     g.div_ow = make_fastdiv((uint32_t)L.OW);
-    const int grid = std::min(g.n_tiles, kNumSMs * stem_tc_ctas_per_sm(L.Cout));
+    const int grid = std::min(g.n_tiles, kNumSMs * stem_tc_ctas_per_sm(L.Cout, L.tf32));
     const int n_mma = (L.Cout + 15) / 16 * 16;
+    if (L.tf32)
+        return L.out_nhwc ? launch_stem_tf32<true>(L, n_mma, g, grid, s, status)
+                          : launch_stem_tf32<false>(L, n_mma, g, grid, s, status);
     const bool pairs = L.KS == 3 && L.stride == 2 && L.pad == 1 && (L.W & 1) == 0;
     if (L.out_nhwc)
         return pairs ? launch_stem_tc_as<true, true>(L, n_mma, g, grid, s, status)
@@ -823,7 +1019,7 @@ cudaError_t launch_stem_tc(const StemLaunch &L, cudaStream_t s) {
 
 cudaError_t launch_stem(const StemLaunch &L, cudaStream_t s) {
     if (L.N == 0) return cudaSuccess;
-    if (stem_uses_tensor_cores(L.kind, L.in_nhwc, L.c_pad, L.KS, L.Cout, (long long)L.N * L.OH * L.OW))
+    if (stem_uses_tensor_cores(L.tf32 ? 3 : L.kind, L.in_nhwc, L.c_pad, L.KS, L.Cout, (long long)L.N * L.OH * L.OW))
         return launch_stem_tc(L, s);
     switch (L.kind) {
         case 0: return launch_cout<0>(L, s);

@@ -288,3 +288,26 @@ def test_split_k_with_residual_and_two_inputs(cuda_lib):
         again = nhwc_to_nchw(layer(xa, residual=rr, x_b=xb).float().cpu().numpy())
         assert np.array_equal(again, y)
 
+
+
+@pytest.mark.parametrize("out_layout", [B.CBS_NHWC, B.CBS_NCHW])
+@pytest.mark.parametrize("shape", [
+    (2, 3, 16, 3, 2, 38, 38),      # the stem's shape, ragged last tile
+    (2, 3, 16, 3, 2, 37, 37),      # odd width
+    (1, 4, 32, 3, 1, 19, 19),      # stride 1
+    (3, 1, 48, 1, 1, 9, 9),        # 1x1: one K slice
+    (1, 2, 64, 2, 2, 50, 34),      # 2x2 filter (4 taps), C_out 64
+    (1, 3, 20, 3, 2, 22, 22),      # C_out 20: per-channel stores
+    (4, 3, 16, 3, 2, 160, 160),    # several tiles per persistent CTA
+])
+def test_tensor_core_stem_tf32(cuda_lib, out_layout, shape):
+    """TF32 layers with at most 4 input channels and k <= 3 run on the TF32
+    tensor-core stem (taps straight into 32-byte-swizzled K slices)."""
+    n, c_in, c_out, k, stride, h, w = shape
+    spec = wl.LayerSpec(c_in, c_out, k, stride, h, w)
+    x, p = wl.layer_inputs(spec, n, layer_index=5)
+    y, layer = run_tc(spec, x, p, B.CBS_TF32, out_layout=out_layout)
+    pl = layer.plan
+    assert pl.variant == B.CBS_VARIANT_STEM and pl.block_m == 128 and pl.threads == 256
+    assert pl.grid_ctas == min(pl.m_tiles, 152 * 4)
+    check(y, spec, x, p, "tf32", shape)
