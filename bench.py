@@ -112,9 +112,13 @@ WORKLOADS = {
     "layer_list_bf16_n16_residual": dict(kind="list", layers=wl.LAYER_LIST, n=16, prec="bf16", residual=True),
     # asymmetric activations: input codes with zero point -20, outputs with -100
     "layer_list_int8_n16_asym": dict(kind="list", layers=wl.LAYER_LIST, n=16, prec="int8", zero_points=(-20, -100)),
+    # FP32 with NHWC activations: layers with enough pixel tiles run the
+    # 3xTF32 tensor-core kernel (the FP32 bar), the stem its direct kernel.
+    "layer_list_fp32_n16_nhwc": dict(kind="list", layers=wl.LAYER_LIST, n=16, prec="fp32", layout="nhwc"),
 }
 EXTRA_DEFAULT = ("layer_list_bf16_n16", "layer_list_tf32_n16", "layer_list_int8_n16", "chain_fp32_n1",
-                 "chain_bf16_n16", "layer_list_bf16_n16_residual", "layer_list_int8_n16_asym")
+                 "chain_bf16_n16", "layer_list_bf16_n16_residual", "layer_list_int8_n16_asym",
+                 "layer_list_fp32_n16_nhwc")
 
 
 # DRAM traffic of the dominant kernel over one step of a workload, from one
@@ -130,6 +134,10 @@ TRAFFIC = {
 # Variant of the dominant kernel per precision (the direct small-channel
 # kernel runs the stem and is reported per layer, not here).
 DOMINANT_VARIANT = {"fp32": 0, "tf32": 1, "bf16": 2, "int8": 3}
+VARIANT_NAMES = {0: "simt_fp32", 1: "tc_tf32", 2: "tc_bf16", 3: "tc_int8", 4: "stem", 5: "tc_tf32x3"}
+KERNEL_NAMES = {0: "simt_conv_kernel (FP32 FMA)", 1: "tc_conv_kernel<TF32>", 2: "tc_conv_kernel<BF16>",
+                3: "tc_conv_staged_kernel<INT8>", 5: "tc_conv_staged_kernel<TF32X3> (FP32 as 3 TF32 products)"}
+X3_VARIANT = 5
 
 
 def sources_digest(files) -> str:
@@ -183,10 +191,14 @@ class ListWorkload:
         self.s_y = int8_scales() if self.prec == "int8" else [None] * len(self.specs)
         self.res = [bool(cfg.get("residual")) and s.c_in == s.c_out and s.stride == 1 for s in self.specs]
         z_x, z_y = cfg.get("zero_points", (0, 0))
+        # FP32 reads NCHW as given unless the workload asks for NHWC; the
+        # other precisions read the packed NHWC form.
+        self.nhwc = self.prec != "fp32" or cfg.get("layout") == "nhwc"
+        lay = B.CBS_NHWC if self.nhwc else B.CBS_NCHW
         for i, spec in enumerate(self.specs):
             x, p = wl.layer_inputs(spec, self.n, seed=0, layer_index=i)
             desc = make_desc(self.n, spec.c_in, spec.h, spec.width, spec.c_out, spec.k, spec.stride, spec.pad,
-                             prec=cp, residual=int(self.res[i]), zero_point_x=z_x, zero_point_y=z_y)
+                             prec=cp, in_layout=lay, residual=int(self.res[i]), zero_point_x=z_x, zero_point_y=z_y)
             self.layers.append(FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, s_x=s_x,
                                                device=device))
             host_x.append(x)
@@ -199,7 +211,7 @@ class ListWorkload:
         packed = []
         for layer, x in zip(self.layers, host_x):
             xd = torch.from_numpy(x).to(device)
-            packed.append(layer.pack_input(xd) if (self.prec != "fp32") else xd)
+            packed.append(layer.pack_input(xd) if self.nhwc else xd)
         torch.cuda.synchronize()
         self.xs = [[t.clone() for t in packed] for _ in range(self.R)]
         self.ys = [[layer.empty_y() for layer in self.layers] for _ in range(self.R)]
@@ -341,7 +353,11 @@ def measure(name, steps, warmup, device, peaks, sample_clocks=False):
         f, by = sp.flops(n), sp.alg_bytes(n, ab) + extra[j]
         t_c, t_m = f / (peak * 1e12), by / (hbm * 1e9)
         bound = "compute" if t_c >= t_m else "hbm"
+        if layer.plan.variant == X3_VARIANT:   # three TF32 products per multiply-add
+            t_c = f / (peak_for("tf32", peaks)[0] / 3 * 1e12)
+            bound = "compute" if t_c >= t_m else "hbm"
         row = {"layer": j + 1, "shape": f"{sp.c_in}->{sp.c_out} k{sp.k} s{sp.stride} {sp.h}" + (" +r" if extra[j] else ""),
+               "variant": VARIANT_NAMES.get(layer.plan.variant, str(layer.plan.variant)),
                "tile": f"{layer.plan.block_m}x{layer.plan.block_n}", "split_k": layer.plan.split_k,
                "mflop": round(f / 1e6, 2), "alg_mb": round(by / 1e6, 3), "bound": bound,
                "roofline_us": round(max(t_c, t_m) * 1e6, 3)}
@@ -416,18 +432,27 @@ def run_ours(args, rank: int, world: int):
     value = job_tflops(flops_step, world, ms_step)
     rows = head["layers"]
     peak = head["peak_tflops"]
-    kernel = {"fp32": "simt_conv_kernel (FP32 FMA)", "tf32": "tc_conv_kernel<TF32>",
-              "bf16": "tc_conv_kernel<BF16>", "int8": "tc_conv_i8_kernel"}[w.prec]
-    # The dominant kernel: every layer the plan gives to it (all but the stem).
-    dom = [(sp, r) for (sp, layer), r in zip(w.rows(), rows) if layer.plan.variant == DOMINANT_VARIANT[w.prec]]
+    # The dominant kernel: the variant (the stem's kernel aside) with the most
+    # measured time in a step, and every layer the plans give to it.
+    t_by_variant = {}
+    for (sp, layer), r in zip(w.rows(), rows):
+        if layer.plan.variant != B.CBS_VARIANT_STEM:
+            t_by_variant[layer.plan.variant] = t_by_variant.get(layer.plan.variant, 0.0) + r["us"]
+    dom_variant = max(t_by_variant, key=t_by_variant.get) if t_by_variant else DOMINANT_VARIANT[w.prec]
+    kernel = KERNEL_NAMES[dom_variant]
+    dom = [(sp, r) for (sp, layer), r in zip(w.rows(), rows) if layer.plan.variant == dom_variant]
     dom_flops = sum(sp.flops(n) for sp, _ in dom)
     dom_us = sum(r["us"] for _, r in dom)
     achieved = dom_flops / (dom_us * 1e-6) / 1e12
     traffic = traffic_for(args.workload)
-    roofline = {"bound": "alu" if w.prec == "fp32" else "tensor",
+    bound, peak_label = ("alu" if w.prec == "fp32" else "tensor"), head["peak"]
+    if dom_variant == X3_VARIANT:   # FP32 as three TF32 products on the tensor cores
+        peak = round(peak_for("tf32", peaks)[0] / 3, 2)
+        bound, peak_label = "tensor", "tensor: measured bf16 burst x nominal tf32/bf16 (1.1/2.25) / 3 products"
+    roofline = {"bound": bound,
                 "kernel": f"{kernel}, the {len(dom)} launches of one step",
                 "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "peak_source": head["peak"] + f" ({peak_src})",
+                "frac": round(achieved / peak, 4), "peak_source": peak_label + f" ({peak_src})",
                 "traffic": traffic,
                 "traffic_note": ("DRAM bytes of those launches in one step (ncu, cold cache)" if traffic is not None
                                  else "no capture of the current kernel sources"),
@@ -443,7 +468,7 @@ def run_ours(args, rank: int, world: int):
         "dtype": {"fp32": "f32", "tf32": "tf32", "bf16": "bf16", "int8": "int8"}[w.prec],
         "data": "synthetic (seeded N(0,1) inputs, He-init weights, random BN statistics)",
         "config": {"workload": args.workload, "layers": len(rows), "batch": n,
-                   "layout": "NCHW" if w.prec == "fp32" else "NHWC", "l2": head["l2"],
+                   "layout": "NHWC" if getattr(w, "nhwc", w.prec != "fp32") else "NCHW", "l2": head["l2"],
                    "timing": ("K steps captured in one CUDA graph of programmatic dependent launches, CUDA events around "
                               "its replay on the launching stream; per-launch durations from a replay of the same K steps "
                               "captured with an event between launches"),

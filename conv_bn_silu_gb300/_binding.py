@@ -25,6 +25,7 @@ CBS_NCHW, CBS_NHWC = 0, 1
 CBS_FP32, CBS_TF32, CBS_BF16, CBS_INT8 = 0, 1, 2, 3
 CBS_VARIANT_SIMT_FP32, CBS_VARIANT_TC_TF32, CBS_VARIANT_TC_BF16, CBS_VARIANT_TC_INT8 = 0, 1, 2, 3
 CBS_VARIANT_STEM = 4
+CBS_VARIANT_TC_TF32X3 = 5
 CBS_ACT_SILU, CBS_ACT_IDENTITY = 0, 1
 CBS_LAUNCH_PDL = 1
 

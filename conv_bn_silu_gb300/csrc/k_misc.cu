@@ -42,6 +42,20 @@ __global__ void __launch_bounds__(kFoldThreads) fold_kernel(const FoldLaunch a) 
         if (threadIdx.x == 0) static_cast<float *>(a.bias)[co] = b_fold;
         return;
     }
+    if (a.variant == CBS_VARIANT_TC_TF32X3) {
+        // Head = w' with its low 13 mantissa bits cleared (a TF32 number) in
+        // rows 0..C_out-1; tail = w' - head (exact) in rows C_out..2 C_out-1.
+        float *out = static_cast<float *>(a.w_packed);
+        for (int k = threadIdx.x; k < kpad; k += blockDim.x) {
+            const int tap = k / a.c_in_pad, ci = k - tap * a.c_in_pad;
+            const float v = ci < a.C_in ? __fmul_rn(wrow[ci * KK + tap], s_c) : 0.0f;
+            const float head = __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
+            out[(size_t)co * kpad + k] = head;
+            out[(size_t)(a.C_out + co) * kpad + k] = __fsub_rn(v, head);
+        }
+        if (threadIdx.x == 0) static_cast<float *>(a.bias)[co] = b_fold;
+        return;
+    }
     if (a.variant == CBS_VARIANT_TC_TF32 || a.variant == CBS_VARIANT_TC_BF16) {
         for (int k = threadIdx.x; k < kpad; k += blockDim.x) {
             const int tap = k / a.c_in_pad, ci = k - tap * a.c_in_pad;

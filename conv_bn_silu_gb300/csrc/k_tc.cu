@@ -143,9 +143,14 @@ __device__ __forceinline__ float silu_fast(float z) {
     return fmaf(h, t, h);
 }
 
+// SiLU(z) = z / (1 + e^-z) with the hardware exp and a fast division:
+// relative error near 1e-6, inside the FP32 bar (the 3xTF32 variant).
+__device__ __forceinline__ float silu_precise(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
 // Bias + SiLU + store of 16 consecutive output channels of one pixel.
+template <bool PRECISE = false>
 __device__ __forceinline__ float activate(const TcParams &p, float z) {
-    return p.act == CBS_ACT_IDENTITY ? z : silu_fast(z);
+    return p.act == CBS_ACT_IDENTITY ? z : (PRECISE ? silu_precise(z) : silu_fast(z));
 }
 
 // Adds the residual of 16 consecutive channels nbase.. of one output element
@@ -237,7 +242,7 @@ __device__ __forceinline__ void stage16(const TcParams &p, uint32_t blk, int row
     }
 }
 
-template <int KIND>
+template <int KIND, bool PRECISE = false>
 __device__ __forceinline__ void epi_store16(const TcParams &p, const float *bias, int m, int img, int oh, int ow,
                                             int nbase, const uint32_t (&v)[16]) {
     float bv[16];
@@ -245,7 +250,7 @@ __device__ __forceinline__ void epi_store16(const TcParams &p, const float *bias
     load_bias16(p, bias, nbase, bv);
     float o[16];
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj) o[jj] = activate(p, __uint_as_float(v[jj]) + bv[jj]);
+    for (int jj = 0; jj < 16; ++jj) o[jj] = activate<PRECISE>(p, __uint_as_float(v[jj]) + bv[jj]);
     if (p.residual) {
         if (p.out_nhwc) {
             add_residual16_nhwc<KIND>(p, m, nbase, o);
@@ -873,18 +878,33 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t u_lo, uint32_t u_hi) {
 }
 
 
-// Persistent INT8 kernel.  Warps 0-1: TMA producers; warp 2: TMEM + MMA
-// issuer; warps 3-10: epilogue; warps 11-14: int8 -> bf16 converters.
+// What the converter warps of tc_conv_staged_kernel make of the staging tile.
+enum StagedKind { kStagedI8 = 0, kStagedX3 = 1 };
+
+// Persistent kernel whose A operand passes through a staging tile and
+// converter warps on its way to the tensor cores.  Warps 0-1: TMA producers;
+// warp 2: TMEM + MMA issuer; warps 3-10: epilogue; warps 11-14: converters.
+//   kStagedI8: int8 codes widened to bf16 operands (exact), exact integer
+//              sums in chunks, the specified requantisation.
+//   kStagedX3: fp32 activations split into a TF32 head (written back in
+//              place, so the tensor cores see it exactly) and the remainder
+//              (the tail); the fold splits the weights the same way.  Each K
+//              slice runs three kind::tf32 MMAs (tail x head, head x tail,
+//              head x head) into one FP32 accumulator, which drops only the
+//              tail x tail term: FP32-level accuracy on the tensor cores.
+template <int SK>
 __global__ void __launch_bounds__(kThreadsI8, 1)
-tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
-                  const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                      const __grid_constant__ CUtensorMap tmB, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t *base_ptr = smem_raw + (base - raw_addr);
     const int S = p.stages;
-    // Stage s holds kg K steps: [kg x operand A bf16 | kg x operand B bf16 |
-    // kg x staging A int8], each block 1024-aligned.
+    // Stage s holds kg K steps, each block 1024-aligned:
+    //   INT8: [kg x operand A bf16 | kg x operand B bf16 | kg x staging A int8];
+    //   X3:   [kg x A tail | kg x B head | kg x B tail | kg x staging A fp32,
+    //          the A head once converted].
     // Barriers: raw_full[S], conv_done[S], free[S], acc_full[2], acc_empty[2], drain.
     const uint32_t bars = base + S * p.stage_bytes;
     uint64_t *bar_ptr = reinterpret_cast<uint64_t *>(base_ptr + S * p.stage_bytes);
@@ -898,8 +918,9 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     auto acce_bar = [&](int a) { return bars + 8u * (3 * S + 2 + a); };
     const uint32_t drain_bar = bars + 8u * (3 * S + 4);
     const int kg = p.kg;
+    constexpr int NB = SK == kStagedX3 ? 2 : 1;                      // weight tiles per K step
     const int op_b_off = kg * p.a_bytes;                              // a_bytes = 128 x RB: 1 KB multiple
-    const int stg_off = op_b_off + kg * p.b_tile_stride;
+    const int stg_off = op_b_off + NB * kg * p.b_tile_stride;
     const int stg_stride = (p.stg_bytes + 1023) & ~1023;
     const int nstage = p.ksteps / kg;
 
@@ -962,11 +983,14 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         break;
                     }
                     const uint32_t sb = base + s * p.stage_bytes;
-                    if (lane == 0) ptx::mbar_arrive_expect_tx(raw_bar(s), (uint32_t)(kg * (p.stg_bytes + p.b_bytes)));
+                    if (lane == 0)
+                        ptx::mbar_arrive_expect_tx(raw_bar(s), (uint32_t)(kg * (p.stg_bytes + NB * p.b_bytes)));
                     __syncwarp();
-                    if (lane < 2 * kg) {
+                    if (lane < (1 + NB) * kg) {
+                        // Lanes 0..kg-1: A boxes; then kg B boxes (X3: kg heads, kg tails).
                         const bool is_a = lane < kg;
-                        const int kk = is_a ? lane : lane - kg;
+                        const int kk = is_a ? lane : (lane - kg) % kg;
+                        const int tail = is_a ? 0 : (lane - kg) / kg;
                         const int i = st * kg + kk;
                         const int tap = i / p.cblocks, cb = i - tap * p.cblocks;
                         if (is_a) {
@@ -981,8 +1005,9 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             else
                                 ptx::tma_load_2d(dst, tm, raw_bar(s), c0, m0);
                         } else {
-                            ptx::tma_load_2d(sb + op_b_off + kk * p.b_tile_stride, &tmB, raw_bar(s),
-                                             tap * p.c_in_pad + cb * p.CB, n0);
+                            // X3 weight tails are rows C_out.. of the packed weights.
+                            ptx::tma_load_2d(sb + op_b_off + (tail * kg + kk) * p.b_tile_stride, &tmB, raw_bar(s),
+                                             tap * p.c_in_pad + cb * p.CB, n0 + tail * p.C_out);
                         }
                     }
                     last_g = g;
@@ -1018,10 +1043,21 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint32_t sb = base + s * p.stage_bytes;
                     for (int kk = 0; kk < kg; ++kk) {
                         const int i = st * kg + kk;
-                        const int chunk = i / p.kpc;
-                        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_stride + chunk * p.chunk_stride);
-                        issue_kstep<kBF16>(d_tmem, dhi, sb + kk * p.a_bytes, sb + op_b_off + kk * p.b_tile_stride, p.idesc,
-                                           kslices, (i % p.kpc) == 0);
+                        if constexpr (SK == kStagedX3) {
+                            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_stride);
+                            const uint32_t a_head = sb + stg_off + kk * stg_stride, a_tail = sb + kk * p.a_bytes;
+                            const uint32_t b_head = sb + op_b_off + kk * p.b_tile_stride;
+                            const uint32_t b_tail = sb + op_b_off + (kg + kk) * p.b_tile_stride;
+                            issue_kstep<kTF32>(d_tmem, dhi, a_tail, b_head, p.idesc, kslices, i == 0);
+                            issue_kstep<kTF32>(d_tmem, dhi, a_head, b_tail, p.idesc, kslices, false);
+                            issue_kstep<kTF32>(d_tmem, dhi, a_head, b_head, p.idesc, kslices, false);
+                        } else {
+                            const int chunk = i / p.kpc;
+                            const uint32_t d_tmem =
+                                tmem_base + (uint32_t)(acc * p.acc_stride + chunk * p.chunk_stride);
+                            issue_kstep<kBF16>(d_tmem, dhi, sb + kk * p.a_bytes, sb + op_b_off + kk * p.b_tile_stride,
+                                               p.idesc, kslices, (i % p.kpc) == 0);
+                        }
                     }
                     ptx::mma_commit(free_bar(s));
                 }
@@ -1029,6 +1065,53 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 ptx::mma_commit(accf_bar(acc));
             }
             ptx::mma_commit(drain_bar);
+        }
+    } else if (warp >= kConvFirstI8 && SK == kStagedX3) {
+        // Converters: thread (warp - kConvFirstI8) * 32 + lane splits row `row`
+        // of every staging tile: head = the value with its low 13 mantissa
+        // bits cleared (a TF32 number), tail = value - head (exact).
+        const int row = (warp - kConvFirstI8) * 32 + lane;
+        int g = 0;
+        for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
+            bool ok = true;
+            for (int st = 0; st < nstage; ++st, ++g) {
+                const int s = g % S, u = g / S;
+                if (!ptx::mbar_wait_bounded(raw_bar(s), u & 1, kWaitLimitNs)) {
+                    abort_now(p, abort_flag);
+                    ok = false;
+                    break;
+                }
+                const uint32_t sb = base + s * p.stage_bytes;
+                for (int kk = 0; kk < kg; ++kk) {
+                    const uint32_t head_row = sb + stg_off + kk * stg_stride + row * p.RB;
+                    const uint32_t tail_row = sb + kk * p.a_bytes + row * p.RB;
+                    for (int c = 0; c < p.RB; c += 16) {
+                        const uint32_t ha = swz(head_row + c, p.op_mask);
+                        uint32_t w[4];
+                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                                     : "r"(ha));
+                        uint32_t h[4];
+                        float l[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            h[q] = w[q] & 0xFFFFE000u;
+                            l[q] = __fsub_rn(__uint_as_float(w[q]), __uint_as_float(h[q]));
+                        }
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(ha), "r"(h[0]), "r"(h[1]),
+                                     "r"(h[2]), "r"(h[3])
+                                     : "memory");
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(swz(tail_row + c, p.op_mask)),
+                                     "f"(l[0]), "f"(l[1]), "f"(l[2]), "f"(l[3])
+                                     : "memory");
+                    }
+                }
+                // Make the generic-proxy writes visible to the tensor cores.
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(conv_bar(s));
+            }
+            if (!ok) break;
         }
     } else if (warp >= kConvFirstI8) {
         // Converters: thread (warp - kConvFirstI8) * 32 + lane widens row `row`
@@ -1147,43 +1230,53 @@ tc_conv_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 ow = rem - oh * p.OW;
             }
             const uint32_t t_row = tmem_base + (uint32_t)(acc * p.acc_stride) + ((uint32_t)(32 * q) << 16);
-            for (int c0 = 16 * half; c0 < p.BN; c0 += 32) {
-                const int nbase = n0 + c0;
-                int accv[16];
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) accv[jj] = nbase + jj < p.C_out ? __ldg(p.bias_i32 + nbase + jj) : 0;
-                for (int ch = 0; ch < p.nchunks; ++ch) {
+            if constexpr (SK == kStagedX3) {
+                for (int c0 = 16 * half; c0 < p.BN; c0 += 32) {
                     uint32_t v[16];
-                    ptx::tmem_ld16(t_row + (uint32_t)(ch * p.chunk_stride + c0), v);
+                    ptx::tmem_ld16(t_row + (uint32_t)c0, v);
                     ptx::tmem_ld_wait();
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) accv[jj] += __float2int_rn(__uint_as_float(v[jj]));
+                    if (m >= p.M || n0 + c0 >= p.C_out) continue;
+                    epi_store16<kTF32, true>(p, p.bias, m, img, oh, ow, n0 + c0, v);
                 }
-                if (m >= p.M || nbase >= p.C_out) continue;
-                uint32_t qw[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int qv = requant_i8(accv[jj], nbase + jj < p.C_out ? __ldg(p.m_c + nbase + jj) : 0.0f,
-                                              p.inv_s_y, p.zp_y);
-                    qw[jj >> 2] |= (uint32_t)(uint8_t)(int8_t)qv << (8 * (jj & 3));
-                }
-                if (p.out_nhwc) {
-                    int8_t *yr = static_cast<int8_t *>(p.y) + (size_t)m * p.C_out + nbase;
-                    if (nbase + 16 <= p.C_out && (p.C_out & 15) == 0) {
-                        *reinterpret_cast<uint4 *>(yr) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-                    } else {
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj)
-                            if (nbase + jj < p.C_out) yr[jj] = (int8_t)(qw[jj >> 2] >> (8 * (jj & 3)));
+            } else {
+                for (int c0 = 16 * half; c0 < p.BN; c0 += 32) {
+                    const int nbase = n0 + c0;
+                    int accv[16];
+    #pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) accv[jj] = nbase + jj < p.C_out ? __ldg(p.bias_i32 + nbase + jj) : 0;
+                    for (int ch = 0; ch < p.nchunks; ++ch) {
+                        uint32_t v[16];
+                        ptx::tmem_ld16(t_row + (uint32_t)(ch * p.chunk_stride + c0), v);
+                        ptx::tmem_ld_wait();
+    #pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) accv[jj] += __float2int_rn(__uint_as_float(v[jj]));
                     }
-                } else {
-                    const size_t plane = (size_t)p.OH * p.out_row_stride;
-                    const size_t pix = (size_t)oh * p.out_row_stride + ow;
-#pragma unroll
+                    if (m >= p.M || nbase >= p.C_out) continue;
+                    uint32_t qw[4] = {0u, 0u, 0u, 0u};
+    #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
-                        if (nbase + jj >= p.C_out) continue;
-                        static_cast<int8_t *>(p.y)[((size_t)img * p.C_out + nbase + jj) * plane + pix] =
-                            (int8_t)(qw[jj >> 2] >> (8 * (jj & 3)));
+                        const int qv = requant_i8(accv[jj], nbase + jj < p.C_out ? __ldg(p.m_c + nbase + jj) : 0.0f,
+                                                  p.inv_s_y, p.zp_y);
+                        qw[jj >> 2] |= (uint32_t)(uint8_t)(int8_t)qv << (8 * (jj & 3));
+                    }
+                    if (p.out_nhwc) {
+                        int8_t *yr = static_cast<int8_t *>(p.y) + (size_t)m * p.C_out + nbase;
+                        if (nbase + 16 <= p.C_out && (p.C_out & 15) == 0) {
+                            *reinterpret_cast<uint4 *>(yr) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+                        } else {
+    #pragma unroll
+                            for (int jj = 0; jj < 16; ++jj)
+                                if (nbase + jj < p.C_out) yr[jj] = (int8_t)(qw[jj >> 2] >> (8 * (jj & 3)));
+                        }
+                    } else {
+                        const size_t plane = (size_t)p.OH * p.out_row_stride;
+                        const size_t pix = (size_t)oh * p.out_row_stride + ow;
+    #pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            if (nbase + jj >= p.C_out) continue;
+                            static_cast<int8_t *>(p.y)[((size_t)img * p.C_out + nbase + jj) * plane + pix] =
+                                (int8_t)(qw[jj >> 2] >> (8 * (jj & 3)));
+                        }
                     }
                 }
             }
@@ -1259,7 +1352,9 @@ int next_pow2(int v) {
     return p;
 }
 
-int elem_bytes_of(int variant) { return variant == CBS_VARIANT_TC_TF32 ? 4 : 2; }
+int elem_bytes_of(int variant) {
+    return variant == CBS_VARIANT_TC_TF32 || variant == CBS_VARIANT_TC_TF32X3 ? 4 : 2;
+}
 
 }  // namespace
 
@@ -1446,6 +1541,7 @@ bool tc_config(const cbs_layer_desc &d, long long M, int oh, int RB, int ksteps,
 cbs_status plan_tc(cbs_plan_t &p) {
     const cbs_layer_desc &d = p.desc;
     const bool i8 = p.variant == CBS_VARIANT_TC_INT8;
+    const bool x3 = p.variant == CBS_VARIANT_TC_TF32X3;   // FP32 through the staged kernel
     const bool tf32 = p.variant == CBS_VARIANT_TC_TF32;
     const int eb = i8 ? 1 : elem_bytes_of(p.variant);
     int RB, CB, nchunks = 1;
@@ -1469,17 +1565,19 @@ cbs_status plan_tc(cbs_plan_t &p) {
     }
     p.k_gemm = d.k * d.k * p.c_in_pad;
     p.x_bytes = (size_t)d.n * d.h * d.w * p.c_in_pad * eb;
-    p.w_packed_bytes = (size_t)d.c_out * p.k_gemm * (tf32 ? 4 : 2);
+    // X3: weight heads in rows 0..C_out-1, tails in rows C_out..2 C_out-1.
+    p.w_packed_bytes = (size_t)d.c_out * p.k_gemm * (x3 ? 8 : (tf32 ? 4 : 2));
     if (d.pad > 127 || (p.oh - 1) * d.stride - d.pad - d.h + 1 < -128 || (p.ow - 1) * d.stride - d.pad - d.w + 1 < -128)
         return fail(CBS_ERR_UNSUPPORTED, "padding outside the im2col corner range");
-    if (d.force_split_k > 1 && i8) return fail(CBS_ERR_UNSUPPORTED, "split-K is not built for the INT8 kernel");
+    if (d.force_split_k > 1 && (i8 || x3))
+        return fail(CBS_ERR_UNSUPPORTED, "split-K is not built for the staged (INT8, 3xTF32) kernel");
     const long long M = (long long)d.n * p.oh * p.ow;
     const int ksteps = d.k * d.k * (p.c_in_pad / CB);
     p.block_k = CB;
     p.split_k = 1;
     p.workspace_bytes = 0;
 
-    if (i8) {
+    if (i8 || x3) {
         p.m_tiles = ceil_div(M, kBM);
         // TMEM holds two accumulator buffers of nchunks * next_pow2(BN)
         // columns (rounded to a power of two): nchunks * next_pow2(BN) <= 256.
@@ -1509,10 +1607,12 @@ cbs_status plan_tc(cbs_plan_t &p) {
         p.block_n = BN;
         p.n_tiles = ceil_div(d.c_out, BN);
         p.b_resident = 0;
-        // One K step: bf16 operand A, bf16 weights, int8 staging tile.  The
-        // MMA issuer waits twice per stage, so a stage carries the most K
-        // steps (up to 4, dividing the K steps) that still leave 3 stages.
-        const int kstep_bytes = kBM * RB + round_up(BN * RB, 1024) + round_up(kBM * CB, 1024);
+        // One K step: operand A (INT8: bf16; X3: the tail), the weights
+        // (X3: head and tail), the staging tile (int8 codes; X3: fp32, the
+        // head once converted).  The MMA issuer waits twice per stage, so a
+        // stage carries the most K steps (up to 4, dividing the K steps)
+        // that still leave 3 stages.
+        const int kstep_bytes = kBM * RB + (x3 ? 2 : 1) * round_up(BN * RB, 1024) + round_up(kBM * (x3 ? RB : CB), 1024);
         int kg = 1;
         for (int c = 4; c >= 1; --c) {
             if (d.force_k_group > 0 && c != d.force_k_group) continue;
@@ -1529,7 +1629,7 @@ cbs_status plan_tc(cbs_plan_t &p) {
         if (stages > 32) stages = 32;
         if (stages < 2) {
             if (2 * stage > kSmemBudget)
-                return fail(CBS_ERR_UNSUPPORTED, "INT8: two stages of %d K steps do not fit shared memory", kg);
+                return fail(CBS_ERR_UNSUPPORTED, "two stages of %d K steps do not fit shared memory", kg);
             stages = 2;
         }
         int nprod = kMaxProducersI8;
@@ -1636,14 +1736,16 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     const DriverFns &fns = driver_fns();
     if (!fns.ok) return fail(CBS_ERR_CUDA, "cannot resolve cuTensorMapEncode* from the driver");
     const bool i8 = pl.variant == CBS_VARIANT_TC_INT8;
-    if (pl.variant != CBS_VARIANT_TC_TF32 && pl.variant != CBS_VARIANT_TC_BF16 && !i8)
+    const bool x3 = pl.variant == CBS_VARIANT_TC_TF32X3;
+    const bool staged = i8 || x3;                                  // tc_conv_staged_kernel
+    const bool f32ops = pl.variant == CBS_VARIANT_TC_TF32 || x3;   // 32-bit operands
+    if (pl.variant != CBS_VARIANT_TC_TF32 && pl.variant != CBS_VARIANT_TC_BF16 && !staged)
         return fail(CBS_ERR_UNSUPPORTED, "variant %d", pl.variant);
     const int eb_x = i8 ? 1 : elem_bytes_of(pl.variant);          // activation bytes in memory
-    const int eb_w = pl.variant == CBS_VARIANT_TC_TF32 ? 4 : 2;   // operand bytes in shared memory
-    const CUtensorMapDataType dt_x = pl.variant == CBS_VARIANT_TC_TF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+    const int eb_w = f32ops ? 4 : 2;                              // operand bytes in shared memory
+    const CUtensorMapDataType dt_x = f32ops ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                      : i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const CUtensorMapDataType dt_w = pl.variant == CBS_VARIANT_TC_TF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapDataType dt_w = f32ops ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const int CB = pl.block_k;           // channels per K step
     const int RB = CB * eb_w;            // operand row bytes
     const int XB = CB * eb_x;            // activation row bytes as loaded
@@ -1666,20 +1768,21 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     }
     P.BN = BN; P.stages = pl.stages;
     P.m_tiles = pl.m_tiles; P.n_tiles = pl.n_tiles;
-    const int mmul = i8 ? 1 : pl.block_m / kBM;
+    const int mmul = staged ? 1 : pl.block_m / kBM;
     if (pl.block_m != kBM * mmul || mmul < 1 || mmul > 2) return fail(CBS_ERR_PLAN_MISMATCH, "block_m %d", pl.block_m);
     P.mmul = mmul;
-    P.win = i8 ? 0 : pl.window;
+    P.win = staged ? 0 : pl.window;
     P.split = pl.split_k < 1 ? 1 : pl.split_k;
     if (P.split > 1) {
-        if (i8 || pl.window || pl.b_resident) return fail(CBS_ERR_PLAN_MISMATCH, "split-K plan with windowed A or resident weights");
+        if (staged || pl.window || pl.b_resident)
+            return fail(CBS_ERR_PLAN_MISMATCH, "split-K plan with windowed A, resident weights or staged A");
         if (!workspace) return fail(CBS_ERR_WORKSPACE, "split-K plan without a workspace");
         const size_t counter_bytes = (size_t)round_up(pl.m_tiles * pl.n_tiles * kSplitCounterSlots * 4, 256);
         P.counters = static_cast<unsigned int *>(workspace);
         P.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + counter_bytes);
     }
     P.kg = P.win ? 1 : pl.k_group;
-    P.b_res = i8 ? 0 : pl.b_resident;
+    P.b_res = staged ? 0 : pl.b_resident;
     P.SB = (P.win && !P.b_res) ? pl.k_group : 0;
     if (P.kg < 1 || P.ksteps % P.kg) return fail(CBS_ERR_PLAN_MISMATCH, "k_group %d", pl.k_group);
     if (P.win && !P.b_res && (P.SB < 1 || P.SB > 32)) return fail(CBS_ERR_PLAN_MISMATCH, "weight ring %d", P.SB);
@@ -1697,11 +1800,11 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
         P.a_box_bytes = wg.R_box * wg.Wp * RB;
         if (pl.m_tiles != d.n * wg.tiles_per_img) return fail(CBS_ERR_PLAN_MISMATCH, "window tiles");
     }
-    if (i8) {
+    if (staged) {
         int nprod = kMaxProducersI8;
         while (nprod > 1 && (pl.stages < 2 * nprod || pl.stages % nprod != 0)) nprod /= 2;
         P.nprod = nprod;
-        P.stage_bytes = P.kg * (P.a_bytes + P.b_tile_stride + round_up(kBM * CB, 1024));
+        P.stage_bytes = P.kg * (P.a_bytes + (x3 ? 2 : 1) * P.b_tile_stride + round_up(kBM * XB, 1024));
         if (1024 + pl.stages * P.stage_bytes + 8 * (3 * pl.stages + 5) + 16 > pl.smem_bytes)
             return fail(CBS_ERR_PLAN_MISMATCH, "plan's shared memory does not hold its stages");
     } else {
@@ -1734,6 +1837,12 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
         P.zp_y = d.zero_point_y;
         P.in_h = d.h;
         P.in_w = d.w;
+    } else if (x3) {
+        P.stg_bytes = kBM * XB;     // fp32 staging rows, swizzled like the operands (XB = RB)
+        P.kpc = P.ksteps;
+        P.nchunks = 1;
+        P.stg_mask = P.op_mask = RB == 128 ? 7u : RB == 64 ? 3u : 1u;
+        P.bias = static_cast<const float *>(bias);
     } else {
         P.nchunks = 1;
         P.bias = static_cast<const float *>(bias);
@@ -1741,7 +1850,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     P.im2col = !(d.k == 1 && d.stride == 1 && d.pad == 0);
     P.out_nhwc = d.out_layout == CBS_NHWC;
     P.out_row_stride = pl.out_row_stride;
-    const uint32_t fmt = pl.variant == CBS_VARIANT_TC_TF32 ? 2u : 1u;  // TF32 : BF16 operands
+    const uint32_t fmt = f32ops ? 2u : 1u;  // TF32 : BF16 operands
     P.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
     P.swz = desc_swizzle_code(RB);
     // Two accumulator buffers (double buffering across tiles); INT8 chunks
@@ -1819,7 +1928,8 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
         std::memcpy(&tmA2, &tmA, sizeof(tmA));
     }
     {
-        const cuuint64_t dims[2] = {(cuuint64_t)pl.k_gemm, (cuuint64_t)d.c_out};
+        // X3: the weight tails follow the heads as C_out more rows.
+        const cuuint64_t dims[2] = {(cuuint64_t)pl.k_gemm, (cuuint64_t)d.c_out * (x3 ? 2 : 1)};
         const cuuint64_t strides[1] = {(cuuint64_t)pl.k_gemm * eb_w};
         const cuuint32_t box[2] = {(cuuint32_t)CB, (cuuint32_t)BN};
         r = fns.tiled(&tmB, dt_w, 2, const_cast<void *>(w_packed), dims, strides, box, estr1,
@@ -1837,9 +1947,14 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     } else if (pl.variant == CBS_VARIANT_TC_BF16) {
         e = set_max_dyn_smem(tc_conv_kernel<kBF16>, pl.smem_bytes);
         if (e == cudaSuccess) e = launch_kernel(tc_conv_kernel<kBF16>, grid, kThreads, pl.smem_bytes, s, tmA, tmA2, tmB, tmY, P);
+    } else if (i8) {
+        auto kern = tc_conv_staged_kernel<kStagedI8>;
+        e = set_max_dyn_smem(kern, pl.smem_bytes);
+        if (e == cudaSuccess) e = launch_kernel(kern, grid, kThreadsI8, pl.smem_bytes, s, tmA, tmA2, tmB, P);
     } else {
-        e = set_max_dyn_smem(tc_conv_i8_kernel, pl.smem_bytes);
-        if (e == cudaSuccess) e = launch_kernel(tc_conv_i8_kernel, grid, kThreadsI8, pl.smem_bytes, s, tmA, tmA2, tmB, P);
+        auto kern = tc_conv_staged_kernel<kStagedX3>;
+        e = set_max_dyn_smem(kern, pl.smem_bytes);
+        if (e == cudaSuccess) e = launch_kernel(kern, grid, kThreadsI8, pl.smem_bytes, s, tmA, tmA2, tmB, P);
     }
     return cuda_check(e, "tensor-core kernel launch");
 }

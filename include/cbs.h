@@ -77,7 +77,9 @@ typedef enum cbs_variant {
     CBS_VARIANT_TC_TF32 = 1,    /* tcgen05 kind::tf32, TMA im2col/tile loads, TMEM accumulator */
     CBS_VARIANT_TC_BF16 = 2,    /* tcgen05 kind::f16 (bf16 operands) */
     CBS_VARIANT_TC_INT8 = 3,    /* int8 values on tcgen05 kind::f16, exact integer sums */
-    CBS_VARIANT_STEM = 4        /* direct CUDA-core convolution for C_in <= 4 (any precision) */
+    CBS_VARIANT_STEM = 4,       /* direct CUDA-core convolution for C_in <= 4 (any precision) */
+    CBS_VARIANT_TC_TF32X3 = 5   /* FP32 on tcgen05 kind::tf32: operands split into a TF32 head and a tail,
+                                   three MMAs per K slice (head x head + head x tail + tail x head) */
 } cbs_variant;
 
 /* One layer.  Padding is symmetric; OH = (H + 2*pad - k)/stride + 1. */
@@ -163,9 +165,17 @@ typedef struct cbs_plan_t {
  * per call-site shape instead of one for all 40 convolutions).
  *   d:   host pointer to the layer; out: host pointer, filled on success.
  * Host only: makes no CUDA call and may be used without a GPU.
+ * Variant choice (force_variant = -1): STEM for the small-channel stems
+ * below; else the precision's own variant, except that an FP32 layer takes
+ * TC_TF32X3 (the FP32 bar on the tensor cores) when it has NHWC input, each
+ * input's channel count a multiple of 8, at least 48 tiles of 128 output
+ * pixels, and no forced tile field; it falls back to SIMT FP32 when no
+ * 3xTF32 configuration fits.  Its input is then the same bytes as for SIMT
+ * FP32.
  * Input format the plan expects (see x_bytes):
  *   SIMT FP32: x in d->in_layout, float, exactly C_in channels.
- *   TF32/BF16/INT8: x NHWC with c_in_pad channels (extra channels zero).
+ *   TF32/BF16/INT8 and TF32X3 (FP32): x NHWC with c_in_pad channels (extra
+ *   channels zero; TF32X3: c_in_pad = C_in rounded up to 8).
  *   STEM (chosen for C_in <= 4, C_out <= 64, k <= 7): x in d->in_layout;
  *   NHWC pixels hold c_in_pad = 4 channels for TF32/BF16/INT8, C_in for FP32.
  *   Two-input plans (d->c_in_b > 0): x holds the first c_in - c_in_b channels
@@ -183,6 +193,8 @@ CBS_API cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out);
  * (r, s, ci), and casts or quantises them:
  *   SIMT FP32: float  [k*k*C_in][C_out]
  *   TF32, STEM with FP32/TF32: float [C_out][k*k*c_in_pad] (padding channels zero)
+ *   TF32X3:    float [2*C_out][k*k*c_in_pad]: rows 0..C_out-1 the heads (w' with
+ *              its low 13 mantissa bits cleared), rows C_out.. the tails w' - head
  *   BF16:      bf16   [C_out][k*k*c_in_pad]   (round to nearest even)
  *   INT8:      int8 codes held exactly as bf16 [C_out][k*k*c_in_pad];
  *              s_w[c] = max|w'[c,:]| / 127, q = rne(w'/s_w), m_c[c] = s_x * s_w[c],

@@ -1,0 +1,171 @@
+"""GPU parity of the FP32 layer on the tensor cores (CBS_VARIANT_TC_TF32X3)
+against the CPU oracle, at the FP32 bar (relative L2 <= 1e-5).
+
+The variant splits every fp32 activation and weight into a TF32 head and the
+remainder and sums three kind::tf32 products per K slice, so it must meet
+the same bar as the CUDA-core FP32 kernel, which plain TF32 misses by about
+two orders of magnitude (relative L2 ~1e-3).  Covered: 1x1 2-D tile loads
+and im2col boxes, strides 1 and 2, ragged pixel tiles and channel counts
+(C_in padded to 8, C_out not a multiple of 16), 32-, 64- and 128-byte
+channel blocks, several K steps per stage, NCHW and NHWC output, the
+identity activation with a residual, two inputs, and the plan and
+workspace rules of the variant."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conv_bn_silu_gb300 import _binding as B
+from conv_bn_silu_gb300 import workloads as wl
+from conv_bn_silu_gb300.layer import FusedConvBnSilu, make_desc
+from helpers import TOL_FP32_REL_L2, nhwc_to_nchw, rel_l2
+
+X3 = B.CBS_VARIANT_TC_TF32X3
+
+
+def desc_x3(n, spec, out_layout=B.CBS_NHWC, **kw):
+    return make_desc(n, spec.c_in, spec.h, spec.width, spec.c_out, spec.k, spec.stride, spec.pad,
+                     prec=B.CBS_FP32, in_layout=B.CBS_NHWC, out_layout=out_layout, force_variant=X3, **kw)
+
+
+def run_x3(spec, x, p, out_layout=B.CBS_NHWC, **kw):
+    layer = FusedConvBnSilu(desc_x3(x.shape[0], spec, out_layout, **kw), p.w, p.gamma, p.beta, p.mean, p.var,
+                            p.eps)
+    assert layer.plan.variant == X3
+    y = layer(layer.pack_input(torch.from_numpy(x).cuda()))
+    torch.cuda.synchronize()
+    y = y.cpu().numpy()
+    return (nhwc_to_nchw(y) if out_layout == B.CBS_NHWC else y), layer
+
+
+def ref_of(spec, x, p):
+    return oracle.conv_bn_silu_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, spec.stride, spec.pad)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("out_layout", [B.CBS_NHWC, B.CBS_NCHW])
+@pytest.mark.parametrize("shape", [
+    (2, 64, 64, 3, 1, 20, 20),       # im2col boxes, 128-byte channel blocks, 3x3 s1
+    (1, 32, 96, 3, 2, 21, 19),       # stride 2, ragged pixel tile
+    (2, 256, 128, 1, 1, 12, 12),     # 1x1: 2-D tile boxes, several K steps
+    (1, 3, 16, 3, 2, 38, 38),        # C_in padded to 8: 32-byte channel blocks
+    (1, 16, 20, 3, 1, 17, 13),       # 64-byte blocks, C_out 20 (ragged N tile)
+    (1, 128, 256, 3, 2, 10, 10),     # wide N: several N tiles
+])
+def test_fp32_on_tensor_cores(cuda_lib, out_layout, shape):
+    n, c_in, c_out, k, stride, h, w = shape
+    spec = wl.LayerSpec(c_in, c_out, k, stride, h, w)
+    x, p = wl.layer_inputs(spec, n, layer_index=31)
+    y, _ = run_x3(spec, x, p, out_layout)
+    e = rel_l2(y, ref_of(spec, x, p))
+    assert e <= TOL_FP32_REL_L2, e
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("c_in,kg", [(128, 1), (128, 2), (24, 3)])   # 48 KB or 12 KB per K step
+def test_k_steps_per_stage(cuda_lib, c_in, kg):
+    spec = wl.LayerSpec(c_in, 64, 3, 1, 14, 14)
+    x, p = wl.layer_inputs(spec, 1, layer_index=32)
+    y, layer = run_x3(spec, x, p, force_k_group=kg)
+    assert layer.plan.k_group == kg
+    assert rel_l2(y, ref_of(spec, x, p)) <= TOL_FP32_REL_L2
+
+
+@pytest.mark.gpu
+def test_list_layer_batch16_sample(cuda_lib):
+    """A list layer at batch 16 (many tiles per persistent CTA): images 0 and
+    15 against the oracle."""
+    spec = wl.LAYER_LIST[5]
+    x, p = wl.layer_inputs(spec, 16, layer_index=5)
+    y, _ = run_x3(spec, x, p)
+    for i in (0, 15):
+        want = ref_of(spec, x[i:i + 1], p)
+        assert rel_l2(y[i:i + 1], want) <= TOL_FP32_REL_L2
+
+
+@pytest.mark.gpu
+def test_identity_residual_and_two_inputs(cuda_lib):
+    n, c_a, c_b, c_out, h = 1, 32, 32, 48, 11
+    spec = wl.LayerSpec(c_a + c_b, c_out, 3, 1, h)
+    x, p = wl.layer_inputs(spec, n, layer_index=33)
+    r = np.random.default_rng(12).standard_normal((n, h, h, c_out)).astype(np.float32)
+    desc = desc_x3(n, spec, activation=B.CBS_ACT_IDENTITY, residual=1, c_in_b=c_b)
+    layer = FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps)
+    xa, xb = layer.pack_inputs(torch.from_numpy(np.ascontiguousarray(x[:, :c_a])).cuda(),
+                               torch.from_numpy(np.ascontiguousarray(x[:, c_a:])).cuda())
+    y = layer(xa, residual=torch.from_numpy(r).cuda(), x_b=xb)
+    torch.cuda.synchronize()
+    want = oracle.conv_bn_act_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, 1, 1, act=B.CBS_ACT_IDENTITY,
+                                  residual=np.ascontiguousarray(r.transpose(0, 3, 1, 2)))
+    assert rel_l2(nhwc_to_nchw(y.cpu().numpy()), want) <= TOL_FP32_REL_L2
+
+
+@pytest.mark.gpu
+def test_more_accurate_than_tf32(cuda_lib):
+    """The split is what buys the accuracy: the same layer as plain TF32 is
+    far off the FP32 bar."""
+    spec = wl.LayerSpec(64, 64, 3, 1, 16, 16)
+    x, p = wl.layer_inputs(spec, 1, layer_index=34)
+    y3, _ = run_x3(spec, x, p)
+    desc = make_desc(1, 64, 16, 16, 64, 3, 1, 1, prec=B.CBS_TF32, in_layout=B.CBS_NHWC, out_layout=B.CBS_NHWC)
+    tf = FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps)
+    yt = nhwc_to_nchw(tf(tf.pack_input(torch.from_numpy(x).cuda())).cpu().numpy())
+    want = ref_of(spec, x, p)
+    e3, et = rel_l2(y3, want), rel_l2(yt, want)
+    assert e3 <= TOL_FP32_REL_L2 and et > 20 * e3, (e3, et)
+
+
+def test_plan_rules(cuda_lib):
+    """Host-side plan of the variant (no GPU call): FP32 only, NHWC input,
+    no split-K, both weight halves in w_packed, staged-kernel launch shape."""
+    spec = wl.LayerSpec(64, 96, 3, 1, 20, 20)
+    pl = B.cbs_plan(desc_x3(2, spec))
+    assert pl.variant == X3 and pl.block_m == 128 and pl.threads == 480
+    assert pl.c_in_pad == 64 and pl.block_k == 32
+    assert pl.w_packed_bytes == 2 * 96 * 9 * 64 * 4
+    assert pl.split_k == 1 and pl.workspace_bytes == 0
+    assert pl.x_bytes == 2 * 20 * 20 * 64 * 4
+    with pytest.raises(B.CbsError):   # FP32 only
+        B.cbs_plan(make_desc(1, 64, 20, 20, 96, 3, 1, prec=B.CBS_TF32, in_layout=B.CBS_NHWC, force_variant=X3))
+    with pytest.raises(B.CbsError):   # NHWC input
+        B.cbs_plan(make_desc(1, 64, 20, 20, 96, 3, 1, prec=B.CBS_FP32, in_layout=B.CBS_NCHW, force_variant=X3))
+    with pytest.raises(B.CbsError):   # no split-K
+        B.cbs_plan(desc_x3(1, spec, force_split_k=2))
+
+
+def test_automatic_choice(cuda_lib):
+    """FP32 layers with NHWC input take the 3xTF32 kernel on their own once
+    they have 48 or more tiles of 128 pixels and channel counts that are
+    multiples of 8 (the input bytes are then those of the CUDA-core kernel);
+    otherwise the CUDA-core kernel (host-side, no GPU call)."""
+    def variant(n, c_in, hw, c_out, k, stride, **kw):
+        return B.cbs_plan(make_desc(n, c_in, hw, hw, c_out, k, stride, prec=B.CBS_FP32, **kw)).variant
+    nhwc = dict(in_layout=B.CBS_NHWC)
+    assert variant(16, 64, 80, 64, 3, 1, **nhwc) == X3               # 6400 x 16 pixels
+    assert variant(1, 64, 80, 64, 3, 1, **nhwc) == X3                # 50 tiles
+    assert variant(1, 128, 40, 128, 3, 1, **nhwc) == B.CBS_VARIANT_SIMT_FP32   # 13 tiles: split-K wins
+    assert variant(16, 64, 80, 64, 3, 1) == B.CBS_VARIANT_SIMT_FP32  # NCHW input
+    assert variant(16, 20, 80, 64, 3, 1, **nhwc) == B.CBS_VARIANT_SIMT_FP32   # 20 channels: would need padding
+    assert variant(16, 3, 640, 16, 3, 2, **nhwc) == B.CBS_VARIANT_STEM
+    p = B.cbs_plan(make_desc(16, 64, 80, 80, 64, 3, 1, prec=B.CBS_FP32, **nhwc))
+    simt = B.cbs_plan(make_desc(16, 64, 80, 80, 64, 3, 1, prec=B.CBS_FP32, force_variant=B.CBS_VARIANT_SIMT_FP32,
+                                **nhwc))
+    assert p.x_bytes == simt.x_bytes and p.y_bytes == simt.y_bytes and p.desc.force_variant == -1
+    two = B.cbs_plan(make_desc(16, 384, 40, 40, 128, 1, 1, prec=B.CBS_FP32, c_in_b=128, **nhwc))
+    assert two.variant == X3 and two.x_b_bytes == 16 * 40 * 40 * 128 * 4
+
+
+@pytest.mark.gpu
+def test_automatic_choice_parity(cuda_lib):
+    """A list layer at batch 16 with NHWC input through the default plan."""
+    spec = wl.LAYER_LIST[3]
+    x, p = wl.layer_inputs(spec, 16, layer_index=3)
+    desc = make_desc(16, spec.c_in, spec.h, spec.width, spec.c_out, spec.k, spec.stride, spec.pad, prec=B.CBS_FP32,
+                     in_layout=B.CBS_NHWC, out_layout=B.CBS_NCHW)
+    layer = FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps)
+    assert layer.plan.variant == X3
+    y = layer(layer.pack_input(torch.from_numpy(x).cuda()))
+    torch.cuda.synchronize()
+    y = y.cpu().numpy()
+    for i in (0, 9):
+        assert rel_l2(y[i:i + 1], ref_of(spec, x[i:i + 1], p)) <= TOL_FP32_REL_L2
