@@ -53,9 +53,6 @@ constexpr int kEpiWarps = 8;                     // two per TMEM lane quadrant
 constexpr int kThreads = 32 * (kEpiFirst + kEpiWarps);        // TF32/BF16: 416
 constexpr int kMaxProducersI8 = 2;               // INT8: warps 0..1
 constexpr int kMmaWarpI8 = kMaxProducersI8;      // warp 2
-constexpr int kEpiFirstI8 = kMmaWarpI8 + 1;      // warps 3..10
-constexpr int kConvFirstI8 = kEpiFirstI8 + kEpiWarps;  // warps 11..14: int8 -> bf16 converters
-constexpr int kThreadsI8 = 32 * (kConvFirstI8 + 4);    // 480
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kSmemBudget = 222 * 1024;           // stages + resident weights + barriers
 
@@ -881,6 +878,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t u_lo, uint32_t u_hi) {
 // What the converter warps of tc_conv_staged_kernel make of the staging tile.
 enum StagedKind { kStagedI8 = 0, kStagedX3 = 1 };
 
+// Warp roles of tc_conv_staged_kernel: producers (warps 0-1), the MMA issuer
+// (warp 2), kEpi epilogue warps, 4 converter warps.  The INT8 epilogue's
+// specified requantisation (about 35 dependent operations per output) bounds
+// the INT8 layers, so INT8 runs 16 epilogue warps, each on 8-column groups;
+// X3 runs 8 on 16-column groups.  Epilogue warp w reads TMEM lane quadrant
+// w % 4, as tcgen05.ld requires.
+template <int SK>
+struct StagedLayout {
+    static constexpr int kEpi = SK == kStagedI8 ? 16 : 8;
+    static constexpr int kEpiFirst = kMmaWarpI8 + 1;
+    static constexpr int kConvFirst = kEpiFirst + kEpi;
+    static constexpr int kThreads = 32 * (kConvFirst + 4);
+    static constexpr int kGroup = SK == kStagedI8 ? 8 : 16;   // accumulator columns per TMEM load
+};
+
 // Persistent kernel whose A operand passes through a staging tile and
 // converter warps on its way to the tensor cores.  Warps 0-1: TMA producers;
 // warp 2: TMEM + MMA issuer; warps 3-10: epilogue; warps 11-14: converters.
@@ -893,7 +905,7 @@ enum StagedKind { kStagedI8 = 0, kStagedX3 = 1 };
 //              head x head) into one FP32 accumulator, which drops only the
 //              tail x tail term: FP32-level accuracy on the tensor cores.
 template <int SK>
-__global__ void __launch_bounds__(kThreadsI8, 1)
+__global__ void __launch_bounds__(StagedLayout<SK>::kThreads, 1)
 tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                       const __grid_constant__ CUtensorMap tmB, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -924,6 +936,7 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     const int stg_stride = (p.stg_bytes + 1023) & ~1023;
     const int nstage = p.ksteps / kg;
 
+    using L = StagedLayout<SK>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_tiles = p.m_tiles * p.n_tiles;
 
@@ -935,7 +948,7 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(accf_bar(a), 1);
-            ptx::mbar_init(acce_bar(a), kEpiWarps);   // one arrive per epilogue warp
+            ptx::mbar_init(acce_bar(a), L::kEpi);   // one arrive per epilogue warp
         }
         ptx::mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -1066,11 +1079,11 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             }
             ptx::mma_commit(drain_bar);
         }
-    } else if (warp >= kConvFirstI8 && SK == kStagedX3) {
-        // Converters: thread (warp - kConvFirstI8) * 32 + lane splits row `row`
+    } else if (warp >= L::kConvFirst && SK == kStagedX3) {
+        // Converters: thread (warp - kConvFirst) * 32 + lane splits row `row`
         // of every staging tile: head = the value with its low 13 mantissa
         // bits cleared (a TF32 number), tail = value - head (exact).
-        const int row = (warp - kConvFirstI8) * 32 + lane;
+        const int row = (warp - L::kConvFirst) * 32 + lane;
         int g = 0;
         for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
             bool ok = true;
@@ -1113,10 +1126,10 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             }
             if (!ok) break;
         }
-    } else if (warp >= kConvFirstI8) {
-        // Converters: thread (warp - kConvFirstI8) * 32 + lane widens row `row`
+    } else if (warp >= L::kConvFirst) {
+        // Converters: thread (warp - kConvFirst) * 32 + lane widens row `row`
         // of every staging tile into the swizzled bf16 operand.
-        const int row = (warp - kConvFirstI8) * 32 + lane;
+        const int row = (warp - L::kConvFirst) * 32 + lane;
         const int in_bytes = p.CB;
         // With an input zero point: the code of a real zero, as a bf16 pair.
         const uint32_t zcode = p.zp_x ? pack_bf16x2((uint32_t)(p.zp_x + 128), (uint32_t)(p.zp_x + 128)) : 0u;
@@ -1205,9 +1218,11 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             if (!ok) break;
         }
     } else {
-        // Epilogue warps 3..10: quadrant warp % 4, alternate 16-column groups.
+        // Epilogue warps: quadrant warp % 4; the kEpi / 4 warps of a quadrant
+        // take every (kEpi / 4)-th group of kGroup columns.
+        constexpr int G = L::kGroup, NSUB = L::kEpi / 4;
         const int q = warp & 3;
-        const int half = (warp - kEpiFirstI8) >> 2;
+        const int sub = (warp - L::kEpiFirst) >> 2;
         const int erow = 32 * q + lane;
         int j = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++j) {
@@ -1231,7 +1246,7 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             }
             const uint32_t t_row = tmem_base + (uint32_t)(acc * p.acc_stride) + ((uint32_t)(32 * q) << 16);
             if constexpr (SK == kStagedX3) {
-                for (int c0 = 16 * half; c0 < p.BN; c0 += 32) {
+                for (int c0 = G * sub; c0 < p.BN; c0 += G * NSUB) {
                     uint32_t v[16];
                     ptx::tmem_ld16(t_row + (uint32_t)c0, v);
                     ptx::tmem_ld_wait();
@@ -1239,40 +1254,40 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     epi_store16<kTF32, true>(p, p.bias, m, img, oh, ow, n0 + c0, v);
                 }
             } else {
-                for (int c0 = 16 * half; c0 < p.BN; c0 += 32) {
+                for (int c0 = G * sub; c0 < p.BN; c0 += G * NSUB) {
                     const int nbase = n0 + c0;
-                    int accv[16];
-    #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) accv[jj] = nbase + jj < p.C_out ? __ldg(p.bias_i32 + nbase + jj) : 0;
+                    int accv[G];
+#pragma unroll
+                    for (int jj = 0; jj < G; ++jj) accv[jj] = nbase + jj < p.C_out ? __ldg(p.bias_i32 + nbase + jj) : 0;
                     for (int ch = 0; ch < p.nchunks; ++ch) {
-                        uint32_t v[16];
-                        ptx::tmem_ld16(t_row + (uint32_t)(ch * p.chunk_stride + c0), v);
+                        uint32_t v[G];
+                        ptx::tmem_ld8(t_row + (uint32_t)(ch * p.chunk_stride + c0), v);
                         ptx::tmem_ld_wait();
-    #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) accv[jj] += __float2int_rn(__uint_as_float(v[jj]));
+#pragma unroll
+                        for (int jj = 0; jj < G; ++jj) accv[jj] += __float2int_rn(__uint_as_float(v[jj]));
                     }
                     if (m >= p.M || nbase >= p.C_out) continue;
-                    uint32_t qw[4] = {0u, 0u, 0u, 0u};
-    #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
+                    uint32_t qw[G / 4] = {};
+#pragma unroll
+                    for (int jj = 0; jj < G; ++jj) {
                         const int qv = requant_i8(accv[jj], nbase + jj < p.C_out ? __ldg(p.m_c + nbase + jj) : 0.0f,
                                                   p.inv_s_y, p.zp_y);
                         qw[jj >> 2] |= (uint32_t)(uint8_t)(int8_t)qv << (8 * (jj & 3));
                     }
                     if (p.out_nhwc) {
                         int8_t *yr = static_cast<int8_t *>(p.y) + (size_t)m * p.C_out + nbase;
-                        if (nbase + 16 <= p.C_out && (p.C_out & 15) == 0) {
-                            *reinterpret_cast<uint4 *>(yr) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+                        if (nbase + G <= p.C_out && (p.C_out & (G - 1)) == 0) {
+                            *reinterpret_cast<uint2 *>(yr) = make_uint2(qw[0], qw[1]);
                         } else {
-    #pragma unroll
-                            for (int jj = 0; jj < 16; ++jj)
+#pragma unroll
+                            for (int jj = 0; jj < G; ++jj)
                                 if (nbase + jj < p.C_out) yr[jj] = (int8_t)(qw[jj >> 2] >> (8 * (jj & 3)));
                         }
                     } else {
                         const size_t plane = (size_t)p.OH * p.out_row_stride;
                         const size_t pix = (size_t)oh * p.out_row_stride + ow;
-    #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
+#pragma unroll
+                        for (int jj = 0; jj < G; ++jj) {
                             if (nbase + jj >= p.C_out) continue;
                             static_cast<int8_t *>(p.y)[((size_t)img * p.C_out + nbase + jj) * plane + pix] =
                                 (int8_t)(qw[jj >> 2] >> (8 * (jj & 3)));
@@ -1592,14 +1607,20 @@ cbs_status plan_tc(cbs_plan_t &p) {
         } else {
             const int full = round_up(d.c_out, 16) < max_bn ? round_up(d.c_out, 16) : max_bn;
             if (full < 16) return fail(CBS_ERR_UNSUPPORTED, "INT8: %d exact-sum chunks exceed TMEM", nchunks);
-            // Waves of tiles over the SMs x the MMA cost of a tile (flat below
-            // N = 64): fewer, wider tiles unless they leave SMs idle.
+            // Waves of tiles over the SMs x the cost of a tile: INT8, the MMAs
+            // (flat below N = 64); X3, a fixed share for loading and
+            // splitting the A tile (every N tile repeats it) plus the MMAs.
+            // Fewer, wider tiles unless they leave SMs idle.  (X3 measured on
+            // GB300 at batch 16: the C_out = 128 list layers run 10-13% faster
+            // with one N tile of 128 than with two of 64; with C_out = 256 and
+            // 50 pixel tiles, three N tiles of 96 beat two of 128.)
             BN = full;
             double best = 1e300;
             for (int c : {full, 256, 192, 128, 96, 64}) {
                 if (c > full || c < 16) continue;
                 const long long tiles = (long long)p.m_tiles * ((d.c_out + c - 1) / c);
-                const double cost = (double)((tiles + kNumSMs - 1) / kNumSMs) * (c > 64 ? c : 64);
+                const double per_tile = x3 ? 128.0 + c : (c > 64 ? c : 64);
+                const double cost = (double)((tiles + kNumSMs - 1) / kNumSMs) * per_tile;
                 if (cost < best * 0.99) { best = cost; BN = c; }
             }
         }
@@ -1636,7 +1657,7 @@ cbs_status plan_tc(cbs_plan_t &p) {
         while (nprod > 1 && (stages < 2 * nprod)) nprod /= 2;
         stages = stages / nprod * nprod;
         p.stages = stages;
-        p.threads = kThreadsI8;
+        p.threads = i8 ? StagedLayout<kStagedI8>::kThreads : StagedLayout<kStagedX3>::kThreads;
         p.smem_bytes = 1024 + stages * stage + 8 * (3 * stages + 5) + 16;
         const long long tiles = (long long)p.m_tiles * p.n_tiles;
         p.grid_ctas = (int)(tiles < kNumSMs ? tiles : kNumSMs);
@@ -1950,11 +1971,13 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     } else if (i8) {
         auto kern = tc_conv_staged_kernel<kStagedI8>;
         e = set_max_dyn_smem(kern, pl.smem_bytes);
-        if (e == cudaSuccess) e = launch_kernel(kern, grid, kThreadsI8, pl.smem_bytes, s, tmA, tmA2, tmB, P);
+        if (e == cudaSuccess)
+            e = launch_kernel(kern, grid, StagedLayout<kStagedI8>::kThreads, pl.smem_bytes, s, tmA, tmA2, tmB, P);
     } else {
         auto kern = tc_conv_staged_kernel<kStagedX3>;
         e = set_max_dyn_smem(kern, pl.smem_bytes);
-        if (e == cudaSuccess) e = launch_kernel(kern, grid, kThreadsI8, pl.smem_bytes, s, tmA, tmA2, tmB, P);
+        if (e == cudaSuccess)
+            e = launch_kernel(kern, grid, StagedLayout<kStagedX3>::kThreads, pl.smem_bytes, s, tmA, tmA2, tmB, P);
     }
     return cuda_check(e, "tensor-core kernel launch");
 }
