@@ -125,10 +125,12 @@ EXTRA_DEFAULT = ("layer_list_bf16_n16", "layer_list_tf32_n16", "layer_list_int8_
 # ncu capture of the default bench command's first warm-up step
 # (dram__bytes_read.sum + dram__bytes_write.sum summed over that kernel's
 # launches; the summary and command are in profiles/).  A figure is reported
-# only while the kernel's sources are the ones the counters were taken from.
+# only while the kernel's sources and the measured plan table (which picks
+# its tiles) are the ones the counters were taken from.
 TRAFFIC = {
-    "layer_list_fp32_n1": {"kernel": "simt_conv_kernel", "launches": 11, "bytes": 28487680,
-                           "sources": ("k_simt.cu", "cbs_internal.cuh"), "digest": "1efc6b90d4ea3d05",
+    "layer_list_fp32_n1": {"kernel": "simt_conv_kernel", "launches": 11, "bytes": 28486400,
+                           "sources": ("k_simt.cu", "cbs_internal.cuh", "../tuned_plans.json"),
+                           "digest": "65f3cdee48197696",
                            "profile": "profiles/launches_layer_list_fp32_n1.md"},
 }
 # Variant of the dominant kernel per precision (the direct small-channel

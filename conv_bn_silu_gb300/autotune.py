@@ -3,7 +3,8 @@ that `tuning.tuned_desc` reads.
 
 For every distinct layer shape of the benchmark workloads (the twelve-layer
 list at batch 16 in BF16, TF32 and INT8, the 40-layer chain at batch 16 in
-BF16 and TF32, and both at batch 1 in FP32), each candidate configuration is
+BF16 and TF32, both at batch 1 in FP32, and the list at batch 16 in FP32 with
+NHWC activations on the 3xTF32 kernel), each candidate configuration is
 planned, folded and timed as a CUDA graph of repeated launches over rotating
 input copies.  A shape gets a table entry when its fastest candidate beats the
 cost-model plan by 3% or more.
@@ -38,6 +39,8 @@ def workload_shapes():
     for prec in ("bf16", "tf32"):
         out += [(prec, 16, s, B.CBS_NHWC) for s in chain]
     out += [("fp32", 1, s, B.CBS_NCHW) for s in list(wl.LAYER_LIST) + chain + [wl.SINGLE_LAYER]]
+    # FP32 with NHWC activations at batch 16: the 3xTF32 tensor-core kernel
+    out += [("fp32", 16, s, B.CBS_NHWC) for s in wl.LAYER_LIST]
     seen, uniq = set(), []
     for prec, n, s, lay in out:
         k = (prec, n, s, lay)
@@ -51,7 +54,12 @@ def candidates(prec, spec, base):
     """Descriptor force-field sets to try for one shape."""
     full = min(256, -(-spec.c_out // 16) * 16)
     bns = [b for b in (32, 48, 64, 96, 128, 192, 256) if b <= full] or [full]
-    if prec == "fp32":
+    if prec == "fp32" and base.in_layout == B.CBS_NHWC:
+        # 3xTF32: the variant is forced with the tile fields (a forced tile
+        # field alone keeps an FP32 plan on the CUDA cores).
+        for kg, bn in itertools.product((1, 2, 3, 4), bns):
+            yield dict(force_variant=B.CBS_VARIANT_TC_TF32X3, force_k_group=kg, force_block_n=bn)
+    elif prec == "fp32":
         for (bm, bn), sk in itertools.product(SIMT_TILES, (1, 2, 3, 4, 6, 8, 12, 16)):
             yield dict(force_variant=B.CBS_VARIANT_SIMT_FP32, force_block_m=bm, force_block_n=bn, force_split_k=sk)
     elif prec == "int8":
@@ -104,7 +112,7 @@ def tune(reps: int = 10, log=print):
         s_x = float(wl.S_X_INT8) if prec == "int8" else 0.0
         auto = FusedConvBnSilu(base, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, s_x=s_x, tuned=False)
         xd = torch.from_numpy(x).cuda()
-        x0 = auto.pack_input(xd) if prec != "fp32" else xd
+        x0 = auto.pack_input(xd) if (prec != "fp32" or lay == B.CBS_NHWC) else xd
         nbytes = x0.numel() * x0.element_size()
         copies = int(min(8, max(2, math.ceil((256 << 20) / max(nbytes, 1)))))
         xs = [x0] + [x0.clone() for _ in range(copies - 1)]
