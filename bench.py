@@ -115,6 +115,7 @@ WORKLOADS = {
     # FP32 with NHWC activations: layers with enough pixel tiles run the
     # 3xTF32 tensor-core kernel (the FP32 bar), the stem its direct kernel.
     "layer_list_fp32_n16_nhwc": dict(kind="list", layers=wl.LAYER_LIST, n=16, prec="fp32", layout="nhwc"),
+    "layer_list_fp32_n1_nhwc": dict(kind="list", layers=wl.LAYER_LIST, n=1, prec="fp32", layout="nhwc"),
 }
 EXTRA_DEFAULT = ("layer_list_bf16_n16", "layer_list_tf32_n16", "layer_list_int8_n16", "chain_fp32_n1",
                  "chain_bf16_n16", "layer_list_bf16_n16_residual", "layer_list_int8_n16_asym",

@@ -54,14 +54,17 @@ def candidates(prec, spec, base):
     """Descriptor force-field sets to try for one shape."""
     full = min(256, -(-spec.c_out // 16) * 16)
     bns = [b for b in (32, 48, 64, 96, 128, 192, 256) if b <= full] or [full]
-    if prec == "fp32" and base.in_layout == B.CBS_NHWC:
-        # 3xTF32: the variant is forced with the tile fields (a forced tile
-        # field alone keeps an FP32 plan on the CUDA cores).
-        for kg, bn in itertools.product((1, 2, 3, 4), bns):
-            yield dict(force_variant=B.CBS_VARIANT_TC_TF32X3, force_k_group=kg, force_block_n=bn)
-    elif prec == "fp32":
-        for (bm, bn), sk in itertools.product(SIMT_TILES, (1, 2, 3, 4, 6, 8, 12, 16)):
-            yield dict(force_variant=B.CBS_VARIANT_SIMT_FP32, force_block_m=bm, force_block_n=bn, force_split_k=sk)
+    if prec == "fp32":
+        if base.in_layout == B.CBS_NHWC:
+            # 3xTF32: the variant is forced with the tile fields (a forced
+            # tile field alone keeps an FP32 plan on the CUDA cores).
+            for kg, bn in itertools.product((1, 2, 3, 4), bns):
+                yield dict(force_variant=B.CBS_VARIANT_TC_TF32X3, force_k_group=kg, force_block_n=bn)
+        else:
+            # the CUDA-core kernel
+            for (bm, bn), sk in itertools.product(SIMT_TILES, (1, 2, 3, 4, 6, 8, 12, 16)):
+                yield dict(force_variant=B.CBS_VARIANT_SIMT_FP32, force_block_m=bm, force_block_n=bn,
+                           force_split_k=sk)
     elif prec == "int8":
         for kg, bn in itertools.product((1, 2, 3, 4), bns):
             yield dict(force_k_group=kg, force_block_n=bn)
