@@ -119,7 +119,7 @@ WORKLOADS = {
 }
 EXTRA_DEFAULT = ("layer_list_bf16_n16", "layer_list_tf32_n16", "layer_list_int8_n16", "chain_fp32_n1",
                  "chain_bf16_n16", "layer_list_bf16_n16_residual", "layer_list_int8_n16_asym",
-                 "layer_list_fp32_n16_nhwc")
+                 "layer_list_fp32_n16_nhwc", "layer_list_fp32_n1_nhwc")
 
 
 # DRAM traffic of the dominant kernel over one step of a workload, from one

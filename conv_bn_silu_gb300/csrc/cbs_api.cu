@@ -201,10 +201,6 @@ const char *cbs_status_string(cbs_status s) {
     return "CBS_ERR_UNKNOWN";
 }
 
-// Auto-selection of the 3xTF32 variant for FP32 NHWC layers: at least this
-// many 128-pixel tiles (a third of the SMs).
-constexpr int kX3Tile = 128, kX3MinTiles = 48;
-
 cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
     if (!d || !out) return fail(CBS_ERR_INVALID_ARG, "desc or plan pointer is NULL");
     const cbs_layer_desc D = *d;
@@ -252,18 +248,17 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
     if (variant < 0) {
         variant = stem_fits ? (int)CBS_VARIANT_STEM : D.prec;  // FP32->SIMT, TF32, BF16, INT8
         // FP32 with NHWC input runs on the tensor cores (3xTF32, within the
-        // FP32 bar) once the layer has 128-pixel tiles for a third of the
-        // SMs.  Measured on GB300: at batch 16 the list layers run 1.3-3.4x
-        // faster than on the CUDA cores, while at batch 1 the CUDA-core
-        // kernel and its split-K win on the small-spatial layers.  Only when
-        // every input's channel count is a multiple of 8: the NHWC input then
-        // needs no padding and is the same bytes for either kernel.  A
+        // FP32 bar; split-K where the tiles leave SMs idle).  Measured on
+        // GB300 over the list layers: 1.3-3.4x faster than the CUDA cores at
+        // batch 16, and faster on every layer at batch 1 (by 2-40%).  Only
+        // when every input's channel count is a multiple of 8: the NHWC input
+        // then needs no padding and is the same bytes for either kernel.  A
         // descriptor that forces a tile field is tuning the CUDA-core kernel.
         const int c_a = D.c_in - D.c_in_b;
         const bool forces_tiles = D.force_split_k > 0 || D.force_block_n > 0 || D.force_block_m > 0 ||
                                   D.force_k_group > 0 || D.force_b_resident != 0 || D.force_window > 0;
         if (variant == CBS_VARIANT_SIMT_FP32 && D.in_layout == CBS_NHWC && c_a % 8 == 0 && D.c_in_b % 8 == 0 &&
-            !forces_tiles && (M + kX3Tile - 1) / kX3Tile >= kX3MinTiles) {
+            !forces_tiles) {
             variant = CBS_VARIANT_TC_TF32X3;
             auto_x3 = true;
         }

@@ -892,6 +892,7 @@ struct StagedLayout {
     static constexpr int kThreads = 32 * (kConvFirst + 4);
     static constexpr int kGroup = SK == kStagedI8 ? 8 : 16;   // accumulator columns per TMEM load
 };
+static_assert(StagedLayout<kStagedX3>::kEpi <= kSplitCounterSlots, "one split-K counter per X3 epilogue warp");
 
 // Persistent kernel whose A operand passes through a staging tile and
 // converter warps on its way to the tensor cores.  Warps 0-1: TMA producers;
@@ -939,6 +940,7 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     using L = StagedLayout<SK>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_tiles = p.m_tiles * p.n_tiles;
+    const int num_units = num_tiles * p.split;   // X3 split-K: (tile, K part) units; else tiles
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -976,7 +978,9 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         // then B boxes; TMA issue throughput scales with issuing lanes.
         if (warp < p.nprod) {
             int g = 0;
-            for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
+            for (int uu = blockIdx.x; uu < num_units && !aborted(abort_flag); uu += gridDim.x) {
+                int t, st0, st1;
+                unit_range(uu, p.split, nstage, t, st0, st1);
                 int m0, n0;
                 tile_coords(t, p.n_tiles, kBM, m0, n0, p.BN);
                 const int img = m0 / p.OHW;
@@ -984,7 +988,7 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 const int oh = rem / p.OW, ow = rem - (rem / p.OW) * p.OW;
                 const int wc = ow * p.stride - p.pad, hc = oh * p.stride - p.pad;
                 bool ok = true;
-                for (int st = 0; st < nstage; ++st, ++g) {
+                for (int st = st0; st < st1; ++st, ++g) {
                     if (g % p.nprod != warp) continue;
                     const int s = g % S, u = g / S;
                     bool got = true;
@@ -1034,7 +1038,9 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             const int kslices = p.RB / 32;
             const uint64_t dhi = ptx::smem_desc(0u, 16u, sbo, p.swz);
             int g = 0, j = 0;
-            for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x, ++j) {
+            for (int uu = blockIdx.x; uu < num_units && !aborted(abort_flag); uu += gridDim.x, ++j) {
+                int t, st0, st1;
+                unit_range(uu, p.split, nstage, t, st0, st1);
                 const int acc = j & 1, ua = j >> 1;
                 if (!ptx::mbar_wait_bounded(acce_bar(acc), (ua & 1) ^ 1, kWaitLimitNs)) {
                     abort_now(p, abort_flag);
@@ -1042,7 +1048,7 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 }
                 ptx::tc_fence_after();
                 bool ok = true;
-                for (int st = 0; st < nstage; ++st, ++g) {
+                for (int st = st0; st < st1; ++st, ++g) {
                     const int s = g % S, u = g / S;
                     // conv_done follows raw_full (the converters waited on it),
                     // and raw_full also carries the B tiles.
@@ -1061,7 +1067,7 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                             const uint32_t a_head = sb + stg_off + kk * stg_stride, a_tail = sb + kk * p.a_bytes;
                             const uint32_t b_head = sb + op_b_off + kk * p.b_tile_stride;
                             const uint32_t b_tail = sb + op_b_off + (kg + kk) * p.b_tile_stride;
-                            issue_kstep<kTF32>(d_tmem, dhi, a_tail, b_head, p.idesc, kslices, i == 0);
+                            issue_kstep<kTF32>(d_tmem, dhi, a_tail, b_head, p.idesc, kslices, i == st0 * kg);
                             issue_kstep<kTF32>(d_tmem, dhi, a_head, b_tail, p.idesc, kslices, false);
                             issue_kstep<kTF32>(d_tmem, dhi, a_head, b_head, p.idesc, kslices, false);
                         } else {
@@ -1085,9 +1091,11 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         // bits cleared (a TF32 number), tail = value - head (exact).
         const int row = (warp - L::kConvFirst) * 32 + lane;
         int g = 0;
-        for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
+        for (int uu = blockIdx.x; uu < num_units && !aborted(abort_flag); uu += gridDim.x) {
+            int t, st0, st1;
+            unit_range(uu, p.split, nstage, t, st0, st1);
             bool ok = true;
-            for (int st = 0; st < nstage; ++st, ++g) {
+            for (int st = st0; st < st1; ++st, ++g) {
                 const int s = g % S, u = g / S;
                 if (!ptx::mbar_wait_bounded(raw_bar(s), u & 1, kWaitLimitNs)) {
                     abort_now(p, abort_flag);
@@ -1225,7 +1233,9 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         const int sub = (warp - L::kEpiFirst) >> 2;
         const int erow = 32 * q + lane;
         int j = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++j) {
+        for (int uu = blockIdx.x; uu < num_units; uu += gridDim.x, ++j) {
+            int t, st0, st1;
+            unit_range(uu, p.split, nstage, t, st0, st1);
             const int acc = j & 1, ua = j >> 1;
             bool ok = !aborted(abort_flag) && ptx::mbar_wait_bounded(accf_bar(acc), ua & 1, kWaitLimitNs);
             ok = __all_sync(0xffffffffu, ok);
@@ -1246,6 +1256,53 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             }
             const uint32_t t_row = tmem_base + (uint32_t)(acc * p.acc_stride) + ((uint32_t)(32 * q) << 16);
             if constexpr (SK == kStagedX3) {
+                if (p.split > 1) {
+                    // This warp's region of the partial tile (rows erow,
+                    // its column groups), column-major: a warp's 32 rows of
+                    // one column are 128 contiguous bytes.
+                    const int part = uu - t * p.split;
+                    float *mine = p.partials + ((size_t)t * p.split + part) * (size_t)(kBM * p.BN);
+                    for (int c0 = G * sub; c0 < p.BN; c0 += G * NSUB) {
+                        uint32_t v[16];
+                        ptx::tmem_ld16(t_row + (uint32_t)c0, v);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj)
+                            __stcg(mine + (size_t)(c0 + jj) * kBM + erow, __uint_as_float(v[jj]));
+                    }
+                    // The accumulator has been read: hand it back to the MMA issuer.
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(acce_bar(acc));
+                    __threadfence();
+                    __syncwarp();
+                    unsigned int prev = 0u;
+                    unsigned int *counter = p.counters + (size_t)t * kSplitCounterSlots + (warp - L::kEpiFirst);
+                    if (lane == 0) prev = atomicAdd(counter, 1u);
+                    prev = __shfl_sync(0xffffffffu, prev, 0);
+                    if (prev != (unsigned int)(p.split - 1)) continue;
+                    // Last part of this region: sum the parts in order, then the epilogue.
+                    if (lane == 0) *counter = 0u;   // ready for the next launch
+                    __threadfence();
+                    const float *parts = p.partials + (size_t)t * p.split * (size_t)(kBM * p.BN);
+                    for (int c0 = G * sub; c0 < p.BN; c0 += G * NSUB) {
+                        float sum[16];
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) sum[jj] = 0.0f;
+                        for (int k2 = 0; k2 < p.split; ++k2) {
+                            const float *src = parts + (size_t)k2 * (kBM * p.BN) + (size_t)c0 * kBM + erow;
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) sum[jj] += __ldcg(src + (size_t)jj * kBM);
+                        }
+                        if (m < p.M && n0 + c0 < p.C_out) {
+                            uint32_t v[16];
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) v[jj] = __float_as_uint(sum[jj]);
+                            epi_store16<kTF32, true>(p, p.bias, m, img, oh, ow, n0 + c0, v);
+                        }
+                    }
+                    continue;
+                }
                 for (int c0 = G * sub; c0 < p.BN; c0 += G * NSUB) {
                     uint32_t v[16];
                     ptx::tmem_ld16(t_row + (uint32_t)c0, v);
@@ -1584,8 +1641,7 @@ cbs_status plan_tc(cbs_plan_t &p) {
     p.w_packed_bytes = (size_t)d.c_out * p.k_gemm * (x3 ? 8 : (tf32 ? 4 : 2));
     if (d.pad > 127 || (p.oh - 1) * d.stride - d.pad - d.h + 1 < -128 || (p.ow - 1) * d.stride - d.pad - d.w + 1 < -128)
         return fail(CBS_ERR_UNSUPPORTED, "padding outside the im2col corner range");
-    if (d.force_split_k > 1 && (i8 || x3))
-        return fail(CBS_ERR_UNSUPPORTED, "split-K is not built for the staged (INT8, 3xTF32) kernel");
+    if (d.force_split_k > 1 && i8) return fail(CBS_ERR_UNSUPPORTED, "split-K is not built for the INT8 kernel");
     const long long M = (long long)d.n * p.oh * p.ow;
     const int ksteps = d.k * d.k * (p.c_in_pad / CB);
     p.block_k = CB;
@@ -1598,50 +1654,77 @@ cbs_status plan_tc(cbs_plan_t &p) {
         // columns (rounded to a power of two): nchunks * next_pow2(BN) <= 256.
         int max_bn = 256;
         while (max_bn >= 16 && nchunks * max_bn > 256) max_bn /= 2;
-        int BN;
+        // One K step: operand A (INT8: bf16; X3: the tail), the weights
+        // (X3: head and tail), the staging tile (int8 codes; X3: fp32, the
+        // head once converted).
+        auto kstep_bytes_of = [&](int c) {
+            return kBM * RB + (x3 ? 2 : 1) * round_up(c * RB, 1024) + round_up(kBM * (x3 ? RB : CB), 1024);
+        };
+        // K steps per stage: the MMA issuer waits twice per stage, so a stage
+        // carries the most K steps (up to 4, dividing the K steps) that still
+        // leave two stages in shared memory; a split needs at least as many
+        // stages per tile as parts.
+        auto kgroup_of = [&](int c, int want_split) {
+            const int kb = kstep_bytes_of(c);
+            for (int g = 4; g >= 1; --g) {
+                if (d.force_k_group > 0 && g != d.force_k_group) continue;
+                if (want_split > 1 && d.force_k_group <= 0 && g > 1 && ksteps / g < want_split) continue;
+                if (ksteps % g == 0 && ((200 * 1024) / (g * kb) >= 2 || g == 1 || d.force_k_group > 0)) return g;
+            }
+            return 1;
+        };
         if (d.force_block_n > 0) {
-            BN = d.force_block_n;
-            if (BN % 16 || BN < 16 || BN > 256) return fail(CBS_ERR_INVALID_ARG, "block_n %d: 16..256, multiple of 16", BN);
-            if (BN > max_bn)
-                return fail(CBS_ERR_UNSUPPORTED, "block_n %d with %d exact-sum chunks exceeds TMEM", BN, nchunks);
-        } else {
-            const int full = round_up(d.c_out, 16) < max_bn ? round_up(d.c_out, 16) : max_bn;
-            if (full < 16) return fail(CBS_ERR_UNSUPPORTED, "INT8: %d exact-sum chunks exceed TMEM", nchunks);
-            // Waves of tiles over the SMs x the cost of a tile: INT8, the MMAs
-            // (flat below N = 64); X3, a fixed share for loading and
-            // splitting the A tile (every N tile repeats it) plus the MMAs.
-            // Fewer, wider tiles unless they leave SMs idle.  (X3 measured on
-            // GB300 at batch 16: the C_out = 128 list layers run 10-13% faster
-            // with one N tile of 128 than with two of 64; with C_out = 256 and
-            // 50 pixel tiles, three N tiles of 96 beat two of 128.)
-            BN = full;
+            const int c = d.force_block_n;
+            if (c % 16 || c < 16 || c > 256) return fail(CBS_ERR_INVALID_ARG, "block_n %d: 16..256, multiple of 16", c);
+            if (c > max_bn)
+                return fail(CBS_ERR_UNSUPPORTED, "block_n %d with %d exact-sum chunks exceeds TMEM", c, nchunks);
+        }
+        const int full = round_up(d.c_out, 16) < max_bn ? round_up(d.c_out, 16) : max_bn;
+        if (full < 16) return fail(CBS_ERR_UNSUPPORTED, "INT8: %d exact-sum chunks exceed TMEM", nchunks);
+        // N tile (and X3 split-K parts) from waves of work units over the
+        // SMs x the cost of a unit:
+        //   INT8: the MMAs of a tile (flat below N = 64);
+        //   X3:   per K step, a fixed share for loading and splitting the A
+        //         tile (every N tile repeats it) plus the MMAs, and for a
+        //         split the partial tile written and summed.  A split only
+        //         fills SMs that a single wave of tiles leaves idle.
+        // Measured on GB300 (X3): at batch 16 the C_out = 128 list layers run
+        // 10-13% faster with one N tile of 128 than with two of 64; at batch
+        // 1 the chosen splits are the measured best or within a few percent
+        // (e.g. 128->256 3x3 s2 at 20x20: N tile 32 in 4 parts, 14.7 us
+        // against 19.8 us on the CUDA cores).
+        int BN = d.force_block_n > 0 ? d.force_block_n : full;
+        int split = d.force_split_k > 1 ? d.force_split_k : 1;
+        {
             double best = 1e300;
-            for (int c : {full, 256, 192, 128, 96, 64}) {
-                if (c > full || c < 16) continue;
+            for (int c : {full, 256, 192, 128, 96, 64, 32}) {
+                if (c > full || c < 16 || (c == 32 && !x3 && c != full)) continue;
+                if (d.force_block_n > 0 && c != d.force_block_n) continue;
                 const long long tiles = (long long)p.m_tiles * ((d.c_out + c - 1) / c);
-                const double per_tile = x3 ? 128.0 + c : (c > 64 ? c : 64);
-                const double cost = (double)((tiles + kNumSMs - 1) / kNumSMs) * per_tile;
-                if (cost < best * 0.99) { best = cost; BN = c; }
+                if (!x3) {
+                    const double cost = (double)((tiles + kNumSMs - 1) / kNumSMs) * (c > 64 ? c : 64);
+                    if (cost < best * 0.99) { best = cost; BN = c; }
+                    continue;
+                }
+                const int sp0 = d.force_split_k >= 1 ? d.force_split_k : 1;
+                const int sp1 = d.force_split_k >= 1 ? d.force_split_k : (tiles < kNumSMs ? 16 : 1);
+                for (int sp = sp0; sp <= sp1; ++sp) {
+                    const int g = kgroup_of(c, sp);
+                    const int nst = ksteps / g;
+                    if (sp > nst) break;
+                    const long long units = tiles * sp;
+                    const double cost = (double)((units + kNumSMs - 1) / kNumSMs) * ((nst + sp - 1) / sp) * g *
+                                            (128.0 + c) + (sp > 1 ? 2.0 * sp * c : 0.0);
+                    if (cost < best * 0.99) { best = cost; BN = c; split = sp; }
+                }
             }
         }
         p.block_m = kBM;
         p.block_n = BN;
         p.n_tiles = ceil_div(d.c_out, BN);
         p.b_resident = 0;
-        // One K step: operand A (INT8: bf16; X3: the tail), the weights
-        // (X3: head and tail), the staging tile (int8 codes; X3: fp32, the
-        // head once converted).  The MMA issuer waits twice per stage, so a
-        // stage carries the most K steps (up to 4, dividing the K steps)
-        // that still leave 3 stages.
-        const int kstep_bytes = kBM * RB + (x3 ? 2 : 1) * round_up(BN * RB, 1024) + round_up(kBM * (x3 ? RB : CB), 1024);
-        int kg = 1;
-        for (int c = 4; c >= 1; --c) {
-            if (d.force_k_group > 0 && c != d.force_k_group) continue;
-            if (ksteps % c == 0 && ((200 * 1024) / (c * kstep_bytes) >= 2 || c == 1 || d.force_k_group > 0)) {
-                kg = c;
-                break;
-            }
-        }
+        const int kstep_bytes = kstep_bytes_of(BN);
+        const int kg = kgroup_of(BN, split);
         if (d.force_k_group > 0 && kg != d.force_k_group)
             return fail(CBS_ERR_UNSUPPORTED, "INT8: k_group %d does not divide %d K steps", d.force_k_group, ksteps);
         p.k_group = kg;
@@ -1660,7 +1743,16 @@ cbs_status plan_tc(cbs_plan_t &p) {
         p.threads = i8 ? StagedLayout<kStagedI8>::kThreads : StagedLayout<kStagedX3>::kThreads;
         p.smem_bytes = 1024 + stages * stage + 8 * (3 * stages + 5) + 16;
         const long long tiles = (long long)p.m_tiles * p.n_tiles;
-        p.grid_ctas = (int)(tiles < kNumSMs ? tiles : kNumSMs);
+        // X3 split-K: the K stages of a tile in `split` parts, partial tiles
+        // in the workspace, summed in order by the last part.
+        if (split > ksteps / kg)
+            return fail(CBS_ERR_UNSUPPORTED, "split-K %d exceeds the %d pipeline stages of a tile", split, ksteps / kg);
+        p.split_k = split;
+        if (split > 1)
+            p.workspace_bytes = (size_t)round_up((int)tiles * kSplitCounterSlots * 4, 256) +
+                                (size_t)tiles * split * kBM * BN * 4;
+        const long long units = tiles * split;
+        p.grid_ctas = (int)(units < kNumSMs ? units : kNumSMs);
         return CBS_OK;
     }
 
@@ -1795,8 +1887,8 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     P.win = staged ? 0 : pl.window;
     P.split = pl.split_k < 1 ? 1 : pl.split_k;
     if (P.split > 1) {
-        if (staged || pl.window || pl.b_resident)
-            return fail(CBS_ERR_PLAN_MISMATCH, "split-K plan with windowed A, resident weights or staged A");
+        if (i8 || pl.window || pl.b_resident)
+            return fail(CBS_ERR_PLAN_MISMATCH, "split-K plan with windowed A, resident weights or INT8");
         if (!workspace) return fail(CBS_ERR_WORKSPACE, "split-K plan without a workspace");
         const size_t counter_bytes = (size_t)round_up(pl.m_tiles * pl.n_tiles * kSplitCounterSlots * 4, 256);
         P.counters = static_cast<unsigned int *>(workspace);

@@ -167,11 +167,10 @@ typedef struct cbs_plan_t {
  * Host only: makes no CUDA call and may be used without a GPU.
  * Variant choice (force_variant = -1): STEM for the small-channel stems
  * below; else the precision's own variant, except that an FP32 layer takes
- * TC_TF32X3 (the FP32 bar on the tensor cores) when it has NHWC input, each
- * input's channel count a multiple of 8, at least 48 tiles of 128 output
- * pixels, and no forced tile field; it falls back to SIMT FP32 when no
- * 3xTF32 configuration fits.  Its input is then the same bytes as for SIMT
- * FP32.
+ * TC_TF32X3 (the FP32 bar on the tensor cores, split-K where its tiles leave
+ * SMs idle) when it has NHWC input, each input's channel count a multiple
+ * of 8 and no forced tile field; it falls back to SIMT FP32 when no 3xTF32
+ * configuration fits.  Its input is then the same bytes as for SIMT FP32.
  * Input format the plan expects (see x_bytes):
  *   SIMT FP32: x in d->in_layout, float, exactly C_in channels.
  *   TF32/BF16/INT8 and TF32X3 (FP32): x NHWC with c_in_pad channels (extra

@@ -167,7 +167,8 @@ def test_two_input_plans(cuda_lib):
     ok = 1 << 20
     # CUDA-core FP32, both layouts: x holds c_in - c_in_b channels, x_b the rest
     for lay in (B.CBS_NCHW, B.CBS_NHWC):
-        p = B.cbs_plan(make_desc(2, 384, 40, 40, 128, 1, 1, in_layout=lay, c_in_b=128))
+        p = B.cbs_plan(make_desc(2, 384, 40, 40, 128, 1, 1, in_layout=lay, c_in_b=128,
+                                 force_variant=B.CBS_VARIANT_SIMT_FP32))
         assert p.variant == B.CBS_VARIANT_SIMT_FP32
         assert p.x_bytes == 2 * 40 * 40 * 256 * 4 and p.x_b_bytes == 2 * 40 * 40 * 128 * 4
     # tensor cores: a channel block never straddles the two inputs

@@ -60,7 +60,8 @@ def ref(x, p, spec):
 ])
 def test_cuda_core_two_inputs(cuda_lib, layouts, shape):
     n, c_a, c_b, c_out, k, stride, h, w = shape
-    got, x, p, spec, layer = run_cat(n, c_a, c_b, c_out, k, stride, h, w, "fp32", *layouts)
+    got, x, p, spec, layer = run_cat(n, c_a, c_b, c_out, k, stride, h, w, "fp32", *layouts,
+                                     force_variant=B.CBS_VARIANT_SIMT_FP32)
     assert layer.plan.variant == B.CBS_VARIANT_SIMT_FP32
     assert rel_l2(got, ref(x, p, spec)) <= TOL_FP32_REL_L2
 

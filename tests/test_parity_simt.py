@@ -20,6 +20,8 @@ pytestmark = pytest.mark.gpu
 
 def run_simt(spec, x, p, in_layout=B.CBS_NCHW, out_layout=B.CBS_NCHW, **kw):
     n = x.shape[0]
+    if in_layout == B.CBS_NHWC:   # FP32 NHWC layers would otherwise take the 3xTF32 kernel
+        kw.setdefault("force_variant", B.CBS_VARIANT_SIMT_FP32)
     desc = make_desc(n, spec.c_in, spec.h, spec.width, spec.c_out, spec.k, spec.stride, spec.pad,
                      prec=B.CBS_FP32, in_layout=in_layout, out_layout=out_layout, **kw)
     layer = FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps)

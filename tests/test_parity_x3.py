@@ -117,33 +117,44 @@ def test_more_accurate_than_tf32(cuda_lib):
 
 def test_plan_rules(cuda_lib):
     """Host-side plan of the variant (no GPU call): FP32 only, NHWC input,
-    no split-K, both weight halves in w_packed, staged-kernel launch shape."""
+    both weight halves in w_packed, staged-kernel launch shape, split-K
+    workspace."""
     spec = wl.LayerSpec(64, 96, 3, 1, 20, 20)
     pl = B.cbs_plan(desc_x3(2, spec))
     assert pl.variant == X3 and pl.block_m == 128 and pl.threads == 480
     assert pl.c_in_pad == 64 and pl.block_k == 32
     assert pl.w_packed_bytes == 2 * 96 * 9 * 64 * 4
-    assert pl.split_k == 1 and pl.workspace_bytes == 0
     assert pl.x_bytes == 2 * 20 * 20 * 64 * 4
+    # a layer with a wave of tiles or more runs unsplit; fewer tiles than SMs
+    # take K parts to fill them
+    big = B.cbs_plan(desc_x3(16, wl.LayerSpec(64, 64, 3, 1, 80, 80)))
+    assert big.split_k == 1 and big.workspace_bytes == 0
+    assert pl.m_tiles * pl.n_tiles < 152 and pl.split_k > 1
+    assert pl.m_tiles * pl.n_tiles * pl.split_k <= 152 or pl.split_k == 1
     with pytest.raises(B.CbsError):   # FP32 only
         B.cbs_plan(make_desc(1, 64, 20, 20, 96, 3, 1, prec=B.CBS_TF32, in_layout=B.CBS_NHWC, force_variant=X3))
     with pytest.raises(B.CbsError):   # NHWC input
         B.cbs_plan(make_desc(1, 64, 20, 20, 96, 3, 1, prec=B.CBS_FP32, in_layout=B.CBS_NCHW, force_variant=X3))
-    with pytest.raises(B.CbsError):   # no split-K
-        B.cbs_plan(desc_x3(1, spec, force_split_k=2))
+    # split-K on request: partial tiles and one counter per epilogue warp per tile
+    sp = B.cbs_plan(desc_x3(2, spec, force_split_k=3))
+    tiles = sp.m_tiles * sp.n_tiles
+    assert sp.split_k == 3 and sp.grid_ctas == min(152, tiles * 3)
+    assert sp.workspace_bytes == -(-tiles * 8 * 4 // 256) * 256 + tiles * 3 * 128 * sp.block_n * 4
+    with pytest.raises(B.CbsError):   # more parts than pipeline stages
+        B.cbs_plan(desc_x3(1, wl.LayerSpec(64, 64, 1, 1, 20, 20), force_split_k=8))
 
 
 def test_automatic_choice(cuda_lib):
-    """FP32 layers with NHWC input take the 3xTF32 kernel on their own once
-    they have 48 or more tiles of 128 pixels and channel counts that are
-    multiples of 8 (the input bytes are then those of the CUDA-core kernel);
-    otherwise the CUDA-core kernel (host-side, no GPU call)."""
+    """FP32 layers with NHWC input and channel counts that are multiples of
+    8 take the 3xTF32 kernel on their own (the input bytes are then those of
+    the CUDA-core kernel); otherwise the CUDA-core kernel (host-side, no GPU
+    call)."""
     def variant(n, c_in, hw, c_out, k, stride, **kw):
         return B.cbs_plan(make_desc(n, c_in, hw, hw, c_out, k, stride, prec=B.CBS_FP32, **kw)).variant
     nhwc = dict(in_layout=B.CBS_NHWC)
     assert variant(16, 64, 80, 64, 3, 1, **nhwc) == X3               # 6400 x 16 pixels
     assert variant(1, 64, 80, 64, 3, 1, **nhwc) == X3                # 50 tiles
-    assert variant(1, 128, 40, 128, 3, 1, **nhwc) == B.CBS_VARIANT_SIMT_FP32   # 13 tiles: split-K wins
+    assert variant(1, 128, 40, 128, 3, 1, **nhwc) == X3                # 13 pixel tiles: K parts fill the SMs
     assert variant(16, 64, 80, 64, 3, 1) == B.CBS_VARIANT_SIMT_FP32  # NCHW input
     assert variant(16, 20, 80, 64, 3, 1, **nhwc) == B.CBS_VARIANT_SIMT_FP32   # 20 channels: would need padding
     assert variant(16, 3, 640, 16, 3, 2, **nhwc) == B.CBS_VARIANT_STEM
@@ -169,3 +180,46 @@ def test_automatic_choice_parity(cuda_lib):
     y = y.cpu().numpy()
     for i in (0, 9):
         assert rel_l2(y[i:i + 1], ref_of(spec, x[i:i + 1], p)) <= TOL_FP32_REL_L2
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape,split", [
+    ((1, 256, 256, 3, 1, 20, 20), 8),      # the 20x20 list layer at batch 1: 4 x 3 tiles
+    ((1, 128, 128, 3, 1, 40, 40), 4),      # the 40x40 list layer at batch 1
+    ((1, 64, 96, 3, 2, 21, 19), 5),        # ragged pixels, parts of unequal length
+    ((2, 384, 128, 1, 1, 12, 12), 3),      # 1x1, 2-D tile boxes
+])
+def test_split_k(cuda_lib, shape, split):
+    """3xTF32 with K split over CTAs: each part's partial tile in the
+    workspace, summed in order by the last arriving part."""
+    n, c_in, c_out, k, stride, h, w = shape
+    spec = wl.LayerSpec(c_in, c_out, k, stride, h, w)
+    x, p = wl.layer_inputs(spec, n, layer_index=35)
+    for out_layout in (B.CBS_NHWC, B.CBS_NCHW):
+        y, layer = run_x3(spec, x, p, out_layout, force_split_k=split)
+        assert layer.plan.split_k == split
+        assert rel_l2(y, ref_of(spec, x, p)) <= TOL_FP32_REL_L2
+        # a second launch finds the counters back at zero
+        y2 = layer(layer.pack_input(torch.from_numpy(x).cuda()))
+        torch.cuda.synchronize()
+        y2 = y2.cpu().numpy()
+        y2 = nhwc_to_nchw(y2) if out_layout == B.CBS_NHWC else y2
+        assert np.array_equal(y, y2)
+
+
+@pytest.mark.gpu
+def test_split_k_residual_two_inputs(cuda_lib):
+    n, c_a, c_b, c_out, h = 1, 64, 64, 64, 10
+    spec = wl.LayerSpec(c_a + c_b, c_out, 3, 1, h)
+    x, p = wl.layer_inputs(spec, n, layer_index=36)
+    r = np.random.default_rng(13).standard_normal((n, h, h, c_out)).astype(np.float32)
+    desc = desc_x3(n, spec, activation=B.CBS_ACT_IDENTITY, residual=1, c_in_b=c_b, force_split_k=6)
+    layer = FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps)
+    assert layer.plan.split_k == 6
+    xa, xb = layer.pack_inputs(torch.from_numpy(np.ascontiguousarray(x[:, :c_a])).cuda(),
+                               torch.from_numpy(np.ascontiguousarray(x[:, c_a:])).cuda())
+    y = layer(xa, residual=torch.from_numpy(r).cuda(), x_b=xb)
+    torch.cuda.synchronize()
+    want = oracle.conv_bn_act_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, 1, 1, act=B.CBS_ACT_IDENTITY,
+                                  residual=np.ascontiguousarray(r.transpose(0, 3, 1, 2)))
+    assert rel_l2(nhwc_to_nchw(y.cpu().numpy()), want) <= TOL_FP32_REL_L2
