@@ -894,6 +894,29 @@ struct StagedLayout {
 };
 static_assert(StagedLayout<kStagedX3>::kEpi <= kSplitCounterSlots, "one split-K counter per X3 epilogue warp");
 
+// X3 sums at most this many K terms into one TMEM accumulator.  The tensor
+// cores' accumulation error grows linearly with the number of terms added
+// into one accumulator (measured on GB300: relative L2 ~8e-9 per term, so
+// 1.5e-5 at K = 2304 against the FP32 bar of 1e-5); consecutive chunks of K
+// go to separate accumulators, summed in order in FP32 by the epilogue.
+constexpr int kX3ChunkTerms = 384;
+
+// Sum, in order and in FP32, of 16 accumulator columns over the first nch
+// K-step chunks (TMEM column offsets chunk_stride apart).
+__device__ __forceinline__ void x3_chunk_sum(uint32_t taddr, int nch, int chunk_stride, float (&sum)[16]) {
+    uint32_t v[16];
+    ptx::tmem_ld16(taddr, v);
+    ptx::tmem_ld_wait();
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) sum[jj] = __uint_as_float(v[jj]);
+    for (int ch = 1; ch < nch; ++ch) {
+        ptx::tmem_ld16(taddr + (uint32_t)(ch * chunk_stride), v);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) sum[jj] = __fadd_rn(sum[jj], __uint_as_float(v[jj]));
+    }
+}
+
 // Persistent kernel whose A operand passes through a staging tile and
 // converter warps on its way to the tensor cores.  Warps 0-1: TMA producers;
 // warp 2: TMEM + MMA issuer; warps 3-10: epilogue; warps 11-14: converters.
@@ -1048,6 +1071,7 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 }
                 ptx::tc_fence_after();
                 bool ok = true;
+                int kc = 0, chunk = 0;   // X3: K step within the current accumulator chunk, and that chunk
                 for (int st = st0; st < st1; ++st, ++g) {
                     const int s = g % S, u = g / S;
                     // conv_done follows raw_full (the converters waited on it),
@@ -1063,11 +1087,16 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     for (int kk = 0; kk < kg; ++kk) {
                         const int i = st * kg + kk;
                         if constexpr (SK == kStagedX3) {
-                            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_stride);
+                            if (kc == p.kpc) {   // this unit's next chunk of K steps
+                                kc = 0;
+                                ++chunk;
+                            }
+                            const bool first = kc++ == 0;
+                            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_stride + chunk * p.chunk_stride);
                             const uint32_t a_head = sb + stg_off + kk * stg_stride, a_tail = sb + kk * p.a_bytes;
                             const uint32_t b_head = sb + op_b_off + kk * p.b_tile_stride;
                             const uint32_t b_tail = sb + op_b_off + (kg + kk) * p.b_tile_stride;
-                            issue_kstep<kTF32>(d_tmem, dhi, a_tail, b_head, p.idesc, kslices, i == st0 * kg);
+                            issue_kstep<kTF32>(d_tmem, dhi, a_tail, b_head, p.idesc, kslices, first);
                             issue_kstep<kTF32>(d_tmem, dhi, a_head, b_tail, p.idesc, kslices, false);
                             issue_kstep<kTF32>(d_tmem, dhi, a_head, b_head, p.idesc, kslices, false);
                         } else {
@@ -1256,6 +1285,8 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             }
             const uint32_t t_row = tmem_base + (uint32_t)(acc * p.acc_stride) + ((uint32_t)(32 * q) << 16);
             if constexpr (SK == kStagedX3) {
+                // K-step chunks this unit wrote (parts of a split differ by a stage).
+                const int nch = ((st1 - st0) * kg + p.kpc - 1) / p.kpc;
                 if (p.split > 1) {
                     // This warp's region of the partial tile (rows erow,
                     // its column groups), column-major: a warp's 32 rows of
@@ -1263,12 +1294,10 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     const int part = uu - t * p.split;
                     float *mine = p.partials + ((size_t)t * p.split + part) * (size_t)(kBM * p.BN);
                     for (int c0 = G * sub; c0 < p.BN; c0 += G * NSUB) {
-                        uint32_t v[16];
-                        ptx::tmem_ld16(t_row + (uint32_t)c0, v);
-                        ptx::tmem_ld_wait();
+                        float sum[16];
+                        x3_chunk_sum(t_row + (uint32_t)c0, nch, p.chunk_stride, sum);
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj)
-                            __stcg(mine + (size_t)(c0 + jj) * kBM + erow, __uint_as_float(v[jj]));
+                        for (int jj = 0; jj < 16; ++jj) __stcg(mine + (size_t)(c0 + jj) * kBM + erow, sum[jj]);
                     }
                     // The accumulator has been read: hand it back to the MMA issuer.
                     ptx::tc_fence_before();
@@ -1304,10 +1333,12 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     continue;
                 }
                 for (int c0 = G * sub; c0 < p.BN; c0 += G * NSUB) {
-                    uint32_t v[16];
-                    ptx::tmem_ld16(t_row + (uint32_t)c0, v);
-                    ptx::tmem_ld_wait();
+                    float sum[16];
+                    x3_chunk_sum(t_row + (uint32_t)c0, nch, p.chunk_stride, sum);
                     if (m >= p.M || n0 + c0 >= p.C_out) continue;
+                    uint32_t v[16];
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) v[jj] = __float_as_uint(sum[jj]);
                     epi_store16<kTF32, true>(p, p.bias, m, img, oh, ow, n0 + c0, v);
                 }
             } else {
@@ -1422,6 +1453,15 @@ int next_pow2(int v) {
     int p = 1;
     while (p < v) p <<= 1;
     return p;
+}
+
+// X3: K steps per accumulator chunk (CB channels a step), and the chunks
+// of the longest part when the nstage = ksteps / kg stages are split.
+int x3_kpc(int CB) { return kX3ChunkTerms / CB > 1 ? kX3ChunkTerms / CB : 1; }
+int x3_chunks(int ksteps, int kg, int split, int CB) {
+    const int nst = ksteps / kg;
+    const int unit_ksteps = (nst + split - 1) / split * kg;
+    return (unit_ksteps + x3_kpc(CB) - 1) / x3_kpc(CB);
 }
 
 int elem_bytes_of(int variant) {
@@ -1686,13 +1726,17 @@ cbs_status plan_tc(cbs_plan_t &p) {
         //   INT8: the MMAs of a tile (flat below N = 64);
         //   X3:   per K step, a fixed share for loading and splitting the A
         //         tile (every N tile repeats it) plus the MMAs, and for a
-        //         split the partial tile written and summed.  A split only
-        //         fills SMs that a single wave of tiles leaves idle.
+        //         split the partial tiles written and summed.  A split fills
+        //         SMs that a single wave of tiles leaves idle; with a wave or
+        //         more, only the fewest parts whose accumulator chunks fit
+        //         TMEM with that N tile.
         // Measured on GB300 (X3): at batch 16 the C_out = 128 list layers run
-        // 10-13% faster with one N tile of 128 than with two of 64; at batch
-        // 1 the chosen splits are the measured best or within a few percent
-        // (e.g. 128->256 3x3 s2 at 20x20: N tile 32 in 4 parts, 14.7 us
-        // against 19.8 us on the CUDA cores).
+        // 10-13% faster with one N tile of 128 than with two of 64, and
+        // 128->128 3x3 at 40x40 takes 68 us in 3 parts of N = 128 against
+        // 87 us unsplit with N = 64; at batch 1 the chosen splits are the
+        // measured best or within a few percent (e.g. 128->256 3x3 s2 at
+        // 20x20: N tile 32 in 4 parts, 14.7 us against 19.8 us on the CUDA
+        // cores).
         int BN = d.force_block_n > 0 ? d.force_block_n : full;
         int split = d.force_split_k > 1 ? d.force_split_k : 1;
         {
@@ -1706,16 +1750,21 @@ cbs_status plan_tc(cbs_plan_t &p) {
                     if (cost < best * 0.99) { best = cost; BN = c; }
                     continue;
                 }
-                const int sp0 = d.force_split_k >= 1 ? d.force_split_k : 1;
-                const int sp1 = d.force_split_k >= 1 ? d.force_split_k : (tiles < kNumSMs ? 16 : 1);
+                const bool forced = d.force_split_k >= 1;
+                const int sp0 = forced ? d.force_split_k : 1;
+                const int sp1 = forced ? d.force_split_k : 16;
                 for (int sp = sp0; sp <= sp1; ++sp) {
                     const int g = kgroup_of(c, sp);
                     const int nst = ksteps / g;
                     if (sp > nst) break;
+                    // two accumulator buffers of (K-step chunks per part) x N columns in TMEM
+                    if (x3_chunks(ksteps, g, sp, CB) * next_pow2(c) > 256) continue;
                     const long long units = tiles * sp;
                     const double cost = (double)((units + kNumSMs - 1) / kNumSMs) * ((nst + sp - 1) / sp) * g *
-                                            (128.0 + c) + (sp > 1 ? 2.0 * sp * c : 0.0);
+                                            (128.0 + c) + (sp > 1 ? 4.0 * sp * c : 0.0);
                     if (cost < best * 0.99) { best = cost; BN = c; split = sp; }
+                    // A wave of tiles or more: only the fewest parts whose chunks fit TMEM.
+                    if (!forced && tiles >= kNumSMs) break;
                 }
             }
         }
@@ -1725,6 +1774,9 @@ cbs_status plan_tc(cbs_plan_t &p) {
         p.b_resident = 0;
         const int kstep_bytes = kstep_bytes_of(BN);
         const int kg = kgroup_of(BN, split);
+        if (x3 && x3_chunks(ksteps, kg, split, CB) * next_pow2(BN) > 256)
+            return fail(CBS_ERR_UNSUPPORTED, "3xTF32: %d K-step chunks of N = %d exceed TMEM (split K or narrow N)",
+                        x3_chunks(ksteps, kg, split, CB), BN);
         if (d.force_k_group > 0 && kg != d.force_k_group)
             return fail(CBS_ERR_UNSUPPORTED, "INT8: k_group %d does not divide %d K steps", d.force_k_group, ksteps);
         p.k_group = kg;
@@ -1952,8 +2004,8 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
         P.in_w = d.w;
     } else if (x3) {
         P.stg_bytes = kBM * XB;     // fp32 staging rows, swizzled like the operands (XB = RB)
-        P.kpc = P.ksteps;
-        P.nchunks = 1;
+        P.kpc = x3_kpc(CB);
+        P.nchunks = x3_chunks(P.ksteps, P.kg, P.split, CB);
         P.stg_mask = P.op_mask = RB == 128 ? 7u : RB == 64 ? 3u : 1u;
         P.bias = static_cast<const float *>(bias);
     } else {
@@ -1970,7 +2022,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     // sit at power-of-two column offsets inside a buffer.
     P.chunk_stride = next_pow2(BN);
     {
-        const int cols = i8 ? P.nchunks * P.chunk_stride : mmul * P.bnp;
+        const int cols = staged ? P.nchunks * P.chunk_stride : mmul * P.bnp;
         P.acc_stride = next_pow2(cols) < 16 ? 16 : next_pow2(cols);
     }
     P.tmem_cols = (uint32_t)(2 * P.acc_stride < 32 ? 32 : 2 * P.acc_stride);

@@ -223,3 +223,78 @@ def test_split_k_residual_two_inputs(cuda_lib):
     want = oracle.conv_bn_act_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, 1, 1, act=B.CBS_ACT_IDENTITY,
                                   residual=np.ascontiguousarray(r.transpose(0, 3, 1, 2)))
     assert rel_l2(nhwc_to_nchw(y.cpu().numpy()), want) <= TOL_FP32_REL_L2
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("ow_case", [(40, 48), (20, 32)])
+def test_padded_rows_and_guard_bands_untouched(cuda_lib, ow_case):
+    """NCHW output with a padded row pitch from the 3xTF32 kernel (unsplit
+    and split): pad columns and a guard band after the buffer keep their
+    sentinel."""
+    size, pitch = ow_case
+    spec = wl.LayerSpec(64, 32, 3, 1, size)
+    x, p = wl.layer_inputs(spec, 2, layer_index=37)
+    for split in (1, 3):
+        desc = desc_x3(2, spec, out_layout=B.CBS_NCHW, out_row_stride=pitch, force_split_k=split)
+        layer = FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps)
+        assert layer.plan.variant == X3 and layer.plan.split_k == split
+        guard = 4096
+        n_el = 2 * 32 * size * pitch
+        buf = torch.full((n_el + guard,), float("nan"), dtype=torch.float32, device="cuda")
+        sentinel_bits = buf[:1].view(torch.int32).item()
+        y = buf[:n_el].view(2, 32, size, pitch)
+        layer(layer.pack_input(torch.from_numpy(x).cuda()), y)
+        torch.cuda.synchronize()
+        host = buf.cpu()
+        bits = host.view(torch.int32).numpy()
+        yv = host[:n_el].view(2, 32, size, pitch).numpy()
+        assert np.all(bits[n_el:] == sentinel_bits)
+        assert np.all(yv[..., size:].view(np.int32) == sentinel_bits)
+        assert rel_l2(yv[..., :size], ref_of(spec, x, p)) <= TOL_FP32_REL_L2
+
+
+@pytest.mark.gpu
+def test_empty_batch_is_a_noop(cuda_lib):
+    spec = wl.LayerSpec(64, 64, 3, 1, 8)
+    _, p = wl.layer_inputs(spec, 1)
+    layer = FusedConvBnSilu(desc_x3(0, spec), p.w, p.gamma, p.beta, p.mean, p.var, p.eps)
+    assert layer.plan.variant == X3
+    y = layer(torch.empty((0, 8, 8, 64), dtype=torch.float32, device="cuda"),
+              torch.empty((0, 8, 8, 64), dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+    assert y.numel() == 0
+
+
+@pytest.mark.gpu
+def test_automatic_split_matches_unsplit(cuda_lib):
+    """A batch-1 list layer through the default plan (3xTF32, K in parts)
+    against the same layer unsplit: both within the FP32 bar, and each
+    launch of the split plan gives the same bits."""
+    spec = wl.LAYER_LIST[10]
+    x, p = wl.layer_inputs(spec, 1, layer_index=10)
+    auto = FusedConvBnSilu(desc_x3(1, spec), p.w, p.gamma, p.beta, p.mean, p.var, p.eps, tuned=False)
+    one = FusedConvBnSilu(desc_x3(1, spec, force_split_k=1), p.w, p.gamma, p.beta, p.mean, p.var, p.eps,
+                          tuned=False)
+    assert auto.plan.split_k > 1 and one.plan.split_k == 1
+    xd = torch.from_numpy(x).cuda()
+    ya = [nhwc_to_nchw(auto(auto.pack_input(xd)).cpu().numpy()) for _ in range(3)]
+    y1 = nhwc_to_nchw(one(one.pack_input(xd)).cpu().numpy())
+    want = ref_of(spec, x, p)
+    assert rel_l2(ya[0], want) <= TOL_FP32_REL_L2 and rel_l2(y1, want) <= TOL_FP32_REL_L2
+    for y in ya[1:]:
+        assert np.array_equal(y.view(np.int32), ya[0].view(np.int32))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("c_in,kw", [(512, {"force_split_k": 1, "force_block_n": 16}), (1024, {})])
+def test_long_k_within_fp32_bar(cuda_lib, c_in, kw):
+    """Long reductions (K = 4608 in one part, K = 9216 through the default
+    plan): the tensor cores' accumulation error grows with the number of
+    terms in one accumulator, so K is summed in chunks of at most 384 terms
+    into separate accumulators and the chunks are added in FP32."""
+    spec = wl.LayerSpec(c_in, 16, 3, 1, 12, 12)
+    x, p = wl.layer_inputs(spec, 1, layer_index=41)
+    y, layer = run_x3(spec, x, p, **kw)
+    if "force_split_k" in kw:
+        assert layer.plan.split_k == 1
+    assert rel_l2(y, ref_of(spec, x, p)) <= TOL_FP32_REL_L2
