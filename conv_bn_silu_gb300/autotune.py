@@ -3,8 +3,8 @@ that `tuning.tuned_desc` reads.
 
 For every distinct layer shape of the benchmark workloads (the twelve-layer
 list at batch 16 in BF16, TF32 and INT8, the 40-layer chain at batch 16 in
-BF16 and TF32, both at batch 1 in FP32, and the list at batch 16 in FP32 with
-NHWC activations on the 3xTF32 kernel), each candidate configuration is
+BF16 and TF32, both at batch 1 in FP32, and the list at batches 1 and 16 in
+FP32 with NHWC activations on the 3xTF32 kernel), each candidate configuration is
 planned, folded and timed as a CUDA graph of repeated launches over rotating
 input copies.  A shape gets a table entry when its fastest candidate beats the
 cost-model plan by 3% or more.
@@ -39,8 +39,8 @@ def workload_shapes():
     for prec in ("bf16", "tf32"):
         out += [(prec, 16, s, B.CBS_NHWC) for s in chain]
     out += [("fp32", 1, s, B.CBS_NCHW) for s in list(wl.LAYER_LIST) + chain + [wl.SINGLE_LAYER]]
-    # FP32 with NHWC activations at batch 16: the 3xTF32 tensor-core kernel
-    out += [("fp32", 16, s, B.CBS_NHWC) for s in wl.LAYER_LIST]
+    # FP32 with NHWC activations: the 3xTF32 tensor-core kernel
+    out += [("fp32", n, s, B.CBS_NHWC) for n in (16, 1) for s in wl.LAYER_LIST]
     seen, uniq = set(), []
     for prec, n, s, lay in out:
         k = (prec, n, s, lay)
@@ -56,10 +56,10 @@ def candidates(prec, spec, base):
     bns = [b for b in (32, 48, 64, 96, 128, 192, 256) if b <= full] or [full]
     if prec == "fp32":
         if base.in_layout == B.CBS_NHWC:
-            # 3xTF32: the variant is forced with the tile fields (a forced
-            # tile field alone keeps an FP32 plan on the CUDA cores).
-            for kg, bn in itertools.product((1, 2, 3, 4), bns):
-                yield dict(force_variant=B.CBS_VARIANT_TC_TF32X3, force_k_group=kg, force_block_n=bn)
+            # 3xTF32: N tile and K parts; the variant is forced with them (a
+            # forced tile field alone keeps an FP32 plan on the CUDA cores).
+            for sk, bn in itertools.product((1, 2, 3, 4, 5, 6, 8, 9, 12, 16), bns):
+                yield dict(force_variant=B.CBS_VARIANT_TC_TF32X3, force_split_k=sk, force_block_n=bn)
         else:
             # the CUDA-core kernel
             for (bm, bn), sk in itertools.product(SIMT_TILES, (1, 2, 3, 4, 6, 8, 12, 16)):
