@@ -340,7 +340,9 @@ CBS_API cbs_status cbs_maxpool2d(const void *x, void *y, int n, int c, int h, in
  * scratch comes from a 16 MiB array the library defines in device memory
  * (present on every GPU that loads the library, until the process exits).
  *   p: a CBS_VARIANT_SIMT_FP32 plan with workspace_bytes <= 16 MiB (larger
- *      plans fail with CBS_ERR_WORKSPACE; other variants CBS_ERR_UNSUPPORTED);
+ *      plans fail with CBS_ERR_WORKSPACE; other variants CBS_ERR_UNSUPPORTED).
+ *      An FP32 layer with NHWC input plans TC_TF32X3 by default: set
+ *      force_variant = CBS_VARIANT_SIMT_FP32 in its descriptor for this call;
  *   x, w_packed, bias, y: as for cbs_conv_bn_silu_f32 (device, 16-byte aligned).
  * The first call on a device looks up the array's address with that device
  * current; make it before any stream capture.  Every call shares the array
