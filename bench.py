@@ -107,6 +107,7 @@ WORKLOADS = {
     "chain_fp32_n1": dict(kind="chain", n=1, prec="fp32"),
     "chain_bf16_n16": dict(kind="chain", n=16, prec="bf16"),
     "chain_tf32_n16": dict(kind="chain", n=16, prec="tf32"),
+    "chain_fp32_n1_nhwc": dict(kind="chain", n=1, prec="fp32", layout="nhwc"),
     # The list with the residual form of the epilogue, y = SiLU(BN(conv)) + r, on every
     # stride-1 layer whose input and output shapes match (a bottleneck's skip add).
     "layer_list_bf16_n16_residual": dict(kind="list", layers=wl.LAYER_LIST, n=16, prec="bf16", residual=True),
@@ -119,7 +120,7 @@ WORKLOADS = {
 }
 EXTRA_DEFAULT = ("layer_list_bf16_n16", "layer_list_tf32_n16", "layer_list_int8_n16", "chain_fp32_n1",
                  "chain_bf16_n16", "layer_list_bf16_n16_residual", "layer_list_int8_n16_asym",
-                 "layer_list_fp32_n16_nhwc", "layer_list_fp32_n1_nhwc")
+                 "layer_list_fp32_n16_nhwc", "layer_list_fp32_n1_nhwc", "chain_fp32_n1_nhwc")
 
 
 # DRAM traffic of the dominant kernel over one step of a workload, from one
@@ -242,9 +243,12 @@ class ChainWorkload:
 
     def __init__(self, cfg, device):
         import torch
+        from conv_bn_silu_gb300 import _binding as B
         from conv_bn_silu_gb300.chain import Chain
         self.cfg, self.n, self.prec = cfg, cfg["n"], cfg["prec"]
-        self.chain = Chain(self.prec, self.n, device=device)
+        lay = B.CBS_NHWC if cfg.get("layout") == "nhwc" else None
+        self.chain = Chain(self.prec, self.n, device=device, layout=lay)
+        self.nhwc = self.chain.layout == B.CBS_NHWC
         self.frame = torch.from_numpy(wl.frame(self.n)).to(device)
         self.specs = [cl.spec for cl in self.chain.specs]
         self.layers = self.chain.layers

@@ -9,8 +9,9 @@ two-input layer: it reads the upsampled layer 10 and layer 7 straight from
 their buffers (the channel concatenation happens in its input loads), so the
 only glue kernel is the 2x upsample.
 
-FP32 runs the CUDA-core variant in NCHW; TF32, BF16 and INT8 run the
-tensor-core variants in NHWC, where only the frame needs packing.
+FP32 runs in NCHW by default, on the CUDA cores; with layout=NHWC its layers
+take the 3xTF32 tensor-core variant (the FP32 bar).  TF32, BF16 and INT8 run
+the tensor-core variants in NHWC.  In NHWC only the frame needs packing.
 """
 from __future__ import annotations
 
@@ -25,13 +26,17 @@ PRECS = {"fp32": B.CBS_FP32, "tf32": B.CBS_TF32, "bf16": B.CBS_BF16}
 
 
 class Chain:
-    def __init__(self, prec: str, n: int, seed: int = 0, device="cuda"):
+    def __init__(self, prec: str, n: int, seed: int = 0, device="cuda", layout: int | None = None):
         self.prec = prec
         self.n = n
         self.device = torch.device(device)
         self.specs = wl.chain_layers()
         cp = PRECS[prec]
-        self.layout = B.CBS_NCHW if prec == "fp32" else B.CBS_NHWC
+        if layout is None:
+            layout = B.CBS_NCHW if prec == "fp32" else B.CBS_NHWC
+        if prec != "fp32" and layout != B.CBS_NHWC:
+            raise ValueError("the tensor-core precisions run the chain in NHWC")
+        self.layout = layout
         self.layers = []
         for i, cl in enumerate(self.specs):
             s = cl.spec

@@ -44,9 +44,12 @@ def bf16_round(a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).float().numpy()
 
 
-@pytest.mark.parametrize("prec,n", [("fp32", 1), ("tf32", 16), ("bf16", 16)])
-def test_chain_teacher_forced(cuda_lib, prec, n):
-    chain = Chain(prec, n)
+@pytest.mark.parametrize("prec,n,layout", [("fp32", 1, None), ("fp32", 1, B.CBS_NHWC), ("tf32", 16, None),
+                                           ("bf16", 16, None)])
+def test_chain_teacher_forced(cuda_lib, prec, n, layout):
+    """FP32 in NHWC runs the 3xTF32 tensor-core variant (split-K on the small
+    layers) and is held to the FP32 bar like the CUDA-core chain."""
+    chain = Chain(prec, n, layout=layout)
     frame = wl.frame(n)
     sel = [0] if n == 1 else [0, n - 1]
     ins, outs = oracle_chain(chain, np.ascontiguousarray(frame[sel]))
