@@ -11,9 +11,10 @@ from conv_bn_silu_gb300.chain import Chain
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("prec,n", [("bf16", 2), ("fp32", 1), ("tf32", 1)])
-def test_chain_bits_with_and_without_pdl(cuda_lib, prec, n):
-    chain = Chain(prec, n)
+@pytest.mark.parametrize("prec,n,layout", [("bf16", 2, None), ("fp32", 1, None), ("tf32", 1, None),
+                                           ("fp32", 1, B.CBS_NHWC)])   # 3xTF32, split-K counters across launches
+def test_chain_bits_with_and_without_pdl(cuda_lib, prec, n, layout):
+    chain = Chain(prec, n, layout=layout)
     g = torch.Generator().manual_seed(3)
     frame = torch.randn((n, 3, 640, 640), generator=g).cuda()
     outs = {}
