@@ -72,8 +72,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        // try_wait with a suspend-time hint: the thread may sleep up to 1 us
+        // in the barrier instead of spinning, which leaves issue slots to
+        // the warps that have work (measured: BF16 list 0.2735 -> 0.2697 ms).
+        uint32_t ok;
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "r"(1000u)
+            : "memory");
+        if (ok) return true;
         if (globaltimer() - t0 > limit_ns) return false;
     }
 }
