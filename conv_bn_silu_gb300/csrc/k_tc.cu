@@ -1277,7 +1277,7 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             tile_coords(t, p.n_tiles, kBM, m0, n0, p.BN);
             const int m = m0 + erow;
             int img = 0, oh = 0, ow = 0;
-            if (m < p.M) {
+            if (m < p.M && !p.out_nhwc) {   // NHWC addresses need only m
                 img = m / p.OHW;
                 const int rem = m - img * p.OHW;
                 oh = rem / p.OW;
