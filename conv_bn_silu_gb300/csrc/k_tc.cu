@@ -713,7 +713,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 m = (img * p.OH + oh) * p.OW + ow;
             } else {
                 valid = m < p.M;
-                if (valid) {
+                if (valid && !p.out_nhwc) {   // NHWC addresses need only m
                     img = m / p.OHW;
                     const int rem = m - img * p.OHW;
                     oh = rem / p.OW;
