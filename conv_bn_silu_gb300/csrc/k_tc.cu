@@ -893,6 +893,7 @@ struct StagedLayout {
     static constexpr int kGroup = SK == kStagedI8 ? 8 : 16;   // accumulator columns per TMEM load
 };
 static_assert(StagedLayout<kStagedX3>::kEpi <= kSplitCounterSlots, "one split-K counter per X3 epilogue warp");
+static_assert(StagedLayout<kStagedI8>::kGroup == 8, "the INT8 epilogue loads its bias and scales as two 16-byte pairs");
 
 // X3 sums at most this many K terms into one TMEM accumulator.  The tensor
 // cores' accumulation error grows linearly with the number of terms added
@@ -1345,8 +1346,23 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 for (int c0 = G * sub; c0 < p.BN; c0 += G * NSUB) {
                     const int nbase = n0 + c0;
                     int accv[G];
+                    float mcv[G];
+                    if (nbase + G <= p.C_out) {   // G = 8: two 16-byte loads each (both arrays 16-byte aligned)
+                        const int4 b0 = __ldg(reinterpret_cast<const int4 *>(p.bias_i32 + nbase));
+                        const int4 b1 = __ldg(reinterpret_cast<const int4 *>(p.bias_i32 + nbase + 4));
+                        const float4 s0 = __ldg(reinterpret_cast<const float4 *>(p.m_c + nbase));
+                        const float4 s1 = __ldg(reinterpret_cast<const float4 *>(p.m_c + nbase + 4));
+                        accv[0] = b0.x; accv[1] = b0.y; accv[2] = b0.z; accv[3] = b0.w;
+                        accv[4] = b1.x; accv[5] = b1.y; accv[6] = b1.z; accv[7] = b1.w;
+                        mcv[0] = s0.x; mcv[1] = s0.y; mcv[2] = s0.z; mcv[3] = s0.w;
+                        mcv[4] = s1.x; mcv[5] = s1.y; mcv[6] = s1.z; mcv[7] = s1.w;
+                    } else {
 #pragma unroll
-                    for (int jj = 0; jj < G; ++jj) accv[jj] = nbase + jj < p.C_out ? __ldg(p.bias_i32 + nbase + jj) : 0;
+                        for (int jj = 0; jj < G; ++jj) {
+                            accv[jj] = nbase + jj < p.C_out ? __ldg(p.bias_i32 + nbase + jj) : 0;
+                            mcv[jj] = nbase + jj < p.C_out ? __ldg(p.m_c + nbase + jj) : 0.0f;
+                        }
+                    }
                     for (int ch = 0; ch < p.nchunks; ++ch) {
                         uint32_t v[G];
                         ptx::tmem_ld8(t_row + (uint32_t)(ch * p.chunk_stride + c0), v);
@@ -1358,8 +1374,7 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     uint32_t qw[G / 4] = {};
 #pragma unroll
                     for (int jj = 0; jj < G; ++jj) {
-                        const int qv = requant_i8(accv[jj], nbase + jj < p.C_out ? __ldg(p.m_c + nbase + jj) : 0.0f,
-                                                  p.inv_s_y, p.zp_y);
+                        const int qv = requant_i8(accv[jj], mcv[jj], p.inv_s_y, p.zp_y);
                         qw[jj >> 2] |= (uint32_t)(uint8_t)(int8_t)qv << (8 * (jj & 3));
                     }
                     if (p.out_nhwc) {
