@@ -220,6 +220,66 @@ __global__ void __launch_bounds__(kPackSmallThreads) pack_nhwc_small_kernel(cons
     }
 }
 
+// Four consecutive pixels of 4 padded channels, packed into 16, 32 or 64
+// contiguous output bytes.
+template <typename T>
+__device__ __forceinline__ void store16(T *dst, const T (&v)[16]);
+template <>
+__device__ __forceinline__ void store16<float>(float *dst, const float (&v)[16]) {
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+        reinterpret_cast<float4 *>(dst)[p] = make_float4(v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3]);
+}
+template <>
+__device__ __forceinline__ void store16<__nv_bfloat16>(__nv_bfloat16 *dst, const __nv_bfloat16 (&v)[16]) {
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        w[k] = (uint32_t)__bfloat16_as_ushort(v[2 * k]) | ((uint32_t)__bfloat16_as_ushort(v[2 * k + 1]) << 16);
+    reinterpret_cast<uint4 *>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4 *>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+template <>
+__device__ __forceinline__ void store16<int8_t>(int8_t *dst, const int8_t (&v)[16]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        w[k] = (uint32_t)(uint8_t)v[4 * k] | ((uint32_t)(uint8_t)v[4 * k + 1] << 8) |
+               ((uint32_t)(uint8_t)v[4 * k + 2] << 16) | ((uint32_t)(uint8_t)v[4 * k + 3] << 24);
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ float lane_of(const float4 &v, int p) {
+    return p == 0 ? v.x : (p == 1 ? v.y : (p == 2 ? v.z : v.w));
+}
+
+// pack_nhwc_small_kernel for 4 padded channels and W a multiple of 4: four
+// pixels per thread, one 16-byte load per input plane and 16-64 contiguous
+// output bytes, so each thread keeps several wide loads in flight.
+template <typename T>
+__global__ void __launch_bounds__(kPackSmallThreads) pack_nhwc_quad_kernel(const float *__restrict__ x,
+                                                                           T *__restrict__ out, int C, int H, int W,
+                                                                           int rows, float s_x, int zp) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+    const int w4 = blockIdx.x * kPackSmallThreads + threadIdx.x;   // quad of pixels 4 w4 .. 4 w4 + 3
+    if (w4 >= (W >> 2)) return;
+    const size_t hw = (size_t)H * W;   // a multiple of 4
+    for (int row = blockIdx.y; row < rows; row += gridDim.y) {   // row = n * H + h
+        const int n = row / H, h = row - n * H;
+        const float4 *src = reinterpret_cast<const float4 *>(x + (size_t)n * C * hw + (size_t)h * W) + w4;
+        float4 pl[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) pl[c] = c < C ? __ldg(src + c * (hw >> 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        T v[16];
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[4 * p + c] = c < C ? convert_out<T>(lane_of(pl[c], p), s_x, zp) : zero_code<T>();
+        store16<T>(out + ((size_t)row * W + 4 * (size_t)w4) * 4, v);
+    }
+}
+
 template <typename T>
 __global__ void pack_nchw_kernel(const float *__restrict__ x, T *__restrict__ out, size_t count,
                                  float s_x, int zp) {
@@ -374,7 +434,16 @@ cudaError_t launch_fold(const FoldLaunch &L, cudaStream_t s) {
 
 cudaError_t launch_pack_input(const float *x, void *out, int N, int C, int H, int W, int c_pad,
                               int to_nhwc, int dtype, float s_x, int zp, cudaStream_t s) {
-    if (to_nhwc && c_pad <= 8) {
+    if (to_nhwc && c_pad == 4 && W % 4 == 0) {   // x and out are 16-byte aligned (checked by the caller)
+        const int gx = (W / 4 + kPackSmallThreads - 1) / kPackSmallThreads;
+        const int rows = N * H;
+        int gy = kNumSMs * 32 / gx;
+        gy = gy < 1 ? 1 : (gy > rows ? rows : (gy > 65535 ? 65535 : gy));
+        const dim3 grid(gx, gy);
+        if (dtype == 0) launch_kernel(pack_nhwc_quad_kernel<float>, grid, kPackSmallThreads, 0, s, x, (float *)out, C, H, W, rows, s_x, zp);
+        else if (dtype == 1) launch_kernel(pack_nhwc_quad_kernel<__nv_bfloat16>, grid, kPackSmallThreads, 0, s, x, (__nv_bfloat16 *)out, C, H, W, rows, s_x, zp);
+        else launch_kernel(pack_nhwc_quad_kernel<int8_t>, grid, kPackSmallThreads, 0, s, x, (int8_t *)out, C, H, W, rows, s_x, zp);
+    } else if (to_nhwc && c_pad <= 8) {
         const int gx = (W + kPackSmallThreads - 1) / kPackSmallThreads;
         const int rows = N * H;
         int gy = kNumSMs * 32 / gx;

@@ -62,11 +62,13 @@ def test_pack_input_fp32_nhwc(cuda_lib):
 
 @pytest.mark.parametrize("prec", [B.CBS_BF16, B.CBS_INT8, B.CBS_TF32])
 @pytest.mark.parametrize("c_in", [3, 8, 24])
-def test_pack_input_nhwc_exact(cuda_lib, prec, c_in):
+@pytest.mark.parametrize("w", [21, 24])
+def test_pack_input_nhwc_exact(cuda_lib, prec, c_in, w):
     """Entry packing to NHWC, padded channels zero: bf16 round-to-nearest-even,
     int8 q = rne(clamp(x / s_x, -128, 127)), float copied; few channels take
-    the one-thread-per-pixel kernel, more the tiled transpose."""
-    n, h, w = 2, 19, 21
+    the one-thread-per-pixel kernel (four pixels per thread when 4 padded
+    channels and W a multiple of 4), more the tiled transpose."""
+    n, h = 2, 19
     spec = wl.LayerSpec(c_in, 32, 3, 1, h, w)
     x, p = wl.layer_inputs(spec, n)
     s_x = 0.0125
