@@ -298,3 +298,54 @@ def test_long_k_within_fp32_bar(cuda_lib, c_in, kw):
     if "force_split_k" in kw:
         assert layer.plan.split_k == 1
     assert rel_l2(y, ref_of(spec, x, p)) <= TOL_FP32_REL_L2
+
+
+def test_planner_matches_measured_choices(cuda_lib):
+    """The 3xTF32 planner's N tile and K parts for the list layers (host-side,
+    no GPU call) are the configurations measured fastest on GB300, or within a
+    few percent of them: at batch 16 one N tile of 128 in 2 parts for the
+    128->128 3x3 layer, 3 parts of 128 for 256->256 3x3; at batch 1 K parts
+    that fill the SMs."""
+    want = {
+        16: {6: (128, 1), 7: (128, 2), 8: (256, 3), 10: (128, 3), 11: (128, 1)},
+        1: {5: (64, 3), 8: (32, 4), 9: (32, 4), 11: (32, 2)},
+    }
+    for n, layers in want.items():
+        for li, (bn, split) in layers.items():
+            s = wl.LAYER_LIST[li]
+            pl = B.cbs_plan(make_desc(n, s.c_in, s.h, s.width, s.c_out, s.k, s.stride, s.pad, prec=B.CBS_FP32,
+                                      in_layout=B.CBS_NHWC))
+            assert pl.variant == X3 and (pl.block_n, pl.split_k) == (bn, split), (n, li, pl.block_n, pl.split_k)
+
+
+def test_planner_keeps_accumulators_in_tmem(cuda_lib):
+    """Every 3xTF32 plan over a spread of shapes: two accumulator buffers of
+    (K-step chunks of at most 384 terms in the longest part) x N columns fit
+    the 512 TMEM columns, parts never outnumber pipeline stages, and the
+    grid never exceeds the SMs or the units."""
+    rng = np.random.default_rng(5)
+    def npow2(v):
+        q = 1
+        while q < v:
+            q *= 2
+        return q
+    for _ in range(400):
+        c_in = int(rng.choice([8, 16, 24, 32, 64, 96, 128, 256, 384, 512, 1024]))
+        c_out = int(rng.choice([16, 32, 48, 64, 96, 128, 192, 256, 320]))
+        k = int(rng.choice([1, 3, 5]))
+        stride = int(rng.choice([1, 2]))
+        hw = int(rng.integers(k, 90))
+        n = int(rng.choice([1, 2, 16]))
+        d = make_desc(n, c_in, hw, hw, c_out, k, stride, prec=B.CBS_FP32, in_layout=B.CBS_NHWC,
+                      force_variant=X3)
+        pl = B.cbs_plan(d)
+        cb = pl.block_k
+        ksteps = k * k * pl.c_in_pad // cb
+        nst = ksteps // pl.k_group
+        assert 1 <= pl.split_k <= nst
+        unit = -(-nst // pl.split_k) * pl.k_group
+        kpc = max(1, 384 // cb)
+        chunks = -(-unit // kpc)
+        assert 2 * chunks * npow2(pl.block_n) <= 512, (c_in, c_out, k, hw, n, pl.block_n, pl.split_k)
+        units = pl.m_tiles * pl.n_tiles * pl.split_k
+        assert pl.grid_ctas == min(152, units)
