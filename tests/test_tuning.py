@@ -58,3 +58,29 @@ def test_two_input_layers_are_keyed_apart():
     table = {shape_key(one): {"force": {"force_block_n": 64}}}
     assert tuned_desc(one, table).force_block_n == 64
     assert tuned_desc(two, table).force_block_n == 0
+
+
+def test_fp32_nhwc_candidates_force_the_variant(cuda_lib):
+    """A forced tile field keeps an FP32 plan on the CUDA cores, so every
+    autotune candidate for an FP32 NHWC shape names its variant too, and each
+    one that plans lands on that variant (host-side, no GPU call)."""
+    from conv_bn_silu_gb300 import autotune
+    for prec, n, spec, lay in autotune.workload_shapes():
+        if prec != "fp32" or lay != B.CBS_NHWC:
+            continue
+        base = make_desc(n, spec.c_in, spec.h, spec.width, spec.c_out, spec.k, spec.stride, spec.pad,
+                         prec=B.CBS_FP32, in_layout=lay, out_layout=lay)
+        for force in autotune.candidates(prec, spec, base):
+            assert force.get("force_variant") == B.CBS_VARIANT_TC_TF32X3, force
+            d = make_desc(n, spec.c_in, spec.h, spec.width, spec.c_out, spec.k, spec.stride, spec.pad,
+                          prec=B.CBS_FP32, in_layout=lay, out_layout=lay, **force)
+            try:
+                pl = B.cbs_plan(d)
+            except B.CbsError:
+                continue
+            assert pl.variant == B.CBS_VARIANT_TC_TF32X3
+    # the table's FP32 NHWC entries force the variant as well
+    for key, entry in tuning.load_table().items():
+        fields = key.split(":")
+        if fields[0] == str(B.CBS_FP32) and fields[9] == str(B.CBS_NHWC):
+            assert entry["force"].get("force_variant") == B.CBS_VARIANT_TC_TF32X3, key
