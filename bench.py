@@ -9,8 +9,11 @@ device duration is measured in the same run.  Inputs and outputs rotate over
 five copies (5 x 55 MB > the 126 MB L2), so no step finds its inputs in L2
 from the step before.
 
-Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on
-the host cores on the same workload and metric instead.
+Prints ONE compact JSON line (rank 0): the headline value, the roofline of
+the dominant kernel, the end-to-end figure, the CPU baseline and the clocks.
+`--detail PATH` writes the full record (per-layer rows; with `--extra`, the
+other workloads too).  `--impl reference` times the CPU oracle on the host
+cores on the same workload and metric instead.
 """
 from __future__ import annotations
 
@@ -367,7 +370,7 @@ def measure(name, steps, warmup, device, peaks, sample_clocks=False):
                "variant": VARIANT_NAMES.get(layer.plan.variant, str(layer.plan.variant)),
                "tile": f"{layer.plan.block_m}x{layer.plan.block_n}", "split_k": layer.plan.split_k,
                "mflop": round(f / 1e6, 2), "alg_mb": round(by / 1e6, 3), "bound": bound,
-               "roofline_us": round(max(t_c, t_m) * 1e6, 3)}
+               "roofline_us": round(max(t_c, t_m) * 1e6, 3), "compute_us": round(t_c * 1e6, 3)}
         if per_layer_us is not None:
             u = float(per_layer_us[j])
             row.update(us=round(u, 3), tflops=round(f / (u * 1e-6) / 1e12, 3),
@@ -396,8 +399,10 @@ def measure(name, steps, warmup, device, peaks, sample_clocks=False):
         k3 = [r for r in rows if " k3 " in r["shape"] and r["bound"] == "compute"]
         mem = [r for r in rows if r not in k3]
         if k3:
-            out["k3_compute_bound_frac_of_tensor_peak"] = round(
-                sum(r["mflop"] for r in k3) * 1e6 / (sum(r["us"] for r in k3) * 1e-6) / (peak * 1e12), 4)
+            # each layer against the compute peak of the arithmetic its variant runs
+            # (FP32 ALU, TF32, BF16, or TF32/3 for the 3xTF32 kernel)
+            out["k3_compute_bound_frac_of_own_compute_peak"] = round(
+                sum(r["compute_us"] for r in k3) / sum(r["us"] for r in k3), 4)
         if mem:
             out["hbm_bound_frac_of_hbm"] = round(
                 sum(r["alg_mb"] for r in mem) * 1e6 / (sum(r["us"] for r in mem) * 1e-6) / (hbm * 1e9), 4)
@@ -486,7 +491,7 @@ def run_ours(args, rank: int, world: int):
         "gpu_launches": args.steps * w.launches_per_step,
         "e2e": e2e, "clocks": clocks, "peaks_source": peak_src,
     }
-    if rank == 0 and not args.no_extra:
+    if rank == 0 and args.extra:
         extra = {}
         for name in EXTRA_DEFAULT:
             if name == args.workload:
@@ -502,6 +507,31 @@ def run_ours(args, rank: int, world: int):
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w)
     return out
+
+
+def compact(out: dict) -> dict:
+    """The one JSON line the bench prints: the headline figures only (a few
+    hundred bytes).  Per-layer rows, the other workloads' summaries and the
+    CPU baseline's per-layer times go to the --detail file."""
+    rf = out["roofline"]
+    line = {k: out[k] for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                                "us_per_frame", "higher_is_better", "scaling", "vs_baseline", "dtype", "data")}
+    cfg = out["config"]
+    line["config"] = {k: cfg[k] for k in ("workload", "layers", "batch", "layout", "l2", "parallelism", "launch")}
+    line["roofline"] = {k: rf[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+    line["roofline"].update(kernel=rf["kernel"], algorithmic_bytes=rf["algorithmic_bytes"],
+                            peak_source=rf["peak_source"],
+                            frac_of_layer_roofline_sum=rf["frac_of_layer_roofline_sum"])
+    e = out["e2e"]
+    line["e2e"] = {k: e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step", "ms_per_step",
+                                     "mode") if k in e}
+    cb = out.get("cpu_baseline")
+    if cb is not None:
+        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample", "machine")}
+    line["gpu_launches"] = out["gpu_launches"]
+    ck = out.get("clocks") or {}
+    line["clocks"] = {k: ck.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")}
+    return line
 
 
 def run_e2e(w, device, args, flops_step, world):
@@ -663,7 +693,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="layer_list_fp32_n1", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-extra", action="store_true", help="skip the other configs' summaries")
+    ap.add_argument("--extra", action="store_true",
+                    help="also measure the other workloads (summaries go to the --detail file)")
+    ap.add_argument("--no-extra", action="store_true", help="(default) measure the chosen workload only")
+    ap.add_argument("--detail", default=None,
+                    help="write the full record (per-layer rows, clocks, extras, CPU baseline detail) "
+                         "as JSON to this path")
     ap.add_argument("--no-pdl", action="store_true",
                     help="plain launches instead of programmatic dependent launches (for comparison)")
     args = ap.parse_args()
@@ -686,7 +721,12 @@ def main():
     build.build()
     out = run_ours(args, rank, world)
     if rank == 0:
-        print(json.dumps(out), flush=True)
+        if args.detail:
+            d = os.path.dirname(os.path.abspath(args.detail))
+            os.makedirs(d, exist_ok=True)
+            with open(args.detail, "w") as fh:
+                json.dump(out, fh, indent=1)
+        print(json.dumps(compact(out)), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
