@@ -11,16 +11,11 @@ import oracle
 from conv_bn_silu_gb300 import _binding as B
 from conv_bn_silu_gb300 import workloads as wl
 from conv_bn_silu_gb300.layer import FusedConvBnSilu, make_desc
-from helpers import (TOL_FP32_REL_L2, TOL_TC_MAX_ABS, TOL_TC_REL_L2, max_scaled_err, nchw_to_nhwc, nhwc_to_nchw,
-                     rel_l2)
+from helpers import TOL_FP32_REL_L2, bf16_round, check_tc, nchw_to_nhwc, nhwc_to_nchw, rel_l2, tc_refs
 
 pytestmark = pytest.mark.gpu
 
 PRECS = {"fp32": B.CBS_FP32, "tf32": B.CBS_TF32, "bf16": B.CBS_BF16}
-
-
-def bf16_round(a):
-    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).float().numpy()
 
 
 def run(spec, n, prec, act, with_res, in_layout, out_layout, in_place=False, **kw):
@@ -51,21 +46,21 @@ def run(spec, n, prec, act, with_res, in_layout, out_layout, in_place=False, **k
     if out_layout == B.CBS_NHWC:
         out = nhwc_to_nchw(out)
     out = out[..., :spec.ow]
-    ref_x = oracle.conv_bn_act_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, spec.stride, spec.pad, act=act,
-                                   residual=r if with_res else None)
-    x_read = bf16_round(x) if prec == "bf16" else x
-    ref_read = oracle.conv_bn_act_f32(x_read, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, spec.stride, spec.pad,
-                                      act=act, residual=r if with_res else None)
-    return out, ref_x, ref_read, layer
-
-
-def check(prec, out, ref_x, ref_read, what):
-    e = rel_l2(out, ref_x)
     if prec == "fp32":
+        ref = oracle.conv_bn_act_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, spec.stride, spec.pad,
+                                     act=act, residual=r if with_res else None)
+        refs = (ref, ref)
+    else:
+        refs = tc_refs(prec, x, p, spec.stride, spec.pad, act=act, residual=r if with_res else None)
+    return out, refs[0], refs[1], layer
+
+
+def check(prec, out, ref_x, ref_max, what):
+    if prec == "fp32":
+        e = rel_l2(out, ref_x)
         assert e <= TOL_FP32_REL_L2, (what, e)
     else:
-        m = max_scaled_err(out, ref_read)
-        assert e <= TOL_TC_REL_L2 and m <= TOL_TC_MAX_ABS, (what, e, m)
+        check_tc(prec, out, (ref_x, ref_max), what)
 
 
 @pytest.mark.parametrize("act,with_res", [(B.CBS_ACT_IDENTITY, False), (B.CBS_ACT_SILU, True),

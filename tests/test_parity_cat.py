@@ -15,15 +15,11 @@ import oracle
 from conv_bn_silu_gb300 import _binding as B
 from conv_bn_silu_gb300 import workloads as wl
 from conv_bn_silu_gb300.layer import FusedConvBnSilu, make_desc
-from helpers import TOL_FP32_REL_L2, TOL_TC_MAX_ABS, TOL_TC_REL_L2, max_scaled_err, nhwc_to_nchw, rel_l2
+from helpers import TOL_FP32_REL_L2, check_tc, nhwc_to_nchw, rel_l2, tc_refs
 
 pytestmark = pytest.mark.gpu
 
 PRECS = {"fp32": B.CBS_FP32, "tf32": B.CBS_TF32, "bf16": B.CBS_BF16}
-
-
-def bf16_round(a):
-    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).float().numpy()
 
 
 def run_cat(n, c_a, c_b, c_out, k, stride, h, w, prec, in_layout, out_layout, **kw):
@@ -92,10 +88,7 @@ def test_tensor_core_two_inputs(cuda_lib, prec, case):
     assert layer.plan.variant == PRECS[prec]
     if kw.get("force_window"):
         assert layer.plan.window == 1
-    e = rel_l2(got, ref(x, p, spec))
-    x_read = bf16_round(x) if prec == "bf16" else x
-    m = max_scaled_err(got, ref(x_read, p, spec))
-    assert e <= TOL_TC_REL_L2 and m <= TOL_TC_MAX_ABS, (e, m)
+    check_tc(prec, got, tc_refs(prec, x, p, spec.stride, spec.pad))
 
 
 def test_two_input_residual_identity(cuda_lib):
