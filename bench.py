@@ -33,9 +33,9 @@ if ROOT not in sys.path:
 
 from conv_bn_silu_gb300 import workloads as wl  # noqa: E402
 
-# FP32 CUDA-core peak: 152 SMs x 128 FP32 lanes x 2 FLOP per FMA x 2.07 GHz.
-SM_COUNT, FP32_LANES, SM_MAX_GHZ = 152, 128, 2.070
-FP32_ALU_PEAK_TFLOPS = SM_COUNT * FP32_LANES * 2 * SM_MAX_GHZ / 1e3
+# FP32 CUDA-core peak: SMs x 128 FP32 lanes x 2 FLOP per FMA x the maximum SM
+# clock (GB300: 152 SMs, 2.07 GHz; both are read from the device when there is one).
+DEFAULT_SMS, FP32_LANES, DEFAULT_SM_MAX_GHZ = 152, 128, 2.070
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 126 * 2**20
 
@@ -167,11 +167,28 @@ def act_bytes(prec: str) -> int:
     return {"fp32": 4, "tf32": 4, "bf16": 2, "int8": 1}[prec]
 
 
+def device_sms() -> int:
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return int(torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count)
+    except Exception:
+        pass
+    return DEFAULT_SMS
+
+
+def fp32_alu_peak(peaks):
+    """(TFLOP/s, label): SMs x 128 lanes x 2 x the maximum SM clock."""
+    sms = device_sms()
+    ghz = float(peaks.get("sm_max_mhz", DEFAULT_SM_MAX_GHZ * 1e3)) / 1e3
+    return sms * FP32_LANES * 2 * ghz / 1e3, f"alu: {sms} SMs x {FP32_LANES} FP32 lanes x 2 x {ghz:.3g} GHz"
+
+
 def peak_for(prec: str, peaks):
     """(bound-kind peak in TFLOP/s, label) of the arithmetic a variant runs on."""
     bf16 = float(peaks["bf16_tflops"])
     if prec == "fp32":
-        return FP32_ALU_PEAK_TFLOPS, "alu: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz"
+        return fp32_alu_peak(peaks)
     if prec == "tf32":
         return bf16 * 1.1 / 2.25, "tensor: measured bf16 burst x nominal tf32/bf16 (1.1/2.25)"
     return bf16, "tensor: measured bf16 burst" + (" (int8 codes on bf16 MMA)" if prec == "int8" else "")

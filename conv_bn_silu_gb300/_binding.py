@@ -34,7 +34,7 @@ EXPORTED = (
     "cbs_upsample2x_concat", "cbs_workspace_init", "cbs_read_device_status", "cbs_status_string",
     "cbs_last_error", "cbs_abi_version", "cbs_conv_bn_silu_f32_noalloc", "cbs_conv_bn_act",
     "cbs_conv_bn_act_cat", "cbs_set_launch_options", "cbs_launch_options", "cbs_maxpool2d",
-    "cbs_conv_bn_silu_i8_cat",
+    "cbs_conv_bn_silu_i8_cat", "cbs_selftest_wait_timeout",
 )
 
 
@@ -43,7 +43,7 @@ class cbs_layer_desc(ctypes.Structure):
         "n", "c_in", "h", "w", "c_out", "k", "stride", "pad", "in_layout", "out_layout", "prec",
         "force_variant", "force_split_k", "force_block_n", "force_block_m", "out_row_stride",
         "force_k_group", "force_b_resident", "force_window", "activation", "residual", "c_in_b",
-        "zero_point_x", "zero_point_y")]
+        "zero_point_x", "zero_point_y", "num_sms")]
 
 
 class cbs_plan_t(ctypes.Structure):
@@ -87,6 +87,7 @@ def lib():
         L.cbs_conv_bn_silu_f32_noalloc.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P]
         L.cbs_workspace_init.argtypes = [P, Z, P]
         L.cbs_read_device_status.argtypes = [ctypes.POINTER(I), I, P]
+        L.cbs_selftest_wait_timeout.argtypes = [I, P]
         L.cbs_status_string.argtypes = [I]
         L.cbs_status_string.restype = ctypes.c_char_p
         L.cbs_last_error.argtypes = []
@@ -212,3 +213,9 @@ def cbs_read_device_status(reset: bool, stream) -> int:
     _check(lib().cbs_read_device_status(ctypes.byref(out), 1 if reset else 0, stream),
            "cbs_read_device_status")
     return out.value
+
+
+def cbs_selftest_wait_timeout(limit_us: int, stream):
+    """Enqueue the diagnostic kernel whose bounded wait runs out after
+    limit_us microseconds and records a timeout in the status word."""
+    _check(lib().cbs_selftest_wait_timeout(int(limit_us), stream), "cbs_selftest_wait_timeout")

@@ -75,9 +75,10 @@ SimtCost simt_cost(const cbs_layer_desc &d, int oh, int ow, int t, int split) {
                               (double)kc / kSimtBK * (a_pt * 7 + b_pt * 6 + 12) + T.tm * T.tn * 9.0 + 150.0 +
                               (splits > 1 ? T.tm * T.tn * (0.5 * splits + 2) : 0.0);
     const double cta_warp_instr = per_thread * nt / 32.0;
-    const long long slots = (long long)kNumSMs * res;
+    const long long sms = plan_sms(d);
+    const long long slots = sms * res;
     const long long waves = (ctas + slots - 1) / slots;
-    const long long per_sm = (ctas + kNumSMs - 1) / kNumSMs < res ? (ctas + kNumSMs - 1) / kNumSMs : res;
+    const long long per_sm = (ctas + sms - 1) / sms < res ? (ctas + sms - 1) / sms : res;
     const double warps = (double)per_sm * nt / 32.0;
     const double ipc = 4.0 * 0.7 * (warps >= 24 ? 1.0 : warps / 24.0);
     double cycles = (double)waves * per_sm * cta_warp_instr / ipc;
@@ -165,6 +166,7 @@ StemLaunch stem_launch(const cbs_plan_t &p, const void *x, const void *w, const 
     L.residual = nullptr;
     L.zp_x = d.prec == CBS_INT8 ? d.zero_point_x : 0;
     L.zp_y = d.prec == CBS_INT8 ? d.zero_point_y : 0;
+    L.grid = p.grid_ctas;
     return L;
 }
 
@@ -226,6 +228,8 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
         return fail(CBS_ERR_INVALID_ARG, "c_in_b %d: 0 (one input) or 1..c_in-1 (c_in = %d)", D.c_in_b, D.c_in);
     if (D.prec != CBS_INT8 && (D.zero_point_x || D.zero_point_y))
         return fail(CBS_ERR_INVALID_ARG, "zero points apply to INT8 plans only");
+    if (D.num_sms < 0 || D.num_sms > 4096)
+        return fail(CBS_ERR_INVALID_ARG, "num_sms %d: 0 (the GB300's 152) or the device's SM count", D.num_sms);
     if (D.zero_point_x < -128 || D.zero_point_x > 127 || D.zero_point_y < -128 || D.zero_point_y > 127)
         return fail(CBS_ERR_INVALID_ARG, "zero points must lie in [-128, 127] (z_x %d, z_y %d)", D.zero_point_x,
                     D.zero_point_y);
@@ -324,7 +328,7 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
         p.m_tiles = (int)((M + p.block_m - 1) / p.block_m);
         p.n_tiles = 1;
         // the tensor-core stem is persistent: kStemTcCtasPerSm CTAs per SM walk the tiles
-        p.grid_ctas = tc ? std::min(p.m_tiles, kNumSMs * stem_tc_ctas_per_sm(D.c_out, tc_kind == 3)) : p.m_tiles;
+        p.grid_ctas = tc ? std::min(p.m_tiles, plan_sms(D) * stem_tc_ctas_per_sm(D.c_out, tc_kind == 3)) : p.m_tiles;
         p.threads = 256;
         p.smem_bytes = tc ? (tc_kind == 3 ? kStemTf32SmemBytes : kStemTcSmemBytes) : D.k * D.k * p.c_in_pad * cout_t * 4;
         p.workspace_bytes = 0;
@@ -604,6 +608,13 @@ cbs_status cbs_workspace_init(void *workspace, size_t bytes, void *stream) {
 cbs_status cbs_read_device_status(int *status_out, int reset, void *stream) {
     if (!status_out) return fail(CBS_ERR_INVALID_ARG, "status_out is NULL");
     return read_and_reset_status(status_out, reset, (cudaStream_t)stream);
+}
+
+cbs_status cbs_selftest_wait_timeout(int limit_us, void *stream) {
+    if (limit_us < 1 || limit_us > 100000)
+        return fail(CBS_ERR_INVALID_ARG, "limit_us %d: 1 .. 100000", limit_us);
+    return cuda_check(launch_wait_selftest((unsigned long long)limit_us * 1000ull, (cudaStream_t)stream),
+                      "wait self-test launch");
 }
 
 }  // extern "C"

@@ -10,9 +10,23 @@
 
 namespace cbs {
 
-// GB300: 152 SMs on two dies.  cbs_plan is host-only and makes no CUDA call,
-// so it plans for this count; launches size their grids from the plan.
-constexpr int kNumSMs = 152;
+// GB300: 152 SMs on two dies.  cbs_plan is host-only and makes no CUDA call:
+// it plans for the descriptor's num_sms (this count when 0); launches size
+// their grids from the plan.
+constexpr int kDefaultNumSMs = 152;
+inline int plan_sms(const cbs_layer_desc &d) { return d.num_sms > 0 ? d.num_sms : kDefaultNumSMs; }
+// SM count of the current device, for the grids of kernels that have no plan
+// (packing and glue); the GB300's count if the query fails.
+int current_device_sms();
+// Process-unique ID of the calling thread's current CUDA context (0 if none).
+// A device reset, or a primary context released and made again, gives a new
+// ID: addresses of the library's device globals are cached per ID.
+cbs_status current_context_id(unsigned long long *id);
+// Device address of the status word that bounded waits report into.
+unsigned int *device_status_word();
+// One CTA whose bounded wait on a barrier nothing arrives at runs out after
+// limit_ns (cbs_selftest_wait_timeout).
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s);
 // Dynamic shared memory ceiling set once on every kernel that opts in above
 // 48 KB (the sm_100-family per-block maximum).  Each launch asks for its own
 // size below it; a fixed ceiling means a launch recorded in a CUDA graph stays
@@ -117,6 +131,7 @@ struct StemLaunch {
     int act;                   // cbs_activation (float kinds)
     const void *residual;      // nullable, element type and layout of y (float kinds)
     int zp_x, zp_y;            // INT8 zero points of input and output codes
+    int grid;                  // tensor-core stems: persistent CTAs (the plan's grid_ctas)
 };
 cudaError_t launch_stem(const StemLaunch &L, cudaStream_t s);
 // TF32, BF16 and INT8 stems (4-channel NHWC input, k <= 3, C_out <= 64;

@@ -18,7 +18,10 @@
 //    CBS_ERR_WORKSPACE.
 //  - The first call on a device looks up the array's device address (with
 //    that device current) and caches it; make that first call before any
-//    stream capture.
+//    stream capture.  The cache is keyed on the device's current context
+//    (its process-unique context ID): after a device reset, or once the
+//    primary context has been released and made again, the module is loaded
+//    afresh, so the next call looks the address up again.
 //  - Every call shares the one array and it keeps the last call's contents.
 //    Each call zeroes the split-K arrival counters on its stream before its
 //    kernel runs.  Calls whose kernels may overlap on the GPU (different
@@ -39,7 +42,11 @@ constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB per device
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void *g_scratch_ptr[kMaxDevices] = {nullptr};
+struct ScratchEntry {
+    unsigned long long ctx_id = 0;   // context the address belongs to (0: none yet)
+    void *ptr = nullptr;
+};
+ScratchEntry g_scratch[kMaxDevices];
 std::mutex g_scratch_mutex;
 
 cbs_status scratch_for_current_device(void **out) {
@@ -47,14 +54,20 @@ cbs_status scratch_for_current_device(void **out) {
     cbs_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
     if (st != CBS_OK) return st;
     if (dev < 0 || dev >= kMaxDevices) return fail(CBS_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    unsigned long long ctx = 0;
+    if ((st = current_context_id(&ctx)) != CBS_OK) return st;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[dev]) {
+    ScratchEntry &e = g_scratch[dev];
+    if (!e.ptr || ctx == 0 || e.ctx_id != ctx) {
         void *p = nullptr;
         st = cuda_check(cudaGetSymbolAddress(&p, g_noalloc_scratch), "cudaGetSymbolAddress(scratch)");
         if (st != CBS_OK) return st;
-        g_scratch_ptr[dev] = p;
+        // The lookup makes the device's primary context current if none was.
+        if ((st = current_context_id(&ctx)) != CBS_OK) return st;
+        e.ptr = p;
+        e.ctx_id = ctx;
     }
-    *out = g_scratch_ptr[dev];
+    *out = e.ptr;
     return CBS_OK;
 }
 

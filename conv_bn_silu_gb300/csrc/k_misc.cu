@@ -1,7 +1,10 @@
 // k_misc.cu -- setup and glue kernels: BN folding and weight packing, the
 // chain-entry layout conversion, the upsample+concat neck glue, and the
 // device status word that bounded waits report into.
+#include <cuda.h>
 #include <cuda_bf16.h>
+
+#include <mutex>
 
 #include "cbs_internal.cuh"
 #include "tc_ptx.cuh"
@@ -417,9 +420,75 @@ __global__ void maxpool_kernel(const T *__restrict__ x, T *__restrict__ y, int N
 
 __device__ unsigned int g_cbs_status_word;
 
+// Diagnostic for the timeout path: thread 0 waits, through the same bounded
+// mbarrier wait the tensor-core kernels use, on a barrier that nothing
+// arrives at.  After limit_ns the wait gives up and the kernel records a
+// timeout in the status word, as a kernel does when one of its waits runs out.
+__global__ void wait_selftest_kernel(unsigned long long limit_ns, unsigned int *status) {
+    __shared__ __align__(8) unsigned long long bar;
+    const uint32_t b = ptx::smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(b, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !ptx::mbar_wait_bounded(b, 0, limit_ns)) atomicOr(status, 1u);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s) {
+    unsigned int *status = device_status_word();
+    if (!status) return cudaErrorInvalidValue;
+    wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns, status);
+    return cudaGetLastError();
+}
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+cbs_status current_context_id(unsigned long long *id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q1, q2;
+        void *p1 = nullptr, *p2 = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p1, 12000, cudaEnableDefault, &q1) ==
+                cudaSuccess &&
+            q1 == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &p2, 12000, cudaEnableDefault, &q2) == cudaSuccess &&
+            q2 == cudaDriverEntryPointSuccess) {
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p1);
+            get_id = reinterpret_cast<CtxGetIdFn>(p2);
+        }
+    });
+    if (!get_current || !get_id) return fail(CBS_ERR_CUDA, "driver entry points cuCtxGetCurrent/cuCtxGetId unavailable");
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuCtxGetCurrent failed");
+    *id = 0;
+    if (ctx && get_id(ctx, id) != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuCtxGetId failed");
+    return CBS_OK;
+}
+
+int current_device_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kDefaultNumSMs;
+    if (cached[dev] <= 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return kDefaultNumSMs;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+namespace {
+
 int grid_for(size_t count, int threads) {
     size_t blocks = (count + threads - 1) / threads;
-    const size_t cap = (size_t)kNumSMs * 16;
+    const size_t cap = (size_t)current_device_sms() * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     return (int)blocks;
@@ -437,7 +506,7 @@ cudaError_t launch_pack_input(const float *x, void *out, int N, int C, int H, in
     if (to_nhwc && c_pad == 4 && W % 4 == 0) {   // x and out are 16-byte aligned (checked by the caller)
         const int gx = (W / 4 + kPackSmallThreads - 1) / kPackSmallThreads;
         const int rows = N * H;
-        int gy = kNumSMs * 32 / gx;
+        int gy = current_device_sms() * 32 / gx;
         gy = gy < 1 ? 1 : (gy > rows ? rows : (gy > 65535 ? 65535 : gy));
         const dim3 grid(gx, gy);
         if (dtype == 0) launch_kernel(pack_nhwc_quad_kernel<float>, grid, kPackSmallThreads, 0, s, x, (float *)out, C, H, W, rows, s_x, zp);
@@ -446,7 +515,7 @@ cudaError_t launch_pack_input(const float *x, void *out, int N, int C, int H, in
     } else if (to_nhwc && c_pad <= 8) {
         const int gx = (W + kPackSmallThreads - 1) / kPackSmallThreads;
         const int rows = N * H;
-        int gy = kNumSMs * 32 / gx;
+        int gy = current_device_sms() * 32 / gx;
         gy = gy < 1 ? 1 : (gy > rows ? rows : (gy > 65535 ? 65535 : gy));
         const dim3 grid(gx, gy);
         if (dtype == 0) launch_kernel(pack_nhwc_small_kernel<float>, grid, kPackSmallThreads, 0, s, x, (float *)out, C, H, W, rows, c_pad, s_x, zp);
@@ -501,14 +570,22 @@ cudaError_t launch_maxpool(const void *x, void *y, int n, int c, int h, int w, i
 }
 
 unsigned int *device_status_word() {
-    // One address per device; looked up once per device.
+    // One address per device and context: looked up again after a device
+    // reset (the module, and the word with it, is then loaded afresh).
     static unsigned int *cache[64] = {nullptr};
+    static unsigned long long cache_ctx[64] = {0};
+    static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!cache[dev]) {
+    unsigned long long ctx = 0;
+    if (current_context_id(&ctx) != CBS_OK) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev] || ctx == 0 || cache_ctx[dev] != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_cbs_status_word) != cudaSuccess) return nullptr;
+        if (current_context_id(&ctx) != CBS_OK) return nullptr;
         cache[dev] = static_cast<unsigned int *>(p);
+        cache_ctx[dev] = ctx;
     }
     return cache[dev];
 }

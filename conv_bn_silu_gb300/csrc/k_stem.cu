@@ -1002,7 +1002,7 @@ cudaError_t launch_stem_tc(const StemLaunch &L, cudaStream_t s) {
     g.n_tiles = (int)((total + 127) / 128);
     g.div_ohw = make_fastdiv((uint32_t)(L.OH * L.OW));
     g.div_ow = make_fastdiv((uint32_t)L.OW);
-    const int grid = std::min(g.n_tiles, kNumSMs * stem_tc_ctas_per_sm(L.Cout, L.tf32));
+    const int grid = std::min(g.n_tiles, L.grid);   // the plan's persistent CTAs
     const int n_mma = (L.Cout + 15) / 16 * 16;
     if (L.tf32)
         return L.out_nhwc ? launch_stem_tf32<true>(L, n_mma, g, grid, s, status)

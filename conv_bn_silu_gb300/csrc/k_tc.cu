@@ -1590,11 +1590,11 @@ bool tc_config_window(const cbs_layer_desc &d, int oh, int RB, int ksteps, bool 
     c.nprod = tc_producers_max(c.stages, c.b_res ? kMaxProducers : kMaxProducers - 1);
     const long long tiles = (long long)c.m_tiles * c.n_tiles;
     if (c.b_res && c.n_tiles > 1) {
-        const long long g = tiles < kNumSMs ? tiles : (long long)(kNumSMs / c.n_tiles) * c.n_tiles;
+        const long long g = tiles < plan_sms(d) ? tiles : (long long)(plan_sms(d) / c.n_tiles) * c.n_tiles;
         if (g <= 0) return false;
         c.grid = (int)g;
     } else {
-        c.grid = (int)(tiles < kNumSMs ? tiles : kNumSMs);
+        c.grid = (int)(tiles < plan_sms(d) ? tiles : plan_sms(d));
     }
     const double tpc = (double)((tiles + c.grid - 1) / c.grid);
     const int kslices = RB / 32;
@@ -1637,11 +1637,11 @@ bool tc_config(const cbs_layer_desc &d, long long M, int oh, int RB, int ksteps,
     const long long tiles = (long long)c.m_tiles * c.n_tiles;
     if (b_res && c.n_tiles > 1) {
         // Every CTA keeps one N tile: the grid is a multiple of n_tiles.
-        const long long g = tiles < kNumSMs ? tiles : (long long)(kNumSMs / c.n_tiles) * c.n_tiles;
+        const long long g = tiles < plan_sms(d) ? tiles : (long long)(plan_sms(d) / c.n_tiles) * c.n_tiles;
         if (g <= 0) return false;
         c.grid = (int)g;
     } else {
-        c.grid = (int)(tiles < kNumSMs ? tiles : kNumSMs);
+        c.grid = (int)(tiles < plan_sms(d) ? tiles : plan_sms(d));
     }
     const double tpc = (double)((tiles + c.grid - 1) / c.grid);   // tiles of the busiest CTA
     const int kslices = RB / 32;
@@ -1761,7 +1761,7 @@ cbs_status plan_tc(cbs_plan_t &p) {
                 if (d.force_block_n > 0 && c != d.force_block_n) continue;
                 const long long tiles = (long long)p.m_tiles * ((d.c_out + c - 1) / c);
                 if (!x3) {
-                    const double cost = (double)((tiles + kNumSMs - 1) / kNumSMs) * (c > 64 ? c : 64);
+                    const double cost = (double)((tiles + plan_sms(d) - 1) / plan_sms(d)) * (c > 64 ? c : 64);
                     if (cost < best * 0.99) { best = cost; BN = c; }
                     continue;
                 }
@@ -1775,11 +1775,11 @@ cbs_status plan_tc(cbs_plan_t &p) {
                     // two accumulator buffers of (K-step chunks per part) x N columns in TMEM
                     if (x3_chunks(ksteps, g, sp, CB) * next_pow2(c) > 256) continue;
                     const long long units = tiles * sp;
-                    const double cost = (double)((units + kNumSMs - 1) / kNumSMs) * ((nst + sp - 1) / sp) * g *
+                    const double cost = (double)((units + plan_sms(d) - 1) / plan_sms(d)) * ((nst + sp - 1) / sp) * g *
                                             (128.0 + c) + (sp > 1 ? 4.0 * sp * c : 0.0);
                     if (cost < best * 0.99) { best = cost; BN = c; split = sp; }
                     // A wave of tiles or more: only the fewest parts whose chunks fit TMEM.
-                    if (!forced && tiles >= kNumSMs) break;
+                    if (!forced && tiles >= plan_sms(d)) break;
                 }
             }
         }
@@ -1819,7 +1819,7 @@ cbs_status plan_tc(cbs_plan_t &p) {
             p.workspace_bytes = (size_t)round_up((int)tiles * kSplitCounterSlots * 4, 256) +
                                 (size_t)tiles * split * kBM * BN * 4;
         const long long units = tiles * split;
-        p.grid_ctas = (int)(units < kNumSMs ? units : kNumSMs);
+        p.grid_ctas = (int)(units < plan_sms(d) ? units : plan_sms(d));
         return CBS_OK;
     }
 
@@ -1890,7 +1890,7 @@ cbs_status plan_tc(cbs_plan_t &p) {
     }
     p.split_k = split;
     if (split > 1) {
-        best.grid = tiles * split < kNumSMs ? tiles * split : kNumSMs;
+        best.grid = tiles * split < plan_sms(d) ? tiles * split : plan_sms(d);
         p.workspace_bytes = (size_t)round_up(tiles * kSplitCounterSlots * 4, 256) +
                             (size_t)tiles * split * (kBM * best.mmul) * best.BN * 4;
     }

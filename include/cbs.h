@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define CBS_ABI_VERSION 3
+#define CBS_ABI_VERSION 4
 
 /* Exported symbols (the library is built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -122,6 +122,9 @@ typedef struct cbs_layer_desc {
                             a uint8 code u with zero point z_u is q = u - 128, z_x = z_u - 128).
                             0 = symmetric.  Must be 0 for the other precisions. */
     int zero_point_y;    /* INT8: zero point z_y in [-128, 127] of the output codes. */
+    int num_sms;         /* SMs of the device the layer will run on (cudaDevAttrMultiProcessorCount):
+                            grids, waves and split-K are sized for it.  0 = 152, the GB300's count.
+                            cbs_plan stays a pure host function: it never queries the device. */
 } cbs_layer_desc;
 
 /* A plan: plain data, owned by the caller, filled by cbs_plan. */
@@ -384,6 +387,19 @@ CBS_API cbs_status cbs_workspace_init(void *workspace, size_t bytes, void *strea
  * reset != 0 clears the flag.
  */
 CBS_API cbs_status cbs_read_device_status(int *status_out, int reset, void *stream);
+
+/*
+ * cbs_selftest_wait_timeout -- diagnostic of the timeout path (no passage of
+ * the pages has a counterpart).  Enqueues one CTA on `stream` whose thread
+ * waits, through the same bounded mbarrier wait the tensor-core kernels use,
+ * on a barrier that nothing arrives at.  After limit_us microseconds
+ * (1 .. 100000) the wait gives up and the kernel records a timeout in the
+ * status word, exactly as a layer kernel does when one of its waits runs
+ * out; cbs_read_device_status then reports CBS_ERR_TIMEOUT.  Nothing faults
+ * and the context stays usable.  Errors: CBS_ERR_INVALID_ARG for limit_us
+ * out of range, CBS_ERR_CUDA if the launch fails.
+ */
+CBS_API cbs_status cbs_selftest_wait_timeout(int limit_us, void *stream);
 
 /* Static string for a status code. */
 CBS_API const char *cbs_status_string(cbs_status s);

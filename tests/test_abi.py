@@ -28,10 +28,10 @@ def test_library_exports_every_declared_symbol(cuda_lib):
 
 
 def test_abi_version_and_struct_sizes(cuda_lib):
-    assert B.cbs_abi_version() == 3
+    assert B.cbs_abi_version() == 4
     plan = B.cbs_plan(make_desc(1, 16, 40, 40, 32, 3, 1))
     assert plan.size == ctypes.sizeof(B.cbs_plan_t)
-    assert plan.abi_version == 3
+    assert plan.abi_version == 4
 
 
 def test_status_strings(cuda_lib):
@@ -280,3 +280,25 @@ def test_split_k_plan_rules(cuda_lib):
         with pytest.raises(B.CbsError) as e:
             B.cbs_plan(make_desc(2, 64, 16, 16, 64, 3, 1, prec=B.CBS_BF16, force_split_k=2, **kw))
         assert e.value.status == B.CBS_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("prec,n", [(B.CBS_BF16, 16), (B.CBS_INT8, 16), (B.CBS_FP32, 1)])
+def test_plan_follows_the_sm_count(cuda_lib, prec, n):
+    """num_sms = 0 plans for the GB300's 152 SMs; another count sizes the
+    persistent grids (at most one CTA per SM for the tensor-core kernels)
+    and the waves for that device."""
+    layout = B.CBS_NHWC if prec != B.CBS_FP32 else B.CBS_NCHW
+    for i, s in enumerate(wl.LAYER_LIST[1:], start=1):
+        d0 = make_desc(n, s.c_in, s.h, s.width, s.c_out, s.k, s.stride, prec=prec, in_layout=layout, num_sms=0)
+        d152 = make_desc(n, s.c_in, s.h, s.width, s.c_out, s.k, s.stride, prec=prec, in_layout=layout, num_sms=152)
+        d76 = make_desc(n, s.c_in, s.h, s.width, s.c_out, s.k, s.stride, prec=prec, in_layout=layout, num_sms=76)
+        p0, p152, p76 = B.cbs_plan(d0), B.cbs_plan(d152), B.cbs_plan(d76)
+        assert bytes(p0)[:ctypes.sizeof(B.cbs_plan_t) - ctypes.sizeof(B.cbs_layer_desc)] == \
+            bytes(p152)[:ctypes.sizeof(B.cbs_plan_t) - ctypes.sizeof(B.cbs_layer_desc)], i
+        if p76.variant in (B.CBS_VARIANT_TC_TF32, B.CBS_VARIANT_TC_BF16, B.CBS_VARIANT_TC_INT8,
+                           B.CBS_VARIANT_TC_TF32X3):
+            assert p76.grid_ctas <= 76 and p152.grid_ctas <= 152, i
+            assert p152.grid_ctas == min(152, p152.m_tiles * p152.n_tiles * p152.split_k) or p152.b_resident, i
+    with pytest.raises(B.CbsError) as e:
+        B.cbs_plan(make_desc(1, 16, 40, 40, 32, 3, 1, num_sms=-1))
+    assert e.value.status == B.CBS_ERR_INVALID_ARG
