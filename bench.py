@@ -111,6 +111,10 @@ WORKLOADS = {
     "chain_bf16_n16": dict(kind="chain", n=16, prec="bf16"),
     "chain_tf32_n16": dict(kind="chain", n=16, prec="tf32"),
     "chain_fp32_n1_nhwc": dict(kind="chain", n=1, prec="fp32", layout="nhwc"),
+    # The whole synthetic frame: the chain with the SPPF block (two more fused
+    # layers and the three chained 5x5 pools in one glue kernel).
+    "frame_fp32_n1": dict(kind="chain", n=1, prec="fp32", sppf=True),
+    "frame_bf16_n16": dict(kind="chain", n=16, prec="bf16", sppf=True),
     # The list with the residual form of the epilogue, y = SiLU(BN(conv)) + r, on every
     # stride-1 layer whose input and output shapes match (a bottleneck's skip add).
     "layer_list_bf16_n16_residual": dict(kind="list", layers=wl.LAYER_LIST, n=16, prec="bf16", residual=True),
@@ -123,7 +127,8 @@ WORKLOADS = {
 }
 EXTRA_DEFAULT = ("layer_list_bf16_n16", "layer_list_tf32_n16", "layer_list_int8_n16", "chain_fp32_n1",
                  "chain_bf16_n16", "layer_list_bf16_n16_residual", "layer_list_int8_n16_asym",
-                 "layer_list_fp32_n16_nhwc", "layer_list_fp32_n1_nhwc", "chain_fp32_n1_nhwc")
+                 "layer_list_fp32_n16_nhwc", "layer_list_fp32_n1_nhwc", "chain_fp32_n1_nhwc", "frame_fp32_n1",
+                 "frame_bf16_n16")
 
 
 # DRAM traffic of the dominant kernel over one step of a workload, from one
@@ -257,9 +262,10 @@ class ListWorkload:
 
 
 class ChainWorkload:
-    """The 40-layer whole-frame chain; one step = one frame batch (frame
-    packing, 40 fused layers, one upsample kernel; layer 11 reads its two
-    concatenated inputs straight from their buffers)."""
+    """The 40-layer whole-frame chain, or the whole frame with the SPPF block;
+    one step = one frame batch (frame packing, the fused layers, the upsample
+    kernel and, in the frame, the SPPF pool kernel; two-input layers read
+    their concatenated inputs straight from their buffers)."""
 
     def __init__(self, cfg, device):
         import torch
@@ -267,7 +273,7 @@ class ChainWorkload:
         from conv_bn_silu_gb300.chain import Chain
         self.cfg, self.n, self.prec = cfg, cfg["n"], cfg["prec"]
         lay = B.CBS_NHWC if cfg.get("layout") == "nhwc" else None
-        self.chain = Chain(self.prec, self.n, device=device, layout=lay)
+        self.chain = Chain(self.prec, self.n, device=device, layout=lay, sppf=bool(cfg.get("sppf")))
         self.nhwc = self.chain.layout == B.CBS_NHWC
         self.frame = torch.from_numpy(wl.frame(self.n)).to(device)
         self.specs = [cl.spec for cl in self.chain.specs]
@@ -282,14 +288,7 @@ class ChainWorkload:
         c = self.chain
         B.cbs_pack_input(c.layers[0].plan, self.frame, c.x0, 0.0, stream_id)
         for i, layer in enumerate(c.layers):
-            src = c.specs[i].src
-            if src[0] == "upcat":
-                a = c.outs[src[1]]
-                if c.layout == B.CBS_NHWC:
-                    n, h, w, ca = a.shape
-                else:
-                    n, ca, h, w = a.shape
-                B.cbs_upsample2x_concat(a, ca, None, 0, c.glue, n, 2 * h, 2 * w, c.layout, a.element_size(), stream_id)
+            c.glue_before(i, stream_id)
             if events is not None:
                 events[i].record(stream)
             layer(c.input_of(i), c.outs[i], stream=stream_id, x_b=c.second_input_of(i))

@@ -34,7 +34,7 @@ EXPORTED = (
     "cbs_upsample2x_concat", "cbs_workspace_init", "cbs_read_device_status", "cbs_status_string",
     "cbs_last_error", "cbs_abi_version", "cbs_conv_bn_silu_f32_noalloc", "cbs_conv_bn_act",
     "cbs_conv_bn_act_cat", "cbs_set_launch_options", "cbs_launch_options", "cbs_maxpool2d",
-    "cbs_conv_bn_silu_i8_cat", "cbs_selftest_wait_timeout",
+    "cbs_conv_bn_silu_i8_cat", "cbs_selftest_wait_timeout", "cbs_sppf_pool",
 )
 
 
@@ -84,6 +84,7 @@ def lib():
         L.cbs_conv_bn_silu_i8_cat.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P, F, P, P, Z, P]
         L.cbs_upsample2x_concat.argtypes = [P, I, P, I, P, I, I, I, I, I, P]
         L.cbs_maxpool2d.argtypes = [P, P, I, I, I, I, I, I, I, I, I, P]
+        L.cbs_sppf_pool.argtypes = [P, P, I, I, I, I, I, I, I, P]
         L.cbs_conv_bn_silu_f32_noalloc.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P]
         L.cbs_workspace_init.argtypes = [P, Z, P]
         L.cbs_read_device_status.argtypes = [ctypes.POINTER(I), I, P]
@@ -170,6 +171,10 @@ def cbs_conv_bn_silu_i8_cat(plan, x, x_b, w_packed, bias_i32, m_c, s_y, y, works
 
 def cbs_maxpool2d(x, y, n, c, h, w, k, stride, pad, layout, prec, stream):
     _check(lib().cbs_maxpool2d(_p(x), _p(y), n, c, h, w, k, stride, pad, layout, prec, stream), "cbs_maxpool2d")
+
+
+def cbs_sppf_pool(x, y, n, c, h, w, k, layout, prec, stream):
+    _check(lib().cbs_sppf_pool(_p(x), _p(y), n, c, h, w, k, layout, prec, stream), "cbs_sppf_pool")
 
 
 def cbs_set_launch_options(flags: int):

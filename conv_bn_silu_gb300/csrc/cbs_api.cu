@@ -581,6 +581,20 @@ cbs_status cbs_maxpool2d(const void *x, void *y, int n, int c, int h, int w, int
                       "max-pool launch");
 }
 
+cbs_status cbs_sppf_pool(const void *x, void *y, int n, int c, int h, int w, int k, int layout, int prec,
+                         void *stream) {
+    CBS_TRY(check_ptr(x, "x"));
+    CBS_TRY(check_ptr(y, "y"));
+    if (n < 0 || n > 65535 || c < 1 || h < 1 || w < 1 || k < 1 || k > 7 || !(k & 1))
+        return fail(CBS_ERR_INVALID_ARG, "bad SPPF pool shape (n=%d c=%d h=%d w=%d k=%d; odd k <= 7)", n, c, h, w, k);
+    if (layout != CBS_NCHW && layout != CBS_NHWC) return fail(CBS_ERR_INVALID_ARG, "unknown layout %d", layout);
+    if (prec < CBS_FP32 || prec > CBS_INT8) return fail(CBS_ERR_INVALID_ARG, "unknown precision %d", prec);
+    if (n == 0) return CBS_OK;
+    const int eb = prec == CBS_BF16 ? 2 : (prec == CBS_INT8 ? 1 : 4);
+    return cuda_check(launch_sppf_pool(x, y, n, c, h, w, k, layout == CBS_NHWC, eb, (cudaStream_t)stream),
+                      "SPPF pool launch");
+}
+
 cbs_status cbs_upsample2x_concat(const void *a, int ca, const void *b, int cb, void *out, int n, int h,
                                  int w, int layout, int elem_bytes, void *stream) {
     CBS_TRY(check_ptr(a, "a"));

@@ -182,6 +182,8 @@ cudaError_t launch_upsample_concat(const void *a, int ca, const void *b, int cb,
                                    int n, int h, int w, int nhwc, int elem_bytes,
                                    cudaStream_t s);
 
+cudaError_t launch_sppf_pool(const void *x, void *y, int n, int c, int h, int w, int k, int nhwc, int eb,
+                             cudaStream_t s);
 cudaError_t launch_maxpool(const void *x, void *y, int n, int c, int h, int w, int k, int stride, int pad, int nhwc,
                            int elem_bytes, cudaStream_t s);
 

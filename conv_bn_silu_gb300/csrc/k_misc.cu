@@ -418,6 +418,114 @@ __global__ void maxpool_kernel(const T *__restrict__ x, T *__restrict__ y, int N
     }
 }
 
+// ---------------------------------------------------------------- SPPF pools
+// y = concat(p(x), p(p(x)), p(p(p(x)))) along channels, p = the k x k max
+// pool with stride 1 and padding k/2 whose padded positions take no part (the
+// SPPF block's three chained pools; "YOLO26N Inference Optimisation", kernel
+// profile: maxpool2d, three per frame).  One CTA per (16x16 output tile,
+// image, group of kSppfCg channels) keeps the tile with a halo of 3 (k/2) in
+// shared memory.  Positions outside the image hold the type's lowest value:
+// every window holds its own in-image centre, so the lowest value never wins
+// over a real one and the max equals the max over the in-image positions.
+// Each pool is a horizontal, then a vertical running max in shared memory;
+// the region it covers shrinks by k/2 per pool, and after each pool the
+// tile's interior goes to its channel slice of y.  A NaN in a window gives NaN.
+constexpr int kSppfTile = 16;
+
+template <typename T>
+struct PoolOps;
+template <>
+struct PoolOps<float> {
+    static __device__ __forceinline__ float lowest() { return __int_as_float(0xff800000); }   // -inf
+    static __device__ __forceinline__ float mx(float a, float b) {
+        return a != a ? a : (b != b ? b : (a > b ? a : b));
+    }
+};
+template <>
+struct PoolOps<__nv_bfloat16> {
+    static __device__ __forceinline__ __nv_bfloat16 lowest() { return __ushort_as_bfloat16(0xff80); }   // -inf
+    static __device__ __forceinline__ bool nan(__nv_bfloat16 v) { return (__bfloat16_as_ushort(v) & 0x7fffu) > 0x7f80u; }
+    static __device__ __forceinline__ __nv_bfloat16 mx(__nv_bfloat16 a, __nv_bfloat16 b) {
+        return nan(a) ? a : (nan(b) ? b : (__bfloat162float(a) > __bfloat162float(b) ? a : b));
+    }
+};
+template <>
+struct PoolOps<int8_t> {
+    static __device__ __forceinline__ int8_t lowest() { return (int8_t)-128; }
+    static __device__ __forceinline__ int8_t mx(int8_t a, int8_t b) { return a > b ? a : b; }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) sppf_pool_kernel(const T *__restrict__ x, T *__restrict__ y, int N, int C,
+                                                        int H, int W, int hk, int cg, int tiles_w, int nhwc) {
+    extern __shared__ __align__(16) uint8_t sppf_smem[];
+    using O = PoolOps<T>;
+    const int R = 3 * hk, S = kSppfTile + 2 * R;
+    T *buf = reinterpret_cast<T *>(sppf_smem);
+    T *tmp = buf + (size_t)S * S * cg;
+    const int n = blockIdx.y;
+    const int c0 = blockIdx.z * cg;
+    const int oh0 = (blockIdx.x / tiles_w) * kSppfTile, ow0 = (blockIdx.x % tiles_w) * kSppfTile;
+    const int C3 = 3 * C;
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+    // The tile and its halo; the lowest value outside the image and past C.
+    for (int e = threadIdx.x; e < S * S * cg; e += blockDim.x) {
+        const int c = e % cg, pos = e / cg;
+        const int ih = oh0 - R + pos / S, iw = ow0 - R + pos % S;
+        T v = O::lowest();
+        if (ih >= 0 && ih < H && iw >= 0 && iw < W && c0 + c < C)
+            v = nhwc ? x[(((size_t)n * H + ih) * W + iw) * C + c0 + c] : x[(((size_t)n * C + c0 + c) * H + ih) * W + iw];
+        buf[e] = v;
+    }
+    __syncthreads();
+    for (int r = 1; r <= 3; ++r) {
+        const int ext = (3 - r) * hk;
+        // Horizontal max over rows [R-ext-hk, R+T+ext+hk) and columns [R-ext, R+T+ext).
+        {
+            const int y0 = R - ext - hk, ny = kSppfTile + 2 * (ext + hk);
+            const int x0 = R - ext, nx = kSppfTile + 2 * ext;
+            for (int e = threadIdx.x; e < ny * nx * cg; e += blockDim.x) {
+                const int c = e % cg, pos = e / cg;
+                const int yy = y0 + pos / nx, xx = x0 + pos % nx;
+                const T *row = buf + ((size_t)yy * S) * cg + c;
+                T v = row[(size_t)(xx - hk) * cg];
+                for (int dx = -hk + 1; dx <= hk; ++dx) v = O::mx(v, row[(size_t)(xx + dx) * cg]);
+                tmp[((size_t)yy * S + xx) * cg + c] = v;
+            }
+        }
+        __syncthreads();
+        // Vertical max into buf over rows and columns [R-ext, R+T+ext).
+        {
+            const int y0 = R - ext, nyx = kSppfTile + 2 * ext;
+            for (int e = threadIdx.x; e < nyx * nyx * cg; e += blockDim.x) {
+                const int c = e % cg, pos = e / cg;
+                const int yy = y0 + pos / nyx, xx = y0 + pos % nyx;
+                const int ih = oh0 - R + yy, iw = ow0 - R + xx;
+                T v = O::lowest();
+                if (ih >= 0 && ih < H && iw >= 0 && iw < W) {
+                    const T *col = tmp + (size_t)xx * cg + c;
+                    v = col[(size_t)(yy - hk) * S * cg];
+                    for (int dy = -hk + 1; dy <= hk; ++dy) v = O::mx(v, col[(size_t)(yy + dy) * S * cg]);
+                }
+                buf[((size_t)yy * S + xx) * cg + c] = v;
+            }
+        }
+        __syncthreads();
+        // Pool r over the tile's interior to channel slice r - 1 of y.
+        for (int e = threadIdx.x; e < kSppfTile * kSppfTile * cg; e += blockDim.x) {
+            const int c = e % cg, pos = e / cg;
+            const int oh = oh0 + pos / kSppfTile, ow = ow0 + pos % kSppfTile;
+            if (oh >= H || ow >= W || c0 + c >= C) continue;
+            const T v = buf[((size_t)(R + pos / kSppfTile) * S + R + pos % kSppfTile) * cg + c];
+            const int ch = (r - 1) * C + c0 + c;
+            if (nhwc) y[(((size_t)n * H + oh) * W + ow) * C3 + ch] = v;
+            else y[(((size_t)n * C3 + ch) * H + oh) * W + ow] = v;
+        }
+        // The next pool's horizontal pass reads buf, which these writes only read.
+    }
+}
+
 __device__ unsigned int g_cbs_status_word;
 
 // Diagnostic for the timeout path: thread 0 waits, through the same bounded
@@ -567,6 +675,31 @@ cudaError_t launch_maxpool(const void *x, void *y, int n, int c, int h, int w, i
                              n, c, h, w, oh, ow, k, stride, pad, nhwc);
     return launch_kernel(maxpool_kernel<int8_t>, g, 256, 0, s, (const int8_t *)x, (int8_t *)y, n, c, h, w, oh, ow, k,
                          stride, pad, nhwc);
+}
+
+cudaError_t launch_sppf_pool(const void *x, void *y, int n, int c, int h, int w, int k, int nhwc, int eb,
+                             cudaStream_t s) {
+    const int hk = k / 2, S = kSppfTile + 6 * hk;
+    // Channels per CTA: 32 bytes of each pixel; two S x S buffers in shared memory.
+    const int cg = 32 / eb;
+    const int smem = 2 * S * S * cg * eb;
+    const int tiles_w = (w + kSppfTile - 1) / kSppfTile, tiles_h = (h + kSppfTile - 1) / kSppfTile;
+    const dim3 grid(tiles_w * tiles_h, n, (c + cg - 1) / cg);
+    if (grid.z > 65535 || n > 65535) return cudaErrorInvalidValue;
+    cudaError_t e;
+    if (eb == 4) {
+        if ((e = set_max_dyn_smem(sppf_pool_kernel<float>, smem)) != cudaSuccess) return e;
+        return launch_kernel(sppf_pool_kernel<float>, grid, 256, smem, s, (const float *)x, (float *)y, n, c, h, w,
+                             hk, cg, tiles_w, nhwc);
+    }
+    if (eb == 2) {
+        if ((e = set_max_dyn_smem(sppf_pool_kernel<__nv_bfloat16>, smem)) != cudaSuccess) return e;
+        return launch_kernel(sppf_pool_kernel<__nv_bfloat16>, grid, 256, smem, s, (const __nv_bfloat16 *)x,
+                             (__nv_bfloat16 *)y, n, c, h, w, hk, cg, tiles_w, nhwc);
+    }
+    if ((e = set_max_dyn_smem(sppf_pool_kernel<int8_t>, smem)) != cudaSuccess) return e;
+    return launch_kernel(sppf_pool_kernel<int8_t>, grid, 256, smem, s, (const int8_t *)x, (int8_t *)y, n, c, h, w, hk,
+                         cg, tiles_w, nhwc);
 }
 
 unsigned int *device_status_word() {

@@ -127,6 +127,9 @@ class FusedConvBnSilu:
     def empty_y(self):
         return torch.empty(self.y_shape(), dtype=self.x_dtype, device=self.device)
 
+    def empty_x_b(self):
+        return torch.empty(self.x_b_shape(), dtype=self.x_dtype, device=self.device)
+
     # ----------------------------------------------------------------- calls
     def pack_input(self, x_nchw: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
         """NCHW float32 device tensor -> the plan's input format (kernel)."""
@@ -193,6 +196,20 @@ def maxpool2d(x: torch.Tensor, k: int, stride: int, pad: int, layout: int, out: 
     shape = (n, oh, ow, c) if layout == B.CBS_NHWC else (n, c, oh, ow)
     out = torch.empty(shape, dtype=x.dtype, device=x.device) if out is None else out
     B.cbs_maxpool2d(x, out, n, c, h, w, k, stride, pad, layout, _PREC_OF_DTYPE[x.dtype], current_stream())
+    return out
+
+
+def sppf_pool(x: torch.Tensor, k: int, layout: int, out: torch.Tensor | None = None):
+    """The SPPF block's three chained k x k stride-1 max pools of x, side by
+    side along channels (kernel)."""
+    if layout == B.CBS_NHWC:
+        n, h, w, c = x.shape
+        shape = (n, h, w, 3 * c)
+    else:
+        n, c, h, w = x.shape
+        shape = (n, 3 * c, h, w)
+    out = torch.empty(shape, dtype=x.dtype, device=x.device) if out is None else out
+    B.cbs_sppf_pool(x, out, n, c, h, w, k, layout, _PREC_OF_DTYPE[x.dtype], current_stream())
     return out
 
 

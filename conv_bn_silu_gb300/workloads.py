@@ -90,15 +90,17 @@ LAYER_LIST = (
 @dataclass(frozen=True)
 class ChainLayer:
     spec: LayerSpec
-    src: tuple   # ("frame",) | ("layer", i) | ("upcat", i_upsampled, i_skip)
+    src: tuple   # ("frame",) | ("layer", i) | ("upcat", i_upsampled, i_skip) | ("sppf", i)
 
 
 def _repeats(c: int, size: int, count: int):
     return [LayerSpec(c, c, 1 if i % 2 == 0 else 3, 1, size) for i in range(count)]
 
 
-def chain_layers() -> tuple:
-    """The 40-layer whole-frame chain.
+def chain_layers(sppf: bool = False) -> tuple:
+    """The 40-layer whole-frame chain, or with sppf=True the whole synthetic
+    frame: the same chain with the SPPF block of the detector's backbone
+    inserted after layer 10.
 
     Layers 0..10: the list's first eleven layers in order, from the frame.
     Layer 11: the list's 384->128 1x1 layer on concat(upsample2x(out10), out7)
@@ -107,17 +109,36 @@ def chain_layers() -> tuple:
     10 at 80x80 with 64 channels branching from layer 5, 9 at 40x40 with 128
     channels following layer 11, 9 at 20x20 with 256 channels branching from
     layer 10.
+
+    With sppf=True (42 layers), layer 11 is the SPPF's first 1x1 conv
+    (256->128 at 20x20, on out10), its output goes through three chained 5x5
+    stride-1 max pools, and layer 12 is the SPPF's second 1x1 conv (512->256)
+    on concat(out11, pool(out11), pool^2(out11), pool^3(out11)) (source
+    ("sppf", 11)).  Layer 13 is the neck layer on concat(upsample2x(out12),
+    out7), and the 20x20 repeats branch from the SPPF output (layer 12); the
+    80x80 repeats still branch from layer 5 and the 40x40 ones follow the
+    neck layer.
     """
     out = []
     for i, spec in enumerate(LAYER_LIST[:11]):
         out.append(ChainLayer(spec, ("frame",) if i == 0 else ("layer", i - 1)))
-    out.append(ChainLayer(LAYER_LIST[11], ("upcat", 10, 7)))
-    for stage_c, size, count, first_src in ((64, 80, 10, 5), (128, 40, 9, 11), (256, 20, 9, 10)):
+    deep = 10
+    if sppf:
+        out.append(ChainLayer(LayerSpec(256, 128, 1, 1, 20), ("layer", 10)))
+        out.append(ChainLayer(LayerSpec(512, 256, 1, 1, 20), ("sppf", 11)))
+        deep = 12
+    neck = len(out)
+    out.append(ChainLayer(LAYER_LIST[11], ("upcat", deep, 7)))
+    for stage_c, size, count, first_src in ((64, 80, 10, 5), (128, 40, 9, neck), (256, 20, 9, deep)):
         for j, spec in enumerate(_repeats(stage_c, size, count)):
             src = ("layer", first_src) if j == 0 else ("layer", len(out) - 1)
             out.append(ChainLayer(spec, src))
-    assert len(out) == 40
+    assert len(out) == (42 if sppf else 40)
     return tuple(out)
+
+
+# Max pool of the SPPF block: 5x5, stride 1, padding 2.
+SPPF_POOL_K = 5
 
 
 @dataclass

@@ -333,6 +333,25 @@ CBS_API cbs_status cbs_maxpool2d(const void *x, void *y, int n, int c, int h, in
                                  int layout, int prec, void *stream);
 
 /*
+ * cbs_sppf_pool -- the SPPF block's three chained max pools in one launch
+ * (page 1, "YOLO26N Inference Optimisation", kernel profile and "Op-by-op
+ * impact": maxpool2d, three per frame, each a 5x5 stride-1 pool feeding the
+ * next, their outputs concatenated with the pools' input):
+ *   y = concat(p(x), p(p(x)), p(p(p(x))))   along channels,
+ *   p = the k x k max pool with stride 1 and padding k/2, positions outside
+ *       the image taking no part (cbs_maxpool2d with stride 1, pad k/2).
+ * The result is the same, bit for bit, as three cbs_maxpool2d calls.  The
+ * fourth part of the block's concatenation, x itself, is not copied: the next
+ * layer reads concat(x, y) through a two-input plan (c_in_b = 3c).
+ * x: [n][c][h][w] (NCHW) or [n][h][w][c] (NHWC); y: [n][3c][h][w] or
+ * [n][h][w][3c].  k odd, 1..7.  prec: element type as for cbs_maxpool2d.
+ * A NaN in a window gives NaN.  Errors: CBS_ERR_INVALID_ARG for shapes and
+ * enums (n <= 65535).
+ */
+CBS_API cbs_status cbs_sppf_pool(const void *x, void *y, int n, int c, int h, int w, int k, int layout, int prec,
+                                 void *stream);
+
+/*
  * cbs_conv_bn_silu_f32_noalloc -- the FP32 CUDA-core fused layer for callers
  * that cannot allocate device memory.  No passage of the pages has a
  * counterpart: this is a deployment interface, not part of the method.

@@ -28,24 +28,46 @@ def upcat(a, b):
     return np.concatenate([a.repeat(2, axis=2).repeat(2, axis=3), b], axis=1)
 
 
+def sppf_cat(a):
+    """SPPF glue on an NCHW array: concat(a, p(a), p(p(a)), p(p(p(a)))), p the
+    5x5 stride-1 max pool with padding 2 (the oracle's pool applied three times)."""
+    parts, cur = [a], a
+    for _ in range(3):
+        cur = oracle.maxpool2d_f32(cur, wl.SPPF_POOL_K, 1, wl.SPPF_POOL_K // 2)
+        parts.append(cur)
+    return np.concatenate(parts, axis=1)
+
+
 def oracle_chain(chain, frame):
     """Oracle inputs and outputs of every layer (NCHW float32)."""
     ins, outs = [], []
     for i, cl in enumerate(chain.specs):
         s, src = cl.spec, cl.src
-        x = frame if src[0] == "frame" else outs[src[1]] if src[0] == "layer" else upcat(outs[src[1]], outs[src[2]])
+        if src[0] == "frame":
+            x = frame
+        elif src[0] == "layer":
+            x = outs[src[1]]
+        elif src[0] == "sppf":
+            x = sppf_cat(outs[src[1]])
+        else:
+            x = upcat(outs[src[1]], outs[src[2]])
         p = chain.params(i)
         ins.append(x)
         outs.append(oracle.conv_bn_silu_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, s.stride, s.pad))
     return ins, outs
 
 
-@pytest.mark.parametrize("prec,n,layout", [("fp32", 1, None), ("fp32", 1, B.CBS_NHWC), ("tf32", 16, None),
-                                           ("bf16", 16, None)])
-def test_chain_teacher_forced(cuda_lib, prec, n, layout):
+@pytest.mark.parametrize("prec,n,layout,sppf", [("fp32", 1, None, False), ("fp32", 1, B.CBS_NHWC, False),
+                                                ("tf32", 16, None, False), ("bf16", 16, None, False),
+                                                ("fp32", 1, None, True), ("bf16", 16, None, True)])
+def test_chain_teacher_forced(cuda_lib, prec, n, layout, sppf):
     """FP32 in NHWC runs the 3xTF32 tensor-core variant (split-K on the small
-    layers) and is held to the FP32 bar like the CUDA-core chain."""
-    chain = Chain(prec, n, layout=layout)
+    layers) and is held to the FP32 bar like the CUDA-core chain.  With sppf,
+    the whole synthetic frame: the SPPF block (1x1 conv, the three chained
+    pools in one glue kernel, 1x1 conv over the four-way concatenation read
+    as two inputs) after layer 10; its free-running run also checks the pool
+    glue inside the frame."""
+    chain = Chain(prec, n, layout=layout, sppf=sppf)
     frame = wl.frame(n)
     ins, outs = oracle_chain(chain, frame)
     s = torch.cuda.current_stream().cuda_stream
@@ -71,7 +93,7 @@ def test_chain_teacher_forced(cuda_lib, prec, n, layout):
             ref_max = outs[i] if prec == "tf32" else bf16_operand_ref(x_full, chain.params(i), sp.stride, sp.pad)
             e, _ = check_tc(prec, got, (outs[i], ref_max), i)
         worst.append(e)
-    print(f"{prec} n={n}: teacher-forced worst rel L2 {max(worst):.3e}")
+    print(f"{prec} n={n} sppf={sppf}: teacher-forced worst rel L2 {max(worst):.3e}")
 
     # Free-running chain from the frame.
     frame_dev = torch.from_numpy(frame).cuda()
@@ -82,5 +104,5 @@ def test_chain_teacher_forced(cuda_lib, prec, n, layout):
         y = to_nchw_numpy(chain.outs[i], chain.layout)
         assert np.isfinite(y).all(), i
         drift.append(rel_l2(y, outs[i]))
-    print(f"{prec} n={n}: free-running drift, last layer {drift[-1]:.3e}, max {max(drift):.3e}")
+    print(f"{prec} n={n} sppf={sppf}: free-running drift, last layer {drift[-1]:.3e}, max {max(drift):.3e}")
     assert max(drift) < 0.2
