@@ -14,6 +14,8 @@ from .oracle import (  # noqa: F401
     maxpool2d_f32,
     spec_exp,
     quantize_act,
+    dequantize_i8,
+    round_bf16,
     fold_quant_i8,
     requant,
     conv_i8,

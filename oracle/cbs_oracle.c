@@ -257,6 +257,38 @@ ORACLE_API void oracle_quantize_act_zp(const float *x, size_t count, float s_x, 
     }
 }
 
+/* Dequantisation at a seam between an INT8 layer and a layer kept in float
+ * ("Edge optimisation of YOLO26", Highlights: sensitive layers are kept in
+ * float; the affine scheme r = s (q - z) of Jacob et al., CVPR 2018):
+ *   r = (float)(q - z) * s,   one float multiply (q - z is exact in float). */
+ORACLE_API void oracle_dequantize_i8(const int8_t *q, size_t count, float s, int z, float *r)
+{
+#pragma omp parallel for
+    for (size_t i = 0; i < count; ++i) r[i] = (float)((int)q[i] - z) * s;
+}
+
+/* Round to bfloat16 (the upper 16 bits of the float), to nearest with ties
+ * to even, and return the rounded value as float: the format in which a
+ * layer kept in BF16 receives its input.  NaN stays NaN. */
+ORACLE_API void oracle_round_bf16(const float *x, size_t count, float *out)
+{
+#pragma omp parallel for
+    for (size_t i = 0; i < count; ++i) {
+        uint32_t u;
+        memcpy(&u, &x[i], 4);
+        if ((u & 0x7fffffffu) > 0x7f800000u) {
+            u |= 0x00400000u;            /* quiet NaN */
+        } else {
+            const uint32_t rest = u & 0xffffu, keep = u >> 16;
+            /* above half an ulp, or exactly half with an odd kept part: round up */
+            if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) u = (keep + 1u) << 16;
+            else u = keep << 16;
+        }
+        u &= 0xffff0000u;
+        memcpy(&out[i], &u, 4);
+    }
+}
+
 /* Fold BN into the weights and quantise them per output channel.
  *   s_c   = gamma / sqrtf(var + eps)
  *   w'    = w * s_c                      b' = beta - mean * s_c

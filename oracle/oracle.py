@@ -51,6 +51,8 @@ def _load():
         lib.oracle_requant_zp.restype = ctypes.c_int8
         lib.oracle_conv_i8_zp.argtypes = [P, P, P, P, F, I, I, I, I, I, I, I, I, I, I, P, P]
         lib.oracle_conv_i8_zp.restype = I
+        lib.oracle_dequantize_i8.argtypes = [P, Z, F, I, P]
+        lib.oracle_round_bf16.argtypes = [P, Z, P]
         _lib = lib
     return _lib
 
@@ -171,6 +173,22 @@ def quantize_act(x, s_x: float, z_x: int = 0) -> np.ndarray:
     else:
         _load().oracle_quantize_act(_ptr(x), x.size, s_x, _ptr(q))
     return q
+
+
+def dequantize_i8(q, s: float, z: int = 0) -> np.ndarray:
+    """r = float(q - z) * s (one float multiply), same shape as q."""
+    q = np.ascontiguousarray(q, np.int8)
+    r = np.empty(q.shape, np.float32)
+    _load().oracle_dequantize_i8(_ptr(q), q.size, float(s), int(z), _ptr(r))
+    return r
+
+
+def round_bf16(x) -> np.ndarray:
+    """float32 values rounded to bfloat16 (nearest even), as float32."""
+    x = _f32(x)
+    out = np.empty_like(x)
+    _load().oracle_round_bf16(_ptr(x), x.size, _ptr(out))
+    return out
 
 
 def fold_quant_i8(w, gamma, beta, mean, var, eps: float, s_x: float):

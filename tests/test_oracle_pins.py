@@ -499,3 +499,45 @@ def test_maxpool_padding_takes_no_part_and_nan_propagates():
     assert np.all(oracle.maxpool2d_f32(x, 3, 1, 1) == -5)
     x[0, 0, 1, 1] = np.nan
     assert np.isnan(oracle.maxpool2d_f32(x, 3, 1, 1)).all()
+
+
+# ------------------------------------------------------------ INT8 seams
+def test_round_bf16_matches_torch_conversion():
+    """oracle.round_bf16 against torch's float32 -> bfloat16 conversion (a
+    library routine, round to nearest even), on random magnitudes, on exact
+    ties with even and odd kept parts, subnormals, infinities and zero."""
+    import torch
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal(200000) * np.exp2(rng.integers(-140, 120, 200000))).astype(np.float32)
+    ties = np.array([0x3f808000, 0x3f818000, 0xbf808000, 0xbf818000, 0x3f80ffff, 0x3f807fff,
+                     0x00008000, 0x00018000, 0x7f7f8000, 0x00000001], dtype=np.uint32).view(np.float32)
+    special = np.array([0.0, -0.0, np.inf, -np.inf, 1e-45, -3e-39], dtype=np.float32)
+    x = np.concatenate([x, ties, special])
+    want = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+    got = oracle.round_bf16(x)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    nan = oracle.round_bf16(np.array([np.nan], np.float32))
+    assert np.isnan(nan).all()
+
+
+def test_dequantize_power_of_two_scale_is_exact():
+    """With s = 2^k the product (q - z) * s is exact: the closed form in
+    integer arithmetic."""
+    q = np.arange(-128, 128, dtype=np.int8)
+    for k in (-7, -1, 0, 3):
+        for z in (0, -128, 17, 127):
+            got = oracle.dequantize_i8(q, float(2.0 ** k), z)
+            want = np.array([(int(v) - z) * 2.0 ** k for v in q])
+            assert np.array_equal(got.astype(np.float64), want)
+
+
+def test_dequantize_inverts_the_quantiser():
+    """dequantize(quantize(x)) is within half a step of x wherever the
+    quantiser does not saturate: scale and zero point mean the same thing
+    on both sides of a seam (a sign or offset slip fails this)."""
+    rng = np.random.default_rng(5)
+    for s, z in ((0.0347809, 0), (0.05, -40), (0.013, 90)):
+        lo, hi = (-128 - z + 0.5) * s, (127 - z - 0.5) * s
+        x = rng.uniform(lo, hi, 100000).astype(np.float32)
+        r = oracle.dequantize_i8(oracle.quantize_act(x, s, z), s, z)
+        assert np.max(np.abs(r.astype(np.float64) - x)) <= s / 2 * (1 + 1e-5)
