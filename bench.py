@@ -114,6 +114,10 @@ WORKLOADS = {
     # The whole synthetic frame: the chain with the SPPF block (two more fused
     # layers and the three chained 5x5 pools in one glue kernel).
     "frame_fp32_n1": dict(kind="chain", n=1, prec="fp32", sppf=True),
+    # The 40-layer chain on INT8 layers; and with the first layer (the raw
+    # frame's) and the last kept in BF16, with quantise/dequantise seams.
+    "chain_int8_n16": dict(kind="chain", n=16, prec="int8"),
+    "chain_int8_n16_keepfloat": dict(kind="chain", n=16, prec="int8", keep_float=(0, 39)),
     "frame_bf16_n16": dict(kind="chain", n=16, prec="bf16", sppf=True),
     # The list with the residual form of the epilogue, y = SiLU(BN(conv)) + r, on every
     # stride-1 layer whose input and output shapes match (a bottleneck's skip add).
@@ -128,7 +132,7 @@ WORKLOADS = {
 EXTRA_DEFAULT = ("layer_list_bf16_n16", "layer_list_tf32_n16", "layer_list_int8_n16", "chain_fp32_n1",
                  "chain_bf16_n16", "layer_list_bf16_n16_residual", "layer_list_int8_n16_asym",
                  "layer_list_fp32_n16_nhwc", "layer_list_fp32_n1_nhwc", "chain_fp32_n1_nhwc", "frame_fp32_n1",
-                 "frame_bf16_n16")
+                 "frame_bf16_n16", "chain_int8_n16", "chain_int8_n16_keepfloat")
 
 
 # DRAM traffic of the dominant kernel over one step of a workload, from one
@@ -204,6 +208,11 @@ def int8_scales():
     return json.load(open(path))["layer_list"]
 
 
+def int8_chain_scales():
+    path = os.path.join(ROOT, "tests", "golden", "int8_chain_scales.json")
+    return json.load(open(path))["chain"]
+
+
 class ListWorkload:
     """Independent layers, each on its own resident input; inputs and outputs
     rotate over R copies so one rotation exceeds twice the L2 size."""
@@ -273,25 +282,27 @@ class ChainWorkload:
         from conv_bn_silu_gb300.chain import Chain
         self.cfg, self.n, self.prec = cfg, cfg["n"], cfg["prec"]
         lay = B.CBS_NHWC if cfg.get("layout") == "nhwc" else None
-        self.chain = Chain(self.prec, self.n, device=device, layout=lay, sppf=bool(cfg.get("sppf")))
+        kw = {}
+        if self.prec == "int8":
+            kw = dict(out_scales=int8_chain_scales(), keep_float=cfg.get("keep_float", ()))
+        self.chain = Chain(self.prec, self.n, device=device, layout=lay, sppf=bool(cfg.get("sppf")), **kw)
         self.nhwc = self.chain.layout == B.CBS_NHWC
         self.frame = torch.from_numpy(wl.frame(self.n)).to(device)
         self.specs = [cl.spec for cl in self.chain.specs]
         self.layers = self.chain.layers
-        ab = act_bytes(self.prec)
-        self.step_bytes = self.chain.alg_bytes(ab)
+        self.step_bytes = self.chain.alg_bytes()
         self.R = 1
         self.launches_per_step = self.chain.launches_per_frame()
 
     def step(self, r, stream_id, events=None, stream=None):
         from conv_bn_silu_gb300 import _binding as B
         c = self.chain
-        B.cbs_pack_input(c.layers[0].plan, self.frame, c.x0, 0.0, stream_id)
-        for i, layer in enumerate(c.layers):
+        c.pack_frame(self.frame, stream_id)
+        for i in range(len(c.layers)):
             c.glue_before(i, stream_id)
             if events is not None:
                 events[i].record(stream)
-            layer(c.input_of(i), c.outs[i], stream=stream_id, x_b=c.second_input_of(i))
+            c.call(i, stream_id)
         if events is not None:
             events[len(c.layers)].record(stream)
 

@@ -34,7 +34,8 @@ EXPORTED = (
     "cbs_upsample2x_concat", "cbs_workspace_init", "cbs_read_device_status", "cbs_status_string",
     "cbs_last_error", "cbs_abi_version", "cbs_conv_bn_silu_f32_noalloc", "cbs_conv_bn_act",
     "cbs_conv_bn_act_cat", "cbs_set_launch_options", "cbs_launch_options", "cbs_maxpool2d",
-    "cbs_conv_bn_silu_i8_cat", "cbs_selftest_wait_timeout", "cbs_sppf_pool",
+    "cbs_conv_bn_silu_i8_cat", "cbs_selftest_wait_timeout", "cbs_sppf_pool", "cbs_dequantize_i8",
+    "cbs_quantize_i8",
 )
 
 
@@ -85,6 +86,8 @@ def lib():
         L.cbs_upsample2x_concat.argtypes = [P, I, P, I, P, I, I, I, I, I, P]
         L.cbs_maxpool2d.argtypes = [P, P, I, I, I, I, I, I, I, I, I, P]
         L.cbs_sppf_pool.argtypes = [P, P, I, I, I, I, I, I, I, P]
+        L.cbs_dequantize_i8.argtypes = [P, P, Z, F, I, I, P]
+        L.cbs_quantize_i8.argtypes = [P, I, P, Z, F, I, P]
         L.cbs_conv_bn_silu_f32_noalloc.argtypes = [ctypes.POINTER(cbs_plan_t), P, P, P, P, P]
         L.cbs_workspace_init.argtypes = [P, Z, P]
         L.cbs_read_device_status.argtypes = [ctypes.POINTER(I), I, P]
@@ -175,6 +178,15 @@ def cbs_maxpool2d(x, y, n, c, h, w, k, stride, pad, layout, prec, stream):
 
 def cbs_sppf_pool(x, y, n, c, h, w, k, layout, prec, stream):
     _check(lib().cbs_sppf_pool(_p(x), _p(y), n, c, h, w, k, layout, prec, stream), "cbs_sppf_pool")
+
+
+def cbs_dequantize_i8(q, out, count, s, z, out_prec, stream):
+    _check(lib().cbs_dequantize_i8(_p(q), _p(out), int(count), float(s), int(z), int(out_prec), stream),
+           "cbs_dequantize_i8")
+
+
+def cbs_quantize_i8(x, in_prec, q, count, s, z, stream):
+    _check(lib().cbs_quantize_i8(_p(x), int(in_prec), _p(q), int(count), float(s), int(z), stream), "cbs_quantize_i8")
 
 
 def cbs_set_launch_options(flags: int):

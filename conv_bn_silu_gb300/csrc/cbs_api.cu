@@ -581,6 +581,31 @@ cbs_status cbs_maxpool2d(const void *x, void *y, int n, int c, int h, int w, int
                       "max-pool launch");
 }
 
+cbs_status cbs_dequantize_i8(const int8_t *q, void *out, size_t count, float s, int z, int out_prec,
+                             void *stream) {
+    CBS_TRY(check_ptr(q, "q"));
+    CBS_TRY(check_ptr(out, "out"));
+    if (!(s > 0.0f) || !(s < 3.0e38f)) return fail(CBS_ERR_INVALID_ARG, "scale must be positive and finite");
+    if (z < -128 || z > 127) return fail(CBS_ERR_INVALID_ARG, "zero point %d outside [-128, 127]", z);
+    if (out_prec != CBS_FP32 && out_prec != CBS_TF32 && out_prec != CBS_BF16)
+        return fail(CBS_ERR_INVALID_ARG, "output precision must be FP32, TF32 or BF16");
+    if (count == 0) return CBS_OK;
+    return cuda_check(launch_dequantize_i8(q, out, count, s, z, out_prec == CBS_BF16, (cudaStream_t)stream),
+                      "dequantise launch");
+}
+
+cbs_status cbs_quantize_i8(const void *x, int in_prec, int8_t *q, size_t count, float s, int z, void *stream) {
+    CBS_TRY(check_ptr(x, "x"));
+    CBS_TRY(check_ptr(q, "q"));
+    if (!(s > 0.0f) || !(s < 3.0e38f)) return fail(CBS_ERR_INVALID_ARG, "scale must be positive and finite");
+    if (z < -128 || z > 127) return fail(CBS_ERR_INVALID_ARG, "zero point %d outside [-128, 127]", z);
+    if (in_prec != CBS_FP32 && in_prec != CBS_TF32 && in_prec != CBS_BF16)
+        return fail(CBS_ERR_INVALID_ARG, "input precision must be FP32, TF32 or BF16");
+    if (count == 0) return CBS_OK;
+    return cuda_check(launch_quantize_i8(x, in_prec == CBS_BF16, q, count, s, z, (cudaStream_t)stream),
+                      "quantise launch");
+}
+
 cbs_status cbs_sppf_pool(const void *x, void *y, int n, int c, int h, int w, int k, int layout, int prec,
                          void *stream) {
     CBS_TRY(check_ptr(x, "x"));

@@ -182,6 +182,9 @@ cudaError_t launch_upsample_concat(const void *a, int ca, const void *b, int cb,
                                    int n, int h, int w, int nhwc, int elem_bytes,
                                    cudaStream_t s);
 
+cudaError_t launch_dequantize_i8(const int8_t *q, void *out, size_t count, float s, int z, int out_bf16,
+                                 cudaStream_t st);
+cudaError_t launch_quantize_i8(const void *x, int in_bf16, int8_t *q, size_t count, float s, int z, cudaStream_t st);
 cudaError_t launch_sppf_pool(const void *x, void *y, int n, int c, int h, int w, int k, int nhwc, int eb,
                              cudaStream_t s);
 cudaError_t launch_maxpool(const void *x, void *y, int n, int c, int h, int w, int k, int stride, int pad, int nhwc,

@@ -422,15 +422,17 @@ __global__ void maxpool_kernel(const T *__restrict__ x, T *__restrict__ y, int N
 // y = concat(p(x), p(p(x)), p(p(p(x)))) along channels, p = the k x k max
 // pool with stride 1 and padding k/2 whose padded positions take no part (the
 // SPPF block's three chained pools; "YOLO26N Inference Optimisation", kernel
-// profile: maxpool2d, three per frame).  One CTA per (16x16 output tile,
-// image, group of kSppfCg channels) keeps the tile with a halo of 3 (k/2) in
-// shared memory.  Positions outside the image hold the type's lowest value:
-// every window holds its own in-image centre, so the lowest value never wins
-// over a real one and the max equals the max over the in-image positions.
-// Each pool is a horizontal, then a vertical running max in shared memory;
-// the region it covers shrinks by k/2 per pool, and after each pool the
-// tile's interior goes to its channel slice of y.  A NaN in a window gives NaN.
-constexpr int kSppfTile = 16;
+// profile: maxpool2d, three per frame).  One CTA per (output tile of up to
+// 32 x 32, image, group of 32 bytes of channels) keeps the tile with a halo of
+// 3 (k/2) in shared memory.  Positions outside the image hold the type's
+// lowest value: every window holds its own in-image centre, so the lowest
+// value never wins over a real one and the max equals the max over the
+// in-image positions.  Each pool is a horizontal, then a vertical running
+// max in shared memory over a region that shrinks by k/2 per pool; after
+// each pool the tile's interior goes to its channel slice of y.  A NaN in a
+// window gives NaN.  Rows are spread over the warps and (column, channel)
+// pairs over the lanes, so no index needs a division by a runtime value.
+constexpr int kSppfMaxTile = 32;
 
 template <typename T>
 struct PoolOps;
@@ -455,74 +457,221 @@ struct PoolOps<int8_t> {
     static __device__ __forceinline__ int8_t mx(int8_t a, int8_t b) { return a > b ? a : b; }
 };
 
+// Max of two 16-byte vectors of T, element by element (NaN-propagating for
+// the float types); the vector of lowest values.
 template <typename T>
+struct VecPool;
+template <>
+struct VecPool<float> {
+    static __device__ __forceinline__ uint4 lowest() { return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u); }
+    static __device__ __forceinline__ uint32_t m1(uint32_t a, uint32_t b) {
+        return __float_as_uint(PoolOps<float>::mx(__uint_as_float(a), __uint_as_float(b)));
+    }
+    static __device__ __forceinline__ uint4 mx(uint4 a, uint4 b) {
+        return make_uint4(m1(a.x, b.x), m1(a.y, b.y), m1(a.z, b.z), m1(a.w, b.w));
+    }
+};
+template <>
+struct VecPool<__nv_bfloat16> {
+    static __device__ __forceinline__ uint4 lowest() { return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u); }
+    static __device__ __forceinline__ uint32_t m1(uint32_t a, uint32_t b) {
+        __nv_bfloat162 r = __hmax2_nan(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
+        return *reinterpret_cast<uint32_t *>(&r);
+    }
+    static __device__ __forceinline__ uint4 mx(uint4 a, uint4 b) {
+        return make_uint4(m1(a.x, b.x), m1(a.y, b.y), m1(a.z, b.z), m1(a.w, b.w));
+    }
+};
+template <>
+struct VecPool<int8_t> {
+    static __device__ __forceinline__ uint4 lowest() { return make_uint4(0x80808080u, 0x80808080u, 0x80808080u, 0x80808080u); }
+    static __device__ __forceinline__ uint4 mx(uint4 a, uint4 b) {
+        return make_uint4(__vmaxs4(a.x, b.x), __vmaxs4(a.y, b.y), __vmaxs4(a.z, b.z), __vmaxs4(a.w, b.w));
+    }
+};
+
+// Shared memory holds, per position of the tile and its halo, the CTA's 32
+// bytes of channels as two 16-byte vectors.  Global memory is read and
+// written in 16-byte vectors where a pixel's channels are 16-byte multiples
+// (NHWC with C * sizeof(T) a multiple of 16), element by element otherwise.
+template <typename T, int HK>
 __global__ void __launch_bounds__(256) sppf_pool_kernel(const T *__restrict__ x, T *__restrict__ y, int N, int C,
-                                                        int H, int W, int hk, int cg, int tiles_w, int nhwc) {
+                                                        int H, int W, int TH, int TW, int tiles_w, int nhwc) {
     extern __shared__ __align__(16) uint8_t sppf_smem[];
-    using O = PoolOps<T>;
-    const int R = 3 * hk, S = kSppfTile + 2 * R;
-    T *buf = reinterpret_cast<T *>(sppf_smem);
-    T *tmp = buf + (size_t)S * S * cg;
+    using V = VecPool<T>;
+    constexpr int VE = 16 / (int)sizeof(T);   // elements per 16-byte vector
+    constexpr int CG = 2 * VE;                // channels per CTA
+    constexpr int R = 3 * HK;
+    const int SH = TH + 2 * R, SW = TW + 2 * R;
+    uint4 *buf = reinterpret_cast<uint4 *>(sppf_smem);
+    uint4 *tmp = buf + (size_t)SH * SW * 2;
     const int n = blockIdx.y;
-    const int c0 = blockIdx.z * cg;
-    const int oh0 = (blockIdx.x / tiles_w) * kSppfTile, ow0 = (blockIdx.x % tiles_w) * kSppfTile;
+    const int c0 = blockIdx.z * CG;
+    const int oh0 = (blockIdx.x / tiles_w) * TH, ow0 = (blockIdx.x % tiles_w) * TW;
     const int C3 = 3 * C;
+    const bool vec = nhwc && (C * (int)sizeof(T)) % 16 == 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
     // The tile and its halo; the lowest value outside the image and past C.
-    for (int e = threadIdx.x; e < S * S * cg; e += blockDim.x) {
-        const int c = e % cg, pos = e / cg;
-        const int ih = oh0 - R + pos / S, iw = ow0 - R + pos % S;
-        T v = O::lowest();
-        if (ih >= 0 && ih < H && iw >= 0 && iw < W && c0 + c < C)
-            v = nhwc ? x[(((size_t)n * H + ih) * W + iw) * C + c0 + c] : x[(((size_t)n * C + c0 + c) * H + ih) * W + iw];
-        buf[e] = v;
+    for (int yy = warp; yy < SH; yy += nwarps) {
+        const int ih = oh0 - R + yy;
+        for (int i = lane; i < SW * 2; i += 32) {
+            const int xx = i >> 1, v = i & 1;
+            const int iw = ow0 - R + xx;
+            const int cv = c0 + v * VE;
+            uint4 val = V::lowest();
+            if (ih >= 0 && ih < H && iw >= 0 && iw < W && cv < C) {
+                if (vec) {
+                    val = __ldg(reinterpret_cast<const uint4 *>(x + (((size_t)n * H + ih) * W + iw) * C + cv));
+                } else {
+                    T e[VE];
+                    const T *lw = reinterpret_cast<const T *>(&val);
+#pragma unroll
+                    for (int j = 0; j < VE; ++j)
+                        e[j] = cv + j < C ? (nhwc ? x[(((size_t)n * H + ih) * W + iw) * C + cv + j]
+                                                  : x[(((size_t)n * C + cv + j) * H + ih) * W + iw])
+                                          : lw[j];
+                    val = *reinterpret_cast<const uint4 *>(e);
+                }
+            }
+            buf[(size_t)yy * SW * 2 + i] = val;
+        }
     }
     __syncthreads();
+#pragma unroll 1
     for (int r = 1; r <= 3; ++r) {
-        const int ext = (3 - r) * hk;
-        // Horizontal max over rows [R-ext-hk, R+T+ext+hk) and columns [R-ext, R+T+ext).
-        {
-            const int y0 = R - ext - hk, ny = kSppfTile + 2 * (ext + hk);
-            const int x0 = R - ext, nx = kSppfTile + 2 * ext;
-            for (int e = threadIdx.x; e < ny * nx * cg; e += blockDim.x) {
-                const int c = e % cg, pos = e / cg;
-                const int yy = y0 + pos / nx, xx = x0 + pos % nx;
-                const T *row = buf + ((size_t)yy * S) * cg + c;
-                T v = row[(size_t)(xx - hk) * cg];
-                for (int dx = -hk + 1; dx <= hk; ++dx) v = O::mx(v, row[(size_t)(xx + dx) * cg]);
-                tmp[((size_t)yy * S + xx) * cg + c] = v;
+        const int ext = (3 - r) * HK;
+        // Horizontal max over rows [R-ext-HK, R+TH+ext+HK) and columns [R-ext, R+TW+ext).
+        const int hx0 = R - ext, hnx = TW + 2 * ext;
+        for (int yy = R - ext - HK + warp; yy < R + TH + ext + HK; yy += nwarps) {
+            const uint4 *row = buf + (size_t)yy * SW * 2;
+            uint4 *trow = tmp + (size_t)yy * SW * 2;
+            for (int i = lane; i < hnx * 2; i += 32) {
+                const int j = hx0 * 2 + i;   // (column, vector) index within the row
+                uint4 m = row[j - 2 * HK];
+#pragma unroll
+                for (int dx = -HK + 1; dx <= HK; ++dx) m = V::mx(m, row[j + 2 * dx]);
+                trow[j] = m;
             }
         }
         __syncthreads();
-        // Vertical max into buf over rows and columns [R-ext, R+T+ext).
-        {
-            const int y0 = R - ext, nyx = kSppfTile + 2 * ext;
-            for (int e = threadIdx.x; e < nyx * nyx * cg; e += blockDim.x) {
-                const int c = e % cg, pos = e / cg;
-                const int yy = y0 + pos / nyx, xx = y0 + pos % nyx;
-                const int ih = oh0 - R + yy, iw = ow0 - R + xx;
-                T v = O::lowest();
+        // Vertical max into buf over rows and columns [R-ext, R+T+ext); the lowest
+        // value outside the image.
+        for (int yy = R - ext + warp; yy < R + TH + ext; yy += nwarps) {
+            const int ih = oh0 - R + yy;
+            uint4 *brow = buf + (size_t)yy * SW * 2;
+            for (int i = lane; i < hnx * 2; i += 32) {
+                const int j = hx0 * 2 + i;
+                const int iw = ow0 - R + (j >> 1);
+                uint4 m = V::lowest();
                 if (ih >= 0 && ih < H && iw >= 0 && iw < W) {
-                    const T *col = tmp + (size_t)xx * cg + c;
-                    v = col[(size_t)(yy - hk) * S * cg];
-                    for (int dy = -hk + 1; dy <= hk; ++dy) v = O::mx(v, col[(size_t)(yy + dy) * S * cg]);
+                    const uint4 *col = tmp + j;
+                    m = col[(size_t)(yy - HK) * SW * 2];
+#pragma unroll
+                    for (int dy = -HK + 1; dy <= HK; ++dy) m = V::mx(m, col[(size_t)(yy + dy) * SW * 2]);
                 }
-                buf[((size_t)yy * S + xx) * cg + c] = v;
+                brow[j] = m;
             }
         }
         __syncthreads();
-        // Pool r over the tile's interior to channel slice r - 1 of y.
-        for (int e = threadIdx.x; e < kSppfTile * kSppfTile * cg; e += blockDim.x) {
-            const int c = e % cg, pos = e / cg;
-            const int oh = oh0 + pos / kSppfTile, ow = ow0 + pos % kSppfTile;
-            if (oh >= H || ow >= W || c0 + c >= C) continue;
-            const T v = buf[((size_t)(R + pos / kSppfTile) * S + R + pos % kSppfTile) * cg + c];
-            const int ch = (r - 1) * C + c0 + c;
-            if (nhwc) y[(((size_t)n * H + oh) * W + ow) * C3 + ch] = v;
-            else y[(((size_t)n * C3 + ch) * H + oh) * W + ow] = v;
+        // Pool r over the tile's interior to channel slice r - 1 of y (the next
+        // pool's horizontal pass only reads buf as well).
+        for (int ty = warp; ty < TH; ty += nwarps) {
+            const int oh = oh0 + ty;
+            if (oh >= H) break;
+            const uint4 *brow = buf + (size_t)(R + ty) * SW * 2;
+            for (int i = lane; i < TW * 2; i += 32) {
+                const int tx = i >> 1, v = i & 1;
+                const int ow = ow0 + tx;
+                const int cv = c0 + v * VE;
+                if (ow >= W || cv >= C) continue;
+                const uint4 val = brow[(R + tx) * 2 + v];
+                const int ch = (r - 1) * C + cv;
+                if (vec) {
+                    *reinterpret_cast<uint4 *>(y + (((size_t)n * H + oh) * W + ow) * C3 + ch) = val;
+                } else {
+                    const T *e = reinterpret_cast<const T *>(&val);
+#pragma unroll
+                    for (int j = 0; j < VE; ++j) {
+                        if (cv + j >= C) break;
+                        if (nhwc) y[(((size_t)n * H + oh) * W + ow) * C3 + ch + j] = e[j];
+                        else y[(((size_t)n * C3 + ch + j) * H + oh) * W + ow] = e[j];
+                    }
+                }
+            }
         }
-        // The next pool's horizontal pass reads buf, which these writes only read.
+    }
+}
+
+// ------------------------------------------------------------ INT8 seams
+// Between an INT8 layer and a layer kept in float ("Edge optimisation of
+// YOLO26", Highlights: sensitive layers stay in float), in the affine scheme
+// r = s (q - z):
+//   dequantise: r = (float)(q - z) * s, one IEEE multiply, then (BF16) the
+//               round-to-nearest-even conversion;
+//   quantise:   q = clamp(rne(x / s) + z, -128, 127), IEEE division (the
+//               quantiser of the chain's entry packing).
+// Elementwise over count values; 16 codes per thread (16-byte code vectors),
+// the last ragged group element by element.
+template <typename TO>
+__device__ __forceinline__ void store_deq(TO *out, size_t i, float v);
+template <>
+__device__ __forceinline__ void store_deq<float>(float *out, size_t i, float v) { out[i] = v; }
+template <>
+__device__ __forceinline__ void store_deq<__nv_bfloat16>(__nv_bfloat16 *out, size_t i, float v) {
+    out[i] = __float2bfloat16_rn(v);
+}
+
+template <typename TO>
+__global__ void dequantize_i8_kernel(const int8_t *__restrict__ q, TO *__restrict__ out, size_t count, float s, int z) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+    const size_t groups = (count + 15) / 16;
+    for (size_t g = blockIdx.x * (size_t)blockDim.x + threadIdx.x; g < groups; g += (size_t)gridDim.x * blockDim.x) {
+        const size_t i0 = g * 16;
+        if (i0 + 16 <= count) {
+            const uint4 w = __ldg(reinterpret_cast<const uint4 *>(q + i0));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int code = (int)(int8_t)(ws[j >> 2] >> (8 * (j & 3)));
+                store_deq<TO>(out, i0 + j, __fmul_rn((float)(code - z), s));
+            }
+        } else {
+            for (size_t i = i0; i < count; ++i) store_deq<TO>(out, i, __fmul_rn((float)((int)q[i] - z), s));
+        }
+    }
+}
+
+template <typename TI>
+__device__ __forceinline__ float load_val(const TI *x, size_t i);
+template <>
+__device__ __forceinline__ float load_val<float>(const float *x, size_t i) { return x[i]; }
+template <>
+__device__ __forceinline__ float load_val<__nv_bfloat16>(const __nv_bfloat16 *x, size_t i) {
+    return __bfloat162float(x[i]);
+}
+
+template <typename TI>
+__global__ void quantize_i8_kernel(const TI *__restrict__ x, int8_t *__restrict__ q, size_t count, float s, int z) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+    const size_t groups = (count + 15) / 16;
+    for (size_t g = blockIdx.x * (size_t)blockDim.x + threadIdx.x; g < groups; g += (size_t)gridDim.x * blockDim.x) {
+        const size_t i0 = g * 16;
+        const int n = i0 + 16 <= count ? 16 : (int)(count - i0);
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        for (int j = 0; j < n; ++j) {
+            float v = __fadd_rn(rintf(__fdiv_rn(load_val<TI>(x, i0 + j), s)), (float)z);
+            v = fminf(fmaxf(v, -128.0f), 127.0f);
+            w[j >> 2] |= (uint32_t)(uint8_t)(int8_t)v << (8 * (j & 3));
+        }
+        if (n == 16) {
+            *reinterpret_cast<uint4 *>(q + i0) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+            for (int j = 0; j < n; ++j) q[i0 + j] = (int8_t)(w[j >> 2] >> (8 * (j & 3)));
+        }
     }
 }
 
@@ -677,29 +826,47 @@ cudaError_t launch_maxpool(const void *x, void *y, int n, int c, int h, int w, i
                          stride, pad, nhwc);
 }
 
-cudaError_t launch_sppf_pool(const void *x, void *y, int n, int c, int h, int w, int k, int nhwc, int eb,
-                             cudaStream_t s) {
-    const int hk = k / 2, S = kSppfTile + 6 * hk;
-    // Channels per CTA: 32 bytes of each pixel; two S x S buffers in shared memory.
-    const int cg = 32 / eb;
-    const int smem = 2 * S * S * cg * eb;
-    const int tiles_w = (w + kSppfTile - 1) / kSppfTile, tiles_h = (h + kSppfTile - 1) / kSppfTile;
+template <typename T>
+cudaError_t launch_sppf_typed(const void *x, void *y, int n, int c, int h, int w, int hk, int nhwc, cudaStream_t s) {
+    // Output tile: the whole image up to 32 x 32 (a 20x20 map is one tile).
+    const int th = h < kSppfMaxTile ? h : kSppfMaxTile, tw = w < kSppfMaxTile ? w : kSppfMaxTile;
+    const int cg = 32 / (int)sizeof(T);   // two 16-byte vectors of channels per CTA
+    const int smem = 2 * (th + 6 * hk) * (tw + 6 * hk) * 32;
+    const int tiles_w = (w + tw - 1) / tw, tiles_h = (h + th - 1) / th;
     const dim3 grid(tiles_w * tiles_h, n, (c + cg - 1) / cg);
     if (grid.z > 65535 || n > 65535) return cudaErrorInvalidValue;
-    cudaError_t e;
-    if (eb == 4) {
-        if ((e = set_max_dyn_smem(sppf_pool_kernel<float>, smem)) != cudaSuccess) return e;
-        return launch_kernel(sppf_pool_kernel<float>, grid, 256, smem, s, (const float *)x, (float *)y, n, c, h, w,
-                             hk, cg, tiles_w, nhwc);
+    auto launch = [&](auto kern) -> cudaError_t {
+        cudaError_t e = set_max_dyn_smem(kern, smem);
+        if (e != cudaSuccess) return e;
+        return launch_kernel(kern, grid, 256, smem, s, (const T *)x, (T *)y, n, c, h, w, th, tw, tiles_w, nhwc);
+    };
+    switch (hk) {
+    case 0: return launch(sppf_pool_kernel<T, 0>);
+    case 1: return launch(sppf_pool_kernel<T, 1>);
+    case 2: return launch(sppf_pool_kernel<T, 2>);
+    default: return launch(sppf_pool_kernel<T, 3>);
     }
-    if (eb == 2) {
-        if ((e = set_max_dyn_smem(sppf_pool_kernel<__nv_bfloat16>, smem)) != cudaSuccess) return e;
-        return launch_kernel(sppf_pool_kernel<__nv_bfloat16>, grid, 256, smem, s, (const __nv_bfloat16 *)x,
-                             (__nv_bfloat16 *)y, n, c, h, w, hk, cg, tiles_w, nhwc);
-    }
-    if ((e = set_max_dyn_smem(sppf_pool_kernel<int8_t>, smem)) != cudaSuccess) return e;
-    return launch_kernel(sppf_pool_kernel<int8_t>, grid, 256, smem, s, (const int8_t *)x, (int8_t *)y, n, c, h, w, hk,
-                         cg, tiles_w, nhwc);
+}
+
+cudaError_t launch_sppf_pool(const void *x, void *y, int n, int c, int h, int w, int k, int nhwc, int eb,
+                             cudaStream_t s) {
+    const int hk = k / 2;   // odd k <= 7 (checked by the caller)
+    if (eb == 4) return launch_sppf_typed<float>(x, y, n, c, h, w, hk, nhwc, s);
+    if (eb == 2) return launch_sppf_typed<__nv_bfloat16>(x, y, n, c, h, w, hk, nhwc, s);
+    return launch_sppf_typed<int8_t>(x, y, n, c, h, w, hk, nhwc, s);
+}
+
+cudaError_t launch_dequantize_i8(const int8_t *q, void *out, size_t count, float s, int z, int out_bf16,
+                                 cudaStream_t st) {
+    const int g = grid_for((count + 15) / 16, 256);
+    if (out_bf16) return launch_kernel(dequantize_i8_kernel<__nv_bfloat16>, g, 256, 0, st, q, (__nv_bfloat16 *)out, count, s, z);
+    return launch_kernel(dequantize_i8_kernel<float>, g, 256, 0, st, q, (float *)out, count, s, z);
+}
+
+cudaError_t launch_quantize_i8(const void *x, int in_bf16, int8_t *q, size_t count, float s, int z, cudaStream_t st) {
+    const int g = grid_for((count + 15) / 16, 256);
+    if (in_bf16) return launch_kernel(quantize_i8_kernel<__nv_bfloat16>, g, 256, 0, st, (const __nv_bfloat16 *)x, q, count, s, z);
+    return launch_kernel(quantize_i8_kernel<float>, g, 256, 0, st, (const float *)x, q, count, s, z);
 }
 
 unsigned int *device_status_word() {

@@ -333,6 +333,25 @@ CBS_API cbs_status cbs_maxpool2d(const void *x, void *y, int n, int c, int h, in
                                  int layout, int prec, void *stream);
 
 /*
+ * cbs_dequantize_i8, cbs_quantize_i8 -- the seams between INT8 layers and
+ * layers kept in float (page 3, "Edge optimisation of YOLO26", "Highlights":
+ * a layer-sensitivity analysis keeps some layers in float), in the affine
+ * scheme r = s (q - z) of the INT8 path:
+ *   dequantise: out[i] = (float)(q[i] - z) * s    (one IEEE multiply; BF16
+ *               output rounded to nearest even)
+ *   quantise:   q[i] = clamp(rne(x[i] / s) + z, -128, 127)   (IEEE division;
+ *               the quantiser of cbs_pack_input)
+ * count values, elementwise, any layout (NHWC activations whose channel
+ * counts are the same in both formats).  out_prec / in_prec: CBS_FP32 or
+ * CBS_TF32 (float), or CBS_BF16 (bfloat16).  s > 0, z in [-128, 127].
+ * Errors: CBS_ERR_INVALID_ARG, CBS_ERR_MISALIGNED (16-byte alignment).
+ */
+CBS_API cbs_status cbs_dequantize_i8(const int8_t *q, void *out, size_t count, float s, int z, int out_prec,
+                                     void *stream);
+CBS_API cbs_status cbs_quantize_i8(const void *x, int in_prec, int8_t *q, size_t count, float s, int z,
+                                   void *stream);
+
+/*
  * cbs_sppf_pool -- the SPPF block's three chained max pools in one launch
  * (page 1, "YOLO26N Inference Optimisation", kernel profile and "Op-by-op
  * impact": maxpool2d, three per frame, each a 5x5 stride-1 pool feeding the
