@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(256) stem_kernel(const StemLaunch a) {
 #pragma unroll
         for (int c = 0; c < COUT; ++c) {
             if (KIND == 2)
-                oq[c] = c < a.Cout ? requant_i8((int)((unsigned)__float2int_rn(accf[j][c]) + (unsigned)bias_i[c]),
+                oq[c] = c < a.Cout ? requant_i8_fast((int)((unsigned)__float2int_rn(accf[j][c]) + (unsigned)bias_i[c]),
                                                 mc[c], a.inv_s_y, a.zp_y)
                                    : 0;
             else
@@ -704,7 +704,7 @@ __global__ void __launch_bounds__(256) stem_tc_i8_kernel(const StemLaunch a, int
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
                 const int acc = (int)((unsigned)__float2int_rn(__uint_as_float(v[jj])) + (unsigned)sBias[c0 + jj]);
-                q[jj] = requant_i8(acc, sMc[c0 + jj], a.inv_s_y, a.zp_y);
+                q[jj] = requant_i8_fast(acc, sMc[c0 + jj], a.inv_s_y, a.zp_y);
             }
             if (OUT_NHWC && c0 + 8 <= a.Cout && (a.Cout & 7) == 0) {
                 uint32_t lo = 0u, hi = 0u;

@@ -91,6 +91,7 @@ struct TcParams {
     int a_box_bytes;           // one A box: 128 * mmul * RB
     int st_mode;               // 1: NHWC output staged in shared memory and written by TMA stores
     int cbw;                   // columns of one staged store block (128 bytes of output)
+    int nblk;                  // staged store blocks per tile row: ceil(BN / cbw)
     int stg_bytes_total;       // bytes of the staging region (8 warps x 4 KB) when st_mode
     int bias_smem;             // 1: the folded bias is copied to shared memory at start
     int bias_bytes_smem;       // bytes reserved for it
@@ -148,6 +149,22 @@ __device__ __forceinline__ float silu_precise(float z) { return __fdividef(z, 1.
 template <bool PRECISE = false>
 __device__ __forceinline__ float activate(const TcParams &p, float z) {
     return p.act == CBS_ACT_IDENTITY ? z : (PRECISE ? silu_precise(z) : silu_fast(z));
+}
+
+// o = act(v + b) for 16 accumulator values.
+template <bool PRECISE = false>
+__device__ __forceinline__ void activate16(const TcParams &p, const uint32_t (&v)[16], const float (&bv)[16],
+                                           float (&o)[16]) {
+    if (p.act == CBS_ACT_IDENTITY) {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) o[jj] = __uint_as_float(v[jj]) + bv[jj];
+    } else if (PRECISE) {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) o[jj] = silu_precise(__uint_as_float(v[jj]) + bv[jj]);
+    } else {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) o[jj] = silu_fast(__uint_as_float(v[jj]) + bv[jj]);
+    }
 }
 
 // Adds the residual of 16 consecutive channels nbase.. of one output element
@@ -208,8 +225,7 @@ template <int KIND>
 __device__ __forceinline__ void stage16(const TcParams &p, uint32_t blk, int row, int c, const float (&bv)[16],
                                         const uint32_t (&v)[16], int m, int nbase) {
     float o[16];
-#pragma unroll
-    for (int jj = 0; jj < 16; ++jj) o[jj] = activate(p, __uint_as_float(v[jj]) + bv[jj]);
+    activate16(p, v, bv, o);
     if (p.residual && m < p.M) add_residual16_nhwc<KIND>(p, m, nbase, o);
     const uint32_t rbase = blk + (uint32_t)row * 128u;
     if (KIND == kTF32) {
@@ -246,8 +262,7 @@ __device__ __forceinline__ void epi_store16(const TcParams &p, const float *bias
     const bool full = nbase + 16 <= p.C_out;
     load_bias16(p, bias, nbase, bv);
     float o[16];
-#pragma unroll
-    for (int jj = 0; jj < 16; ++jj) o[jj] = activate<PRECISE>(p, __uint_as_float(v[jj]) + bv[jj]);
+    activate16<PRECISE>(p, v, bv, o);
     if (p.residual) {
         if (p.out_nhwc) {
             add_residual16_nhwc<KIND>(p, m, nbase, o);
@@ -313,6 +328,11 @@ __device__ __forceinline__ void epi_store16(const TcParams &p, const float *bias
 // run at the same time share A rows through L2.  When the grid is a multiple
 // of n_tiles, every tile of a CTA has the same N tile (resident weights).
 __device__ __forceinline__ void tile_coords(int t, int n_tiles, int tile_m, int &m0, int &n0, int BN) {
+    if (n_tiles == 1) {   // most bandwidth-bound layers: no division per tile
+        m0 = t * tile_m;
+        n0 = 0;
+        return;
+    }
     const int mt = t / n_tiles;
     m0 = mt * tile_m;
     n0 = (t - mt * n_tiles) * BN;
@@ -450,9 +470,11 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // wait for the previous one before touching global memory.
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
-    if (p.bias_smem) {
-        for (int i = threadIdx.x; i < p.C_out; i += blockDim.x) bias_sm[i] = p.bias[i];
-        __syncthreads();
+    if (p.bias_smem && warp >= kEpiFirst) {
+        // Only the epilogue warps read the bias: they copy it and wait for
+        // one another (named barrier 1) while the producers already load.
+        for (int i = threadIdx.x - 32 * kEpiFirst; i < p.C_out; i += 32 * kEpiWarps) bias_sm[i] = p.bias[i];
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
     }
     const uint32_t tmem_base = *tmem_slot;
     const float *bias = p.bias_smem ? bias_sm : p.bias;
@@ -511,6 +533,15 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             for (int u = blockIdx.x; u < num_units && !aborted(abort_flag); u += gridDim.x) {
                 int t, st0, st1;
                 unit_range(u, p.split, nstage, t, st0, st1);
+                // Stages g .. g + (st1 - st0) - 1 belong to this unit: a unit
+                // none of whose stages is this warp's costs no address math
+                // (with one stage per tile, each producer owns every nprod-th tile).
+                int own = (warp - g) % p.nprod;
+                if (own < 0) own += p.nprod;
+                if (own >= st1 - st0) {
+                    g += st1 - st0;
+                    continue;
+                }
                 int m0, n0;
                 tile_coords(t, p.n_tiles, tile_m, m0, n0, p.BN);
                 int img, wc, hc;
@@ -679,7 +710,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // sub-tiles the two warps of a lane quadrant take one sub-tile each;
         // with one they take alternate 16-column groups.
         const int q = warp & 3;
-        const int h = (warp - kEpiFirst) >> 2;
+        const int widx = warp - kEpiFirst;
+        const int h = widx >> 2;
         const int sub = p.mmul == 2 ? h : 0;
         const int cstart = p.mmul == 2 ? 0 : 16 * h;
         const int cstep = p.mmul == 2 ? 16 : 32;
@@ -741,7 +773,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 __threadfence();
                 __syncwarp();
                 unsigned int prev = 0u;
-                unsigned int *counter = p.counters + (size_t)t * kSplitCounterSlots + (warp - kEpiFirst);
+                unsigned int *counter = p.counters + (size_t)t * kSplitCounterSlots + widx;
                 if (lane == 0) prev = atomicAdd(counter, 1u);
                 prev = __shfl_sync(0xffffffffu, prev, 0);
                 if (prev != (unsigned int)(p.split - 1)) continue;
@@ -773,7 +805,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 // store (coalesced, asynchronous; rows past M and columns
                 // past C_out are clipped by the tensor bounds).
                 const uint32_t blk = stg_base + (uint32_t)((warp - kEpiFirst) * kStageBlockBytes);
-                const int nblk = (p.BN + p.cbw - 1) / p.cbw;
+                const int nblk = p.nblk;
                 for (int b = p.mmul == 2 ? 0 : h; b < nblk; b += p.mmul == 2 ? 1 : 2) {
                     const int bc0 = b * p.cbw;
                     const int bcols = p.BN - bc0 < p.cbw ? p.BN - bc0 : p.cbw;
@@ -1005,6 +1037,14 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             for (int uu = blockIdx.x; uu < num_units && !aborted(abort_flag); uu += gridDim.x) {
                 int t, st0, st1;
                 unit_range(uu, p.split, nstage, t, st0, st1);
+                // Skip, without its address math, a unit none of whose stages
+                // g .. g + (st1 - st0) - 1 is this warp's.
+                int own = (warp - g) % p.nprod;
+                if (own < 0) own += p.nprod;
+                if (own >= st1 - st0) {
+                    g += st1 - st0;
+                    continue;
+                }
                 int m0, n0;
                 tile_coords(t, p.n_tiles, kBM, m0, n0, p.BN);
                 const int img = m0 / p.OHW;
@@ -1374,7 +1414,7 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     uint32_t qw[G / 4] = {};
 #pragma unroll
                     for (int jj = 0; jj < G; ++jj) {
-                        const int qv = requant_i8(accv[jj], mcv[jj], p.inv_s_y, p.zp_y);
+                        const int qv = requant_i8_fast(accv[jj], mcv[jj], p.inv_s_y, p.zp_y);
                         qw[jj >> 2] |= (uint32_t)(uint8_t)(int8_t)qv << (8 * (jj & 3));
                     }
                     if (p.out_nhwc) {
@@ -1995,6 +2035,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
         const bool tf32 = pl.variant == CBS_VARIANT_TC_TF32;
         P.st_mode = (P.win || P.split > 1) ? 0 : tc_store_mode(d, BN, pl.n_tiles, tf32);
         P.cbw = 128 / tc_out_bytes(tf32);
+        P.nblk = (P.BN + P.cbw - 1) / P.cbw;
         P.stg_bytes_total = P.st_mode ? kEpiWarps * kStageBlockBytes : 0;
         P.bias_bytes_smem = tc_bias_smem_bytes(d);
         P.bias_smem = P.bias_bytes_smem > 0;

@@ -13,11 +13,13 @@ from .oracle import (  # noqa: F401
     conv_bn_act_f32,
     maxpool2d_f32,
     spec_exp,
+    spec_exp_max_rel_err,
     quantize_act,
     dequantize_i8,
     round_bf16,
     fold_quant_i8,
     requant,
+    requant_array,
     conv_i8,
     num_threads,
     set_threads,

@@ -257,6 +257,30 @@ ORACLE_API void oracle_quantize_act_zp(const float *x, size_t count, float s_x, 
     }
 }
 
+/* Largest relative error of oracle_spec_exp against the double-precision
+ * exp over every float x in [lo, hi] (walked by bit pattern): the bound an
+ * error analysis of the INT8 epilogue may rely on. */
+ORACLE_API double oracle_spec_exp_max_rel_err(float lo, float hi)
+{
+    /* Floats in [lo, hi] in increasing order, mapped to a monotone integer key. */
+    uint32_t ulo, uhi;
+    memcpy(&ulo, &lo, 4);
+    memcpy(&uhi, &hi, 4);
+    const int64_t klo = (ulo & 0x80000000u) ? -(int64_t)(ulo & 0x7fffffffu) : (int64_t)ulo;
+    const int64_t khi = (uhi & 0x80000000u) ? -(int64_t)(uhi & 0x7fffffffu) : (int64_t)uhi;
+    double worst = 0.0;
+#pragma omp parallel for reduction(max : worst) schedule(static)
+    for (int64_t k = klo; k <= khi; ++k) {
+        const uint32_t u = k < 0 ? (0x80000000u | (uint32_t)(-k)) : (uint32_t)k;
+        float x;
+        memcpy(&x, &u, 4);
+        const double ref = exp((double)x);
+        const double err = fabs((double)oracle_spec_exp(x) - ref) / ref;
+        if (err > worst) worst = err;
+    }
+    return worst;
+}
+
 /* Dequantisation at a seam between an INT8 layer and a layer kept in float
  * ("Edge optimisation of YOLO26", Highlights: sensitive layers are kept in
  * float; the affine scheme r = s (q - z) of Jacob et al., CVPR 2018):
@@ -355,6 +379,14 @@ ORACLE_API int8_t oracle_requant_zp(int32_t acc, float m_c, float inv_s_y, int z
     float v = rne(u * inv_s_y) + (float)z_y;
     v = v < -128.0f ? -128.0f : (v > 127.0f ? 127.0f : v);
     return (int8_t)v;
+}
+
+/* oracle_requant_zp over arrays of accumulators and scales (one output each). */
+ORACLE_API void oracle_requant_zp_array(const int32_t *acc, const float *m_c, size_t count, float inv_s_y, int z_y,
+                                        int8_t *q)
+{
+#pragma omp parallel for
+    for (size_t i = 0; i < count; ++i) q[i] = oracle_requant_zp(acc[i], m_c[i], inv_s_y, z_y);
 }
 
 /* INT8 layer: integer convolution (int64 accumulation; the sum must fit in

@@ -53,6 +53,9 @@ def _load():
         lib.oracle_conv_i8_zp.restype = I
         lib.oracle_dequantize_i8.argtypes = [P, Z, F, I, P]
         lib.oracle_round_bf16.argtypes = [P, Z, P]
+        lib.oracle_requant_zp_array.argtypes = [P, P, Z, F, I, P]
+        lib.oracle_spec_exp_max_rel_err.argtypes = [F, F]
+        lib.oracle_spec_exp_max_rel_err.restype = ctypes.c_double
         _lib = lib
     return _lib
 
@@ -163,6 +166,11 @@ def spec_exp(x) -> np.ndarray:
     return y
 
 
+def spec_exp_max_rel_err(lo: float, hi: float) -> float:
+    """Largest relative error of spec_exp against double exp over every float in [lo, hi]."""
+    return float(_load().oracle_spec_exp_max_rel_err(float(lo), float(hi)))
+
+
 def quantize_act(x, s_x: float, z_x: int = 0) -> np.ndarray:
     """q = clamp(rne(x / s_x), -128, 127); with a zero point z_x (asymmetric
     activations), q = clamp(rne(x / s_x) + z_x, -128, 127)."""
@@ -209,6 +217,16 @@ def requant(acc: int, m_c: float, inv_s_y: float, z_y: int = 0) -> int:
     if z_y:
         return int(_load().oracle_requant_zp(int(acc), float(m_c), float(inv_s_y), int(z_y)))
     return int(_load().oracle_requant(int(acc), float(m_c), float(inv_s_y)))
+
+
+def requant_array(acc, m_c, inv_s_y: float, z_y: int = 0) -> np.ndarray:
+    """requant of every (acc[i], m_c[i]) with one inv_s_y and output zero point."""
+    acc = np.ascontiguousarray(acc, np.int32)
+    m_c = _f32(m_c)
+    assert acc.shape == m_c.shape
+    q = np.empty(acc.shape, np.int8)
+    _load().oracle_requant_zp_array(_ptr(acc), _ptr(m_c), acc.size, float(inv_s_y), int(z_y), _ptr(q))
+    return q
 
 
 def conv_i8(q_x, q_w, bias_i32, m_c, s_y: float, stride: int, pad: int, return_acc: bool = False,
