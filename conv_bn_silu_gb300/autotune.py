@@ -3,7 +3,7 @@ that `tuning.tuned_desc` reads.
 
 For every distinct layer shape of the benchmark workloads (the twelve-layer
 list at batch 16 in BF16, TF32 and INT8, the 40-layer chain at batch 16 in
-BF16 and TF32, both at batch 1 in FP32, and the list at batches 1 and 16 in
+BF16, TF32 and INT8, both at batch 1 in FP32, and the list at batches 1 and 16 in
 FP32 with NHWC activations on the 3xTF32 kernel), each candidate configuration is
 planned, folded and timed as a CUDA graph of repeated launches over rotating
 input copies.  A shape gets a table entry when its fastest candidate beats the
@@ -36,7 +36,7 @@ def workload_shapes():
     chain = [cl.spec for cl in wl.chain_layers()]
     for prec in ("bf16", "tf32", "int8"):
         out += [(prec, 16, s, B.CBS_NHWC) for s in wl.LAYER_LIST]
-    for prec in ("bf16", "tf32"):
+    for prec in ("bf16", "tf32", "int8"):
         out += [(prec, 16, s, B.CBS_NHWC) for s in chain]
     out += [("fp32", 1, s, B.CBS_NCHW) for s in list(wl.LAYER_LIST) + chain + [wl.SINGLE_LAYER]]
     # FP32 with NHWC activations: the 3xTF32 tensor-core kernel
