@@ -4,7 +4,8 @@ layers a sensitivity analysis marks kept in float), against the oracle.
 
 - Seams: cbs_dequantize_i8 and cbs_quantize_i8 bit for bit against the
   oracle's dequantiser (with its bfloat16 rounding) and quantiser.
-- Teacher-forced chain: the oracle runs the whole chain (INT8 layers on
+- Teacher-forced chain (batch 16 all-INT8; batch 4 with layers kept in
+  float): the oracle runs the whole chain (INT8 layers on
   codes; layers kept in float on the bfloat16-rounded dequantised input,
   their output rounded to bfloat16 and quantised with the calibrated scale
   for the next INT8 layer).  Each GPU layer is fed the oracle's input for it:
@@ -104,9 +105,10 @@ def to_device_nhwc(a, dtype, channels):
     return t.contiguous().cuda()
 
 
-@pytest.mark.parametrize("keep_float", [(), (0, 11, 20, 39)])
-def test_int8_chain_teacher_forced(cuda_lib, keep_float):
-    n = 2
+@pytest.mark.parametrize("keep_float,n", [((), 16), ((0, 11, 20, 39), 4)])
+def test_int8_chain_teacher_forced(cuda_lib, keep_float, n):
+    """All INT8 at batch 16 (every image checked), and with four layers kept
+    in BF16 at batch 4."""
     chain = Chain("int8", n, out_scales=SCALES["chain"], keep_float=keep_float)
     assert chain.in_scale == np.float32(SCALES["input_scale"])
     frame = wl.frame(n)
