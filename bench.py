@@ -144,7 +144,7 @@ EXTRA_DEFAULT = ("layer_list_bf16_n16", "layer_list_tf32_n16", "layer_list_int8_
 TRAFFIC = {
     "layer_list_fp32_n1": {"kernel": "simt_conv_kernel", "launches": 11, "bytes": 28470784,
                            "sources": ("k_simt.cu", "cbs_internal.cuh", "../tuned_plans.json"),
-                           "digest": "41996aa4e4712878",
+                           "digest": "951e3c2c8486827e",
                            "profile": "profiles/launches_layer_list_fp32_n1.md"},
 }
 # Variant of the dominant kernel per precision (the direct small-channel
@@ -157,10 +157,20 @@ X3_VARIANT = 5
 
 
 def sources_digest(files) -> str:
+    """Hash of the kernel sources and, for the measured plan table, of its
+    entries that pick CUDA-core tiles (force_variant 0): the tensor-core
+    entries do not change the CUDA-core kernel's traffic."""
     import hashlib
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "conv_bn_silu_gb300", "csrc", f), "rb") as fh:
+        path = os.path.join(ROOT, "conv_bn_silu_gb300", "csrc", f)
+        if f.endswith("tuned_plans.json"):
+            with open(path) as fh:
+                plans = json.load(fh).get("plans", {})
+            simt = {k: v for k, v in plans.items() if v.get("force", {}).get("force_variant") == 0}
+            h.update(json.dumps(simt, sort_keys=True).encode())
+            continue
+        with open(path, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 

@@ -47,10 +47,11 @@ namespace {
 
 constexpr int kBM = 128;                         // rows of one MMA (one TMEM lane per pixel)
 constexpr int kMaxProducers = 4;                 // warps 0..3
-constexpr int kMmaWarp = kMaxProducers;          // warp 4: TMEM + MMA issuer
-constexpr int kEpiFirst = kMmaWarp + 1;          // warps 5..12: epilogue
+constexpr int kMmaWarp = kMaxProducers;          // warp 4: TMEM, and the MMA issuer of sub-tile 0
+constexpr int kMmaWarps = 2;                     // warps 4, 5: one MMA issuer per 128-pixel sub-tile
+constexpr int kEpiFirst = kMmaWarp + kMmaWarps;  // warps 6..13: epilogue
 constexpr int kEpiWarps = 8;                     // two per TMEM lane quadrant
-constexpr int kThreads = 32 * (kEpiFirst + kEpiWarps);        // TF32/BF16: 416
+constexpr int kThreads = 32 * (kEpiFirst + kEpiWarps);        // TF32/BF16: 448
 constexpr int kMaxProducersI8 = 2;               // INT8: warps 0..1
 constexpr int kMmaWarpI8 = kMaxProducersI8;      // warp 2
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
@@ -437,20 +438,26 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int num_units = num_tiles * p.split;    // split-K: (tile, K part) units
     const int b_step_bytes = p.BN * p.RB;         // bytes of one B tile as loaded
 
+    // Each 128-pixel sub-tile has its own MMA-issuing thread (lane 0 of warp
+    // kMmaWarp + sub-tile): a thread that waits on a barrier once per stage
+    // issues an MMA only every ~110-160 cycles, against 48-65 cycles of
+    // tensor-pipe time for N <= 128, and two issuers overlap their waits.
+    // Every barrier the MMAs release counts one commit per issuer.
+    const uint32_t n_iss = (uint32_t)p.mmul;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(full_bar(s), 1);
-            ptx::mbar_init(empty_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), n_iss);
         }
         for (int a = 0; a < 2; ++a) {
-            ptx::mbar_init(accf_bar(a), 1);
+            ptx::mbar_init(accf_bar(a), n_iss);
             ptx::mbar_init(acce_bar(a), kEpiWarps);   // one arrive per epilogue warp
         }
-        ptx::mbar_init(drain_bar, 1);
+        ptx::mbar_init(drain_bar, n_iss);
         ptx::mbar_init(bfull_bar, 1);                 // producer warp 0 loads the resident weights
         for (int b = 0; b < p.SB; ++b) {
             ptx::mbar_init(wfull_bar(b), 1);
-            ptx::mbar_init(wempty_bar(b), 1);
+            ptx::mbar_init(wempty_bar(b), n_iss);
         }
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -610,8 +617,9 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if (!ok) break;
             }
         }
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) {
+    } else if (warp < kMmaWarp + kMmaWarps) {
+        const int mi = warp - kMmaWarp;   // the sub-tile whose MMAs this warp issues
+        if (lane == 0 && mi < p.mmul) {
             const uint32_t sbo = 8u * p.RB;
             const int kslices = p.RB / 32;
             const uint32_t sub_bytes = (uint32_t)(kBM * p.RB);   // one 128-row sub-tile of an A box
@@ -631,7 +639,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_stride);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_stride + mi * p.bnp);
                 if (p.win) {
                     // Row of the window that holds the tile's first position.
                     const int mt = t / p.n_tiles;
@@ -665,9 +673,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             // A view starting at any 128-byte row: the descriptor's
                             // start address alone places it (absolute swizzle).
                             const uint32_t a0 = window + (uint32_t)(row0 + r * p.Wp + c) * p.RB;
-                            for (int mi = 0; mi < p.mmul; ++mi)
-                                issue_kstep<KIND>(d_tmem + (uint32_t)(mi * p.bnp), dhi, a0 + mi * sub_bytes, b_addr, p.idesc,
-                                                  kslices, cb == 0 && tap == 0);
+                            issue_kstep<KIND>(d_tmem, dhi, a0 + mi * sub_bytes, b_addr, p.idesc, kslices,
+                                              cb == 0 && tap == 0);
                             if (!p.b_res) {
                                 ptx::mma_commit(wempty_bar(ws));   // weight slot free once these MMAs are done
                                 ++gw;
@@ -694,9 +701,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         const uint32_t a_addr = sbase + kk * p.a_box_bytes;
                         const uint32_t b_addr = p.b_res ? b_base + i * p.b_tile_stride
                                                         : sbase + p.kg * p.a_box_bytes + kk * p.b_tile_stride;
-                        for (int mi = 0; mi < p.mmul; ++mi)
-                            issue_kstep<KIND>(d_tmem + (uint32_t)(mi * p.bnp), dhi, a_addr + mi * sub_bytes, b_addr, p.idesc,
-                                              kslices, i == st0 * p.kg);
+                        issue_kstep<KIND>(d_tmem, dhi, a_addr + mi * sub_bytes, b_addr, p.idesc, kslices,
+                                          i == st0 * p.kg);
                     }
                     ptx::mma_commit(empty_bar(s));
                 }
@@ -1546,14 +1552,24 @@ int tc_producers(int stages) {
 // GB300 costs the planner works from (SM cycles, measured with single-SM
 // probes): a warp issuing TMA copies gets one box through every ~570 cycles
 // whatever its size, and all SMs loading at once fill from L2 at ~70 B/cycle
-// each; an MMA with fresh operands costs ~95 cycles for N <= 128 (a commit
-// per stage included) and N/2 beyond (TF32: twice that), and the issuing
-// thread loses ~270 cycles per stage barrier it waits on.
+// each.  An issuing thread that waits on a stage barrier gets one MMA out
+// every ~95 cycles and loses ~270 cycles per wait; the tensor pipe itself
+// takes 48 cycles per M=128, K=16 bf16 MMA up to N=64 and N/2 beyond (TF32:
+// twice that).  Each 128-pixel sub-tile has its own issuing thread, so the
+// MMA time of a tile is the larger of one issuer's time and the pipe time
+// of all its sub-tiles.
 constexpr double kClkPerBox = 570.0, kFillBytesPerClk = 70.0, kClkPerStageWait = 270.0;
+constexpr double kClkPerMmaIssue = 95.0;
 
-double tc_mma_clk(int N, bool tf32) {
+double tc_pipe_clk(int N, bool tf32) {
     const double c = tf32 ? (double)N : 0.5 * N;
-    return c > 95.0 ? c : 95.0;
+    return c > 48.0 ? c : 48.0;
+}
+
+double tc_tile_mma_clk(double n_mma, double waits, int mmul, int N, bool tf32) {
+    const double issue = n_mma * kClkPerMmaIssue + waits * kClkPerStageWait;
+    const double pipe = n_mma * mmul * tc_pipe_clk(N, tf32);
+    return issue > pipe ? issue : pipe;
 }
 
 // Output bytes per element of a TF32/BF16 layer (float or bfloat16).
@@ -1638,8 +1654,8 @@ bool tc_config_window(const cbs_layer_desc &d, int oh, int RB, int ksteps, bool 
     }
     const double tpc = (double)((tiles + c.grid - 1) / c.grid);
     const int kslices = RB / 32;
-    const double mma = tpc * ((double)ksteps * kslices * c.mmul * tc_mma_clk(c.BN, tf32) +
-                              (double)cblocks * kClkPerStageWait + (c.b_res ? 0.0 : (double)ksteps * 100.0));
+    const double mma = tpc * (tc_tile_mma_clk((double)ksteps * kslices, (double)cblocks, c.mmul, c.BN, tf32) +
+                              (c.b_res ? 0.0 : (double)ksteps * 100.0));
     const double boxes = tpc * cblocks + (c.b_res ? (double)ksteps : tpc * ksteps);
     const double bytes = tpc * cblocks * (double)c.a_box_bytes + (c.b_res ? (double)ksteps : tpc * ksteps) * b_bytes;
     const double t_box = boxes * 140.0, t_fill = bytes / kFillBytesPerClk;
@@ -1685,7 +1701,7 @@ bool tc_config(const cbs_layer_desc &d, long long M, int oh, int RB, int ksteps,
     }
     const double tpc = (double)((tiles + c.grid - 1) / c.grid);   // tiles of the busiest CTA
     const int kslices = RB / 32;
-    const double mma = tpc * ((double)ksteps * kslices * mmul * tc_mma_clk(BN, tf32) + (double)(ksteps / kg) * kClkPerStageWait);
+    const double mma = tpc * tc_tile_mma_clk((double)ksteps * kslices, (double)(ksteps / kg), mmul, BN, tf32);
     const double boxes = tpc * ksteps * (b_res ? 1.0 : 2.0) + (b_res ? (double)ksteps : 0.0);
     const double bytes = tpc * ksteps * (double)(c.a_box_bytes + (b_res ? 0 : b_bytes)) + (b_res ? (double)ksteps * b_bytes : 0.0);
     // Boxes of one stage go out from parallel lanes; the SM's TMA engine
