@@ -331,6 +331,12 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
         p.grid_ctas = tc ? std::min(p.m_tiles, plan_sms(D) * stem_tc_ctas_per_sm(D.c_out, tc_kind == 3)) : p.m_tiles;
         p.threads = 256;
         p.smem_bytes = tc ? (tc_kind == 3 ? kStemTf32SmemBytes : kStemTcSmemBytes) : D.k * D.k * p.c_in_pad * cout_t * 4;
+        if (tc && stem_s2_kernel_applies(tc_kind, D.k, D.stride, D.pad, D.w, D.c_out, D.out_layout == CBS_NHWC,
+                                         D.residual != 0)) {
+            // two tiles per step on the stem's own kernel
+            p.grid_ctas = std::min((p.m_tiles + 1) / 2, plan_sms(D) * kStemS2CtasPerSm);
+            p.smem_bytes = kStemS2SmemBytes;
+        }
         p.workspace_bytes = 0;
     } else if (variant == CBS_VARIANT_SIMT_FP32) {
         plan_simt(p);

@@ -157,6 +157,17 @@ inline int stem_tc_ctas_per_sm(int cout, int tf32 = 0) {
 }
 // A ring + B (64 rows x 128 B) + bias + two mbarriers + TMEM slot + 1 KB for alignment
 constexpr int kStemTcSmemBytes = kStemTcStages * 16384 + 8192 + 64 * 4 + 16 + 16 + 1024;
+// The 640x640-class BF16 stem (3x3, stride 2, pad 1, even input width, 16
+// output channels, NHWC output, no residual) runs a kernel of its own: two
+// 128-pixel tiles per step, one thread per output pixel, a ring of
+// kStemS2Stages pairs of A tiles, kStemS2CtasPerSm CTAs per SM.
+inline bool stem_s2_kernel_applies(int kind, int ks, int stride, int pad, int w, int cout, int out_nhwc,
+                                   bool residual) {
+    return kind == 1 && ks == 3 && stride == 2 && pad == 1 && (w & 1) == 0 && cout == 16 && out_nhwc && !residual;
+}
+constexpr int kStemS2Stages = 4, kStemS2CtasPerSm = 2;
+// A ring (24 KB per pair) + B panels (2 KB) + bias + two mbarriers + TMEM slot + 1 KB for alignment
+constexpr int kStemS2SmemBytes = kStemS2Stages * 24576 + 2048 + 16 * 4 + 16 + 16 + 1024;
 constexpr int kStemMaxCin = 4, kStemMaxCout = 64, kStemMaxK = 7;
 
 // ---------------------------------------------------------------- misc kernels

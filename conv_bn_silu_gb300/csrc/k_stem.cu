@@ -554,6 +554,203 @@ __global__ void __launch_bounds__(256) stem_tc_bf16_kernel(const StemLaunch a, i
     }
 }
 
+// The detector's BF16 stem on its own kernel: 3x3, stride 2, pad 1 over
+// 4-channel NHWC pixels of even input width, 16 output channels, NHWC output,
+// no residual.  The general kernel above splits each output pixel over two
+// threads, which both re-derive its position, and takes one 128-pixel tile
+// per block-wide barrier.  Here each step takes two tiles (256 pixels, one
+// per thread: warps 0-3 the first tile, 4-7 the second, TMEM lane t % 128),
+// and a thread gathers its pixel's three kernel rows (two 16-byte pixel pairs
+// each, the K layout of the general kernel's pair form) and stores all 16 of
+// its output channels as two 16-byte vectors.  A row's 96 bytes of K sit in
+// two panels with no padding (K 0..31 in a 64-byte-swizzled panel, K 32..47
+// in a 32-byte-swizzled one), so a ring of kStemS2Stages pairs keeps several
+// pairs of loads in flight per CTA.
+constexpr int kS2Tile = 12288, kS2Pair = 2 * kS2Tile, kS2Panel1 = 8192;
+
+// Shared-memory offset of 16-byte K chunk q (0..5) of row r of a tile laid
+// out as above (the swizzles act on address bits, so the tile is 1024-byte
+// aligned).
+__device__ __forceinline__ uint32_t s2_chunk(int r, int q) {
+    return q < 4 ? (uint32_t)(r * 64 + ((q ^ ((r >> 1) & 3)) << 4))
+                 : (uint32_t)(kS2Panel1 + r * 32 + (((q - 4) ^ ((r >> 2) & 1)) << 4));
+}
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+template <bool SILU>
+__global__ void __launch_bounds__(256) stem_tc_bf16_s2_kernel(const StemLaunch a, StemTcGeom g,
+                                                              unsigned int *status) {
+    constexpr int S = kStemS2Stages;
+    extern __shared__ uint8_t stem_smem_raw[];
+    const uint32_t raw = ptx::smem_u32(stem_smem_raw);
+    uint8_t *base = stem_smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t *sA = base;                                           // S pairs x 2 tiles x 12 KB
+    uint8_t *sB = base + S * kS2Pair;                             // panels of 16 rows: 1 KB, then 512 B
+    float *sBias = reinterpret_cast<float *>(sB + 2048);          // 16, halved (tanh form of SiLU)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sBias + 16);    // 2
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
+
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int sub = t >> 7, row = t & 127;
+    if (warp == 0) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 64);   // two buffers x two tiles x 16 columns
+        ptx::tmem_relinquish();
+    }
+    if (t == 0) {
+        ptx::mbar_init(ptx::smem_u32(&bars[0]), 1);
+        ptx::mbar_init(ptx::smem_u32(&bars[1]), 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
+    // B row co: output channel co's weights in the pair K layout.  Chunk 2r:
+    // (0, tap (r, 0)) -- its first pixel is unused; chunk 2r + 1: taps
+    // (r, 1), (r, 2).  The B tile has A's two panels: 16 rows of 64 bytes
+    // at sB, 16 rows of 32 bytes at sB + 1 KB.
+    if (t < 96) {
+        const int co = t / 6, q = t - co * 6;
+        const uint2 *wr = static_cast<const uint2 *>(a.w) + co * 9;   // [16][9] taps of 4 bf16
+        uint2 lo = make_uint2(0u, 0u), hi = make_uint2(0u, 0u);
+        const int r = q >> 1;
+        if ((q & 1) == 0) {
+            hi = wr[3 * r];
+        } else {
+            lo = wr[3 * r + 1];
+            hi = wr[3 * r + 2];
+        }
+        const uint32_t off = q < 4 ? (uint32_t)(co * 64 + ((q ^ ((co >> 1) & 3)) << 4))
+                                   : (uint32_t)(1024 + co * 32 + (((q - 4) ^ ((co >> 2) & 1)) << 4));
+        *reinterpret_cast<uint4 *>(sB + off) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+    if (t < 16) sBias[t] = 0.5f * static_cast<const float *>(a.bias)[t];
+
+    const int n_pairs = (g.n_tiles + 1) >> 1;
+    const int n_local = (int)blockIdx.x < n_pairs ? (n_pairs - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int ohw = a.OH * a.OW;
+    const uint8_t *xb = static_cast<const uint8_t *>(a.x);
+    const long long row_bytes = (long long)a.W * 8;
+    const uint32_t sA_u32 = ptx::smem_u32(sA);
+    const uint32_t my_tile = (uint32_t)(sub * kS2Tile);
+
+    // Issue this thread's copies of local pair i into stage i % S (an empty
+    // group past the last pair).
+    auto gather = [&](int i) {
+        if (i < n_local) {
+            const int pix = (((int)blockIdx.x + i * (int)gridDim.x) * 2 + sub) * 128 + row;
+            const bool valid = pix < g.total;
+            const int img = fast_div(pix, g.div_ohw);
+            const int rem = pix - img * ohw;
+            const int oh = fast_div(rem, g.div_ow);
+            const int ow = rem - oh * a.OW;
+            const int ih0 = 2 * oh - 1;
+            // Byte offset of the pixel pair at input column 2 ow - 2 of row ih0
+            // (16-byte aligned: W and 2 ow - 2 are even); read only in bounds.
+            const long long off0 = (((long long)img * a.H + ih0) * a.W + 2 * ow - 2) * 8;
+            const uint32_t dst = sA_u32 + (uint32_t)((i % S) * kS2Pair) + my_tile;
+#pragma unroll
+            for (int r = 0; r < 3; ++r) {
+                const bool rin = valid && (unsigned)(ih0 + r) < (unsigned)a.H;
+                const bool lin = rin && ow > 0;
+                const long long off = off0 + r * row_bytes;
+                ptx::cp_async_16(dst + s2_chunk(row, 2 * r), lin ? (const void *)(xb + off) : a.x, lin ? 16u : 0u);
+                ptx::cp_async_16(dst + s2_chunk(row, 2 * r + 1), rin ? (const void *)(xb + off + 16) : a.x,
+                                 rin ? 16u : 0u);
+            }
+        }
+        ptx::cp_async_commit();
+    };
+
+#pragma unroll 1
+    for (int i = 0; i < S - 1; ++i) gather(i);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    float bh[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) bh[c] = sBias[c];
+    // Panel 0: 64-byte rows, 64-byte swizzle (8-row groups 512 B apart);
+    // panel 1: 32-byte rows, 32-byte swizzle (256 B apart).
+    const uint64_t d64 = ptx::smem_desc(0u, 16u, 512u, 4u), d32 = ptx::smem_desc(0u, 16u, 256u, 6u);
+    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(16 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    const uint32_t sB_u32 = ptx::smem_u32(sB);
+    const uint64_t bd0 = d64 | (uint64_t)((sB_u32 & 0x3FFFFu) >> 4);
+    const uint64_t bd1 = d32 | (uint64_t)(((sB_u32 + 1024u) & 0x3FFFFu) >> 4);
+    const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(sub * 16);
+    __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(a.y);
+    bool failed = false;
+#pragma unroll 1
+    for (int i = 0; i <= n_local; ++i) {
+        if (i < n_local) {
+            ptx::cp_async_wait<S - 2>();   // this thread's copies of pair i have landed
+            // Zero the unused first pixel of each kernel row's first pair.
+            uint8_t *tp = sA + (i % S) * kS2Pair + my_tile;
+#pragma unroll
+            for (int r = 0; r < 3; ++r) *reinterpret_cast<uint2 *>(tp + s2_chunk(row, 2 * r)) = make_uint2(0u, 0u);
+            ptx::fence_proxy_async_smem();
+        }
+        ptx::tc_fence_before();
+        if (__syncthreads_or(failed)) break;
+        ptx::tc_fence_after();
+        if (i < n_local && t == 0) {
+#pragma unroll
+            for (int sb = 0; sb < 2; ++sb) {
+                const uint32_t ta = sA_u32 + (uint32_t)((i % S) * kS2Pair + sb * kS2Tile);
+                const uint64_t a0 = d64 | (uint64_t)((ta & 0x3FFFFu) >> 4);
+                const uint64_t a1 = d32 | (uint64_t)(((ta + (uint32_t)kS2Panel1) & 0x3FFFFu) >> 4);
+                const uint32_t acc = tmem + (uint32_t)((i & 1) * 32 + sb * 16);
+                ptx::mma_f16(acc, a0, bd0, idesc, 0u);             // K 0..15
+                ptx::mma_f16(acc, a0 + 2u, bd0 + 2u, idesc, 1u);   // K 16..31: 32 bytes on
+                ptx::mma_f16(acc, a1, bd1, idesc, 1u);             // K 32..47
+            }
+            ptx::mma_commit(ptx::smem_u32(&bars[i & 1]));
+        }
+        if (i == 0) {
+            gather(S - 1);
+            continue;
+        }
+        const int j = i - 1;
+        bool ok = ptx::mbar_wait_bounded(ptx::smem_u32(&bars[j & 1]), (uint32_t)((j >> 1) & 1), kStemWaitNs);
+        ok = __all_sync(0xffffffffu, ok);   // warp-uniform before .sync.aligned loads
+        if (!ok) {
+            failed = true;
+            if (lane == 0) atomicOr(status, 1u);
+            continue;
+        }
+        ptx::tc_fence_after();
+        // Pair j's MMAs have completed: its stage takes pair j + S.
+        gather(j + S);
+        uint32_t v[16];
+        ptx::tmem_ld16(t_lane + (uint32_t)((j & 1) * 32), v);
+        ptx::tmem_ld_wait();
+        const int pix = (((int)blockIdx.x + j * (int)gridDim.x) * 2 + sub) * 128 + row;
+        if (pix < g.total) {
+            uint32_t o[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float h0 = fmaf(__uint_as_float(v[2 * c]), 0.5f, bh[2 * c]);
+                const float h1 = fmaf(__uint_as_float(v[2 * c + 1]), 0.5f, bh[2 * c + 1]);
+                o[c] = SILU ? cvt_bf16x2(silu_tanh(h0), silu_tanh(h1)) : cvt_bf16x2(h0 + h0, h1 + h1);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(y + (size_t)pix * 16);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+    }
+    ptx::cp_async_wait<0>();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 64);
+    }
+}
+
 // INT8 codes widened to bfloat16 (exact for |q| <= 128: the float has at most
 // 8 significant bits, so its top 16 bits are the bfloat16).
 __device__ __forceinline__ uint32_t codes_to_bf16x2(int lo, int hi) {
@@ -1002,6 +1199,13 @@ cudaError_t launch_stem_tc(const StemLaunch &L, cudaStream_t s) {
     g.n_tiles = (int)((total + 127) / 128);
     g.div_ohw = make_fastdiv((uint32_t)(L.OH * L.OW));
     g.div_ow = make_fastdiv((uint32_t)L.OW);
+    if (stem_s2_kernel_applies(L.kind, L.KS, L.stride, L.pad, L.W, L.Cout, L.out_nhwc, L.residual != nullptr)) {
+        const int grid = std::min((g.n_tiles + 1) / 2, L.grid);   // the plan's persistent CTAs
+        auto kern = L.act != CBS_ACT_IDENTITY ? stem_tc_bf16_s2_kernel<true> : stem_tc_bf16_s2_kernel<false>;
+        const cudaError_t e = set_max_dyn_smem(kern, kStemS2SmemBytes);
+        if (e != cudaSuccess) return e;
+        return launch_kernel(kern, grid, 256, kStemS2SmemBytes, s, L, g, status);
+    }
     const int grid = std::min(g.n_tiles, L.grid);   // the plan's persistent CTAs
     const int n_mma = (L.Cout + 15) / 16 * 16;
     if (L.tf32)
