@@ -333,9 +333,10 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
         p.smem_bytes = tc ? (tc_kind == 3 ? kStemTf32SmemBytes : kStemTcSmemBytes) : D.k * D.k * p.c_in_pad * cout_t * 4;
         if (tc && stem_s2_kernel_applies(tc_kind, D.k, D.stride, D.pad, D.w, D.c_out, D.out_layout == CBS_NHWC,
                                          D.residual != 0)) {
-            // two tiles per step on the stem's own kernel
-            p.grid_ctas = std::min((p.m_tiles + 1) / 2, plan_sms(D) * kStemS2CtasPerSm);
-            p.smem_bytes = kStemS2SmemBytes;
+            // the stem's own kernel: one band of output rows per CTA
+            p.grid_ctas = std::min(D.n * p.oh, plan_sms(D) * kStemRowsCtasPerSm);
+            p.smem_bytes = stem_rows_smem_bytes(D.w);
+            p.threads = kStemRowsThreads;
         }
         p.workspace_bytes = 0;
     } else if (variant == CBS_VARIANT_SIMT_FP32) {

@@ -554,168 +554,190 @@ __global__ void __launch_bounds__(256) stem_tc_bf16_kernel(const StemLaunch a, i
     }
 }
 
-// The detector's BF16 stem on its own kernel: 3x3, stride 2, pad 1 over
-// 4-channel NHWC pixels of even input width, 16 output channels, NHWC output,
-// no residual.  The general kernel above splits each output pixel over two
-// threads, which both re-derive its position, and takes one 128-pixel tile
-// per block-wide barrier.  Here each step takes two tiles (256 pixels, one
-// per thread: warps 0-3 the first tile, 4-7 the second, TMEM lane t % 128),
-// and a thread gathers its pixel's three kernel rows (two 16-byte pixel pairs
-// each, the K layout of the general kernel's pair form) and stores all 16 of
-// its output channels as two 16-byte vectors.  A row's 96 bytes of K sit in
-// two panels with no padding (K 0..31 in a 64-byte-swizzled panel, K 32..47
-// in a 32-byte-swizzled one), so a ring of kStemS2Stages pairs keeps several
-// pairs of loads in flight per CTA.
-constexpr int kS2Tile = 12288, kS2Pair = 2 * kS2Tile, kS2Panel1 = 8192;
-
-// Shared-memory offset of 16-byte K chunk q (0..5) of row r of a tile laid
-// out as above (the swizzles act on address bits, so the tile is 1024-byte
-// aligned).
-__device__ __forceinline__ uint32_t s2_chunk(int r, int q) {
-    return q < 4 ? (uint32_t)(r * 64 + ((q ^ ((r >> 1) & 3)) << 4))
-                 : (uint32_t)(kS2Panel1 + r * 32 + (((q - 4) ^ ((r >> 2) & 1)) << 4));
-}
+// The detector's BF16 stem on a kernel of its own: 3x3, stride 2, pad 1 over
+// 4-channel NHWC pixels of even input width W, 16 output channels, NHWC
+// output, no residual.  The general kernel above gathers every output
+// pixel's window from L2 (96 bytes per pixel, three times the input); this
+// one walks whole output rows.  Each CTA takes a band of consecutive output
+// rows (n, oh); one TMA box brings each input row into shared memory once
+// (zero-filled above and below the image), and the CTA rewrites it as the
+// rows of the MMA's A operand: for output column k, 32 bytes = the pixel
+// pair (2k-2, 2k-1) with its first pixel zeroed, then the pair (2k, 2k+1)
+// (the pair K layout of the general kernel; the zeroed pixel's weights are
+// zero, and zeroing it keeps a non-finite neighbour out of the sum).  That
+// rewrite is stored 32-byte swizzled, so output row oh is, per kernel row r,
+// ceil(OW / 128) M=128 MMAs whose A is a 128-row slice of input row
+// 2 oh - 1 + r's rewrite.  Input row 2 oh + 1 is also row 2 (oh + 1) - 1:
+// each input row is loaded and rewritten once per band.
+//
+// Per step (one output row): warps 0-7 rewrite the step's new input rows
+// (loaded kStemRowsAhead steps earlier); barrier; warp 8 issues the MMAs
+// into accumulator buffer step % 2 and the input loads of step +
+// kStemRowsAhead, while warps 0-7 wait for the previous step's MMAs and run
+// its epilogue.  The issuing thread never waits on a barrier with its MMAs
+// in flight (such a wait stalls it for ~700 cycles on GB300).  Rewrites go to a ring of kStemRowsESlots slots: step s writes
+// slots 2s, 2s+1 (mod 6) and its MMAs read 2s-1 .. 2s+1, so a slot is
+// rewritten only after the MMAs of steps s-2 and s-3 -- both waited for --
+// have read it.
 __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
 
+struct StemRowsGeom {
+    int rows;        // output rows N * OH
+    int mtiles;      // M=128 tiles per output row: ceil(OW / 128)
+    int eslot;       // bytes of one rewritten input row: mtiles * 4096
+    int raw;         // bytes of one input row: W * 8
+    int rawstride;   // bytes between raw row slots: raw rounded up to 256 (B stays swizzle-aligned)
+};
+
+// Offset of 16-byte chunk c (0, 1) of A row k in a 32-byte-swizzled slot.
+__device__ __forceinline__ uint32_t rows_chunk(int k, int c) { return (uint32_t)(k * 32 + ((c ^ ((k >> 2) & 1)) << 4)); }
+
 template <bool SILU>
-__global__ void __launch_bounds__(256) stem_tc_bf16_s2_kernel(const StemLaunch a, StemTcGeom g,
-                                                              unsigned int *status) {
-    constexpr int S = kStemS2Stages;
+__global__ void __launch_bounds__(kStemRowsThreads) stem_tc_bf16_rows_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                                const StemLaunch a, StemRowsGeom g,
+                                                                unsigned int *status) {
+    constexpr int D = kStemRowsAhead, NE = kStemRowsESlots;
     extern __shared__ uint8_t stem_smem_raw[];
-    const uint32_t raw = ptx::smem_u32(stem_smem_raw);
-    uint8_t *base = stem_smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    uint8_t *sA = base;                                           // S pairs x 2 tiles x 12 KB
-    uint8_t *sB = base + S * kS2Pair;                             // panels of 16 rows: 1 KB, then 512 B
-    float *sBias = reinterpret_cast<float *>(sB + 2048);          // 16, halved (tanh form of SiLU)
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sBias + 16);    // 2
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
+    const uint32_t raw_u32 = ptx::smem_u32(stem_smem_raw);
+    uint8_t *base = stem_smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
+    uint8_t *sE = base;                                           // NE rewritten rows
+    uint8_t *sR = sE + NE * g.eslot;                              // 2D + 1 raw input rows
+    uint8_t *sB = sR + (2 * D + 1) * g.rawstride;                 // 3 kernel rows x 16 x 32 B
+    float *sBias = reinterpret_cast<float *>(sB + 1536);          // 16, halved (tanh form of SiLU)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sBias + 16);    // raw_full[D], mma_done[2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + D + 2);
+    const uint32_t sE_u32 = ptx::smem_u32(sE), sR_u32 = ptx::smem_u32(sR), sB_u32 = ptx::smem_u32(sB);
+    auto raw_bar = [&](int i) { return ptx::smem_u32(&bars[i]); };
+    auto mma_bar = [&](int i) { return ptx::smem_u32(&bars[D + i]); };
 
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int sub = t >> 7, row = t & 127;
+    const uint32_t tcols = 2 * g.mtiles * 16 <= 32 ? 32u : (2 * g.mtiles * 16 <= 64 ? 64u : 128u);
     if (warp == 0) {
-        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 64);   // two buffers x two tiles x 16 columns
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), tcols);   // two buffers x mtiles x 16 columns
         ptx::tmem_relinquish();
     }
     if (t == 0) {
-        ptx::mbar_init(ptx::smem_u32(&bars[0]), 1);
-        ptx::mbar_init(ptx::smem_u32(&bars[1]), 1);
+        for (int i = 0; i < D + 2; ++i) ptx::mbar_init(ptx::smem_u32(&bars[i]), 1);
         ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tmX);
     }
     __syncthreads();
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
-    // B row co: output channel co's weights in the pair K layout.  Chunk 2r:
-    // (0, tap (r, 0)) -- its first pixel is unused; chunk 2r + 1: taps
-    // (r, 1), (r, 2).  The B tile has A's two panels: 16 rows of 64 bytes
-    // at sB, 16 rows of 32 bytes at sB + 1 KB.
-    if (t < 96) {
-        const int co = t / 6, q = t - co * 6;
-        const uint2 *wr = static_cast<const uint2 *>(a.w) + co * 9;   // [16][9] taps of 4 bf16
-        uint2 lo = make_uint2(0u, 0u), hi = make_uint2(0u, 0u);
-        const int r = q >> 1;
-        if ((q & 1) == 0) {
-            hi = wr[3 * r];
-        } else {
-            lo = wr[3 * r + 1];
-            hi = wr[3 * r + 2];
-        }
-        const uint32_t off = q < 4 ? (uint32_t)(co * 64 + ((q ^ ((co >> 1) & 3)) << 4))
-                                   : (uint32_t)(1024 + co * 32 + (((q - 4) ^ ((co >> 2) & 1)) << 4));
-        *reinterpret_cast<uint4 *>(sB + off) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    // B for kernel row r at sB + 512 r: output channel co's 32 bytes, chunk 0 =
+    // (0, tap (r, 0)), chunk 1 = (tap (r, 1), tap (r, 2)), 32-byte swizzled.
+    if (t < 48) {
+        const int r = t >> 4, co = t & 15;
+        const uint2 *wr = static_cast<const uint2 *>(a.w) + co * 9 + 3 * r;   // [16][9] taps of 4 bf16
+        const uint2 w0 = wr[0], w1 = wr[1], w2 = wr[2];
+        uint8_t *rowp = sB + r * 512;
+        *reinterpret_cast<uint4 *>(rowp + rows_chunk(co, 0)) = make_uint4(0u, 0u, w0.x, w0.y);
+        *reinterpret_cast<uint4 *>(rowp + rows_chunk(co, 1)) = make_uint4(w1.x, w1.y, w2.x, w2.y);
     }
     if (t < 16) sBias[t] = 0.5f * static_cast<const float *>(a.bias)[t];
 
-    const int n_pairs = (g.n_tiles + 1) >> 1;
-    const int n_local = (int)blockIdx.x < n_pairs ? (n_pairs - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const int ohw = a.OH * a.OW;
-    const uint8_t *xb = static_cast<const uint8_t *>(a.x);
-    const long long row_bytes = (long long)a.W * 8;
-    const uint32_t sA_u32 = ptx::smem_u32(sA);
-    const uint32_t my_tile = (uint32_t)(sub * kS2Tile);
-
-    // Issue this thread's copies of local pair i into stage i % S (an empty
-    // group past the last pair).
-    auto gather = [&](int i) {
-        if (i < n_local) {
-            const int pix = (((int)blockIdx.x + i * (int)gridDim.x) * 2 + sub) * 128 + row;
-            const bool valid = pix < g.total;
-            const int img = fast_div(pix, g.div_ohw);
-            const int rem = pix - img * ohw;
-            const int oh = fast_div(rem, g.div_ow);
-            const int ow = rem - oh * a.OW;
-            const int ih0 = 2 * oh - 1;
-            // Byte offset of the pixel pair at input column 2 ow - 2 of row ih0
-            // (16-byte aligned: W and 2 ow - 2 are even); read only in bounds.
-            const long long off0 = (((long long)img * a.H + ih0) * a.W + 2 * ow - 2) * 8;
-            const uint32_t dst = sA_u32 + (uint32_t)((i % S) * kS2Pair) + my_tile;
-#pragma unroll
-            for (int r = 0; r < 3; ++r) {
-                const bool rin = valid && (unsigned)(ih0 + r) < (unsigned)a.H;
-                const bool lin = rin && ow > 0;
-                const long long off = off0 + r * row_bytes;
-                ptx::cp_async_16(dst + s2_chunk(row, 2 * r), lin ? (const void *)(xb + off) : a.x, lin ? 16u : 0u);
-                ptx::cp_async_16(dst + s2_chunk(row, 2 * r + 1), rin ? (const void *)(xb + off + 16) : a.x,
-                                 rin ? 16u : 0u);
-            }
+    // This CTA's band of output rows.
+    const int R0 = (int)((long long)blockIdx.x * g.rows / gridDim.x);
+    const int nsteps = (int)((long long)(blockIdx.x + 1) * g.rows / gridDim.x) - R0;
+    const int OW = a.OW;
+    // Input loads of step s (one TMA box per input row), issued by lanes 0-2
+    // of the calling warp in parallel (a thread waits ~570 cycles per box):
+    // rows 2 oh and 2 oh + 1 into raw slots 2s, 2s + 1 (mod 2D), and at the
+    // band's first step row 2 oh - 1 into slot 2D.
+    auto issue_loads = [&](int s) {
+        const int R = R0 + s, img = R / a.OH, oh = R - img * a.OH;
+        const bool with_a = s == 0 && oh > 0;
+        const uint32_t bar = raw_bar(s % D);
+        if (lane == 0) ptx::mbar_arrive_expect_tx(bar, (uint32_t)((with_a ? 3 : 2) * g.raw));
+        __syncwarp();
+        if (lane < 2)
+            ptx::tma_load_4d(sR_u32 + (uint32_t)(((2 * s + lane) % (2 * D)) * g.rawstride), &tmX, bar, 0, 0,
+                             2 * oh + lane, img);
+        else if (lane == 2 && with_a)
+            ptx::tma_load_4d(sR_u32 + (uint32_t)(2 * D * g.rawstride), &tmX, bar, 0, 0, 2 * oh - 1, img);
+    };
+    // Rewrite raw slot `rs` into A-row slot `es` (column k: pair k-1 with its
+    // first pixel zeroed, then pair k).
+    auto rewrite = [&](int rs, int es) {
+        const uint8_t *rp = sR + rs * g.rawstride;
+        uint8_t *ep = sE + es * g.eslot;
+        for (int k = t; k < OW; k += 256) {   // warps 0-7
+            const uint4 pk = *reinterpret_cast<const uint4 *>(rp + 16 * k);
+            const uint2 pm = k > 0 ? *reinterpret_cast<const uint2 *>(rp + 16 * k - 8) : make_uint2(0u, 0u);
+            *reinterpret_cast<uint4 *>(ep + rows_chunk(k, 0)) = make_uint4(0u, 0u, pm.x, pm.y);
+            *reinterpret_cast<uint4 *>(ep + rows_chunk(k, 1)) = pk;
         }
-        ptx::cp_async_commit();
     };
 
-#pragma unroll 1
-    for (int i = 0; i < S - 1; ++i) gather(i);
+    if (warp == 8)
+        for (int s = 0; s < D && s < nsteps; ++s) issue_loads(s);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    float bh[16];
+    float bh[8];
+    const int q = warp & 3, h = (warp >> 2) & 1;   // TMEM lane quadrant, column half (8 h .. 8 h + 7)
 #pragma unroll
-    for (int c = 0; c < 16; ++c) bh[c] = sBias[c];
-    // Panel 0: 64-byte rows, 64-byte swizzle (8-row groups 512 B apart);
-    // panel 1: 32-byte rows, 32-byte swizzle (256 B apart).
-    const uint64_t d64 = ptx::smem_desc(0u, 16u, 512u, 4u), d32 = ptx::smem_desc(0u, 16u, 256u, 6u);
+    for (int c = 0; c < 8; ++c) bh[c] = sBias[8 * h + c];
+    const uint64_t d32 = ptx::smem_desc(0u, 16u, 256u, 6u);   // 32-byte rows, 8-row groups 256 B apart
     const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(16 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-    const uint32_t sB_u32 = ptx::smem_u32(sB);
-    const uint64_t bd0 = d64 | (uint64_t)((sB_u32 & 0x3FFFFu) >> 4);
-    const uint64_t bd1 = d32 | (uint64_t)(((sB_u32 + 1024u) & 0x3FFFFu) >> 4);
-    const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(sub * 16);
+    const int bufcols = g.mtiles * 16;
     __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(a.y);
     bool failed = false;
+    const bool issuer = warp == 8;
+    int issued = D < nsteps ? D : nsteps;   // steps whose loads have been issued (thread 0, then warp 8)
+    int stop = nsteps;                      // loads of steps >= stop may still be in flight at exit
 #pragma unroll 1
-    for (int i = 0; i <= n_local; ++i) {
-        if (i < n_local) {
-            ptx::cp_async_wait<S - 2>();   // this thread's copies of pair i have landed
-            // Zero the unused first pixel of each kernel row's first pair.
-            uint8_t *tp = sA + (i % S) * kS2Pair + my_tile;
-#pragma unroll
-            for (int r = 0; r < 3; ++r) *reinterpret_cast<uint2 *>(tp + s2_chunk(row, 2 * r)) = make_uint2(0u, 0u);
-            ptx::fence_proxy_async_smem();
+    for (int s = 0; s <= nsteps; ++s) {
+        if (s < nsteps && !issuer) {
+            if (!ptx::mbar_wait_bounded(raw_bar(s % D), (uint32_t)((s / D) & 1), kStemWaitNs)) {
+                failed = true;
+                if (lane == 0) atomicOr(status, 1u);
+            } else {
+                const int R = R0 + s, oh = R - (R / a.OH) * a.OH;
+                rewrite((2 * s) % (2 * D), (2 * s) % NE);
+                rewrite((2 * s + 1) % (2 * D), (2 * s + 1) % NE);
+                if (s == 0 && oh > 0) rewrite(2 * D, NE - 1);
+                ptx::fence_proxy_async_smem();
+            }
         }
         ptx::tc_fence_before();
-        if (__syncthreads_or(failed)) break;
-        ptx::tc_fence_after();
-        if (i < n_local && t == 0) {
-#pragma unroll
-            for (int sb = 0; sb < 2; ++sb) {
-                const uint32_t ta = sA_u32 + (uint32_t)((i % S) * kS2Pair + sb * kS2Tile);
-                const uint64_t a0 = d64 | (uint64_t)((ta & 0x3FFFFu) >> 4);
-                const uint64_t a1 = d32 | (uint64_t)(((ta + (uint32_t)kS2Panel1) & 0x3FFFFu) >> 4);
-                const uint32_t acc = tmem + (uint32_t)((i & 1) * 32 + sb * 16);
-                ptx::mma_f16(acc, a0, bd0, idesc, 0u);             // K 0..15
-                ptx::mma_f16(acc, a0 + 2u, bd0 + 2u, idesc, 1u);   // K 16..31: 32 bytes on
-                ptx::mma_f16(acc, a1, bd1, idesc, 1u);             // K 32..47
-            }
-            ptx::mma_commit(ptx::smem_u32(&bars[i & 1]));
+        if (__syncthreads_or(failed)) {
+            stop = s;
+            break;
         }
-        if (i == 0) {
-            gather(S - 1);
+        ptx::tc_fence_after();
+        if (issuer) {
+            if (s >= nsteps) continue;
+            const int R = R0 + s, oh = R - (R / a.OH) * a.OH;
+            if (lane == 0) {
+                const int r0 = oh == 0 ? 1 : 0;   // kernel row 0 of output row 0 is padding
+                const uint32_t d0 = tmem + (uint32_t)((s & 1) * bufcols);
+                for (int r = r0; r < 3; ++r) {
+                    const int es = ((2 * s - 1 + r) % NE + NE) % NE;
+                    const uint64_t bd = d32 | (uint64_t)(((sB_u32 + (uint32_t)(r * 512)) & 0x3FFFFu) >> 4);
+                    for (int m = 0; m < g.mtiles; ++m) {
+                        const uint64_t ad =
+                            d32 | (uint64_t)(((sE_u32 + (uint32_t)(es * g.eslot + m * 4096)) & 0x3FFFFu) >> 4);
+                        ptx::mma_f16(d0 + (uint32_t)(m * 16), ad, bd, idesc, r > r0 ? 1u : 0u);
+                    }
+                }
+                ptx::mma_commit(mma_bar(s & 1));
+            }
+            // Step s's raw slots and load barrier are free: they take step s + D.
+            if (s + D < nsteps) {
+                issue_loads(s + D);
+                issued = s + D + 1;
+            }
             continue;
         }
-        const int j = i - 1;
-        bool ok = ptx::mbar_wait_bounded(ptx::smem_u32(&bars[j & 1]), (uint32_t)((j >> 1) & 1), kStemWaitNs);
+        if (s == 0) continue;
+        const int j = s - 1;
+        bool ok = ptx::mbar_wait_bounded(mma_bar(j & 1), (uint32_t)((j >> 1) & 1), kStemWaitNs);
         ok = __all_sync(0xffffffffu, ok);   // warp-uniform before .sync.aligned loads
         if (!ok) {
             failed = true;
@@ -723,31 +745,39 @@ __global__ void __launch_bounds__(256) stem_tc_bf16_s2_kernel(const StemLaunch a
             continue;
         }
         ptx::tc_fence_after();
-        // Pair j's MMAs have completed: its stage takes pair j + S.
-        gather(j + S);
-        uint32_t v[16];
-        ptx::tmem_ld16(t_lane + (uint32_t)((j & 1) * 32), v);
-        ptx::tmem_ld_wait();
-        const int pix = (((int)blockIdx.x + j * (int)gridDim.x) * 2 + sub) * 128 + row;
-        if (pix < g.total) {
-            uint32_t o[8];
+        // Epilogue of output row R0 + j: this warp's 32 TMEM lanes of each
+        // M tile, output channels 8 h .. 8 h + 7 (16 bytes per pixel).
+        const size_t pix0 = (size_t)(R0 + j) * OW;
+        const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((j & 1) * bufcols + 8 * h);
+        uint32_t v[kStemRowsMaxMtiles][8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float h0 = fmaf(__uint_as_float(v[2 * c]), 0.5f, bh[2 * c]);
-                const float h1 = fmaf(__uint_as_float(v[2 * c + 1]), 0.5f, bh[2 * c + 1]);
-                o[c] = SILU ? cvt_bf16x2(silu_tanh(h0), silu_tanh(h1)) : cvt_bf16x2(h0 + h0, h1 + h1);
+        for (int m = 0; m < kStemRowsMaxMtiles; ++m)
+            if (m < g.mtiles && m * 128 + 32 * q < OW) ptx::tmem_ld8(tl + (uint32_t)(m * 16), v[m]);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int m = 0; m < kStemRowsMaxMtiles; ++m) {
+            const int k = m * 128 + 32 * q + lane;
+            if (m < g.mtiles && k < OW) {
+                uint32_t o[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float h0 = fmaf(__uint_as_float(v[m][2 * c]), 0.5f, bh[2 * c]);
+                    const float h1 = fmaf(__uint_as_float(v[m][2 * c + 1]), 0.5f, bh[2 * c + 1]);
+                    o[c] = SILU ? cvt_bf16x2(silu_tanh(h0), silu_tanh(h1)) : cvt_bf16x2(h0 + h0, h1 + h1);
+                }
+                *reinterpret_cast<uint4 *>(y + (pix0 + (size_t)k) * 16 + 8 * h) = make_uint4(o[0], o[1], o[2], o[3]);
             }
-            uint4 *dst = reinterpret_cast<uint4 *>(y + (size_t)pix * 16);
-            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
     }
-    ptx::cp_async_wait<0>();
+    // After a timeout: let the loads already issued land before the CTA exits.
+    if (issuer && lane == 0)
+        for (int k = stop; k < issued; ++k)
+            ptx::mbar_wait_bounded(raw_bar(k % D), (uint32_t)((k / D) & 1), kStemWaitNs);
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, 64);
+        ptx::tmem_dealloc(tmem, tcols);
     }
 }
 
@@ -1200,11 +1230,32 @@ cudaError_t launch_stem_tc(const StemLaunch &L, cudaStream_t s) {
     g.div_ohw = make_fastdiv((uint32_t)(L.OH * L.OW));
     g.div_ow = make_fastdiv((uint32_t)L.OW);
     if (stem_s2_kernel_applies(L.kind, L.KS, L.stride, L.pad, L.W, L.Cout, L.out_nhwc, L.residual != nullptr)) {
-        const int grid = std::min((g.n_tiles + 1) / 2, L.grid);   // the plan's persistent CTAs
-        auto kern = L.act != CBS_ACT_IDENTITY ? stem_tc_bf16_s2_kernel<true> : stem_tc_bf16_s2_kernel<false>;
-        const cudaError_t e = set_max_dyn_smem(kern, kStemS2SmemBytes);
+        // Input rows as [N][H][nb][bx] bf16 (bx: the largest multiple of 8
+        // dividing 4 W, at most 256): one TMA box {bx, nb, 1, 1} per row.
+        const int row_el = 4 * L.W;
+        int bx = 8;
+        for (int c = 8; c <= 256 && c <= row_el; c += 8)
+            if (row_el % c == 0) bx = c;
+        const int nb = row_el / bx;
+        if (nb > 256) return cudaErrorInvalidValue;
+        const cuuint64_t dims[4] = {(cuuint64_t)bx, (cuuint64_t)nb, (cuuint64_t)L.H, (cuuint64_t)L.N};
+        const cuuint64_t strides[3] = {(cuuint64_t)bx * 2, (cuuint64_t)L.W * 8, (cuuint64_t)L.H * L.W * 8};
+        const cuuint32_t box[4] = {(cuuint32_t)bx, (cuuint32_t)nb, 1u, 1u};
+        CUtensorMap tm;
+        if (encode_plain_map(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, L.x, dims, strides, box) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        StemRowsGeom rg;
+        rg.rows = L.N * L.OH;
+        rg.mtiles = (L.OW + 127) / 128;
+        rg.eslot = rg.mtiles * 4096;
+        rg.raw = L.W * 8;
+        rg.rawstride = (rg.raw + 255) / 256 * 256;
+        const int smem = stem_rows_smem_bytes(L.W);
+        const int grid = std::min(rg.rows, L.grid);   // the plan's CTAs, one band of output rows each
+        auto kern = L.act != CBS_ACT_IDENTITY ? stem_tc_bf16_rows_kernel<true> : stem_tc_bf16_rows_kernel<false>;
+        const cudaError_t e = set_max_dyn_smem(kern, smem);
         if (e != cudaSuccess) return e;
-        return launch_kernel(kern, grid, 256, kStemS2SmemBytes, s, L, g, status);
+        return launch_kernel(kern, grid, kStemRowsThreads, (size_t)smem, s, tm, L, rg, status);
     }
     const int grid = std::min(g.n_tiles, L.grid);   // the plan's persistent CTAs
     const int n_mma = (L.Cout + 15) / 16 * 16;

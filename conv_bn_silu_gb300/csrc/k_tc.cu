@@ -1502,6 +1502,20 @@ const DriverFns &driver_fns() {
     return fns;
 }
 
+}  // namespace
+
+CUresult encode_plain_map(CUtensorMap *tm, CUtensorMapDataType dt, int rank, const void *ptr, const cuuint64_t *dims,
+                          const cuuint64_t *strides, const cuuint32_t *box) {
+    const DriverFns &fns = driver_fns();
+    if (!fns.ok) return CUDA_ERROR_NOT_FOUND;
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return fns.tiled(tm, dt, (cuuint32_t)rank, const_cast<void *>(ptr), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+namespace {
+
 CUtensorMapSwizzle swizzle_for(int rb) {
     return rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : rb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
 }

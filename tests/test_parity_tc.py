@@ -108,18 +108,19 @@ def test_tensor_core_stem(cuda_lib, out_layout, shape):
     x, p = wl.layer_inputs(spec, n, layer_index=4)
     y, layer = run_tc(spec, x, p, B.CBS_BF16, out_layout=out_layout)
     pl = layer.plan
-    assert pl.variant == B.CBS_VARIANT_STEM and pl.block_m == 128 and pl.threads == 256
+    assert pl.variant == B.CBS_VARIANT_STEM and pl.block_m == 128
     sms = layer.desc.num_sms
     if pair_stem_kernel(spec, out_layout):
-        assert pl.grid_ctas == min((pl.m_tiles + 1) // 2, sms * 2)   # two tiles per step, two CTAs per SM
+        assert pl.threads == 288 and pl.grid_ctas == min(n * spec.oh, sms * 2)   # bands of output rows, two CTAs per SM
     else:
+        assert pl.threads == 256
         assert pl.grid_ctas == min(pl.m_tiles, sms * (5 if c_out <= 32 else 4))   # 4 x 128 TMEM columns for wide C_out
     check(y, spec, x, p, "bf16", shape)
 
 
 def pair_stem_kernel(spec, out_layout):
-    """The shapes the stem's two-tile kernel takes: 3x3, stride 2, pad 1,
-    even input width, 16 output channels, NHWC output."""
+    """The shapes the stem's row kernel takes: 3x3, stride 2, pad 1, even
+    input width up to 1024, 16 output channels, NHWC output."""
     return (spec.k == 3 and spec.stride == 2 and spec.pad == 1 and spec.width % 2 == 0 and spec.c_out == 16
             and out_layout == B.CBS_NHWC)
 
@@ -129,18 +130,20 @@ def pair_stem_kernel(spec, out_layout):
     (1, 3, 16, 3, 2, 2, 2),        # one output pixel: one pair of tiles, the second empty
     (3, 3, 16, 3, 2, 37, 38),      # odd height: the last output row's third kernel row is padding
     (2, 4, 16, 3, 2, 30, 62),      # four channels, non-square, odd tile count
-    (16, 3, 16, 3, 2, 320, 320),   # 1600 tile pairs: each CTA goes round the stage ring
+    (16, 3, 16, 3, 2, 320, 320),   # 2560 output rows: bands of ~8 rows, round the slot rings
+    (2, 3, 16, 3, 2, 640, 640),    # the detector's width: three M tiles per output row, the last ragged
+    (5, 3, 16, 3, 2, 9, 200),      # bands that cross images (output row 0 inside a band)
 ])
 def test_stem_pair_kernel(cuda_lib, act, shape):
-    """The BF16 stem's two-tile kernel (one thread per output pixel) against
-    the oracle, with and without SiLU."""
+    """The BF16 stem's row kernel (TMA input rows, rewritten in shared memory
+    as MMA operand rows) against the oracle, with and without SiLU."""
     n, c_in, c_out, k, stride, h, w = shape
     spec = wl.LayerSpec(c_in, c_out, k, stride, h, w)
     assert pair_stem_kernel(spec, B.CBS_NHWC)
     x, p = wl.layer_inputs(spec, n, layer_index=4)
     y, layer = run_tc(spec, x, p, B.CBS_BF16, activation=act)
     assert layer.plan.variant == B.CBS_VARIANT_STEM
-    assert layer.plan.grid_ctas == min((layer.plan.m_tiles + 1) // 2, layer.desc.num_sms * 2)
+    assert layer.plan.grid_ctas == min(n * spec.oh, layer.desc.num_sms * 2)
     check_tc("bf16", y, tc_refs("bf16", x, p, spec.stride, spec.pad, act=act), (shape, act))
 
 
