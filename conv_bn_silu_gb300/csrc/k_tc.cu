@@ -384,6 +384,30 @@ __device__ __forceinline__ void issue_kstep(uint32_t d, uint64_t dhi, uint32_t a
     }
 }
 
+// The same from ready descriptors (the address field advanced by the caller).
+template <int KIND>
+__device__ __forceinline__ void issue_kstep_desc(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, int kslices,
+                                                 bool first) {
+    if (kslices == 4) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t acc = (first && k == 0) ? 0u : 1u;
+            if (KIND == kTF32)
+                ptx::mma_tf32(d, ad + 2u * k, bd + 2u * k, idesc, acc);
+            else
+                ptx::mma_f16(d, ad + 2u * k, bd + 2u * k, idesc, acc);
+        }
+    } else {
+        for (int k = 0; k < kslices; ++k) {
+            const uint32_t acc = (first && k == 0) ? 0u : 1u;
+            if (KIND == kTF32)
+                ptx::mma_tf32(d, ad + 2u * k, bd + 2u * k, idesc, acc);
+            else
+                ptx::mma_f16(d, ad + 2u * k, bd + 2u * k, idesc, acc);
+        }
+    }
+}
+
 __device__ __forceinline__ void abort_now(const TcParams &p, int *abort_flag) {
     atomicOr(p.status, 1u);
     *(volatile int *)abort_flag = 1;
@@ -654,30 +678,49 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         }
                         ptx::tc_fence_after();
                         const uint32_t window = stage0 + s * p.stage_bytes;
-                        for (int tap = 0; tap < kk2 && ok; ++tap) {
-                            const int r = tap / p.ks, c = tap - r * p.ks;
-                            uint32_t b_addr;
-                            int ws = 0;
-                            if (p.b_res) {
-                                b_addr = b_base + (tap * p.cblocks + cb) * p.b_tile_stride;
-                            } else {
-                                ws = gw % p.SB;
-                                if (!ptx::mbar_wait_bounded(wfull_bar(ws), (gw / p.SB) & 1, kWaitLimitNs)) {
-                                    abort_now(p, abort_flag);
-                                    ok = false;
-                                    break;
-                                }
-                                ptx::tc_fence_after();
-                                b_addr = b_base + ws * p.b_tile_stride;
+                        if (p.b_res) {
+                            // Resident weights: no wait between taps.  The
+                            // descriptors advance by constant steps (address
+                            // field in 16-byte units): a tap to the right is one
+                            // window row on, a tap below is Wp rows on.  A
+                            // thread issuing MMAs pays for every scalar
+                            // instruction between them.
+                            const uint64_t a_first =
+                                dhi | (uint64_t)(((window + (uint32_t)row0 * p.RB + mi * sub_bytes) & 0x3FFFFu) >> 4);
+                            const uint64_t b_first =
+                                dhi | (uint64_t)(((b_base + (uint32_t)(cb * p.b_tile_stride)) & 0x3FFFFu) >> 4);
+                            const uint64_t a_col = (uint64_t)(p.RB >> 4), a_row = (uint64_t)((p.Wp * p.RB) >> 4);
+                            const uint64_t b_tap = (uint64_t)((p.cblocks * p.b_tile_stride) >> 4);
+                            uint64_t ar = a_first, bd = b_first;
+                            for (int r = 0; r < p.ks; ++r, ar += a_row) {
+                                uint64_t ad = ar;
+                                for (int c = 0; c < p.ks; ++c, ad += a_col, bd += b_tap)
+                                    issue_kstep_desc<KIND>(d_tmem, ad, bd, p.idesc, kslices, cb == 0 && r == 0 && c == 0);
                             }
+                            ptx::mma_commit(empty_bar(s));
+                            continue;
+                        }
+                        // Streamed weights: each tap waits for its slot of the ring.
+                        int r = 0, c = 0;   // tap (r, c) = tap / ks, tap % ks, without a division
+                        for (int tap = 0; tap < kk2 && ok; ++tap) {
+                            const int ws = gw % p.SB;
+                            if (!ptx::mbar_wait_bounded(wfull_bar(ws), (gw / p.SB) & 1, kWaitLimitNs)) {
+                                abort_now(p, abort_flag);
+                                ok = false;
+                                break;
+                            }
+                            ptx::tc_fence_after();
+                            const uint32_t b_addr = b_base + ws * p.b_tile_stride;
                             // A view starting at any 128-byte row: the descriptor's
                             // start address alone places it (absolute swizzle).
                             const uint32_t a0 = window + (uint32_t)(row0 + r * p.Wp + c) * p.RB;
                             issue_kstep<KIND>(d_tmem, dhi, a0 + mi * sub_bytes, b_addr, p.idesc, kslices,
                                               cb == 0 && tap == 0);
-                            if (!p.b_res) {
-                                ptx::mma_commit(wempty_bar(ws));   // weight slot free once these MMAs are done
-                                ++gw;
+                            ptx::mma_commit(wempty_bar(ws));   // weight slot free once these MMAs are done
+                            ++gw;
+                            if (++c == p.ks) {
+                                c = 0;
+                                ++r;
                             }
                         }
                         if (!ok) break;
@@ -696,14 +739,15 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     ptx::tc_fence_after();
                     const uint32_t sbase = stage0 + s * p.stage_bytes;
-                    for (int kk = 0; kk < p.kg; ++kk) {
-                        const int i = st * p.kg + kk;
-                        const uint32_t a_addr = sbase + kk * p.a_box_bytes;
-                        const uint32_t b_addr = p.b_res ? b_base + i * p.b_tile_stride
-                                                        : sbase + p.kg * p.a_box_bytes + kk * p.b_tile_stride;
-                        issue_kstep<KIND>(d_tmem, dhi, a_addr + mi * sub_bytes, b_addr, p.idesc, kslices,
-                                          i == st0 * p.kg);
-                    }
+                    // K step kk of the stage: A box kk (this issuer's 128-row
+                    // half), B tile st * kg + kk (resident) or kk (in the stage).
+                    const uint32_t b0 = p.b_res ? b_base + (uint32_t)(st * p.kg * p.b_tile_stride)
+                                                : sbase + (uint32_t)(p.kg * p.a_box_bytes);
+                    uint64_t ad = dhi | (uint64_t)(((sbase + mi * sub_bytes) & 0x3FFFFu) >> 4);
+                    uint64_t bd = dhi | (uint64_t)((b0 & 0x3FFFFu) >> 4);
+                    const uint64_t a_step = (uint64_t)(p.a_box_bytes >> 4), b_step = (uint64_t)(p.b_tile_stride >> 4);
+                    for (int kk = 0; kk < p.kg; ++kk, ad += a_step, bd += b_step)
+                        issue_kstep_desc<KIND>(d_tmem, ad, bd, p.idesc, kslices, st == st0 && kk == 0);
                     ptx::mma_commit(empty_bar(s));
                 }
                 if (!ok) break;
