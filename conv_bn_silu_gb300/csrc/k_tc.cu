@@ -1162,7 +1162,14 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 }
                 ptx::tc_fence_after();
                 bool ok = true;
-                int kc = 0, chunk = 0;   // X3: K step within the current accumulator chunk, and that chunk
+                // K step within the current accumulator chunk, and that chunk
+                // (counted, not divided: the issuing thread pays for every
+                // instruction between its MMAs).  X3 units start at chunk 0.
+                int kc = 0, chunk = 0;
+                if constexpr (SK != kStagedX3) {
+                    chunk = (st0 * kg) / p.kpc;
+                    kc = st0 * kg - chunk * p.kpc;
+                }
                 for (int st = st0; st < st1; ++st, ++g) {
                     const int s = g % S, u = g / S;
                     // conv_done follows raw_full (the converters waited on it),
@@ -1176,7 +1183,6 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     ptx::tc_fence_after();
                     const uint32_t sb = base + s * p.stage_bytes;
                     for (int kk = 0; kk < kg; ++kk) {
-                        const int i = st * kg + kk;
                         if constexpr (SK == kStagedX3) {
                             if (kc == p.kpc) {   // this unit's next chunk of K steps
                                 kc = 0;
@@ -1191,11 +1197,15 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                             issue_kstep<kTF32>(d_tmem, dhi, a_head, b_tail, p.idesc, kslices, false);
                             issue_kstep<kTF32>(d_tmem, dhi, a_head, b_head, p.idesc, kslices, false);
                         } else {
-                            const int chunk = i / p.kpc;
+                            if (kc == p.kpc) {
+                                kc = 0;
+                                ++chunk;
+                            }
+                            const bool first = kc++ == 0;
                             const uint32_t d_tmem =
                                 tmem_base + (uint32_t)(acc * p.acc_stride + chunk * p.chunk_stride);
                             issue_kstep<kBF16>(d_tmem, dhi, sb + kk * p.a_bytes, sb + op_b_off + kk * p.b_tile_stride,
-                                               p.idesc, kslices, (i % p.kpc) == 0);
+                                               p.idesc, kslices, first);
                         }
                     }
                     ptx::mma_commit(free_bar(s));
