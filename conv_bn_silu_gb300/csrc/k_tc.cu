@@ -456,7 +456,6 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = p.ksteps;
     const int nstage = p.win ? p.cblocks : nk / p.kg;   // stages per tile
-    const int kk2 = p.ks * p.ks;
     const int tile_m = kBM * p.mmul;
     const int num_tiles = p.m_tiles * p.n_tiles;
     const int num_units = num_tiles * p.split;    // split-K: (tile, K part) units
@@ -522,8 +521,10 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
                 const int n0 = (t % p.n_tiles) * p.BN;
                 bool ok = true;
+                // A ring slot holds one kernel row: the weight tiles of its ks taps.
+                const uint32_t slot_bytes = (uint32_t)(p.ks * p.b_tile_stride);
                 for (int cb = 0; cb < p.cblocks && ok; ++cb) {
-                    for (int tap = 0; tap < kk2; ++tap, ++gw) {
+                    for (int r = 0; r < p.ks; ++r, ++gw) {
                         if (gw % p.SB != lane) continue;
                         const int u = gw / p.SB;
                         if (!ptx::mbar_wait_bounded(wempty_bar(lane), (u & 1) ^ 1, kWaitLimitNs) || aborted(abort_flag)) {
@@ -531,9 +532,10 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             ok = false;
                             break;
                         }
-                        ptx::mbar_arrive_expect_tx(wfull_bar(lane), (uint32_t)b_step_bytes);
-                        ptx::tma_load_2d(b_base + lane * p.b_tile_stride, &tmB, wfull_bar(lane),
-                                         tap * p.c_in_pad + cb * p.CB, n0);
+                        ptx::mbar_arrive_expect_tx(wfull_bar(lane), (uint32_t)(p.ks * b_step_bytes));
+                        for (int c = 0; c < p.ks; ++c)
+                            ptx::tma_load_2d(b_base + lane * slot_bytes + (uint32_t)(c * p.b_tile_stride), &tmB,
+                                             wfull_bar(lane), (r * p.ks + c) * p.c_in_pad + cb * p.CB, n0);
                         last_w = gw;
                     }
                 }
@@ -700,9 +702,15 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             ptx::mma_commit(empty_bar(s));
                             continue;
                         }
-                        // Streamed weights: each tap waits for its slot of the ring.
-                        int r = 0, c = 0;   // tap (r, c) = tap / ks, tap % ks, without a division
-                        for (int tap = 0; tap < kk2 && ok; ++tap) {
+                        // Streamed weights: one wait per kernel row (its ks taps'
+                        // weight tiles share a ring slot).
+                        const uint64_t a_first =
+                            dhi | (uint64_t)(((window + (uint32_t)row0 * p.RB + mi * sub_bytes) & 0x3FFFFu) >> 4);
+                        const uint64_t a_col = (uint64_t)(p.RB >> 4), a_row = (uint64_t)((p.Wp * p.RB) >> 4);
+                        const uint64_t b_col = (uint64_t)(p.b_tile_stride >> 4);
+                        const uint32_t slot_bytes = (uint32_t)(p.ks * p.b_tile_stride);
+                        uint64_t ar = a_first;
+                        for (int r = 0; r < p.ks; ++r, ar += a_row) {
                             const int ws = gw % p.SB;
                             if (!ptx::mbar_wait_bounded(wfull_bar(ws), (gw / p.SB) & 1, kWaitLimitNs)) {
                                 abort_now(p, abort_flag);
@@ -710,18 +718,12 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                 break;
                             }
                             ptx::tc_fence_after();
-                            const uint32_t b_addr = b_base + ws * p.b_tile_stride;
-                            // A view starting at any 128-byte row: the descriptor's
-                            // start address alone places it (absolute swizzle).
-                            const uint32_t a0 = window + (uint32_t)(row0 + r * p.Wp + c) * p.RB;
-                            issue_kstep<KIND>(d_tmem, dhi, a0 + mi * sub_bytes, b_addr, p.idesc, kslices,
-                                              cb == 0 && tap == 0);
-                            ptx::mma_commit(wempty_bar(ws));   // weight slot free once these MMAs are done
+                            uint64_t ad = ar;
+                            uint64_t bd = dhi | (uint64_t)(((b_base + ws * slot_bytes) & 0x3FFFFu) >> 4);
+                            for (int c = 0; c < p.ks; ++c, ad += a_col, bd += b_col)
+                                issue_kstep_desc<KIND>(d_tmem, ad, bd, p.idesc, kslices, cb == 0 && r == 0 && c == 0);
+                            ptx::mma_commit(wempty_bar(ws));   // the slot is free once these MMAs are done
                             ++gw;
-                            if (++c == p.ks) {
-                                c = 0;
-                                ++r;
-                            }
                         }
                         if (!ok) break;
                         ptx::mma_commit(empty_bar(s));
@@ -1701,9 +1703,9 @@ bool tc_config_window(const cbs_layer_desc &d, int oh, int RB, int ksteps, bool 
     c.st_mode = 0;
     c.extra_bytes = tc_bias_smem_bytes(d);
     int cap = 0;
-    for (int sb : {8, 4}) {
+    for (int sb : {4, 2}) {   // streamed weights: slots of one kernel row (k taps) each
         c.SB = c.b_res ? 0 : sb;
-        c.b_region = c.b_res ? ksteps * c.b_tile_stride : c.SB * c.b_tile_stride;
+        c.b_region = c.b_res ? ksteps * c.b_tile_stride : c.SB * d.k * c.b_tile_stride;
         const int barrier_bytes = 8 * (2 * 16 + 6 + 2 * c.SB) + 16;
         cap = (kSmemBudget - c.b_region - c.extra_bytes - barrier_bytes) / c.stage_bytes;
         if (cap >= 2 || c.b_res) break;
@@ -1723,7 +1725,7 @@ bool tc_config_window(const cbs_layer_desc &d, int oh, int RB, int ksteps, bool 
     const double tpc = (double)((tiles + c.grid - 1) / c.grid);
     const int kslices = RB / 32;
     const double mma = tpc * (tc_tile_mma_clk((double)ksteps * kslices, (double)cblocks, c.mmul, c.BN, tf32) +
-                              (c.b_res ? 0.0 : (double)ksteps * 100.0));
+                              (c.b_res ? 0.0 : (double)(ksteps / d.k) * kClkPerStageWait));
     const double boxes = tpc * cblocks + (c.b_res ? (double)ksteps : tpc * ksteps);
     const double bytes = tpc * cblocks * (double)c.a_box_bytes + (c.b_res ? (double)ksteps : tpc * ksteps) * b_bytes;
     const double t_box = boxes * 140.0, t_fill = bytes / kFillBytesPerClk;
@@ -2094,7 +2096,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     P.a_bytes = kBM * RB; P.b_bytes = BN * RB;
     P.a_box_bytes = kBM * mmul * RB;
     P.b_tile_stride = round_up(P.b_bytes, 1024);
-    P.b_region = P.b_res ? P.ksteps * P.b_tile_stride : P.SB * P.b_tile_stride;
+    P.b_region = P.b_res ? P.ksteps * P.b_tile_stride : P.SB * d.k * P.b_tile_stride;
     if (P.win) {
         TcWindow wg;
         if (!tc_window_geometry(d, pl.oh, RB, kBM * mmul, wg)) return fail(CBS_ERR_PLAN_MISMATCH, "window geometry");
