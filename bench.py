@@ -130,7 +130,7 @@ WORKLOADS = {
     "layer_list_fp32_n1_nhwc": dict(kind="list", layers=wl.LAYER_LIST, n=1, prec="fp32", layout="nhwc"),
 }
 EXTRA_DEFAULT = ("layer_list_bf16_n16", "layer_list_tf32_n16", "layer_list_int8_n16", "chain_fp32_n1",
-                 "chain_bf16_n16", "layer_list_bf16_n16_residual", "layer_list_int8_n16_asym",
+                 "chain_bf16_n16", "chain_tf32_n16", "layer_list_bf16_n16_residual", "layer_list_int8_n16_asym",
                  "layer_list_fp32_n16_nhwc", "layer_list_fp32_n1_nhwc", "chain_fp32_n1_nhwc", "frame_fp32_n1",
                  "frame_bf16_n16", "chain_int8_n16", "chain_int8_n16_keepfloat")
 

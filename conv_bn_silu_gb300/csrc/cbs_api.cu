@@ -334,8 +334,8 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
         if (tc && stem_s2_kernel_applies(tc_kind, D.k, D.stride, D.pad, D.w, D.c_out, D.out_layout == CBS_NHWC,
                                          D.residual != 0)) {
             // the stem's own kernel: one band of output rows per CTA
-            p.grid_ctas = std::min(D.n * p.oh, plan_sms(D) * kStemRowsCtasPerSm);
-            p.smem_bytes = stem_rows_smem_bytes(D.w);
+            p.grid_ctas = std::min(D.n * p.oh, plan_sms(D) * stem_rows_ctas_per_sm(tc_kind));
+            p.smem_bytes = stem_rows_smem_bytes(tc_kind, D.w);
             p.threads = kStemRowsThreads;
         }
         p.workspace_bytes = 0;

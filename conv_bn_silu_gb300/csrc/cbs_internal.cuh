@@ -158,28 +158,32 @@ inline int stem_tc_ctas_per_sm(int cout, int tf32 = 0) {
 }
 // A ring + B (64 rows x 128 B) + bias + two mbarriers + TMEM slot + 1 KB for alignment
 constexpr int kStemTcSmemBytes = kStemTcStages * 16384 + 8192 + 64 * 4 + 16 + 16 + 1024;
-// The 640x640-class BF16 stem (3x3, stride 2, pad 1, even input width, 16
-// output channels, NHWC output, no residual) runs a kernel of its own that
-// walks whole output rows: TMA brings each input row into shared memory once,
-// the CTA rewrites it as the rows of the MMA's A operand, and each output row
-// is ceil(OW / 128) M=128 MMAs per kernel row.  kStemRowsCtasPerSm CTAs per
-// SM; kStemRowsAhead output rows of input loads in flight per CTA.
-constexpr int kStemRowsCtasPerSm = 2, kStemRowsAhead = 3, kStemRowsESlots = 6;
+// The 640x640-class BF16 and TF32 stems (3x3, stride 2, pad 1, even input
+// width, 16 output channels, NHWC output, no residual) run a kernel of their
+// own that walks whole output rows: TMA brings each input row into shared
+// memory once, the CTA rewrites it as the rows of the MMA's A operand, and
+// each output row is ceil(OW / 128) M=128 MMAs per kernel row.  Kind 1 is
+// BF16, 3 TF32; stem_rows_ctas_per_sm CTAs per SM; kStemRowsAhead output rows
+// of input loads in flight per CTA.
+constexpr int kStemRowsAhead = 3, kStemRowsESlots = 6;
 constexpr int kStemRowsThreads = 288;   // warps 0-7: rewrite and epilogue; warp 8: TMA and MMA issue
 constexpr int kStemRowsMaxMtiles = 4;   // OW <= 512: two accumulator buffers of 64 columns
+inline int stem_rows_ctas_per_sm(int kind) { return kind == 3 ? 1 : 2; }
 // Shared memory of the row kernel for an input width w (0 if it does not
-// apply): A-row slots, raw input rows, B, bias, barriers, TMEM slot, alignment.
-inline int stem_rows_smem_bytes(int w) {
+// fit): A-row slots, raw input rows, B, bias, barriers, TMEM slot, alignment.
+inline int stem_rows_smem_bytes(int kind, int w) {
+    const int px = kind == 3 ? 16 : 8, er = 4 * px;
     const int ow = w / 2, mtiles = (ow + 127) / 128;
     if (mtiles > kStemRowsMaxMtiles) return 0;
-    const int bytes = kStemRowsESlots * mtiles * 4096 + (2 * kStemRowsAhead + 1) * ((w * 8 + 255) / 256 * 256) + 1536 + 16 * 4 +
-                      8 * (kStemRowsAhead + 2) + 16 + 1024;
-    return bytes <= (228 * 1024) / kStemRowsCtasPerSm - 1024 ? bytes : 0;
+    const int bytes = kStemRowsESlots * mtiles * 128 * er + (2 * kStemRowsAhead + 1) * ((w * px + 1023) / 1024 * 1024) +
+                      3 * 16 * er + 16 * 4 + 8 * (kStemRowsAhead + 2) + 16 + 1024;
+    const int cap = kind == 3 ? 227 * 1024 : (228 * 1024) / 2 - 1024;
+    return bytes <= cap ? bytes : 0;
 }
 inline bool stem_s2_kernel_applies(int kind, int ks, int stride, int pad, int w, int cout, int out_nhwc,
                                    bool residual) {
-    return kind == 1 && ks == 3 && stride == 2 && pad == 1 && (w & 1) == 0 && cout == 16 && out_nhwc && !residual &&
-           stem_rows_smem_bytes(w) > 0;
+    return (kind == 1 || kind == 3) && ks == 3 && stride == 2 && pad == 1 && (w & 1) == 0 && cout == 16 && out_nhwc &&
+           !residual && stem_rows_smem_bytes(kind, w) > 0;
 }
 // Encodes a tiled TMA tensor map (no swizzle, no interleave, zero fill
 // outside the tensor) through the driver's entry point.

@@ -554,19 +554,20 @@ __global__ void __launch_bounds__(256) stem_tc_bf16_kernel(const StemLaunch a, i
     }
 }
 
-// The detector's BF16 stem on a kernel of its own: 3x3, stride 2, pad 1 over
-// 4-channel NHWC pixels of even input width W, 16 output channels, NHWC
-// output, no residual.  The general kernel above gathers every output
+// The detector's BF16 and TF32 stems on a kernel of their own: 3x3, stride
+// 2, pad 1 over 4-channel NHWC pixels of even input width W, 16 output
+// channels, NHWC output, no residual.  The general kernel above gathers every output
 // pixel's window from L2 (96 bytes per pixel, three times the input); this
 // one walks whole output rows.  Each CTA takes a band of consecutive output
 // rows (n, oh); one TMA box brings each input row into shared memory once
 // (zero-filled above and below the image), and the CTA rewrites it as the
-// rows of the MMA's A operand: for output column k, 32 bytes = the pixel
-// pair (2k-2, 2k-1) with its first pixel zeroed, then the pair (2k, 2k+1)
-// (the pair K layout of the general kernel; the zeroed pixel's weights are
-// zero, and zeroing it keeps a non-finite neighbour out of the sum).  That
-// rewrite is stored 32-byte swizzled, so output row oh is, per kernel row r,
-// ceil(OW / 128) M=128 MMAs whose A is a 128-row slice of input row
+// rows of the MMA's A operand: for output column k, the pixel pair
+// (2k-2, 2k-1) with its first pixel zeroed, then the pair (2k, 2k+1) (the
+// pair K layout of the general kernel; the zeroed pixel's weights are zero,
+// and zeroing it keeps a non-finite neighbour out of the sum): 32 bytes in
+// BF16, stored 32-byte swizzled (one K=16 MMA per kernel row), 64 bytes in
+// TF32, stored 64-byte swizzled (two K=8 MMAs).  Output row oh is, per kernel
+// row r, ceil(OW / 128) M=128 tiles whose A is a 128-row slice of input row
 // 2 oh - 1 + r's rewrite.  Input row 2 oh + 1 is also row 2 (oh + 1) - 1:
 // each input row is loaded and rewritten once per band.
 //
@@ -588,26 +589,37 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
 struct StemRowsGeom {
     int rows;        // output rows N * OH
     int mtiles;      // M=128 tiles per output row: ceil(OW / 128)
-    int eslot;       // bytes of one rewritten input row: mtiles * 4096
-    int raw;         // bytes of one input row: W * 8
-    int rawstride;   // bytes between raw row slots: raw rounded up to 256 (B stays swizzle-aligned)
+    int eslot;       // bytes of one rewritten input row: mtiles * 128 * (A row bytes)
+    int raw;         // bytes of one input row: W * (pixel bytes)
+    int rawstride;   // bytes between raw row slots: raw rounded up to 1024 (B stays swizzle-aligned)
 };
 
-// Offset of 16-byte chunk c (0, 1) of A row k in a 32-byte-swizzled slot.
-__device__ __forceinline__ uint32_t rows_chunk(int k, int c) { return (uint32_t)(k * 32 + ((c ^ ((k >> 2) & 1)) << 4)); }
+// Offset of 16-byte chunk c of A row k in a slot of ER-byte rows, swizzled
+// as TMA and the tensor cores swizzle them (16-byte chunk bits XOR address
+// bits 7.. : one bit for 32-byte rows, two for 64-byte rows).
+template <int ER>
+__device__ __forceinline__ uint32_t rows_chunk(int k, int c) {
+    return ER == 32 ? (uint32_t)(k * 32 + ((c ^ ((k >> 2) & 1)) << 4))
+                    : (uint32_t)(k * 64 + ((c ^ ((k >> 1) & 3)) << 4));
+}
 
-template <bool SILU>
-__global__ void __launch_bounds__(kStemRowsThreads) stem_tc_bf16_rows_kernel(const __grid_constant__ CUtensorMap tmX,
-                                                                const StemLaunch a, StemRowsGeom g,
-                                                                unsigned int *status) {
+// KIND 1: BF16 pixels (8 bytes); KIND 3: TF32, float pixels (16 bytes).
+template <int KIND, bool SILU>
+__global__ void __launch_bounds__(kStemRowsThreads) stem_tc_rows_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                                        const StemLaunch a, StemRowsGeom g,
+                                                                        unsigned int *status) {
     constexpr int D = kStemRowsAhead, NE = kStemRowsESlots;
+    constexpr int PX = KIND == 3 ? 16 : 8;     // bytes of one input pixel
+    constexpr int ER = 4 * PX;                 // bytes of one A row (one kernel row of one output column)
+    constexpr int TILE = 128 * ER;             // bytes of one M=128 slice of a rewritten row
+    constexpr int NW = kStemRowsThreads / 32 - 1;   // rewrite and epilogue warps; warp NW issues
     extern __shared__ uint8_t stem_smem_raw[];
     const uint32_t raw_u32 = ptx::smem_u32(stem_smem_raw);
     uint8_t *base = stem_smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
     uint8_t *sE = base;                                           // NE rewritten rows
     uint8_t *sR = sE + NE * g.eslot;                              // 2D + 1 raw input rows
-    uint8_t *sB = sR + (2 * D + 1) * g.rawstride;                 // 3 kernel rows x 16 x 32 B
-    float *sBias = reinterpret_cast<float *>(sB + 1536);          // 16, halved (tanh form of SiLU)
+    uint8_t *sB = sR + (2 * D + 1) * g.rawstride;                 // 3 kernel rows x 16 x ER bytes
+    float *sBias = reinterpret_cast<float *>(sB + 3 * 16 * ER);   // 16, halved (tanh form of SiLU)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sBias + 16);    // raw_full[D], mma_done[2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + D + 2);
     const uint32_t sE_u32 = ptx::smem_u32(sE), sR_u32 = ptx::smem_u32(sR), sB_u32 = ptx::smem_u32(sB);
@@ -628,15 +640,22 @@ __global__ void __launch_bounds__(kStemRowsThreads) stem_tc_bf16_rows_kernel(con
     __syncthreads();
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
-    // B for kernel row r at sB + 512 r: output channel co's 32 bytes, chunk 0 =
-    // (0, tap (r, 0)), chunk 1 = (tap (r, 1), tap (r, 2)), 32-byte swizzled.
+    // B for kernel row r at sB + 16 ER r: output channel co's ER bytes in the
+    // A rows' layout: (0, tap (r, 0)), then (tap (r, 1), tap (r, 2)).
     if (t < 48) {
         const int r = t >> 4, co = t & 15;
-        const uint2 *wr = static_cast<const uint2 *>(a.w) + co * 9 + 3 * r;   // [16][9] taps of 4 bf16
-        const uint2 w0 = wr[0], w1 = wr[1], w2 = wr[2];
-        uint8_t *rowp = sB + r * 512;
-        *reinterpret_cast<uint4 *>(rowp + rows_chunk(co, 0)) = make_uint4(0u, 0u, w0.x, w0.y);
-        *reinterpret_cast<uint4 *>(rowp + rows_chunk(co, 1)) = make_uint4(w1.x, w1.y, w2.x, w2.y);
+        uint8_t *rowp = sB + r * 16 * ER;
+        if (KIND == 1) {
+            const uint2 *wr = static_cast<const uint2 *>(a.w) + co * 9 + 3 * r;   // [16][9] taps of 4 bf16
+            const uint2 w0 = wr[0], w1 = wr[1], w2 = wr[2];
+            *reinterpret_cast<uint4 *>(rowp + rows_chunk<ER>(co, 0)) = make_uint4(0u, 0u, w0.x, w0.y);
+            *reinterpret_cast<uint4 *>(rowp + rows_chunk<ER>(co, 1)) = make_uint4(w1.x, w1.y, w2.x, w2.y);
+        } else {
+            const uint4 *wr = static_cast<const uint4 *>(a.w) + co * 9 + 3 * r;   // [16][9] taps of 4 floats
+            *reinterpret_cast<uint4 *>(rowp + rows_chunk<ER>(co, 0)) = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int c = 0; c < 3; ++c) *reinterpret_cast<uint4 *>(rowp + rows_chunk<ER>(co, c + 1)) = wr[c];
+        }
     }
     if (t < 16) sBias[t] = 0.5f * static_cast<const float *>(a.bias)[t];
 
@@ -665,15 +684,25 @@ __global__ void __launch_bounds__(kStemRowsThreads) stem_tc_bf16_rows_kernel(con
     auto rewrite = [&](int rs, int es) {
         const uint8_t *rp = sR + rs * g.rawstride;
         uint8_t *ep = sE + es * g.eslot;
-        for (int k = t; k < OW; k += 256) {   // warps 0-7
-            const uint4 pk = *reinterpret_cast<const uint4 *>(rp + 16 * k);
-            const uint2 pm = k > 0 ? *reinterpret_cast<const uint2 *>(rp + 16 * k - 8) : make_uint2(0u, 0u);
-            *reinterpret_cast<uint4 *>(ep + rows_chunk(k, 0)) = make_uint4(0u, 0u, pm.x, pm.y);
-            *reinterpret_cast<uint4 *>(ep + rows_chunk(k, 1)) = pk;
+        for (int k = t; k < OW; k += 32 * NW) {   // warps 0 .. NW-1
+            if (KIND == 1) {
+                const uint4 pk = *reinterpret_cast<const uint4 *>(rp + 16 * k);
+                const uint2 pm = k > 0 ? *reinterpret_cast<const uint2 *>(rp + 16 * k - 8) : make_uint2(0u, 0u);
+                *reinterpret_cast<uint4 *>(ep + rows_chunk<ER>(k, 0)) = make_uint4(0u, 0u, pm.x, pm.y);
+                *reinterpret_cast<uint4 *>(ep + rows_chunk<ER>(k, 1)) = pk;
+            } else {
+                const uint4 pm = k > 0 ? *reinterpret_cast<const uint4 *>(rp + 32 * k - 16) : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 p0 = *reinterpret_cast<const uint4 *>(rp + 32 * k);
+                const uint4 p1 = *reinterpret_cast<const uint4 *>(rp + 32 * k + 16);
+                *reinterpret_cast<uint4 *>(ep + rows_chunk<ER>(k, 0)) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(ep + rows_chunk<ER>(k, 1)) = pm;
+                *reinterpret_cast<uint4 *>(ep + rows_chunk<ER>(k, 2)) = p0;
+                *reinterpret_cast<uint4 *>(ep + rows_chunk<ER>(k, 3)) = p1;
+            }
         }
     };
 
-    if (warp == 8)
+    if (warp == NW)
         for (int s = 0; s < D && s < nsteps; ++s) issue_loads(s);
     ptx::tc_fence_before();
     __syncthreads();
@@ -683,12 +712,13 @@ __global__ void __launch_bounds__(kStemRowsThreads) stem_tc_bf16_rows_kernel(con
     const int q = warp & 3, h = (warp >> 2) & 1;   // TMEM lane quadrant, column half (8 h .. 8 h + 7)
 #pragma unroll
     for (int c = 0; c < 8; ++c) bh[c] = sBias[8 * h + c];
-    const uint64_t d32 = ptx::smem_desc(0u, 16u, 256u, 6u);   // 32-byte rows, 8-row groups 256 B apart
-    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(16 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    // ER-byte rows, 8-row groups 8 ER apart; swizzle code 6 (32 B) or 4 (64 B).
+    const uint64_t dsw = ptx::smem_desc(0u, 16u, 8u * ER, ER == 32 ? 6u : 4u);
+    constexpr uint32_t fmt = KIND == 3 ? 2u : 1u;   // TF32 : BF16 operands
+    const uint32_t idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(16 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
     const int bufcols = g.mtiles * 16;
-    __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(a.y);
     bool failed = false;
-    const bool issuer = warp == 8;
+    const bool issuer = warp == NW;
     int issued = D < nsteps ? D : nsteps;   // steps whose loads have been issued (thread 0, then warp 8)
     int stop = nsteps;                      // loads of steps >= stop may still be in flight at exit
 #pragma unroll 1
@@ -719,11 +749,16 @@ __global__ void __launch_bounds__(kStemRowsThreads) stem_tc_bf16_rows_kernel(con
                 const uint32_t d0 = tmem + (uint32_t)((s & 1) * bufcols);
                 for (int r = r0; r < 3; ++r) {
                     const int es = ((2 * s - 1 + r) % NE + NE) % NE;
-                    const uint64_t bd = d32 | (uint64_t)(((sB_u32 + (uint32_t)(r * 512)) & 0x3FFFFu) >> 4);
+                    const uint64_t bd = dsw | (uint64_t)(((sB_u32 + (uint32_t)(r * 16 * ER)) & 0x3FFFFu) >> 4);
                     for (int m = 0; m < g.mtiles; ++m) {
                         const uint64_t ad =
-                            d32 | (uint64_t)(((sE_u32 + (uint32_t)(es * g.eslot + m * 4096)) & 0x3FFFFu) >> 4);
-                        ptx::mma_f16(d0 + (uint32_t)(m * 16), ad, bd, idesc, r > r0 ? 1u : 0u);
+                            dsw | (uint64_t)(((sE_u32 + (uint32_t)(es * g.eslot + m * TILE)) & 0x3FFFFu) >> 4);
+                        if (KIND == 1) {
+                            ptx::mma_f16(d0 + (uint32_t)(m * 16), ad, bd, idesc, r > r0 ? 1u : 0u);
+                        } else {   // two K=8 slices, 32 bytes apart
+                            ptx::mma_tf32(d0 + (uint32_t)(m * 16), ad, bd, idesc, r > r0 ? 1u : 0u);
+                            ptx::mma_tf32(d0 + (uint32_t)(m * 16), ad + 2u, bd + 2u, idesc, 1u);
+                        }
                     }
                 }
                 ptx::mma_commit(mma_bar(s & 1));
@@ -746,7 +781,7 @@ __global__ void __launch_bounds__(kStemRowsThreads) stem_tc_bf16_rows_kernel(con
         }
         ptx::tc_fence_after();
         // Epilogue of output row R0 + j: this warp's 32 TMEM lanes of each
-        // M tile, output channels 8 h .. 8 h + 7 (16 bytes per pixel).
+        // M tile, output channels 8 h .. 8 h + 7.
         const size_t pix0 = (size_t)(R0 + j) * OW;
         const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((j & 1) * bufcols + 8 * h);
         uint32_t v[kStemRowsMaxMtiles][8];
@@ -758,14 +793,22 @@ __global__ void __launch_bounds__(kStemRowsThreads) stem_tc_bf16_rows_kernel(con
         for (int m = 0; m < kStemRowsMaxMtiles; ++m) {
             const int k = m * 128 + 32 * q + lane;
             if (m < g.mtiles && k < OW) {
-                uint32_t o[4];
+                float o[8];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float h0 = fmaf(__uint_as_float(v[m][2 * c]), 0.5f, bh[2 * c]);
-                    const float h1 = fmaf(__uint_as_float(v[m][2 * c + 1]), 0.5f, bh[2 * c + 1]);
-                    o[c] = SILU ? cvt_bf16x2(silu_tanh(h0), silu_tanh(h1)) : cvt_bf16x2(h0 + h0, h1 + h1);
+                for (int c = 0; c < 8; ++c) {
+                    const float hv = fmaf(__uint_as_float(v[m][c]), 0.5f, bh[c]);
+                    o[c] = SILU ? silu_tanh(hv) : hv + hv;
                 }
-                *reinterpret_cast<uint4 *>(y + (pix0 + (size_t)k) * 16 + 8 * h) = make_uint4(o[0], o[1], o[2], o[3]);
+                const size_t off = (pix0 + (size_t)k) * 16 + 8 * h;
+                if (KIND == 1) {
+                    *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.y) + off) =
+                        make_uint4(cvt_bf16x2(o[0], o[1]), cvt_bf16x2(o[2], o[3]), cvt_bf16x2(o[4], o[5]),
+                                   cvt_bf16x2(o[6], o[7]));
+                } else {
+                    float4 *yp = reinterpret_cast<float4 *>(static_cast<float *>(a.y) + off);
+                    yp[0] = make_float4(o[0], o[1], o[2], o[3]);
+                    yp[1] = make_float4(o[4], o[5], o[6], o[7]);
+                }
             }
         }
     }
@@ -1229,30 +1272,37 @@ cudaError_t launch_stem_tc(const StemLaunch &L, cudaStream_t s) {
     g.n_tiles = (int)((total + 127) / 128);
     g.div_ohw = make_fastdiv((uint32_t)(L.OH * L.OW));
     g.div_ow = make_fastdiv((uint32_t)L.OW);
-    if (stem_s2_kernel_applies(L.kind, L.KS, L.stride, L.pad, L.W, L.Cout, L.out_nhwc, L.residual != nullptr)) {
-        // Input rows as [N][H][nb][bx] bf16 (bx: the largest multiple of 8
-        // dividing 4 W, at most 256): one TMA box {bx, nb, 1, 1} per row.
-        const int row_el = 4 * L.W;
-        int bx = 8;
-        for (int c = 8; c <= 256 && c <= row_el; c += 8)
+    const int rk = L.tf32 ? 3 : L.kind;   // the row kernel's kind: 1 BF16, 3 TF32
+    if (stem_s2_kernel_applies(rk, L.KS, L.stride, L.pad, L.W, L.Cout, L.out_nhwc, L.residual != nullptr)) {
+        // Input rows as [N][H][nb][bx] elements (bx: the largest multiple of
+        // 16 bytes dividing a row, at most 256 elements): one TMA box
+        // {bx, nb, 1, 1} per row.
+        const int esz = rk == 3 ? 4 : 2, px = 4 * esz;
+        const int row_el = 4 * L.W, unit = 16 / esz;
+        int bx = 0;
+        for (int c = unit; c <= 256 && c <= row_el; c += unit)
             if (row_el % c == 0) bx = c;
+        if (bx == 0) return cudaErrorInvalidValue;
         const int nb = row_el / bx;
         if (nb > 256) return cudaErrorInvalidValue;
         const cuuint64_t dims[4] = {(cuuint64_t)bx, (cuuint64_t)nb, (cuuint64_t)L.H, (cuuint64_t)L.N};
-        const cuuint64_t strides[3] = {(cuuint64_t)bx * 2, (cuuint64_t)L.W * 8, (cuuint64_t)L.H * L.W * 8};
+        const cuuint64_t strides[3] = {(cuuint64_t)bx * esz, (cuuint64_t)L.W * px, (cuuint64_t)L.H * L.W * px};
         const cuuint32_t box[4] = {(cuuint32_t)bx, (cuuint32_t)nb, 1u, 1u};
         CUtensorMap tm;
-        if (encode_plain_map(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, L.x, dims, strides, box) != CUDA_SUCCESS)
+        if (encode_plain_map(&tm, rk == 3 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, L.x,
+                             dims, strides, box) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
         StemRowsGeom rg;
         rg.rows = L.N * L.OH;
         rg.mtiles = (L.OW + 127) / 128;
-        rg.eslot = rg.mtiles * 4096;
-        rg.raw = L.W * 8;
-        rg.rawstride = (rg.raw + 255) / 256 * 256;
-        const int smem = stem_rows_smem_bytes(L.W);
+        rg.eslot = rg.mtiles * 128 * 4 * px;
+        rg.raw = L.W * px;
+        rg.rawstride = (rg.raw + 1023) / 1024 * 1024;
+        const int smem = stem_rows_smem_bytes(rk, L.W);
         const int grid = std::min(rg.rows, L.grid);   // the plan's CTAs, one band of output rows each
-        auto kern = L.act != CBS_ACT_IDENTITY ? stem_tc_bf16_rows_kernel<true> : stem_tc_bf16_rows_kernel<false>;
+        const bool silu = L.act != CBS_ACT_IDENTITY;
+        auto kern = rk == 3 ? (silu ? stem_tc_rows_kernel<3, true> : stem_tc_rows_kernel<3, false>)
+                            : (silu ? stem_tc_rows_kernel<1, true> : stem_tc_rows_kernel<1, false>);
         const cudaError_t e = set_max_dyn_smem(kern, smem);
         if (e != cudaSuccess) return e;
         return launch_kernel(kern, grid, kStemRowsThreads, (size_t)smem, s, tm, L, rg, status);

@@ -125,6 +125,7 @@ def pair_stem_kernel(spec, out_layout):
             and out_layout == B.CBS_NHWC)
 
 
+@pytest.mark.parametrize("prec", ["bf16", "tf32"])
 @pytest.mark.parametrize("act", [B.CBS_ACT_SILU, B.CBS_ACT_IDENTITY])
 @pytest.mark.parametrize("shape", [
     (1, 3, 16, 3, 2, 2, 2),        # one output pixel: one pair of tiles, the second empty
@@ -134,17 +135,19 @@ def pair_stem_kernel(spec, out_layout):
     (2, 3, 16, 3, 2, 640, 640),    # the detector's width: three M tiles per output row, the last ragged
     (5, 3, 16, 3, 2, 9, 200),      # bands that cross images (output row 0 inside a band)
 ])
-def test_stem_pair_kernel(cuda_lib, act, shape):
-    """The BF16 stem's row kernel (TMA input rows, rewritten in shared memory
-    as MMA operand rows) against the oracle, with and without SiLU."""
+def test_stem_pair_kernel(cuda_lib, prec, act, shape):
+    """The BF16 and TF32 stems' row kernel (TMA input rows, rewritten in
+    shared memory as MMA operand rows) against the oracle, with and without
+    SiLU."""
     n, c_in, c_out, k, stride, h, w = shape
     spec = wl.LayerSpec(c_in, c_out, k, stride, h, w)
     assert pair_stem_kernel(spec, B.CBS_NHWC)
     x, p = wl.layer_inputs(spec, n, layer_index=4)
-    y, layer = run_tc(spec, x, p, B.CBS_BF16, activation=act)
-    assert layer.plan.variant == B.CBS_VARIANT_STEM
-    assert layer.plan.grid_ctas == min(n * spec.oh, layer.desc.num_sms * 2)
-    check_tc("bf16", y, tc_refs("bf16", x, p, spec.stride, spec.pad, act=act), (shape, act))
+    y, layer = run_tc(spec, x, p, PRECS[prec], activation=act)
+    assert layer.plan.variant == B.CBS_VARIANT_STEM and layer.plan.threads == 288
+    ctas = 2 if prec == "bf16" else 1   # the TF32 rows take twice the shared memory
+    assert layer.plan.grid_ctas == min(n * spec.oh, layer.desc.num_sms * ctas)
+    check_tc(prec, y, tc_refs(prec, x, p, spec.stride, spec.pad, act=act), (shape, act))
 
 
 @pytest.mark.parametrize("prec", ["bf16", "tf32"])
@@ -319,12 +322,16 @@ def test_split_k_with_residual_and_two_inputs(cuda_lib):
 ])
 def test_tensor_core_stem_tf32(cuda_lib, out_layout, shape):
     """TF32 layers with at most 4 input channels and k <= 3 run on the TF32
-    tensor-core stem (taps straight into 32-byte-swizzled K slices)."""
+    tensor-core stems (taps straight into 32-byte-swizzled K slices, or for
+    the detector's 3x3 s2 16-channel NHWC case the row kernel)."""
     n, c_in, c_out, k, stride, h, w = shape
     spec = wl.LayerSpec(c_in, c_out, k, stride, h, w)
     x, p = wl.layer_inputs(spec, n, layer_index=5)
     y, layer = run_tc(spec, x, p, B.CBS_TF32, out_layout=out_layout)
     pl = layer.plan
-    assert pl.variant == B.CBS_VARIANT_STEM and pl.block_m == 128 and pl.threads == 256
-    assert pl.grid_ctas == min(pl.m_tiles, 152 * 4)
+    assert pl.variant == B.CBS_VARIANT_STEM and pl.block_m == 128
+    if pair_stem_kernel(spec, out_layout):
+        assert pl.threads == 288 and pl.grid_ctas == min(n * spec.oh, layer.desc.num_sms)   # one CTA per SM
+    else:
+        assert pl.threads == 256 and pl.grid_ctas == min(pl.m_tiles, layer.desc.num_sms * 4)
     check(y, spec, x, p, "tf32", shape)
