@@ -95,6 +95,7 @@ struct TcParams {
     int nblk;                  // staged store blocks per tile row: ceil(BN / cbw)
     int stg_bytes_total;       // bytes of the staging region (8 warps x 4 KB) when st_mode
     int bias_smem;             // 1: the folded bias is copied to shared memory at start
+    int bias_half;             // 1: that copy holds b / 2 (SiLU's tanh form takes h = (z + b) / 2 as one FMA)
     int bias_bytes_smem;       // bytes reserved for it
     // Windowed A (stride 1, pad k/2): tiles are runs of padded positions
     // q = oh * Wp + ow' of one image (ow' < Wp = W + 2 pad; columns ow' >= OW
@@ -162,6 +163,15 @@ __device__ __forceinline__ void activate16(const TcParams &p, const uint32_t (&v
     } else if (PRECISE) {
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) o[jj] = silu_precise(__uint_as_float(v[jj]) + bv[jj]);
+    } else if (p.bias_half) {
+        // bv holds b / 2: h = z / 2 in one FMA (halving is exact).
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            const float h = fmaf(__uint_as_float(v[jj]), 0.5f, bv[jj]);
+            float t;
+            asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+            o[jj] = fmaf(h, t, h);
+        }
     } else {
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) o[jj] = silu_fast(__uint_as_float(v[jj]) + bv[jj]);
@@ -503,7 +513,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (p.bias_smem && warp >= kEpiFirst) {
         // Only the epilogue warps read the bias: they copy it and wait for
         // one another (named barrier 1) while the producers already load.
-        for (int i = threadIdx.x - 32 * kEpiFirst; i < p.C_out; i += 32 * kEpiWarps) bias_sm[i] = p.bias[i];
+        for (int i = threadIdx.x - 32 * kEpiFirst; i < p.C_out; i += 32 * kEpiWarps)
+            bias_sm[i] = p.bias_half ? 0.5f * p.bias[i] : p.bias[i];
         asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
     }
     const uint32_t tmem_base = *tmem_slot;
@@ -2125,6 +2136,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
         P.stg_bytes_total = P.st_mode ? kEpiWarps * kStageBlockBytes : 0;
         P.bias_bytes_smem = tc_bias_smem_bytes(d);
         P.bias_smem = P.bias_bytes_smem > 0;
+        P.bias_half = P.bias_smem && d.activation != CBS_ACT_IDENTITY;
         if (1024 + P.b_region + pl.stages * P.stage_bytes + P.stg_bytes_total + P.bias_bytes_smem +
                 8 * (2 * pl.stages + 6 + 2 * P.SB) + 16 > pl.smem_bytes)
             return fail(CBS_ERR_PLAN_MISMATCH, "plan's shared memory does not hold its stages");
