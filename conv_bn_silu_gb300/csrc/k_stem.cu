@@ -592,6 +592,7 @@ struct StemRowsGeom {
     int eslot;       // bytes of one rewritten input row: mtiles * 128 * (A row bytes)
     int raw;         // bytes of one input row: W * (pixel bytes)
     int rawstride;   // bytes between raw row slots: raw rounded up to 1024 (B stays swizzle-aligned)
+    FastDiv div_oh;  // by OH: output row R = img * OH + oh
 };
 
 // Offset of 16-byte chunk c of A row k in a slot of ER-byte rows, swizzled
@@ -668,7 +669,7 @@ __global__ void __launch_bounds__(kStemRowsThreads) stem_tc_rows_kernel(const __
     // rows 2 oh and 2 oh + 1 into raw slots 2s, 2s + 1 (mod 2D), and at the
     // band's first step row 2 oh - 1 into slot 2D.
     auto issue_loads = [&](int s) {
-        const int R = R0 + s, img = R / a.OH, oh = R - img * a.OH;
+        const int R = R0 + s, img = fast_div(R, g.div_oh), oh = R - img * a.OH;
         const bool with_a = s == 0 && oh > 0;
         const uint32_t bar = raw_bar(s % D);
         if (lane == 0) ptx::mbar_arrive_expect_tx(bar, (uint32_t)((with_a ? 3 : 2) * g.raw));
@@ -728,7 +729,7 @@ __global__ void __launch_bounds__(kStemRowsThreads) stem_tc_rows_kernel(const __
                 failed = true;
                 if (lane == 0) atomicOr(status, 1u);
             } else {
-                const int R = R0 + s, oh = R - (R / a.OH) * a.OH;
+                const int R = R0 + s, oh = R - fast_div(R, g.div_oh) * a.OH;
                 rewrite((2 * s) % (2 * D), (2 * s) % NE);
                 rewrite((2 * s + 1) % (2 * D), (2 * s + 1) % NE);
                 if (s == 0 && oh > 0) rewrite(2 * D, NE - 1);
@@ -743,7 +744,7 @@ __global__ void __launch_bounds__(kStemRowsThreads) stem_tc_rows_kernel(const __
         ptx::tc_fence_after();
         if (issuer) {
             if (s >= nsteps) continue;
-            const int R = R0 + s, oh = R - (R / a.OH) * a.OH;
+            const int R = R0 + s, oh = R - fast_div(R, g.div_oh) * a.OH;
             if (lane == 0) {
                 const int r0 = oh == 0 ? 1 : 0;   // kernel row 0 of output row 0 is padding
                 const uint32_t d0 = tmem + (uint32_t)((s & 1) * bufcols);
@@ -1298,6 +1299,7 @@ cudaError_t launch_stem_tc(const StemLaunch &L, cudaStream_t s) {
         rg.eslot = rg.mtiles * 128 * 4 * px;
         rg.raw = L.W * px;
         rg.rawstride = (rg.raw + 1023) / 1024 * 1024;
+        rg.div_oh = make_fastdiv((uint32_t)L.OH);
         const int smem = stem_rows_smem_bytes(rk, L.W);
         const int grid = std::min(rg.rows, L.grid);   // the plan's CTAs, one band of output rows each
         const bool silu = L.act != CBS_ACT_IDENTITY;
