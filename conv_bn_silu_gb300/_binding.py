@@ -44,14 +44,14 @@ class cbs_layer_desc(ctypes.Structure):
         "n", "c_in", "h", "w", "c_out", "k", "stride", "pad", "in_layout", "out_layout", "prec",
         "force_variant", "force_split_k", "force_block_n", "force_block_m", "out_row_stride",
         "force_k_group", "force_b_resident", "force_window", "activation", "residual", "c_in_b",
-        "zero_point_x", "zero_point_y", "num_sms")]
+        "zero_point_x", "zero_point_y", "num_sms", "force_issuer_split")]
 
 
 class cbs_plan_t(ctypes.Structure):
     _fields_ = [("size", ctypes.c_uint32), ("abi_version", ctypes.c_uint32)] + \
         [(n, ctypes.c_int) for n in (
             "variant", "block_m", "block_n", "block_k", "stages", "split_k", "k_group", "b_resident", "window",
-            "c_in_pad", "k_gemm",
+            "issuer_split", "c_in_pad", "k_gemm",
             "oh", "ow", "out_row_stride", "m_tiles", "n_tiles", "grid_ctas", "threads",
             "smem_bytes")] + \
         [(n, ctypes.c_size_t) for n in (

@@ -70,7 +70,12 @@ def candidates(prec, spec, base):
             yield dict(force_k_group=kg, force_block_n=bn)
     else:
         for bm, kg, br, bn in itertools.product((128, 256), (1, 2, 3, 4), (-1, 1), bns):
-            yield dict(force_block_m=bm, force_k_group=kg, force_b_resident=br, force_block_n=bn)
+            yield dict(force_block_m=bm, force_k_group=kg, force_b_resident=br, force_block_n=bn,
+                       force_issuer_split=-1)
+            if bm == 128 and bn <= 128:
+                # 128-pixel tiles: K stages alternating between the two MMA issuers
+                yield dict(force_block_m=bm, force_k_group=kg, force_b_resident=br, force_block_n=bn,
+                           force_issuer_split=1)
         if spec.stride == 1:
             for bm, br, bn in itertools.product((128, 256), (-1, 1), bns):
                 yield dict(force_block_m=bm, force_b_resident=br, force_block_n=bn, force_window=1)

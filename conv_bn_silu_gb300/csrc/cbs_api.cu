@@ -240,6 +240,7 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
     p.abi_version = CBS_ABI_VERSION;
     p.desc = D;
     p.k_group = 1;
+    p.issuer_split = 1;
     p.oh = (D.h + 2 * D.pad - D.k) / D.stride + 1;
     p.ow = (D.w + 2 * D.pad - D.k) / D.stride + 1;
     const long long M = (long long)D.n * p.oh * p.ow;
@@ -260,7 +261,8 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
         // descriptor that forces a tile field is tuning the CUDA-core kernel.
         const int c_a = D.c_in - D.c_in_b;
         const bool forces_tiles = D.force_split_k > 0 || D.force_block_n > 0 || D.force_block_m > 0 ||
-                                  D.force_k_group > 0 || D.force_b_resident != 0 || D.force_window > 0;
+                                  D.force_k_group > 0 || D.force_b_resident != 0 || D.force_window > 0 ||
+                                  D.force_issuer_split > 0;
         if (variant == CBS_VARIANT_SIMT_FP32 && D.in_layout == CBS_NHWC && c_a % 8 == 0 && D.c_in_b % 8 == 0 &&
             !forces_tiles) {
             variant = CBS_VARIANT_TC_TF32X3;
@@ -277,6 +279,10 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
             return fail(CBS_ERR_INVALID_ARG, "variant %d does not compute precision %d", variant, D.prec);
     }
     p.variant = variant;
+    if (D.force_issuer_split < -1 || D.force_issuer_split > 1)
+        return fail(CBS_ERR_INVALID_ARG, "force_issuer_split %d: -1, 0 or 1", D.force_issuer_split);
+    if (D.force_issuer_split > 0 && variant != CBS_VARIANT_TC_TF32 && variant != CBS_VARIANT_TC_BF16)
+        return fail(CBS_ERR_UNSUPPORTED, "the issuer split belongs to the TF32/BF16 tensor-core variants");
 
     if (D.out_row_stride != 0) {
         if (D.out_layout != CBS_NCHW)

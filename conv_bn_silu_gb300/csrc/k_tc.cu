@@ -84,6 +84,10 @@ struct TcParams {
     uint32_t op_mask;          // operand swizzle mask
     // TF32/BF16 tall tiles, grouped K steps, resident weights
     int mmul;                  // 128-pixel sub-tiles per tile (one A box of 128*mmul rows)
+    int kpar;                  // 2: a 128-pixel tile's stages are split between the two MMA issuers by
+                               //    the parity of the stage count g (with an even ring, each ring slot
+                               //    always goes to the same issuer), each into its own accumulator,
+                               //    added by the epilogue; else 1
     int kg;                    // K steps per stage (divides ksteps)
     int b_res;                 // weights resident for the whole launch
     int bnp;                   // TMEM columns between sub-tile accumulators (power of two >= BN)
@@ -418,6 +422,31 @@ __device__ __forceinline__ void issue_kstep_desc(uint32_t d, uint64_t ad, uint64
     }
 }
 
+// Loads columns c0 .. c0+15 (and c1 .. c1+15 when `two`) of this warp's TMEM
+// lanes.  With the issuer split the tile's sum is spread over two
+// accumulators, `half` columns apart, and the halves are added (two waits
+// instead of one keep a third 16-column array out of the registers).
+__device__ __forceinline__ void tmem_ld_acc(uint32_t t_row, uint32_t c0, uint32_t c1, bool two, bool split2,
+                                            uint32_t half, uint32_t (&v0)[16], uint32_t (&v1)[16]) {
+    ptx::tmem_ld16(t_row + c0, v0);
+    if (two) ptx::tmem_ld16(t_row + c1, v1);
+    if (!split2) {
+        ptx::tmem_ld_wait();
+        return;
+    }
+    uint32_t w[16];
+    ptx::tmem_ld16(t_row + half + c0, w);
+    ptx::tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v0[i] = __float_as_uint(__uint_as_float(v0[i]) + __uint_as_float(w[i]));
+    if (two) {
+        ptx::tmem_ld16(t_row + half + c1, w);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v1[i] = __float_as_uint(__uint_as_float(v1[i]) + __uint_as_float(w[i]));
+    }
+}
+
 __device__ __forceinline__ void abort_now(const TcParams &p, int *abort_flag) {
     atomicOr(p.status, 1u);
     *(volatile int *)abort_flag = 1;
@@ -476,11 +505,13 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // issues an MMA only every ~110-160 cycles, against 48-65 cycles of
     // tensor-pipe time for N <= 128, and two issuers overlap their waits.
     // Every barrier the MMAs release counts one commit per issuer.
-    const uint32_t n_iss = (uint32_t)p.mmul;
+    // With kpar = 2 each stage is read by one issuer (the one of its count's
+    // parity); otherwise by all mmul issuers.
+    const uint32_t n_iss = (uint32_t)(p.mmul * p.kpar);
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(full_bar(s), 1);
-            ptx::mbar_init(empty_bar(s), n_iss);
+            ptx::mbar_init(empty_bar(s), (uint32_t)p.mmul);
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(accf_bar(a), n_iss);
@@ -655,11 +686,13 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
         }
     } else if (warp < kMmaWarp + kMmaWarps) {
-        const int mi = warp - kMmaWarp;   // the sub-tile whose MMAs this warp issues
-        if (lane == 0 && mi < p.mmul) {
+        // The sub-tile whose MMAs this warp issues, or with kpar = 2 the
+        // parity of the stages it takes.
+        const int mi = warp - kMmaWarp;
+        if (lane == 0 && mi < p.mmul * p.kpar) {
             const uint32_t sbo = 8u * p.RB;
             const int kslices = p.RB / 32;
-            const uint32_t sub_bytes = (uint32_t)(kBM * p.RB);   // one 128-row sub-tile of an A box
+            const uint32_t sub_bytes = p.kpar == 2 ? 0u : (uint32_t)(kBM * p.RB);   // one 128-row sub-tile of an A box
             const uint64_t dhi = ptx::smem_desc(0u, 16u, sbo, p.swz);
             bool ok = true;
             if (p.b_res && blockIdx.x < num_tiles && !ptx::mbar_wait_bounded(bfull_bar, 0, kWaitLimitNs)) {
@@ -743,7 +776,13 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     ptx::mma_commit(accf_bar(acc));
                     continue;
                 }
+                bool fresh = true;   // this issuer's accumulator not yet written for this tile
                 for (int st = st0; st < st1; ++st, ++g) {
+                    // kpar = 2: the stage belongs to the issuer of g's parity.  The
+                    // ring depth is even, so slot g % S always goes to the same
+                    // issuer, which takes its uses in order: its parity waits
+                    // never see a slot two phases behind.
+                    if (p.kpar == 2 && (g & 1) != mi) continue;
                     const int s = g % S, us = g / S;
                     if (!ptx::mbar_wait_bounded(full_bar(s), us & 1, kWaitLimitNs)) {
                         abort_now(p, abort_flag);
@@ -760,7 +799,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     uint64_t bd = dhi | (uint64_t)((b0 & 0x3FFFFu) >> 4);
                     const uint64_t a_step = (uint64_t)(p.a_box_bytes >> 4), b_step = (uint64_t)(p.b_tile_stride >> 4);
                     for (int kk = 0; kk < p.kg; ++kk, ad += a_step, bd += b_step)
-                        issue_kstep_desc<KIND>(d_tmem, ad, bd, p.idesc, kslices, st == st0 && kk == 0);
+                        issue_kstep_desc<KIND>(d_tmem, ad, bd, p.idesc, kslices, fresh && kk == 0);
+                    fresh = false;
                     ptx::mma_commit(empty_bar(s));
                 }
                 if (!ok) break;
@@ -877,9 +917,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     for (int c = 0; c < bcols; c += 32) {
                         uint32_t v0[16], v1[16];
                         const bool two = c + 16 < bcols;
-                        ptx::tmem_ld16(t_row + (uint32_t)(bc0 + c), v0);
-                        if (two) ptx::tmem_ld16(t_row + (uint32_t)(bc0 + c + 16), v1);
-                        ptx::tmem_ld_wait();
+                        tmem_ld_acc(t_row, (uint32_t)(bc0 + c), (uint32_t)(bc0 + c + 16), two, p.kpar == 2,
+                                    (uint32_t)p.bnp, v0, v1);
                         float bv[16];
                         load_bias16(p, bias, n0 + bc0 + c, bv);
                         stage16<KIND>(p, blk, lane, c, bv, v0, m, n0 + bc0 + c);
@@ -900,9 +939,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     // Two loads, one wait: 32 columns in flight per thread.
                     uint32_t v0[16], v1[16];
                     const bool two = c0 + cstep < p.BN;
-                    ptx::tmem_ld16(t_row + (uint32_t)c0, v0);
-                    if (two) ptx::tmem_ld16(t_row + (uint32_t)(c0 + cstep), v1);
-                    ptx::tmem_ld_wait();
+                    tmem_ld_acc(t_row, (uint32_t)c0, (uint32_t)(c0 + cstep), two, p.kpar == 2, (uint32_t)p.bnp, v0, v1);
                     if (valid) {
                         if (n0 + c0 < p.C_out) epi_store16<KIND>(p, bias, m, img, oh, ow, n0 + c0, v0);
                         if (two && n0 + c0 + cstep < p.C_out)
@@ -1647,6 +1684,15 @@ double tc_pipe_clk(int N, bool tf32) {
     return c > 48.0 ? c : 48.0;
 }
 
+// Two MMA-issuing threads on one 128-pixel tile (issuer split): each takes
+// the stages of one parity of the CTA's running stage count, into an
+// accumulator of its own.  Needs at least two stages per tile (so each
+// accumulator gets one) and both accumulators of both TMEM buffers within
+// the 512 columns.  The ring depth is made even where it is used.
+bool tc_issuer_split_fits(int mmul, int win, int stages_per_tile, int BN) {
+    return mmul == 1 && !win && stages_per_tile >= 2 && 4 * next_pow2(BN) <= 512;
+}
+
 double tc_tile_mma_clk(double n_mma, double waits, int mmul, int N, bool tf32) {
     const double issue = n_mma * kClkPerMmaIssue + waits * kClkPerStageWait;
     const double pipe = n_mma * mmul * tc_pipe_clk(N, tf32);
@@ -1689,7 +1735,7 @@ bool tc_window_geometry(const cbs_layer_desc &d, int oh, int RB, int tile_m, TcW
 }
 
 struct TcConfig {
-    int BN, mmul, b_res, kg, stages, nprod, st_mode, extra_bytes, win, SB;
+    int BN, mmul, b_res, kg, stages, nprod, st_mode, extra_bytes, win, SB, kpar;
     TcWindow wg;
     int m_tiles, n_tiles, grid;
     int stage_bytes, b_region, b_tile_stride, a_box_bytes;
@@ -1752,9 +1798,10 @@ bool tc_config_window(const cbs_layer_desc &d, int oh, int RB, int ksteps, bool 
 
 // Shared-memory layout and cost of one configuration (false if it does not fit).
 bool tc_config(const cbs_layer_desc &d, long long M, int oh, int RB, int ksteps, bool tf32, int BN, int mmul,
-               int b_res, int kg, int win, TcConfig &c) {
-    c.BN = BN; c.mmul = mmul; c.b_res = b_res; c.kg = kg; c.win = win; c.SB = 0;
-    if (win) return tc_config_window(d, oh, RB, ksteps, tf32, c);
+               int b_res, int kg, int win, int kpar, TcConfig &c) {
+    c.BN = BN; c.mmul = mmul; c.b_res = b_res; c.kg = kg; c.win = win; c.SB = 0; c.kpar = kpar;
+    if (kpar == 2 && !tc_issuer_split_fits(mmul, win, ksteps / kg, BN)) return false;
+    if (win) return kpar == 1 && tc_config_window(d, oh, RB, ksteps, tf32, c);
     if (kg * (b_res ? 1 : 2) > 32) return false;   // one issuing lane per box of a stage
     c.a_box_bytes = kBM * mmul * RB;
     const int b_bytes = BN * RB;
@@ -1770,6 +1817,7 @@ bool tc_config(const cbs_layer_desc &d, long long M, int oh, int RB, int ksteps,
     if (cap > 16) cap = 16;
     if (cap < 2) return false;
     c.stages = cap >= 4 ? cap - cap % 4 : cap;
+    if (kpar == 2) c.stages -= c.stages & 1;   // even: each ring slot then always feeds the same issuer
     c.nprod = tc_producers(c.stages);
     const long long tiles = (long long)c.m_tiles * c.n_tiles;
     if (b_res && c.n_tiles > 1) {
@@ -1782,7 +1830,10 @@ bool tc_config(const cbs_layer_desc &d, long long M, int oh, int RB, int ksteps,
     }
     const double tpc = (double)((tiles + c.grid - 1) / c.grid);   // tiles of the busiest CTA
     const int kslices = RB / 32;
-    const double mma = tpc * tc_tile_mma_clk((double)ksteps * kslices, (double)(ksteps / kg), mmul, BN, tf32);
+    // With the issuer split each issuer takes half the MMAs and waits; the
+    // tensor pipe still runs all of them.
+    const double mma = tpc * tc_tile_mma_clk((double)ksteps * kslices / kpar, (double)(ksteps / kg) / kpar,
+                                             mmul * kpar, BN, tf32);
     const double boxes = tpc * ksteps * (b_res ? 1.0 : 2.0) + (b_res ? (double)ksteps : 0.0);
     const double bytes = tpc * ksteps * (double)(c.a_box_bytes + (b_res ? 0 : b_bytes)) + (b_res ? (double)ksteps * b_bytes : 0.0);
     // Boxes of one stage go out from parallel lanes; the SM's TMA engine
@@ -1792,7 +1843,8 @@ bool tc_config(const cbs_layer_desc &d, long long M, int oh, int RB, int ksteps,
     // Epilogue: one thread per pixel and 16-column group; eight warps cover
     // two sub-tiles, or split one sub-tile's columns.
     const double vals = mmul == 2 ? (double)BN : 0.5 * BN;
-    const double epi = tpc * (250.0 + (c.st_mode ? 25.0 : 45.0) * vals);
+    // (the issuer split reads and adds a second accumulator)
+    const double epi = tpc * (250.0 + ((c.st_mode ? 25.0 : 45.0) + (kpar == 2 ? 10.0 : 0.0)) * vals);
     double cyc = mma > tma ? mma : tma;
     if (epi > cyc) cyc = epi;
     // Pipeline fill: the first stage's loads (and a resident weight tile)
@@ -1999,15 +2051,29 @@ cbs_status plan_tc(cbs_plan_t &p) {
                         if (d.force_split_k > 1 && d.force_k_group <= 0 && ksteps / kg < d.force_split_k) continue;
                         if (win && kg > 1) break;                  // a window stage is one channel block
                         if (d.force_k_group > 0 && kg != d.force_k_group) continue;
-                        TcConfig c;
-                        if (!tc_config(d, M, p.oh, RB, ksteps, tf32, BN, mmul, b_res, kg, win, c)) continue;
-                        if (c.cycles < best.cycles * 0.99) best = c;
+                        for (int kpar = 1; kpar <= 2; ++kpar) {
+                            // The issuer split on request only: measured on the
+                            // list layers at batch 16 it beat the best one-issuer
+                            // plan on 2 of the 19 it applies to (by 3-4%) and lost
+                            // up to 64% on the others: 256-pixel tiles share each
+                            // weight box between two sub-tiles, the split does not.
+                            if ((d.force_issuer_split > 0) != (kpar == 2)) continue;
+                            if (kpar == 2 && d.force_split_k > 1) continue;   // split-K keeps one issuer per tile
+                            TcConfig c;
+                            if (!tc_config(d, M, p.oh, RB, ksteps, tf32, BN, mmul, b_res, kg, win, kpar, c)) continue;
+                            if (c.cycles < best.cycles * 0.99) best = c;
+                        }
                     }
                 }
             }
         }
     }
-    if (best.cycles >= 1e299) return fail(CBS_ERR_UNSUPPORTED, "no tensor-core tile configuration fits shared memory");
+    if (best.cycles >= 1e299) {
+        if (d.force_issuer_split > 0)
+            return fail(CBS_ERR_UNSUPPORTED, "no configuration takes the issuer split (block_m 128, im2col A, no "
+                                             "split-K, two or more stages per tile, N tile <= 128)");
+        return fail(CBS_ERR_UNSUPPORTED, "no tensor-core tile configuration fits shared memory");
+    }
     // Split-K on request only.  A launch with fewer tiles than SMs leaves
     // SMs idle, and splitting K over S parts balances the MMAs (e.g. 100
     // tiles of 256x128 over 152 SMs: 288 -> 192 MMAs on the busiest SM at
@@ -2036,6 +2102,7 @@ cbs_status plan_tc(cbs_plan_t &p) {
     p.k_group = best.win ? best.SB : best.kg;   // windowed plans: weight-ring slots
     p.b_resident = best.b_res;
     p.window = best.win;
+    p.issuer_split = best.kpar;
     p.stages = best.stages;
     p.m_tiles = best.m_tiles;
     p.n_tiles = best.n_tiles;
@@ -2104,6 +2171,11 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     if (P.kg < 1 || P.ksteps % P.kg) return fail(CBS_ERR_PLAN_MISMATCH, "k_group %d", pl.k_group);
     if (P.win && !P.b_res && (P.SB < 1 || P.SB > 32)) return fail(CBS_ERR_PLAN_MISMATCH, "weight ring %d", P.SB);
     P.bnp = next_pow2(BN);
+    P.kpar = staged ? 1 : pl.issuer_split;
+    if (P.kpar != 1 && P.kpar != 2) return fail(CBS_ERR_PLAN_MISMATCH, "issuer_split %d", pl.issuer_split);
+    if (P.kpar == 2 && (staged || P.split > 1 || P.stages % 2 || !tc_issuer_split_fits(mmul, P.win, P.ksteps / P.kg, BN)))
+        return fail(CBS_ERR_PLAN_MISMATCH, "issuer split with block_m %d, window %d, split-K %d, %d stages, N tile %d",
+                    pl.block_m, P.win, P.split, P.stages, BN);
     P.a_bytes = kBM * RB; P.b_bytes = BN * RB;
     P.a_box_bytes = kBM * mmul * RB;
     P.b_tile_stride = round_up(P.b_bytes, 1024);
@@ -2176,7 +2248,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     // sit at power-of-two column offsets inside a buffer.
     P.chunk_stride = next_pow2(BN);
     {
-        const int cols = staged ? P.nchunks * P.chunk_stride : mmul * P.bnp;
+        const int cols = staged ? P.nchunks * P.chunk_stride : mmul * P.kpar * P.bnp;
         P.acc_stride = next_pow2(cols) < 16 ? 16 : next_pow2(cols);
     }
     P.tmem_cols = (uint32_t)(2 * P.acc_stride < 32 ? 32 : 2 * P.acc_stride);

@@ -37,7 +37,7 @@ def make_desc(n, c_in, h, w, c_out, k, stride, pad=None, prec=B.CBS_FP32, in_lay
               out_layout=None, force_variant=-1, force_split_k=0, force_block_n=0,
               force_block_m=0, out_row_stride=0, force_k_group=0, force_b_resident=0,
               force_window=0, activation=B.CBS_ACT_SILU, residual=0, c_in_b=0, zero_point_x=0,
-              zero_point_y=0, num_sms=None) -> B.cbs_layer_desc:
+              zero_point_y=0, num_sms=None, force_issuer_split=0) -> B.cbs_layer_desc:
     """A layer descriptor; num_sms defaults to the current device's SM count."""
     if num_sms is None:
         num_sms = device_sms()
@@ -55,7 +55,8 @@ def make_desc(n, c_in, h, w, c_out, k, stride, pad=None, prec=B.CBS_FP32, in_lay
                         out_row_stride=out_row_stride, force_k_group=force_k_group,
                         force_b_resident=force_b_resident, force_window=force_window,
                         activation=activation, residual=residual, c_in_b=c_in_b, zero_point_x=zero_point_x,
-                        zero_point_y=zero_point_y, num_sms=num_sms).items():
+                        zero_point_y=zero_point_y, num_sms=num_sms,
+                        force_issuer_split=force_issuer_split).items():
         setattr(d, name, int(v))
     return d
 

@@ -21,7 +21,7 @@ TABLE_PATH = os.path.join(HERE, "tuned_plans.json")
 
 # Descriptor fields a table entry may set.
 FORCE_FIELDS = ("force_variant", "force_split_k", "force_block_n", "force_block_m", "force_k_group",
-                "force_b_resident", "force_window")
+                "force_b_resident", "force_window", "force_issuer_split")
 _DEFAULTS = {"force_variant": -1}
 
 _table = None

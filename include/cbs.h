@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define CBS_ABI_VERSION 4
+#define CBS_ABI_VERSION 5
 
 /* Exported symbols (the library is built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -125,6 +125,13 @@ typedef struct cbs_layer_desc {
     int num_sms;         /* SMs of the device the layer will run on (cudaDevAttrMultiProcessorCount):
                             grids, waves and split-K are sized for it.  0 = 152, the GB300's count.
                             cbs_plan stays a pure host function: it never queries the device. */
+    int force_issuer_split; /* TF32/BF16: 1 = the K stages of each 128-pixel tile alternate
+                            between the kernel's two MMA-issuing threads, each summing into an
+                            accumulator of its own that the epilogue adds (needs block_m 128,
+                            im2col A, no split-K, at least two stages per tile and an N tile of
+                            at most 128); 0 or -1 = one issuing thread per 128-pixel tile.  On
+                            request only: measured slower than the planner's choice on most
+                            layers.  Must be 0 or -1 for the other variants. */
 } cbs_layer_desc;
 
 /* A plan: plain data, owned by the caller, filled by cbs_plan. */
@@ -143,6 +150,8 @@ typedef struct cbs_plan_t {
                                window once per channel block and every filter tap reads a
                                shifted view of it (block_m positions of the padded grid
                                oh * (W + 2 pad) + ow'); 0 = one im2col box per tap */
+    int issuer_split;       /* TF32/BF16: 2 = each 128-pixel tile's K stages alternate between
+                               two MMA-issuing threads (see force_issuer_split); else 1 */
     int c_in_pad;           /* channels per input pixel as stored (NHWC tensor-core variants
                                pad C_in to a 16-byte multiple; SIMT: = c_in) */
     int k_gemm;             /* GEMM K = k*k*c_in_pad: length of one packed weight row */

@@ -28,10 +28,10 @@ def test_library_exports_every_declared_symbol(cuda_lib):
 
 
 def test_abi_version_and_struct_sizes(cuda_lib):
-    assert B.cbs_abi_version() == 4
+    assert B.cbs_abi_version() == 5
     plan = B.cbs_plan(make_desc(1, 16, 40, 40, 32, 3, 1))
     assert plan.size == ctypes.sizeof(B.cbs_plan_t)
-    assert plan.abi_version == 4
+    assert plan.abi_version == 5
 
 
 def test_status_strings(cuda_lib):
@@ -302,3 +302,68 @@ def test_plan_follows_the_sm_count(cuda_lib, prec, n):
     with pytest.raises(B.CbsError) as e:
         B.cbs_plan(make_desc(1, 16, 40, 40, 32, 3, 1, num_sms=-1))
     assert e.value.status == B.CBS_ERR_INVALID_ARG
+
+
+def _ksteps(plan):
+    """K steps of a TF32/BF16 plan: block_k channels per step, every tap."""
+    return plan.desc.k * plan.desc.k * (plan.c_in_pad // plan.block_k)
+
+
+@pytest.mark.parametrize("prec", [B.CBS_BF16, B.CBS_TF32])
+def test_issuer_split_plan_invariants(cuda_lib, prec):
+    """Every plan that splits a tile's K stages between the two MMA issuers
+    has 128-pixel tiles, im2col A, one K part, an even pipeline depth (each
+    ring slot then always feeds the same issuer), two or more stages per tile
+    and an N tile of at most 128 (two accumulators per TMEM buffer)."""
+    shapes = list(wl.LAYER_LIST[1:]) + [cl.spec for cl in wl.chain_layers(sppf=True)]
+    seen = 0
+    for s in shapes:
+        for n in (1, 16):
+            for kw in ({}, {"force_issuer_split": 1}, {"force_block_m": 128}, {"force_k_group": 3}):
+                try:
+                    pl = B.cbs_plan(make_desc(n, s.c_in, s.h, s.width, s.c_out, s.k, s.stride, prec=prec, **kw))
+                except B.CbsError as e:
+                    assert e.status == B.CBS_ERR_UNSUPPORTED and kw, (s, kw)
+                    continue
+                if pl.variant == B.CBS_VARIANT_STEM:
+                    assert pl.issuer_split == 1
+                    continue
+                assert pl.issuer_split in (1, 2)
+                if kw.get("force_issuer_split") == 1:
+                    assert pl.issuer_split == 2, (s, n)
+                else:
+                    assert pl.issuer_split == 1, (s, n, kw)     # on request only
+                if pl.issuer_split == 2:
+                    seen += 1
+                    assert pl.block_m == 128 and pl.window == 0 and pl.split_k == 1, (s, n, kw)
+                    assert pl.stages % 2 == 0 and pl.stages >= 2, (s, n, kw)
+                    assert _ksteps(pl) // pl.k_group >= 2 and pl.block_n <= 128, (s, n, kw)
+    assert seen > 0
+
+
+def test_issuer_split_plan_rules(cuda_lib):
+    """force_issuer_split: 0 and -1 keep one issuer per 128-pixel tile; 1
+    where no configuration can take it, or on another variant, is refused;
+    other values are invalid."""
+    d = dict(n=16, c_in=64, h=40, w=40, c_out=128, k=3, stride=1, prec=B.CBS_BF16)
+    for v in (0, -1):
+        assert B.cbs_plan(make_desc(force_issuer_split=v, **d)).issuer_split == 1
+    forced = B.cbs_plan(make_desc(force_issuer_split=1, **d))
+    assert forced.issuer_split == 2 and forced.block_m == 128 and forced.stages % 2 == 0
+    refused = [
+        dict(d, force_block_m=256),                                  # 256-pixel tiles have two sub-tile issuers
+        dict(d, force_window=1),                                     # windowed A
+        dict(d, force_split_k=2),                                    # split-K
+        dict(d, c_in=32, k=1, force_k_group=1, prec=B.CBS_BF16),     # one K step: one stage per tile
+        dict(d, c_out=256, force_block_n=256),                       # N tile over 128
+        dict(d, prec=B.CBS_INT8),                                    # another variant
+        dict(n=1, c_in=64, h=40, w=40, c_out=128, k=3, stride=1, prec=B.CBS_FP32),
+    ]
+    for kw in refused:
+        with pytest.raises(B.CbsError) as e:
+            B.cbs_plan(make_desc(force_issuer_split=1, **kw))
+        assert e.value.status == B.CBS_ERR_UNSUPPORTED, kw
+    for v in (2, -2):
+        with pytest.raises(B.CbsError) as e:
+            B.cbs_plan(make_desc(force_issuer_split=v, **d))
+        assert e.value.status == B.CBS_ERR_INVALID_ARG

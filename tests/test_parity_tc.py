@@ -265,6 +265,62 @@ def test_windowed_a(cuda_lib, prec, bm, bres, shape):
     check(y, spec, x, p, prec, (shape, bm, pl.b_resident, pl.block_n, pl.stages, pl.k_group))
 
 
+ISSUER_SPLIT_SHAPES = [  # (n, c_in, c_out, k, stride, h, K steps per stage, resident weights)
+    (2, 32, 64, 3, 1, 20, 3, -1),     # 3 stages per tile (odd): a tile's first stage alternates issuers
+    (2, 32, 64, 3, 1, 20, 3, 1),      # the same with resident weights
+    (8, 32, 64, 3, 1, 80, 3, -1),     # 400 tiles: up to three per CTA, both TMEM buffers reused
+    (3, 32, 48, 3, 2, 17, 1, -1),     # 9 stages, stride 2, N tile 48, ragged pixels
+    (2, 32, 200, 3, 1, 9, 1, 1),      # two N tiles, the second ragged; resident weights
+    (4, 128, 96, 1, 1, 13, 1, -1),    # 1x1, ragged pixel count
+    (1, 64, 40, 3, 2, 17, 1, -1),     # ragged output channels
+]
+
+
+@pytest.mark.parametrize("prec", ["bf16", "tf32"])
+@pytest.mark.parametrize("shape", ISSUER_SPLIT_SHAPES)
+def test_issuer_split(cuda_lib, prec, shape):
+    """128-pixel tiles whose K stages alternate between the two MMA issuers
+    (each into its own accumulator, added by the epilogue; on request)
+    against the oracle, beside the same plan with one issuer; repeated calls
+    agree."""
+    n, c_in, c_out, k, stride, h, kg, bres = shape
+    spec = wl.LayerSpec(c_in, c_out, k, stride, h)
+    x, p = wl.layer_inputs(spec, n, layer_index=19)
+    kw = dict(force_block_m=128, force_k_group=kg, force_b_resident=bres)
+    y, layer = run_tc(spec, x, p, PRECS[prec], force_issuer_split=1, **kw)
+    pl = layer.plan
+    ksteps = k * k * (pl.c_in_pad // pl.block_k)
+    assert pl.issuer_split == 2 and pl.block_m == 128 and pl.stages % 2 == 0, (pl.issuer_split, pl.stages)
+    assert (pl.k_group, pl.b_resident) == (kg, 1 if bres > 0 else 0)
+    if shape[:6] == (2, 32, 64, 3, 1, 20):
+        assert (ksteps // kg) % 2 == 1     # the odd stage count is what the case is for
+    check(y, spec, x, p, prec, (shape, pl.block_n, pl.stages, ksteps // kg))
+    y_again, _ = run_tc(spec, x, p, PRECS[prec], force_issuer_split=1, **kw)
+    assert np.array_equal(y, y_again)
+    y_one, one = run_tc(spec, x, p, PRECS[prec], force_issuer_split=-1, **kw)
+    assert one.plan.issuer_split == 1
+    check(y_one, spec, x, p, prec, (shape, "one issuer"))
+
+
+def test_issuer_split_with_residual_two_inputs_and_identity(cuda_lib):
+    """The issuer split beside the residual add, the channel concatenation
+    and the identity activation."""
+    spec = wl.LayerSpec(96, 64, 3, 1, 14)
+    x, p = wl.layer_inputs(spec, 2, layer_index=20)
+    r = np.random.default_rng(5).standard_normal((2, 64, 14, 14)).astype(np.float32)
+    for act in (B.CBS_ACT_SILU, B.CBS_ACT_IDENTITY):
+        desc = make_desc(2, 96, 14, 14, 64, 3, 1, prec=B.CBS_BF16, force_issuer_split=1, residual=1, c_in_b=32,
+                         activation=act)
+        layer = FusedConvBnSilu(desc, p.w, p.gamma, p.beta, p.mean, p.var, p.eps)
+        assert layer.plan.issuer_split == 2
+        xa, xb = layer.pack_inputs(torch.from_numpy(np.ascontiguousarray(x[:, :64])).cuda(),
+                                   torch.from_numpy(np.ascontiguousarray(x[:, 64:])).cuda())
+        rr = torch.from_numpy(np.ascontiguousarray(r.transpose(0, 2, 3, 1))).cuda().to(torch.bfloat16)
+        y = nhwc_to_nchw(layer(xa, residual=rr, x_b=xb).float().cpu().numpy())
+        rb = torch.from_numpy(r).to(torch.bfloat16).float().numpy()
+        check_tc("bf16", y, tc_refs("bf16", x, p, 1, 1, act=act, residual=rb), act)
+
+
 def test_no_timeout_reported(cuda_lib):
     assert B.cbs_read_device_status(True, torch.cuda.current_stream().cuda_stream) == B.CBS_OK
 
