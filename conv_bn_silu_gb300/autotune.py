@@ -10,6 +10,11 @@ input copies.  A shape gets a table entry when its fastest candidate beats the
 cost-model plan by 3% or more.
 
     python -m conv_bn_silu_gb300.autotune OUT.json [--reps 10]
+
+One shape under given force fields, timed the same way (no table written):
+
+    python -m conv_bn_silu_gb300.autotune --time PREC N C_IN C_OUT K STRIDE H W \
+        [--force FIELD=VALUE ...] [--reps 10]
 """
 from __future__ import annotations
 
@@ -76,7 +81,7 @@ def candidates(prec, spec, base):
                 # 128-pixel tiles: K stages alternating between the two MMA issuers
                 yield dict(force_block_m=bm, force_k_group=kg, force_b_resident=br, force_block_n=bn,
                            force_issuer_split=1)
-        if spec.stride == 1:
+        if spec.stride == 1 or (spec.stride == 2 and spec.k == 3):
             for bm, br, bn in itertools.product((128, 256), (-1, 1), bns):
                 yield dict(force_block_m=bm, force_b_resident=br, force_block_n=bn, force_window=1)
 
@@ -162,11 +167,52 @@ def tune(reps: int = 10, log=print):
     return plans
 
 
+def time_plan(prec: str, n: int, spec: wl.LayerSpec, force: dict, reps: int = 10):
+    """Microseconds per launch of one layer shape planned with `force` (NHWC
+    for the tensor-core precisions, NCHW for FP32), and its plan."""
+    cp = PRECS[prec]
+    lay = B.CBS_NCHW if prec == "fp32" else B.CBS_NHWC
+    d = make_desc(n, spec.c_in, spec.h, spec.width, spec.c_out, spec.k, spec.stride, spec.pad, prec=cp,
+                  in_layout=lay, out_layout=lay, **force)
+    x, p = wl.layer_inputs(spec, n, layer_index=0)
+    s_x = float(wl.S_X_INT8) if prec == "int8" else 0.0
+    layer = FusedConvBnSilu(d, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, s_x=s_x, tuned=False)
+    xd = torch.from_numpy(x).cuda()
+    x0 = layer.pack_input(xd) if (prec != "fp32" or lay == B.CBS_NHWC) else xd
+    nbytes = x0.numel() * x0.element_size()
+    copies = int(min(8, max(2, math.ceil((256 << 20) / max(nbytes, 1)))))
+    xs = [x0] + [x0.clone() for _ in range(copies - 1)]
+    ys = [layer.empty_y() for _ in range(copies)]
+    us = Timer(reps)(layer, xs, ys, 0.05)
+    status = B.cbs_read_device_status(True, torch.cuda.current_stream().cuda_stream)
+    if status != B.CBS_OK:
+        raise RuntimeError(f"a kernel reported {B.status_name(status)}")
+    return us, layer.plan
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("out")
+    ap.add_argument("out", nargs="?")
     ap.add_argument("--reps", type=int, default=10)
+    ap.add_argument("--time", nargs=8, metavar=("PREC", "N", "C_IN", "C_OUT", "K", "STRIDE", "H", "W"))
+    ap.add_argument("--force", action="append", default=[], metavar="FIELD=VALUE")
     args = ap.parse_args()
+    if args.time:
+        prec = args.time[0]
+        n, c_in, c_out, k, stride, h, w = (int(v) for v in args.time[1:])
+        force = {}
+        for f in args.force:
+            name, _, v = f.partition("=")
+            if name not in FORCE_FIELDS:
+                raise SystemExit(f"unknown force field {name} (one of {', '.join(FORCE_FIELDS)})")
+            force[name] = int(v)
+        us, pl = time_plan(prec, n, wl.LayerSpec(c_in, c_out, k, stride, h, w), force, args.reps)
+        print(f"{prec} n{n} {c_in}->{c_out} k{k} s{stride} {h}x{w} {force}: {us:.2f} us "
+              f"(bm{pl.block_m} bn{pl.block_n} kg{pl.k_group} st{pl.stages} br{pl.b_resident} win{pl.window} "
+              f"split{pl.split_k} iss{pl.issuer_split})")
+        return
+    if not args.out:
+        ap.error("OUT.json is required unless --time is given")
     plans = tune(args.reps)
     meta = {"device": torch.cuda.get_device_name(0), "created_by": "conv_bn_silu_gb300/autotune.py",
             "timing": f"CUDA graph of {args.reps} launches over rotating input copies, second replay timed",

@@ -106,8 +106,17 @@ struct TcParams {
     // are computed and dropped), and one TMA box brings the zero-padded input
     // window of a tile and channel block; tap (r, s) is the window viewed from
     // row r * Wp + s on.
+    // Stride 2 (3x3, pad 1): a tile is a block of tile_h output rows x tile_w
+    // output columns (ncol blocks across an image), on a grid of Wp = tile_w + 1
+    // positions per row; two boxes per window, plane 0 with the even input
+    // rows from the block's first output row oh0 on and plane 1 (at
+    // plane1_off) with the odd rows from oh0 - 1; a plane row is read as pairs
+    // of pixels (PR = 2 RB bytes per operand row, swizzle swz_a), Wp pairs from
+    // pair ow0 - 1 on.
     int win;
     int Wp, tiles_per_img, R_box;
+    int s2, PR, plane1_off, tile_w, tile_h, ncol;
+    uint32_t swz_a;            // descriptor swizzle code of the window's operand rows
     int SB;                    // weight-ring stages when the weights are streamed (windowed)
     int act;                   // cbs_activation
     const void *residual;      // nullable: added after the activation (y's layout and element type)
@@ -620,7 +629,15 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 int m0, n0;
                 tile_coords(t, p.n_tiles, tile_m, m0, n0, p.BN);
                 int img, wc, hc;
-                if (p.win) {
+                if (p.win && p.s2) {
+                    // Stride-2 block: pairs from ow0 - 1, plane rows from oh0 - 1.
+                    const int mt = t / p.n_tiles;
+                    img = mt / p.tiles_per_img;
+                    const int tl = mt - img * p.tiles_per_img;
+                    const int rblk = tl / p.ncol;
+                    wc = (tl - rblk * p.ncol) * p.tile_w - 1;
+                    hc = rblk * p.tile_h - 1;
+                } else if (p.win) {
                     // Window of the tile: padded columns -pad .. W+pad-1 of the
                     // input rows from (first output row) - pad on.
                     const int mt = t / p.n_tiles;
@@ -653,7 +670,15 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         ptx::mbar_arrive_expect_tx(full_bar(s), p.win ? (uint32_t)p.a_box_bytes
                                                                       : (uint32_t)(p.kg * (p.a_box_bytes + (p.b_res ? 0 : b_step_bytes))));
                     __syncwarp();
-                    if (p.win) {
+                    if (p.win && p.s2) {
+                        // Stride 2: plane 0 (even input rows) from output row
+                        // hc + 1 = oh0 on, plane 1 (odd rows) from oh0 - 1;
+                        // both from pair wc = -1 on.
+                        if (lane == 0)
+                            ptx::tma_load_4d(sbase, &tmA, full_bar(s), 0, wc, hc + 1, img);
+                        else if (lane == 1)
+                            ptx::tma_load_4d(sbase + (uint32_t)p.plane1_off, &tmA2, full_bar(s), 0, wc, hc, img);
+                    } else if (p.win) {
                         // A window stage is channel block st of the first or the second input.
                         const bool second = st >= p.ca_blocks;
                         if (lane == 0)
@@ -692,8 +717,11 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (lane == 0 && mi < p.mmul * p.kpar) {
             const uint32_t sbo = 8u * p.RB;
             const int kslices = p.RB / 32;
-            const uint32_t sub_bytes = p.kpar == 2 ? 0u : (uint32_t)(kBM * p.RB);   // one 128-row sub-tile of an A box
+            // one 128-row sub-tile of an A box (stride-2 windows: 128 pairs)
+            const uint32_t sub_bytes = p.kpar == 2 ? 0u : (uint32_t)(kBM * (p.s2 ? p.PR : p.RB));
             const uint64_t dhi = ptx::smem_desc(0u, 16u, sbo, p.swz);
+            // Stride-2 windows: operand rows of PR bytes (pairs of pixels).
+            const uint64_t dhi_a = p.s2 ? ptx::smem_desc(0u, 16u, 8u * (uint32_t)p.PR, p.swz_a) : dhi;
             bool ok = true;
             if (p.b_res && blockIdx.x < num_tiles && !ptx::mbar_wait_bounded(bfull_bar, 0, kWaitLimitNs)) {
                 abort_now(p, abort_flag);
@@ -714,7 +742,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     // Row of the window that holds the tile's first position.
                     const int mt = t / p.n_tiles;
                     const int q0 = (mt - (mt / p.tiles_per_img) * p.tiles_per_img) * tile_m;
-                    const int row0 = q0 - (q0 / p.Wp) * p.Wp;
+                    const int row0 = p.s2 ? 0 : q0 - (q0 / p.Wp) * p.Wp;   // stride-2 blocks start a window row
                     for (int cb = 0; cb < p.cblocks; ++cb, ++g) {
                         const int s = g % S, u = g / S;
                         if (!ptx::mbar_wait_bounded(full_bar(s), u & 1, kWaitLimitNs)) {
@@ -724,6 +752,46 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         }
                         ptx::tc_fence_after();
                         const uint32_t window = stage0 + s * p.stage_bytes;
+                        if (p.s2) {
+                            // 3x3 stride 2 (one channel block): kernel row r
+                            // reads plane 1 (r = 0, 2; one plane row on for
+                            // r = 2) or plane 0 (r = 1); column c reads the
+                            // second pixel of pair ow - 1 (c = 0), the first of
+                            // pair ow (c = 1) or its second (c = 2).
+                            const uint32_t abase = window + (uint32_t)row0 * p.PR + mi * sub_bytes;
+                            const uint32_t prow = (uint32_t)(p.Wp * p.PR), p1 = (uint32_t)p.plane1_off;
+                            const uint32_t pr = (uint32_t)p.PR, rb = (uint32_t)p.RB;
+                            const uint32_t roff[3] = {p1, 0u, p1 + prow};
+                            const uint32_t coff[3] = {rb, pr, pr + rb};
+                            const uint64_t b_col = (uint64_t)(p.b_tile_stride >> 4);
+                            for (int r = 0; r < 3; ++r) {
+                                uint64_t bd;
+                                int ws = 0;
+                                if (p.b_res) {
+                                    bd = dhi | (uint64_t)(((b_base + (uint32_t)(3 * r * p.b_tile_stride)) & 0x3FFFFu) >> 4);
+                                } else {
+                                    ws = gw % p.SB;
+                                    if (!ptx::mbar_wait_bounded(wfull_bar(ws), (gw / p.SB) & 1, kWaitLimitNs)) {
+                                        abort_now(p, abort_flag);
+                                        ok = false;
+                                        break;
+                                    }
+                                    ptx::tc_fence_after();
+                                    bd = dhi | (uint64_t)(((b_base + (uint32_t)(ws * 3 * p.b_tile_stride)) & 0x3FFFFu) >> 4);
+                                }
+                                for (int c = 0; c < 3; ++c, bd += b_col) {
+                                    const uint64_t ad = dhi_a | (uint64_t)(((abase + roff[r] + coff[c]) & 0x3FFFFu) >> 4);
+                                    issue_kstep_desc<KIND>(d_tmem, ad, bd, p.idesc, kslices, r == 0 && c == 0);
+                                }
+                                if (!p.b_res) {
+                                    ptx::mma_commit(wempty_bar(ws));   // the slot is free once these MMAs are done
+                                    ++gw;
+                                }
+                            }
+                            if (!ok) break;
+                            ptx::mma_commit(empty_bar(s));
+                            continue;
+                        }
                         if (p.b_res) {
                             // Resident weights: no wait between taps.  The
                             // descriptors advance by constant steps (address
@@ -837,7 +905,19 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int m = m0 + row;
             int img = 0, oh = 0, ow = 0;
             bool valid;
-            if (p.win) {
+            if (p.win && p.s2) {
+                // Position row = oh' * Wp + ow' of a stride-2 block: keep it
+                // when it lies in the block and in the image.
+                const int mt = t / p.n_tiles;
+                img = mt / p.tiles_per_img;
+                const int tl = mt - img * p.tiles_per_img;
+                const int rblk = tl / p.ncol;
+                const int ohl = row / p.Wp, owl = row - ohl * p.Wp;
+                oh = rblk * p.tile_h + ohl;
+                ow = (tl - rblk * p.ncol) * p.tile_w + owl;
+                valid = ohl < p.tile_h && owl < p.tile_w && oh < p.OH && ow < p.OW;
+                m = (img * p.OH + oh) * p.OW + ow;
+            } else if (p.win) {
                 // Position q of the padded grid: keep it when ow' < OW.
                 const int mt = t / p.n_tiles;
                 img = mt / p.tiles_per_img;
@@ -1720,16 +1800,85 @@ int tc_producers_max(int stages, int maxp) {
     return 1;
 }
 
-// Window geometry of the windowed A path (stride 1, odd k, pad k/2, 128-byte
-// channel blocks): padded row width and input rows of one window box.
+// Window geometry of the windowed A path: padded row width, input rows of
+// one window box, and the bytes of one window stage.
+// - Stride 1 (odd k, pad k/2, 128-byte channel blocks): one box of R_box
+//   input rows of Wp = W + 2 pad pixels; tap (r, s) is the window viewed from
+//   row r * Wp + s on.
+// - Stride 2 (3x3, pad 1, even W, one channel block of 32 or 64 bytes per
+//   pixel, one input): tiles are blocks of tile_h output rows x tile_w output
+//   columns (ncol blocks across), computed on a grid of Wp = tile_w + 1
+//   positions per row (the last one dropped).  Two boxes per tile: plane 0
+//   with the even input rows from the block's first output row oh0 on
+//   (R_box = tile_h rows) and plane 1 with the odd ones from oh0 - 1
+//   (tile_h + 1 rows), both Wp pairs of pixels wide from pair ow0 - 1 on.  A
+//   plane row is read as pairs of pixels, PR = 2 RB bytes per operand row;
+//   position q = oh' * Wp + ow' then reads, for every tap, one operand row
+//   at a fixed offset from q (the taps of output column ow are pixels
+//   2 ow - 1, 2 ow and 2 ow + 1: the second half of pair ow - 1 and both
+//   halves of pair ow).
 struct TcWindow {
     int Wp, R_box, tiles_per_img;
+    int tile_w, tile_h, ncol;  // stride 2: output block of a tile, blocks across
+    int s2, PR;             // stride-2 pair window; operand row bytes (RB or 2 RB)
+    int a_box_bytes;        // bytes the loads of one window stage bring
+    int plane1_off;         // byte offset of plane 1 in a stage (stride 2)
+    int stage_bytes;        // one window stage, with spare rows, 1024-byte aligned parts
 };
-bool tc_window_geometry(const cbs_layer_desc &d, int oh, int RB, int tile_m, TcWindow &w) {
-    if (d.stride != 1 || d.k % 2 == 0 || d.pad != d.k / 2 || RB != 128) return false;
-    w.Wp = d.w + 2 * d.pad;
-    w.R_box = (tile_m - 1) / w.Wp + 2 + 2 * d.pad;
-    if (w.Wp > 256 || w.R_box > 256) return false;
+bool tc_window_geometry(const cbs_layer_desc &d, int oh, int RB, int cblocks, int tile_m, TcWindow &w) {
+    if (d.stride == 1) {
+        if (d.k % 2 == 0 || d.pad != d.k / 2 || RB != 128) return false;
+        w.s2 = 0;
+        w.PR = RB;
+        w.Wp = d.w + 2 * d.pad;
+        w.R_box = (tile_m - 1) / w.Wp + 2 + 2 * d.pad;
+        if (w.Wp > 256 || w.R_box > 256) return false;
+        w.a_box_bytes = w.R_box * w.Wp * RB;
+        w.plane1_off = 0;
+        // The last taps of the last (dropped) columns read up to k-2 rows
+        // past the box: the stage keeps 8 spare rows.
+        w.stage_bytes = round_up((w.R_box * w.Wp + 8) * RB, 1024);
+    } else if (d.stride == 2) {
+        if (d.k != 3 || d.pad != 1 || d.w % 2 || d.h < 2 || cblocks != 1 || (RB != 32 && RB != 64) || d.c_in_b > 0)
+            return false;
+        w.s2 = 1;
+        w.PR = 2 * RB;
+        const int ow = d.w / 2;
+        // Column blocks: the most output pixels per computed position, then
+        // the fewest window bytes per image.
+        double best_use = -1.0, best_bytes = 0.0;
+        int best_ncol = 0;
+        for (int ncol = 1; ncol <= 16 && ncol <= ow; ++ncol) {
+            const int tw = (ow + ncol - 1) / ncol, wp = tw + 1, th = tile_m / wp;
+            if (th < 1 || wp > 256 || th + 1 > 256) continue;
+            const int rblocks = (oh + th - 1) / th;
+            const double use = (double)ow * oh / ((double)ncol * rblocks * tile_m);
+            const double bytes = (double)ncol * rblocks * (2 * th + 1) * wp * w.PR;
+            if (use > best_use * 1.01 || (use > best_use * 0.99 && bytes < best_bytes)) {
+                best_use = use;
+                best_bytes = bytes;
+                best_ncol = ncol;
+            }
+        }
+        if (best_ncol == 0) return false;
+        w.ncol = best_ncol;
+        w.tile_w = (ow + w.ncol - 1) / w.ncol;
+        w.Wp = w.tile_w + 1;
+        w.tile_h = tile_m / w.Wp;
+        w.R_box = w.tile_h;
+        w.a_box_bytes = (2 * w.tile_h + 1) * w.Wp * w.PR;
+        // Positions past the block (the dropped column, and the tile's rows
+        // past tile_h * Wp) read up to tile_m - tile_h * Wp + Wp + 1 pairs
+        // past each plane's box: both keep that many spare pairs, and 8 more.
+        const int spare = tile_m - w.tile_h * w.Wp + w.Wp + 8;
+        w.plane1_off = round_up((w.tile_h * w.Wp + spare) * w.PR, 1024);
+        w.stage_bytes = w.plane1_off + round_up(((w.tile_h + 1) * w.Wp + spare) * w.PR, 1024);
+        w.tiles_per_img = w.ncol * ((oh + w.tile_h - 1) / w.tile_h);
+        return true;
+    } else {
+        return false;
+    }
+    w.tile_w = w.tile_h = w.ncol = 0;
     w.tiles_per_img = (oh * w.Wp + tile_m - 1) / tile_m;
     return true;
 }
@@ -1746,13 +1895,11 @@ struct TcConfig {
 // for all k*k taps), weights resident or in a ring of SB single-tile slots.
 bool tc_config_window(const cbs_layer_desc &d, int oh, int RB, int ksteps, bool tf32, TcConfig &c) {
     const int tile_m = kBM * c.mmul;
-    if (!tc_window_geometry(d, oh, RB, tile_m, c.wg)) return false;
     const int cblocks = ksteps / (d.k * d.k);
+    if (!tc_window_geometry(d, oh, RB, cblocks, tile_m, c.wg)) return false;
     c.kg = 1;
-    c.a_box_bytes = c.wg.R_box * c.wg.Wp * RB;
-    // The last taps of the last (dropped) columns read up to k-2 rows past the
-    // box: the stage keeps 8 spare rows.
-    c.stage_bytes = ((c.wg.R_box * c.wg.Wp + 8) * RB + 1023) / 1024 * 1024;
+    c.a_box_bytes = c.wg.a_box_bytes;
+    c.stage_bytes = c.wg.stage_bytes;
     const int b_bytes = c.BN * RB;
     c.b_tile_stride = (b_bytes + 1023) / 1024 * 1024;
     c.m_tiles = d.n * c.wg.tiles_per_img;
@@ -1783,7 +1930,7 @@ bool tc_config_window(const cbs_layer_desc &d, int oh, int RB, int ksteps, bool 
     const int kslices = RB / 32;
     const double mma = tpc * (tc_tile_mma_clk((double)ksteps * kslices, (double)cblocks, c.mmul, c.BN, tf32) +
                               (c.b_res ? 0.0 : (double)(ksteps / d.k) * kClkPerStageWait));
-    const double boxes = tpc * cblocks + (c.b_res ? (double)ksteps : tpc * ksteps);
+    const double boxes = tpc * cblocks * (c.wg.s2 ? 2 : 1) + (c.b_res ? (double)ksteps : tpc * ksteps);
     const double bytes = tpc * cblocks * (double)c.a_box_bytes + (c.b_res ? (double)ksteps : tpc * ksteps) * b_bytes;
     const double t_box = boxes * 140.0, t_fill = bytes / kFillBytesPerClk;
     const double tma = t_box > t_fill ? t_box : t_fill;
@@ -2182,11 +2329,20 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     P.b_region = P.b_res ? P.ksteps * P.b_tile_stride : P.SB * d.k * P.b_tile_stride;
     if (P.win) {
         TcWindow wg;
-        if (!tc_window_geometry(d, pl.oh, RB, kBM * mmul, wg)) return fail(CBS_ERR_PLAN_MISMATCH, "window geometry");
+        if (!tc_window_geometry(d, pl.oh, RB, P.cblocks, kBM * mmul, wg))
+            return fail(CBS_ERR_PLAN_MISMATCH, "window geometry");
         P.Wp = wg.Wp;
         P.R_box = wg.R_box;
         P.tiles_per_img = wg.tiles_per_img;
-        P.a_box_bytes = wg.R_box * wg.Wp * RB;
+        P.a_box_bytes = wg.a_box_bytes;
+        P.s2 = wg.s2;
+        P.PR = wg.PR;
+        P.plane1_off = wg.plane1_off;
+        P.tile_w = wg.tile_w;
+        P.tile_h = wg.tile_h;
+        P.ncol = wg.ncol;
+        P.swz_a = desc_swizzle_code(wg.PR);
+        P.stage_bytes = wg.stage_bytes;
         if (pl.m_tiles != d.n * wg.tiles_per_img) return fail(CBS_ERR_PLAN_MISMATCH, "window tiles");
     }
     if (staged) {
@@ -2199,8 +2355,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     } else {
         P.nprod = P.win ? tc_producers_max(pl.stages, P.b_res ? kMaxProducers : kMaxProducers - 1)
                         : tc_producers(pl.stages);
-        P.stage_bytes = P.win ? round_up((P.R_box * P.Wp + 8) * RB, 1024)
-                              : P.kg * P.a_box_bytes + (P.b_res ? 0 : P.kg * P.b_tile_stride);
+        if (!P.win) P.stage_bytes = P.kg * P.a_box_bytes + (P.b_res ? 0 : P.kg * P.b_tile_stride);
         const bool tf32 = pl.variant == CBS_VARIANT_TC_TF32;
         P.st_mode = (P.win || P.split > 1) ? 0 : tc_store_mode(d, BN, pl.n_tiles, tf32);
         P.cbw = 128 / tc_out_bytes(tf32);
@@ -2310,8 +2465,28 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
         }
         return CBS_OK;
     };
+    // Stride-2 window plane rp (0: even input rows, 1: odd): rows 2 i + rp of
+    // every image, each row as W / 2 pairs of pixels (one pair per box row).
+    auto make_plane_map = [&](CUtensorMap *tm, int rp) -> cbs_status {
+        const size_t pix = (size_t)pl.c_in_pad * eb_x;
+        const char *gptr = static_cast<const char *>(x) + (size_t)rp * d.w * pix;
+        const cuuint64_t dims[4] = {(cuuint64_t)(2 * pl.c_in_pad), (cuuint64_t)(d.w / 2),
+                                    (cuuint64_t)((d.h + 1 - rp) / 2), (cuuint64_t)d.n};
+        const cuuint64_t strides[3] = {(cuuint64_t)(2 * pix), (cuuint64_t)(2 * d.w * pix),
+                                       (cuuint64_t)((size_t)d.h * d.w * pix)};
+        const cuuint32_t box[4] = {(cuuint32_t)(2 * pl.c_in_pad), (cuuint32_t)P.Wp, (cuuint32_t)(P.R_box + rp), 1u};
+        const cuuint32_t es4[4] = {1, 1, 1, 1};
+        CUresult res = fns.tiled(tm, dt_x, 4, const_cast<char *>(gptr), dims, strides, box, es4,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(P.PR), CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (res != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuTensorMapEncodeTiled (window plane %d) failed (%d)", rp, (int)res);
+        return CBS_OK;
+    };
     alignas(64) CUtensorMap tmA2;
-    if (d.c_in_b > 0) {
+    if (P.s2) {
+        CBS_TRY(make_plane_map(&tmA, 0));
+        CBS_TRY(make_plane_map(&tmA2, 1));
+    } else if (d.c_in_b > 0) {
         CBS_TRY(make_a_map(&tmA, x, c_a, "A"));
         CBS_TRY(make_a_map(&tmA2, x_b, pl.c_in_pad - c_a, "A of x_b"));
     } else {

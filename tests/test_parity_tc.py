@@ -321,6 +321,49 @@ def test_issuer_split_with_residual_two_inputs_and_identity(cuda_lib):
         check_tc("bf16", y, tc_refs("bf16", x, p, 1, 1, act=act, residual=rb), act)
 
 
+WINDOW_S2_SHAPES = [  # (n, c_in, c_out, h, w, N tile tried first): 3x3, stride 2, pad 1
+    (2, 16, 32, 64, 64, 32),         # 32-byte pixels (BF16), several tiles per image
+    (2, 32, 64, 40, 40, 64),         # 64-byte pixels (BF16), 64-byte TF32 pixels with 16 channels below
+    (1, 16, 48, 17, 18, 48),         # odd height: the planes have 9 and 8 rows; ragged last tile
+    (3, 8, 40, 9, 14, 48),           # 8 channels (TF32: 32-byte pixels), ragged output channels
+    (1, 16, 200, 12, 12, 128),       # several N tiles, the last ragged
+    (2, 16, 16, 2, 2, 16),           # one output pixel per image: every tap but one in the padding
+]
+
+
+@pytest.mark.parametrize("prec", ["bf16", "tf32"])
+@pytest.mark.parametrize("bm,bres", [(128, -1), (256, -1), (128, 1), (256, 1)])
+@pytest.mark.parametrize("shape", WINDOW_S2_SHAPES)
+def test_windowed_a_stride2(cuda_lib, prec, bm, bres, shape):
+    """3x3 stride-2 layers with the windowed A operand: per tile, one box of
+    the even input rows and one of the odd rows, each row read as pairs of
+    pixels; every tap a view of one of them.  Resident weights that do not
+    fit fall back to the weight ring; shapes whose window does not fit
+    shared memory are refused by the planner."""
+    n, c_in, c_out, h, w, bn = shape
+    spec = wl.LayerSpec(c_in, c_out, 3, 2, h, w)
+    x, p = wl.layer_inputs(spec, n, layer_index=21)
+    kw = None
+    for cand in (dict(force_block_n=bn, force_b_resident=bres), dict(force_b_resident=bres),
+                 dict(force_block_n=bn, force_b_resident=-1), dict(force_b_resident=-1)):
+        cand.update(force_window=1, force_block_m=bm)
+        try:
+            B.cbs_plan(make_desc(n, c_in, h, w, c_out, 3, 2, prec=PRECS[prec], **cand))
+            kw = cand
+            break
+        except B.CbsError as e:
+            assert e.status == B.CBS_ERR_UNSUPPORTED
+    if kw is None:
+        pytest.skip("window does not fit shared memory")
+    for out_layout in (B.CBS_NHWC, B.CBS_NCHW):
+        y, layer = run_tc(spec, x, p, PRECS[prec], out_layout=out_layout, **kw)
+        pl = layer.plan
+        assert pl.window == 1 and pl.block_m == bm
+        check(y, spec, x, p, prec, (shape, bm, pl.b_resident, pl.block_n, pl.stages, pl.k_group, out_layout))
+    y2, _ = run_tc(spec, x, p, PRECS[prec], out_layout=B.CBS_NCHW, **kw)
+    assert np.array_equal(y, y2)
+
+
 def test_no_timeout_reported(cuda_lib):
     assert B.cbs_read_device_status(True, torch.cuda.current_stream().cuda_stream) == B.CBS_OK
 
