@@ -142,9 +142,14 @@ EXTRA_DEFAULT = ("layer_list_bf16_n16", "layer_list_tf32_n16", "layer_list_int8_
 # only while the kernel's sources and the measured plan table (which picks
 # its tiles) are the ones the counters were taken from.
 TRAFFIC = {
-    "layer_list_fp32_n1": {"kernel": "simt_conv_kernel", "launches": 11, "bytes": 28478976,
-                           "sources": ("k_simt.cu", "cbs_internal.cuh", "../tuned_plans.json"),
-                           "digest": "1798aa6ec09f0cdd",
+    # The 3xTF32 layers of the batch-1 FP32 list take NCHW input: each is a
+    # repack of x to NHWC (pack_nhwc_kernel) and the tensor-core kernel, and
+    # the figure covers both launches of each.
+    "layer_list_fp32_n1": {"variant": 5, "kernel": "tc_conv_staged_kernel<TF32X3> + pack_nhwc_kernel<float>",
+                           "launches": 10, "bytes": None,
+                           "sources": ("k_tc.cu", "k_misc.cu", "cbs_api.cu", "cbs_internal.cuh",
+                                       "../tuned_plans.json"),
+                           "digest": None,
                            "profile": "profiles/launches_layer_list_fp32_n1.md"},
 }
 # Variant of the dominant kernel per precision (the direct small-channel
@@ -156,10 +161,11 @@ KERNEL_NAMES = {0: "simt_conv_kernel (FP32 FMA)", 1: "tc_conv_kernel<TF32>", 2: 
 X3_VARIANT = 5
 
 
-def sources_digest(files) -> str:
-    """Hash of the kernel sources and, for the measured plan table, of its
-    entries that pick CUDA-core tiles (force_variant 0): the tensor-core
-    entries do not change the CUDA-core kernel's traffic."""
+def sources_digest(files, table_prefix="0:", table_suffix=":0:0") -> str:
+    """Hash of the kernel sources and, for the measured plan table, of the
+    entries of the workload's shapes (by default FP32 with NCHW layouts: the
+    key starts with the precision and ends with the two layouts); the other
+    entries do not change these launches."""
     import hashlib
     h = hashlib.sha256()
     for f in files:
@@ -167,17 +173,17 @@ def sources_digest(files) -> str:
         if f.endswith("tuned_plans.json"):
             with open(path) as fh:
                 plans = json.load(fh).get("plans", {})
-            simt = {k: v for k, v in plans.items() if v.get("force", {}).get("force_variant") == 0}
-            h.update(json.dumps(simt, sort_keys=True).encode())
+            mine = {k: v for k, v in plans.items() if k.startswith(table_prefix) and k.endswith(table_suffix)}
+            h.update(json.dumps(mine, sort_keys=True).encode())
             continue
         with open(path, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def traffic_for(workload: str):
+def traffic_for(workload: str, variant: int):
     t = TRAFFIC.get(workload)
-    if t is None or sources_digest(t["sources"]) != t["digest"]:
+    if t is None or t["variant"] != variant or sources_digest(t["sources"]) != t["digest"]:
         return None
     return t["bytes"]
 
@@ -265,7 +271,7 @@ class ListWorkload:
         self.ys = [[layer.empty_y() for layer in self.layers] for _ in range(self.R)]
         self.rs = [[layer.empty_y().normal_() if r else None for layer, r in zip(self.layers, self.res)]
                    for _ in range(self.R)]
-        self.launches_per_step = len(self.layers)
+        self.launches_per_step = sum(layer.launches for layer in self.layers)   # repacks included
 
     def step(self, r, stream_id, events=None, stream=None):
         for j, layer in enumerate(self.layers):
@@ -493,18 +499,20 @@ def run_ours(args, rank: int, world: int):
     dom_flops = sum(sp.flops(n) for sp, _ in dom)
     dom_us = sum(r["us"] for _, r in dom)
     achieved = dom_flops / (dom_us * 1e-6) / 1e12
-    traffic = traffic_for(args.workload)
+    traffic = traffic_for(args.workload, dom_variant)
     bound, peak_label = ("alu" if w.prec == "fp32" else "tensor"), head["peak"]
     if dom_variant == X3_VARIANT:   # FP32 as three TF32 products on the tensor cores
         peak = round(peak_for("tf32", peaks)[0] / 3, 2)
         bound, peak_label = "tensor", "tensor: measured bf16 burst x nominal tf32/bf16 (1.1/2.25) / 3 products"
+    repacked = sum(1 for sp, layer in w.rows() if layer.plan.variant == dom_variant and layer.launches == 2)
     roofline = {"bound": bound,
-                "kernel": f"{kernel}, the {len(dom)} launches of one step",
+                "kernel": (f"{kernel}, the {len(dom)} launches of one step"
+                           + (f" ({repacked} of them after a repack of their NCHW input, timed with it)" if repacked else "")),
                 "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_label + f" ({peak_src})",
                 "traffic": traffic,
-                "traffic_note": ("DRAM bytes of those launches in one step (ncu, cold cache)" if traffic is not None
-                                 else "no capture of the current kernel sources"),
+                "traffic_note": ((f"DRAM bytes in one step of {TRAFFIC[args.workload]['kernel']} (ncu, cold cache)")
+                                 if traffic is not None else "no capture of the current kernel sources"),
                 "algorithmic_bytes": sum(sp.alg_bytes(n, act_bytes(w.prec)) for sp, _ in dom),
                 "sum_layer_roofline_us": head["sum_layer_roofline_us"],
                 "frac_of_layer_roofline_sum": head["frac_of_layer_roofline_sum"]}

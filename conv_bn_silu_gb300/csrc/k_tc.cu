@@ -84,10 +84,6 @@ struct TcParams {
     uint32_t op_mask;          // operand swizzle mask
     // TF32/BF16 tall tiles, grouped K steps, resident weights
     int mmul;                  // 128-pixel sub-tiles per tile (one A box of 128*mmul rows)
-    int kpar;                  // 2: a 128-pixel tile's stages are split between the two MMA issuers by
-                               //    the parity of the stage count g (with an even ring, each ring slot
-                               //    always goes to the same issuer), each into its own accumulator,
-                               //    added by the epilogue; else 1
     int kg;                    // K steps per stage (divides ksteps)
     int b_res;                 // weights resident for the whole launch
     int bnp;                   // TMEM columns between sub-tile accumulators (power of two >= BN)
@@ -106,17 +102,8 @@ struct TcParams {
     // are computed and dropped), and one TMA box brings the zero-padded input
     // window of a tile and channel block; tap (r, s) is the window viewed from
     // row r * Wp + s on.
-    // Stride 2 (3x3, pad 1): a tile is a block of tile_h output rows x tile_w
-    // output columns (ncol blocks across an image), on a grid of Wp = tile_w + 1
-    // positions per row; two boxes per window, plane 0 with the even input
-    // rows from the block's first output row oh0 on and plane 1 (at
-    // plane1_off) with the odd rows from oh0 - 1; a plane row is read as pairs
-    // of pixels (PR = 2 RB bytes per operand row, swizzle swz_a), Wp pairs from
-    // pair ow0 - 1 on.
     int win;
     int Wp, tiles_per_img, R_box;
-    int s2, PR, plane1_off, tile_w, tile_h, ncol;
-    uint32_t swz_a;            // descriptor swizzle code of the window's operand rows
     int SB;                    // weight-ring stages when the weights are streamed (windowed)
     int act;                   // cbs_activation
     const void *residual;      // nullable: added after the activation (y's layout and element type)
@@ -140,6 +127,21 @@ struct TcParams {
     int split;
     float *partials;           // [tiles][split][tile_m * BN]
     unsigned int *counters;    // [tiles][kEpiWarps], zero between launches
+    // Fields of the two kernel modes (last, so that the plain kernel's fields
+    // keep their offsets).
+    int kpar;                  // 2: a 128-pixel tile's stages are split between the two MMA issuers by
+                               //    the parity of the stage count g (with an even ring, each ring slot
+                               //    always goes to the same issuer), each into its own accumulator,
+                               //    added by the epilogue; else 1
+    // Stride-2 window (3x3, pad 1): a tile is a block of tile_h output rows x tile_w
+    // output columns (ncol blocks across an image), on a grid of Wp = tile_w + 1
+    // positions per row; two boxes per window, plane 0 with the even input
+    // rows from the block's first output row oh0 on and plane 1 (at
+    // plane1_off) with the odd rows from oh0 - 1; a plane row is read as pairs
+    // of pixels (PR = 2 RB bytes per operand row, swizzle swz_a), Wp pairs from
+    // pair ow0 - 1 on.
+    int s2, PR, plane1_off, tile_w, tile_h, ncol;
+    uint32_t swz_a;            // descriptor swizzle code of the window's operand rows
 };
 
 constexpr int kSplitCounterSlots = 8;   // one per epilogue warp
@@ -463,15 +465,24 @@ __device__ __forceinline__ void abort_now(const TcParams &p, int *abort_flag) {
 
 __device__ __forceinline__ bool aborted(int *abort_flag) { return *(volatile int *)abort_flag != 0; }
 
+// Kernel modes: the plain kernel; the issuer split (a 128-pixel tile's K
+// stages alternate between the two MMA issuers); the stride-2 window.  The
+// two rarely used paths are instantiations of their own: as runtime branches
+// of one kernel they cost the plain path 2-4% (measured on the BF16 and TF32
+// lists at batch 16), the epilogue-bound layers most.
+constexpr int kModePlain = 0, kModeIssuerSplit = 1, kModeStride2Window = 2;
+
 // Persistent tensor-core kernel (TF32 / BF16).  Each CTA walks the tiles
 // t = blockIdx.x, blockIdx.x + gridDim.x, ...; the producers' stage ring and
 // the MMA issuer run ahead across tile boundaries, and the accumulators are
 // double-buffered in TMEM so the epilogue of tile j overlaps the MMAs of
 // tile j+1.
-template <int KIND>
+template <int KIND, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY, const TcParams p) {
+    constexpr bool KPAR = MODE == kModeIssuerSplit;     // p.kpar == 2
+    constexpr bool S2 = MODE == kModeStride2Window;     // p.win && p.s2
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Buffers start on a 1024-byte boundary of the shared window (the
     // swizzle atoms of TMA and of the MMA descriptors are address based).
@@ -516,7 +527,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // Every barrier the MMAs release counts one commit per issuer.
     // With kpar = 2 each stage is read by one issuer (the one of its count's
     // parity); otherwise by all mmul issuers.
-    const uint32_t n_iss = (uint32_t)(p.mmul * p.kpar);
+    const uint32_t n_iss = (uint32_t)(p.mmul * (KPAR ? 2 : 1));
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(full_bar(s), 1);
@@ -629,7 +640,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 int m0, n0;
                 tile_coords(t, p.n_tiles, tile_m, m0, n0, p.BN);
                 int img, wc, hc;
-                if (p.win && p.s2) {
+                if (S2) {
                     // Stride-2 block: pairs from ow0 - 1, plane rows from oh0 - 1.
                     const int mt = t / p.n_tiles;
                     img = mt / p.tiles_per_img;
@@ -670,7 +681,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         ptx::mbar_arrive_expect_tx(full_bar(s), p.win ? (uint32_t)p.a_box_bytes
                                                                       : (uint32_t)(p.kg * (p.a_box_bytes + (p.b_res ? 0 : b_step_bytes))));
                     __syncwarp();
-                    if (p.win && p.s2) {
+                    if (S2) {
                         // Stride 2: plane 0 (even input rows) from output row
                         // hc + 1 = oh0 on, plane 1 (odd rows) from oh0 - 1;
                         // both from pair wc = -1 on.
@@ -714,14 +725,14 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // The sub-tile whose MMAs this warp issues, or with kpar = 2 the
         // parity of the stages it takes.
         const int mi = warp - kMmaWarp;
-        if (lane == 0 && mi < p.mmul * p.kpar) {
+        if (lane == 0 && mi < p.mmul * (KPAR ? 2 : 1)) {
             const uint32_t sbo = 8u * p.RB;
             const int kslices = p.RB / 32;
             // one 128-row sub-tile of an A box (stride-2 windows: 128 pairs)
-            const uint32_t sub_bytes = p.kpar == 2 ? 0u : (uint32_t)(kBM * (p.s2 ? p.PR : p.RB));
+            const uint32_t sub_bytes = KPAR ? 0u : (uint32_t)(kBM * (S2 ? p.PR : p.RB));
             const uint64_t dhi = ptx::smem_desc(0u, 16u, sbo, p.swz);
             // Stride-2 windows: operand rows of PR bytes (pairs of pixels).
-            const uint64_t dhi_a = p.s2 ? ptx::smem_desc(0u, 16u, 8u * (uint32_t)p.PR, p.swz_a) : dhi;
+            const uint64_t dhi_a = S2 ? ptx::smem_desc(0u, 16u, 8u * (uint32_t)p.PR, p.swz_a) : dhi;
             bool ok = true;
             if (p.b_res && blockIdx.x < num_tiles && !ptx::mbar_wait_bounded(bfull_bar, 0, kWaitLimitNs)) {
                 abort_now(p, abort_flag);
@@ -742,7 +753,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     // Row of the window that holds the tile's first position.
                     const int mt = t / p.n_tiles;
                     const int q0 = (mt - (mt / p.tiles_per_img) * p.tiles_per_img) * tile_m;
-                    const int row0 = p.s2 ? 0 : q0 - (q0 / p.Wp) * p.Wp;   // stride-2 blocks start a window row
+                    const int row0 = S2 ? 0 : q0 - (q0 / p.Wp) * p.Wp;   // stride-2 blocks start a window row
                     for (int cb = 0; cb < p.cblocks; ++cb, ++g) {
                         const int s = g % S, u = g / S;
                         if (!ptx::mbar_wait_bounded(full_bar(s), u & 1, kWaitLimitNs)) {
@@ -752,7 +763,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         }
                         ptx::tc_fence_after();
                         const uint32_t window = stage0 + s * p.stage_bytes;
-                        if (p.s2) {
+                        if (S2) {
                             // 3x3 stride 2 (one channel block): kernel row r
                             // reads plane 1 (r = 0, 2; one plane row on for
                             // r = 2) or plane 0 (r = 1); column c reads the
@@ -850,7 +861,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     // ring depth is even, so slot g % S always goes to the same
                     // issuer, which takes its uses in order: its parity waits
                     // never see a slot two phases behind.
-                    if (p.kpar == 2 && (g & 1) != mi) continue;
+                    if (KPAR && (g & 1) != mi) continue;
                     const int s = g % S, us = g / S;
                     if (!ptx::mbar_wait_bounded(full_bar(s), us & 1, kWaitLimitNs)) {
                         abort_now(p, abort_flag);
@@ -867,7 +878,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     uint64_t bd = dhi | (uint64_t)((b0 & 0x3FFFFu) >> 4);
                     const uint64_t a_step = (uint64_t)(p.a_box_bytes >> 4), b_step = (uint64_t)(p.b_tile_stride >> 4);
                     for (int kk = 0; kk < p.kg; ++kk, ad += a_step, bd += b_step)
-                        issue_kstep_desc<KIND>(d_tmem, ad, bd, p.idesc, kslices, fresh && kk == 0);
+                        issue_kstep_desc<KIND>(d_tmem, ad, bd, p.idesc, kslices, (KPAR ? fresh : st == st0) && kk == 0);
                     fresh = false;
                     ptx::mma_commit(empty_bar(s));
                 }
@@ -905,7 +916,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int m = m0 + row;
             int img = 0, oh = 0, ow = 0;
             bool valid;
-            if (p.win && p.s2) {
+            if (S2) {
                 // Position row = oh' * Wp + ow' of a stride-2 block: keep it
                 // when it lies in the block and in the image.
                 const int mt = t / p.n_tiles;
@@ -997,7 +1008,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     for (int c = 0; c < bcols; c += 32) {
                         uint32_t v0[16], v1[16];
                         const bool two = c + 16 < bcols;
-                        tmem_ld_acc(t_row, (uint32_t)(bc0 + c), (uint32_t)(bc0 + c + 16), two, p.kpar == 2,
+                        tmem_ld_acc(t_row, (uint32_t)(bc0 + c), (uint32_t)(bc0 + c + 16), two, KPAR,
                                     (uint32_t)p.bnp, v0, v1);
                         float bv[16];
                         load_bias16(p, bias, n0 + bc0 + c, bv);
@@ -1019,7 +1030,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     // Two loads, one wait: 32 columns in flight per thread.
                     uint32_t v0[16], v1[16];
                     const bool two = c0 + cstep < p.BN;
-                    tmem_ld_acc(t_row, (uint32_t)c0, (uint32_t)(c0 + cstep), two, p.kpar == 2, (uint32_t)p.bnp, v0, v1);
+                    tmem_ld_acc(t_row, (uint32_t)c0, (uint32_t)(c0 + cstep), two, KPAR, (uint32_t)p.bnp, v0, v1);
                     if (valid) {
                         if (n0 + c0 < p.C_out) epi_store16<KIND>(p, bias, m, img, oh, ow, n0 + c0, v0);
                         if (two && n0 + c0 + cstep < p.C_out)
@@ -2507,12 +2518,16 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     dim3 grid(pl.grid_ctas, 1, 1);  // persistent: each CTA walks tiles blockIdx.x + i * gridDim.x
     if (pl.smem_bytes > kMaxDynSmem) return fail(CBS_ERR_UNSUPPORTED, "plan needs %d bytes of shared memory", pl.smem_bytes);
     cudaError_t e;
-    if (pl.variant == CBS_VARIANT_TC_TF32) {
-        e = set_max_dyn_smem(tc_conv_kernel<kTF32>, pl.smem_bytes);
-        if (e == cudaSuccess) e = launch_kernel(tc_conv_kernel<kTF32>, grid, kThreads, pl.smem_bytes, s, tmA, tmA2, tmB, tmY, P);
-    } else if (pl.variant == CBS_VARIANT_TC_BF16) {
-        e = set_max_dyn_smem(tc_conv_kernel<kBF16>, pl.smem_bytes);
-        if (e == cudaSuccess) e = launch_kernel(tc_conv_kernel<kBF16>, grid, kThreads, pl.smem_bytes, s, tmA, tmA2, tmB, tmY, P);
+    if (pl.variant == CBS_VARIANT_TC_TF32 || pl.variant == CBS_VARIANT_TC_BF16) {
+        using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcParams);
+        const int mode = P.kpar == 2 ? kModeIssuerSplit : (P.win && P.s2 ? kModeStride2Window : kModePlain);
+        const Kern kerns[2][3] = {{tc_conv_kernel<kTF32, kModePlain>, tc_conv_kernel<kTF32, kModeIssuerSplit>,
+                                   tc_conv_kernel<kTF32, kModeStride2Window>},
+                                  {tc_conv_kernel<kBF16, kModePlain>, tc_conv_kernel<kBF16, kModeIssuerSplit>,
+                                   tc_conv_kernel<kBF16, kModeStride2Window>}};
+        const Kern kern = kerns[pl.variant == CBS_VARIANT_TC_BF16 ? 1 : 0][mode];
+        e = set_max_dyn_smem(kern, pl.smem_bytes);
+        if (e == cudaSuccess) e = launch_kernel(kern, grid, kThreads, pl.smem_bytes, s, tmA, tmA2, tmB, tmY, P);
     } else if (i8) {
         auto kern = tc_conv_staged_kernel<kStagedI8>;
         e = set_max_dyn_smem(kern, pl.smem_bytes);

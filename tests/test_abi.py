@@ -45,17 +45,46 @@ def test_status_strings(cuda_lib):
 def test_plan_fp32_layer_list(cuda_lib, i):
     s = wl.LAYER_LIST[i]
     p = B.cbs_plan(make_desc(1, s.c_in, s.h, s.width, s.c_out, s.k, s.stride))
-    # three-channel stems take the direct CUDA-core kernel, the rest the implicit GEMM
-    assert p.variant == (B.CBS_VARIANT_STEM if s.c_in <= 4 else B.CBS_VARIANT_SIMT_FP32)
+    # Three-channel stems take the direct CUDA-core kernel; 3x3 stride-1 layers
+    # the 3xTF32 tensor-core kernel on an NHWC repack of the NCHW input (in the
+    # workspace); the rest the CUDA-core implicit GEMM.
+    x3 = s.c_in > 4 and s.k == 3 and s.stride == 1
+    assert p.variant == (B.CBS_VARIANT_STEM if s.c_in <= 4 else
+                         B.CBS_VARIANT_TC_TF32X3 if x3 else B.CBS_VARIANT_SIMT_FP32)
     assert (p.oh, p.ow) == (s.oh, s.ow)
     assert p.out_row_stride == s.ow
     assert p.x_bytes == s.c_in * s.h * s.width * 4
     assert p.y_bytes == s.c_out * s.oh * s.ow * 4
-    assert p.w_packed_bytes == s.c_out * s.c_in * s.k * s.k * 4
+    # (3xTF32 keeps each weight as a TF32 head and the remainder)
+    assert p.w_packed_bytes == s.c_out * s.c_in * s.k * s.k * 4 * (2 if x3 else 1)
     assert p.m_tiles * p.block_m >= s.oh * s.ow
     assert p.n_tiles * p.block_n >= s.c_out
-    assert p.split_k >= 1 and p.grid_ctas == p.m_tiles * p.n_tiles * p.split_k
-    assert (p.workspace_bytes > 0) == (p.split_k > 1)
+    if x3:
+        repack = (s.c_in * s.h * s.width * 4 + 255) // 256 * 256
+        assert p.workspace_bytes >= repack and p.grid_ctas <= 152
+        assert (p.workspace_bytes > repack) == (p.split_k > 1)
+    else:
+        assert p.split_k >= 1 and p.grid_ctas == p.m_tiles * p.n_tiles * p.split_k
+        assert (p.workspace_bytes > 0) == (p.split_k > 1)
+
+
+def test_fp32_nchw_tensor_core_rules(cuda_lib):
+    """NCHW FP32 layers go to the 3xTF32 kernel only for k >= 3 at stride 1
+    with C_in a multiple of 8 and nothing forced; forcing the variant takes
+    any one-input NCHW layer there; a two-input NCHW layer cannot."""
+    X3 = B.CBS_VARIANT_TC_TF32X3
+    auto = lambda **kw: B.cbs_plan(make_desc(**dict(dict(n=1, c_in=64, h=20, w=20, c_out=64, k=3, stride=1), **kw)))
+    assert auto().variant == X3
+    assert auto(stride=2).variant == B.CBS_VARIANT_SIMT_FP32
+    assert auto(k=1).variant == B.CBS_VARIANT_SIMT_FP32
+    assert auto(c_in=60).variant == B.CBS_VARIANT_SIMT_FP32
+    assert auto(force_block_m=64).variant == B.CBS_VARIANT_SIMT_FP32        # a forced tile is the CUDA-core kernel's
+    forced = auto(k=1, c_in=20, force_variant=X3)
+    assert forced.variant == X3 and forced.c_in_pad == 24 and forced.x_bytes == 20 * 20 * 20 * 4
+    assert forced.workspace_bytes >= 24 * 20 * 20 * 4
+    with pytest.raises(B.CbsError) as e:
+        auto(c_in_b=32, force_variant=X3)
+    assert e.value.status == B.CBS_ERR_UNSUPPORTED
 
 
 def test_plan_stem_rules(cuda_lib):

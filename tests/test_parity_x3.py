@@ -116,9 +116,9 @@ def test_more_accurate_than_tf32(cuda_lib):
 
 
 def test_plan_rules(cuda_lib):
-    """Host-side plan of the variant (no GPU call): FP32 only, NHWC input,
-    both weight halves in w_packed, staged-kernel launch shape, split-K
-    workspace."""
+    """Host-side plan of the variant (no GPU call): FP32 only, NHWC input or
+    an NCHW one repacked in the workspace, both weight halves in w_packed,
+    staged-kernel launch shape, split-K workspace."""
     spec = wl.LayerSpec(64, 96, 3, 1, 20, 20)
     pl = B.cbs_plan(desc_x3(2, spec))
     assert pl.variant == X3 and pl.block_m == 128 and pl.threads == 480
@@ -133,8 +133,10 @@ def test_plan_rules(cuda_lib):
     assert pl.m_tiles * pl.n_tiles * pl.split_k <= 152 or pl.split_k == 1
     with pytest.raises(B.CbsError):   # FP32 only
         B.cbs_plan(make_desc(1, 64, 20, 20, 96, 3, 1, prec=B.CBS_TF32, in_layout=B.CBS_NHWC, force_variant=X3))
-    with pytest.raises(B.CbsError):   # NHWC input
-        B.cbs_plan(make_desc(1, 64, 20, 20, 96, 3, 1, prec=B.CBS_FP32, in_layout=B.CBS_NCHW, force_variant=X3))
+    # NCHW input: its NHWC repack comes first in the workspace, the K parts' scratch after it
+    nchw = B.cbs_plan(make_desc(2, 64, 20, 20, 96, 3, 1, prec=B.CBS_FP32, in_layout=B.CBS_NCHW, force_variant=X3))
+    assert nchw.variant == X3 and nchw.x_bytes == pl.x_bytes and nchw.split_k == pl.split_k
+    assert nchw.workspace_bytes == -(-2 * 20 * 20 * 64 * 4 // 256) * 256 + pl.workspace_bytes
     # split-K on request: partial tiles and one counter per epilogue warp per tile
     sp = B.cbs_plan(desc_x3(2, spec, force_split_k=3))
     tiles = sp.m_tiles * sp.n_tiles
@@ -155,7 +157,9 @@ def test_automatic_choice(cuda_lib):
     assert variant(16, 64, 80, 64, 3, 1, **nhwc) == X3               # 6400 x 16 pixels
     assert variant(1, 64, 80, 64, 3, 1, **nhwc) == X3                # 50 tiles
     assert variant(1, 128, 40, 128, 3, 1, **nhwc) == X3                # 13 pixel tiles: K parts fill the SMs
-    assert variant(16, 64, 80, 64, 3, 1) == B.CBS_VARIANT_SIMT_FP32  # NCHW input
+    assert variant(16, 64, 80, 64, 3, 1) == X3                        # NCHW input, 3x3 stride 1: repacked
+    assert variant(16, 64, 80, 64, 3, 2) == B.CBS_VARIANT_SIMT_FP32   # NCHW input, stride 2
+    assert variant(16, 64, 80, 64, 1, 1) == B.CBS_VARIANT_SIMT_FP32   # NCHW input, 1x1
     assert variant(16, 20, 80, 64, 3, 1, **nhwc) == B.CBS_VARIANT_SIMT_FP32   # 20 channels: would need padding
     assert variant(16, 3, 640, 16, 3, 2, **nhwc) == B.CBS_VARIANT_STEM
     p = B.cbs_plan(make_desc(16, 64, 80, 80, 64, 3, 1, prec=B.CBS_FP32, **nhwc))
@@ -349,3 +353,65 @@ def test_planner_keeps_accumulators_in_tmem(cuda_lib):
         assert 2 * chunks * npow2(pl.block_n) <= 512, (c_in, c_out, k, hw, n, pl.block_n, pl.split_k)
         units = pl.m_tiles * pl.n_tiles * pl.split_k
         assert pl.grid_ctas == min(152, units)
+
+
+def run_nchw(spec, x, p, out_layout=B.CBS_NCHW, residual=None, **kw):
+    """The layer with NCHW input: the 3xTF32 kernel on the library's own NHWC
+    repack of x (in the workspace)."""
+    d = make_desc(x.shape[0], spec.c_in, spec.h, spec.width, spec.c_out, spec.k, spec.stride, spec.pad,
+                  prec=B.CBS_FP32, in_layout=B.CBS_NCHW, out_layout=out_layout, **kw)
+    layer = FusedConvBnSilu(d, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, tuned=False)
+    xd = torch.from_numpy(x).cuda()
+    y = layer(xd, residual=residual)
+    torch.cuda.synchronize()
+    y = y.cpu().numpy()
+    return (nhwc_to_nchw(y) if out_layout == B.CBS_NHWC else y[..., :layer.plan.ow]), layer
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("out_layout", [B.CBS_NCHW, B.CBS_NHWC])
+@pytest.mark.parametrize("shape,kw", [
+    ((1, 16, 32, 3, 2, 320, 320), {"force_variant": X3}),   # list layer 2: the largest repack
+    ((1, 64, 64, 3, 1, 80, 80), {}),                         # list layer 6 (chosen without forcing)
+    ((1, 256, 256, 3, 1, 20, 20), {}),                       # list layer 11: K parts in the workspace too
+    ((2, 24, 40, 3, 1, 17, 13), {}),                         # ragged pixels and output channels
+    ((2, 24, 40, 3, 2, 17, 13), {"force_variant": X3}),      # the same at stride 2
+    ((1, 20, 16, 3, 1, 9, 11), {"force_variant": X3}),       # C_in 20: the repack pads channels to 24
+    ((3, 64, 96, 1, 1, 9, 9), {"force_variant": X3}),        # 1x1 on request
+    ((1, 128, 128, 3, 1, 40, 40), {"force_variant": X3, "force_split_k": 3}),   # forced K parts
+])
+def test_fp32_nchw_input_on_tensor_cores(cuda_lib, out_layout, shape, kw):
+    n, c_in, c_out, k, stride, h, w = shape
+    spec = wl.LayerSpec(c_in, c_out, k, stride, h, w)
+    x, p = wl.layer_inputs(spec, n, layer_index=34)
+    y, layer = run_nchw(spec, x, p, out_layout, **kw)
+    pl = layer.plan
+    assert pl.variant == X3
+    assert pl.x_bytes == x.nbytes
+    assert pl.workspace_bytes >= n * h * w * pl.c_in_pad * 4
+    e = rel_l2(y, ref_of(spec, x, p))
+    assert e <= TOL_FP32_REL_L2, e
+    y2, _ = run_nchw(spec, x, p, out_layout, **kw)
+    assert np.array_equal(y, y2)
+
+
+@pytest.mark.gpu
+def test_fp32_nchw_input_padded_rows_and_residual(cuda_lib):
+    """NCHW in and out with a padded output row pitch, the identity
+    activation and a residual: columns past OW stay untouched."""
+    spec = wl.LayerSpec(32, 48, 3, 1, 21, 21)
+    x, p = wl.layer_inputs(spec, 2, layer_index=35)
+    r = np.random.default_rng(6).standard_normal((2, 48, 21, 21)).astype(np.float32)
+    stride = 32
+    rp = np.zeros((2, 48, 21, stride), np.float32)
+    rp[..., :21] = r
+    d = make_desc(2, 32, 21, 21, 48, 3, 1, prec=B.CBS_FP32, in_layout=B.CBS_NCHW, out_layout=B.CBS_NCHW,
+                  out_row_stride=stride, activation=B.CBS_ACT_IDENTITY, residual=1)
+    layer = FusedConvBnSilu(d, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, tuned=False)
+    assert layer.plan.variant == X3
+    y = torch.full((2, 48, 21, stride), 7.0, device="cuda")
+    layer(torch.from_numpy(x).cuda(), y, residual=torch.from_numpy(rp).cuda())
+    y = y.cpu().numpy()
+    want = oracle.conv_bn_act_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, 1, 1, act=1, residual=r)
+    assert rel_l2(y[..., :21], want) <= TOL_FP32_REL_L2
+    assert np.all(y[..., 21:] == 7.0)
