@@ -146,10 +146,10 @@ TRAFFIC = {
     # repack of x to NHWC (pack_nhwc_kernel) and the tensor-core kernel, and
     # the figure covers both launches of each.
     "layer_list_fp32_n1": {"variant": 5, "kernel": "tc_conv_staged_kernel<TF32X3> + pack_nhwc_kernel<float>",
-                           "launches": 10, "bytes": None,
+                           "launches": 10, "bytes": 23022592,
                            "sources": ("k_tc.cu", "k_misc.cu", "cbs_api.cu", "cbs_internal.cuh",
                                        "../tuned_plans.json"),
-                           "digest": None,
+                           "digest": "af24c8bbd5f68c17",
                            "profile": "profiles/launches_layer_list_fp32_n1.md"},
 }
 # Variant of the dominant kernel per precision (the direct small-channel

@@ -180,13 +180,19 @@ typedef struct cbs_plan_t {
  * Variant choice (force_variant = -1): STEM for the small-channel stems
  * below; else the precision's own variant, except that an FP32 layer takes
  * TC_TF32X3 (the FP32 bar on the tensor cores, split-K where its tiles leave
- * SMs idle) when it has NHWC input, each input's channel count a multiple
- * of 8 and no forced tile field; it falls back to SIMT FP32 when no 3xTF32
- * configuration fits.  Its input is then the same bytes as for SIMT FP32.
+ * SMs idle) when each input's channel count is a multiple of 8, no tile
+ * field is forced, and either its input is NHWC or it is a one-input layer
+ * with NCHW input, k >= 3 and stride 1; it falls back to SIMT FP32 when no
+ * 3xTF32 configuration fits.  Its input is then the same bytes as for SIMT
+ * FP32.
  * Input format the plan expects (see x_bytes):
  *   SIMT FP32: x in d->in_layout, float, exactly C_in channels.
  *   TF32/BF16/INT8 and TF32X3 (FP32): x NHWC with c_in_pad channels (extra
  *   channels zero; TF32X3: c_in_pad = C_in rounded up to 8).
+ *   TF32X3 with NCHW input (one input only): x NCHW float, exactly C_in
+ *   channels; the call repacks it to NHWC at the start of the workspace
+ *   (workspace_bytes includes those N*H*W*c_in_pad floats, rounded up to
+ *   256 bytes, before the kernel's own split-K scratch).
  *   STEM (chosen for C_in <= 4, C_out <= 64, k <= 7): x in d->in_layout;
  *   NHWC pixels hold c_in_pad = 4 channels for TF32/BF16/INT8, C_in for FP32.
  *   Two-input plans (d->c_in_b > 0): x holds the first c_in - c_in_b channels
