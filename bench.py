@@ -142,13 +142,11 @@ EXTRA_DEFAULT = ("layer_list_bf16_n16", "layer_list_tf32_n16", "layer_list_int8_
 # only while the kernel's sources and the measured plan table (which picks
 # its tiles) are the ones the counters were taken from.
 TRAFFIC = {
-    # The 3xTF32 layers of the batch-1 FP32 list take NCHW input: each is a
-    # repack of x to NHWC (pack_nhwc_kernel) and the tensor-core kernel, and
-    # the figure covers both launches of each.
-    "layer_list_fp32_n1": {"variant": 5, "kernel": "tc_conv_staged_kernel<TF32X3> + pack_nhwc_kernel<float>",
-                           "launches": 10, "bytes": 23022592,
-                           "sources": ("k_tc.cu", "k_misc.cu", "cbs_api.cu", "cbs_internal.cuh",
-                                       "../tuned_plans.json"),
+    # The 3xTF32 layers of the batch-1 FP32 list read their NCHW input in the
+    # kernel (its converter warps gather it).
+    "layer_list_fp32_n1": {"variant": 5, "kernel": "tc_conv_staged_kernel<TF32X3, NCHW gather>",
+                           "launches": 5, "bytes": None,
+                           "sources": ("k_tc.cu", "cbs_api.cu", "cbs_internal.cuh", "../tuned_plans.json"),
                            "digest": "af24c8bbd5f68c17",
                            "profile": "profiles/launches_layer_list_fp32_n1.md"},
 }
@@ -271,7 +269,7 @@ class ListWorkload:
         self.ys = [[layer.empty_y() for layer in self.layers] for _ in range(self.R)]
         self.rs = [[layer.empty_y().normal_() if r else None for layer, r in zip(self.layers, self.res)]
                    for _ in range(self.R)]
-        self.launches_per_step = sum(layer.launches for layer in self.layers)   # repacks included
+        self.launches_per_step = len(self.layers)
 
     def step(self, r, stream_id, events=None, stream=None):
         for j, layer in enumerate(self.layers):
@@ -504,10 +502,8 @@ def run_ours(args, rank: int, world: int):
     if dom_variant == X3_VARIANT:   # FP32 as three TF32 products on the tensor cores
         peak = round(peak_for("tf32", peaks)[0] / 3, 2)
         bound, peak_label = "tensor", "tensor: measured bf16 burst x nominal tf32/bf16 (1.1/2.25) / 3 products"
-    repacked = sum(1 for sp, layer in w.rows() if layer.plan.variant == dom_variant and layer.launches == 2)
     roofline = {"bound": bound,
-                "kernel": (f"{kernel}, the {len(dom)} launches of one step"
-                           + (f" ({repacked} of them after a repack of their NCHW input, timed with it)" if repacked else "")),
+                "kernel": f"{kernel}, the {len(dom)} launches of one step",
                 "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_label + f" ({peak_src})",
                 "traffic": traffic,

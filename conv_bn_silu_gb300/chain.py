@@ -173,7 +173,7 @@ class Chain:
 
     def launches_per_frame(self) -> int:
         # fused layers, frame packing, one upsample kernel, the SPPF pool kernel, the seams
-        return sum(layer.launches for layer in self.layers) + 2 + (1 if self.sppf else 0) + len(self.seams)
+        return len(self.layers) + 2 + (1 if self.sppf else 0) + len(self.seams)
 
     def _shape(self, a):
         if self.layout == B.CBS_NHWC:

@@ -269,11 +269,7 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
             auto_x3 = true;
         }
         // FP32 with NCHW input, a k x k filter (k >= 3) and stride 1: the same
-        // kernel on a copy of the input repacked to NHWC in the workspace.
-        // Measured at batch 1 on the list's 3x3 stride-1 layers (64, 128 and
-        // 256 channels), repack and kernel take 18-22% less time than the
-        // CUDA cores; on its stride-2 layers (an input four times the output)
-        // and its 1x1 layers they take longer.
+        // kernel, its converter warps reading the NCHW input themselves.
         if (variant == CBS_VARIANT_SIMT_FP32 && D.in_layout == CBS_NCHW && D.c_in_b == 0 && D.c_in % 8 == 0 &&
             D.k >= 3 && D.stride == 1 && !forces_tiles) {
             variant = CBS_VARIANT_TC_TF32X3;
@@ -309,7 +305,7 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
     } else if (variant == CBS_VARIANT_SIMT_FP32) {
         p.c_in_pad = D.c_in;
     } else {
-        // 3xTF32 takes NCHW input too (repacked to NHWC in the workspace).
+        // 3xTF32 takes NCHW input too (one input: its converters read it).
         if (D.in_layout != CBS_NHWC && !(variant == CBS_VARIANT_TC_TF32X3 && D.c_in_b == 0))
             return fail(CBS_ERR_UNSUPPORTED, "tensor-core variants read NHWC input (use cbs_pack_input)");
         p.c_in_pad = round_up(D.c_in, (int)(16 / eb));
@@ -370,11 +366,8 @@ cbs_status cbs_plan(const cbs_layer_desc *d, cbs_plan_t *out) {
             out->desc.force_variant = D.force_variant;
             return CBS_OK;
         }
-        if (x3_repacks_input(p)) {
-            // NCHW input: the NHWC copy comes first in the workspace.
-            p.x_bytes = (size_t)D.n * D.c_in * D.h * D.w * eb;
-            p.workspace_bytes += x3_repack_span(p);
-        }
+        if (p.variant == CBS_VARIANT_TC_TF32X3 && D.in_layout == CBS_NCHW)
+            p.x_bytes = (size_t)D.n * D.c_in * D.h * D.w * eb;   // read as given
     }
     if (D.c_in_b > 0) {   // x holds the first c_in - c_in_b channels, x_b the rest (plus padding)
         const int c_a = D.c_in - D.c_in_b;
@@ -500,16 +493,6 @@ cbs_status conv_act_impl(const cbs_plan_t *p, const void *x, const void *x_b, co
             L.partials = (float *)((char *)workspace + counters);
         }
         return cuda_check(launch_simt(L, (cudaStream_t)stream), "SIMT kernel launch");
-    }
-    if (x3_repacks_input(*p)) {
-        // NCHW input of the 3xTF32 kernel: repack it to NHWC in the workspace
-        // first (the kernel's grid waits for the repack's).
-        void *packed = workspace;
-        CBS_TRY(cuda_check(launch_pack_input(static_cast<const float *>(x), packed, d.n, d.c_in, d.h, d.w, p->c_in_pad,
-                                             1, 0, 1.0f, 0, (cudaStream_t)stream),
-                           "repack kernel launch"));
-        x = packed;
-        workspace = static_cast<char *>(workspace) + x3_repack_span(*p);
     }
     return launch_tc(*p, x, d.c_in_b > 0 ? x_b : nullptr, w_packed, bias, nullptr, 0.0f, residual, y, workspace,
                      (cudaStream_t)stream);

@@ -207,17 +207,6 @@ struct FoldLaunch {
 cudaError_t launch_fold(const FoldLaunch &L, cudaStream_t s);
 
 // dtype codes for packing: 0 float, 1 bf16, 2 int8 (quantised with s_x)
-// 3xTF32 plans with NCHW input run on an NHWC copy of x made at the start of
-// the workspace; the kernel's own scratch (split-K counters and partials)
-// follows it, 256-byte aligned.
-inline bool x3_repacks_input(const cbs_plan_t &p) {
-    return p.variant == CBS_VARIANT_TC_TF32X3 && p.desc.in_layout == CBS_NCHW;
-}
-inline size_t x3_repack_span(const cbs_plan_t &p) {
-    if (!x3_repacks_input(p)) return 0;
-    const size_t bytes = (size_t)p.desc.n * p.desc.h * p.desc.w * p.c_in_pad * sizeof(float);
-    return (bytes + 255) / 256 * 256;
-}
 cudaError_t launch_pack_input(const float *x_nchw, void *out, int N, int C, int H, int W,
                               int c_pad, int to_nhwc, int dtype, float s_x, int zp, cudaStream_t s);
 

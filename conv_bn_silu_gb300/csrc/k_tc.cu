@@ -142,6 +142,10 @@ struct TcParams {
     // pair ow0 - 1 on.
     int s2, PR, plane1_off, tile_w, tile_h, ncol;
     uint32_t swz_a;            // descriptor swizzle code of the window's operand rows
+    // 3xTF32 with NCHW input: the converter warps read x (N, c_in, in_h, in_w
+    // floats) themselves.
+    const float *x_nchw;
+    int c_in;
 };
 
 constexpr int kSplitCounterSlots = 8;   // one per epilogue warp
@@ -1152,7 +1156,7 @@ __device__ __forceinline__ void x3_chunk_sum(uint32_t taddr, int nch, int chunk_
 //              slice runs three kind::tf32 MMAs (tail x head, head x tail,
 //              head x head) into one FP32 accumulator, which drops only the
 //              tail x tail term: FP32-level accuracy on the tensor cores.
-template <int SK>
+template <int SK, bool GATHER>
 __global__ void __launch_bounds__(StagedLayout<SK>::kThreads, 1)
 tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                       const __grid_constant__ CUtensorMap tmB, const TcParams p) {
@@ -1189,6 +1193,9 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     const int num_tiles = p.m_tiles * p.n_tiles;
     const int num_units = num_tiles * p.split;   // X3 split-K: (tile, K part) units; else tiles
 
+    // GATHER (3xTF32, NCHW input): the producers load the weights only; the
+    // converter warps read the activations from global memory themselves.
+    static_assert(!GATHER || SK == kStagedX3, "the NCHW gather is the 3xTF32 kernel's");
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(raw_bar(s), 1);
@@ -1202,8 +1209,10 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         ptx::mbar_init(drain_bar, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
-        ptx::prefetch_tmap(&tmA);
-        if (p.ca_blocks < p.cblocks) ptx::prefetch_tmap(&tmA2);
+        if (!GATHER) {
+            ptx::prefetch_tmap(&tmA);
+            if (p.ca_blocks < p.cblocks) ptx::prefetch_tmap(&tmA2);
+        }
         ptx::prefetch_tmap(&tmB);
     }
     if (warp == kMmaWarpI8) {
@@ -1256,9 +1265,9 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     }
                     const uint32_t sb = base + s * p.stage_bytes;
                     if (lane == 0)
-                        ptx::mbar_arrive_expect_tx(raw_bar(s), (uint32_t)(kg * (p.stg_bytes + NB * p.b_bytes)));
+                        ptx::mbar_arrive_expect_tx(raw_bar(s), (uint32_t)(kg * ((GATHER ? 0 : p.stg_bytes) + NB * p.b_bytes)));
                     __syncwarp();
-                    if (lane < (1 + NB) * kg) {
+                    if (lane < (1 + NB) * kg && !(GATHER && lane < kg)) {   // GATHER: no A boxes
                         // Lanes 0..kg-1: A boxes; then kg B boxes (X3: kg heads, kg tails).
                         const bool is_a = lane < kg;
                         const int kk = is_a ? lane : (lane - kg) % kg;
@@ -1355,6 +1364,91 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 ptx::mma_commit(accf_bar(acc));
             }
             ptx::mma_commit(drain_bar);
+        }
+    } else if (warp >= L::kConvFirst && GATHER) {
+        // Converters, NCHW input: thread (warp - kConvFirst) * 32 + lane owns
+        // row `row` (output pixel m0 + row) of every A tile.  For each K step
+        // (filter tap, block of CB channels) it loads its pixel's CB input
+        // values from global memory (the 32 threads of a warp read 32
+        // consecutive output columns of one channel row), zero outside the
+        // image, past C_in and past M, and writes the TF32 head (the value
+        // with its low 13 mantissa bits cleared) and the exact remainder into
+        // the two operand tiles.
+        const int row = (warp - L::kConvFirst) * 32 + lane;
+        const size_t plane = (size_t)p.in_h * p.in_w;
+        int g = 0;
+        for (int uu = blockIdx.x; uu < num_units && !aborted(abort_flag); uu += gridDim.x) {
+            int t, st0, st1;
+            unit_range(uu, p.split, nstage, t, st0, st1);
+            int m0, n0;
+            tile_coords(t, p.n_tiles, kBM, m0, n0, p.BN);
+            const int m = m0 + row;
+            const bool mvalid = m < p.M;
+            const int img = mvalid ? m / p.OHW : 0;
+            const int rem = mvalid ? m - img * p.OHW : 0;
+            const int oh = rem / p.OW, ow = rem - (rem / p.OW) * p.OW;
+            const int ih0 = oh * p.stride - p.pad, iw0 = ow * p.stride - p.pad;
+            const float *ximg = p.x_nchw + (size_t)img * p.c_in * plane;
+            // Filter row, column and channel block of the unit's first K step.
+            const int i0 = st0 * kg;
+            const int tap0 = i0 / p.cblocks;
+            int cbk = i0 - tap0 * p.cblocks, r = tap0 / p.ks, cc = tap0 - (tap0 / p.ks) * p.ks;
+            bool ok = true;
+            for (int st = st0; st < st1; ++st, ++g) {
+                const int s = g % S, u = g / S;
+                // The stage's A tiles are free once the MMAs that read them
+                // have completed (the producer waits on the same barrier).
+                // Warp-uniform: the stage ends in __syncwarp.
+                const bool got = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(free_bar(s), (u & 1) ^ 1, kWaitLimitNs));
+                if (!got) {
+                    if (lane == 0) abort_now(p, abort_flag);
+                    ok = false;
+                    break;
+                }
+                const uint32_t sb = base + s * p.stage_bytes;
+                for (int kk = 0; kk < kg; ++kk) {
+                    const int ih = ih0 + r, iw = iw0 + cc, c0 = cbk * p.CB;
+                    const bool in = mvalid && (unsigned)ih < (unsigned)p.in_h && (unsigned)iw < (unsigned)p.in_w;
+                    const float *src = ximg + (in ? (size_t)c0 * plane + (size_t)ih * p.in_w + iw : 0);
+                    float v[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        v[c] = (in && c < p.CB && c0 + c < p.c_in) ? __ldg(src + (size_t)c * plane) : 0.0f;
+                    const uint32_t head_row = sb + stg_off + kk * stg_stride + row * p.RB;
+                    const uint32_t tail_row = sb + kk * p.a_bytes + row * p.RB;
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        if (c < p.CB) {
+                            uint32_t h[4];
+                            float l[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                h[q] = __float_as_uint(v[c + q]) & 0xFFFFE000u;
+                                l[q] = __fsub_rn(v[c + q], __uint_as_float(h[q]));
+                            }
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(swz(head_row + 4 * c, p.op_mask)),
+                                         "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                                         : "memory");
+                            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(swz(tail_row + 4 * c, p.op_mask)),
+                                         "f"(l[0]), "f"(l[1]), "f"(l[2]), "f"(l[3])
+                                         : "memory");
+                        }
+                    }
+                    // The next K step: channel block, then filter column, then row.
+                    if (++cbk == p.cblocks) {
+                        cbk = 0;
+                        if (++cc == p.ks) {
+                            cc = 0;
+                            ++r;
+                        }
+                    }
+                }
+                // Make the generic-proxy writes visible to the tensor cores.
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(conv_bar(s));
+            }
+            if (!ok) break;
         }
     } else if (warp >= L::kConvFirst && SK == kStagedX3) {
         // Converters: thread (warp - kConvFirst) * 32 + lane splits row `row`
@@ -2395,6 +2489,14 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
         P.in_h = d.h;
         P.in_w = d.w;
     } else if (x3) {
+        if (d.in_layout == CBS_NCHW) {
+            // NCHW input: the converter warps read x themselves (no A boxes).
+            if (d.c_in_b > 0) return fail(CBS_ERR_PLAN_MISMATCH, "two-input 3xTF32 plan with NCHW input");
+            P.x_nchw = static_cast<const float *>(x);
+            P.c_in = d.c_in;
+            P.in_h = d.h;
+            P.in_w = d.w;
+        }
         P.stg_bytes = kBM * XB;     // fp32 staging rows, swizzled like the operands (XB = RB)
         P.kpc = x3_kpc(CB);
         P.nchunks = x3_chunks(P.ksteps, P.kg, P.split, CB);
@@ -2500,7 +2602,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     } else if (d.c_in_b > 0) {
         CBS_TRY(make_a_map(&tmA, x, c_a, "A"));
         CBS_TRY(make_a_map(&tmA2, x_b, pl.c_in_pad - c_a, "A of x_b"));
-    } else {
+    } else if (!P.x_nchw) {
         CBS_TRY(make_a_map(&tmA, x, pl.c_in_pad, "A"));
         std::memcpy(&tmA2, &tmA, sizeof(tmA));
     }
@@ -2513,6 +2615,11 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
                       CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(RB), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuTensorMapEncodeTiled (B) failed (%d)", (int)r);
+    }
+    if (P.x_nchw) {
+        // No A boxes: the A parameters hold a valid map that is never read.
+        std::memcpy(&tmA, &tmB, sizeof(tmB));
+        std::memcpy(&tmA2, &tmB, sizeof(tmB));
     }
 
     dim3 grid(pl.grid_ctas, 1, 1);  // persistent: each CTA walks tiles blockIdx.x + i * gridDim.x
@@ -2529,12 +2636,12 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
         e = set_max_dyn_smem(kern, pl.smem_bytes);
         if (e == cudaSuccess) e = launch_kernel(kern, grid, kThreads, pl.smem_bytes, s, tmA, tmA2, tmB, tmY, P);
     } else if (i8) {
-        auto kern = tc_conv_staged_kernel<kStagedI8>;
+        auto kern = tc_conv_staged_kernel<kStagedI8, false>;
         e = set_max_dyn_smem(kern, pl.smem_bytes);
         if (e == cudaSuccess)
             e = launch_kernel(kern, grid, StagedLayout<kStagedI8>::kThreads, pl.smem_bytes, s, tmA, tmA2, tmB, P);
     } else {
-        auto kern = tc_conv_staged_kernel<kStagedX3>;
+        auto kern = P.x_nchw ? tc_conv_staged_kernel<kStagedX3, true> : tc_conv_staged_kernel<kStagedX3, false>;
         e = set_max_dyn_smem(kern, pl.smem_bytes);
         if (e == cudaSuccess)
             e = launch_kernel(kern, grid, StagedLayout<kStagedX3>::kThreads, pl.smem_bytes, s, tmA, tmA2, tmB, P);

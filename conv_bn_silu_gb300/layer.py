@@ -125,13 +125,6 @@ class FusedConvBnSilu:
     def empty_x(self):
         return torch.empty(self.x_shape(), dtype=self.x_dtype, device=self.device)
 
-    @property
-    def launches(self) -> int:
-        """Kernel launches of one call: two when the plan repacks an NCHW
-        input for the 3xTF32 kernel, else one."""
-        p = self.plan
-        return 2 if (p.variant == B.CBS_VARIANT_TC_TF32X3 and p.desc.in_layout == B.CBS_NCHW) else 1
-
     def empty_y(self):
         return torch.empty(self.y_shape(), dtype=self.x_dtype, device=self.device)
 

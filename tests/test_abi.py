@@ -46,8 +46,8 @@ def test_plan_fp32_layer_list(cuda_lib, i):
     s = wl.LAYER_LIST[i]
     p = B.cbs_plan(make_desc(1, s.c_in, s.h, s.width, s.c_out, s.k, s.stride))
     # Three-channel stems take the direct CUDA-core kernel; 3x3 stride-1 layers
-    # the 3xTF32 tensor-core kernel on an NHWC repack of the NCHW input (in the
-    # workspace); the rest the CUDA-core implicit GEMM.
+    # the 3xTF32 tensor-core kernel (reading the NCHW input as given); the rest
+    # the CUDA-core implicit GEMM.
     x3 = s.c_in > 4 and s.k == 3 and s.stride == 1
     assert p.variant == (B.CBS_VARIANT_STEM if s.c_in <= 4 else
                          B.CBS_VARIANT_TC_TF32X3 if x3 else B.CBS_VARIANT_SIMT_FP32)
@@ -60,9 +60,7 @@ def test_plan_fp32_layer_list(cuda_lib, i):
     assert p.m_tiles * p.block_m >= s.oh * s.ow
     assert p.n_tiles * p.block_n >= s.c_out
     if x3:
-        repack = (s.c_in * s.h * s.width * 4 + 255) // 256 * 256
-        assert p.workspace_bytes >= repack and p.grid_ctas <= 152
-        assert (p.workspace_bytes > repack) == (p.split_k > 1)
+        assert p.grid_ctas <= 152 and (p.workspace_bytes > 0) == (p.split_k > 1)
     else:
         assert p.split_k >= 1 and p.grid_ctas == p.m_tiles * p.n_tiles * p.split_k
         assert (p.workspace_bytes > 0) == (p.split_k > 1)
@@ -81,7 +79,6 @@ def test_fp32_nchw_tensor_core_rules(cuda_lib):
     assert auto(force_block_m=64).variant == B.CBS_VARIANT_SIMT_FP32        # a forced tile is the CUDA-core kernel's
     forced = auto(k=1, c_in=20, force_variant=X3)
     assert forced.variant == X3 and forced.c_in_pad == 24 and forced.x_bytes == 20 * 20 * 20 * 4
-    assert forced.workspace_bytes >= 24 * 20 * 20 * 4
     with pytest.raises(B.CbsError) as e:
         auto(c_in_b=32, force_variant=X3)
     assert e.value.status == B.CBS_ERR_UNSUPPORTED
