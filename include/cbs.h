@@ -190,9 +190,7 @@ typedef struct cbs_plan_t {
  *   TF32/BF16/INT8 and TF32X3 (FP32): x NHWC with c_in_pad channels (extra
  *   channels zero; TF32X3: c_in_pad = C_in rounded up to 8).
  *   TF32X3 with NCHW input (one input only): x NCHW float, exactly C_in
- *   channels; the call repacks it to NHWC at the start of the workspace
- *   (workspace_bytes includes those N*H*W*c_in_pad floats, rounded up to
- *   256 bytes, before the kernel's own split-K scratch).
+ *   channels, read as given by the kernel.
  *   STEM (chosen for C_in <= 4, C_out <= 64, k <= 7): x in d->in_layout;
  *   NHWC pixels hold c_in_pad = 4 channels for TF32/BF16/INT8, C_in for FP32.
  *   Two-input plans (d->c_in_b > 0): x holds the first c_in - c_in_b channels
