@@ -1111,12 +1111,15 @@ enum StagedKind { kStagedI8 = 0, kStagedX3 = 1 };
 // the INT8 layers, so INT8 runs 16 epilogue warps, each on 8-column groups;
 // X3 runs 8 on 16-column groups.  Epilogue warp w reads TMEM lane quadrant
 // w % 4, as tcgen05.ld requires.
-template <int SK>
+template <int SK, bool GATHER = false>
 struct StagedLayout {
     static constexpr int kEpi = SK == kStagedI8 ? 16 : 8;
     static constexpr int kEpiFirst = kMmaWarpI8 + 1;
     static constexpr int kConvFirst = kEpiFirst + kEpi;
-    static constexpr int kThreads = 32 * (kConvFirst + 4);
+    // Converter warps: 4, one row of 32 pixels each; the NCHW gather takes 8
+    // (two per row, each half of the channels) for twice the loads in flight.
+    static constexpr int kConv = GATHER ? 8 : 4;
+    static constexpr int kThreads = 32 * (kConvFirst + kConv);
     static constexpr int kGroup = SK == kStagedI8 ? 8 : 16;   // accumulator columns per TMEM load
 };
 static_assert(StagedLayout<kStagedX3>::kEpi <= kSplitCounterSlots, "one split-K counter per X3 epilogue warp");
@@ -1157,7 +1160,7 @@ __device__ __forceinline__ void x3_chunk_sum(uint32_t taddr, int nch, int chunk_
 //              head x head) into one FP32 accumulator, which drops only the
 //              tail x tail term: FP32-level accuracy on the tensor cores.
 template <int SK, bool GATHER>
-__global__ void __launch_bounds__(StagedLayout<SK>::kThreads, 1)
+__global__ void __launch_bounds__(StagedLayout<SK, GATHER>::kThreads, 1)
 tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                       const __grid_constant__ CUtensorMap tmB, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1188,7 +1191,7 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     const int stg_stride = (p.stg_bytes + 1023) & ~1023;
     const int nstage = p.ksteps / kg;
 
-    using L = StagedLayout<SK>;
+    using L = StagedLayout<SK, GATHER>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_tiles = p.m_tiles * p.n_tiles;
     const int num_units = num_tiles * p.split;   // X3 split-K: (tile, K part) units; else tiles
@@ -1199,7 +1202,7 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(raw_bar(s), 1);
-            ptx::mbar_init(conv_bar(s), 4);   // one arrive per converter warp
+            ptx::mbar_init(conv_bar(s), L::kConv);   // one arrive per converter warp
             ptx::mbar_init(free_bar(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -1374,7 +1377,11 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         // image, past C_in and past M, and writes the TF32 head (the value
         // with its low 13 mantissa bits cleared) and the exact remainder into
         // the two operand tiles.
-        const int row = (warp - L::kConvFirst) * 32 + lane;
+        // Warps kConvFirst + w and kConvFirst + 4 + w share rows 32 w ..
+        // 32 w + 31: the first takes channels 0 .. CB/2 - 1 of each K step,
+        // the second the rest.
+        const int row = ((warp - L::kConvFirst) & 3) * 32 + lane;
+        const int ch0 = ((warp - L::kConvFirst) >> 2) * (p.CB / 2), chn = p.CB / 2;
         const size_t plane = (size_t)p.in_h * p.in_w;
         int g = 0;
         for (int uu = blockIdx.x; uu < num_units && !aborted(abort_flag); uu += gridDim.x) {
@@ -1407,18 +1414,19 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 }
                 const uint32_t sb = base + s * p.stage_bytes;
                 for (int kk = 0; kk < kg; ++kk) {
-                    const int ih = ih0 + r, iw = iw0 + cc, c0 = cbk * p.CB;
+                    const int ih = ih0 + r, iw = iw0 + cc, c0 = cbk * p.CB + ch0;
                     const bool in = mvalid && (unsigned)ih < (unsigned)p.in_h && (unsigned)iw < (unsigned)p.in_w;
                     const float *src = ximg + (in ? (size_t)c0 * plane + (size_t)ih * p.in_w + iw : 0);
-                    float v[32];
+                    float v[16];
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        v[c] = (in && c < p.CB && c0 + c < p.c_in) ? __ldg(src + (size_t)c * plane) : 0.0f;
-                    const uint32_t head_row = sb + stg_off + kk * stg_stride + row * p.RB;
-                    const uint32_t tail_row = sb + kk * p.a_bytes + row * p.RB;
+                    for (int c = 0; c < 16; ++c)
+                        v[c] = (in && c < chn && c0 + c < p.c_in) ? __ldg(src + (size_t)c * plane) : 0.0f;
+                    // This warp's channels start ch0 channels (4 ch0 bytes) into the row.
+                    const uint32_t head_row = sb + stg_off + kk * stg_stride + row * p.RB + 4 * ch0;
+                    const uint32_t tail_row = sb + kk * p.a_bytes + row * p.RB + 4 * ch0;
 #pragma unroll
-                    for (int c = 0; c < 32; c += 4) {
-                        if (c < p.CB) {
+                    for (int c = 0; c < 16; c += 4) {
+                        if (c < chn) {
                             uint32_t h[4];
                             float l[4];
 #pragma unroll
@@ -2248,7 +2256,9 @@ cbs_status plan_tc(cbs_plan_t &p) {
         while (nprod > 1 && (stages < 2 * nprod)) nprod /= 2;
         stages = stages / nprod * nprod;
         p.stages = stages;
-        p.threads = i8 ? StagedLayout<kStagedI8>::kThreads : StagedLayout<kStagedX3>::kThreads;
+        p.threads = i8 ? StagedLayout<kStagedI8>::kThreads
+                       : d.in_layout == CBS_NCHW ? StagedLayout<kStagedX3, true>::kThreads   // NCHW: 8 converter warps
+                                                 : StagedLayout<kStagedX3>::kThreads;
         p.smem_bytes = 1024 + stages * stage + 8 * (3 * stages + 5) + 16;
         const long long tiles = (long long)p.m_tiles * p.n_tiles;
         // X3 split-K: the K stages of a tile in `split` parts, partial tiles
@@ -2642,9 +2652,10 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
             e = launch_kernel(kern, grid, StagedLayout<kStagedI8>::kThreads, pl.smem_bytes, s, tmA, tmA2, tmB, P);
     } else {
         auto kern = P.x_nchw ? tc_conv_staged_kernel<kStagedX3, true> : tc_conv_staged_kernel<kStagedX3, false>;
+        const int threads = P.x_nchw ? StagedLayout<kStagedX3, true>::kThreads : StagedLayout<kStagedX3>::kThreads;
+        if (pl.threads != threads) return fail(CBS_ERR_PLAN_MISMATCH, "threads %d", pl.threads);
         e = set_max_dyn_smem(kern, pl.smem_bytes);
-        if (e == cudaSuccess)
-            e = launch_kernel(kern, grid, StagedLayout<kStagedX3>::kThreads, pl.smem_bytes, s, tmA, tmA2, tmB, P);
+        if (e == cudaSuccess) e = launch_kernel(kern, grid, threads, pl.smem_bytes, s, tmA, tmA2, tmB, P);
     }
     return cuda_check(e, "tensor-core kernel launch");
 }

@@ -45,10 +45,11 @@ def test_status_strings(cuda_lib):
 def test_plan_fp32_layer_list(cuda_lib, i):
     s = wl.LAYER_LIST[i]
     p = B.cbs_plan(make_desc(1, s.c_in, s.h, s.width, s.c_out, s.k, s.stride))
-    # Three-channel stems take the direct CUDA-core kernel; 3x3 stride-1 layers
-    # the 3xTF32 tensor-core kernel (reading the NCHW input as given); the rest
-    # the CUDA-core implicit GEMM.
-    x3 = s.c_in > 4 and s.k == 3 and s.stride == 1
+    # Three-channel stems take the direct CUDA-core kernel; layers with 32 or
+    # more channels and a 3x3 filter, or 64 or more channels, the 3xTF32
+    # tensor-core kernel (reading the NCHW input as given); the rest the
+    # CUDA-core implicit GEMM.
+    x3 = s.c_in >= 32 and (s.k == 3 or s.c_in >= 64)
     assert p.variant == (B.CBS_VARIANT_STEM if s.c_in <= 4 else
                          B.CBS_VARIANT_TC_TF32X3 if x3 else B.CBS_VARIANT_SIMT_FP32)
     assert (p.oh, p.ow) == (s.oh, s.ow)
@@ -67,14 +68,18 @@ def test_plan_fp32_layer_list(cuda_lib, i):
 
 
 def test_fp32_nchw_tensor_core_rules(cuda_lib):
-    """NCHW FP32 layers go to the 3xTF32 kernel only for k >= 3 at stride 1
-    with C_in a multiple of 8 and nothing forced; forcing the variant takes
-    any one-input NCHW layer there; a two-input NCHW layer cannot."""
+    """NCHW FP32 layers go to the 3xTF32 kernel when C_in is a multiple of 8,
+    at least 32, and either k >= 3 or C_in >= 64, with nothing forced;
+    forcing the variant takes any one-input NCHW layer there; a two-input
+    NCHW layer cannot."""
     X3 = B.CBS_VARIANT_TC_TF32X3
     auto = lambda **kw: B.cbs_plan(make_desc(**dict(dict(n=1, c_in=64, h=20, w=20, c_out=64, k=3, stride=1), **kw)))
     assert auto().variant == X3
-    assert auto(stride=2).variant == B.CBS_VARIANT_SIMT_FP32
-    assert auto(k=1).variant == B.CBS_VARIANT_SIMT_FP32
+    assert auto(stride=2).variant == X3
+    assert auto(k=1).variant == X3
+    assert auto(k=1, c_in=32).variant == B.CBS_VARIANT_SIMT_FP32
+    assert auto(c_in=32).variant == X3
+    assert auto(c_in=16).variant == B.CBS_VARIANT_SIMT_FP32
     assert auto(c_in=60).variant == B.CBS_VARIANT_SIMT_FP32
     assert auto(force_block_m=64).variant == B.CBS_VARIANT_SIMT_FP32        # a forced tile is the CUDA-core kernel's
     forced = auto(k=1, c_in=20, force_variant=X3)

@@ -157,9 +157,11 @@ def test_automatic_choice(cuda_lib):
     assert variant(16, 64, 80, 64, 3, 1, **nhwc) == X3               # 6400 x 16 pixels
     assert variant(1, 64, 80, 64, 3, 1, **nhwc) == X3                # 50 tiles
     assert variant(1, 128, 40, 128, 3, 1, **nhwc) == X3                # 13 pixel tiles: K parts fill the SMs
-    assert variant(16, 64, 80, 64, 3, 1) == X3                        # NCHW input, 3x3 stride 1
-    assert variant(16, 64, 80, 64, 3, 2) == B.CBS_VARIANT_SIMT_FP32   # NCHW input, stride 2
-    assert variant(16, 64, 80, 64, 1, 1) == B.CBS_VARIANT_SIMT_FP32   # NCHW input, 1x1
+    assert variant(16, 64, 80, 64, 3, 1) == X3                        # NCHW input, 3x3
+    assert variant(16, 64, 80, 64, 3, 2) == X3                        # NCHW input, stride 2
+    assert variant(16, 64, 80, 64, 1, 1) == X3                        # NCHW input, 1x1 with 64 channels
+    assert variant(16, 32, 80, 64, 1, 1) == B.CBS_VARIANT_SIMT_FP32   # NCHW input, 1x1 with 32 channels
+    assert variant(16, 16, 80, 64, 3, 2) == B.CBS_VARIANT_SIMT_FP32   # NCHW input, 16 channels
     assert variant(16, 20, 80, 64, 3, 1, **nhwc) == B.CBS_VARIANT_SIMT_FP32   # 20 channels: would need padding
     assert variant(16, 3, 640, 16, 3, 2, **nhwc) == B.CBS_VARIANT_STEM
     p = B.cbs_plan(make_desc(16, 64, 80, 80, 64, 3, 1, prec=B.CBS_FP32, **nhwc))
@@ -374,7 +376,7 @@ def run_nchw(spec, x, p, out_layout=B.CBS_NCHW, residual=None, **kw):
     ((1, 16, 32, 3, 2, 320, 320), {"force_variant": X3}),   # list layer 2: 16 channels, 64-byte blocks
     ((1, 64, 64, 3, 1, 80, 80), {}),                         # list layer 6 (chosen without forcing)
     ((1, 256, 256, 3, 1, 20, 20), {}),                       # list layer 11: K parts in the workspace too
-    ((2, 24, 40, 3, 1, 17, 13), {}),                         # ragged pixels and output channels
+    ((2, 24, 40, 3, 1, 17, 13), {"force_variant": X3}),      # ragged pixels and output channels
     ((2, 24, 40, 3, 2, 17, 13), {"force_variant": X3}),      # the same at stride 2
     ((1, 20, 16, 3, 1, 9, 11), {"force_variant": X3}),       # C_in 20: the gather zero-fills channels 20..23
     ((3, 64, 96, 1, 1, 9, 9), {"force_variant": X3}),        # 1x1 on request
