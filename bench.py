@@ -1,7 +1,8 @@
 """Benchmark of the fused Conv2d + folded BN + SiLU layer on GB300.
 
-Default workload: the twelve-layer YOLO26n-scale list at batch 1 in FP32
-(CUDA-core variant), NCHW in and out.  One step = the twelve fused layers,
+Default workload: the twelve-layer YOLO26n-scale list at batch 1 in FP32,
+NCHW in and out (the planner's choice per layer: the 3xTF32 tensor-core
+kernel reading NCHW, the CUDA-core implicit GEMM, the direct stem kernel).  One step = the twelve fused layers,
 each on its own seeded synthetic input, all resident in HBM.  The K timed
 steps run as one captured CUDA graph (no host launch overhead inside the
 timed region) with timing events between every kernel, so each launch's
