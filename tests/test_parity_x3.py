@@ -417,3 +417,30 @@ def test_fp32_nchw_input_padded_rows_and_residual(cuda_lib):
     want = oracle.conv_bn_act_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, 1, 1, act=1, residual=r)
     assert rel_l2(y[..., :21], want) <= TOL_FP32_REL_L2
     assert np.all(y[..., 21:] == 7.0)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("i", [5, 10])
+def test_fp32_nchw_input_batch16(cuda_lib, i):
+    """List layers 6 and 11 at batch 16 with NCHW input, every image against
+    the oracle: the converter warps' gather over several tiles per persistent
+    CTA (layer 6: 800 tiles) and over K parts (layer 11), images crossed
+    inside tiles."""
+    spec = wl.LAYER_LIST[i]
+    x, p = wl.layer_inputs(spec, 16, layer_index=i)
+    y, layer = run_nchw(spec, x, p)
+    pl = layer.plan
+    assert pl.variant == X3 and (pl.m_tiles * pl.n_tiles > 152 or pl.split_k > 1)
+    e = rel_l2(y, ref_of(spec, x, p))
+    assert e <= TOL_FP32_REL_L2, e
+
+
+def test_nchw_mode_launch_shape(cuda_lib):
+    """Host-side: the NCHW mode runs 608 threads (eight converter warps), the
+    NHWC kernel 480 (four); both use the same tiles and shared memory."""
+    kw = dict(prec=B.CBS_FP32, force_variant=X3)
+    nchw = B.cbs_plan(make_desc(2, 64, 20, 20, 96, 3, 1, in_layout=B.CBS_NCHW, **kw))
+    nhwc = B.cbs_plan(make_desc(2, 64, 20, 20, 96, 3, 1, in_layout=B.CBS_NHWC, **kw))
+    assert (nchw.threads, nhwc.threads) == (608, 480)
+    assert (nchw.block_m, nchw.block_n, nchw.stages, nchw.split_k, nchw.smem_bytes) == \
+        (nhwc.block_m, nhwc.block_n, nhwc.stages, nhwc.split_k, nhwc.smem_bytes)
