@@ -380,6 +380,8 @@ def run_nchw(spec, x, p, out_layout=B.CBS_NCHW, residual=None, **kw):
     ((2, 24, 40, 3, 2, 17, 13), {"force_variant": X3}),      # the same at stride 2
     ((1, 20, 16, 3, 1, 9, 11), {"force_variant": X3}),       # C_in 20: the gather zero-fills channels 20..23
     ((3, 64, 96, 1, 1, 9, 9), {"force_variant": X3}),        # 1x1 on request
+    ((2, 32, 16, 3, 1, 1, 1), {"force_variant": X3}),        # 1x1 image: every tap but the centre in the padding
+    ((3, 64, 40, 3, 2, 1, 2), {"force_variant": X3}),        # 1x2 image at stride 2
     ((1, 128, 128, 3, 1, 40, 40), {"force_variant": X3, "force_split_k": 3}),   # forced K parts
 ])
 def test_fp32_nchw_input_on_tensor_cores(cuda_lib, out_layout, shape, kw):
