@@ -61,3 +61,25 @@ def test_compact_line_is_small_and_complete():
     for key in ("value", "unit", "cores", "kind", "sample"):
         assert key in d["cpu_baseline"], key
     assert "layers" not in d and "extra" not in d
+
+
+def test_traffic_figure_is_gated():
+    """bench.py reports the recorded DRAM traffic only for the variant it was
+    captured on and while the sources and plan-table entries hash to the
+    recorded digest; a changed source or another dominant kernel gives null."""
+    import bench
+    t = bench.TRAFFIC["layer_list_fp32_n1"]
+    assert bench.traffic_for("layer_list_fp32_n1", t["variant"]) == t["bytes"]
+    assert bench.traffic_for("layer_list_fp32_n1", (t["variant"] + 1) % 6) is None
+    assert bench.traffic_for("no_such_workload", t["variant"]) is None
+    saved = dict(t)
+    try:
+        t["digest"] = "0" * 16
+        assert bench.traffic_for("layer_list_fp32_n1", t["variant"]) is None
+    finally:
+        t.clear()
+        t.update(saved)
+    # the plan-table part of the digest covers only the workload's own entries
+    d0 = bench.sources_digest(("../tuned_plans.json",))
+    d1 = bench.sources_digest(("../tuned_plans.json",), table_prefix="2:", table_suffix=":1:1")
+    assert d0 != d1
