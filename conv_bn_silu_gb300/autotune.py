@@ -70,10 +70,17 @@ def candidates(prec, spec, base):
             for (bm, bn), sk in itertools.product(SIMT_TILES, (1, 2, 3, 4, 6, 8, 12, 16)):
                 yield dict(force_variant=B.CBS_VARIANT_SIMT_FP32, force_block_m=bm, force_block_n=bn,
                            force_split_k=sk)
-            # 3xTF32 on the library's NHWC repack of the input
+            # 3xTF32 reading the NCHW input: the converter warps' own loads,
+            # and flat TMA boxes where every filter row of a tile is one
+            # aligned run of a channel row
             if spec.c_in % 8 == 0:
+                flat = (spec.stride == 1 and spec.k <= 7 and spec.width % 4 == 0 and
+                        (base.n == 1 or (spec.oh * spec.ow) % 128 == 0))
                 for sk, bn in itertools.product((1, 2, 3, 4, 5, 6, 8), bns):
                     yield dict(force_variant=B.CBS_VARIANT_TC_TF32X3, force_split_k=sk, force_block_n=bn)
+                    if flat:
+                        yield dict(force_variant=B.CBS_VARIANT_TC_TF32X3, force_split_k=sk, force_block_n=bn,
+                                   force_window=1)
     elif prec == "int8":
         for kg, bn in itertools.product((1, 2, 3, 4), bns):
             yield dict(force_k_group=kg, force_block_n=bn)

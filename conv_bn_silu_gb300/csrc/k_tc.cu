@@ -143,9 +143,11 @@ struct TcParams {
     int s2, PR, plane1_off, tile_w, tile_h, ncol;
     uint32_t swz_a;            // descriptor swizzle code of the window's operand rows
     // 3xTF32 with NCHW input: the converter warps read x (N, c_in, in_h, in_w
-    // floats) themselves.
+    // floats) themselves, or (flat boxes) from one TMA box per K step of
+    // raw_bytes, raw_stride bytes apart in a stage.
     const float *x_nchw;
     int c_in;
+    int raw_bytes, raw_stride;
 };
 
 constexpr int kSplitCounterSlots = 8;   // one per epilogue warp
@@ -1111,14 +1113,31 @@ enum StagedKind { kStagedI8 = 0, kStagedX3 = 1 };
 // the INT8 layers, so INT8 runs 16 epilogue warps, each on 8-column groups;
 // X3 runs 8 on 16-column groups.  Epilogue warp w reads TMEM lane quadrant
 // w % 4, as tcgen05.ld requires.
-template <int SK, bool GATHER = false>
+// How the 3xTF32 kernel's A operand arrives:
+//   kX3Nhwc:   NHWC input, TMA im2col or 2-D boxes into the fp32 staging tile;
+//   kX3Gather: NCHW input, the converter warps load it from global memory;
+//   kX3Flat:   NCHW input of a stride-1 layer with k = 2 pad + 1 (output grid
+//              = input grid), batch 1 or whole tiles per image: a channel
+//              row of the image is a flat run of H W floats, and the input
+//              of filter tap (r, s) at pixel m of a tile is element
+//              m + (r - pad) W + (s - pad) of it, except where s - pad takes
+//              a column past the row's ends.  One TMA box of kFlatBoxW
+//              pixels x CB channels per K step, from the 16-byte aligned
+//              element m0 + (r - pad) W - 4, serves the column offsets
+//              -pad .. pad of the filter row (the planner takes pad <= 3);
+//              rows above and below the image are the box's zero fill, and
+//              the converters zero the columns that wrap.
+constexpr int kX3Nhwc = 0, kX3Gather = 1, kX3Flat = 2;
+constexpr int kFlatBoxW = 136;   // 128 pixels + 4 either side
+
+template <int SK, int AMODE = kX3Nhwc>
 struct StagedLayout {
     static constexpr int kEpi = SK == kStagedI8 ? 16 : 8;
     static constexpr int kEpiFirst = kMmaWarpI8 + 1;
     static constexpr int kConvFirst = kEpiFirst + kEpi;
-    // Converter warps: 4, one row of 32 pixels each; the NCHW gather takes 8
-    // (two per row, each half of the channels) for twice the loads in flight.
-    static constexpr int kConv = GATHER ? 8 : 4;
+    // Converter warps: 4, one row of 32 pixels each; the NCHW modes take 8
+    // (two per row, each half of the channels): twice the loads in flight.
+    static constexpr int kConv = AMODE != kX3Nhwc ? 8 : 4;
     static constexpr int kThreads = 32 * (kConvFirst + kConv);
     static constexpr int kGroup = SK == kStagedI8 ? 8 : 16;   // accumulator columns per TMEM load
 };
@@ -1159,8 +1178,8 @@ __device__ __forceinline__ void x3_chunk_sum(uint32_t taddr, int nch, int chunk_
 //              slice runs three kind::tf32 MMAs (tail x head, head x tail,
 //              head x head) into one FP32 accumulator, which drops only the
 //              tail x tail term: FP32-level accuracy on the tensor cores.
-template <int SK, bool GATHER>
-__global__ void __launch_bounds__(StagedLayout<SK, GATHER>::kThreads, 1)
+template <int SK, int AMODE>
+__global__ void __launch_bounds__(StagedLayout<SK, AMODE>::kThreads, 1)
 tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                       const __grid_constant__ CUtensorMap tmB, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1191,14 +1210,18 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     const int stg_stride = (p.stg_bytes + 1023) & ~1023;
     const int nstage = p.ksteps / kg;
 
-    using L = StagedLayout<SK, GATHER>;
+    using L = StagedLayout<SK, AMODE>;
+    constexpr bool GATHER = AMODE == kX3Gather, FLAT = AMODE == kX3Flat;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_tiles = p.m_tiles * p.n_tiles;
     const int num_units = num_tiles * p.split;   // X3 split-K: (tile, K part) units; else tiles
 
     // GATHER (3xTF32, NCHW input): the producers load the weights only; the
     // converter warps read the activations from global memory themselves.
-    static_assert(!GATHER || SK == kStagedX3, "the NCHW gather is the 3xTF32 kernel's");
+    // FLAT: the producers load one box of raw NCHW input per K step, after
+    // the stage's head tiles (raw_off), for the converters to split.
+    static_assert(AMODE == kX3Nhwc || SK == kStagedX3, "the NCHW modes are the 3xTF32 kernel's");
+    const int raw_off = stg_off + kg * stg_stride;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(raw_bar(s), 1);
@@ -1268,7 +1291,8 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     }
                     const uint32_t sb = base + s * p.stage_bytes;
                     if (lane == 0)
-                        ptx::mbar_arrive_expect_tx(raw_bar(s), (uint32_t)(kg * ((GATHER ? 0 : p.stg_bytes) + NB * p.b_bytes)));
+                        ptx::mbar_arrive_expect_tx(
+                            raw_bar(s), (uint32_t)(kg * ((GATHER ? 0 : FLAT ? p.raw_bytes : p.stg_bytes) + NB * p.b_bytes)));
                     __syncwarp();
                     if (lane < (1 + NB) * kg && !(GATHER && lane < kg)) {   // GATHER: no A boxes
                         // Lanes 0..kg-1: A boxes; then kg B boxes (X3: kg heads, kg tails).
@@ -1277,7 +1301,18 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                         const int tail = is_a ? 0 : (lane - kg) / kg;
                         const int i = st * kg + kk;
                         const int tap = i / p.cblocks, cb = i - tap * p.cblocks;
-                        if (is_a) {
+                        if (FLAT && is_a) {
+                            // Filter row r's pixels of this tile: elements x0 + 4 ..
+                            // x0 + 131 (+ s - pad) of channel rows y0 .. y0 + CB - 1.
+                            const int r = tap / p.ks;
+                            const int x0 = (m0 - img * p.OHW) + (r - p.pad) * p.in_w - 4;
+                            const int y0 = img * p.c_in + cb * p.CB;
+                            if (x0 & 3) {
+                                abort_now(p, abort_flag);   // the planner keeps x0 16-byte aligned
+                            } else {
+                                ptx::tma_load_2d(sb + raw_off + kk * p.raw_stride, &tmA, raw_bar(s), x0, y0);
+                            }
+                        } else if (is_a) {
                             const int r = tap / p.ks, tt = tap - r * p.ks;
                             const uint32_t dst = sb + stg_off + kk * stg_stride;
                             const bool second = cb >= p.ca_blocks;   // channel block of the second input
@@ -1449,6 +1484,84 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                             cc = 0;
                             ++r;
                         }
+                    }
+                }
+                // Make the generic-proxy writes visible to the tensor cores.
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(conv_bar(s));
+            }
+            if (!ok) break;
+        }
+    } else if (warp >= L::kConvFirst && FLAT) {
+        // Converters, NCHW input in flat boxes: thread (warp - kConvFirst) * 32
+        // + lane owns row `row` (output pixel m0 + row) of every A tile, as in
+        // the gather above, but reads its values from the stage's raw box
+        // (channel c of the K step at element c * kFlatBoxW + row + 4 + s - pad,
+        // consecutive rows at consecutive words), zero where the filter
+        // column leaves the image row, past C_in and past M.
+        const int row = ((warp - L::kConvFirst) & 3) * 32 + lane;
+        const int ch0 = ((warp - L::kConvFirst) >> 2) * (p.CB / 2), chn = p.CB / 2;
+        int g = 0;
+        for (int uu = blockIdx.x; uu < num_units && !aborted(abort_flag); uu += gridDim.x) {
+            int t, st0, st1;
+            unit_range(uu, p.split, nstage, t, st0, st1);
+            int m0, n0;
+            tile_coords(t, p.n_tiles, kBM, m0, n0, p.BN);
+            const int m = m0 + row;
+            const bool mvalid = m < p.M;
+            const int ow = mvalid ? (m % p.OHW) % p.OW : 0;
+            const int i0 = st0 * kg;
+            const int tap0 = i0 / p.cblocks;
+            int cbk = i0 - tap0 * p.cblocks, cc = tap0 - (tap0 / p.ks) * p.ks;
+            bool ok = true;
+            for (int st = st0; st < st1; ++st, ++g) {
+                const int s = g % S, u = g / S;
+                // The raw boxes and the B tiles have landed; the producer
+                // waited for the stage's previous MMAs before loading them.
+                const bool got = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(raw_bar(s), u & 1, kWaitLimitNs));
+                if (!got) {
+                    if (lane == 0) abort_now(p, abort_flag);
+                    ok = false;
+                    break;
+                }
+                const uint32_t sb = base + s * p.stage_bytes;
+                for (int kk = 0; kk < kg; ++kk) {
+                    const int iw = ow + cc - p.pad, c0 = cbk * p.CB + ch0;
+                    const bool in = mvalid && (unsigned)iw < (unsigned)p.in_w;
+                    const uint32_t src = sb + raw_off + kk * p.raw_stride + 4u * (ch0 * kFlatBoxW + row + 4 + cc - p.pad);
+                    float v[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        v[c] = 0.0f;
+                        if (in && c < chn && c0 + c < p.c_in)
+                            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[c]) : "r"(src + 4u * c * kFlatBoxW));
+                    }
+                    const uint32_t head_row = sb + stg_off + kk * stg_stride + row * p.RB + 4 * ch0;
+                    const uint32_t tail_row = sb + kk * p.a_bytes + row * p.RB + 4 * ch0;
+#pragma unroll
+                    for (int c = 0; c < 16; c += 4) {
+                        if (c < chn) {
+                            uint32_t h[4];
+                            float l[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                h[q] = __float_as_uint(v[c + q]) & 0xFFFFE000u;
+                                l[q] = __fsub_rn(v[c + q], __uint_as_float(h[q]));
+                            }
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(swz(head_row + 4 * c, p.op_mask)),
+                                         "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                                         : "memory");
+                            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(swz(tail_row + 4 * c, p.op_mask)),
+                                         "f"(l[0]), "f"(l[1]), "f"(l[2]), "f"(l[3])
+                                         : "memory");
+                        }
+                    }
+                    // The next K step: channel block, then filter column (the
+                    // row is the producer's).
+                    if (++cbk == p.cblocks) {
+                        cbk = 0;
+                        if (++cc == p.ks) cc = 0;
                     }
                 }
                 // Make the generic-proxy writes visible to the tensor cores.
@@ -2158,11 +2271,25 @@ cbs_status plan_tc(cbs_plan_t &p) {
         // columns (rounded to a power of two): nchunks * next_pow2(BN) <= 256.
         int max_bn = 256;
         while (max_bn >= 16 && nchunks * max_bn > 256) max_bn /= 2;
+        // X3 with NCHW input: flat boxes (window = 1) for stride-1 layers
+        // whose output grid is the input grid, with W a multiple of 4 (the
+        // boxes start 16-byte aligned) and no tile spanning two images.
+        const bool flat_fits = x3 && d.in_layout == CBS_NCHW && d.c_in_b == 0 && d.stride == 1 &&
+                               d.k == 2 * d.pad + 1 && d.pad <= 3 && d.w % 4 == 0 &&
+                               (d.n == 1 || ((long long)p.oh * p.ow) % kBM == 0) &&
+                               (long long)d.n * d.c_in < (1LL << 31);
+        if (x3 && d.force_window > 0 && !flat_fits)
+            return fail(CBS_ERR_UNSUPPORTED,
+                        "flat input boxes need 3xTF32 with one NCHW input, stride 1, k = 2 pad + 1 <= 7, W a "
+                        "multiple of 4 and batch 1 or whole 128-pixel tiles per image");
+        const bool flat = flat_fits && d.force_window > 0;
+        p.window = flat ? 1 : 0;
         // One K step: operand A (INT8: bf16; X3: the tail), the weights
         // (X3: head and tail), the staging tile (int8 codes; X3: fp32, the
-        // head once converted).
+        // head once converted), and with flat boxes the raw box.
         auto kstep_bytes_of = [&](int c) {
-            return kBM * RB + (x3 ? 2 : 1) * round_up(c * RB, 1024) + round_up(kBM * (x3 ? RB : CB), 1024);
+            return kBM * RB + (x3 ? 2 : 1) * round_up(c * RB, 1024) + round_up(kBM * (x3 ? RB : CB), 1024) +
+                   (flat ? round_up(kFlatBoxW * CB * 4, 1024) : 0);
         };
         // K steps per stage: the MMA issuer waits twice per stage, so a stage
         // carries the most K steps (up to 4, dividing the K steps) that still
@@ -2256,8 +2383,10 @@ cbs_status plan_tc(cbs_plan_t &p) {
         while (nprod > 1 && (stages < 2 * nprod)) nprod /= 2;
         stages = stages / nprod * nprod;
         p.stages = stages;
+        static_assert(StagedLayout<kStagedX3, kX3Gather>::kThreads == StagedLayout<kStagedX3, kX3Flat>::kThreads,
+                      "the NCHW modes launch the same threads");
         p.threads = i8 ? StagedLayout<kStagedI8>::kThreads
-                       : d.in_layout == CBS_NCHW ? StagedLayout<kStagedX3, true>::kThreads   // NCHW: 8 converter warps
+                       : d.in_layout == CBS_NCHW ? StagedLayout<kStagedX3, kX3Gather>::kThreads   // 8 converter warps
                                                  : StagedLayout<kStagedX3>::kThreads;
         p.smem_bytes = 1024 + stages * stage + 8 * (3 * stages + 5) + 16;
         const long long tiles = (long long)p.m_tiles * p.n_tiles;
@@ -2420,7 +2549,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     P.win = staged ? 0 : pl.window;
     P.split = pl.split_k < 1 ? 1 : pl.split_k;
     if (P.split > 1) {
-        if (i8 || pl.window || pl.b_resident)
+        if (i8 || P.win || pl.b_resident)
             return fail(CBS_ERR_PLAN_MISMATCH, "split-K plan with windowed A, resident weights or INT8");
         if (!workspace) return fail(CBS_ERR_WORKSPACE, "split-K plan without a workspace");
         const size_t counter_bytes = (size_t)round_up(pl.m_tiles * pl.n_tiles * kSplitCounterSlots * 4, 256);
@@ -2464,7 +2593,9 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
         int nprod = kMaxProducersI8;
         while (nprod > 1 && (pl.stages < 2 * nprod || pl.stages % nprod != 0)) nprod /= 2;
         P.nprod = nprod;
-        P.stage_bytes = P.kg * (P.a_bytes + (x3 ? 2 : 1) * P.b_tile_stride + round_up(kBM * XB, 1024));
+        // 3xTF32 flat NCHW boxes: one raw box per K step after the head tiles.
+        const int raw_stride = (x3 && d.in_layout == CBS_NCHW && pl.window) ? round_up(kFlatBoxW * CB * 4, 1024) : 0;
+        P.stage_bytes = P.kg * (P.a_bytes + (x3 ? 2 : 1) * P.b_tile_stride + round_up(kBM * XB, 1024) + raw_stride);
         if (1024 + pl.stages * P.stage_bytes + 8 * (3 * pl.stages + 5) + 16 > pl.smem_bytes)
             return fail(CBS_ERR_PLAN_MISMATCH, "plan's shared memory does not hold its stages");
     } else {
@@ -2500,12 +2631,22 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
         P.in_w = d.w;
     } else if (x3) {
         if (d.in_layout == CBS_NCHW) {
-            // NCHW input: the converter warps read x themselves (no A boxes).
+            // NCHW input: the converter warps read x themselves (no A boxes),
+            // or split the flat boxes the producers load.
             if (d.c_in_b > 0) return fail(CBS_ERR_PLAN_MISMATCH, "two-input 3xTF32 plan with NCHW input");
             P.x_nchw = static_cast<const float *>(x);
             P.c_in = d.c_in;
             P.in_h = d.h;
             P.in_w = d.w;
+            if (pl.window) {
+                if (d.stride != 1 || d.k != 2 * d.pad + 1 || d.pad > 3 || d.w % 4 || pl.oh != d.h || pl.ow != d.w ||
+                    (d.n > 1 && P.OHW % kBM))
+                    return fail(CBS_ERR_PLAN_MISMATCH, "flat input boxes for this shape");
+                P.raw_bytes = kFlatBoxW * CB * 4;
+                P.raw_stride = round_up(P.raw_bytes, 1024);   // as in the stage size above
+            }
+        } else if (pl.window) {
+            return fail(CBS_ERR_PLAN_MISMATCH, "3xTF32 flat input boxes with NHWC input");
         }
         P.stg_bytes = kBM * XB;     // fp32 staging rows, swizzled like the operands (XB = RB)
         P.kpc = x3_kpc(CB);
@@ -2612,6 +2753,16 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
     } else if (d.c_in_b > 0) {
         CBS_TRY(make_a_map(&tmA, x, c_a, "A"));
         CBS_TRY(make_a_map(&tmA2, x_b, pl.c_in_pad - c_a, "A of x_b"));
+    } else if (P.x_nchw && P.raw_bytes) {
+        // Flat boxes: x as rows of H W floats, one per (image, channel).
+        const cuuint64_t dims[2] = {(cuuint64_t)d.h * d.w, (cuuint64_t)d.n * d.c_in};
+        const cuuint64_t strides[1] = {(cuuint64_t)d.h * d.w * 4};
+        const cuuint32_t box[2] = {(cuuint32_t)kFlatBoxW, (cuuint32_t)CB};
+        const CUresult res = fns.tiled(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(x), dims, strides,
+                                       box, estr1, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                       CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (res != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuTensorMapEncodeTiled (flat NCHW boxes) failed (%d)", (int)res);
+        std::memcpy(&tmA2, &tmA, sizeof(tmA));
     } else if (!P.x_nchw) {
         CBS_TRY(make_a_map(&tmA, x, pl.c_in_pad, "A"));
         std::memcpy(&tmA2, &tmA, sizeof(tmA));
@@ -2626,7 +2777,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(CBS_ERR_CUDA, "cuTensorMapEncodeTiled (B) failed (%d)", (int)r);
     }
-    if (P.x_nchw) {
+    if (P.x_nchw && !P.raw_bytes) {
         // No A boxes: the A parameters hold a valid map that is never read.
         std::memcpy(&tmA, &tmB, sizeof(tmB));
         std::memcpy(&tmA2, &tmB, sizeof(tmB));
@@ -2646,13 +2797,15 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
         e = set_max_dyn_smem(kern, pl.smem_bytes);
         if (e == cudaSuccess) e = launch_kernel(kern, grid, kThreads, pl.smem_bytes, s, tmA, tmA2, tmB, tmY, P);
     } else if (i8) {
-        auto kern = tc_conv_staged_kernel<kStagedI8, false>;
+        auto kern = tc_conv_staged_kernel<kStagedI8, kX3Nhwc>;
         e = set_max_dyn_smem(kern, pl.smem_bytes);
         if (e == cudaSuccess)
             e = launch_kernel(kern, grid, StagedLayout<kStagedI8>::kThreads, pl.smem_bytes, s, tmA, tmA2, tmB, P);
     } else {
-        auto kern = P.x_nchw ? tc_conv_staged_kernel<kStagedX3, true> : tc_conv_staged_kernel<kStagedX3, false>;
-        const int threads = P.x_nchw ? StagedLayout<kStagedX3, true>::kThreads : StagedLayout<kStagedX3>::kThreads;
+        auto kern = !P.x_nchw    ? tc_conv_staged_kernel<kStagedX3, kX3Nhwc>
+                    : P.raw_bytes ? tc_conv_staged_kernel<kStagedX3, kX3Flat>
+                                  : tc_conv_staged_kernel<kStagedX3, kX3Gather>;
+        const int threads = P.x_nchw ? StagedLayout<kStagedX3, kX3Gather>::kThreads : StagedLayout<kStagedX3>::kThreads;
         if (pl.threads != threads) return fail(CBS_ERR_PLAN_MISMATCH, "threads %d", pl.threads);
         e = set_max_dyn_smem(kern, pl.smem_bytes);
         if (e == cudaSuccess) e = launch_kernel(kern, grid, threads, pl.smem_bytes, s, tmA, tmA2, tmB, P);

@@ -102,7 +102,12 @@ typedef struct cbs_layer_desc {
     int force_b_resident;/* TF32/BF16: 0 = choose; 1 = keep weights resident in shared memory;
                             -1 = stream them with every K step */
     int force_window;    /* TF32/BF16: 1 = windowed A (stride 1, odd k, pad k/2, channel blocks of
-                            128 bytes); 0 or -1 = im2col A */
+                            128 bytes); 0 or -1 = im2col A.
+                            TF32X3 with NCHW input: 1 = flat input boxes (stride 1, k = 2 pad + 1
+                            <= 7, W a multiple of 4, and N = 1 or OH*OW a multiple of 128;
+                            CBS_ERR_UNSUPPORTED otherwise); 0 or -1 = the converter warps load the
+                            input themselves.  TF32X3 with NHWC input: must not be 1.  The
+                            CUDA-core, stem and INT8 variants ignore it. */
     int activation;      /* cbs_activation (0 = SiLU) */
     int residual;        /* 1: add a residual tensor to the activated output, y = act(z) + r
                             (page 1's profile: the element-wise adds beside the convolutions);
@@ -149,7 +154,11 @@ typedef struct cbs_plan_t {
     int window;             /* TF32/BF16, stride 1: 1 = each tile loads its zero-padded input
                                window once per channel block and every filter tap reads a
                                shifted view of it (block_m positions of the padded grid
-                               oh * (W + 2 pad) + ow'); 0 = one im2col box per tap */
+                               oh * (W + 2 pad) + ow'); 0 = one im2col box per tap.
+                               TF32X3 with NCHW input: 1 = each K step's input arrives as one
+                               TMA box of 136 pixels of a filter row's flat H*W channel rows
+                               (the converter warps zero the columns that wrap); 0 = the
+                               converter warps load it from global memory */
     int issuer_split;       /* TF32/BF16: 2 = each 128-pixel tile's K stages alternate between
                                two MMA-issuing threads (see force_issuer_split); else 1 */
     int c_in_pad;           /* channels per input pixel as stored (NHWC tensor-core variants

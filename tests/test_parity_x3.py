@@ -437,6 +437,109 @@ def test_fp32_nchw_input_batch16(cuda_lib, i):
     assert e <= TOL_FP32_REL_L2, e
 
 
+FLAT = {"force_variant": X3, "force_window": 1}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("out_layout", [B.CBS_NCHW, B.CBS_NHWC])
+@pytest.mark.parametrize("shape,kw", [
+    ((1, 64, 64, 1, 1, 80, 80), FLAT),                       # list layer 5: 1x1
+    ((1, 64, 64, 3, 1, 80, 80), FLAT),                       # list layer 6
+    ((1, 128, 128, 3, 1, 40, 40), FLAT),                     # list layer 8
+    ((1, 256, 256, 1, 1, 20, 20), FLAT),                     # list layer 10
+    ((1, 256, 256, 3, 1, 20, 20), FLAT),                     # list layer 11: K parts in the workspace
+    ((1, 384, 128, 1, 1, 40, 40), FLAT),                     # list layer 12
+    ((1, 20, 16, 3, 1, 12, 12), FLAT),                       # C_in 20: 8-channel blocks, channels 20..23 zero
+    ((2, 24, 40, 3, 1, 16, 16), FLAT),                       # batch 2, two whole tiles per image
+    ((1, 32, 48, 5, 1, 20, 24), FLAT),                       # 5x5, pad 2
+    ((1, 32, 16, 7, 1, 12, 8), FLAT),                        # 7x7, pad 3: column offsets -3..3
+    ((1, 64, 64, 3, 1, 4, 4), FLAT),                         # 4x4 image: one partial tile, rows in the fill
+    ((1, 32, 40, 3, 1, 8, 100), FLAT),                       # rows of 100: tiles end mid-row
+    ((1, 128, 128, 3, 1, 40, 40), dict(FLAT, force_split_k=3)),   # forced K parts
+])
+def test_fp32_nchw_flat_boxes(cuda_lib, out_layout, shape, kw):
+    """NCHW input in flat TMA boxes (stride-1 layers with k = 2 pad + 1):
+    every filter row's pixels as one box per K step, the wrapped columns
+    zeroed by the converters."""
+    n, c_in, c_out, k, stride, h, w = shape
+    spec = wl.LayerSpec(c_in, c_out, k, stride, h, w)
+    x, p = wl.layer_inputs(spec, n, layer_index=36)
+    y, layer = run_nchw(spec, x, p, out_layout, **kw)
+    pl = layer.plan
+    assert pl.variant == X3 and pl.window == 1 and pl.threads == 608
+    assert pl.x_bytes == x.nbytes
+    e = rel_l2(y, ref_of(spec, x, p))
+    assert e <= TOL_FP32_REL_L2, e
+    y2, _ = run_nchw(spec, x, p, out_layout, **kw)
+    assert np.array_equal(y, y2)
+    # the same numbers as the gather, up to the order of the partial sums
+    yg, lg = run_nchw(spec, x, p, out_layout, **{kk: v for kk, v in kw.items() if kk != "force_window"})
+    assert lg.plan.window == 0
+    assert rel_l2(y, yg) <= TOL_FP32_REL_L2
+
+
+@pytest.mark.gpu
+def test_fp32_nchw_flat_boxes_padded_rows_and_residual(cuda_lib):
+    """Flat boxes with a padded NCHW output pitch, the identity activation
+    and a residual: columns past OW stay untouched."""
+    spec = wl.LayerSpec(32, 48, 3, 1, 20, 20)
+    x, p = wl.layer_inputs(spec, 1, layer_index=37)
+    r = np.random.default_rng(7).standard_normal((1, 48, 20, 20)).astype(np.float32)
+    stride = 24
+    rp = np.zeros((1, 48, 20, stride), np.float32)
+    rp[..., :20] = r
+    d = make_desc(1, 32, 20, 20, 48, 3, 1, prec=B.CBS_FP32, in_layout=B.CBS_NCHW, out_layout=B.CBS_NCHW,
+                  out_row_stride=stride, activation=B.CBS_ACT_IDENTITY, residual=1, **FLAT)
+    layer = FusedConvBnSilu(d, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, tuned=False)
+    assert layer.plan.variant == X3 and layer.plan.window == 1
+    y = torch.full((1, 48, 20, stride), 7.0, device="cuda")
+    layer(torch.from_numpy(x).cuda(), y, residual=torch.from_numpy(rp).cuda())
+    y = y.cpu().numpy()
+    want = oracle.conv_bn_act_f32(x, p.w, p.gamma, p.beta, p.mean, p.var, p.eps, 1, 1, act=1, residual=r)
+    assert rel_l2(y[..., :20], want) <= TOL_FP32_REL_L2
+    assert np.all(y[..., 20:] == 7.0)
+
+
+@pytest.mark.gpu
+def test_fp32_nchw_flat_boxes_batch16(cuda_lib):
+    """List layer 6 at batch 16 in flat boxes, every image against the
+    oracle: 50 whole tiles per image, persistent CTAs walking several."""
+    spec = wl.LAYER_LIST[5]
+    x, p = wl.layer_inputs(spec, 16, layer_index=5)
+    y, layer = run_nchw(spec, x, p, **FLAT)
+    assert layer.plan.window == 1 and layer.plan.m_tiles == 800
+    e = rel_l2(y, ref_of(spec, x, p))
+    assert e <= TOL_FP32_REL_L2, e
+
+
+def test_nchw_flat_box_rules(cuda_lib):
+    """Host-side: flat boxes only where every filter row of a tile is one
+    aligned run of an NCHW channel row; their raw boxes add to each stage."""
+    def plan(n, c_in, h, w, k, stride, pad=None, **kw):
+        return B.cbs_plan(make_desc(n, c_in, h, w, 64, k, stride, pad, prec=B.CBS_FP32, in_layout=B.CBS_NCHW,
+                                    **dict(FLAT, **kw)))
+    pl = plan(1, 64, 80, 80, 3, 1)
+    assert pl.window == 1 and pl.threads == 608
+    gather = B.cbs_plan(make_desc(1, 64, 80, 80, 64, 3, 1, prec=B.CBS_FP32, in_layout=B.CBS_NCHW,
+                                  force_variant=X3, force_split_k=pl.split_k, force_block_n=pl.block_n))
+    assert gather.window == 0
+    def kstep_bytes(q):   # shared memory = 1 KB alignment + stages x K steps + barriers
+        return (q.smem_bytes - 1024 - 8 * (3 * q.stages + 5) - 16) // (q.stages * q.k_group)
+    assert kstep_bytes(pl) - kstep_bytes(gather) == 136 * 32 * 4   # one raw box of 136 pixels x 32 channels
+    assert plan(2, 64, 16, 16, 3, 1).window == 1            # 256 pixels: two whole tiles per image
+    for bad in (dict(n=1, c_in=64, h=80, w=80, k=3, stride=2),     # stride 2
+                dict(n=1, c_in=64, h=80, w=80, k=3, stride=1, pad=0),   # output grid smaller than the input
+                dict(n=1, c_in=64, h=21, w=21, k=3, stride=1),     # W not a multiple of 4
+                dict(n=2, c_in=64, h=20, w=20, k=3, stride=1),     # 400 pixels: tiles would span images
+                dict(n=1, c_in=64, h=20, w=20, k=9, stride=1)):    # pad 4: column offsets past the box
+        with pytest.raises(B.CbsError) as ei:
+            plan(**bad)
+        assert ei.value.status == B.CBS_ERR_UNSUPPORTED
+    with pytest.raises(B.CbsError) as ei:
+        B.cbs_plan(make_desc(1, 64, 80, 80, 64, 3, 1, prec=B.CBS_FP32, in_layout=B.CBS_NHWC, **FLAT))
+    assert ei.value.status == B.CBS_ERR_UNSUPPORTED
+
+
 def test_nchw_mode_launch_shape(cuda_lib):
     """Host-side: the NCHW mode runs 608 threads (eight converter warps), the
     NHWC kernel 480 (four); both use the same tiles and shared memory."""
