@@ -143,11 +143,11 @@ struct TcParams {
     int s2, PR, plane1_off, tile_w, tile_h, ncol;
     uint32_t swz_a;            // descriptor swizzle code of the window's operand rows
     // 3xTF32 with NCHW input: the converter warps read x (N, c_in, in_h, in_w
-    // floats) themselves, or (flat boxes) from one TMA box per K step of
-    // raw_bytes, raw_stride bytes apart in a stage.
+    // floats) themselves, or (flat boxes) from one TMA box of raw_bytes per
+    // K step, landed over the stage's A tiles.
     const float *x_nchw;
     int c_in;
-    int raw_bytes, raw_stride;
+    int raw_bytes;
 };
 
 constexpr int kSplitCounterSlots = 8;   // one per epilogue warp
@@ -1126,7 +1126,11 @@ enum StagedKind { kStagedI8 = 0, kStagedX3 = 1 };
 //              element m0 + (r - pad) W - 4, serves the column offsets
 //              -pad .. pad of the filter row (the planner takes pad <= 3);
 //              rows above and below the image are the box's zero fill, and
-//              the converters zero the columns that wrap.
+//              the converters zero the columns that wrap.  The box lands
+//              over the stage's A tail and head tiles, which the converters
+//              then overwrite with the split values (one K step per stage:
+//              [B head | B tail | A tail | A head]), so a stage is no larger
+//              than the gather's.
 constexpr int kX3Nhwc = 0, kX3Gather = 1, kX3Flat = 2;
 constexpr int kFlatBoxW = 136;   // 128 pixels + 4 either side
 
@@ -1218,10 +1222,11 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
 
     // GATHER (3xTF32, NCHW input): the producers load the weights only; the
     // converter warps read the activations from global memory themselves.
-    // FLAT: the producers load one box of raw NCHW input per K step, after
-    // the stage's head tiles (raw_off), for the converters to split.
+    // FLAT (one K step per stage): the weight tiles first, then the A tail
+    // and head tiles, where the producers land the raw NCHW box.
     static_assert(AMODE == kX3Nhwc || SK == kStagedX3, "the NCHW modes are the 3xTF32 kernel's");
-    const int raw_off = stg_off + kg * stg_stride;
+    const int b_off = FLAT ? 0 : op_b_off;
+    const int flat_tail = NB * p.b_tile_stride, flat_head = flat_tail + p.a_bytes;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(raw_bar(s), 1);
@@ -1310,7 +1315,7 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                             if (x0 & 3) {
                                 abort_now(p, abort_flag);   // the planner keeps x0 16-byte aligned
                             } else {
-                                ptx::tma_load_2d(sb + raw_off + kk * p.raw_stride, &tmA, raw_bar(s), x0, y0);
+                                ptx::tma_load_2d(sb + flat_tail, &tmA, raw_bar(s), x0, y0);
                             }
                         } else if (is_a) {
                             const int r = tap / p.ks, tt = tap - r * p.ks;
@@ -1325,7 +1330,7 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                                 ptx::tma_load_2d(dst, tm, raw_bar(s), c0, m0);
                         } else {
                             // X3 weight tails are rows C_out.. of the packed weights.
-                            ptx::tma_load_2d(sb + op_b_off + (tail * kg + kk) * p.b_tile_stride, &tmB, raw_bar(s),
+                            ptx::tma_load_2d(sb + b_off + (tail * kg + kk) * p.b_tile_stride, &tmB, raw_bar(s),
                                              tap * p.c_in_pad + cb * p.CB, n0 + tail * p.C_out);
                         }
                     }
@@ -1378,9 +1383,10 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                             }
                             const bool first = kc++ == 0;
                             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_stride + chunk * p.chunk_stride);
-                            const uint32_t a_head = sb + stg_off + kk * stg_stride, a_tail = sb + kk * p.a_bytes;
-                            const uint32_t b_head = sb + op_b_off + kk * p.b_tile_stride;
-                            const uint32_t b_tail = sb + op_b_off + (kg + kk) * p.b_tile_stride;
+                            const uint32_t a_head = sb + (FLAT ? flat_head : stg_off + kk * stg_stride);
+                            const uint32_t a_tail = sb + (FLAT ? flat_tail : kk * p.a_bytes);
+                            const uint32_t b_head = sb + b_off + kk * p.b_tile_stride;
+                            const uint32_t b_tail = sb + b_off + (kg + kk) * p.b_tile_stride;
                             issue_kstep<kTF32>(d_tmem, dhi, a_tail, b_head, p.idesc, kslices, first);
                             issue_kstep<kTF32>(d_tmem, dhi, a_head, b_tail, p.idesc, kslices, false);
                             issue_kstep<kTF32>(d_tmem, dhi, a_head, b_head, p.idesc, kslices, false);
@@ -1494,16 +1500,20 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             if (!ok) break;
         }
     } else if (warp >= L::kConvFirst && FLAT) {
-        // Converters, NCHW input in flat boxes: thread (warp - kConvFirst) * 32
-        // + lane owns row `row` (output pixel m0 + row) of every A tile, as in
-        // the gather above, but reads its values from the stage's raw box
-        // (channel c of the K step at element c * kFlatBoxW + row + 4 + s - pad,
-        // consecutive rows at consecutive words), zero where the filter
-        // column leaves the image row, past C_in and past M.
+        // Converters, NCHW input in flat boxes (one K step per stage): thread
+        // (warp - kConvFirst) * 32 + lane owns row `row` (output pixel m0 +
+        // row) of the A tiles, as in the gather above, but reads its values
+        // from the stage's raw box (channel c of the K step at element
+        // c * kFlatBoxW + row + 4 + s - pad: consecutive rows at consecutive
+        // words), zero where the filter column leaves the image row, past
+        // C_in and past M.  The box lies over the A tiles, so the eight warps
+        // all finish reading before any writes: named barrier 2, whose OR of
+        // the warps' failures also makes them leave together.
         const int row = ((warp - L::kConvFirst) & 3) * 32 + lane;
         const int ch0 = ((warp - L::kConvFirst) >> 2) * (p.CB / 2), chn = p.CB / 2;
         int g = 0;
-        for (int uu = blockIdx.x; uu < num_units && !aborted(abort_flag); uu += gridDim.x) {
+        bool stop = false;
+        for (int uu = blockIdx.x; uu < num_units && !stop; uu += gridDim.x) {
             int t, st0, st1;
             unit_range(uu, p.split, nstage, t, st0, st1);
             int m0, n0;
@@ -1511,65 +1521,60 @@ tc_conv_staged_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             const int m = m0 + row;
             const bool mvalid = m < p.M;
             const int ow = mvalid ? (m % p.OHW) % p.OW : 0;
-            const int i0 = st0 * kg;
-            const int tap0 = i0 / p.cblocks;
-            int cbk = i0 - tap0 * p.cblocks, cc = tap0 - (tap0 / p.ks) * p.ks;
-            bool ok = true;
+            const int tap0 = st0 / p.cblocks;
+            int cbk = st0 - tap0 * p.cblocks, cc = tap0 - (tap0 / p.ks) * p.ks;
             for (int st = st0; st < st1; ++st, ++g) {
                 const int s = g % S, u = g / S;
-                // The raw boxes and the B tiles have landed; the producer
+                // The raw box and the B tiles have landed; the producer
                 // waited for the stage's previous MMAs before loading them.
-                const bool got = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(raw_bar(s), u & 1, kWaitLimitNs));
-                if (!got) {
-                    if (lane == 0) abort_now(p, abort_flag);
-                    ok = false;
+                const bool got = ptx::mbar_wait_bounded(raw_bar(s), u & 1, kWaitLimitNs);
+                const uint32_t sb = base + s * p.stage_bytes;
+                const int iw = ow + cc - p.pad, c0 = cbk * p.CB + ch0;
+                const bool in = got && mvalid && (unsigned)iw < (unsigned)p.in_w;
+                const uint32_t src = sb + flat_tail + 4u * (ch0 * kFlatBoxW + row + 4 + cc - p.pad);
+                float v[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    v[c] = 0.0f;
+                    if (in && c < chn && c0 + c < p.c_in)
+                        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[c]) : "r"(src + 4u * c * kFlatBoxW));
+                }
+                if (ptx::bar_red_or(2, 32 * L::kConv, !got || aborted(abort_flag))) {
+                    if (!got) abort_now(p, abort_flag);
+                    stop = true;
                     break;
                 }
-                const uint32_t sb = base + s * p.stage_bytes;
-                for (int kk = 0; kk < kg; ++kk) {
-                    const int iw = ow + cc - p.pad, c0 = cbk * p.CB + ch0;
-                    const bool in = mvalid && (unsigned)iw < (unsigned)p.in_w;
-                    const uint32_t src = sb + raw_off + kk * p.raw_stride + 4u * (ch0 * kFlatBoxW + row + 4 + cc - p.pad);
-                    float v[16];
+                const uint32_t head_row = sb + flat_head + row * p.RB + 4 * ch0;
+                const uint32_t tail_row = sb + flat_tail + row * p.RB + 4 * ch0;
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        v[c] = 0.0f;
-                        if (in && c < chn && c0 + c < p.c_in)
-                            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[c]) : "r"(src + 4u * c * kFlatBoxW));
-                    }
-                    const uint32_t head_row = sb + stg_off + kk * stg_stride + row * p.RB + 4 * ch0;
-                    const uint32_t tail_row = sb + kk * p.a_bytes + row * p.RB + 4 * ch0;
+                for (int c = 0; c < 16; c += 4) {
+                    if (c < chn) {
+                        uint32_t h[4];
+                        float l[4];
 #pragma unroll
-                    for (int c = 0; c < 16; c += 4) {
-                        if (c < chn) {
-                            uint32_t h[4];
-                            float l[4];
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                h[q] = __float_as_uint(v[c + q]) & 0xFFFFE000u;
-                                l[q] = __fsub_rn(v[c + q], __uint_as_float(h[q]));
-                            }
-                            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(swz(head_row + 4 * c, p.op_mask)),
-                                         "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
-                                         : "memory");
-                            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(swz(tail_row + 4 * c, p.op_mask)),
-                                         "f"(l[0]), "f"(l[1]), "f"(l[2]), "f"(l[3])
-                                         : "memory");
+                        for (int q = 0; q < 4; ++q) {
+                            h[q] = __float_as_uint(v[c + q]) & 0xFFFFE000u;
+                            l[q] = __fsub_rn(v[c + q], __uint_as_float(h[q]));
                         }
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(swz(head_row + 4 * c, p.op_mask)),
+                                     "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                                     : "memory");
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(swz(tail_row + 4 * c, p.op_mask)),
+                                     "f"(l[0]), "f"(l[1]), "f"(l[2]), "f"(l[3])
+                                     : "memory");
                     }
-                    // The next K step: channel block, then filter column (the
-                    // row is the producer's).
-                    if (++cbk == p.cblocks) {
-                        cbk = 0;
-                        if (++cc == p.ks) cc = 0;
-                    }
+                }
+                // The next K step: channel block, then filter column (the
+                // row is the producer's).
+                if (++cbk == p.cblocks) {
+                    cbk = 0;
+                    if (++cc == p.ks) cc = 0;
                 }
                 // Make the generic-proxy writes visible to the tensor cores.
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(conv_bar(s));
             }
-            if (!ok) break;
         }
     } else if (warp >= L::kConvFirst && SK == kStagedX3) {
         // Converters: thread (warp - kConvFirst) * 32 + lane splits row `row`
@@ -2286,16 +2291,17 @@ cbs_status plan_tc(cbs_plan_t &p) {
         p.window = flat ? 1 : 0;
         // One K step: operand A (INT8: bf16; X3: the tail), the weights
         // (X3: head and tail), the staging tile (int8 codes; X3: fp32, the
-        // head once converted), and with flat boxes the raw box.
+        // head once converted).  A flat box lands over the A tail and head.
         auto kstep_bytes_of = [&](int c) {
-            return kBM * RB + (x3 ? 2 : 1) * round_up(c * RB, 1024) + round_up(kBM * (x3 ? RB : CB), 1024) +
-                   (flat ? round_up(kFlatBoxW * CB * 4, 1024) : 0);
+            return kBM * RB + (x3 ? 2 : 1) * round_up(c * RB, 1024) + round_up(kBM * (x3 ? RB : CB), 1024);
         };
+        static_assert(kFlatBoxW <= 2 * kBM, "a flat box (kFlatBoxW x CB floats) fits the A tail and head tiles");
         // K steps per stage: the MMA issuer waits twice per stage, so a stage
         // carries the most K steps (up to 4, dividing the K steps) that still
         // leave two stages in shared memory; a split needs at least as many
         // stages per tile as parts.
         auto kgroup_of = [&](int c, int want_split) {
+            if (flat) return 1;   // the box lands over the stage's one K step of A tiles
             const int kb = kstep_bytes_of(c);
             for (int g = 4; g >= 1; --g) {
                 if (d.force_k_group > 0 && g != d.force_k_group) continue;
@@ -2593,9 +2599,7 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
         int nprod = kMaxProducersI8;
         while (nprod > 1 && (pl.stages < 2 * nprod || pl.stages % nprod != 0)) nprod /= 2;
         P.nprod = nprod;
-        // 3xTF32 flat NCHW boxes: one raw box per K step after the head tiles.
-        const int raw_stride = (x3 && d.in_layout == CBS_NCHW && pl.window) ? round_up(kFlatBoxW * CB * 4, 1024) : 0;
-        P.stage_bytes = P.kg * (P.a_bytes + (x3 ? 2 : 1) * P.b_tile_stride + round_up(kBM * XB, 1024) + raw_stride);
+        P.stage_bytes = P.kg * (P.a_bytes + (x3 ? 2 : 1) * P.b_tile_stride + round_up(kBM * XB, 1024));
         if (1024 + pl.stages * P.stage_bytes + 8 * (3 * pl.stages + 5) + 16 > pl.smem_bytes)
             return fail(CBS_ERR_PLAN_MISMATCH, "plan's shared memory does not hold its stages");
     } else {
@@ -2640,10 +2644,9 @@ cbs_status launch_tc(const cbs_plan_t &pl, const void *x, const void *x_b, const
             P.in_w = d.w;
             if (pl.window) {
                 if (d.stride != 1 || d.k != 2 * d.pad + 1 || d.pad > 3 || d.w % 4 || pl.oh != d.h || pl.ow != d.w ||
-                    (d.n > 1 && P.OHW % kBM))
+                    (d.n > 1 && P.OHW % kBM) || P.kg != 1)
                     return fail(CBS_ERR_PLAN_MISMATCH, "flat input boxes for this shape");
-                P.raw_bytes = kFlatBoxW * CB * 4;
-                P.raw_stride = round_up(P.raw_bytes, 1024);   // as in the stage size above
+                P.raw_bytes = kFlatBoxW * CB * 4;   // over the A tail (kBM * RB bytes) and into the head
             }
         } else if (pl.window) {
             return fail(CBS_ERR_PLAN_MISMATCH, "3xTF32 flat input boxes with NHWC input");

@@ -514,7 +514,8 @@ def test_fp32_nchw_flat_boxes_batch16(cuda_lib):
 
 def test_nchw_flat_box_rules(cuda_lib):
     """Host-side: flat boxes only where every filter row of a tile is one
-    aligned run of an NCHW channel row; their raw boxes add to each stage."""
+    aligned run of an NCHW channel row; a box lands over its K step's A
+    tiles, so a stage (one K step) is the size of the gather's K step."""
     def plan(n, c_in, h, w, k, stride, pad=None, **kw):
         return B.cbs_plan(make_desc(n, c_in, h, w, 64, k, stride, pad, prec=B.CBS_FP32, in_layout=B.CBS_NCHW,
                                     **dict(FLAT, **kw)))
@@ -525,7 +526,8 @@ def test_nchw_flat_box_rules(cuda_lib):
     assert gather.window == 0
     def kstep_bytes(q):   # shared memory = 1 KB alignment + stages x K steps + barriers
         return (q.smem_bytes - 1024 - 8 * (3 * q.stages + 5) - 16) // (q.stages * q.k_group)
-    assert kstep_bytes(pl) - kstep_bytes(gather) == 136 * 32 * 4   # one raw box of 136 pixels x 32 channels
+    assert pl.k_group == 1 and kstep_bytes(pl) == kstep_bytes(gather)
+    assert kstep_bytes(pl) >= 136 * 32 * 4 + 2 * 64 * 128   # the box and the two weight tiles
     assert plan(2, 64, 16, 16, 3, 1).window == 1            # 256 pixels: two whole tiles per image
     for bad in (dict(n=1, c_in=64, h=80, w=80, k=3, stride=2),     # stride 2
                 dict(n=1, c_in=64, h=80, w=80, k=3, stride=1, pad=0),   # output grid smaller than the input
