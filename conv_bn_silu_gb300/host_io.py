@@ -8,7 +8,11 @@ memory, `HostPipeline.run` enqueues
   - layer j's device-to-host output copy on a second copy stream, as soon as
     an event marks the layer as finished;
 so the host link carries inputs and outputs in both directions while the
-kernels run, instead of copy-all / compute-all / copy-all.
+kernels run, instead of copy-all / compute-all / copy-all.  With
+`per_layer=False` a step is copy-all / compute-all / copy-all after all:
+the kernels then follow one another with no event between them (the
+library's programmatic dependent launches overlap their set-up), and the
+copies overlap the neighbouring steps' kernels instead.
 `DoubleBufferedRunner` alternates two such steps on two buffer sets, so one
 step's copies also overlap the neighbouring step's kernels.  The copies are
 cudaMemcpyAsync calls (torch's copy_ on pinned memory) and every layer is a
@@ -22,8 +26,9 @@ import torch
 
 
 class HostPipeline:
-    def __init__(self, n_layers: int, device="cuda"):
+    def __init__(self, n_layers: int, device="cuda", per_layer: bool = True):
         device = torch.device(device)
+        self.per_layer = per_layer
         self.h2d = torch.cuda.Stream(device)
         self.compute = torch.cuda.Stream(device)
         self.d2h = torch.cuda.Stream(device)
@@ -42,6 +47,16 @@ class HostPipeline:
                 xs_d[j].copy_(xs_h[j], non_blocking=True)
                 self.ev_in[j].record(self.h2d)
         sid = self.compute.cuda_stream
+        if not self.per_layer:
+            self.compute.wait_event(self.ev_in[n - 1])   # the copies run in order: all inputs landed
+            for j in range(n):
+                calls[j](sid)
+            self.ev_out[n - 1].record(self.compute)
+            self.d2h.wait_event(self.ev_out[n - 1])
+            with torch.cuda.stream(self.d2h):
+                for j in range(n):
+                    ys_h[j].copy_(ys_d[j], non_blocking=True)
+            return
         for j in range(n):
             self.compute.wait_event(self.ev_in[j])
             calls[j](sid)
@@ -61,7 +76,10 @@ class HostPipeline:
         """The same work recorded once as a CUDA graph (copies, kernels and
         the events between the three streams become graph nodes and edges),
         so a step costs one launch on the host.  Returns a function that
-        replays it and returns once every output is in ys_h."""
+        replays it and returns once every output is in ys_h; the function
+        holds every tensor the graph uses.  Steps that may run at the same
+        time (DoubleBufferedRunner) need their own layer workspaces
+        (FusedConvBnSilu.fork)."""
         graph = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream(self.compute.device)
         cap.wait_stream(torch.cuda.current_stream())
@@ -77,23 +95,28 @@ class HostPipeline:
             if wait:
                 cap.synchronize()
         replay.stream = cap
+        # The graph's copy and kernel nodes hold raw addresses of these
+        # tensors (and of whatever `calls` closes over): they live as long
+        # as the replay does.
+        replay.keep = (graph, calls, xs_h, xs_d, ys_d, ys_h)
         return replay
 
 
 class DoubleBufferedRunner:
-    """Back-to-back steps with two sets of buffers: step i uses set i % 2, and
+    """Back-to-back steps with two (or more) sets of buffers: step i uses set
+    i % len(replays), and
     each set's captured step (HostPipeline.capture) replays on its own stream,
     so step i + 1's input copies run while step i computes and its outputs
     are read back.  A set's next step starts only after its previous one has
     finished (same stream), so no buffer is overwritten while in use."""
 
     def __init__(self, replays):
-        assert len(replays) == 2
+        assert len(replays) >= 2
         self.replays = replays
 
     def run(self, steps: int) -> None:
         """Enqueue `steps` steps, then wait until every output is on the host."""
         for i in range(steps):
-            self.replays[i % 2](wait=False)
+            self.replays[i % len(self.replays)](wait=False)
         for r in self.replays:
             r.stream.synchronize()

@@ -6,6 +6,7 @@ libcbs.so's kernels.
 """
 from __future__ import annotations
 
+import copy
 import torch
 
 from . import _binding as B
@@ -94,6 +95,17 @@ class FusedConvBnSilu:
         if self.workspace is not None:
             B.cbs_workspace_init(self.workspace, int(p.workspace_bytes), s)
         self._keep = (raw, cb)  # inputs of the asynchronous fold stay alive
+
+    def fork(self) -> "FusedConvBnSilu":
+        """The same layer (plan, folded weights and bias shared) with a
+        split-K workspace of its own, for calls that may run at the same time
+        as this layer's on another stream: two launches sharing one workspace
+        would mix their partial tiles and arrival counters."""
+        twin = copy.copy(self)
+        if self.workspace is not None:
+            twin.workspace = torch.empty_like(self.workspace)
+            B.cbs_workspace_init(twin.workspace, int(self.plan.workspace_bytes), current_stream())
+        return twin
 
     # ---------------------------------------------------------------- shapes
     @property

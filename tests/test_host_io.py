@@ -12,8 +12,9 @@ from conv_bn_silu_gb300.layer import FusedConvBnSilu, make_desc
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("per_layer", [True, False])
 @pytest.mark.parametrize("prec", [B.CBS_FP32, B.CBS_BF16])
-def test_pipeline_matches_device_runs(cuda_lib, prec):
+def test_pipeline_matches_device_runs(cuda_lib, prec, per_layer):
     specs = [wl.LayerSpec(16, 32, 3, 2, 64), wl.LayerSpec(32, 32, 1, 1, 40), wl.LayerSpec(64, 128, 3, 1, 20)]
     layers, xs_d = [], []
     for i, s in enumerate(specs):
@@ -27,7 +28,7 @@ def test_pipeline_matches_device_runs(cuda_lib, prec):
     xs_h = [x.cpu().pin_memory() for x in xs_d]
     ys_d = [layer.empty_y() for layer in layers]
     ys_h = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys_d]
-    pipe = HostPipeline(len(layers))
+    pipe = HostPipeline(len(layers), per_layer=per_layer)
     calls = [(lambda st, j=j: layers[j](xs_d[j], ys_d[j], stream=st)) for j in range(len(layers))]
     replay = pipe.capture(calls, xs_h, xs_d, ys_d, ys_h)
     for run in range(6):
@@ -44,9 +45,10 @@ def test_pipeline_matches_device_runs(cuda_lib, prec):
             assert torch.equal(ys_h[j], want[j]), (run, j)
 
 
-def test_double_buffered_runner(cuda_lib):
-    """Two buffer sets, two steps in flight: every step's outputs reach the
-    host and equal a device-resident run."""
+@pytest.mark.parametrize("sets,per_layer", [(2, True), (3, False)])
+def test_double_buffered_runner(cuda_lib, sets, per_layer):
+    """Two or three buffer sets, as many steps in flight: every step's
+    outputs reach the host and equal a device-resident run."""
     from conv_bn_silu_gb300.host_io import DoubleBufferedRunner
     s = wl.LayerSpec(32, 64, 3, 1, 40)
     x, p = wl.layer_inputs(s, 2, layer_index=40)
@@ -54,16 +56,18 @@ def test_double_buffered_runner(cuda_lib):
                             p.beta, p.mean, p.var, p.eps)
     want = layer(torch.from_numpy(x).cuda()).cpu()
     replays, hosts = [], []
-    for r in range(2):
+    for r in range(sets):
         xd, yd = [torch.from_numpy(x).cuda()], [layer.empty_y()]
         xh, yh = [torch.from_numpy(x).pin_memory()], [torch.empty(yd[0].shape).pin_memory()]
-        calls = [lambda st, xd=xd, yd=yd: layer(xd[0], yd[0], stream=st)]
-        replays.append(HostPipeline(1).capture(calls, xh, xd, yd, yh))
+        mine = layer.fork()   # steps in flight together: a split-K workspace each
+        calls = [lambda st, xd=xd, yd=yd, mine=mine: mine(xd[0], yd[0], stream=st)]
+        replays.append(HostPipeline(1, per_layer=per_layer).capture(calls, xh, xd, yd, yh))
         hosts.append(yh[0])
+    torch.cuda.synchronize()   # the forked workspaces are initialised on the current stream
     runner = DoubleBufferedRunner(replays)
     for steps in (1, 2, 7):
         for h in hosts:
             h.zero_()
         runner.run(steps)
-        for r in range(min(steps, 2)):
+        for r in range(min(steps, sets)):
             assert torch.equal(hosts[r], want), (steps, r)
