@@ -581,17 +581,21 @@ def run_e2e(w, device, args, flops_step, world):
     its inputs from pinned host memory (FP32 activations for the FP32 list;
     the packed input format otherwise), runs the layers and reads every output
     back.  Each step is one CUDA graph (conv_bn_silu_gb300.host_io).  The
-    reported value runs three steps in flight on three buffer sets, each step
-    copying all its inputs in, running its layers back to back and copying
-    all its outputs out, so the copies overlap the neighbouring steps'
-    kernels (measured on GB300 for the FP32 list: 0.209-0.211 ms per step,
-    against 0.220-0.222 ms with two sets and each layer's copies overlapping
-    the same step's other layers, whose per-layer events break the kernels'
-    programmatic dependent launches).  A list with fewer than three buffer
-    sets runs two steps in flight with per-layer overlap.  The
-    one-step-at-a-time figure, where the host waits for every step's result,
-    is reported beside it.  The chain copies its frame in and its last output
-    out, one step at a time."""
+    reported value runs four steps in flight on four buffer sets (each with
+    layers of its own split-K workspaces).  A set keeps the step's inputs,
+    and its outputs, as views of one buffer each way, so a step is one copy
+    in, the twelve layers back to back (their programmatic dependent
+    launches intact) and one copy out; the copies overlap the neighbouring
+    steps' kernels.  Measured on GB300 for the FP32 list:
+      0.171-0.174 ms per step, about the device-resident step;
+      0.209-0.211 ms with one copy per tensor;
+      0.220-0.222 ms with two sets and each layer's copies overlapping the
+        same step's other layers, whose per-layer events break the kernels'
+        programmatic dependent launches.
+    A list with fewer than three buffer sets runs two steps in flight with
+    per-layer overlap.  The one-step-at-a-time figure, where the host waits
+    for every step's result, is reported beside it.  The chain copies its
+    frame in and its last output out, one step at a time."""
     import torch
     from conv_bn_silu_gb300.host_io import HostPipeline
     stream = torch.cuda.Stream(device)
@@ -604,7 +608,7 @@ def run_e2e(w, device, args, flops_step, world):
 
     pipelined = None
     if hasattr(w, "xs"):
-        from conv_bn_silu_gb300.host_io import DoubleBufferedRunner
+        from conv_bn_silu_gb300.host_io import DoubleBufferedRunner, pack_layout, packed_views
 
         def capture_set(r, xh, yh, per_layer=True, own_workspaces=False):
             # Steps in flight together run the same layers at once: each
@@ -619,11 +623,33 @@ def run_e2e(w, device, args, flops_step, world):
             return ([x.clone().pin_memory() for x in xs_h],
                     [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys_h])
 
+        x_off, x_total = pack_layout(xs_d)
+        y_off, y_total = pack_layout(ys_d)
+
+        def capture_packed_set(r):
+            # The step's inputs and outputs as views of one device buffer
+            # each, filled from and read back to one pinned host buffer each.
+            layers = [layer.fork() for layer in w.layers]
+            xd = torch.empty(x_total, dtype=torch.uint8, device=device)
+            yd = torch.empty(y_total, dtype=torch.uint8, device=device)
+            xh = torch.empty(x_total, dtype=torch.uint8).pin_memory()
+            yh = torch.empty(y_total, dtype=torch.uint8).pin_memory()
+            for v, x in zip(packed_views(xh, xs_h, x_off), xs_h):
+                v.copy_(x)
+            xv, yv = packed_views(xd, xs_d, x_off), packed_views(yd, ys_d, y_off)
+
+            def call(st):
+                for j in range(len(layers)):
+                    layers[j](xv[j], yv[j], s_y=w.s_y[j], stream=st, residual=w.rs[r][j])
+            return HostPipeline(1, device, per_layer=False).capture([call], [xh], [xd], [yd], [yh])
+
         one = capture_set(0, xs_h, ys_h)
+        packed_sets = 0
         if w.R >= 3:
-            pipelined = DoubleBufferedRunner([capture_set(r, *host_set(), per_layer=False, own_workspaces=True)
-                                              for r in range(3)])
-            pipe_mode = "three steps in flight, whole-step host I/O"
+            packed_sets = min(4, w.R)
+            pipelined = DoubleBufferedRunner([capture_packed_set(r) for r in range(packed_sets)])
+            pipe_mode = (f"{packed_sets} steps in flight, each one copy in and one copy out "
+                         "(inputs and outputs packed in one pinned buffer each way)")
         elif w.R >= 2:
             pipelined = DoubleBufferedRunner([capture_set(r, *host_set(), own_workspaces=True) for r in range(2)])
             pipe_mode = "two steps in flight, double-buffered host I/O"
@@ -646,6 +672,8 @@ def run_e2e(w, device, args, flops_step, world):
     dt_sync = (time.perf_counter() - t) / steps
     h2d = sum(x.numel() * x.element_size() for x in xs_h)
     d2h = sum(y.numel() * y.element_size() for y in ys_h)
+    if pipelined is not None and packed_sets:
+        h2d, d2h = x_total, y_total   # the packed buffers, alignment gaps included
     out = {"h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps, "unit": "TFLOP/s"}
     if pipelined is not None:
         # Throughput with several steps in flight (a buffer set each): every

@@ -102,6 +102,26 @@ class HostPipeline:
         return replay
 
 
+def pack_layout(like: Sequence[torch.Tensor], align: int = 256):
+    """Byte offsets that place tensors shaped like `like` one after another
+    in one buffer, each start a multiple of `align` bytes (the kernels' TMA
+    loads need 16), and the buffer's total size."""
+    offsets, off = [], 0
+    for t in like:
+        offsets.append(off)
+        off += -(-t.numel() * t.element_size() // align) * align
+    return offsets, off
+
+
+def packed_views(buf: torch.Tensor, like: Sequence[torch.Tensor], offsets) -> list:
+    """Views of the uint8 tensor `buf` at `offsets` with the shapes and
+    dtypes of `like`.  A step whose inputs (or outputs) are such views of
+    one buffer moves them with one copy each way, which the host link
+    carries faster than one copy per tensor."""
+    return [buf.narrow(0, o, t.numel() * t.element_size()).view(t.dtype).view(t.shape)
+            for t, o in zip(like, offsets)]
+
+
 class DoubleBufferedRunner:
     """Back-to-back steps with two (or more) sets of buffers: step i uses set
     i % len(replays), and

@@ -71,3 +71,48 @@ def test_double_buffered_runner(cuda_lib, sets, per_layer):
         runner.run(steps)
         for r in range(min(steps, sets)):
             assert torch.equal(hosts[r], want), (steps, r)
+
+
+def test_packed_sets_match_device_runs(cuda_lib):
+    """Three buffer sets in flight, each step's inputs and outputs packed in
+    one buffer per direction (one copy each way), the layers forked per set:
+    every set's outputs equal device-resident runs."""
+    from conv_bn_silu_gb300.host_io import DoubleBufferedRunner, pack_layout, packed_views
+    specs = [wl.LayerSpec(16, 32, 3, 2, 64), wl.LayerSpec(32, 48, 3, 1, 40), wl.LayerSpec(64, 64, 1, 1, 20)]
+    layers, xs = [], []
+    for i, s in enumerate(specs):
+        x, p = wl.layer_inputs(s, 1, layer_index=50 + i)
+        layers.append(FusedConvBnSilu(make_desc(1, s.c_in, s.h, s.width, s.c_out, s.k, s.stride, s.pad),
+                                      p.w, p.gamma, p.beta, p.mean, p.var, p.eps))
+        xs.append(torch.from_numpy(x))
+    want = [layer(x.cuda()).cpu() for layer, x in zip(layers, xs)]
+    ys_like = [layer.empty_y() for layer in layers]
+    x_off, x_total = pack_layout(xs)
+    y_off, y_total = pack_layout(ys_like)
+    replays, outs = [], []
+    for r in range(3):
+        mine = [layer.fork() for layer in layers]
+        xd = torch.zeros(x_total, dtype=torch.uint8, device="cuda")
+        yd = torch.zeros(y_total, dtype=torch.uint8, device="cuda")
+        xh = torch.empty(x_total, dtype=torch.uint8).pin_memory()
+        yh = torch.empty(y_total, dtype=torch.uint8).pin_memory()
+        for v, x in zip(packed_views(xh, xs, x_off), xs):
+            v.copy_(x)
+        xv, yv = packed_views(xd, xs, x_off), packed_views(yd, ys_like, y_off)
+
+        def call(st, mine=mine, xv=xv, yv=yv):
+            for j in range(len(mine)):
+                mine[j](xv[j], yv[j], stream=st)
+        replays.append(HostPipeline(1, per_layer=False).capture([call], [xh], [xd], [yd], [yh]))
+        outs.append(packed_views(yh, ys_like, y_off))
+    torch.cuda.synchronize()
+    runner = DoubleBufferedRunner(replays)
+    for steps in (3, 8):
+        for o in outs:
+            for t in o:
+                t.zero_()
+        runner.run(steps)
+        for r in range(3):
+            for j in range(len(layers)):
+                assert torch.equal(outs[r][j], want[j]), (steps, r, j)
+    assert B.cbs_read_device_status(True, torch.cuda.current_stream().cuda_stream) == B.CBS_OK
