@@ -13,10 +13,14 @@ kernels run, instead of copy-all / compute-all / copy-all.  With
 the kernels then follow one another with no event between them (the
 library's programmatic dependent launches overlap their set-up), and the
 copies overlap the neighbouring steps' kernels instead.
-`DoubleBufferedRunner` alternates two such steps on two buffer sets, so one
-step's copies also overlap the neighbouring step's kernels.  The copies are
-cudaMemcpyAsync calls (torch's copy_ on pinned memory) and every layer is a
-library kernel: nothing is computed on the host.
+`DoubleBufferedRunner` runs such steps in turn over two or more buffer
+sets, so one step's copies also overlap the neighbouring steps' kernels.
+Steps in flight together need layers with workspaces of their own
+(`FusedConvBnSilu.fork`).  `pack_layout` and `packed_views` place a step's
+inputs (or outputs) in one buffer, so the step moves them with one copy
+each way.  The copies are cudaMemcpyAsync calls (torch's copy_ on pinned
+memory) and every layer is a library kernel: nothing is computed on the
+host.
 """
 from __future__ import annotations
 
