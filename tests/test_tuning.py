@@ -84,3 +84,34 @@ def test_fp32_nhwc_candidates_force_the_variant(cuda_lib):
         fields = key.split(":")
         if fields[0] == str(B.CBS_FP32) and fields[9] == str(B.CBS_NHWC):
             assert entry["force"].get("force_variant") == B.CBS_VARIANT_TC_TF32X3, key
+
+
+def test_fp32_nchw_flat_candidates_where_they_plan(cuda_lib):
+    """The tuner offers flat NCHW boxes (force_window = 1, 3xTF32) exactly
+    on the FP32 NCHW shapes the planner takes them for, and every such
+    candidate that plans is a flat-box plan (host-side, no GPU call)."""
+    from conv_bn_silu_gb300 import autotune
+    seen_flat = seen_other = 0
+    for prec, n, spec, lay in autotune.workload_shapes():
+        if prec != "fp32" or lay != B.CBS_NCHW:
+            continue
+        base = make_desc(n, spec.c_in, spec.h, spec.width, spec.c_out, spec.k, spec.stride, spec.pad,
+                         prec=B.CBS_FP32, in_layout=lay, out_layout=lay)
+        cands = list(autotune.candidates(prec, spec, base))
+        flat = [f for f in cands if f.get("force_window") == 1]
+        eligible = (spec.c_in % 8 == 0 and spec.stride == 1 and spec.k == 2 * spec.pad + 1 and spec.pad <= 3
+                    and spec.width % 4 == 0 and (n == 1 or (spec.oh * spec.ow) % 128 == 0))
+        assert bool(flat) == eligible, (spec, n)
+        seen_flat += bool(flat)
+        seen_other += not flat
+        for force in flat:
+            assert force.get("force_variant") == B.CBS_VARIANT_TC_TF32X3, force
+            d = make_desc(n, spec.c_in, spec.h, spec.width, spec.c_out, spec.k, spec.stride, spec.pad,
+                          prec=B.CBS_FP32, in_layout=lay, out_layout=lay, **force)
+            try:
+                pl = B.cbs_plan(d)
+            except B.CbsError as e:
+                assert e.status == B.CBS_ERR_UNSUPPORTED, e   # K parts or N tile that do not fit
+                continue
+            assert pl.variant == B.CBS_VARIANT_TC_TF32X3 and pl.window == 1 and pl.k_group == 1
+    assert seen_flat and seen_other   # both kinds occur among the list and chain shapes
